@@ -1,0 +1,302 @@
+/*
+ * moe.h -- C ABI of libmoe.so, a GB300 (sm_103a) routed Mixture-of-Experts FFN
+ * forward.
+ *
+ * The layer computes, per token t with hidden row h[t] and router logits z[t]:
+ *
+ *   ids, w = route(z[t])                                   (moe_route)
+ *   out[t] = sum_k w[k] * (down_k(act(gate_up_k(h[t]) + b1_k)) + b2_k)
+ *
+ * staged as route -> permute into an expert-contiguous layout
+ * (moe_permute) -> grouped gate_up GEMM with the gated activation fused into its
+ * epilogue (moe_grouped_gemm_act) -> grouped down GEMM (moe_grouped_gemm_down)
+ * -> unpermute and weighted combine (moe_combine); or, when the routes are few,
+ * the indexed per-route path (moe_indexed_mlp).  moe_ffn_forward runs the whole
+ * layer.  Sources are cited per function as (page title, section):
+ *   [TileOPs]    TileOPs "MoE Operators" (one section per op),
+ *   [MoERouter]  ONNX Runtime PR #32126 "[CUDA] Add MoERouter and SwiGLU
+ *                contrib operators",
+ *   [ORT-spec]   ONNX Runtime PR #25619 "Update MoE and qMoE spec",
+ *   [ORT-MoE]    onnx-light-cpu "MoE (CPU)".
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is caller-owned DEVICE memory (cudaMalloc'd or any
+ *    device-accessible allocation).  The library never allocates; scratch space
+ *    comes from the caller's workspace `ws` of `ws_bytes` bytes (see
+ *    moe_workspace_size) and must be 256-byte aligned.
+ *  - Tensors are dense, row-major, with the shapes given in brackets.
+ *    Element types: MOE_F32 (float) or MOE_BF16 (bfloat16) for activations,
+ *    weights, biases and outputs; logits, correction bias, routing weights and
+ *    MoERouter outputs are always float32; ids and index maps int32.
+ *  - Every call is asynchronous on `stream` (0 = legacy default stream) and
+ *    returns a moe_status.  Argument checks happen on the host before anything
+ *    is launched: an invalid call writes nothing.  Outputs that overlap an
+ *    input return MOE_ERR_OVERLAP before any launch (disjoint views of one
+ *    allocation are fine) [TileOPs, MoEPostPermuteFwdOp / MoEGroupedGemmFwdOp].
+ *  - The CONTENTS of index tensors (ids, segment ends, index maps) are not
+ *    checked on the host, since checking would synchronise [TileOPs,
+ *    MoEGroupedGemmFwdOp].  Kernels that meet an out-of-range id or index skip
+ *    that item and latch a device error in the workspace status word;
+ *    moe_sync_status reports it as MOE_ERR_DEVICE.
+ *  - Every wait inside a kernel is bounded; a wait that runs out latches
+ *    MOE_ERR_TIMEOUT in the status word instead of hanging.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* a shape, enum or parameter is out of range          */
+  MOE_ERR_OVERLAP = 2,     /* an output overlaps an input                          */
+  MOE_ERR_UNSUPPORTED = 3, /* a dtype / activation / alignment combination not built */
+  MOE_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed                 */
+  MOE_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait ran out (status word)       */
+  MOE_ERR_DEVICE = 6,      /* a kernel met an out-of-range id / index (status word) */
+  MOE_ERR_WORKSPACE = 7    /* ws is NULL, misaligned or smaller than required      */
+} moe_status;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum moe_scoring { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 } moe_scoring;
+
+typedef enum moe_act_kind {
+  /* silu(gate) * up over a STACKED w_gate_up: F gate rows, then F up rows
+     [TileOPs, MoEGroupedGemmFwdOp]. */
+  MOE_ACT_SILU_AND_MUL = 0,
+  /* clamped SwiGLU G*sigmoid(alpha*G)*(L+beta), G = min(gate, limit),
+     L = clamp(up, -limit, limit), limit <= 0 disables both clamps; rows
+     interleaved (swiglu_fusion 1: row 2j gate j, row 2j+1 up j -- gpt-oss
+     "swigluoai" with limit 7, alpha 1.702, beta 1) or concatenated
+     (swiglu_fusion 2: gate rows then up rows) [MoERouter, SwiGLU;
+     ORT-spec, "SwiGLU Activation Function" and "Fusion Behavior"]. */
+  MOE_ACT_SWIGLU = 1,
+  /* non-gated identity: w_gate_up is [E, F, H] and act(p) = p
+     [ORT-MoE, activation_type "identity"]. */
+  MOE_ACT_IDENTITY = 2
+} moe_act_kind;
+
+/* Router configuration [TileOPs, FusedTopKFwdOp / FusedMoEFwdOp; MoERouter]. */
+typedef struct moe_route_params {
+  int32_t top_k;                 /* K, 1 <= K <= min(E, 64)                            */
+  int32_t scoring;               /* moe_scoring                                        */
+  int32_t renormalize;           /* nonzero: divide the K weights by their sum         */
+  int32_t num_expert_group;      /* G >= 1, must divide E, G <= 32                     */
+  int32_t topk_group;            /* TG, 1 <= TG <= G, TG * E / G >= K                   */
+  float routed_scaling_factor;   /* rsf > 0, multiplies the weights once               */
+  int32_t local_expert_start;    /* MoERouter slice [start, start + count) of [0, E)   */
+  int32_t local_expert_count;    /* 0: no router_probs / weight_scale outputs          */
+  float route_scale;             /* MoERouter weight_scale multiplier                  */
+} moe_route_params;
+
+/* Gated activation fused into the gate_up GEMM epilogue. */
+typedef struct moe_act_params {
+  int32_t kind;          /* moe_act_kind                                          */
+  int32_t swiglu_fusion; /* MOE_ACT_SWIGLU only: 1 interleaved, 2 concatenated      */
+  float limit;           /* SwiGLU clamp; <= 0 disables both clamps                */
+  float alpha;           /* SwiGLU sigmoid scale                                   */
+  float beta;            /* SwiGLU linear offset                                   */
+} moe_act_params;
+
+/* ------------------------------------------------------------------------ */
+/* Router.  [TileOPs, FusedTopKFwdOp and FusedMoEFwdOp; MoERouter, MoERouter]
+ *
+ * Per token t (one warp per token), in float32:
+ *   s = softmax(z[t]) or sigmoid(z[t]);  u = s + correction_bias (selection only);
+ *   G > 1: groups of E/G consecutive experts score the sum of their two best u
+ *          (with a bias) or their best u (without); the TG best groups are kept,
+ *          ties to the lower group index;
+ *   the K largest u among kept experts, ties to the lower expert index -- or the
+ *   given expert_ids[t] (hash routing: selection skipped, bias ignored);
+ *   w_k = s[id_k], divided by sum_j s[id_j] when renormalize, times rsf once.
+ * Selected ids are written in ASCENDING expert order; fixed expert_ids keep
+ * their given order.
+ * MoERouter outputs (when local_expert_count > 0): with w^_k = s[id_k] /
+ * sum_j s[id_j] (always normalised, no rsf), router_probs[t, j] =
+ * log(sum of w^_k over routes on expert local_expert_start + j) if chosen,
+ * else -1e30; weight_scale[t] = route_scale * sum of w^ over local routes
+ * (0 when no chosen expert is local).
+ *
+ *   logits          [T, E] f32
+ *   correction_bias [E] f32 or NULL; requires MOE_SCORING_SIGMOID
+ *   expert_ids      [T, K] i32 or NULL (hash routing)
+ *   topk_weights    [T, K] f32 out;  topk_ids [T, K] i32 out
+ *   router_probs    [T, local_expert_count] f32 out or NULL
+ *   weight_scale    [T] f32 out or NULL (both or neither when count > 0)
+ * E <= 1024.  T == 0 is a no-op. */
+moe_status moe_route(const float* logits, const float* correction_bias,
+                     const int32_t* expert_ids, int T, int E, const moe_route_params* p,
+                     float* topk_weights, int32_t* topk_ids, float* router_probs,
+                     float* weight_scale, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Permute into the tight expert-contiguous layout ("contiguous ·
+ * physical_psum": segment END rows) [TileOPs, MoEPrePermuteFwdOp and
+ * MoEGroupedGemmFwdOp].
+ *
+ * Route r = t*K + k goes to expert topk_ids[r].  seg_end[e] = number of routes
+ * on experts 0..e (inclusive prefix sum).  Rows of expert e hold its routes in
+ * ascending r.  row_to_route[row] = r and route_to_row[r] = row.
+ * expert_input[row, :] = hidden[row_to_route[row] / K, :]; pass NULL
+ * expert_input (and hidden) to build the index maps only.
+ *
+ *   hidden       [T, H] dtype (or NULL)     topk_ids     [T, K] i32
+ *   expert_input [T*K, H] dtype out or NULL seg_end      [E] i32 out
+ *   row_to_route [T*K] i32 out              route_to_row [T*K] i32 out
+ *   ws: >= moe_permute_workspace_size(T*K, E) bytes.
+ * An id outside [0, E) latches MOE_ERR_DEVICE; that route is dropped. */
+moe_status moe_permute(const void* hidden, moe_dtype dtype, const int32_t* topk_ids, int T,
+                       int H, int E, int K, void* expert_input, int32_t* seg_end,
+                       int32_t* row_to_route, int32_t* route_to_row, void* ws,
+                       size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped gate_up GEMM with the gated activation fused into its epilogue
+ * [TileOPs, MoEGroupedGemmFwdOp ("activation"), MoEExpertMLPFwdOp].
+ *
+ * For each expert e and each row m in [seg_end[e-1], seg_end[e]):
+ *   p = a[m, :] . w_gate_up[e, n, :] (+ b_gate_up[e, n])   for every n, in fp32
+ *   out[m, j] = act(p)_j, cast to dtype                     (j < F)
+ * The [M, 2F] product is never written.  bf16 runs on the tcgen05 tensor
+ * cores (TMA-fed, TMEM accumulators) when Hk % 8 == 0, F % 8 == 0 and a,
+ * w_gate_up, out are 16-byte aligned (16-byte TMA strides); f32, and bf16
+ * shapes outside those limits, run a SIMT kernel in exact fp32 FMA.
+ *
+ *   a          [M, Hk] dtype               w_gate_up [E, N1, Hk] dtype
+ *              (N1 = 2F, or F for MOE_ACT_IDENTITY)
+ *   b_gate_up  [E, N1] dtype or NULL (in w_gate_up's row order)
+ *   seg_end    [E] i32, non-decreasing, seg_end[E-1] <= M
+ *   out        [M, F] dtype
+ *   ws: >= MOE_STATUS_BYTES bytes (holds the status word).
+ * E <= 1024.  Rows past seg_end[E-1] are not written. */
+moe_status moe_grouped_gemm_act(const void* a, const void* w_gate_up, const void* b_gate_up,
+                                const int32_t* seg_end, int M, int F, int Hk, int E,
+                                moe_dtype dtype, const moe_act_params* act, void* out, void* ws,
+                                size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Plain grouped down GEMM [TileOPs, MoEGroupedGemmFwdOp (no activation),
+ * MoEExpertMLPFwdOp]: out[m, :] = a[m, :] . w_down[e]^T (+ b_down[e]) in fp32,
+ * cast to dtype, for the rows m of expert e.
+ *
+ *   a [M, F] dtype;  w_down [E, H, F] dtype;  b_down [E, H] dtype or NULL;
+ *   seg_end [E] i32;  out [M, H] dtype;  ws >= MOE_STATUS_BYTES bytes.
+ * Kernel choice as for moe_grouped_gemm_act (tcgen05 for bf16 with H % 8 == 0,
+ * F % 8 == 0 and 16-byte aligned a, w_down, out). */
+moe_status moe_grouped_gemm_down(const void* a, const void* w_down, const void* b_down,
+                                 const int32_t* seg_end, int M, int H, int F, int E,
+                                 moe_dtype dtype, void* out, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Unpermute + weighted combine [TileOPs, MoEPostPermuteFwdOp and
+ * FusedMoEExpertsFwdOp]:
+ *   out[t, :] = scale * sum_{k = 0..K-1} topk_weights[t, k] *
+ *               expert_out[route_to_row[t*K + k], :]
+ * accumulated in fp32 in fixed k order (deterministic, no atomics) and cast
+ * once to dtype.
+ *
+ *   expert_out [M, H] dtype (M = T*K);  topk_weights [T, K] f32;
+ *   route_to_row [T*K] i32;  out [T, H] dtype.
+ * An index outside [0, T*K) contributes nothing (nothing is latched: this
+ * entry point has no workspace). */
+moe_status moe_combine(const void* expert_out, const float* topk_weights,
+                       const int32_t* route_to_row, int T, int K, int H, moe_dtype dtype,
+                       float scale, void* out, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Standalone SwiGLU [MoERouter, section SwiGLU; ORT-spec "SwiGLU Activation
+ * Function", "Fusion Behavior"]:
+ *   G = min(g, limit), L = max(min(l, limit), -limit)   (limit <= 0: no clamp)
+ *   out = G * sigmoid(alpha * G) * (L + beta), arithmetic in float32.
+ * With `up` given, g = gate[r, i] and l = up[r, i] ([R, I] each).  With up ==
+ * NULL, gate is one [R, 2I] projection: swiglu_fusion 2 = [g | l] (gate
+ * first, then up), 1 = interleaved (g, l, g, l, ...).
+ *   out [R, I] dtype. */
+moe_status swiglu(const void* gate, const void* up, int64_t R, int I, moe_dtype dtype,
+                  int swiglu_fusion, float limit, float alpha, float beta, void* out,
+                  cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Indexed small-route expert MLP [TileOPs, IndexedExpertMLPFwdOp]: the same
+ * result as permute + the two grouped GEMMs (silu_and_mul, no bias) +
+ * combine, dispatched per route.  Routes sharing an expert are grouped and
+ * each distinct expert's weights are streamed from HBM once, for all of its
+ * routes, with 128-bit loads.  bf16 only; H % 128 == 0, F % 256 == 0.
+ *
+ *   hidden [T, H] bf16;  w_gate_up [E, 2F, H] bf16 (stacked);  w_down [E, H, F];
+ *   topk_weights [T, K] f32;  topk_ids [T, K] i32;  out [T, H] bf16;
+ *   ws >= moe_workspace_size(T, H, F, E, K, MOE_BF16). */
+moe_status moe_indexed_mlp(const void* hidden, const void* w_gate_up, const void* w_down,
+                           const float* topk_weights, const int32_t* topk_ids, int T, int H,
+                           int F, int E, int K, float scale, void* out, void* ws,
+                           size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* The whole routed MoE FFN forward [TileOPs, FusedMoEFwdOp and
+ * FusedMoEExpertsFwdOp].  Routes with moe_route (rsf folded into the weights,
+ * so it applies once), then runs the indexed path when T*K <= 2E, the
+ * activation is silu_and_mul, there is no bias, dtype is bf16, H % 128 == 0
+ * and F % 256 == 0 [TileOPs, FusedMoEExpertsFwdOp dispatch rule]; otherwise
+ * the staged pipeline permute -> gate_up+act -> down -> combine.
+ *
+ *   hidden [T, H] dtype;  logits [T, E] f32;  w_gate_up [E, N1, H];
+ *   w_down [E, H, F];  correction_bias [E] f32 | NULL;  expert_ids [T, K] | NULL;
+ *   b_gate_up [E, N1] | NULL;  b_down [E, H] | NULL;  out [T, H] dtype;
+ *   topk_weights_out [T, K] f32 | NULL, topk_ids_out [T, K] i32 | NULL
+ *   (optional copies of the routing);  router_probs / weight_scale as in
+ *   moe_route (NULL unless p->local_expert_count > 0);
+ *   ws >= moe_workspace_size(T, H, F, E, K, dtype). */
+moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* w_gate_up,
+                           const void* w_down, const float* correction_bias,
+                           const int32_t* expert_ids, const void* b_gate_up, const void* b_down,
+                           int T, int H, int F, int E, moe_dtype dtype,
+                           const moe_route_params* p, const moe_act_params* act, void* out,
+                           float* topk_weights_out, int32_t* topk_ids_out, float* router_probs,
+                           float* weight_scale, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Sizes and status.  (The workspace query plays the role of the peak-memory
+ * query of [ORT-MoE].) */
+
+/* Bytes at the start of every workspace that hold the device status word. */
+#define MOE_STATUS_BYTES 256
+
+/* Workspace bytes moe_ffn_forward / moe_indexed_mlp need for these extents. */
+size_t moe_workspace_size(int T, int H, int F, int E, int K, moe_dtype dtype);
+
+/* Workspace bytes moe_permute needs for M = T*K routes over E experts. */
+size_t moe_permute_workspace_size(int M, int E);
+
+/* Zero the status word of `ws` (asynchronously, on `stream`). */
+moe_status moe_clear_status(void* ws, cudaStream_t stream);
+
+/* Synchronise `stream`, then read and clear the status word of `ws`:
+ * MOE_OK, MOE_ERR_DEVICE (bad id / index met) or MOE_ERR_TIMEOUT. */
+moe_status moe_sync_status(void* ws, cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status s);
+
+/* Number of this library's kernel launches issued since load (all entry
+ * points, all streams); lets a caller count device work per call. */
+uint64_t moe_launch_count(void);
+
+/* Verification switch: nonzero routes every grouped GEMM (bf16 included) to
+ * the exact-fp32 SIMT kernel instead of the tcgen05 kernel; returns the
+ * previous setting.  Process-wide; not meant to change while calls are in
+ * flight. */
+int moe_set_gemm_simt(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

@@ -1,0 +1,373 @@
+// C ABI of libmoe.so: argument validation, overlap checks, workspace layout and
+// dispatch to the kernels.  Every check runs on the host before any launch, so
+// an invalid call writes nothing.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+static int g_force_simt = 0;
+
+namespace {
+
+struct Span {
+  const void* p;
+  size_t bytes;
+};
+bool overlaps(Span a, Span b) {
+  if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+  uintptr_t a0 = (uintptr_t)a.p, a1 = a0 + a.bytes;
+  uintptr_t b0 = (uintptr_t)b.p, b1 = b0 + b.bytes;
+  return a0 < b1 && b0 < a1;
+}
+// any output overlapping any input, or two outputs overlapping each other
+template <size_t NO, size_t NI>
+bool any_overlap(const Span (&outs)[NO], const Span (&ins)[NI]) {
+  for (size_t i = 0; i < NO; ++i) {
+    for (size_t j = 0; j < NI; ++j)
+      if (overlaps(outs[i], ins[j])) return true;
+    for (size_t j = i + 1; j < NO; ++j)
+      if (overlaps(outs[i], outs[j])) return true;
+  }
+  return false;
+}
+
+size_t esize(moe_dtype d) { return d == MOE_BF16 ? 2 : 4; }
+bool dtype_ok(int d) { return d == MOE_F32 || d == MOE_BF16; }
+
+moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+moe_status check_route(const float* logits, const float* bias, int T, int E,
+                       const moe_route_params* p, const float* w, const int32_t* ids,
+                       const float* probs, const float* wscale) {
+  if (!p || T < 0 || E < 1 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  const int K = p->top_k, G = p->num_expert_group, TG = p->topk_group;
+  if (K < 1 || K > E || K > 64) return MOE_ERR_INVALID_ARG;
+  if (p->scoring != MOE_SCORING_SOFTMAX && p->scoring != MOE_SCORING_SIGMOID)
+    return MOE_ERR_INVALID_ARG;
+  if (bias && p->scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (G < 1 || G > 32 || E % G != 0) return MOE_ERR_INVALID_ARG;
+  if (TG < 1 || TG > G || (long long)TG * (E / G) < K) return MOE_ERR_INVALID_ARG;
+  if (bias && G > 1 && E / G < 2) return MOE_ERR_INVALID_ARG;
+  if (!(p->routed_scaling_factor > 0.f) || !std::isfinite(p->routed_scaling_factor))
+    return MOE_ERR_INVALID_ARG;
+  if (p->local_expert_count < 0) return MOE_ERR_INVALID_ARG;
+  if (p->local_expert_count > 0) {
+    if (p->local_expert_start < 0 || p->local_expert_start + p->local_expert_count > E)
+      return MOE_ERR_INVALID_ARG;
+    if (!probs || !wscale) return MOE_ERR_INVALID_ARG;
+  } else if (probs || wscale) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (T > 0 && (!logits || !w || !ids)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+bool act_ok(const moe_act_params* a) {
+  if (!a) return false;
+  if (a->kind == MOE_ACT_SILU_AND_MUL || a->kind == MOE_ACT_IDENTITY) return true;
+  if (a->kind == MOE_ACT_SWIGLU) return a->swiglu_fusion == 1 || a->swiglu_fusion == 2;
+  return false;
+}
+
+bool ws_ok(const void* ws, size_t have, size_t need) {
+  return ws && ((uintptr_t)ws & 255u) == 0 && have >= need;
+}
+
+bool tc_ok(const void* a, const void* w, const void* out, int Nout, int Kd, int M) {
+  return !g_force_simt && Nout % 8 == 0 && Kd % 8 == 0 && aligned16(a) && aligned16(w) &&
+         aligned16(out) && M < (1 << 30);
+}
+
+// grouped GEMM dispatch; act == nullptr for the plain (down) GEMM
+cudaError_t grouped_gemm(const void* a, const void* w, const void* bias, const int32_t* seg_end,
+                         int M, int Nout, int Kd, int E, moe_dtype dt, const moe_act_params* act,
+                         void* out, int* status, cudaStream_t s) {
+  if (dt == MOE_BF16 && tc_ok(a, w, out, Nout, Kd, M))
+    return launch_gemm_tc(a, w, bias, seg_end, M, Nout, Kd, E, act, out, status, s);
+  return launch_gemm_simt(a, w, bias, seg_end, M, Nout, Kd, E, dt, act, out, status, s);
+}
+
+bool indexed_rule(int T, int H, int F, int E, int K, moe_dtype dt, const moe_act_params* act,
+                  const void* b1, const void* b2) {
+  return (long long)T * K <= 2LL * E && act->kind == MOE_ACT_SILU_AND_MUL && !b1 && !b2 &&
+         dt == MOE_BF16 && H % 128 == 0 && F % 256 == 0;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_route(const float* logits, const float* correction_bias, const int32_t* expert_ids,
+                     int T, int E, const moe_route_params* p, float* topk_weights,
+                     int32_t* topk_ids, float* router_probs, float* weight_scale,
+                     cudaStream_t stream) {
+  moe_status st = check_route(logits, correction_bias, T, E, p, topk_weights, topk_ids,
+                              router_probs, weight_scale);
+  if (st != MOE_OK) return st;
+  if (T == 0) return MOE_OK;
+  const size_t TK = (size_t)T * p->top_k, lc = (size_t)p->local_expert_count;
+  Span outs[] = {{topk_weights, TK * 4}, {topk_ids, TK * 4}, {router_probs, T * lc * 4},
+                 {weight_scale, (size_t)T * 4}};
+  Span ins[] = {{logits, (size_t)T * E * 4}, {correction_bias, (size_t)E * 4},
+                {expert_ids, TK * 4}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  return cuda_status(launch_route(logits, correction_bias, expert_ids, T, E, *p, topk_weights,
+                                  topk_ids, router_probs, weight_scale, stream));
+}
+
+size_t moe_permute_workspace_size(int M, int E) {
+  if (M < 0 || E < 1) return 0;
+  return PermuteWs(M, E).total;
+}
+
+moe_status moe_permute(const void* hidden, moe_dtype dtype, const int32_t* topk_ids, int T, int H,
+                       int E, int K, void* expert_input, int32_t* seg_end, int32_t* row_to_route,
+                       int32_t* route_to_row, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (T < 0 || K < 1 || E < 1 || E > 12288 || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
+  if ((long long)T * K >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+  if (expert_input && (!hidden || H < 1)) return MOE_ERR_INVALID_ARG;
+  if (!seg_end || (T > 0 && (!topk_ids || !row_to_route || !route_to_row)))
+    return MOE_ERR_INVALID_ARG;
+  const int M = T * K;
+  if (!ws_ok(ws, ws_bytes, PermuteWs(M, E).total)) return MOE_ERR_WORKSPACE;
+  const size_t esz = esize(dtype);
+  Span outs[] = {{expert_input, expert_input ? (size_t)M * H * esz : 0},
+                 {seg_end, (size_t)E * 4},
+                 {row_to_route, (size_t)M * 4},
+                 {route_to_row, (size_t)M * 4},
+                 {ws, PermuteWs(M, E).total}};
+  Span ins[] = {{hidden, expert_input ? (size_t)T * H * esz : 0}, {topk_ids, (size_t)M * 4}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  return cuda_status(launch_permute(hidden, (int)esz, topk_ids, T, H, E, K, expert_input, seg_end,
+                                    row_to_route, route_to_row, ws, stream));
+}
+
+moe_status moe_grouped_gemm_act(const void* a, const void* w_gate_up, const void* b_gate_up,
+                                const int32_t* seg_end, int M, int F, int Hk, int E,
+                                moe_dtype dtype, const moe_act_params* act, void* out, void* ws,
+                                size_t ws_bytes, cudaStream_t stream) {
+  if (M < 0 || F < 1 || Hk < 1 || E < 1 || E > kMaxExperts || !dtype_ok(dtype) || !act_ok(act))
+    return MOE_ERR_INVALID_ARG;
+  if (!seg_end || !w_gate_up || (M > 0 && (!a || !out))) return MOE_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, MOE_STATUS_BYTES)) return MOE_ERR_WORKSPACE;
+  const size_t esz = esize(dtype);
+  const size_t N1 = act->kind == MOE_ACT_IDENTITY ? (size_t)F : 2 * (size_t)F;
+  Span outs[] = {{out, (size_t)M * F * esz}};
+  Span ins[] = {{a, (size_t)M * Hk * esz}, {w_gate_up, (size_t)E * N1 * Hk * esz},
+                {b_gate_up, b_gate_up ? (size_t)E * N1 * esz : 0}, {seg_end, (size_t)E * 4},
+                {ws, MOE_STATUS_BYTES}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  if (M == 0) return MOE_OK;
+  return cuda_status(grouped_gemm(a, w_gate_up, b_gate_up, seg_end, M, F, Hk, E, dtype, act, out,
+                                  static_cast<int*>(ws), stream));
+}
+
+moe_status moe_grouped_gemm_down(const void* a, const void* w_down, const void* b_down,
+                                 const int32_t* seg_end, int M, int H, int F, int E,
+                                 moe_dtype dtype, void* out, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  if (M < 0 || H < 1 || F < 1 || E < 1 || E > kMaxExperts || !dtype_ok(dtype))
+    return MOE_ERR_INVALID_ARG;
+  if (!seg_end || !w_down || (M > 0 && (!a || !out))) return MOE_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, MOE_STATUS_BYTES)) return MOE_ERR_WORKSPACE;
+  const size_t esz = esize(dtype);
+  Span outs[] = {{out, (size_t)M * H * esz}};
+  Span ins[] = {{a, (size_t)M * F * esz}, {w_down, (size_t)E * H * F * esz},
+                {b_down, b_down ? (size_t)E * H * esz : 0}, {seg_end, (size_t)E * 4},
+                {ws, MOE_STATUS_BYTES}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  if (M == 0) return MOE_OK;
+  return cuda_status(grouped_gemm(a, w_down, b_down, seg_end, M, H, F, E, dtype, nullptr, out,
+                                  static_cast<int*>(ws), stream));
+}
+
+moe_status moe_combine(const void* expert_out, const float* topk_weights,
+                       const int32_t* route_to_row, int T, int K, int H, moe_dtype dtype,
+                       float scale, void* out, cudaStream_t stream) {
+  if (T < 0 || K < 1 || H < 1 || !dtype_ok(dtype) || !std::isfinite(scale))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!expert_out || !topk_weights || !route_to_row || !out)) return MOE_ERR_INVALID_ARG;
+  const size_t esz = esize(dtype), M = (size_t)T * K;
+  Span outs[] = {{out, (size_t)T * H * esz}};
+  Span ins[] = {{expert_out, M * H * esz}, {topk_weights, M * 4}, {route_to_row, M * 4}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  return cuda_status(
+      launch_combine(expert_out, topk_weights, route_to_row, T, K, H, dtype, scale, out, stream));
+}
+
+moe_status swiglu(const void* gate, const void* up, int64_t R, int I, moe_dtype dtype,
+                  int swiglu_fusion, float limit, float alpha, float beta, void* out,
+                  cudaStream_t stream) {
+  if (R < 0 || I < 1 || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
+  if (!up && swiglu_fusion != 1 && swiglu_fusion != 2) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!gate || !out)) return MOE_ERR_INVALID_ARG;
+  const size_t esz = esize(dtype);
+  const size_t n = (size_t)R * I * esz;
+  Span outs[] = {{out, n}};
+  Span ins[] = {{gate, up ? n : 2 * n}, {up, up ? n : 0}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  return cuda_status(
+      launch_swiglu(gate, up, R, I, dtype, swiglu_fusion, limit, alpha, beta, out, stream));
+}
+
+size_t moe_workspace_size(int T, int H, int F, int E, int K, moe_dtype dtype) {
+  if (T < 0 || H < 1 || F < 1 || E < 1 || K < 1 || !dtype_ok(dtype)) return 0;
+  return ForwardWs(T, H, F, E, K, (int)esize(dtype)).total;
+}
+
+moe_status moe_indexed_mlp(const void* hidden, const void* w_gate_up, const void* w_down,
+                           const float* topk_weights, const int32_t* topk_ids, int T, int H,
+                           int F, int E, int K, float scale, void* out, void* ws,
+                           size_t ws_bytes, cudaStream_t stream) {
+  if (T < 0 || H < 1 || F < 1 || E < 1 || E > 12288 || K < 1 || !std::isfinite(scale))
+    return MOE_ERR_INVALID_ARG;
+  if (H % 128 != 0 || F % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  if (!w_gate_up || !w_down || (T > 0 && (!hidden || !topk_weights || !topk_ids || !out)))
+    return MOE_ERR_INVALID_ARG;
+  ForwardWs L(T, H, F, E, K, 2);
+  if (!ws_ok(ws, ws_bytes, L.total)) return MOE_ERR_WORKSPACE;
+  const size_t M = (size_t)T * K;
+  Span outs[] = {{out, (size_t)T * H * 2}, {ws, L.total}};
+  Span ins[] = {{hidden, (size_t)T * H * 2}, {w_gate_up, (size_t)E * 2 * F * H * 2},
+                {w_down, (size_t)E * H * F * 2}, {topk_weights, M * 4}, {topk_ids, M * 4}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  if (T == 0) return MOE_OK;
+  return cuda_status(launch_indexed(hidden, w_gate_up, w_down, topk_weights, topk_ids, T, H, F, E,
+                                    K, scale, out, ws, L, stream));
+}
+
+moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* w_gate_up,
+                           const void* w_down, const float* correction_bias,
+                           const int32_t* expert_ids, const void* b_gate_up, const void* b_down,
+                           int T, int H, int F, int E, moe_dtype dtype, const moe_route_params* p,
+                           const moe_act_params* act, void* out, float* topk_weights_out,
+                           int32_t* topk_ids_out, float* router_probs, float* weight_scale,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!dtype_ok(dtype) || !act_ok(act) || H < 1 || F < 1) return MOE_ERR_INVALID_ARG;
+  float dummy_w = 0.f;
+  int32_t dummy_i = 0;
+  moe_status st = check_route(logits, correction_bias, T, E, p, &dummy_w, &dummy_i, router_probs,
+                              weight_scale);
+  if (st != MOE_OK) return st;
+  if (!w_gate_up || !w_down || (T > 0 && (!hidden || !out))) return MOE_ERR_INVALID_ARG;
+  const int K = p->top_k;
+  const size_t esz = esize(dtype), M = (size_t)T * K;
+  if (M >= (1ULL << 31)) return MOE_ERR_INVALID_ARG;
+  ForwardWs L(T, H, F, E, K, (int)esz);
+  if (!ws_ok(ws, ws_bytes, L.total)) return MOE_ERR_WORKSPACE;
+  const size_t N1 = act->kind == MOE_ACT_IDENTITY ? (size_t)F : 2 * (size_t)F;
+  const size_t lc = (size_t)p->local_expert_count;
+  Span outs[] = {{out, (size_t)T * H * esz},        {topk_weights_out, M * 4},
+                 {topk_ids_out, M * 4},             {router_probs, T * lc * 4},
+                 {weight_scale, (size_t)T * 4},     {ws, L.total}};
+  Span ins[] = {{hidden, (size_t)T * H * esz},
+                {logits, (size_t)T * E * 4},
+                {w_gate_up, (size_t)E * N1 * H * esz},
+                {w_down, (size_t)E * H * F * esz},
+                {correction_bias, correction_bias ? (size_t)E * 4 : 0},
+                {expert_ids, expert_ids ? M * 4 : 0},
+                {b_gate_up, b_gate_up ? (size_t)E * N1 * esz : 0},
+                {b_down, b_down ? (size_t)E * H * esz : 0}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  if (T == 0) return MOE_OK;
+
+  char* base = static_cast<char*>(ws);
+  float* tw = topk_weights_out ? topk_weights_out : reinterpret_cast<float*>(base + L.topk_w);
+  int32_t* ti = topk_ids_out ? topk_ids_out : reinterpret_cast<int32_t*>(base + L.topk_ids);
+  cudaError_t err = launch_route(logits, correction_bias, expert_ids, T, E, *p, tw, ti,
+                                 router_probs, weight_scale, stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+
+  // routed_scaling_factor is folded into tw by the router: the combine scale is 1
+  if (indexed_rule(T, H, F, E, K, dtype, act, b_gate_up, b_down))
+    return cuda_status(
+        launch_indexed(hidden, w_gate_up, w_down, tw, ti, T, H, F, E, K, 1.0f, out, ws, L, stream));
+
+  int32_t* seg_end = reinterpret_cast<int32_t*>(base + L.seg_end);
+  int32_t* r2r = reinterpret_cast<int32_t*>(base + L.row_to_route);
+  int32_t* route_to_row = reinterpret_cast<int32_t*>(base + L.route_to_row);
+  void* xin = base + L.expert_input;
+  void* a1 = base + L.act;
+  void* y = base + L.y;
+  int* status = reinterpret_cast<int*>(base);
+  err = launch_permute(hidden, (int)esz, ti, T, H, E, K, xin, seg_end, r2r, route_to_row, ws,
+                       stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  err = grouped_gemm(xin, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, dtype, act, a1, status,
+                     stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  err = grouped_gemm(a1, w_down, b_down, seg_end, (int)M, H, F, E, dtype, nullptr, y, status,
+                     stream);
+  if (err != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_combine(y, tw, route_to_row, T, K, H, dtype, 1.0f, out, stream));
+}
+
+moe_status moe_clear_status(void* ws, cudaStream_t stream) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, MOE_STATUS_BYTES, stream));
+}
+
+moe_status moe_sync_status(void* ws, cudaStream_t stream) {
+  if (!ws) return MOE_ERR_WORKSPACE;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word & kDevTimeout) return MOE_ERR_TIMEOUT;
+  if (word & kDevBadIndex) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_OVERLAP: return "an output overlaps an input";
+    case MOE_ERR_UNSUPPORTED: return "unsupported dtype / activation / alignment";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "a bounded in-kernel wait ran out";
+    case MOE_ERR_DEVICE: return "a kernel met an out-of-range id or index";
+    case MOE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+uint64_t moe_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moe_set_gemm_simt(int enable) {
+  int old = g_force_simt;
+  g_force_simt = enable ? 1 : 0;
+  return old;
+}
+
+}  // extern "C"

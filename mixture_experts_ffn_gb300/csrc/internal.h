@@ -1,0 +1,90 @@
+// Host-side declarations shared by the translation units of libmoe.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// device status-word bits (first int of every workspace)
+enum : int {
+  kDevBadIndex = 1,  // an id / index outside its range was met and skipped
+  kDevTimeout = 2,   // a bounded wait ran out
+};
+
+constexpr int kPermuteChunk = 1024;  // routes per permute chunk
+constexpr int kMaxExperts = 1024;    // router / grouped GEMM limit on E
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Permute scratch: [status 256 B][chunk counts C x E][active experts E][num_active 1]
+struct PermuteWs {
+  size_t counts, active, num_active, total;
+  PermuteWs(int M, int E) {
+    size_t C = (size_t)(M + kPermuteChunk - 1) / kPermuteChunk;
+    if (C == 0) C = 1;
+    counts = MOE_STATUS_BYTES;
+    active = align256(counts + C * (size_t)E * 4);
+    num_active = align256(active + (size_t)E * 4);
+    total = align256(num_active + 4);
+  }
+};
+
+// Full forward workspace: the permute scratch first (sharing the status word),
+// then routing, index maps and the staged intermediates.
+struct ForwardWs {
+  size_t topk_w, topk_ids, seg_end, row_to_route, route_to_row, expert_input, act, y, total;
+  ForwardWs(int T, int H, int F, int E, int K, int esz) {
+    size_t M = (size_t)T * K;
+    PermuteWs p((int)M, E);
+    topk_w = p.total;
+    topk_ids = align256(topk_w + M * 4);
+    seg_end = align256(topk_ids + M * 4);
+    row_to_route = align256(seg_end + (size_t)E * 4);
+    route_to_row = align256(row_to_route + M * 4);
+    expert_input = align256(route_to_row + M * 4);
+    act = align256(expert_input + M * (size_t)H * esz);
+    y = align256(act + M * (size_t)F * esz);
+    total = align256(y + M * (size_t)H * esz);
+  }
+};
+
+void count_launch(int n = 1);
+int num_sms();
+
+// ---- launchers (return cudaGetLastError() of their launches) ----
+cudaError_t launch_route(const float* logits, const float* bias, const int32_t* ids_in, int T,
+                         int E, const moe_route_params& p, float* w, int32_t* ids, float* probs,
+                         float* wscale, cudaStream_t s);
+
+cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int T, int H, int E,
+                           int K, void* expert_input, int32_t* seg_end, int32_t* row_to_route,
+                           int32_t* route_to_row, void* ws, cudaStream_t s);
+
+cudaError_t launch_combine(const void* y, const float* w, const int32_t* route_to_row, int T,
+                           int K, int H, moe_dtype dt, float scale, void* out, cudaStream_t s);
+
+cudaError_t launch_swiglu(const void* gate, const void* up, int64_t R, int I, moe_dtype dt,
+                          int fusion, float limit, float alpha, float beta, void* out,
+                          cudaStream_t s);
+
+// SIMT grouped GEMM (exact fp32 FMA; any dtype).  act == nullptr: plain GEMM
+// with N output columns; otherwise N = F act columns read from N1 rows.
+cudaError_t launch_gemm_simt(const void* a, const void* w, const void* bias,
+                             const int32_t* seg_end, int M, int N, int K, int E, moe_dtype dt,
+                             const moe_act_params* act, void* out, int* status, cudaStream_t s);
+
+// tcgen05 grouped GEMM (bf16 operands, fp32 TMEM accumulators).
+cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const int32_t* seg_end,
+                           int M, int N, int K, int E, const moe_act_params* act, void* out,
+                           int* status, cudaStream_t s);
+
+// indexed per-route decode path (bf16, silu_and_mul, no bias)
+cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, const float* w,
+                           const int32_t* ids, int T, int H, int F, int E, int K, float scale,
+                           void* out, void* ws, const ForwardWs& L, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,312 @@
+// Permutation into the tight expert-contiguous layout and the inverse
+// weighted combine.  TileOPs "MoE Operators": MoEPrePermuteFwdOp (rows grouped
+// by expert, layout "contiguous · physical_psum" = segment end rows),
+// MoEPostPermuteFwdOp (restore token order, apply the routing weights once,
+// reduce over k, cast) and FusedMoEExpertsFwdOp (the weighted sum).
+//
+// Permute = 4 launches, all deterministic:
+//   count   : one CTA per chunk of kPermuteChunk routes, shared-memory histogram
+//   scan    : one CTA; per-expert totals, exclusive scan -> seg_end, per-chunk
+//             start offsets, list of experts that have routes
+//   scatter : one warp per chunk; routes of a chunk are ranked in order with
+//             warp match-any, so rows inside an expert follow ascending route
+//   gather  : one warp per row copies the hidden row with 128-bit accesses
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(256) perm_count(const int32_t* __restrict__ ids, int M, int E,
+                                                  int* __restrict__ counts, int* status) {
+  extern __shared__ int hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int r0 = blockIdx.x * kPermuteChunk, r1 = min(M, r0 + kPermuteChunk);
+  bool bad = false;
+  for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+    int id = __ldg(ids + r);
+    if (id >= 0 && id < E) atomicAdd(&hist[id], 1);
+    else bad = true;
+  }
+  if (bad) latch_error(status, kDevBadIndex);
+  __syncthreads();
+  int* out = counts + (size_t)blockIdx.x * E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) out[e] = hist[e];
+}
+
+// Exclusive block scan of one value per thread (blockDim.x <= 1024).
+__device__ int block_exclusive_scan(int v, int* warp_tot /*>= 33*/, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += n;
+  }
+  if (lane == 31) warp_tot[wid] = x;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int w = 0; w < nw; ++w) {
+      int t = warp_tot[w];
+      warp_tot[w] = acc;
+      acc += t;
+    }
+    warp_tot[32] = acc;
+  }
+  __syncthreads();
+  int r = warp_tot[wid] + x - v;
+  *total = warp_tot[32];
+  __syncthreads();
+  return r;
+}
+
+__global__ void __launch_bounds__(1024) perm_scan(int* __restrict__ counts, int C, int E,
+                                                  int32_t* __restrict__ seg_end,
+                                                  int* __restrict__ active,
+                                                  int* __restrict__ num_active) {
+  __shared__ int wt[33];
+  const int nthr = blockDim.x, tid = threadIdx.x;
+  const int per = (E + nthr - 1) / nthr;
+  const int lo = min(E, tid * per), hi = min(E, lo + per);
+  // per-expert totals of this thread's experts
+  int tot_local = 0, act_local = 0;
+  for (int e = lo; e < hi; ++e) {
+    int s = 0;
+    for (int c = 0; c < C; ++c) s += counts[(size_t)c * E + e];
+    tot_local += s;
+    act_local += s > 0;
+  }
+  int total, n_act;
+  int start = block_exclusive_scan(tot_local, wt, &total);
+  int astart = block_exclusive_scan(act_local, wt, &n_act);
+  for (int e = lo; e < hi; ++e) {
+    int run = start;
+    for (int c = 0; c < C; ++c) {
+      int* p = counts + (size_t)c * E + e;
+      int n = *p;
+      *p = run;  // becomes the first row of expert e's routes in chunk c
+      run += n;
+    }
+    seg_end[e] = run;
+    if (run > start) active[astart++] = e;
+    start = run;
+  }
+  if (tid == 0) *num_active = n_act;
+}
+
+__global__ void __launch_bounds__(32) perm_scatter(const int32_t* __restrict__ ids, int M, int E,
+                                                   const int* __restrict__ offsets,
+                                                   int32_t* __restrict__ row_to_route,
+                                                   int32_t* __restrict__ route_to_row) {
+  extern __shared__ int cur[];
+  const int lane = threadIdx.x;
+  const int* off = offsets + (size_t)blockIdx.x * E;
+  for (int e = lane; e < E; e += 32) cur[e] = off[e];
+  __syncwarp();
+  const int r0 = blockIdx.x * kPermuteChunk, r1 = min(M, r0 + kPermuteChunk);
+  constexpr int J = kPermuteChunk / 32;
+  int idv[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    int r = r0 + j * 32 + lane;
+    idv[j] = r < r1 ? __ldg(ids + r) : -1;
+  }
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int r = r0 + j * 32 + lane;
+    if (r0 + j * 32 >= r1) break;  // warp-uniform
+    const bool valid = r < r1;
+    const int id = idv[j];
+    const bool ok = valid && id >= 0 && id < E;
+    const int key = ok ? id : -1 - lane;  // invalid lanes never group
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    const int rank = __popc(peers & lt);
+    const int b = ok ? cur[id] : 0;
+    __syncwarp();
+    if (ok) {
+      const int row = b + rank;
+      row_to_route[row] = r;
+      route_to_row[r] = row;
+      if (rank == 0) cur[id] = b + __popc(peers);
+    } else if (valid) {
+      route_to_row[r] = -1;
+    }
+    __syncwarp();
+  }
+}
+
+// expert_input[row] = hidden[row_to_route[row] / K], rows < seg_end[E-1]
+template <int VEC_BYTES>
+__global__ void __launch_bounds__(256) perm_gather(const char* __restrict__ hidden,
+                                                   const int32_t* __restrict__ row_to_route,
+                                                   const int32_t* __restrict__ seg_end, int E,
+                                                   int K, int T, size_t row_bytes,
+                                                   char* __restrict__ out, int* status) {
+  const int warps = blockDim.x >> 5;
+  const int row = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int n_rows = seg_end[E - 1];
+  if (row >= n_rows) return;
+  const int r = row_to_route[row];
+  const int t = r / K;
+  if (r < 0 || t >= T) {
+    if (lane == 0) latch_error(status, kDevBadIndex);
+    return;
+  }
+  const char* src = hidden + (size_t)t * row_bytes;
+  char* dst = out + (size_t)row * row_bytes;
+  if constexpr (VEC_BYTES == 16) {
+    const int4* s4 = reinterpret_cast<const int4*>(src);
+    int4* d4 = reinterpret_cast<int4*>(dst);
+    const int n = (int)(row_bytes / 16);
+    int i = lane;
+    for (; i + 96 < n; i += 128) {
+      int4 a = __ldg(s4 + i), b = __ldg(s4 + i + 32), c = __ldg(s4 + i + 64), d = __ldg(s4 + i + 96);
+      d4[i] = a;
+      d4[i + 32] = b;
+      d4[i + 64] = c;
+      d4[i + 96] = d;
+    }
+    for (; i < n; i += 32) d4[i] = __ldg(s4 + i);
+  } else {
+    const uint16_t* s2 = reinterpret_cast<const uint16_t*>(src);
+    uint16_t* d2 = reinterpret_cast<uint16_t*>(dst);
+    for (size_t i = lane; i < row_bytes / 2; i += 32) d2[i] = s2[i];
+  }
+}
+
+// out[t] = scale * sum_k w[t,k] * y[route_to_row[t*K+k]], fixed k order, fp32
+template <typename T, int VEC>
+__global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y,
+                                                      const float* __restrict__ w,
+                                                      const int32_t* __restrict__ r2r, int Tn,
+                                                      int K, int H, int M, float scale,
+                                                      T* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int nvec = H / VEC;
+  const int v = blockIdx.y * blockDim.x + threadIdx.x;
+  if (v >= nvec) return;
+  float acc[VEC];
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
+  const int32_t* rr = r2r + (size_t)t * K;
+  const float* ww = w + (size_t)t * K;
+  for (int k = 0; k < K; ++k) {
+    const int row = __ldg(rr + k);
+    if (row < 0 || row >= M) continue;
+    const float wk = __ldg(ww + k);
+    const T* src = y + (size_t)row * H + (size_t)v * VEC;
+    if constexpr (VEC == 8) {  // bf16 x 8 = 16 bytes
+      int4 q = __ldg(reinterpret_cast<const int4*>(src));
+      const uint32_t u[4] = {(uint32_t)q.x, (uint32_t)q.y, (uint32_t)q.z, (uint32_t)q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = fmaf(wk, bf16_lo(u[i]), acc[2 * i]);
+        acc[2 * i + 1] = fmaf(wk, bf16_hi(u[i]), acc[2 * i + 1]);
+      }
+    } else if constexpr (VEC == 4) {  // f32 x 4
+      float4 q = __ldg(reinterpret_cast<const float4*>(src));
+      acc[0] = fmaf(wk, q.x, acc[0]);
+      acc[1] = fmaf(wk, q.y, acc[1]);
+      acc[2] = fmaf(wk, q.z, acc[2]);
+      acc[3] = fmaf(wk, q.w, acc[3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) acc[i] = fmaf(wk, Elem<T>::to_f(src[i]), acc[i]);
+    }
+  }
+  T* dst = out + (size_t)t * H + (size_t)v * VEC;
+  if constexpr (VEC == 8) {
+    int4 q;
+    q.x = (int)pack_bf16x2(scale * acc[0], scale * acc[1]);
+    q.y = (int)pack_bf16x2(scale * acc[2], scale * acc[3]);
+    q.z = (int)pack_bf16x2(scale * acc[4], scale * acc[5]);
+    q.w = (int)pack_bf16x2(scale * acc[6], scale * acc[7]);
+    *reinterpret_cast<int4*>(dst) = q;
+  } else if constexpr (VEC == 4) {
+    *reinterpret_cast<float4*>(dst) =
+        make_float4(scale * acc[0], scale * acc[1], scale * acc[2], scale * acc[3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) dst[i] = Elem<T>::from_f(scale * acc[i]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int T, int H, int E,
+                           int K, void* expert_input, int32_t* seg_end, int32_t* row_to_route,
+                           int32_t* route_to_row, void* ws, cudaStream_t s) {
+  const int M = T * K;
+  PermuteWs L(M, E);
+  char* w = static_cast<char*>(ws);
+  int* status = reinterpret_cast<int*>(w);
+  int* counts = reinterpret_cast<int*>(w + L.counts);
+  int* active = reinterpret_cast<int*>(w + L.active);
+  int* num_active = reinterpret_cast<int*>(w + L.num_active);
+  if (M == 0) {
+    cudaMemsetAsync(seg_end, 0, (size_t)E * 4, s);
+    cudaMemsetAsync(num_active, 0, 4, s);
+    return cudaGetLastError();
+  }
+  const int C = (M + kPermuteChunk - 1) / kPermuteChunk;
+  const size_t hist_smem = (size_t)E * 4;
+  perm_count<<<C, 256, hist_smem, s>>>(ids, M, E, counts, status);
+  perm_scan<<<1, 1024, 0, s>>>(counts, C, E, seg_end, active, num_active);
+  perm_scatter<<<C, 32, hist_smem, s>>>(ids, M, E, counts, row_to_route, route_to_row);
+  count_launch(3);
+  if (expert_input) {
+    const size_t row_bytes = (size_t)H * esz;
+    const int rows_per_block = 8;
+    dim3 grid((M + rows_per_block - 1) / rows_per_block);
+    const bool vec = (row_bytes % 16 == 0) && ((uintptr_t)hidden % 16 == 0) &&
+                     ((uintptr_t)expert_input % 16 == 0);
+    if (vec)
+      perm_gather<16><<<grid, 256, 0, s>>>(static_cast<const char*>(hidden), row_to_route,
+                                           seg_end, E, K, T, row_bytes,
+                                           static_cast<char*>(expert_input), status);
+    else
+      perm_gather<2><<<grid, 256, 0, s>>>(static_cast<const char*>(hidden), row_to_route, seg_end,
+                                          E, K, T, row_bytes, static_cast<char*>(expert_input),
+                                          status);
+    count_launch();
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y, const float* w, const int32_t* r2r, int T, int K, int H,
+                           moe_dtype dt, float scale, void* out, cudaStream_t s) {
+  if (T == 0 || H == 0) return cudaSuccess;
+  const int M = T * K;
+  const bool aligned = ((uintptr_t)y % 16 == 0) && ((uintptr_t)out % 16 == 0);
+  if (dt == MOE_BF16) {
+    using B = __nv_bfloat16;
+    if (aligned && H % 8 == 0) {
+      int nvec = H / 8;
+      dim3 grid(T, (nvec + 127) / 128);
+      combine_kernel<B, 8><<<grid, 128, 0, s>>>(static_cast<const B*>(y), w, r2r, T, K, H, M,
+                                                scale, static_cast<B*>(out));
+    } else {
+      dim3 grid(T, (H + 127) / 128);
+      combine_kernel<B, 1><<<grid, 128, 0, s>>>(static_cast<const B*>(y), w, r2r, T, K, H, M,
+                                                scale, static_cast<B*>(out));
+    }
+  } else {
+    if (aligned && H % 4 == 0) {
+      int nvec = H / 4;
+      dim3 grid(T, (nvec + 127) / 128);
+      combine_kernel<float, 4><<<grid, 128, 0, s>>>(static_cast<const float*>(y), w, r2r, T, K, H,
+                                                    M, scale, static_cast<float*>(out));
+    } else {
+      dim3 grid(T, (H + 127) / 128);
+      combine_kernel<float, 1><<<grid, 128, 0, s>>>(static_cast<const float*>(y), w, r2r, T, K, H,
+                                                    M, scale, static_cast<float*>(out));
+    }
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

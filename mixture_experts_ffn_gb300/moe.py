@@ -1,0 +1,319 @@
+"""Thin Python binding over libmoe.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls, takes CUDA
+tensors, allocates missing outputs and workspaces with torch, and calls the C
+ABI on the current torch stream.  All arithmetic runs in the library's CUDA
+kernels; there is no Python or CPU fallback, and every call raises if the
+library is missing or the device is not a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_OVERLAP, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, \
+    MOE_ERR_TIMEOUT, MOE_ERR_DEVICE, MOE_ERR_WORKSPACE = range(8)
+MOE_F32, MOE_BF16 = 0, 1
+MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
+MOE_ACT_SILU_AND_MUL, MOE_ACT_SWIGLU, MOE_ACT_IDENTITY = 0, 1, 2
+MOE_STATUS_BYTES = 256
+
+# C entry points and their argument types (mirrors include/moe.h)
+_vp, _i, _i64, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, \
+    ctypes.c_size_t
+
+
+class RouteParams(ctypes.Structure):
+    _fields_ = [("top_k", ctypes.c_int32), ("scoring", ctypes.c_int32),
+                ("renormalize", ctypes.c_int32), ("num_expert_group", ctypes.c_int32),
+                ("topk_group", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
+                ("local_expert_start", ctypes.c_int32), ("local_expert_count", ctypes.c_int32),
+                ("route_scale", ctypes.c_float)]
+
+
+class ActParams(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("swiglu_fusion", ctypes.c_int32),
+                ("limit", ctypes.c_float), ("alpha", ctypes.c_float), ("beta", ctypes.c_float)]
+
+
+_SIGNATURES = {
+    "moe_route": [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp],
+    "moe_permute": [_vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
+    "moe_grouped_gemm_act": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp],
+    "moe_grouped_gemm_down": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
+    "moe_combine": [_vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _vp],
+    "swiglu": [_vp, _vp, _i64, _i, _i, _i, _f, _f, _f, _vp, _vp],
+    "moe_indexed_mlp": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp],
+    "moe_ffn_forward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp,
+                        _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
+    "moe_workspace_size": [_i, _i, _i, _i, _i, _i],
+    "moe_permute_workspace_size": [_i, _i],
+    "moe_clear_status": [_vp, _vp],
+    "moe_sync_status": [_vp, _vp],
+    "moe_status_string": [_i],
+    "moe_launch_count": [],
+    "moe_set_gemm_simt": [_i],
+}
+_RESTYPES = {"moe_workspace_size": _sz, "moe_permute_workspace_size": _sz,
+             "moe_status_string": ctypes.c_char_p, "moe_launch_count": ctypes.c_uint64}
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libmoe.so (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with "
+                               "`python -m mixture_experts_ffn_gb300.build`")
+        lib = ctypes.CDLL(path)
+        for name, args in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = _RESTYPES.get(name, ctypes.c_int)
+        _lib = lib
+    return _lib
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = load_library().moe_status_string(status).decode()
+        super().__init__(f"{fn}: {msg} (status {status})")
+        self.status = status
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoEError(fn, status)
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return MOE_BF16
+    if t.dtype == torch.float32:
+        return MOE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("libmoe takes CUDA tensors only")
+            if not t.is_contiguous():
+                raise ValueError("libmoe takes contiguous tensors only")
+
+
+def _ws(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(nbytes, MOE_STATUS_BYTES), dtype=torch.uint8, device=device)
+
+
+def route_params(top_k, scoring="softmax", renormalize=True, num_expert_group=1, topk_group=1,
+                 routed_scaling_factor=1.0, local_expert_start=0, local_expert_count=0,
+                 route_scale=1.0) -> RouteParams:
+    sc = {"softmax": MOE_SCORING_SOFTMAX, "sigmoid": MOE_SCORING_SIGMOID}.get(scoring, scoring)
+    return RouteParams(top_k, sc, int(bool(renormalize)), num_expert_group, topk_group,
+                       routed_scaling_factor, local_expert_start, local_expert_count, route_scale)
+
+
+def act_params(kind=MOE_ACT_SILU_AND_MUL, swiglu_fusion=2, limit=0.0, alpha=1.0,
+               beta=0.0) -> ActParams:
+    return ActParams(kind, swiglu_fusion, limit, alpha, beta)
+
+
+# ----------------------------------------------------------------- entry points
+def moe_workspace_size(T, H, F, E, K, dtype=MOE_BF16) -> int:
+    return load_library().moe_workspace_size(T, H, F, E, K, dtype)
+
+
+def moe_permute_workspace_size(M, E) -> int:
+    return load_library().moe_permute_workspace_size(M, E)
+
+
+def moe_route(logits, p: RouteParams, correction_bias=None, expert_ids=None, topk_weights=None,
+              topk_ids=None, router_probs=None, weight_scale=None):
+    """Router; returns (topk_weights, topk_ids, router_probs, weight_scale)."""
+    lib = load_library()
+    _cuda(logits, correction_bias, expert_ids)
+    T, E = logits.shape
+    dev = logits.device
+    if topk_weights is None:
+        topk_weights = torch.empty((T, p.top_k), dtype=torch.float32, device=dev)
+    if topk_ids is None:
+        topk_ids = torch.empty((T, p.top_k), dtype=torch.int32, device=dev)
+    if p.local_expert_count > 0:
+        if router_probs is None:
+            router_probs = torch.empty((T, p.local_expert_count), dtype=torch.float32, device=dev)
+        if weight_scale is None:
+            weight_scale = torch.empty((T,), dtype=torch.float32, device=dev)
+    _check("moe_route", lib.moe_route(_p(logits), _p(correction_bias), _p(expert_ids), T, E,
+                                      ctypes.byref(p), _p(topk_weights), _p(topk_ids),
+                                      _p(router_probs), _p(weight_scale), _stream()))
+    return topk_weights, topk_ids, router_probs, weight_scale
+
+
+def moe_permute(topk_ids, E: int, hidden=None, ws=None, with_gather=True):
+    """Returns dict(expert_input, seg_end, row_to_route, route_to_row, ws)."""
+    lib = load_library()
+    _cuda(topk_ids, hidden)
+    T, K = topk_ids.shape
+    M = T * K
+    dev = topk_ids.device
+    H = hidden.shape[1] if hidden is not None else 0
+    dt = _dt(hidden) if hidden is not None else MOE_BF16
+    xin = None
+    if with_gather and hidden is not None:
+        xin = torch.empty((M, H), dtype=hidden.dtype, device=dev)
+    seg_end = torch.empty((E,), dtype=torch.int32, device=dev)
+    r2r = torch.empty((M,), dtype=torch.int32, device=dev)
+    route_to_row = torch.empty((M,), dtype=torch.int32, device=dev)
+    need = lib.moe_permute_workspace_size(M, E)
+    if ws is None:
+        ws = _ws(need, dev)
+    _check("moe_permute", lib.moe_permute(_p(hidden if xin is not None else None), dt,
+                                          _p(topk_ids), T, H, E, K, _p(xin), _p(seg_end), _p(r2r),
+                                          _p(route_to_row), _p(ws), ws.numel(), _stream()))
+    return {"expert_input": xin, "seg_end": seg_end, "row_to_route": r2r,
+            "route_to_row": route_to_row, "ws": ws}
+
+
+def moe_grouped_gemm_act(a, w_gate_up, seg_end, F: int, act: ActParams, b_gate_up=None, out=None,
+                         ws=None):
+    lib = load_library()
+    _cuda(a, w_gate_up, seg_end, b_gate_up)
+    M, Hk = a.shape
+    E = w_gate_up.shape[0]
+    if out is None:
+        out = torch.empty((M, F), dtype=a.dtype, device=a.device)
+    if ws is None:
+        ws = _ws(MOE_STATUS_BYTES, a.device)
+        lib.moe_clear_status(_p(ws), _stream())
+    _check("moe_grouped_gemm_act",
+           lib.moe_grouped_gemm_act(_p(a), _p(w_gate_up), _p(b_gate_up), _p(seg_end), M, F, Hk, E,
+                                    _dt(a), ctypes.byref(act), _p(out), _p(ws), ws.numel(),
+                                    _stream()))
+    return out
+
+
+def moe_grouped_gemm_down(a, w_down, seg_end, b_down=None, out=None, ws=None):
+    lib = load_library()
+    _cuda(a, w_down, seg_end, b_down)
+    M, F = a.shape
+    E, H, _ = w_down.shape
+    if out is None:
+        out = torch.empty((M, H), dtype=a.dtype, device=a.device)
+    if ws is None:
+        ws = _ws(MOE_STATUS_BYTES, a.device)
+        lib.moe_clear_status(_p(ws), _stream())
+    _check("moe_grouped_gemm_down",
+           lib.moe_grouped_gemm_down(_p(a), _p(w_down), _p(b_down), _p(seg_end), M, H, F, E,
+                                     _dt(a), _p(out), _p(ws), ws.numel(), _stream()))
+    return out
+
+
+def moe_combine(expert_out, topk_weights, route_to_row, scale=1.0, out=None):
+    lib = load_library()
+    _cuda(expert_out, topk_weights, route_to_row)
+    T, K = topk_weights.shape
+    H = expert_out.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=expert_out.dtype, device=expert_out.device)
+    _check("moe_combine", lib.moe_combine(_p(expert_out), _p(topk_weights), _p(route_to_row), T, K,
+                                          H, _dt(expert_out), scale, _p(out), _stream()))
+    return out
+
+
+def swiglu(gate, up=None, swiglu_fusion=2, limit=0.0, alpha=1.0, beta=0.0, out=None):
+    """The standalone SwiGLU op.  gate [R, 2I] (up None) or gate, up [R, I]."""
+    lib = load_library()
+    _cuda(gate, up)
+    R = gate.shape[0]
+    I = gate.shape[1] if up is not None else gate.shape[1] // 2
+    if out is None:
+        out = torch.empty((R, I), dtype=gate.dtype, device=gate.device)
+    _check("swiglu", lib.swiglu(_p(gate), _p(up), R, I, _dt(gate), swiglu_fusion, limit, alpha,
+                                beta, _p(out), _stream()))
+    return out
+
+
+def moe_indexed_mlp(hidden, w_gate_up, w_down, topk_weights, topk_ids, scale=1.0, out=None,
+                    ws=None):
+    lib = load_library()
+    _cuda(hidden, w_gate_up, w_down, topk_weights, topk_ids)
+    T, H = hidden.shape
+    E, H2, F = w_down.shape
+    K = topk_ids.shape[1]
+    if out is None:
+        out = torch.empty((T, H), dtype=hidden.dtype, device=hidden.device)
+    if ws is None:
+        ws = _ws(lib.moe_workspace_size(T, H, F, E, K, MOE_BF16), hidden.device)
+        lib.moe_clear_status(_p(ws), _stream())
+    _check("moe_indexed_mlp",
+           lib.moe_indexed_mlp(_p(hidden), _p(w_gate_up), _p(w_down), _p(topk_weights),
+                               _p(topk_ids), T, H, F, E, K, scale, _p(out), _p(ws), ws.numel(),
+                               _stream()))
+    return out
+
+
+def moe_ffn_forward(hidden, logits, w_gate_up, w_down, p: RouteParams, act: ActParams,
+                    correction_bias=None, expert_ids=None, b_gate_up=None, b_down=None, out=None,
+                    topk_weights_out=None, topk_ids_out=None, router_probs=None,
+                    weight_scale=None, ws=None):
+    """The whole routed MoE FFN forward; returns ``out`` [T, H]."""
+    lib = load_library()
+    _cuda(hidden, logits, w_gate_up, w_down, correction_bias, expert_ids, b_gate_up, b_down)
+    T, H = hidden.shape
+    E, _, F = w_down.shape
+    if out is None:
+        out = torch.empty_like(hidden)
+    if ws is None:
+        ws = _ws(lib.moe_workspace_size(T, H, F, E, p.top_k, _dt(hidden)), hidden.device)
+        lib.moe_clear_status(_p(ws), _stream())
+    _check("moe_ffn_forward",
+           lib.moe_ffn_forward(_p(hidden), _p(logits), _p(w_gate_up), _p(w_down),
+                               _p(correction_bias), _p(expert_ids), _p(b_gate_up), _p(b_down), T,
+                               H, F, E, _dt(hidden), ctypes.byref(p), ctypes.byref(act), _p(out),
+                               _p(topk_weights_out), _p(topk_ids_out), _p(router_probs),
+                               _p(weight_scale), _p(ws), ws.numel(), _stream()))
+    return out
+
+
+def moe_clear_status(ws):
+    _check("moe_clear_status", load_library().moe_clear_status(_p(ws), _stream()))
+
+
+def moe_sync_status(ws) -> int:
+    """Synchronise the current stream and return (and clear) the status word."""
+    return load_library().moe_sync_status(_p(ws), _stream())
+
+
+def moe_launch_count() -> int:
+    return load_library().moe_launch_count()
+
+
+def moe_set_gemm_simt(enable: bool) -> bool:
+    return bool(load_library().moe_set_gemm_simt(int(bool(enable))))
+
+
+def config_params(cfg):
+    """(RouteParams, ActParams) of a synthetic workload recipe (see synth.MoEConfig)."""
+    p = route_params(cfg.K, cfg.scoring, cfg.renormalize, cfg.G, cfg.TG, cfg.rsf,
+                     cfg.local_start, cfg.local_count, cfg.route_scale)
+    a = act_params(cfg.act, cfg.swiglu_fusion, cfg.limit, cfg.alpha, cfg.beta)
+    return p, a

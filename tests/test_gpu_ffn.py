@@ -1,0 +1,171 @@
+"""The whole forward through moe_ffn_forward against the oracle, on every
+workload recipe: reduced sizes (all tokens checked) and the full sizes the
+benchmark runs (routing and permutation on all tokens, outputs on the fixed
+256-token subset for the large recipes), plus the indexed decode path, the
+dispatch rule, determinism and the device status word."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_ffn_gb300 import synth
+from oracle import moe_oracle as O
+
+from gpu_cases import act_kwargs, make, np_
+from tolerances import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_ffn_gb300 import build, moe as m
+
+    build.build()
+    return m
+
+
+def run_forward(moe, cfg, inp):
+    p, a = moe.config_params(cfg)
+    T = cfg.T
+    tw = torch.empty((T, cfg.K), dtype=torch.float32, device="cuda")
+    ti = torch.empty((T, cfg.K), dtype=torch.int32, device="cuda")
+    probs = wsc = None
+    if cfg.local_count:
+        probs = torch.empty((T, cfg.local_count), dtype=torch.float32, device="cuda")
+        wsc = torch.empty((T,), dtype=torch.float32, device="cuda")
+    ws = torch.empty(moe.moe_workspace_size(T, cfg.H, cfg.F, cfg.E, cfg.K,
+                                            moe.MOE_BF16 if cfg.dtype == "bf16" else moe.MOE_F32),
+                     dtype=torch.uint8, device="cuda")
+    moe.moe_clear_status(ws)
+    out = moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a,
+                              inp["correction_bias"], inp["expert_ids"], inp["b_gate_up"],
+                              inp["b_down"], topk_weights_out=tw, topk_ids_out=ti,
+                              router_probs=probs, weight_scale=wsc, ws=ws)
+    status = moe.moe_sync_status(ws)
+    return out, tw, ti, probs, wsc, status
+
+
+def oracle_forward(cfg, ref, tokens=None):
+    return O.ffn_forward(ref["hidden"], ref["logits"], ref["w_gate_up"], ref["w_down"],
+                         correction_bias=ref["correction_bias"], expert_ids=ref["expert_ids"],
+                         b_gate_up=ref["b_gate_up"], b_down=ref["b_down"], K=cfg.K, F=cfg.F,
+                         scoring=cfg.scoring, renormalize=cfg.renormalize, G=cfg.G, TG=cfg.TG,
+                         rsf=cfg.rsf, dtype=cfg.dtype, local_start=cfg.local_start,
+                         local_count=cfg.local_count, route_scale=cfg.route_scale, tokens=tokens,
+                         **act_kwargs(cfg))
+
+
+def check(moe, cfg, tokens=None):
+    inp, ref = make(cfg)
+    out, tw, ti, probs, wsc, status = run_forward(moe, cfg, inp)
+    assert status == moe.MOE_OK
+    # routing on all tokens
+    r_all = O.route(ref["logits"], cfg.K, cfg.scoring, cfg.renormalize, cfg.G, cfg.TG, cfg.rsf,
+                    ref["correction_bias"], ref["expert_ids"], cfg.local_start, cfg.local_count,
+                    cfg.route_scale)
+    np.testing.assert_array_equal(np_(ti), r_all["topk_ids"])
+    np.testing.assert_allclose(np_(tw), r_all["topk_weights"], rtol=1e-5)
+    if cfg.local_count:
+        sent = r_all["router_probs"] == -1e30
+        got = np_(probs)
+        np.testing.assert_array_equal(got == np.float32(-1e30), sent)
+        np.testing.assert_allclose(got[~sent], r_all["router_probs"][~sent], atol=1e-5)
+        np.testing.assert_allclose(np_(wsc), r_all["weight_scale"], rtol=1e-5, atol=1e-7)
+    # outputs on the token subset
+    r = oracle_forward(cfg, ref, tokens)
+    tok = r["tokens"]
+    got = np_(out)[tok]
+    return assert_close(got, r["out"], cfg.dtype, cfg.name), out
+
+
+SMALL = {
+    "tiny_fp32": {},
+    "qwen3_bf16": dict(T=300, H=256, F=192, E=32, K=8, local_start=8, local_count=8),
+    "deepseek_v3_bf16": dict(T=300, H=320, F=128, E=64, K=8, G=8, TG=4),
+    "gpt_oss_bf16": dict(T=200, H=192, F=160, E=16, K=4),
+    "kimi_k2_decode_bf16": dict(T=16, H=256, F=256, E=96, K=8),
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_ffn_small(moe, name):
+    cfg = synth.CONFIGS[name].replace(**SMALL[name])
+    check(moe, cfg)
+
+
+def test_ffn_small_hash_routing(moe):
+    cfg = synth.CONFIGS["kimi_k2_decode_bf16"].replace(hash_ids=True, T=16, H=256, F=256, E=96)
+    check(moe, cfg)
+
+
+@pytest.mark.parametrize("name,hash_ids", [
+    ("tiny_fp32", False),
+    ("qwen3_bf16", False),
+    ("gpt_oss_bf16", False),
+    ("kimi_k2_decode_bf16", False),
+    ("kimi_k2_decode_bf16", True),
+    ("deepseek_v3_bf16", False),
+])
+def test_ffn_full_size(moe, name, hash_ids):
+    cfg = synth.CONFIGS[name].replace(hash_ids=hash_ids)
+    tokens = None if cfg.T <= 4096 else synth.subset_tokens(cfg.T)
+    if name == "gpt_oss_bf16":
+        tokens = synth.subset_tokens(cfg.T)
+    rep, _ = check(moe, cfg, tokens)
+    print(name, rep)
+
+
+def test_indexed_path_matches_staged(moe):
+    """The decode recipe satisfies the dispatch rule; the indexed kernels and the
+    staged pipeline compute the same layer (both checked against the oracle)."""
+    cfg = synth.CONFIGS["kimi_k2_decode_bf16"].replace(H=1024, F=512, E=64)
+    inp, ref = make(cfg)
+    p, a = moe.config_params(cfg)
+    w, ids, _, _ = moe.moe_route(inp["logits"], p, inp["correction_bias"])
+    y_idx = moe.moe_indexed_mlp(inp["hidden"], inp["w_gate_up"], inp["w_down"], w, ids)
+    perm = moe.moe_permute(ids, cfg.E, inp["hidden"])
+    act = moe.moe_grouped_gemm_act(perm["expert_input"], inp["w_gate_up"], perm["seg_end"], cfg.F, a)
+    y = moe.moe_grouped_gemm_down(act, inp["w_down"], perm["seg_end"])
+    y_st = moe.moe_combine(y, w, perm["route_to_row"])
+    torch.cuda.synchronize()
+    r = oracle_forward(cfg, ref)
+    assert_close(np_(y_idx), r["out"], "bf16", "indexed")
+    assert_close(np_(y_st), r["out"], "bf16", "staged")
+
+
+def test_forward_is_deterministic(moe):
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=512, H=512, F=256, E=64)
+    inp, _ = make(cfg)
+    o1 = run_forward(moe, cfg, inp)[0].clone()
+    o2 = run_forward(moe, cfg, inp)[0]
+    assert torch.equal(o1, o2)
+
+
+def test_forward_bad_hash_ids_latch_device_error(moe):
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=64, H=128, F=64, E=16, K=2)
+    inp, _ = make(cfg)
+    ids = torch.randint(0, 16, (64, 2), dtype=torch.int32, device="cuda")
+    ids[5, 1] = 99
+    inp["expert_ids"] = ids
+    *_, status = run_forward(moe, cfg, inp)
+    assert status == moe.MOE_ERR_DEVICE
+
+
+def test_forward_rejects_overlap_without_writing(moe):
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=64, H=128, F=64, E=16, K=2)
+    inp, _ = make(cfg)
+    p, a = moe.config_params(cfg)
+    before = inp["hidden"].clone()
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a,
+                            out=inp["hidden"])
+    assert ei.value.status == moe.MOE_ERR_OVERLAP
+    assert torch.equal(before, inp["hidden"])
+
+
+def test_empty_batch(moe):
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=0, H=128, F=64, E=16, K=2)
+    inp, _ = make(cfg, guard=False)
+    p, a = moe.config_params(cfg)
+    out = moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a)
+    assert out.shape == (0, 128)

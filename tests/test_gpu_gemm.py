@@ -1,0 +1,134 @@
+"""Grouped GEMMs (gate_up + fused activation, and down) against the oracle on
+ragged expert segments: empty experts, segments shorter and longer than a
+128-row tile, column tiles and k-blocks with ragged tails, every activation
+layout, with and without bias, on the tcgen05 path, the SIMT path and fp32."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as O
+
+from gpu_cases import LazyExperts, np_
+from tolerances import assert_rounded_once
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_ffn_gb300 import build, moe as m
+
+    build.build()
+    return m
+
+
+def _problem(counts, Hk, N1, dtype, bias, seed):
+    g = torch.Generator().manual_seed(seed)
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    E = len(counts)
+    M = int(sum(counts))
+    a = torch.randn((M, Hk), generator=g).to(tdt)
+    w = (torch.randn((E, N1, Hk), generator=g) / Hk ** 0.5).to(tdt)
+    b = (torch.randn((E, N1), generator=g) * 0.02).to(tdt) if bias else None
+    seg_end = torch.tensor(np.cumsum(counts), dtype=torch.int32)
+    return a, w, b, seg_end
+
+
+ACTS = {
+    "silu": dict(kind=0, swiglu_fusion=2),
+    "swiglu_inter": dict(kind=1, swiglu_fusion=1, limit=7.0, alpha=1.702, beta=1.0),
+    "swiglu_concat": dict(kind=1, swiglu_fusion=2, limit=3.0, alpha=1.0, beta=0.0),
+    "swiglu_noclamp": dict(kind=1, swiglu_fusion=1, limit=0.0, alpha=1.3, beta=0.5),
+    "identity": dict(kind=2),
+}
+
+
+@pytest.mark.parametrize("counts,Hk,F,act,bias,dtype,simt", [
+    ([3, 0, 130, 1, 300], 256, 192, "silu", False, "bf16", False),
+    ([129, 127, 0, 256], 320, 160, "swiglu_inter", True, "bf16", False),
+    ([129, 127, 0, 256], 320, 160, "swiglu_concat", True, "bf16", False),
+    ([50, 0, 0, 77, 200], 200, 96, "swiglu_noclamp", False, "bf16", False),  # ragged k-block
+    ([200, 56, 100], 128, 384, "identity", True, "bf16", False),
+    ([1], 64, 8, "silu", False, "bf16", False),                              # one row
+    ([0, 0, 0, 5], 64, 128, "silu", True, "bf16", False),                    # leading empty experts
+    ([3, 0, 130, 1, 300], 256, 192, "silu", True, "bf16", True),             # SIMT, bf16
+    ([129, 127, 0, 256], 320, 160, "swiglu_inter", True, "bf16", True),
+    ([16] * 8, 128, 64, "silu", False, "f32", False),                        # fp32 (SIMT)
+    ([40, 0, 25, 63], 100, 50, "swiglu_inter", True, "f32", False),
+    ([300, 5, 0, 211], 132, 36, "silu", False, "bf16", False),               # F % 8 != 0 -> SIMT
+])
+def test_gemm_act(moe, counts, Hk, F, act, bias, dtype, simt):
+    spec = ACTS[act]
+    N1 = F if spec["kind"] == 2 else 2 * F
+    a, w, b, seg_end = _problem(counts, Hk, N1, dtype, bias, seed=len(counts) * 1000 + Hk)
+    M = a.shape[0]
+    p = moe.act_params(**spec)
+    out = torch.full((M + 7, F), float("nan"), dtype=a.dtype, device="cuda")  # + unwritten rows
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    old = moe.moe_set_gemm_simt(simt)
+    try:
+        a_pad = torch.cat([a, torch.zeros((7, Hk), dtype=a.dtype)])  # rows outside every segment
+        moe.moe_grouped_gemm_act(a_pad.cuda(), w.cuda(),
+                                 seg_end.cuda(), F, p, None if b is None else b.cuda(),
+                                 out=out, ws=ws)
+        assert moe.moe_sync_status(ws) == moe.MOE_OK
+    finally:
+        moe.moe_set_gemm_simt(old)
+    exact = O.grouped_gemm_act(np_(a), np_(w), np_(seg_end), F, spec["kind"],
+                               spec.get("swiglu_fusion", 2), spec.get("limit", 0.0),
+                               spec.get("alpha", 1.0), spec.get("beta", 0.0),
+                               None if b is None else np_(b), dtype=None)
+    got = np_(out)
+    assert np.isnan(got[M:]).all(), "rows past the last segment were written"
+    assert_rounded_once(got[:M], exact, dtype, f"gemm_act {act}")
+
+
+@pytest.mark.parametrize("counts,F,H,bias,dtype,simt", [
+    ([3, 0, 130, 1, 300], 192, 320, True, "bf16", False),
+    ([257, 0, 31], 128, 256, False, "bf16", False),
+    ([10, 20, 0, 400], 72, 136, True, "bf16", False),      # ragged k-block (72 = 64 + 8)
+    ([3, 0, 130, 1, 300], 192, 320, True, "bf16", True),
+    ([16] * 8, 64, 128, False, "f32", False),
+])
+def test_gemm_down(moe, counts, F, H, bias, dtype, simt):
+    a, w, b, seg_end = _problem(counts, F, H, dtype, bias, seed=7 + F)
+    M = a.shape[0]
+    out = torch.full((M, H), float("nan"), dtype=a.dtype, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    old = moe.moe_set_gemm_simt(simt)
+    try:
+        moe.moe_grouped_gemm_down(a.cuda(), w.cuda(), seg_end.cuda(),
+                                  None if b is None else b.cuda(), out=out, ws=ws)
+        assert moe.moe_sync_status(ws) == moe.MOE_OK
+    finally:
+        moe.moe_set_gemm_simt(old)
+    exact = O.grouped_gemm_down(np_(a), np_(w), np_(seg_end), None if b is None else np_(b),
+                                dtype=None)
+    assert_rounded_once(np_(out), exact, dtype, "gemm_down")
+
+
+def test_gemm_act_large_sampled(moe):
+    """Qwen3-style shapes (32768 rows over 128 experts, H 2048, F 768) on the
+    tcgen05 path; the oracle checks the rows of four experts and 64 random rows."""
+    g = torch.Generator().manual_seed(5)
+    E, Hk, F = 128, 2048, 768
+    counts = torch.multinomial(torch.ones(E), 32768, replacement=True, generator=g)
+    counts = torch.bincount(counts, minlength=E).numpy()
+    a = torch.randn((32768, Hk), generator=g).to(torch.bfloat16).cuda()
+    gw = torch.Generator(device="cuda").manual_seed(6)
+    w = (torch.randn((E, 2 * F, Hk), generator=gw, device="cuda") / Hk ** 0.5).to(torch.bfloat16)
+    seg_end = torch.tensor(np.cumsum(counts), dtype=torch.int32, device="cuda")
+    out = moe.moe_grouped_gemm_act(a, w, seg_end, F, moe.act_params(0))
+    torch.cuda.synchronize()
+    ends = np.cumsum(counts)
+    starts = ends - counts
+    rows = set()
+    for e in (0, 1, 77, 127):
+        rows.update(range(starts[e], ends[e]))
+    rows.update(np.random.default_rng(0).integers(0, 32768, 64).tolist())
+    rows = np.array(sorted(rows))
+    exp_of_row = np.searchsorted(ends, rows, side="right")
+    sub_counts = np.bincount(exp_of_row, minlength=E)
+    a_np = a[torch.from_numpy(rows).cuda()].float().cpu().numpy()
+    exact = O.grouped_gemm_act(a_np, LazyExperts(w), np.cumsum(sub_counts), F, 0, dtype=None)
+    assert_rounded_once(np_(out)[rows], exact, "bf16", "gemm_act large")

@@ -1,0 +1,110 @@
+"""Router kernel against the oracle: ids bit-exact, weights within 1e-5
+relative (the pages allow 1e-4), MoERouter outputs, hash routing, ties and
+edge cases."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_ffn_gb300 import synth
+from oracle import moe_oracle as O
+from oracle import cases
+
+from gpu_cases import make, np_
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_ffn_gb300 import build, moe as m
+
+    build.build()
+    return m
+
+
+def _route_both(moe, cfg, inp, ref):
+    p, _ = moe.config_params(cfg)
+    w, ids, probs, ws = moe.moe_route(inp["logits"], p, inp["correction_bias"], inp["expert_ids"])
+    torch.cuda.synchronize()
+    r = O.route(ref["logits"], cfg.K, cfg.scoring, cfg.renormalize, cfg.G, cfg.TG, cfg.rsf,
+                ref["correction_bias"], ref["expert_ids"], cfg.local_start, cfg.local_count,
+                cfg.route_scale)
+    return (np_(w), np_(ids), None if probs is None else np_(probs),
+            None if ws is None else np_(ws)), r
+
+
+@pytest.mark.parametrize("name", list(synth.CONFIGS))
+def test_route_configs(moe, name):
+    cfg = synth.CONFIGS[name]
+    inp, ref = make(cfg.replace(H=64, F=64))  # routing does not depend on H, F
+    (w, ids, probs, wsc), r = _route_both(moe, cfg, inp, ref)
+    np.testing.assert_array_equal(ids, r["topk_ids"])
+    np.testing.assert_allclose(w, r["topk_weights"], rtol=1e-5)
+    if cfg.local_count:
+        sent = r["router_probs"] == -1e30
+        np.testing.assert_array_equal(probs == np.float32(-1e30), sent)
+        np.testing.assert_allclose(probs[~sent], r["router_probs"][~sent], rtol=0, atol=1e-5)
+        np.testing.assert_allclose(wsc, r["weight_scale"], rtol=1e-5, atol=1e-7)
+
+
+@pytest.mark.parametrize("hash_ids", [False, True])
+def test_route_decode_hash(moe, hash_ids):
+    cfg = synth.CONFIGS["kimi_k2_decode_bf16"].replace(hash_ids=hash_ids, H=128, F=256,
+                                                       local_start=100, local_count=64)
+    inp, ref = make(cfg)
+    (w, ids, probs, wsc), r = _route_both(moe, cfg, inp, ref)
+    np.testing.assert_array_equal(ids, r["topk_ids"])
+    np.testing.assert_allclose(w, r["topk_weights"], rtol=1e-5)
+    sent = r["router_probs"] == -1e30
+    np.testing.assert_array_equal(probs == np.float32(-1e30), sent)
+    np.testing.assert_allclose(probs[~sent], r["router_probs"][~sent], atol=1e-5)
+    np.testing.assert_allclose(wsc, r["weight_scale"], rtol=1e-5, atol=1e-7)
+
+
+def test_route_ties_and_edges(moe):
+    dev = "cuda"
+    # equal logits: ids 0..K-1, weights 1/K
+    z = torch.zeros((5, 16), device=dev)
+    w, ids, _, _ = moe.moe_route(z, moe.route_params(4, "softmax", True))
+    assert (np_(ids) == np.arange(4)).all()
+    np.testing.assert_allclose(np_(w), 0.25, rtol=1e-6)
+    # K = E selects everything, in ascending order
+    z = torch.randn((33, 12), device=dev)
+    w, ids, _, _ = moe.moe_route(z, moe.route_params(12, "sigmoid", False))
+    assert (np_(ids) == np.arange(12)).all()
+    # E = 1, K = 1
+    z = torch.randn((7, 1), device=dev)
+    w, ids, _, _ = moe.moe_route(z, moe.route_params(1, "softmax", True, routed_scaling_factor=2.0))
+    assert (np_(ids) == 0).all()
+    np.testing.assert_allclose(np_(w), 2.0, rtol=1e-6)
+    # E not a multiple of 32, groups, bias, T = 1
+    for E, G, TG, K in ((96, 4, 2, 6), (40, 8, 3, 5), (1000, 8, 4, 8), (250, 1, 1, 7)):
+        cfg = synth.MoEConfig("edge", 9, T=1 if E == 250 else 77, H=8, F=8, E=E, K=K,
+                              scoring="sigmoid", G=G, TG=TG, rsf=1.5, cbias_std=0.1 if G > 1 else None)
+        inp, ref = make(cfg)
+        (w, ids, _, _), r = _route_both(moe, cfg, inp, ref)
+        np.testing.assert_array_equal(ids, r["topk_ids"])
+        np.testing.assert_allclose(w, r["topk_weights"], rtol=1e-5)
+
+
+def test_route_golden_cases_on_gpu(moe):
+    import json
+    import os
+
+    path = os.path.join(os.path.dirname(__file__), "golden", "routing_cases.txt")
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        c = json.loads(line)
+        p = moe.route_params(c["K"], c["scoring"], c["renormalize"], c["G"], c["TG"], c["rsf"],
+                             c.get("local_start", 0), c.get("local_count", 0),
+                             c.get("route_scale", 1.0))
+        z = torch.tensor(c["logits"], dtype=torch.float32, device="cuda")
+        b = None if c["bias"] is None else torch.tensor(c["bias"], dtype=torch.float32, device="cuda")
+        w, ids, probs, wsc = moe.moe_route(z, p, b)
+        np.testing.assert_array_equal(np_(ids), np.array(c["ids"]), err_msg=c["name"])
+        np.testing.assert_allclose(np_(w), np.array(c["weights"]), rtol=1e-6, err_msg=c["name"])
+        if "router_probs" in c:
+            np.testing.assert_allclose(np_(probs), np.array(c["router_probs"]), rtol=1e-6)
+            np.testing.assert_allclose(np_(wsc), np.array(c["weight_scale"]), rtol=1e-6)
