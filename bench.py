@@ -1,0 +1,494 @@
+"""Benchmark of the routed MoE FFN forward on GB300.
+
+One step = one full forward (route with the MoERouter outputs -> permute ->
+gate_up GEMM + fused activation -> down GEMM -> combine) of the Qwen3-style
+workload (T=4096 tokens, H=2048, F=768, E=128 experts, top-8, softmax,
+renormalised, silu_and_mul; MoERouter slice [32, 64)) on synthetic seeded
+inputs already resident in HBM.  The L2 is flushed (a 512 MiB write) before
+every timed step and each step is bracketed by CUDA events on the launching
+stream.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain fp64 restatement of the
+method) on the host cores, on a bounded token sample of the same workload.
+Under torchrun with N > 1 each rank runs its own replica of the workload (the
+layer has no cross-token exchange, so the path shards with no collective);
+value = tokens of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "qwen3_bf16"
+METRIC = "MoE FFN fwd tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+_SAMPLER = r"""
+import ctypes, sys, time
+uuid = sys.argv[1]
+lib = ctypes.CDLL("libnvidia-ml.so.1")
+assert lib.nvmlInit_v2() == 0
+n = ctypes.c_uint()
+lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
+h = None
+for i in range(n.value):
+    d = ctypes.c_void_p()
+    lib.nvmlDeviceGetHandleByIndex_v2(i, ctypes.byref(d))
+    buf = ctypes.create_string_buffer(96)
+    lib.nvmlDeviceGetUUID(d, buf, 96)
+    if h is None or (uuid and uuid in buf.value.decode()):
+        h = d
+mx = ctypes.c_uint()
+lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+    lib.nvmlDeviceGetCurrentClocksThrottleReasons
+print("max", mx.value, flush=True)
+clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+while True:
+    lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk))
+    get_reasons(h, ctypes.byref(rs))
+    print(f"{time.time():.6f} {clk.value} {rs.value}", flush=True)
+    time.sleep(0.002)
+"""
+
+
+class ClockSampler:
+    """SM clock and clock-event reasons of this GPU, sampled every ~2 ms by a
+    separate process through NVML (read-only queries), so that short timed
+    regions still get samples; ``mark()`` brackets the timed region."""
+
+    BITS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+            0x4: "sw_power_cap", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index=0):
+        import torch
+
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        except Exception:
+            self.uuid = ""
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen([sys.executable, "-c", _SAMPLER, self.uuid],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.01)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = out.splitlines()
+
+    def summary(self):
+        smax, sm, reasons = None, [], set()
+        for l in self.lines:
+            f = l.split()
+            if len(f) == 2 and f[0] == "max":
+                smax = float(f[1])
+                continue
+            if len(f) != 3:
+                continue
+            t, c, r = float(f[0]), float(f[1]), int(f[2])
+            if self.t0 is not None and not (self.t0 <= t <= (self.t1 or t)):
+                continue
+            sm.append(c)
+            for bit, name in self.BITS.items():
+                if r & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
+
+
+def profile_traffic(kernel: str, src: str):
+    """DRAM bytes per launch from the committed ncu summary of ``kernel``, when
+    the summary was taken on the current source of the kernel."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not h:
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return float(m.group(1)) if sha == h.group(1) else None
+
+
+# --------------------------------------------------------------------- reference
+def run_reference(args, rank, world):
+    """The CPU oracle, as it stands, on a bounded token sample per step."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    from mixture_experts_ffn_gb300 import synth
+    from oracle import cases
+    from oracle import moe_oracle as O
+
+    cfg = synth.CONFIGS[WORKLOAD]
+    inp = synth.make_inputs(cfg, "cpu")
+    n = {k: cases.to_np(v) for k, v in inp.items() if k not in ("w_gate_up", "w_down")}
+    w1 = inp["w_gate_up"].float().numpy()
+    w2 = inp["w_down"].float().numpy()
+    sample = min(args.ref_tokens, cfg.T)
+    per_step = []
+    for step in range(args.warmup + args.steps):
+        toks = synth.subset_tokens(cfg.T, sample)
+        t0 = time.perf_counter()
+        O.ffn_forward(n["hidden"], n["logits"], w1, w2, K=cfg.K, F=cfg.F, scoring=cfg.scoring,
+                      renormalize=cfg.renormalize, rsf=cfg.rsf, dtype=cfg.dtype,
+                      local_start=cfg.local_start, local_count=cfg.local_count,
+                      route_scale=cfg.route_scale, tokens=toks)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            per_step.append(dt)
+    cores = len(os.sched_getaffinity(0))
+    sec = sum(per_step) / len(per_step)
+    value = sample / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": cfg.T, "H": cfg.H, "F": cfg.F, "E": cfg.E,
+                   "K": cfg.K, "sample_tokens_per_step": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample} tokens of the {cfg.T}-token workload per step "
+                                   f"(all their routes and experts), numpy float64"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- ours
+def stage_cost(cfg, D):
+    """Algorithmic FLOPs and bytes per launch of each stage (bf16 operands)."""
+    T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
+    M = T * K
+    lc = cfg.local_count
+    return {
+        "route": (0.0, T * E * 4 + M * 8 + T * lc * 4 + T * 4),
+        "permute": (0.0, M * 4 * 3 + E * 4 + T * H * 2 + M * H * 2),
+        "gemm_act": (4.0 * M * H * F, D * 2 * F * H * 2 + M * H * 2 + M * F * 2),
+        "gemm_down": (2.0 * M * F * H, D * H * F * 2 + M * F * 2 + M * H * 2),
+        "combine": (0.0, M * H * 2 + M * 8 + T * H * 2),
+        "forward": (6.0 * M * H * F, D * 3 * F * H * 2 + T * H * 2 + T * E * 4 + T * H * 2
+                    + M * 8 + T * lc * 4 + T * 4),
+    }
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from mixture_experts_ffn_gb300 import build as mbuild
+    from mixture_experts_ffn_gb300 import moe, synth
+
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(local)
+    if rank == 0 or not os.path.exists(mbuild.LIB):
+        mbuild.build()
+    if world > 1:
+        dist.barrier()
+    dev = torch.device("cuda", local)
+    cfg = synth.CONFIGS[WORKLOAD]
+    inp = synth.make_inputs(cfg, dev)
+    p, a = moe.config_params(cfg)
+    T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    tw = torch.empty((T, K), dtype=torch.float32, device=dev)
+    ti = torch.empty((T, K), dtype=torch.int32, device=dev)
+    probs = torch.empty((T, cfg.local_count), dtype=torch.float32, device=dev)
+    wsc = torch.empty((T,), dtype=torch.float32, device=dev)
+    ws = moe._ws(moe.moe_workspace_size(T, H, F, E, K, moe.MOE_BF16), dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def forward():
+        moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a,
+                            out=out, topk_weights_out=tw, topk_ids_out=ti, router_probs=probs,
+                            weight_scale=wsc, ws=ws)
+
+    def timed(fn, steps, warmup):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        n0 = moe.moe_launch_count()
+        for s, e in ev:
+            flush.zero_()
+            s.record(stream)
+            fn()
+            e.record(stream)
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in ev], moe.moe_launch_count() - n0
+
+    if args.stage:
+        run_stage(args, moe, cfg, inp, p, a, ws, flush, timed)
+        return
+
+    # ---- the timed forward: W warm-up steps, then untimed steps for about a
+    # second so the SM clock leaves its idle state, then exactly K timed steps
+    for _ in range(args.warmup):
+        flush.zero_()
+        forward()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_soak = time.time()
+        soak = 0
+        while time.time() - t_soak < args.soak_s:
+            for _ in range(16):
+                forward()
+            torch.cuda.synchronize()
+            soak += 16
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clk.mark(True)
+        times, launches = timed(forward, args.steps, 0)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clk.mark(False)
+    status = moe.moe_sync_status(ws)
+    ms = sum(times) / len(times)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms / 1e3)
+
+    # ---- per-stage breakdown (rank 0), same inputs, each stage timed alone
+    breakdown = {}
+    roofline = None
+    e2e = None
+    if rank == 0:
+        D = int((torch.bincount(ti.flatten().long(), minlength=E) > 0).sum())
+        costs = stage_cost(cfg, D)
+        perm = moe.moe_permute(ti, E, inp["hidden"])
+        act_out = torch.empty((T * K, F), dtype=torch.bfloat16, device=dev)
+        y = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
+        stage_ws = moe._ws(256, dev)
+        stages = {
+            "route": lambda: moe.moe_route(inp["logits"], p, topk_weights=tw, topk_ids=ti,
+                                           router_probs=probs, weight_scale=wsc),
+            "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"]),
+            "gemm_act": lambda: moe.moe_grouped_gemm_act(perm["expert_input"], inp["w_gate_up"],
+                                                         perm["seg_end"], F, a, out=act_out,
+                                                         ws=stage_ws),
+            "gemm_down": lambda: moe.moe_grouped_gemm_down(act_out, inp["w_down"],
+                                                           perm["seg_end"], out=y, ws=stage_ws),
+            "combine": lambda: moe.moe_combine(y, tw, perm["route_to_row"], out=out),
+        }
+        pk, pk_src = load_peaks()
+        for name, fn in stages.items():
+            st, nl = timed(fn, max(5, args.steps), 3)
+            us = 1e3 * sum(st) / len(st)
+            fl, by = costs[name]
+            t_tc = fl / (pk["bf16_tflops"] * 1e12)
+            t_hbm = by / (pk["hbm_gbs"] * 1e9)
+            bound = "tensor" if t_tc > t_hbm else "hbm"
+            breakdown[name] = {
+                "us": round(us, 2), "launches": nl // max(5, args.steps),
+                "tflops": round(fl / (us * 1e-6) / 1e12, 1),
+                "gbs": round(by / (us * 1e-6) / 1e9, 1), "bound": bound,
+                "frac": round(max(t_tc, t_hbm) / (us * 1e-6), 3),
+            }
+        dom = max(("gemm_act", "gemm_down"), key=lambda k: breakdown[k]["us"])
+        fl, by = costs[dom]
+        b = breakdown[dom]
+        src = os.path.join(ROOT, "mixture_experts_ffn_gb300", "csrc", "gemm_tc.cu")
+        traffic = profile_traffic("gemm_tc_kernel", src) if dom == "gemm_act" else None
+        if b["bound"] == "tensor":
+            ach, peak, unit = fl / (b["us"] * 1e-6) / 1e12, pk["bf16_tflops"], "TFLOP/s"
+        else:
+            ach, peak, unit = by / (b["us"] * 1e-6) / 1e9, pk["hbm_gbs"], "GB/s"
+        roofline = {"kernel": f"gemm_tc_kernel ({dom})", "bound": b["bound"],
+                    "achieved": round(ach, 1), "peak": peak, "unit": unit,
+                    "frac": round(ach / peak, 3), "traffic": traffic,
+                    "peak_source": pk_src,
+                    "algorithmic": {"flops": fl, "bytes": by, "distinct_experts": D}}
+        fwd_fl, fwd_by = costs["forward"]
+        t_roof = max(fwd_fl / (pk["bf16_tflops"] * 1e12), fwd_by / (pk["hbm_gbs"] * 1e9))
+        breakdown["forward_roofline_frac"] = round(t_roof / (ms * 1e-3), 3)
+        breakdown["forward_tflops"] = round(fwd_fl / (ms * 1e-3) / 1e12, 1)
+
+        # ---- end to end through the C ABI with host buffers
+        h_host = inp["hidden"].cpu().pin_memory()
+        l_host = inp["logits"].cpu().pin_memory()
+        o_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        p_host, _ = moe.config_params(cfg.replace(local_count=0))
+        ws_h = moe._ws(moe.moe_workspace_size_host(T, H, F, E, K, moe.MOE_BF16), dev)
+
+        def fwd_host():
+            moe.moe_ffn_forward_host(h_host, l_host, inp["w_gate_up"], inp["w_down"], p_host, a,
+                                     o_host, ws_h)
+
+        et, _ = timed(fwd_host, args.steps, args.warmup)
+        e_ms = sum(et) / len(et)
+        e2e = {"value": T / (e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args, cfg, inp)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "T": T, "H": H, "F": F, "E": E, "K": K,
+                       "scoring": "softmax", "renormalize": True, "act": "silu_and_mul",
+                       "moerouter_slice": [cfg.local_start, cfg.local_count],
+                       "l2": "flushed before every timed step (512 MiB write)",
+                       "soak_steps": soak,
+                       "parallelism": f"replicas x{world}"},
+            "gpu_launches": launches,
+            "launches_per_step": launches // args.steps,
+            "status": int(status),
+            "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
+            "clocks": clk.summary(), "breakdown": breakdown,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
+    """One stage alone on the workload's inputs (for profiler captures)."""
+    import torch
+
+    T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
+    dev = inp["hidden"].device
+    tw, ti, _, _ = moe.moe_route(inp["logits"], p)
+    perm = moe.moe_permute(ti, E, inp["hidden"])
+    act_out = torch.empty((T * K, F), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
+    moe.moe_grouped_gemm_act(perm["expert_input"], inp["w_gate_up"], perm["seg_end"], F, a,
+                             out=act_out)
+    moe.moe_grouped_gemm_down(act_out, inp["w_down"], perm["seg_end"], out=y)
+    fns = {
+        "route": lambda: moe.moe_route(inp["logits"], p, topk_weights=tw, topk_ids=ti),
+        "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"]),
+        "gemm_act": lambda: moe.moe_grouped_gemm_act(perm["expert_input"], inp["w_gate_up"],
+                                                     perm["seg_end"], F, a, out=act_out),
+        "gemm_down": lambda: moe.moe_grouped_gemm_down(act_out, inp["w_down"], perm["seg_end"],
+                                                       out=y),
+        "combine": lambda: moe.moe_combine(y, tw, perm["route_to_row"]),
+    }
+    st, nl = timed(fns[args.stage], args.steps, args.warmup)
+    print(json.dumps({"stage": args.stage, "workload": WORKLOAD,
+                      "us": [round(1e3 * x, 2) for x in st], "launches": nl}), flush=True)
+
+
+def cpu_baseline(args, cfg, inp):
+    """The oracle, as it stands, on a bounded token sample (host cores)."""
+    from mixture_experts_ffn_gb300 import synth
+    from oracle import cases
+    from oracle import moe_oracle as O
+
+    n = {k: cases.to_np(v) for k, v in inp.items() if k not in ("w_gate_up", "w_down")}
+    w1 = inp["w_gate_up"].float().cpu().numpy()
+    w2 = inp["w_down"].float().cpu().numpy()
+    toks = synth.subset_tokens(cfg.T, min(args.ref_tokens, cfg.T))
+    t0 = time.perf_counter()
+    O.ffn_forward(n["hidden"], n["logits"], w1, w2, K=cfg.K, F=cfg.F, scoring=cfg.scoring,
+                  renormalize=cfg.renormalize, rsf=cfg.rsf, dtype=cfg.dtype,
+                  local_start=cfg.local_start, local_count=cfg.local_count,
+                  route_scale=cfg.route_scale, tokens=toks)
+    sec = time.perf_counter() - t0
+    return {"value": round(len(toks) / sec, 2), "unit": "tokens/s",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{len(toks)} of the {cfg.T} tokens of the workload (all their routes), "
+                      f"numpy float64 with its BLAS threads, {sec:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=None,
+                    help="oracle token sample (default 256 for cpu_baseline, 32 per reference "
+                         "step)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--soak-s", type=float, default=1.0,
+                    help="untimed forward steps run for this long before the timed ones")
+    ap.add_argument("--stage", default=None,
+                    choices=["route", "permute", "gemm_act", "gemm_down", "combine"],
+                    help="time one stage alone (for profiler captures)")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local = dist_env()
+    if args.ref_tokens is None:
+        args.ref_tokens = 4096  # the whole workload
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -264,6 +264,28 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
                            float* weight_scale, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* moe_ffn_forward for a caller whose activations live in HOST memory:
+ * hidden_host [T, H] dtype and logits_host [T, E] f32 are copied to device
+ * staging space inside `ws` (cudaMemcpyAsync on `stream`), the layer runs as in
+ * moe_ffn_forward, and the result is copied back into out_host [T, H].  All of
+ * it is asynchronous on `stream`: out_host is valid after the stream is
+ * synchronised.  Host buffers should be page-locked for the copies to overlap
+ * the host; pageable memory works but the copies then synchronise.  Weights,
+ * biases and expert_ids stay device pointers.  Routing outputs are not
+ * returned.  ws >= moe_workspace_size_host(T, H, F, E, K, dtype). */
+moe_status moe_ffn_forward_host(const void* hidden_host, const float* logits_host,
+                                const void* w_gate_up, const void* w_down,
+                                const float* correction_bias, const int32_t* expert_ids,
+                                const void* b_gate_up, const void* b_down, int T, int H, int F,
+                                int E, moe_dtype dtype, const moe_route_params* p,
+                                const moe_act_params* act, void* out_host, void* ws,
+                                size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes of moe_ffn_forward_host: moe_workspace_size plus device
+ * staging for hidden, logits and out. */
+size_t moe_workspace_size_host(int T, int H, int F, int E, int K, moe_dtype dtype);
+
+/* ------------------------------------------------------------------------ */
 /* Sizes and status.  (The workspace query plays the role of the peak-memory
  * query of [ORT-MoE].) */
 

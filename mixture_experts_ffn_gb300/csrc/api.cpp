@@ -331,6 +331,46 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   return cuda_status(launch_combine(y, tw, route_to_row, T, K, H, dtype, 1.0f, out, stream));
 }
 
+size_t moe_workspace_size_host(int T, int H, int F, int E, int K, moe_dtype dtype) {
+  size_t base = moe_workspace_size(T, H, F, E, K, dtype);
+  if (base == 0) return 0;
+  const size_t esz = esize(dtype);
+  return base + align256((size_t)T * H * esz) * 2 + align256((size_t)T * E * 4);
+}
+
+moe_status moe_ffn_forward_host(const void* hidden_host, const float* logits_host,
+                                const void* w_gate_up, const void* w_down,
+                                const float* correction_bias, const int32_t* expert_ids,
+                                const void* b_gate_up, const void* b_down, int T, int H, int F,
+                                int E, moe_dtype dtype, const moe_route_params* p,
+                                const moe_act_params* act, void* out_host, void* ws,
+                                size_t ws_bytes, cudaStream_t stream) {
+  if (!p || !dtype_ok(dtype) || T < 0 || H < 1 || F < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (p->local_expert_count != 0) return MOE_ERR_INVALID_ARG;  // no routing outputs here
+  if (T > 0 && (!hidden_host || !logits_host || !out_host)) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_workspace_size_host(T, H, F, E, p->top_k, dtype);
+  if (need == 0) return MOE_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, need)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  const size_t esz = esize(dtype);
+  const size_t fwd = moe_workspace_size(T, H, F, E, p->top_k, dtype);
+  char* base = static_cast<char*>(ws);
+  void* d_hidden = base + fwd;
+  void* d_out = base + fwd + align256((size_t)T * H * esz);
+  float* d_logits = reinterpret_cast<float*>(base + fwd + 2 * align256((size_t)T * H * esz));
+  if (cudaMemcpyAsync(d_hidden, hidden_host, (size_t)T * H * esz, cudaMemcpyHostToDevice,
+                      stream) != cudaSuccess ||
+      cudaMemcpyAsync(d_logits, logits_host, (size_t)T * E * 4, cudaMemcpyHostToDevice,
+                      stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  moe_status st = moe_ffn_forward(d_hidden, d_logits, w_gate_up, w_down, correction_bias,
+                                  expert_ids, b_gate_up, b_down, T, H, F, E, dtype, p, act, d_out,
+                                  nullptr, nullptr, nullptr, nullptr, ws, fwd, stream);
+  if (st != MOE_OK) return st;
+  return cuda_status(
+      cudaMemcpyAsync(out_host, d_out, (size_t)T * H * esz, cudaMemcpyDeviceToHost, stream));
+}
+
 moe_status moe_clear_status(void* ws, cudaStream_t stream) {
   if (!ws) return MOE_ERR_WORKSPACE;
   return cuda_status(cudaMemsetAsync(ws, 0, MOE_STATUS_BYTES, stream));

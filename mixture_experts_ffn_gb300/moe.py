@@ -52,7 +52,10 @@ _SIGNATURES = {
     "moe_indexed_mlp": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _sz, _vp],
     "moe_ffn_forward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp,
                         _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
+    "moe_ffn_forward_host": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
+                             _vp, _vp, _vp, _sz, _vp],
     "moe_workspace_size": [_i, _i, _i, _i, _i, _i],
+    "moe_workspace_size_host": [_i, _i, _i, _i, _i, _i],
     "moe_permute_workspace_size": [_i, _i],
     "moe_clear_status": [_vp, _vp],
     "moe_sync_status": [_vp, _vp],
@@ -61,6 +64,7 @@ _SIGNATURES = {
     "moe_set_gemm_simt": [_i],
 }
 _RESTYPES = {"moe_workspace_size": _sz, "moe_permute_workspace_size": _sz,
+             "moe_workspace_size_host": _sz,
              "moe_status_string": ctypes.c_char_p, "moe_launch_count": ctypes.c_uint64}
 
 _lib = None
@@ -120,8 +124,11 @@ def _cuda(*ts):
 
 
 def _ws(nbytes: int, device) -> torch.Tensor:
-    # torch's caching allocator returns 512-byte aligned blocks
-    return torch.empty(max(nbytes, MOE_STATUS_BYTES), dtype=torch.uint8, device=device)
+    """A fresh workspace with a cleared status word (torch's caching allocator
+    returns 512-byte aligned blocks)."""
+    ws = torch.empty(max(nbytes, MOE_STATUS_BYTES), dtype=torch.uint8, device=device)
+    ws[:MOE_STATUS_BYTES].zero_()
+    return ws
 
 
 def route_params(top_k, scoring="softmax", renormalize=True, num_expert_group=1, topk_group=1,
@@ -203,7 +210,6 @@ def moe_grouped_gemm_act(a, w_gate_up, seg_end, F: int, act: ActParams, b_gate_u
         out = torch.empty((M, F), dtype=a.dtype, device=a.device)
     if ws is None:
         ws = _ws(MOE_STATUS_BYTES, a.device)
-        lib.moe_clear_status(_p(ws), _stream())
     _check("moe_grouped_gemm_act",
            lib.moe_grouped_gemm_act(_p(a), _p(w_gate_up), _p(b_gate_up), _p(seg_end), M, F, Hk, E,
                                     _dt(a), ctypes.byref(act), _p(out), _p(ws), ws.numel(),
@@ -220,7 +226,6 @@ def moe_grouped_gemm_down(a, w_down, seg_end, b_down=None, out=None, ws=None):
         out = torch.empty((M, H), dtype=a.dtype, device=a.device)
     if ws is None:
         ws = _ws(MOE_STATUS_BYTES, a.device)
-        lib.moe_clear_status(_p(ws), _stream())
     _check("moe_grouped_gemm_down",
            lib.moe_grouped_gemm_down(_p(a), _p(w_down), _p(b_down), _p(seg_end), M, H, F, E,
                                      _dt(a), _p(out), _p(ws), ws.numel(), _stream()))
@@ -263,7 +268,6 @@ def moe_indexed_mlp(hidden, w_gate_up, w_down, topk_weights, topk_ids, scale=1.0
         out = torch.empty((T, H), dtype=hidden.dtype, device=hidden.device)
     if ws is None:
         ws = _ws(lib.moe_workspace_size(T, H, F, E, K, MOE_BF16), hidden.device)
-        lib.moe_clear_status(_p(ws), _stream())
     _check("moe_indexed_mlp",
            lib.moe_indexed_mlp(_p(hidden), _p(w_gate_up), _p(w_down), _p(topk_weights),
                                _p(topk_ids), T, H, F, E, K, scale, _p(out), _p(ws), ws.numel(),
@@ -284,7 +288,6 @@ def moe_ffn_forward(hidden, logits, w_gate_up, w_down, p: RouteParams, act: ActP
         out = torch.empty_like(hidden)
     if ws is None:
         ws = _ws(lib.moe_workspace_size(T, H, F, E, p.top_k, _dt(hidden)), hidden.device)
-        lib.moe_clear_status(_p(ws), _stream())
     _check("moe_ffn_forward",
            lib.moe_ffn_forward(_p(hidden), _p(logits), _p(w_gate_up), _p(w_down),
                                _p(correction_bias), _p(expert_ids), _p(b_gate_up), _p(b_down), T,
@@ -292,6 +295,31 @@ def moe_ffn_forward(hidden, logits, w_gate_up, w_down, p: RouteParams, act: ActP
                                _p(topk_weights_out), _p(topk_ids_out), _p(router_probs),
                                _p(weight_scale), _p(ws), ws.numel(), _stream()))
     return out
+
+
+def moe_workspace_size_host(T, H, F, E, K, dtype=MOE_BF16) -> int:
+    return load_library().moe_workspace_size_host(T, H, F, E, K, dtype)
+
+
+def moe_ffn_forward_host(hidden_host, logits_host, w_gate_up, w_down, p: RouteParams,
+                         act: ActParams, out_host, ws, correction_bias=None, expert_ids=None,
+                         b_gate_up=None, b_down=None):
+    """moe_ffn_forward with hidden / logits / out in host memory (pinned for
+    asynchronous copies); asynchronous on the current stream."""
+    lib = load_library()
+    _cuda(w_gate_up, w_down, correction_bias, expert_ids, b_gate_up, b_down, ws)
+    for t in (hidden_host, logits_host, out_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("moe_ffn_forward_host takes contiguous host tensors")
+    T, H = hidden_host.shape
+    E, _, F = w_down.shape
+    _check("moe_ffn_forward_host",
+           lib.moe_ffn_forward_host(_p(hidden_host), _p(logits_host), _p(w_gate_up), _p(w_down),
+                                    _p(correction_bias), _p(expert_ids), _p(b_gate_up),
+                                    _p(b_down), T, H, F, E, _dt(hidden_host), ctypes.byref(p),
+                                    ctypes.byref(act), _p(out_host), _p(ws), ws.numel(),
+                                    _stream()))
+    return out_host
 
 
 def moe_clear_status(ws):

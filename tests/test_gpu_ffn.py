@@ -142,7 +142,7 @@ def test_forward_is_deterministic(moe):
 
 
 def test_forward_bad_hash_ids_latch_device_error(moe):
-    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=64, H=128, F=64, E=16, K=2)
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=64, H=128, F=64, E=16, K=2, local_count=0)
     inp, _ = make(cfg)
     ids = torch.randint(0, 16, (64, 2), dtype=torch.int32, device="cuda")
     ids[5, 1] = 99
@@ -152,7 +152,7 @@ def test_forward_bad_hash_ids_latch_device_error(moe):
 
 
 def test_forward_rejects_overlap_without_writing(moe):
-    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=64, H=128, F=64, E=16, K=2)
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=64, H=128, F=64, E=16, K=2, local_count=0)
     inp, _ = make(cfg)
     p, a = moe.config_params(cfg)
     before = inp["hidden"].clone()
@@ -164,7 +164,7 @@ def test_forward_rejects_overlap_without_writing(moe):
 
 
 def test_empty_batch(moe):
-    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=0, H=128, F=64, E=16, K=2)
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=0, H=128, F=64, E=16, K=2, local_count=0)
     inp, _ = make(cfg, guard=False)
     p, a = moe.config_params(cfg)
     out = moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a)
