@@ -159,6 +159,35 @@ moe_status moe_permute(const void* hidden, moe_dtype dtype, const int32_t* topk_
                        size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* moe_permute for callers that cannot allocate device memory.  (The pages have
+ * no counterpart: this is a property of the library, not of the method.)
+ *
+ * Some callers cannot call cudaMalloc where they run the layer: cudaMalloc and
+ * cudaFree can synchronise the whole device, and serving runtimes with a fixed
+ * memory budget (or their own allocator owning all device memory) forbid any
+ * allocation after start-up.  This variant takes no workspace: its scratch is
+ * a fixed 1 MiB array in device memory owned by the library, which every GPU
+ * that loads the library holds until the process exits.  The caller still
+ * passes every input and output; arguments, layout and results are those of
+ * moe_permute.
+ *
+ *  - Limit: the permute scratch (256 + ceil(T*K/1024)*E*4 + E*4 bytes, rounded
+ *    up to 256-byte sections) must fit in 1 MiB -- e.g. T*K up to 131072 routes
+ *    with E up to 1024 experts; larger sizes return MOE_ERR_WORKSPACE and launch
+ *    nothing.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and it keeps the last call's
+ *    contents (each call clears what must start at zero): calls that can
+ *    overlap on the GPU -- on different streams, or from different threads --
+ *    race and must be serialised by the caller.
+ *  - Out-of-range ids are dropped as in moe_permute, but the device status bit
+ *    they latch lives in the library's array and is not reported. */
+moe_status moe_permute_noalloc(const void* hidden, moe_dtype dtype, const int32_t* topk_ids,
+                               int T, int H, int E, int K, void* expert_input, int32_t* seg_end,
+                               int32_t* row_to_route, int32_t* route_to_row, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Grouped gate_up GEMM with the gated activation fused into its epilogue
  * [TileOPs, MoEGroupedGemmFwdOp ("activation"), MoEExpertMLPFwdOp].
  *
