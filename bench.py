@@ -32,7 +32,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = "qwen3_bf16"
+WORKLOAD = "qwen3_bf16"  # the default workload (bench line); --workload picks another
 METRIC = "MoE FFN fwd tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -175,7 +175,7 @@ def run_reference(args, rank, world):
     from oracle import cases
     from oracle import moe_oracle as O
 
-    cfg = synth.CONFIGS[WORKLOAD]
+    cfg = synth.CONFIGS[args.workload]
     inp = synth.make_inputs(cfg, "cpu")
     n = {k: cases.to_np(v) for k, v in inp.items() if k not in ("w_gate_up", "w_down")}
     w1 = inp["w_gate_up"].float().numpy()
@@ -186,9 +186,12 @@ def run_reference(args, rank, world):
         toks = synth.subset_tokens(cfg.T, sample)
         t0 = time.perf_counter()
         O.ffn_forward(n["hidden"], n["logits"], w1, w2, K=cfg.K, F=cfg.F, scoring=cfg.scoring,
-                      renormalize=cfg.renormalize, rsf=cfg.rsf, dtype=cfg.dtype,
-                      local_start=cfg.local_start, local_count=cfg.local_count,
-                      route_scale=cfg.route_scale, tokens=toks)
+                      renormalize=cfg.renormalize, G=cfg.G, TG=cfg.TG, rsf=cfg.rsf,
+                      correction_bias=n["correction_bias"], expert_ids=n["expert_ids"],
+                      act=cfg.act, fusion=cfg.swiglu_fusion, limit=cfg.limit, alpha=cfg.alpha,
+                      beta=cfg.beta, b_gate_up=n["b_gate_up"], b_down=n["b_down"],
+                      dtype=cfg.dtype, local_start=cfg.local_start,
+                      local_count=cfg.local_count, route_scale=cfg.route_scale, tokens=toks)
         dt = time.perf_counter() - t0
         if step >= args.warmup:
             per_step.append(dt)
@@ -200,7 +203,7 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "T": cfg.T, "H": cfg.H, "F": cfg.F, "E": cfg.E,
+        "config": {"workload": args.workload, "T": cfg.T, "H": cfg.H, "F": cfg.F, "E": cfg.E,
                    "K": cfg.K, "sample_tokens_per_step": sample},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{sample} tokens of the {cfg.T}-token workload per step "
@@ -213,18 +216,24 @@ def run_reference(args, rank, world):
 
 # --------------------------------------------------------------------- ours
 def stage_cost(cfg, D):
-    """Algorithmic FLOPs and bytes per launch of each stage (bf16 operands)."""
+    """Algorithmic FLOPs and bytes per launch of each stage: the distinct
+    experts' weights (and biases), the stage's own inputs and outputs."""
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
     M = T * K
     lc = cfg.local_count
+    b = 2 if cfg.dtype == "bf16" else 4
+    bias1 = D * 2 * F * b if cfg.bias_std is not None else 0
+    bias2 = D * H * b if cfg.bias_std is not None else 0
+    route = T * E * 4 + M * 8 + T * lc * 4 + (T * 4 if lc else 0)
     return {
-        "route": (0.0, T * E * 4 + M * 8 + T * lc * 4 + T * 4),
-        "permute": (0.0, M * 4 * 3 + E * 4 + T * H * 2 + M * H * 2),
-        "gemm_act": (4.0 * M * H * F, D * 2 * F * H * 2 + M * H * 2 + M * F * 2),
-        "gemm_down": (2.0 * M * F * H, D * H * F * 2 + M * F * 2 + M * H * 2),
-        "combine": (0.0, M * H * 2 + M * 8 + T * H * 2),
-        "forward": (6.0 * M * H * F, D * 3 * F * H * 2 + T * H * 2 + T * E * 4 + T * H * 2
-                    + M * 8 + T * lc * 4 + T * 4),
+        "route": (0.0, route),
+        "permute": (0.0, M * 4 * 3 + E * 4 + T * H * b + M * H * b),
+        "gemm_act": (4.0 * M * H * F, D * 2 * F * H * b + bias1 + M * H * b + M * F * b),
+        "gemm_down": (2.0 * M * F * H, D * H * F * b + bias2 + M * F * b + M * H * b),
+        "combine": (0.0, M * H * b + M * 8 + T * H * b),
+        "indexed_mlp": (6.0 * M * H * F, D * 3 * F * H * b + T * H * b + M * 8 + T * H * b),
+        "forward": (6.0 * M * H * F, D * 3 * F * H * b + bias1 + bias2 + T * H * b + route
+                    + T * H * b),
     }
 
 
@@ -247,23 +256,33 @@ def run_ours(args, rank, world, local):
     if world > 1:
         dist.barrier()
     dev = torch.device("cuda", local)
-    cfg = synth.CONFIGS[WORKLOAD]
+    cfg = synth.CONFIGS[args.workload]
+    if args.override:
+        cfg = cfg.replace(**{k: type(getattr(cfg, k))(v) for k, v in
+                             (kv.split("=") for kv in args.override.split(","))})
     inp = synth.make_inputs(cfg, dev)
     p, a = moe.config_params(cfg)
+    indexed = (cfg.T * cfg.K <= 2 * cfg.E and cfg.act == synth.ACT_SILU_AND_MUL
+               and cfg.bias_std is None and cfg.dtype == "bf16" and cfg.H % 128 == 0
+               and cfg.F % 256 == 0)
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
-    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    tdt = synth.torch_dtype(cfg.dtype)
+    mdt = moe.MOE_BF16 if cfg.dtype == "bf16" else moe.MOE_F32
+    out = torch.empty((T, H), dtype=tdt, device=dev)
     tw = torch.empty((T, K), dtype=torch.float32, device=dev)
     ti = torch.empty((T, K), dtype=torch.int32, device=dev)
-    probs = torch.empty((T, cfg.local_count), dtype=torch.float32, device=dev)
-    wsc = torch.empty((T,), dtype=torch.float32, device=dev)
-    ws = moe._ws(moe.moe_workspace_size(T, H, F, E, K, moe.MOE_BF16), dev)
+    probs = torch.empty((T, cfg.local_count), dtype=torch.float32, device=dev) \
+        if cfg.local_count else None
+    wsc = torch.empty((T,), dtype=torch.float32, device=dev) if cfg.local_count else None
+    ws = moe._ws(moe.moe_workspace_size(T, H, F, E, K, mdt), dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def forward():
         moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a,
-                            out=out, topk_weights_out=tw, topk_ids_out=ti, router_probs=probs,
-                            weight_scale=wsc, ws=ws)
+                            inp["correction_bias"], inp["expert_ids"], inp["b_gate_up"],
+                            inp["b_down"], out=out, topk_weights_out=tw, topk_ids_out=ti,
+                            router_probs=probs, weight_scale=wsc, ws=ws)
 
     def timed(fn, steps, warmup):
         for _ in range(warmup):
@@ -324,20 +343,30 @@ def run_ours(args, rank, world, local):
         D = int((torch.bincount(ti.flatten().long(), minlength=E) > 0).sum())
         costs = stage_cost(cfg, D)
         perm = moe.moe_permute(ti, E, inp["hidden"])
-        act_out = torch.empty((T * K, F), dtype=torch.bfloat16, device=dev)
-        y = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
+        act_out = torch.empty((T * K, F), dtype=tdt, device=dev)
+        y = torch.empty((T * K, H), dtype=tdt, device=dev)
         stage_ws = moe._ws(256, dev)
         stages = {
-            "route": lambda: moe.moe_route(inp["logits"], p, topk_weights=tw, topk_ids=ti,
+            "route": lambda: moe.moe_route(inp["logits"], p, inp["correction_bias"],
+                                           inp["expert_ids"], topk_weights=tw, topk_ids=ti,
                                            router_probs=probs, weight_scale=wsc),
-            "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"]),
-            "gemm_act": lambda: moe.moe_grouped_gemm_act(perm["expert_input"], inp["w_gate_up"],
-                                                         perm["seg_end"], F, a, out=act_out,
-                                                         ws=stage_ws),
-            "gemm_down": lambda: moe.moe_grouped_gemm_down(act_out, inp["w_down"],
-                                                           perm["seg_end"], out=y, ws=stage_ws),
-            "combine": lambda: moe.moe_combine(y, tw, perm["route_to_row"], out=out),
         }
+        if indexed:
+            stages["indexed_mlp"] = lambda: moe.moe_indexed_mlp(inp["hidden"], inp["w_gate_up"],
+                                                                inp["w_down"], tw, ti, out=out,
+                                                                ws=ws)
+        else:
+            stages.update({
+                "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"]),
+                "gemm_act": lambda: moe.moe_grouped_gemm_act(perm["expert_input"],
+                                                             inp["w_gate_up"], perm["seg_end"], F,
+                                                             a, inp["b_gate_up"], out=act_out,
+                                                             ws=stage_ws),
+                "gemm_down": lambda: moe.moe_grouped_gemm_down(act_out, inp["w_down"],
+                                                               perm["seg_end"], inp["b_down"],
+                                                               out=y, ws=stage_ws),
+                "combine": lambda: moe.moe_combine(y, tw, perm["route_to_row"], out=out),
+            })
         pk, pk_src = load_peaks()
         for name, fn in stages.items():
             st, nl = timed(fn, max(5, args.steps), 3)
@@ -352,16 +381,24 @@ def run_ours(args, rank, world, local):
                 "gbs": round(by / (us * 1e-6) / 1e9, 1), "bound": bound,
                 "frac": round(max(t_tc, t_hbm) / (us * 1e-6), 3),
             }
-        dom = max(("gemm_act", "gemm_down"), key=lambda k: breakdown[k]["us"])
+        if indexed:
+            dom = "indexed_mlp"
+            kname = "indexed_gate_up + indexed_down"
+            src = os.path.join(ROOT, "mixture_experts_ffn_gb300", "csrc", "decode.cu")
+            traffic = None
+        else:
+            dom = max(("gemm_act", "gemm_down"), key=lambda k: breakdown[k]["us"])
+            kname = f"gemm_tc_kernel ({dom})"
+            src = os.path.join(ROOT, "mixture_experts_ffn_gb300", "csrc", "gemm_tc.cu")
+            traffic = profile_traffic("gemm_tc_kernel", src) if (
+                dom == "gemm_act" and args.workload == WORKLOAD) else None
         fl, by = costs[dom]
         b = breakdown[dom]
-        src = os.path.join(ROOT, "mixture_experts_ffn_gb300", "csrc", "gemm_tc.cu")
-        traffic = profile_traffic("gemm_tc_kernel", src) if dom == "gemm_act" else None
         if b["bound"] == "tensor":
             ach, peak, unit = fl / (b["us"] * 1e-6) / 1e12, pk["bf16_tflops"], "TFLOP/s"
         else:
             ach, peak, unit = by / (b["us"] * 1e-6) / 1e9, pk["hbm_gbs"], "GB/s"
-        roofline = {"kernel": f"gemm_tc_kernel ({dom})", "bound": b["bound"],
+        roofline = {"kernel": kname, "bound": b["bound"],
                     "achieved": round(ach, 1), "peak": peak, "unit": unit,
                     "frac": round(ach / peak, 3), "traffic": traffic,
                     "peak_source": pk_src,
@@ -374,31 +411,37 @@ def run_ours(args, rank, world, local):
         # ---- end to end through the C ABI with host buffers
         h_host = inp["hidden"].cpu().pin_memory()
         l_host = inp["logits"].cpu().pin_memory()
-        o_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+        o_host = torch.empty((T, H), dtype=tdt).pin_memory()
         p_host, _ = moe.config_params(cfg.replace(local_count=0))
-        ws_h = moe._ws(moe.moe_workspace_size_host(T, H, F, E, K, moe.MOE_BF16), dev)
+        ws_h = moe._ws(moe.moe_workspace_size_host(T, H, F, E, K, mdt), dev)
 
         def fwd_host():
             moe.moe_ffn_forward_host(h_host, l_host, inp["w_gate_up"], inp["w_down"], p_host, a,
-                                     o_host, ws_h)
+                                     o_host, ws_h, inp["correction_bias"], inp["expert_ids"],
+                                     inp["b_gate_up"], inp["b_down"])
 
         et, _ = timed(fwd_host, args.steps, args.warmup)
         e_ms = sum(et) / len(et)
+        eb = 2 if cfg.dtype == "bf16" else 4
         e2e = {"value": T / (e_ms / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2}
+               "h2d_bytes_per_step": T * H * eb + T * E * 4, "d2h_bytes_per_step": T * H * eb}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args, cfg, inp)
 
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic",
-            "config": {"workload": WORKLOAD, "T": T, "H": H, "F": F, "E": E, "K": K,
-                       "scoring": "softmax", "renormalize": True, "act": "silu_and_mul",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg.dtype, "data": "synthetic",
+            "config": {"workload": args.workload, "T": T, "H": H, "F": F, "E": E, "K": K,
+                       "scoring": cfg.scoring, "renormalize": cfg.renormalize,
+                       "groups": [cfg.G, cfg.TG], "rsf": cfg.rsf,
+                       "act": ["silu_and_mul", "swiglu", "identity"][cfg.act],
+                       "path": "indexed" if indexed else "staged",
                        "moerouter_slice": [cfg.local_start, cfg.local_count],
                        "l2": "flushed before every timed step (512 MiB write)",
                        "soak_steps": soak,
@@ -438,7 +481,7 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
         "combine": lambda: moe.moe_combine(y, tw, perm["route_to_row"]),
     }
     st, nl = timed(fns[args.stage], args.steps, args.warmup)
-    print(json.dumps({"stage": args.stage, "workload": WORKLOAD,
+    print(json.dumps({"stage": args.stage, "workload": args.workload,
                       "us": [round(1e3 * x, 2) for x in st], "launches": nl}), flush=True)
 
 
@@ -454,7 +497,10 @@ def cpu_baseline(args, cfg, inp):
     toks = synth.subset_tokens(cfg.T, min(args.ref_tokens, cfg.T))
     t0 = time.perf_counter()
     O.ffn_forward(n["hidden"], n["logits"], w1, w2, K=cfg.K, F=cfg.F, scoring=cfg.scoring,
-                  renormalize=cfg.renormalize, rsf=cfg.rsf, dtype=cfg.dtype,
+                  renormalize=cfg.renormalize, G=cfg.G, TG=cfg.TG, rsf=cfg.rsf,
+                  correction_bias=n["correction_bias"], expert_ids=n["expert_ids"],
+                  act=cfg.act, fusion=cfg.swiglu_fusion, limit=cfg.limit, alpha=cfg.alpha,
+                  beta=cfg.beta, b_gate_up=n["b_gate_up"], b_down=n["b_down"], dtype=cfg.dtype,
                   local_start=cfg.local_start, local_count=cfg.local_count,
                   route_scale=cfg.route_scale, tokens=toks)
     sec = time.perf_counter() - t0
@@ -476,6 +522,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--soak-s", type=float, default=1.0,
                     help="untimed forward steps run for this long before the timed ones")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="workload recipe (mixture_experts_ffn_gb300.synth.CONFIGS); the bench "
+                         "line of record is the default one")
+    ap.add_argument("--override", default="",
+                    help="KEY=VAL[,KEY=VAL] changes to the workload recipe (profiling of "
+                         "reduced cases only; the bench line of record uses none)")
     ap.add_argument("--stage", default=None,
                     choices=["route", "permute", "gemm_act", "gemm_down", "combine"],
                     help="time one stage alone (for profiler captures)")
@@ -483,7 +535,8 @@ def main():
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_env()
     if args.ref_tokens is None:
-        args.ref_tokens = 4096  # the whole workload
+        big = args.workload in ("deepseek_v3_bf16", "gpt_oss_bf16")
+        args.ref_tokens = 256 if big else 4096  # the whole workload when it fits
     if args.impl == "reference":
         run_reference(args, rank, world)
         return

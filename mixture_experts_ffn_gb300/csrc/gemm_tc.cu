@@ -25,12 +25,16 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
+
+using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
@@ -38,7 +42,6 @@ constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
-constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait
 
 enum TcMode { kTcPlain = 0, kTcStacked = 1, kTcInterleaved = 2 };
 
@@ -55,112 +58,25 @@ struct TcShared {
 };
 constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + sizeof(TcShared) + 1024;
 
-// ------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t su32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase of parity `parity`; false on abort or timeout.
-__device__ __noinline__ bool wait_bar(uint64_t* b, uint32_t parity, volatile int* abort_flag,
-                                      int* status) {
-  const uint32_t addr = su32(b);
-  if (mbar_try_wait(addr, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(addr, parity)) return true;
-    if (*abort_flag) return false;
-    if (global_ns() - t0 > kTimeoutNs) {
-      *abort_flag = 1;
-      latch_error(status, kDevTimeout);
-      return false;
-    }
-  }
-}
-// Bounded wait used while draining after an abort (ignores the abort flag).
-__device__ __noinline__ void drain_wait(uint64_t* b, uint32_t parity) {
-  const uint32_t addr = su32(b);
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(addr, parity)) {
-    if (global_ns() - t0 > kTimeoutNs) return;
-  }
-}
 
-__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
-                                       int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(su32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(su32(bar)), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
-                                       int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(su32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(su32(bar)), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-__device__ __forceinline__ void tma_4d(void* dst, const CUtensorMap* m, uint64_t* bar, int c0,
-                                       int c1, int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(su32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(su32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
+constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
 
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
-// 128 bytes, 8-row core groups 1024 bytes apart (stride byte offset).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
-  d |= (uint64_t)1 << 16;                    // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
-  d |= (uint64_t)1 << 46;                    // descriptor version
-  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: D f32, A/B bf16, both K-major, M x N.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t acc) {
+// The four K16 MMAs of one 64-wide k-block and the commit that frees its stage,
+// in one block: descriptors advance by 32 bytes (2 in 16-byte units) per K16.
+__device__ __forceinline__ void umma_kblock(uint32_t d_tmem, uint64_t ad, uint64_t bd,
+                                            uint32_t accumulate, uint32_t bar) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
+      "{\n\t.reg .pred p, t;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(ad), "l"(bd), "r"(kIdesc), "r"(acc)
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %7, %3, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %9, %3, t;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %10, %11, %3, t;\n\t"
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(
+          d_tmem),
+      "l"(ad), "l"(bd), "r"(kIdesc), "r"(accumulate), "r"(bar), "l"(ad + 2), "l"(bd + 2),
+      "l"(ad + 4), "l"(bd + 4), "l"(ad + 6), "l"(bd + 6)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -170,41 +86,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       : "memory");
 }
 
-#define MOE_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
-                  "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : MOE_R8(0), MOE_R8(8), MOE_R8(16), MOE_R8(24)
-      : "r"(taddr));
-}
-#undef MOE_R8
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// store 32 bf16 values (64 bytes) of one row; vector path when all columns valid
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)[32], int n_valid) {
-  if (n_valid >= 32) {
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 u;
-      u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-      u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-      u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-      u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-      d4[q] = u;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < n_valid) dst[i] = __float2bfloat16_rn(v[i]);
-  }
-}
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
@@ -255,12 +136,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ------------------------------------------------ TMA producer
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued[STAGES] = {0, 0, 0, 0};
+      uint32_t issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles);
+      int tile = blockIdx.x;
+      SegTile st{}, nx{};
+      if (tile < total) st = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles);
+      for (; tile < total && ok; tile += gridDim.x) {
+        if (tile + (int)gridDim.x < total)
+          nx = decode_tile(tile + gridDim.x, sh->prefix, seg_end, E, M, BM, n_tiles);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bar(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
+          if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
           uint8_t* a_dst = smem + (size_t)stage * STAGE_BYTES;
           uint8_t* b_dst = a_dst + A_BYTES;
           mbar_expect_tx(&sh->full[stage], STAGE_BYTES);
@@ -276,6 +162,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++issued[stage];
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
+        st = nx;
       }
       if (!ok) {  // let every copy already in flight land before the block exits
         for (int s = 0; s < STAGES; ++s)
@@ -288,22 +175,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, aphase = 0;
       bool ok = true, any = false;
+      // descriptors of stage 0; stage s adds s * STAGE_BYTES to the address field
+      const uint64_t adesc0 = sw128_desc(su32(smem));
+      const uint64_t bdesc0 = sw128_desc(su32(smem + A_BYTES));
+      uint32_t empty_addr[STAGES];
+      for (int s = 0; s < STAGES; ++s) empty_addr[s] = su32(&sh->empty[s]);
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        if (!wait_bar(&sh->tempty[acc], aphase ^ 1u, abort_flag, status)) { ok = false; break; }
+        if (!wait_fast(&sh->tempty[acc], aphase ^ 1u, abort_flag, status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!wait_bar(&sh->full[stage], phase, abort_flag, status)) { ok = false; break; }
+          if (!wait_fast(&sh->full[stage], phase, abort_flag, status)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t a_addr = su32(smem + (size_t)stage * STAGE_BYTES);
-          const uint32_t b_addr = a_addr + A_BYTES;
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            umma(d_tmem, sw128_desc(a_addr + k * 32), sw128_desc(b_addr + k * 32),
-                 (kb | k) != 0 ? 1u : 0u);
-          }
+          const uint64_t off = (uint64_t)((stage * STAGE_BYTES) >> 4);
+          umma_kblock(d_tmem, adesc0 + off, bdesc0 + off, kb != 0 ? 1u : 0u, empty_addr[stage]);
           any = true;
-          umma_commit(&sh->empty[stage]);  // frees the slot once these MMAs retire
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -322,7 +208,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t aphase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles);
-      if (!wait_bar(&sh->tfull[acc], aphase, abort_flag, status)) break;
+      if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
       tc_fence_after();
       const int row = st.m0 + quad * 32 + lane;
       const bool row_ok = row < st.m_end;
@@ -443,6 +329,15 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s) {
   if (M == 0 || N == 0) return cudaSuccess;
+  // The two-SM (cta_group::2) kernel with MOE_TC_2SM=1.  It is correct but, on
+  // ragged expert segments, its 256-row pair tiles pad more rows than the
+  // 128-row tiles here; measured slower on every workload, so not the default.
+  static const bool two_sm = [] {
+    const char* v = getenv("MOE_TC_2SM");
+    return v && v[0] == '1';
+  }();
+  if (two_sm && num_sms() >= 2)
+    return launch_gemm_tc2(a, w, bias, seg_end, M, N, K, E, act, out, status, s);
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
   if (act && act->kind != MOE_ACT_IDENTITY) {

@@ -1,0 +1,451 @@
+// Two-SM variant of the tcgen05 grouped GEMM (same contract and epilogue as
+// gemm_tc.cu; TileOPs "MoE Operators", MoEGroupedGemmFwdOp).
+//
+// A cluster of two CTAs on a pair of SMs computes a 256-row x 256-column tile
+// with tcgen05.mma.cta_group::2 (M256 N256 K16): each CTA loads its own 128
+// rows of A and HALF of the 256 B rows (stacked gated layouts: the leader
+// loads the 128 gate rows, the peer the 128 up rows; otherwise the lower and
+// upper 128 rows), so an SM ingests 32 KB per 64-wide k-block instead of the
+// 48 KB of the one-SM 128x256 tile -- a third fewer bytes per MMA, which is
+// what limits the one-SM kernel (its per-SM load rate, not DRAM or L2).
+//
+// Roles (192 threads in each CTA of the pair):
+//   warp 0 lane 0 (both CTAs): TMA producer for its own A rows and B half; the
+//     copies of both CTAs complete on the LEADER's full barrier (expect-tx of
+//     the whole 64 KB by the leader).
+//   warp 1 (both CTAs): TMEM allocation (cta_group::2); in the leader, lane 0
+//     issues the MMAs and multicasts its commits to both CTAs' empty / tfull
+//     barriers.
+//   warps 2..5 (both CTAs): epilogue of the CTA's 128 rows from its own TMEM;
+//     each thread arrives on the leader's tempty barrier (256 arrivals).
+// Every wait is bounded (2 s) as in gemm_tc.cu; on a timeout the leader drains
+// the copies and MMAs in flight before the pair frees TMEM.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <mutex>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int BMP = 256;                        // rows per CTA pair
+constexpr int BMC = 128;                        // rows per CTA
+constexpr int BN = 256;                         // accumulator columns
+constexpr int BK = 64;
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BMC * BK * 2;           // 16 KB
+constexpr int BH_BYTES = (BN / 2) * BK * 2;     // 16 KB: this CTA's half of B
+constexpr int STAGE_BYTES = A_BYTES + BH_BYTES; // 32 KB
+constexpr int TMEM_COLS = 512;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t kIdesc2 = idesc_bf16(BMP, BN);
+
+enum TcMode { kTcPlain = 0, kTcStacked = 1, kTcInterleaved = 2 };
+
+struct Tc2Shared {
+  uint64_t full[STAGES];   // leader: both CTAs' copies of a stage complete here
+  uint64_t empty[STAGES];  // both: the leader's MMA commit frees the stage
+  uint64_t tfull[2];       // both: accumulator ready
+  uint64_t tempty[2];      // leader: both epilogues have drained the accumulator
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int prefix[kMaxExperts + 1];
+  int scan_tmp[33];
+};
+// 16 KB of slack after the ring keeps every operand read of a stage inside this
+// CTA's shared memory, whatever the MMA reads past its half-tile
+constexpr int GUARD_BYTES = 16 * 1024;
+constexpr size_t kSmemBytes =
+    (size_t)STAGES * STAGE_BYTES + GUARD_BYTES + sizeof(Tc2Shared) + 1024;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared variable in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+// TMA load into this CTA's shared memory, completing on a barrier of either
+// CTA of the pair (shared::cluster address)
+__device__ __forceinline__ void tma2_2d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                        int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma2_3d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                        int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma2_4d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                        int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void umma2(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(ad), "l"(bd), "r"(kIdesc2), "r"(acc)
+      : "memory");
+}
+// the four K16 MMAs of a k-block plus the commit that frees the stage in both CTAs
+__device__ __forceinline__ void umma2_kblock(uint32_t d_tmem, uint64_t ad, uint64_t bd,
+                                             uint32_t accumulate, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %6, %7, %3, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %8, %9, %3, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %10, %11, %3, t;\n\t"
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%5], %12;\n\t}" ::"r"(d_tmem),
+      "l"(ad), "l"(bd), "r"(kIdesc2), "r"(accumulate), "r"(bar), "l"(ad + 2), "l"(bd + 2),
+      "l"(ad + 4), "l"(bd + 4), "l"(ad + 6), "l"(bd + 6), "h"((uint16_t)3)
+      : "memory");
+}
+// arrive (once) on the barrier at this offset in both CTAs when the MMAs issued
+// so far have completed
+__device__ __forceinline__ void umma2_commit_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(su32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void umma2_commit_self(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          su32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc2_kernel(const __grid_constant__ CUtensorMap tm_a,
+                    const __grid_constant__ CUtensorMap tm_b,
+                    const __nv_bfloat16* __restrict__ bias, const int32_t* __restrict__ seg_end,
+                    int M, int Nout, int N1, int K, int E, int mode, int act_kind, float limit,
+                    float alpha, float beta, __nv_bfloat16* __restrict__ out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  Tc2Shared* sh = reinterpret_cast<Tc2Shared*>(smem + (size_t)STAGES * STAGE_BYTES + GUARD_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  volatile int* abort_flag = &sh->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh->tfull[a], 1);
+      mbar_init(&sh->tempty[a], 2 * 128);
+    }
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     su32(&sh->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  const int n_tiles = mode == kTcPlain ? (Nout + BN - 1) / BN : (Nout + BN / 2 - 1) / (BN / 2);
+  const int total = build_tile_prefix(seg_end, E, M, BMP, n_tiles, sh->prefix, sh->scan_tmp);
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+  const int nkb = (K + BK - 1) / BK;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+      bool ok = true;
+      for (int tile = pair; tile < total && ok; tile += npairs) {
+        const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
+          uint8_t* a_dst = smem + (size_t)stage * STAGE_BYTES;
+          uint8_t* b_dst = a_dst + A_BYTES;
+          if (leader) mbar_expect_tx(&sh->full[stage], 2 * STAGE_BYTES);
+          const uint32_t bar = map_to_rank(su32(&sh->full[stage]), 0);
+          const int k0 = kb * BK;
+          tma2_2d(a_dst, &tm_a, bar, k0, st.m0 + BMC * (int)rank);
+          if (mode == kTcStacked) {
+            tma2_4d(b_dst, &tm_b, bar, k0, st.n_idx * (BN / 2), (int)rank, st.e);
+          } else {
+            tma2_3d(b_dst, &tm_b, bar, k0, st.n_idx * BN + (BN / 2) * (int)rank, st.e);
+          }
+          ++issued[stage];
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      if (!ok && leader) {  // both CTAs' copies complete on the leader's barriers
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) drain_wait(&sh->full[s], (issued[s] - 1u) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------ MMA issuer (leader)
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, aphase = 0;
+      bool ok = true, any = false;
+      const uint64_t adesc0 = sw128_desc(su32(smem));
+      const uint64_t bdesc0 = sw128_desc(su32(smem + A_BYTES));
+      uint32_t empty_addr[STAGES];
+      for (int s = 0; s < STAGES; ++s) empty_addr[s] = su32(&sh->empty[s]);
+      for (int tile = pair; tile < total && ok; tile += npairs) {
+        if (!wait_fast(&sh->tempty[acc], aphase ^ 1u, abort_flag, status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_fast(&sh->full[stage], phase, abort_flag, status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t off = (uint64_t)((stage * STAGE_BYTES) >> 4);
+          umma2_kblock(d_tmem, adesc0 + off, bdesc0 + off, kb != 0 ? 1u : 0u, empty_addr[stage]);
+          any = true;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma2_commit_both(&sh->tfull[acc]);
+        if (++acc == 2) { acc = 0; aphase ^= 1u; }
+      }
+      if (!ok && any) {
+        umma2_commit_self(&sh->drain);
+        drain_wait(&sh->drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (both CTAs)
+    const int quad = warp & 3;
+    int acc = 0;
+    uint32_t aphase = 0;
+    const uint32_t tempty_remote[2] = {map_to_rank(su32(&sh->tempty[0]), 0),
+                                       map_to_rank(su32(&sh->tempty[1]), 0)};
+    for (int tile = pair; tile < total; tile += npairs) {
+      const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
+      if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
+      tc_fence_after();
+      const int row = st.m0 + BMC * (int)rank + quad * 32 + lane;
+      const bool row_ok = row < st.m_end;
+      const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+      const __nv_bfloat16* be = bias ? bias + (size_t)st.e * N1 : nullptr;
+      __nv_bfloat16* orow = out + (size_t)row * Nout;
+      if (mode == kTcPlain) {
+        const int n0 = st.n_idx * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col0 = n0 + c * 32;
+          if (col0 >= Nout) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld32(tbase + c * 32, r);
+          tmem_wait_ld();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float b = (be && col0 + i < Nout) ? __bfloat162float(be[col0 + i]) : 0.f;
+            v[i] = __uint_as_float(r[i]) + b;
+          }
+          if (row_ok) store_row32(orow + col0, v, Nout - col0);
+        }
+      } else {
+        const int j0 = st.n_idx * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          const int col0 = j0 + c * 32;
+          if (col0 >= Nout) break;
+          uint32_t g[32], u[32];
+          if (mode == kTcStacked) {
+            tmem_ld32(tbase + c * 32, g);           // gate columns (leader's B half)
+            tmem_ld32(tbase + BN / 2 + c * 32, u);  // up columns (peer's B half)
+          } else {
+            tmem_ld32(tbase + c * 64, g);           // (gate, up) pairs
+            tmem_ld32(tbase + c * 64 + 32, u);
+          }
+          tmem_wait_ld();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float gv, uv;
+            int rg, ru;
+            if (mode == kTcStacked) {
+              gv = __uint_as_float(g[i]);
+              uv = __uint_as_float(u[i]);
+              rg = col0 + i;
+              ru = Nout + col0 + i;
+            } else {
+              const int p = 2 * i;
+              gv = __uint_as_float(p < 32 ? g[p] : u[p - 32]);
+              uv = __uint_as_float(p + 1 < 32 ? g[p + 1] : u[p + 1 - 32]);
+              rg = 2 * (col0 + i);
+              ru = rg + 1;
+            }
+            if (be && col0 + i < Nout) {
+              gv += __bfloat162float(be[rg]);
+              uv += __bfloat162float(be[ru]);
+            }
+            v[i] = act_kind == MOE_ACT_SILU_AND_MUL ? silu_mul(gv, uv)
+                                                    : swiglu_f(gv, uv, limit, alpha, beta);
+          }
+          if (row_ok) store_row32(orow + col0, v, Nout - col0);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_remote(tempty_remote[acc]);
+      if (++acc == 2) { acc = 0; aphase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA frees TMEM or exits while its peer still works
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+  EncodeFn fn = get_encode();
+  if (!fn) return false;
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
+                            const int32_t* seg_end, int M, int N, int K, int E,
+                            const moe_act_params* act, void* out, int* status, cudaStream_t s) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
+  float limit = 0.f, alpha = 1.f, beta = 0.f;
+  if (act && act->kind != MOE_ACT_IDENTITY) {
+    kind = act->kind;
+    mode = (kind == MOE_ACT_SWIGLU && act->swiglu_fusion == 1) ? kTcInterleaved : kTcStacked;
+    N1 = 2 * N;
+    limit = act->limit;
+    alpha = act->alpha;
+    beta = act->beta;
+  }
+  CUtensorMap ma, mb;
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t str[1] = {(cuuint64_t)K * 2};
+    cuuint32_t box[2] = {BK, BMC};
+    if (!encode(&ma, a, 2, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  if (mode == kTcStacked) {
+    cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)N, 2, (cuuint64_t)E};
+    cuuint64_t str[3] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2, (cuuint64_t)2 * N * K * 2};
+    cuuint32_t box[4] = {BK, BN / 2, 1, 1};
+    if (!encode(&mb, w, 4, dims, str, box)) return cudaErrorInvalidValue;
+  } else {
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N1, (cuuint64_t)E};
+    cuuint64_t str[2] = {(cuuint64_t)K * 2, (cuuint64_t)N1 * K * 2};
+    cuuint32_t box[3] = {BK, BN / 2, 1};
+    if (!encode(&mb, w, 3, dims, str, box)) return cudaErrorInvalidValue;
+  }
+  static std::once_flag attr_once;
+  std::call_once(attr_once, [] {
+    cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kSmemBytes);
+  });
+  const int n_tiles = mode == kTcPlain ? (N + BN - 1) / BN : (N + BN / 2 - 1) / (BN / 2);
+  const long long max_tiles = (long long)((M + BMP - 1) / BMP + E) * n_tiles;
+  const int pairs = (int)std::max<long long>(1, std::min<long long>(max_tiles, num_sms() / 2));
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, ma, mb,
+                                     static_cast<const __nv_bfloat16*>(bias), seg_end, M, N, N1,
+                                     K, E, mode, kind, limit, alpha, beta,
+                                     static_cast<__nv_bfloat16*>(out), status);
+  count_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace moe
