@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace moe {
 namespace {
@@ -152,10 +153,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_expect_tx(&sh->full[stage], STAGE_BYTES);
           const int k0 = kb * BK;
           tma_2d(a_dst, &tm_a, &sh->full[stage], k0, st.m0);
-          if (mode == kTcStacked) {
-            const int j0 = st.n_idx * (BN / 2);
-            tma_4d(b_dst, &tm_b, &sh->full[stage], k0, j0, 0, st.e);
-            tma_4d(b_dst + B_BYTES / 2, &tm_b, &sh->full[stage], k0, j0, 1, st.e);
+          if (mode == kTcStacked) {  // gate rows j0.. then up rows F+j0.. in one box
+            tma_4d(b_dst, &tm_b, &sh->full[stage], k0, st.n_idx * (BN / 2), 0, st.e);
           } else {
             tma_3d(b_dst, &tm_b, &sh->full[stage], k0, st.n_idx * BN, st.e);
           }
@@ -292,49 +291,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ------------------------------------------------------------ host side
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn get_encode() {
-  static EncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(p);
-  });
-  return fn;
-}
-
-bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box) {
-  EncodeFn fn = get_encode();
-  if (!fn) return false;
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr),
-                  dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s) {
   if (M == 0 || N == 0) return cudaSuccess;
-  // The two-SM (cta_group::2) kernel with MOE_TC_2SM=1.  It is correct but, on
-  // ragged expert segments, its 256-row pair tiles pad more rows than the
+  // The two-SM (cta_group::2) kernel with MOE_TC_KERNEL=2sm.  It is correct but,
+  // on ragged expert segments, its 256-row pair tiles pad more rows than the
   // 128-row tiles here; measured slower on every workload, so not the default.
   static const bool two_sm = [] {
-    const char* v = getenv("MOE_TC_2SM");
-    return v && v[0] == '1';
+    const char* v = getenv("MOE_TC_KERNEL");
+    return v && v[0] == '2';
   }();
   if (two_sm && num_sms() >= 2)
     return launch_gemm_tc2(a, w, bias, seg_end, M, N, K, E, act, out, status, s);
@@ -353,18 +321,18 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {BK, BM};
-    if (!encode(&ma, a, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tmap::encode_bf16(&ma, a, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   if (mode == kTcStacked) {
     cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)N, 2, (cuuint64_t)E};
     cuuint64_t str[3] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2, (cuuint64_t)2 * N * K * 2};
-    cuuint32_t box[4] = {BK, BN / 2, 1, 1};
-    if (!encode(&mb, w, 4, dims, str, box)) return cudaErrorInvalidValue;
+    cuuint32_t box[4] = {BK, BN / 2, 2, 1};  // 128 gate rows then 128 up rows
+    if (!tmap::encode_bf16(&mb, w, 4, dims, str, box)) return cudaErrorInvalidValue;
   } else {
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N1, (cuuint64_t)E};
     cuuint64_t str[2] = {(cuuint64_t)K * 2, (cuuint64_t)N1 * K * 2};
     cuuint32_t box[3] = {BK, BN, 1};
-    if (!encode(&mb, w, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tmap::encode_bf16(&mb, w, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {

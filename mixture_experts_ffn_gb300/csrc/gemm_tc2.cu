@@ -28,6 +28,7 @@
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "tmap.h"
 
 namespace moe {
 namespace {
@@ -356,35 +357,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn get_encode() {
-  static EncodeFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeFn>(p);
-  });
-  return fn;
-}
-
-bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box) {
-  EncodeFn fn = get_encode();
-  if (!fn) return false;
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims,
-            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
@@ -406,18 +378,18 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {BK, BMC};
-    if (!encode(&ma, a, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tmap::encode_bf16(&ma, a, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
   if (mode == kTcStacked) {
     cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)N, 2, (cuuint64_t)E};
     cuuint64_t str[3] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2, (cuuint64_t)2 * N * K * 2};
     cuuint32_t box[4] = {BK, BN / 2, 1, 1};
-    if (!encode(&mb, w, 4, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tmap::encode_bf16(&mb, w, 4, dims, str, box)) return cudaErrorInvalidValue;
   } else {
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N1, (cuuint64_t)E};
     cuuint64_t str[2] = {(cuuint64_t)K * 2, (cuuint64_t)N1 * K * 2};
     cuuint32_t box[3] = {BK, BN / 2, 1};
-    if (!encode(&mb, w, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tmap::encode_bf16(&mb, w, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {

@@ -11,6 +11,8 @@
 //   scatter : one warp per chunk; routes of a chunk are ranked in order with
 //             warp match-any, so rows inside an expert follow ascending route
 //   gather  : one warp per row copies the hidden row with 128-bit accesses
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
@@ -72,8 +74,16 @@ __global__ void __launch_bounds__(1024) perm_scan(int* __restrict__ counts, int 
   // per-expert totals of this thread's experts
   int tot_local = 0, act_local = 0;
   for (int e = lo; e < hi; ++e) {
-    int s = 0;
-    for (int c = 0; c < C; ++c) s += counts[(size_t)c * E + e];
+    int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
+    int c = 0;
+    for (; c + 4 <= C; c += 4) {  // independent loads in flight
+      s0 += counts[(size_t)c * E + e];
+      s1 += counts[(size_t)(c + 1) * E + e];
+      s2 += counts[(size_t)(c + 2) * E + e];
+      s3 += counts[(size_t)(c + 3) * E + e];
+    }
+    for (; c < C; ++c) s0 += counts[(size_t)c * E + e];
+    const int s = s0 + s1 + s2 + s3;
     tot_local += s;
     act_local += s > 0;
   }
@@ -137,6 +147,66 @@ __global__ void __launch_bounds__(32) perm_scatter(const int32_t* __restrict__ i
   }
 }
 
+// Scatter of one chunk by W warps: warp w ranks its routes with match-any
+// (one round per 32 routes), the per-warp expert counts are prefixed across
+// warps in shared memory, then every route gets row = chunk start of its
+// expert + routes of that expert in earlier warps + its rank in the warp.
+// Rows inside an expert therefore follow ascending route index.
+__global__ void __launch_bounds__(1024) perm_scatter_cta(const int32_t* __restrict__ ids, int M,
+                                                         int E, const int* __restrict__ offsets,
+                                                         int32_t* __restrict__ row_to_route,
+                                                         int32_t* __restrict__ route_to_row) {
+  extern __shared__ int wcnt[];  // [W][E]: counts, then exclusive row bases
+  const int W = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per_warp = kPermuteChunk / W;  // routes per warp, a multiple of 32
+  for (int i = threadIdx.x; i < W * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const int r0 = blockIdx.x * kPermuteChunk + warp * per_warp;
+  const int r1 = min(M, min(blockIdx.x * kPermuteChunk + kPermuteChunk, r0 + per_warp));
+  const uint32_t lt = (1u << lane) - 1u;
+  int* mine = wcnt + (size_t)warp * E;
+  constexpr int kMaxRounds = kPermuteChunk / 32;
+  int rank_of[kMaxRounds];  // rank of this lane's route in round j
+  for (int j = 0; j * 32 < per_warp; ++j) {
+    const int r = r0 + j * 32 + lane;
+    const bool valid = r < r1;
+    const int id = valid ? __ldg(ids + r) : -1;
+    const bool ok = valid && id >= 0 && id < E;
+    const int key = ok ? id : -1 - lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    const int before = ok ? mine[id] : 0;
+    __syncwarp();
+    if (ok && __popc(peers & lt) == 0) mine[id] = before + __popc(peers);
+    __syncwarp();
+    rank_of[j & (kMaxRounds - 1)] = before + __popc(peers & lt);
+  }
+  __syncthreads();
+  // exclusive prefix over warps, per expert, seeded with the chunk's start row
+  const int* off = offsets + (size_t)blockIdx.x * E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = off[e];
+    for (int w = 0; w < W; ++w) {
+      const int c = wcnt[(size_t)w * E + e];
+      wcnt[(size_t)w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int j = 0; j * 32 < per_warp; ++j) {
+    const int r = r0 + j * 32 + lane;
+    if (r >= r1) break;
+    const int id = __ldg(ids + r);
+    if (id >= 0 && id < E) {
+      const int row = mine[id] + rank_of[j & (kMaxRounds - 1)];
+      row_to_route[row] = r;
+      route_to_row[r] = row;
+    } else {
+      route_to_row[r] = -1;
+    }
+  }
+}
+
 // expert_input[row] = hidden[row_to_route[row] / K], rows < seg_end[E-1]
 template <int VEC_BYTES>
 __global__ void __launch_bounds__(256) perm_gather(const char* __restrict__ hidden,
@@ -177,44 +247,54 @@ __global__ void __launch_bounds__(256) perm_gather(const char* __restrict__ hidd
   }
 }
 
-// out[t] = scale * sum_k w[t,k] * y[route_to_row[t*K+k]], fixed k order, fp32
+// out[t] = scale * sum_k w[t,k] * y[route_to_row[t*K+k]], fixed k order, fp32.
+// One item = VEC consecutive columns of one token; persistent grid-stride
+// threads take items i, i + stride, ..., so that each thread keeps several
+// rows' loads in flight and no block is launched for a few loads only.
 template <typename T, int VEC>
-__global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y,
-                                                      const float* __restrict__ w,
-                                                      const int32_t* __restrict__ r2r, int Tn,
-                                                      int K, int H, int M, float scale,
-                                                      T* __restrict__ out) {
-  const int t = blockIdx.x;
-  const int nvec = H / VEC;
-  const int v = blockIdx.y * blockDim.x + threadIdx.x;
-  if (v >= nvec) return;
+__device__ __forceinline__ void combine_item(const T* __restrict__ y, const float* __restrict__ w,
+                                             const int32_t* __restrict__ r2r, int K, int H,
+                                             int M, float scale, T* __restrict__ out, int t,
+                                             int v) {
   float acc[VEC];
 #pragma unroll
   for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
   const int32_t* rr = r2r + (size_t)t * K;
   const float* ww = w + (size_t)t * K;
-  for (int k = 0; k < K; ++k) {
-    const int row = __ldg(rr + k);
-    if (row < 0 || row >= M) continue;
-    const float wk = __ldg(ww + k);
-    const T* src = y + (size_t)row * H + (size_t)v * VEC;
-    if constexpr (VEC == 8) {  // bf16 x 8 = 16 bytes
-      int4 q = __ldg(reinterpret_cast<const int4*>(src));
-      const uint32_t u[4] = {(uint32_t)q.x, (uint32_t)q.y, (uint32_t)q.z, (uint32_t)q.w};
+  for (int k0 = 0; k0 < K; k0 += 8) {
+    // all index and weight loads of the group first, then the row loads
+    int row[8];
+    float wk[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        acc[2 * i] = fmaf(wk, bf16_lo(u[i]), acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wk, bf16_hi(u[i]), acc[2 * i + 1]);
+    for (int j = 0; j < 8; ++j) {
+      const bool in = k0 + j < K;
+      row[j] = in ? __ldg(rr + k0 + j) : -1;
+      wk[j] = in ? __ldg(ww + k0 + j) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const bool ok = row[j] >= 0 && row[j] < M;
+      const T* src = y + (size_t)(ok ? row[j] : 0) * H + (size_t)v * VEC;
+      if constexpr (VEC == 8) {  // bf16 x 8 = 16 bytes
+        int4 q = ok ? __ldg(reinterpret_cast<const int4*>(src)) : make_int4(0, 0, 0, 0);
+        const uint32_t u[4] = {(uint32_t)q.x, (uint32_t)q.y, (uint32_t)q.z, (uint32_t)q.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = fmaf(wk[j], bf16_lo(u[i]), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wk[j], bf16_hi(u[i]), acc[2 * i + 1]);
+        }
+      } else if constexpr (VEC == 4) {  // f32 x 4
+        float4 q = ok ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0, 0, 0, 0);
+        acc[0] = fmaf(wk[j], q.x, acc[0]);
+        acc[1] = fmaf(wk[j], q.y, acc[1]);
+        acc[2] = fmaf(wk[j], q.z, acc[2]);
+        acc[3] = fmaf(wk[j], q.w, acc[3]);
+      } else {
+        if (ok) {
+#pragma unroll
+          for (int i = 0; i < VEC; ++i) acc[i] = fmaf(wk[j], Elem<T>::to_f(src[i]), acc[i]);
+        }
       }
-    } else if constexpr (VEC == 4) {  // f32 x 4
-      float4 q = __ldg(reinterpret_cast<const float4*>(src));
-      acc[0] = fmaf(wk, q.x, acc[0]);
-      acc[1] = fmaf(wk, q.y, acc[1]);
-      acc[2] = fmaf(wk, q.z, acc[2]);
-      acc[3] = fmaf(wk, q.w, acc[3]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < VEC; ++i) acc[i] = fmaf(wk, Elem<T>::to_f(src[i]), acc[i]);
     }
   }
   T* dst = out + (size_t)t * H + (size_t)v * VEC;
@@ -231,6 +311,21 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y,
   } else {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) dst[i] = Elem<T>::from_f(scale * acc[i]);
+  }
+}
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
+                                                      const float* __restrict__ w,
+                                                      const int32_t* __restrict__ r2r, int Tn,
+                                                      int K, int H, int M, float scale,
+                                                      T* __restrict__ out) {
+  const int nvec = H / VEC;
+  const long long items = (long long)Tn * nvec;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < items; i += stride) {
+    const int t = (int)(i / nvec), v = (int)(i - (long long)t * nvec);
+    combine_item<T, VEC>(y, w, r2r, K, H, M, scale, out, t, v);
   }
 }
 
@@ -255,7 +350,22 @@ cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int 
   const size_t hist_smem = (size_t)E * 4;
   perm_count<<<C, 256, hist_smem, s>>>(ids, M, E, counts, status);
   perm_scan<<<1, 1024, 0, s>>>(counts, C, E, seg_end, active, num_active);
-  perm_scatter<<<C, 32, hist_smem, s>>>(ids, M, E, counts, row_to_route, route_to_row);
+  // one CTA of W warps per chunk while W x E counts fit in 96 KB of shared
+  // memory; otherwise one warp per chunk
+  int W = 32;
+  while (W > 1 && (size_t)W * E * 4 > 96 * 1024) W >>= 1;
+  if (W >= 4) {
+    const size_t sm = (size_t)W * E * 4;
+    static bool attr_set = false;
+    if (!attr_set) {
+      cudaFuncSetAttribute(perm_scatter_cta, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           96 * 1024);
+      attr_set = true;
+    }
+    perm_scatter_cta<<<C, W * 32, sm, s>>>(ids, M, E, counts, row_to_route, route_to_row);
+  } else {
+    perm_scatter<<<C, 32, hist_smem, s>>>(ids, M, E, counts, row_to_route, route_to_row);
+  }
   count_launch(3);
   if (expert_input) {
     const size_t row_bytes = (size_t)H * esz;
@@ -281,29 +391,28 @@ cudaError_t launch_combine(const void* y, const float* w, const int32_t* r2r, in
   if (T == 0 || H == 0) return cudaSuccess;
   const int M = T * K;
   const bool aligned = ((uintptr_t)y % 16 == 0) && ((uintptr_t)out % 16 == 0);
+  auto grid_for = [&](int vec) {
+    const long long items = (long long)T * (H / vec);
+    const long long cap = (long long)num_sms() * 8;
+    return (unsigned)std::max<long long>(1, std::min<long long>(cap, (items + 255) / 256));
+  };
   if (dt == MOE_BF16) {
     using B = __nv_bfloat16;
-    if (aligned && H % 8 == 0) {
-      int nvec = H / 8;
-      dim3 grid(T, (nvec + 127) / 128);
-      combine_kernel<B, 8><<<grid, 128, 0, s>>>(static_cast<const B*>(y), w, r2r, T, K, H, M,
-                                                scale, static_cast<B*>(out));
-    } else {
-      dim3 grid(T, (H + 127) / 128);
-      combine_kernel<B, 1><<<grid, 128, 0, s>>>(static_cast<const B*>(y), w, r2r, T, K, H, M,
-                                                scale, static_cast<B*>(out));
-    }
+    if (aligned && H % 8 == 0)
+      combine_kernel<B, 8><<<grid_for(8), 256, 0, s>>>(static_cast<const B*>(y), w, r2r, T, K, H,
+                                                       M, scale, static_cast<B*>(out));
+    else
+      combine_kernel<B, 1><<<grid_for(1), 256, 0, s>>>(static_cast<const B*>(y), w, r2r, T, K, H,
+                                                       M, scale, static_cast<B*>(out));
   } else {
-    if (aligned && H % 4 == 0) {
-      int nvec = H / 4;
-      dim3 grid(T, (nvec + 127) / 128);
-      combine_kernel<float, 4><<<grid, 128, 0, s>>>(static_cast<const float*>(y), w, r2r, T, K, H,
-                                                    M, scale, static_cast<float*>(out));
-    } else {
-      dim3 grid(T, (H + 127) / 128);
-      combine_kernel<float, 1><<<grid, 128, 0, s>>>(static_cast<const float*>(y), w, r2r, T, K, H,
-                                                    M, scale, static_cast<float*>(out));
-    }
+    if (aligned && H % 4 == 0)
+      combine_kernel<float, 4><<<grid_for(4), 256, 0, s>>>(static_cast<const float*>(y), w, r2r,
+                                                           T, K, H, M, scale,
+                                                           static_cast<float*>(out));
+    else
+      combine_kernel<float, 1><<<grid_for(1), 256, 0, s>>>(static_cast<const float*>(y), w, r2r,
+                                                           T, K, H, M, scale,
+                                                           static_cast<float*>(out));
   }
   count_launch();
   return cudaGetLastError();

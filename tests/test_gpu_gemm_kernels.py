@@ -1,6 +1,6 @@
-"""The two-SM (cta_group::2) variant of the tcgen05 grouped GEMM, selected with
-MOE_TC_2SM=1, runs the whole grouped-GEMM parity file in a fresh process (the
-switch is read once per process)."""
+"""The alternative tcgen05 grouped-GEMM kernel -- two-SM cta_group::2 tiles,
+selected with MOE_TC_KERNEL=2sm -- runs the whole grouped-GEMM parity file in a
+fresh process (the switch is read once per process)."""
 import os
 import subprocess
 import sys
@@ -12,8 +12,9 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-def test_two_sm_gemm_parity():
-    env = dict(os.environ, MOE_TC_2SM="1")
+@pytest.mark.parametrize("kernel", ["2sm"])
+def test_alternative_gemm_kernel_parity(kernel):
+    env = dict(os.environ, MOE_TC_KERNEL=kernel)
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(HERE, "test_gpu_gemm.py"),
                         "-q", "-p", "no:cacheprovider"], env=env, capture_output=True, text=True,
                        timeout=900)
