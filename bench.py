@@ -464,7 +464,8 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
 
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
     dev = inp["hidden"].device
-    tw, ti, _, _ = moe.moe_route(inp["logits"], p)
+    p = moe.config_params(cfg.replace(local_count=0))[0]
+    tw, ti, _, _ = moe.moe_route(inp["logits"], p, inp["correction_bias"], inp["expert_ids"])
     perm = moe.moe_permute(ti, E, inp["hidden"])
     act_out = torch.empty((T * K, F), dtype=torch.bfloat16, device=dev)
     y = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
@@ -472,6 +473,8 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
                              out=act_out)
     moe.moe_grouped_gemm_down(act_out, inp["w_down"], perm["seg_end"], out=y)
     fns = {
+        "indexed_mlp": lambda: moe.moe_indexed_mlp(inp["hidden"], inp["w_gate_up"], inp["w_down"],
+                                                   tw, ti),
         "route": lambda: moe.moe_route(inp["logits"], p, topk_weights=tw, topk_ids=ti),
         "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"]),
         "gemm_act": lambda: moe.moe_grouped_gemm_act(perm["expert_input"], inp["w_gate_up"],
@@ -529,7 +532,8 @@ def main():
                     help="KEY=VAL[,KEY=VAL] changes to the workload recipe (profiling of "
                          "reduced cases only; the bench line of record uses none)")
     ap.add_argument("--stage", default=None,
-                    choices=["route", "permute", "gemm_act", "gemm_down", "combine"],
+                    choices=["route", "permute", "gemm_act", "gemm_down", "combine",
+                             "indexed_mlp"],
                     help="time one stage alone (for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

@@ -57,10 +57,40 @@ struct TcShared {
   int prefix[kMaxExperts + 1];
   int scan_tmp[33];
 };
-constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + sizeof(TcShared) + 1024;
+// Output staging: each epilogue warp owns two 2 KB buffers (32 rows x 32 bf16
+// columns, 64-byte swizzle) that it fills from registers and hands to a TMA
+// store, so the output leaves the SM as whole boxes instead of 32 scattered
+// row segments per store instruction (those flood the L1/shared-memory data
+// path that tcgen05.mma reads its operands through).
+constexpr int OUT_BOX = 32;                        // rows and columns of one staged box
+constexpr int OUT_BUF_BYTES = OUT_BOX * OUT_BOX * 2;  // 2 KB
+constexpr int OUT_BYTES = 4 * 2 * OUT_BUF_BYTES;      // 4 warps x 2 buffers
+constexpr size_t kSmemBytes =
+    (size_t)STAGES * STAGE_BYTES + OUT_BYTES + sizeof(TcShared) + 1024;
 
 
 constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
+
+// Epilogue activation math.  The exponential and the quotient use the fast
+// hardware approximations (relative error about 1e-6 over the arguments an
+// activation sees), far below the bf16 rounding of the stored result; every
+// branch on the mode and the activation is resolved at compile time so the 32
+// columns of a chunk are independent instruction streams.
+__device__ __forceinline__ float fast_sigmoid(float x) {
+  return __fdividef(1.0f, 1.0f + __expf(-x));
+}
+template <int ACT>
+__device__ __forceinline__ float gated(float g, float u, float limit, float alpha, float beta) {
+  if constexpr (ACT == MOE_ACT_SILU_AND_MUL) {
+    return g * fast_sigmoid(g) * u;
+  } else {
+    if (limit > 0.0f) {
+      g = fminf(g, limit);
+      u = fmaxf(fminf(u, limit), -limit);
+    }
+    return g * fast_sigmoid(alpha * g) * (u + beta);
+  }
+}
 
 // The four K16 MMAs of one 64-wide k-block and the commit that frees its stage,
 // in one block: descriptors advance by 32 bytes (2 in 16-byte units) per K16.
@@ -88,15 +118,18 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 }
 
 
+template <int MODE, int ACT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __nv_bfloat16* __restrict__ bias, const int32_t* __restrict__ seg_end,
-                   int M, int Nout, int N1, int K, int E, int mode, int act_kind, float limit,
-                   float alpha, float beta, __nv_bfloat16* __restrict__ out, int* status) {
+                   int M, int Nout, int N1, int K, int E, float limit, float alpha, float beta,
+                   const __grid_constant__ CUtensorMap tm_out, int tma_out,
+                   __nv_bfloat16* __restrict__ out, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  TcShared* sh = reinterpret_cast<TcShared*>(smem + (size_t)STAGES * STAGE_BYTES);
+  uint8_t* out_stage = smem + (size_t)STAGES * STAGE_BYTES;  // 1024-byte aligned
+  TcShared* sh = reinterpret_cast<TcShared*>(out_stage + OUT_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile int* abort_flag = &sh->abort;
 
@@ -124,7 +157,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  const int n_tiles = mode == kTcPlain ? (Nout + BN - 1) / BN : (Nout + BN / 2 - 1) / (BN / 2);
+  const int n_tiles = MODE == kTcPlain ? (Nout + BN - 1) / BN : (Nout + BN / 2 - 1) / (BN / 2);
   const int total = build_tile_prefix(seg_end, E, M, BM, n_tiles, sh->prefix, sh->scan_tmp);
   tc_fence_before();
   __syncthreads();
@@ -153,7 +186,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           mbar_expect_tx(&sh->full[stage], STAGE_BYTES);
           const int k0 = kb * BK;
           tma_2d(a_dst, &tm_a, &sh->full[stage], k0, st.m0);
-          if (mode == kTcStacked) {  // gate rows j0.. then up rows F+j0.. in one box
+          if constexpr (MODE == kTcStacked) {  // gate rows j0.. then up rows F+j0.. in one box
             tma_4d(b_dst, &tm_b, &sh->full[stage], k0, st.n_idx * (BN / 2), 0, st.e);
           } else {
             tma_3d(b_dst, &tm_b, &sh->full[stage], k0, st.n_idx * BN, st.e);
@@ -205,6 +238,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
     int acc = 0;
     uint32_t aphase = 0;
+    uint8_t* obufs = out_stage + quad * 2 * OUT_BUF_BYTES;
+    int obuf = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles);
       if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
@@ -214,7 +249,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
       const __nv_bfloat16* be = bias ? bias + (size_t)st.e * N1 : nullptr;
       __nv_bfloat16* orow = out + (size_t)row * Nout;
-      if (mode == kTcPlain) {
+      const int wrow0 = st.m0 + quad * 32;
+      // Whole-box TMA stores only where all 32 rows of this warp belong to the
+      // tile's expert segment; a ragged tail stores row by row instead so it
+      // never writes rows of the next segment.
+      const bool boxed = tma_out && st.m_end - wrow0 >= OUT_BOX;
+      auto emit = [&](const float (&v)[32], int col0) {
+        if (boxed) {
+          uint8_t* buf = obufs + obuf * OUT_BUF_BYTES;
+          if (lane == 0) bulk_wait_read<1>();  // the store from this buffer two boxes ago
+          __syncwarp();
+          // row `lane`, 16-byte chunk q lands at chunk q ^ ((lane >> 1) & 3)
+          // (the 64-byte swizzle the output map describes): conflict-free
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 u;
+            u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+            u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+            u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+            u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = u;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tm_out, buf, col0, wrow0);
+            bulk_commit();
+          }
+          obuf ^= 1;
+        } else if (row_ok) {
+          store_row32(orow + col0, v, Nout - col0);
+        }
+      };
+      if constexpr (MODE == kTcPlain) {
         const int n0 = st.n_idx * BN;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -225,11 +292,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tmem_wait_ld();
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float b = (be && col0 + i < Nout) ? __bfloat162float(be[col0 + i]) : 0.f;
-            v[i] = __uint_as_float(r[i]) + b;
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          if (be) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (col0 + i < Nout) v[i] += __bfloat162float(be[col0 + i]);
           }
-          if (row_ok) store_row32(orow + col0, v, Nout - col0);
+          emit(v, col0);
         }
       } else {
         const int j0 = st.n_idx * (BN / 2);
@@ -238,7 +307,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int col0 = j0 + c * 32;  // activation column
           if (col0 >= Nout) break;
           uint32_t g[32], u[32];
-          if (mode == kTcStacked) {
+          if constexpr (MODE == kTcStacked) {
             tmem_ld32(tbase + c * 32, g);             // gate columns
             tmem_ld32(tbase + BN / 2 + c * 32, u);    // up columns
           } else {
@@ -246,38 +315,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_ld32(tbase + c * 64 + 32, u);
           }
           tmem_wait_ld();
-          float v[32];
+          float gv[32], uv[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            float gv, uv;
-            int rg, ru;
-            if (mode == kTcStacked) {
-              gv = __uint_as_float(g[i]);
-              uv = __uint_as_float(u[i]);
-              rg = col0 + i;
-              ru = Nout + col0 + i;
-            } else {
-              // pair i lives in columns 2i, 2i+1 of the 64 loaded
-              const int p = 2 * i;
-              gv = __uint_as_float(p < 32 ? g[p] : u[p - 32]);
-              uv = __uint_as_float(p + 1 < 32 ? g[p + 1] : u[p + 1 - 32]);
-              rg = 2 * (col0 + i);
-              ru = rg + 1;
+            if constexpr (MODE == kTcStacked) {
+              gv[i] = __uint_as_float(g[i]);
+              uv[i] = __uint_as_float(u[i]);
+            } else {  // pair i lives in columns 2i, 2i+1 of the 64 loaded
+              gv[i] = __uint_as_float(2 * i < 32 ? g[2 * i] : u[2 * i - 32]);
+              uv[i] = __uint_as_float(2 * i + 1 < 32 ? g[2 * i + 1] : u[2 * i + 1 - 32]);
             }
-            if (be && col0 + i < Nout) {
-              gv += __bfloat162float(be[rg]);
-              uv += __bfloat162float(be[ru]);
-            }
-            v[i] = act_kind == MOE_ACT_SILU_AND_MUL ? silu_mul(gv, uv)
-                                                    : swiglu_f(gv, uv, limit, alpha, beta);
           }
-          if (row_ok) store_row32(orow + col0, v, Nout - col0);
+          if (be) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (col0 + i < Nout) {
+                const int rg = MODE == kTcStacked ? col0 + i : 2 * (col0 + i);
+                const int ru = MODE == kTcStacked ? Nout + col0 + i : rg + 1;
+                gv[i] += __bfloat162float(be[rg]);
+                uv[i] += __bfloat162float(be[ru]);
+              }
+            }
+          }
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = gated<ACT>(gv[i], uv[i], limit, alpha, beta);
+          emit(v, col0);
         }
       }
       tc_fence_before();
       mbar_arrive(&sh->tempty[acc]);
       if (++acc == 2) { acc = 0; aphase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();  // every staged box written before the block exits
   }
 
   tc_fence_before();
@@ -336,15 +406,34 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
   }
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
-    cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kSmemBytes);
+    for (auto fn : {gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY>,
+                    gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>,
+                    gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU>,
+                    gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU>})
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   });
   const int n_tiles = mode == kTcPlain ? (N + BN - 1) / BN : (N + BN / 2 - 1) / (BN / 2);
   const long long max_tiles = (long long)((M + BM - 1) / BM + E) * n_tiles;
   const int grid = (int)std::max<long long>(1, std::min<long long>(max_tiles, num_sms()));
-  gemm_tc_kernel<<<grid, NUM_THREADS, kSmemBytes, s>>>(
-      ma, mb, static_cast<const __nv_bfloat16*>(bias), seg_end, M, N, N1, K, E, mode, kind, limit,
-      alpha, beta, static_cast<__nv_bfloat16*>(out), status);
+  // Output map for the staged stores: rows of Nout bf16, 32 x 32 boxes.  TMA
+  // needs a 16-byte aligned base and row pitch; otherwise rows are stored
+  // directly from registers.
+  CUtensorMap mo;
+  int tma_out = 0;
+  if (N % 8 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t str[1] = {(cuuint64_t)N * 2};
+    cuuint32_t box[2] = {OUT_BOX, OUT_BOX};
+    tma_out = tmap::encode_bf16(&mo, out, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
+  }
+  if (!tma_out) mo = ma;  // unused
+  auto* kern = mode == kTcPlain     ? gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY>
+               : mode == kTcInterleaved ? gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU>
+               : kind == MOE_ACT_SWIGLU ? gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU>
+                                        : gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>;
+  kern<<<grid, NUM_THREADS, kSmemBytes, s>>>(ma, mb, static_cast<const __nv_bfloat16*>(bias),
+                                             seg_end, M, N, N1, K, E, limit, alpha, beta, mo,
+                                             tma_out, static_cast<__nv_bfloat16*>(out), status);
   count_launch();
   return cudaGetLastError();
 }

@@ -31,14 +31,16 @@ inline EncodeFn get_encode() {
 }
 
 // rank-D bf16 map: dims[0] is the contiguous dimension; strides in bytes for
-// dims 1..D-1; box in elements
+// dims 1..D-1; box in elements.  The swizzle defaults to 128 bytes (operand
+// tiles read by tcgen05.mma); output staging uses 64 bytes.
 inline bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
-                        const cuuint64_t* strides, const cuuint32_t* box) {
+                        const cuuint64_t* strides, const cuuint32_t* box,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeFn fn = get_encode();
   if (!fn) return false;
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims,
-            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
