@@ -1,0 +1,163 @@
+// Epilogue shared by the tcgen05 grouped-GEMM kernels: the accumulator layout
+// modes, the gated activations, and the drain of one 128-lane x 256-column
+// accumulator to bf16 output rows through swizzled shared-memory staging and
+// TMA stores.
+#pragma once
+
+#include <cuda.h>
+
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace tc {
+
+// How the accumulator columns of a tile map to output columns: plain GEMM
+// columns; gate rows j0.. then up rows F+j0.. (stacked halves); or (gate, up)
+// pairs in consecutive columns (interleaved rows of the weight).
+enum TcMode { kTcPlain = 0, kTcStacked = 1, kTcInterleaved = 2 };
+
+constexpr int kEpiCols = 256;  // accumulator columns of one tile
+
+// Output staging: each epilogue warp owns two 2 KB buffers (32 rows x 32 bf16
+// columns, 64-byte swizzle) that it fills from registers and hands to a TMA
+// store, so the output leaves the SM as whole boxes instead of 32 scattered
+// row segments per store instruction (those flood the L1/shared-memory data
+// path that tcgen05.mma reads its operands through).
+constexpr int OUT_BOX = 32;                        // rows and columns of one staged box
+constexpr int OUT_BUF_BYTES = OUT_BOX * OUT_BOX * 2;  // 2 KB
+constexpr int OUT_BYTES = 4 * 2 * OUT_BUF_BYTES;      // 4 warps x 2 buffers
+
+// Epilogue activation math.  The exponential and the quotient use the fast
+// hardware approximations (relative error about 1e-6 over the arguments an
+// activation sees), far below the bf16 rounding of the stored result; every
+// branch on the mode and the activation is resolved at compile time so the 32
+// columns of a chunk are independent instruction streams.
+__device__ __forceinline__ float fast_sigmoid(float x) {
+  return __fdividef(1.0f, 1.0f + __expf(-x));
+}
+template <int ACT>
+__device__ __forceinline__ float gated(float g, float u, float limit, float alpha, float beta) {
+  if constexpr (ACT == MOE_ACT_SILU_AND_MUL) {
+    return g * fast_sigmoid(g) * u;
+  } else {
+    if (limit > 0.0f) {
+      g = fminf(g, limit);
+      u = fmaxf(fminf(u, limit), -limit);
+    }
+    return g * fast_sigmoid(alpha * g) * (u + beta);
+  }
+}
+
+// Epilogue of one 128-lane x 256-column accumulator for the 32 rows of the
+// calling warp (TMEM lanes 32*(warp%4).., row wrow0 + lane): bias, activation,
+// bf16 rounding and the store.  Rows at or past m_end (the end of the tile's
+// expert segment) are not written.
+template <int MODE, int ACT>
+__device__ __forceinline__ void drain_acc(uint32_t tbase, int wrow0, int m_end, int n_idx, int e,
+                                          const __nv_bfloat16* __restrict__ bias, int N1, int Nout,
+                                          float limit, float alpha, float beta,
+                                          const CUtensorMap* tm_out, int tma_out,
+                                          __nv_bfloat16* __restrict__ out, uint8_t* obufs,
+                                          int& obuf, int lane) {
+  const int row = wrow0 + lane;
+  const bool row_ok = row < m_end;
+  const __nv_bfloat16* be = bias ? bias + (size_t)e * N1 : nullptr;
+  __nv_bfloat16* orow = out + (size_t)row * Nout;
+  // Whole-box TMA stores only where all 32 rows of this warp belong to the
+  // tile's expert segment; a ragged tail stores row by row instead so it
+  // never writes rows of the next segment.
+  const bool boxed = tma_out && m_end - wrow0 >= OUT_BOX;
+  auto emit = [&](const float (&v)[32], int col0) {
+    if (boxed) {
+      uint8_t* buf = obufs + obuf * OUT_BUF_BYTES;
+      if (lane == 0) bulk_wait_read<1>();  // the store from this buffer two boxes ago
+      __syncwarp();
+      // row `lane`, 16-byte chunk q lands at chunk q ^ ((lane >> 1) & 3)
+      // (the 64-byte swizzle the output map describes): conflict-free
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint4 u;
+        u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+        u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+        u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+        u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+        *reinterpret_cast<uint4*>(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = u;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm_out, buf, col0, wrow0);
+        bulk_commit();
+      }
+      obuf ^= 1;
+    } else if (row_ok) {
+      store_row32(orow + col0, v, Nout - col0);
+    }
+  };
+  if constexpr (MODE == kTcPlain) {
+    const int n0 = n_idx * kEpiCols;
+#pragma unroll 1
+    for (int c = 0; c < kEpiCols / 32; ++c) {
+      const int col0 = n0 + c * 32;
+      if (col0 >= Nout) break;  // warp-uniform
+      uint32_t r[32];
+      tmem_ld32(tbase + c * 32, r);
+      tmem_wait_ld();
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+      if (be) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (col0 + i < Nout) v[i] += __bfloat162float(be[col0 + i]);
+      }
+      emit(v, col0);
+    }
+  } else {
+    const int j0 = n_idx * (kEpiCols / 2);
+#pragma unroll 1
+    for (int c = 0; c < kEpiCols / 64; ++c) {
+      const int col0 = j0 + c * 32;  // activation column
+      if (col0 >= Nout) break;
+      uint32_t g[32], u[32];
+      if constexpr (MODE == kTcStacked) {
+        tmem_ld32(tbase + c * 32, g);             // gate columns
+        tmem_ld32(tbase + kEpiCols / 2 + c * 32, u);    // up columns
+      } else {
+        tmem_ld32(tbase + c * 64, g);             // (gate, up) pairs
+        tmem_ld32(tbase + c * 64 + 32, u);
+      }
+      tmem_wait_ld();
+      float gv[32], uv[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        if constexpr (MODE == kTcStacked) {
+          gv[i] = __uint_as_float(g[i]);
+          uv[i] = __uint_as_float(u[i]);
+        } else {  // pair i lives in columns 2i, 2i+1 of the 64 loaded
+          gv[i] = __uint_as_float(2 * i < 32 ? g[2 * i] : u[2 * i - 32]);
+          uv[i] = __uint_as_float(2 * i + 1 < 32 ? g[2 * i + 1] : u[2 * i + 1 - 32]);
+        }
+      }
+      if (be) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (col0 + i < Nout) {
+            const int rg = MODE == kTcStacked ? col0 + i : 2 * (col0 + i);
+            const int ru = MODE == kTcStacked ? Nout + col0 + i : rg + 1;
+            gv[i] += __bfloat162float(be[rg]);
+            uv[i] += __bfloat162float(be[ru]);
+          }
+        }
+      }
+      float v[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = gated<ACT>(gv[i], uv[i], limit, alpha, beta);
+      emit(v, col0);
+    }
+  }
+}
+
+}  // namespace tc
+}  // namespace moe

@@ -10,15 +10,21 @@
 //   tile = 128 rows x 256 accumulator columns; k-block = 64 (one 128-byte
 //   swizzle atom of bf16); 4-stage shared-memory ring of A (16 KB) + B (32 KB).
 //   Gated modes use the 256 accumulator columns as 128 gate + 128 up columns
-//   (stacked: two TMA boxes, gate rows j0.. and up rows F+j0..; interleaved:
+//   (stacked: one 4-D box of gate rows j0.. then up rows F+j0..; interleaved:
 //   256 consecutive rows 2*j0..), giving 128 activation columns per tile.
 // Roles (192 threads, one CTA per SM)
 //   warp 0 lane 0 : TMA producer
 //   warp 1        : TMEM allocator; lane 0 issues tcgen05.mma (M128 N256 K16)
 //   warps 2..5    : epilogue; warp w reads TMEM lanes 32*(w%4).., one row per
-//                   thread, applies bias + activation and stores bf16
+//                   thread, applies bias + activation, rounds to bf16 and
+//                   writes 32x32 boxes through swizzled shared memory and TMA
+//                   stores (gemm_epilogue.cuh)
 //   Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
 //   tile overlap the main loop of the next.
+// What bounds it: the TMA load stream.  Timed apart, the MMAs alone run at
+// close to the tensor peak and the loads alone take ~80% of the whole kernel:
+// each SM takes in about 45-50 bytes per cycle of TMA tiles, well below what
+// DRAM and L2 deliver in aggregate (their counters stay near half of peak).
 // Every mbarrier wait is bounded: a wait that runs out sets MOE's timeout bit
 // in the status word, raises a block-wide abort flag, and the block drains its
 // in-flight copies and MMAs (again bounded) before freeing TMEM and returning.
@@ -30,6 +36,7 @@
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
+#include "gemm_epilogue.cuh"
 #include "tmap.h"
 
 namespace moe {
@@ -44,8 +51,6 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
 
-enum TcMode { kTcPlain = 0, kTcStacked = 1, kTcInterleaved = 2 };
-
 struct TcShared {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
@@ -57,40 +62,11 @@ struct TcShared {
   int prefix[kMaxExperts + 1];
   int scan_tmp[33];
 };
-// Output staging: each epilogue warp owns two 2 KB buffers (32 rows x 32 bf16
-// columns, 64-byte swizzle) that it fills from registers and hands to a TMA
-// store, so the output leaves the SM as whole boxes instead of 32 scattered
-// row segments per store instruction (those flood the L1/shared-memory data
-// path that tcgen05.mma reads its operands through).
-constexpr int OUT_BOX = 32;                        // rows and columns of one staged box
-constexpr int OUT_BUF_BYTES = OUT_BOX * OUT_BOX * 2;  // 2 KB
-constexpr int OUT_BYTES = 4 * 2 * OUT_BUF_BYTES;      // 4 warps x 2 buffers
 constexpr size_t kSmemBytes =
     (size_t)STAGES * STAGE_BYTES + OUT_BYTES + sizeof(TcShared) + 1024;
 
 
 constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
-
-// Epilogue activation math.  The exponential and the quotient use the fast
-// hardware approximations (relative error about 1e-6 over the arguments an
-// activation sees), far below the bf16 rounding of the stored result; every
-// branch on the mode and the activation is resolved at compile time so the 32
-// columns of a chunk are independent instruction streams.
-__device__ __forceinline__ float fast_sigmoid(float x) {
-  return __fdividef(1.0f, 1.0f + __expf(-x));
-}
-template <int ACT>
-__device__ __forceinline__ float gated(float g, float u, float limit, float alpha, float beta) {
-  if constexpr (ACT == MOE_ACT_SILU_AND_MUL) {
-    return g * fast_sigmoid(g) * u;
-  } else {
-    if (limit > 0.0f) {
-      g = fminf(g, limit);
-      u = fmaxf(fminf(u, limit), -limit);
-    }
-    return g * fast_sigmoid(alpha * g) * (u + beta);
-  }
-}
 
 // The four K16 MMAs of one 64-wide k-block and the commit that frees its stage,
 // in one block: descriptors advance by 32 bytes (2 in 16-byte units) per K16.
@@ -244,105 +220,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles);
       if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
       tc_fence_after();
-      const int row = st.m0 + quad * 32 + lane;
-      const bool row_ok = row < st.m_end;
-      const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-      const __nv_bfloat16* be = bias ? bias + (size_t)st.e * N1 : nullptr;
-      __nv_bfloat16* orow = out + (size_t)row * Nout;
-      const int wrow0 = st.m0 + quad * 32;
-      // Whole-box TMA stores only where all 32 rows of this warp belong to the
-      // tile's expert segment; a ragged tail stores row by row instead so it
-      // never writes rows of the next segment.
-      const bool boxed = tma_out && st.m_end - wrow0 >= OUT_BOX;
-      auto emit = [&](const float (&v)[32], int col0) {
-        if (boxed) {
-          uint8_t* buf = obufs + obuf * OUT_BUF_BYTES;
-          if (lane == 0) bulk_wait_read<1>();  // the store from this buffer two boxes ago
-          __syncwarp();
-          // row `lane`, 16-byte chunk q lands at chunk q ^ ((lane >> 1) & 3)
-          // (the 64-byte swizzle the output map describes): conflict-free
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 u;
-            u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-            u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-            u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-            u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-            *reinterpret_cast<uint4*>(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = u;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tm_out, buf, col0, wrow0);
-            bulk_commit();
-          }
-          obuf ^= 1;
-        } else if (row_ok) {
-          store_row32(orow + col0, v, Nout - col0);
-        }
-      };
-      if constexpr (MODE == kTcPlain) {
-        const int n0 = st.n_idx * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          const int col0 = n0 + c * 32;
-          if (col0 >= Nout) break;  // warp-uniform
-          uint32_t r[32];
-          tmem_ld32(tbase + c * 32, r);
-          tmem_wait_ld();
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          if (be) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (col0 + i < Nout) v[i] += __bfloat162float(be[col0 + i]);
-          }
-          emit(v, col0);
-        }
-      } else {
-        const int j0 = st.n_idx * (BN / 2);
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          const int col0 = j0 + c * 32;  // activation column
-          if (col0 >= Nout) break;
-          uint32_t g[32], u[32];
-          if constexpr (MODE == kTcStacked) {
-            tmem_ld32(tbase + c * 32, g);             // gate columns
-            tmem_ld32(tbase + BN / 2 + c * 32, u);    // up columns
-          } else {
-            tmem_ld32(tbase + c * 64, g);             // (gate, up) pairs
-            tmem_ld32(tbase + c * 64 + 32, u);
-          }
-          tmem_wait_ld();
-          float gv[32], uv[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if constexpr (MODE == kTcStacked) {
-              gv[i] = __uint_as_float(g[i]);
-              uv[i] = __uint_as_float(u[i]);
-            } else {  // pair i lives in columns 2i, 2i+1 of the 64 loaded
-              gv[i] = __uint_as_float(2 * i < 32 ? g[2 * i] : u[2 * i - 32]);
-              uv[i] = __uint_as_float(2 * i + 1 < 32 ? g[2 * i + 1] : u[2 * i + 1 - 32]);
-            }
-          }
-          if (be) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (col0 + i < Nout) {
-                const int rg = MODE == kTcStacked ? col0 + i : 2 * (col0 + i);
-                const int ru = MODE == kTcStacked ? Nout + col0 + i : rg + 1;
-                gv[i] += __bfloat162float(be[rg]);
-                uv[i] += __bfloat162float(be[ru]);
-              }
-            }
-          }
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = gated<ACT>(gv[i], uv[i], limit, alpha, beta);
-          emit(v, col0);
-        }
-      }
+      drain_acc<MODE, ACT>(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN),
+                           st.m0 + quad * 32, st.m_end, st.n_idx, st.e, bias, N1, Nout, limit,
+                           alpha, beta, &tm_out, tma_out, out, obufs, obuf, lane);
       tc_fence_before();
       mbar_arrive(&sh->tempty[acc]);
       if (++acc == 2) { acc = 0; aphase ^= 1u; }
@@ -367,9 +247,11 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s) {
   if (M == 0 || N == 0) return cudaSuccess;
-  // The two-SM (cta_group::2) kernel with MOE_TC_KERNEL=2sm.  It is correct but,
-  // on ragged expert segments, its 256-row pair tiles pad more rows than the
-  // 128-row tiles here; measured slower on every workload, so not the default.
+  // The two-SM (cta_group::2) kernel with MOE_TC_KERNEL=2sm.  Its SMs load a
+  // third fewer bytes per MMA, which wins on long uniform segments, but its
+  // 256-row pair tiles pad ragged expert segments (a tail of a few rows costs
+  // a whole pair tile), and on the routed workloads measured it is level or
+  // slower, so it is not the default.
   static const bool two_sm = [] {
     const char* v = getenv("MOE_TC_KERNEL");
     return v && v[0] == '2';
@@ -406,10 +288,10 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
   }
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
-    for (auto fn : {gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY>,
-                    gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>,
-                    gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU>,
-                    gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU>})
+    for (const void* fn : {(const void*)gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY>,
+                           (const void*)gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>,
+                           (const void*)gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU>,
+                           (const void*)gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU>})
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   });
   const int n_tiles = mode == kTcPlain ? (N + BN - 1) / BN : (N + BN / 2 - 1) / (BN / 2);
@@ -427,13 +309,14 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     tma_out = tmap::encode_bf16(&mo, out, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
   }
   if (!tma_out) mo = ma;  // unused
-  auto* kern = mode == kTcPlain     ? gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY>
+  const auto* bias_p = static_cast<const __nv_bfloat16*>(bias);
+  auto* out_p = static_cast<__nv_bfloat16*>(out);
+  auto* kern = mode == kTcPlain       ? gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY>
                : mode == kTcInterleaved ? gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU>
                : kind == MOE_ACT_SWIGLU ? gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU>
                                         : gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>;
-  kern<<<grid, NUM_THREADS, kSmemBytes, s>>>(ma, mb, static_cast<const __nv_bfloat16*>(bias),
-                                             seg_end, M, N, N1, K, E, limit, alpha, beta, mo,
-                                             tma_out, static_cast<__nv_bfloat16*>(out), status);
+  kern<<<grid, NUM_THREADS, kSmemBytes, s>>>(ma, mb, bias_p, seg_end, M, N, N1, K, E, limit,
+                                             alpha, beta, mo, tma_out, out_p, status);
   count_launch();
   return cudaGetLastError();
 }

@@ -1,13 +1,16 @@
-// Two-SM variant of the tcgen05 grouped GEMM (same contract and epilogue as
-// gemm_tc.cu; TileOPs "MoE Operators", MoEGroupedGemmFwdOp).
+// Two-SM variant of the tcgen05 grouped GEMM (same contract as gemm_tc.cu and
+// the same epilogue, gemm_epilogue.cuh; TileOPs "MoE Operators",
+// MoEGroupedGemmFwdOp).
 //
 // A cluster of two CTAs on a pair of SMs computes a 256-row x 256-column tile
 // with tcgen05.mma.cta_group::2 (M256 N256 K16): each CTA loads its own 128
 // rows of A and HALF of the 256 B rows (stacked gated layouts: the leader
 // loads the 128 gate rows, the peer the 128 up rows; otherwise the lower and
 // upper 128 rows), so an SM ingests 32 KB per 64-wide k-block instead of the
-// 48 KB of the one-SM 128x256 tile -- a third fewer bytes per MMA, which is
-// what limits the one-SM kernel (its per-SM load rate, not DRAM or L2).
+// 48 KB of the one-SM 128x256 tile -- a third fewer bytes per MMA, and the
+// one-SM kernel is bound by its per-SM load stream.  The price is the 256-row
+// pair tile: on ragged expert segments the padded rows cost MMA time and
+// loads, which on routed workloads cancels the gain.
 //
 // Roles (192 threads in each CTA of the pair):
 //   warp 0 lane 0 (both CTAs): TMA producer for its own A rows and B half; the
@@ -27,6 +30,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "gemm_epilogue.cuh"
 #include "tc_ptx.cuh"
 #include "tmap.h"
 
@@ -47,8 +51,6 @@ constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t kIdesc2 = idesc_bf16(BMP, BN);
 
-enum TcMode { kTcPlain = 0, kTcStacked = 1, kTcInterleaved = 2 };
-
 struct Tc2Shared {
   uint64_t full[STAGES];   // leader: both CTAs' copies of a stage complete here
   uint64_t empty[STAGES];  // both: the leader's MMA commit frees the stage
@@ -60,11 +62,12 @@ struct Tc2Shared {
   int prefix[kMaxExperts + 1];
   int scan_tmp[33];
 };
-// 16 KB of slack after the ring keeps every operand read of a stage inside this
-// CTA's shared memory, whatever the MMA reads past its half-tile
-constexpr int GUARD_BYTES = 16 * 1024;
+// The 16 KB output staging area follows the ring directly, so it also keeps
+// every operand read of a stage inside this CTA's shared memory, whatever the
+// MMA reads past its half-tile (the MMA never writes shared memory).
+static_assert(OUT_BYTES >= 16 * 1024, "staging doubles as the guard after the ring");
 constexpr size_t kSmemBytes =
-    (size_t)STAGES * STAGE_BYTES + GUARD_BYTES + sizeof(Tc2Shared) + 1024;
+    (size_t)STAGES * STAGE_BYTES + OUT_BYTES + sizeof(Tc2Shared) + 1024;
 
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -154,16 +157,19 @@ __device__ __forceinline__ void umma2_commit_self(uint64_t* bar) {
       : "memory");
 }
 
+template <int MODE, int ACT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
                     const __nv_bfloat16* __restrict__ bias, const int32_t* __restrict__ seg_end,
-                    int M, int Nout, int N1, int K, int E, int mode, int act_kind, float limit,
-                    float alpha, float beta, __nv_bfloat16* __restrict__ out, int* status) {
+                    int M, int Nout, int N1, int K, int E, float limit, float alpha, float beta,
+                    const __grid_constant__ CUtensorMap tm_out, int tma_out,
+                    __nv_bfloat16* __restrict__ out, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  Tc2Shared* sh = reinterpret_cast<Tc2Shared*>(smem + (size_t)STAGES * STAGE_BYTES + GUARD_BYTES);
+  uint8_t* out_stage = smem + (size_t)STAGES * STAGE_BYTES;  // 1024-byte aligned
+  Tc2Shared* sh = reinterpret_cast<Tc2Shared*>(out_stage + OUT_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
@@ -193,7 +199,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
-  const int n_tiles = mode == kTcPlain ? (Nout + BN - 1) / BN : (Nout + BN / 2 - 1) / (BN / 2);
+  const int n_tiles = MODE == kTcPlain ? (Nout + BN - 1) / BN : (Nout + BN / 2 - 1) / (BN / 2);
   const int total = build_tile_prefix(seg_end, E, M, BMP, n_tiles, sh->prefix, sh->scan_tmp);
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t bar = map_to_rank(su32(&sh->full[stage]), 0);
           const int k0 = kb * BK;
           tma2_2d(a_dst, &tm_a, bar, k0, st.m0 + BMC * (int)rank);
-          if (mode == kTcStacked) {
+          if constexpr (MODE == kTcStacked) {
             tma2_4d(b_dst, &tm_b, bar, k0, st.n_idx * (BN / 2), (int)rank, st.e);
           } else {
             tma2_3d(b_dst, &tm_b, bar, k0, st.n_idx * BN + (BN / 2) * (int)rank, st.e);
@@ -272,78 +278,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t aphase = 0;
     const uint32_t tempty_remote[2] = {map_to_rank(su32(&sh->tempty[0]), 0),
                                        map_to_rank(su32(&sh->tempty[1]), 0)};
+    uint8_t* obufs = out_stage + quad * 2 * OUT_BUF_BYTES;
+    int obuf = 0;
     for (int tile = pair; tile < total; tile += npairs) {
       const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
       if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
       tc_fence_after();
-      const int row = st.m0 + BMC * (int)rank + quad * 32 + lane;
-      const bool row_ok = row < st.m_end;
-      const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
-      const __nv_bfloat16* be = bias ? bias + (size_t)st.e * N1 : nullptr;
-      __nv_bfloat16* orow = out + (size_t)row * Nout;
-      if (mode == kTcPlain) {
-        const int n0 = st.n_idx * BN;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          const int col0 = n0 + c * 32;
-          if (col0 >= Nout) break;  // warp-uniform
-          uint32_t r[32];
-          tmem_ld32(tbase + c * 32, r);
-          tmem_wait_ld();
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float b = (be && col0 + i < Nout) ? __bfloat162float(be[col0 + i]) : 0.f;
-            v[i] = __uint_as_float(r[i]) + b;
-          }
-          if (row_ok) store_row32(orow + col0, v, Nout - col0);
-        }
-      } else {
-        const int j0 = st.n_idx * (BN / 2);
-#pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
-          const int col0 = j0 + c * 32;
-          if (col0 >= Nout) break;
-          uint32_t g[32], u[32];
-          if (mode == kTcStacked) {
-            tmem_ld32(tbase + c * 32, g);           // gate columns (leader's B half)
-            tmem_ld32(tbase + BN / 2 + c * 32, u);  // up columns (peer's B half)
-          } else {
-            tmem_ld32(tbase + c * 64, g);           // (gate, up) pairs
-            tmem_ld32(tbase + c * 64 + 32, u);
-          }
-          tmem_wait_ld();
-          float v[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            float gv, uv;
-            int rg, ru;
-            if (mode == kTcStacked) {
-              gv = __uint_as_float(g[i]);
-              uv = __uint_as_float(u[i]);
-              rg = col0 + i;
-              ru = Nout + col0 + i;
-            } else {
-              const int p = 2 * i;
-              gv = __uint_as_float(p < 32 ? g[p] : u[p - 32]);
-              uv = __uint_as_float(p + 1 < 32 ? g[p + 1] : u[p + 1 - 32]);
-              rg = 2 * (col0 + i);
-              ru = rg + 1;
-            }
-            if (be && col0 + i < Nout) {
-              gv += __bfloat162float(be[rg]);
-              uv += __bfloat162float(be[ru]);
-            }
-            v[i] = act_kind == MOE_ACT_SILU_AND_MUL ? silu_mul(gv, uv)
-                                                    : swiglu_f(gv, uv, limit, alpha, beta);
-          }
-          if (row_ok) store_row32(orow + col0, v, Nout - col0);
-        }
-      }
+      drain_acc<MODE, ACT>(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN),
+                           st.m0 + BMC * (int)rank + quad * 32, st.m_end, st.n_idx, st.e, bias,
+                           N1, Nout, limit, alpha, beta, &tm_out, tma_out, out, obufs, obuf,
+                           lane);
       tc_fence_before();
       mbar_arrive_remote(tempty_remote[acc]);
       if (++acc == 2) { acc = 0; aphase ^= 1u; }
     }
+    if (lane == 0) bulk_wait_all();  // every staged box written before the pair exits
   }
 
   tc_fence_before();
@@ -393,9 +342,23 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
   }
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
-    cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kSmemBytes);
+    for (const void* fn : {(const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY>,
+                           (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>,
+                           (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU>,
+                           (const void*)gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU>})
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   });
+  // output map for the staged TMA stores (rows stored directly when the
+  // output's base or pitch is not 16-byte aligned)
+  CUtensorMap mo;
+  int tma_out = 0;
+  if (N % 8 == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t str[1] = {(cuuint64_t)N * 2};
+    cuuint32_t box[2] = {OUT_BOX, OUT_BOX};
+    tma_out = tmap::encode_bf16(&mo, out, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
+  }
+  if (!tma_out) mo = ma;  // unused
   const int n_tiles = mode == kTcPlain ? (N + BN - 1) / BN : (N + BN / 2 - 1) / (BN / 2);
   const long long max_tiles = (long long)((M + BMP - 1) / BMP + E) * n_tiles;
   const int pairs = (int)std::max<long long>(1, std::min<long long>(max_tiles, num_sms() / 2));
@@ -412,9 +375,12 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc2_kernel, ma, mb,
-                                     static_cast<const __nv_bfloat16*>(bias), seg_end, M, N, N1,
-                                     K, E, mode, kind, limit, alpha, beta,
+  auto* kern = mode == kTcPlain       ? gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY>
+               : mode == kTcInterleaved ? gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU>
+               : kind == MOE_ACT_SWIGLU ? gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU>
+                                        : gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<const __nv_bfloat16*>(bias),
+                                     seg_end, M, N, N1, K, E, limit, alpha, beta, mo, tma_out,
                                      static_cast<__nv_bfloat16*>(out), status);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();

@@ -1,6 +1,7 @@
-"""The alternative tcgen05 grouped-GEMM kernel -- two-SM cta_group::2 tiles,
-selected with MOE_TC_KERNEL=2sm -- runs the whole grouped-GEMM parity file in a
-fresh process (the switch is read once per process)."""
+"""The alternative tcgen05 grouped-GEMM kernel -- two-SM cta_group::2 tiles with
+the shared staged-store epilogue, selected with MOE_TC_KERNEL=2sm -- runs the
+whole grouped-GEMM parity file in a fresh process (the switch is read once per
+process)."""
 import os
 import subprocess
 import sys
