@@ -4,9 +4,10 @@ One step = one full forward (route with the MoERouter outputs -> permute ->
 gate_up GEMM + fused activation -> down GEMM -> combine) of the Qwen3-style
 workload (T=4096 tokens, H=2048, F=768, E=128 experts, top-8, softmax,
 renormalised, silu_and_mul; MoERouter slice [32, 64)) on synthetic seeded
-inputs already resident in HBM.  The L2 is flushed (a 512 MiB write) before
-every timed step and each step is bracketed by CUDA events on the launching
-stream.  Prints one JSON line.
+inputs already resident in HBM.  The L2 is flushed before every timed step (a
+512 MiB write, then a 512 MiB read so that the written lines are cleaned
+inside the flush rather than written back inside the timed step) and each step
+is bracketed by CUDA events on the launching stream.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -148,7 +149,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
 
 
-def profile_traffic(kernel: str, src: str):
+# the files the tcgen05 GEMM kernel is compiled from (the ncu summary under
+# profiles/ records their hash, so a stale summary is never quoted)
+GEMM_SOURCES = [os.path.join(ROOT, "mixture_experts_ffn_gb300", "csrc", f)
+                for f in ("gemm_tc.cu", "gemm_epilogue.cuh", "tc_ptx.cuh", "common.cuh")]
+
+
+def sources_sha256(paths):
+    """SHA-256 over the concatenated bytes of a kernel's source files, in order."""
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profile_traffic(kernel: str, srcs):
     """DRAM bytes per launch from the committed ncu summary of ``kernel``, when
     the summary was taken on the current source of the kernel."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{WORKLOAD}.md")
@@ -159,8 +175,7 @@ def profile_traffic(kernel: str, src: str):
     h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
     if not m or not h:
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return float(m.group(1)) if sha == h.group(1) else None
+    return float(m.group(1)) if sources_sha256(srcs) == h.group(1) else None
 
 
 # --------------------------------------------------------------------- reference
@@ -275,7 +290,19 @@ def run_ours(args, rank, world, local):
         if cfg.local_count else None
     wsc = torch.empty((T,), dtype=torch.float32, device=dev) if cfg.local_count else None
     ws = moe._ws(moe.moe_workspace_size(T, H, F, E, K, mdt), dev)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush_w = torch.zeros(512 << 20, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(128 << 20, dtype=torch.float32, device=dev)
+
+    class L2Flush:
+        """Write 512 MiB (evicts everything), then read another 512 MiB: the read
+        forces the write-back of the dirty lines the write left, so the L2
+        holds only clean lines of an unrelated buffer when a step starts."""
+
+        def zero_(self):
+            flush_w.zero_()
+            torch.sum(flush_r)
+
+    flush = L2Flush()
     stream = torch.cuda.current_stream()
 
     def forward():
@@ -384,13 +411,11 @@ def run_ours(args, rank, world, local):
         if indexed:
             dom = "indexed_mlp"
             kname = "indexed_gate_up + indexed_down"
-            src = os.path.join(ROOT, "mixture_experts_ffn_gb300", "csrc", "decode.cu")
             traffic = None
         else:
             dom = max(("gemm_act", "gemm_down"), key=lambda k: breakdown[k]["us"])
             kname = f"gemm_tc_kernel ({dom})"
-            src = os.path.join(ROOT, "mixture_experts_ffn_gb300", "csrc", "gemm_tc.cu")
-            traffic = profile_traffic("gemm_tc_kernel", src) if (
+            traffic = profile_traffic("gemm_tc_kernel", GEMM_SOURCES) if (
                 dom == "gemm_act" and args.workload == WORKLOAD) else None
         fl, by = costs[dom]
         b = breakdown[dom]
@@ -443,7 +468,8 @@ def run_ours(args, rank, world, local):
                        "act": ["silu_and_mul", "swiglu", "identity"][cfg.act],
                        "path": "indexed" if indexed else "staged",
                        "moerouter_slice": [cfg.local_start, cfg.local_count],
-                       "l2": "flushed before every timed step (512 MiB write)",
+                       "l2": "flushed before every timed step (512 MiB write, then 512 MiB "
+                             "read so no dirty lines are written back inside the step)",
                        "soak_steps": soak,
                        "parallelism": f"replicas x{world}"},
             "gpu_launches": launches,
