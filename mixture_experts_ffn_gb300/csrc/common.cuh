@@ -9,6 +9,11 @@
 
 namespace moe {
 
+// Wait for the grids this one depends on (the previous kernel of the stream
+// under programmatic stream serialization, see launch_pdl) to complete and
+// their memory to be visible; a no-op when launched without it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------- element I/O
 template <typename T> struct Elem;
 template <> struct Elem<float> {

@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(kWarps * 32) indexed_gate_up(
     const int32_t* __restrict__ seg_end, const int32_t* __restrict__ row_to_route,
     const int* __restrict__ active, const int* __restrict__ num_active, int T, int H, int F,
     int K, __nv_bfloat16* __restrict__ act) {
+  pdl_wait();  // everything below reads results of earlier launches
   const int D = *num_active;
   const int items_per_e = F / kColsPerItem;
   const int n_items = D * items_per_e;
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(kWarps * 32) indexed_down(
     const __nv_bfloat16* __restrict__ w2, const __nv_bfloat16* __restrict__ act,
     const int32_t* __restrict__ seg_end, const int* __restrict__ active,
     const int* __restrict__ num_active, int H, int F, __nv_bfloat16* __restrict__ y) {
+  pdl_wait();  // everything below reads results of earlier launches
   const int D = *num_active;
   const int items_per_e = H / kColsPerItem;
   const int n_items = D * items_per_e;
@@ -197,11 +199,10 @@ cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, c
                                    route_to_row, ws, s);
   if (err != cudaSuccess) return err;
   const int grid = num_sms() * 4;
-  indexed_gate_up<<<grid, kWarps * 32, 0, s>>>(static_cast<const __nv_bfloat16*>(hidden),
-                                               static_cast<const __nv_bfloat16*>(w1), seg_end, r2r,
-                                               active, num_active, T, H, F, K, act);
-  indexed_down<<<grid, kWarps * 32, 0, s>>>(static_cast<const __nv_bfloat16*>(w2), act, seg_end,
-                                            active, num_active, H, F, y);
+  launch_pdl(indexed_gate_up, grid, kWarps * 32, 0, s, static_cast<const __nv_bfloat16*>(hidden),
+      static_cast<const __nv_bfloat16*>(w1), seg_end, r2r, active, num_active, T, H, F, K, act);
+  launch_pdl(indexed_down, grid, kWarps * 32, 0, s, static_cast<const __nv_bfloat16*>(w2), act,
+      seg_end, active, num_active, H, F, y);
   count_launch(2);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;

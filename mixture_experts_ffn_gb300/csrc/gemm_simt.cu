@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
   __shared__ float Bu[MODE == kPlain ? 1 : SBK][SBN + 4];
   __shared__ int prefix[kMaxExperts + 1];
   __shared__ int scan_tmp[33];
+  pdl_wait();  // everything below reads results of earlier launches
 
   const int n_tiles = (Nout + SBN - 1) / SBN;
   const int total = build_tile_prefix(seg_end, E, M, SBM, n_tiles, prefix, scan_tmp);
@@ -132,14 +133,14 @@ cudaError_t launch_t(const void* a, const void* w, const void* bias, const int32
   const T* B = static_cast<const T*>(bias);
   T* O = static_cast<T*>(out);
   if (mode == kPlain)
-    gemm_simt_kernel<T, kPlain><<<(unsigned)grid, 256, 0, s>>>(A, W, B, seg_end, M, Nout, N1, K, E,
-                                                               kind, limit, alpha, beta, O);
+    launch_pdl(gemm_simt_kernel<T, kPlain>, (unsigned)grid, 256, 0, s, A, W, B, seg_end, M, Nout,
+        N1, K, E, kind, limit, alpha, beta, O);
   else if (mode == kStacked)
-    gemm_simt_kernel<T, kStacked><<<(unsigned)grid, 256, 0, s>>>(A, W, B, seg_end, M, Nout, N1, K,
-                                                                 E, kind, limit, alpha, beta, O);
+    launch_pdl(gemm_simt_kernel<T, kStacked>, (unsigned)grid, 256, 0, s, A, W, B, seg_end, M, Nout,
+        N1, K, E, kind, limit, alpha, beta, O);
   else
-    gemm_simt_kernel<T, kInterleaved><<<(unsigned)grid, 256, 0, s>>>(
-        A, W, B, seg_end, M, Nout, N1, K, E, kind, limit, alpha, beta, O);
+    launch_pdl(gemm_simt_kernel<T, kInterleaved>, (unsigned)grid, 256, 0, s, A, W, B, seg_end, M,
+        Nout, N1, K, E, kind, limit, alpha, beta, O);
   count_launch();
   return cudaGetLastError();
 }

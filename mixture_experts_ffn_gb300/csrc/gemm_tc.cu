@@ -134,6 +134,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   const int n_tiles = MODE == kTcPlain ? (Nout + BN - 1) / BN : (Nout + BN / 2 - 1) / (BN / 2);
+  // barrier init, tensor-map prefetch and TMEM allocation above overlap the
+  // previous launch; seg_end and the operands are read only after this
+  pdl_wait();
   const int total = build_tile_prefix(seg_end, E, M, BM, n_tiles, sh->prefix, sh->scan_tmp);
   tc_fence_before();
   __syncthreads();
@@ -315,8 +318,8 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                : mode == kTcInterleaved ? gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU>
                : kind == MOE_ACT_SWIGLU ? gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU>
                                         : gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>;
-  kern<<<grid, NUM_THREADS, kSmemBytes, s>>>(ma, mb, bias_p, seg_end, M, N, N1, K, E, limit,
-                                             alpha, beta, mo, tma_out, out_p, status);
+  launch_pdl(kern, grid, NUM_THREADS, kSmemBytes, s, ma, mb, bias_p, seg_end, M, N, N1, K, E,
+      limit, alpha, beta, mo, tma_out, out_p, status);
   count_launch();
   return cudaGetLastError();
 }

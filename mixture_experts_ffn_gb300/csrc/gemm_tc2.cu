@@ -200,6 +200,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
   const int n_tiles = MODE == kTcPlain ? (Nout + BN - 1) / BN : (Nout + BN / 2 - 1) / (BN / 2);
+  // barrier init, tensor-map prefetch and TMEM allocation above overlap the
+  // previous launch; seg_end and the operands are read only after this
+  pdl_wait();
   const int total = build_tile_prefix(seg_end, E, M, BMP, n_tiles, sh->prefix, sh->scan_tmp);
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
@@ -368,13 +371,15 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
   cfg.blockDim = dim3(NUM_THREADS);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   auto* kern = mode == kTcPlain       ? gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY>
                : mode == kTcInterleaved ? gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU>
                : kind == MOE_ACT_SWIGLU ? gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU>

@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -54,6 +56,28 @@ struct ForwardWs {
 
 void count_launch(int n = 1);
 int num_sms();
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel of the stream is still finishing, runs whatever
+// does not read earlier results (shared-memory set-up, barrier init, TMEM
+// allocation), and executes griddepcontrol.wait (pdl_wait) before its first
+// access to global memory written by earlier work on the stream.  Every kernel
+// of the library does so, so launches stay ordered transitively.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- launchers (return cudaGetLastError() of their launches) ----
 cudaError_t launch_route(const float* logits, const float* bias, const int32_t* ids_in, int T,

@@ -20,6 +20,7 @@ namespace {
 
 __global__ void __launch_bounds__(256) perm_count(const int32_t* __restrict__ ids, int M, int E,
                                                   int* __restrict__ counts, int* status) {
+  pdl_wait();  // everything below reads results of earlier launches
   extern __shared__ int hist[];
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -67,6 +68,7 @@ __global__ void __launch_bounds__(1024) perm_scan(int* __restrict__ counts, int 
                                                   int32_t* __restrict__ seg_end,
                                                   int* __restrict__ active,
                                                   int* __restrict__ num_active) {
+  pdl_wait();  // everything below reads results of earlier launches
   __shared__ int wt[33];
   const int nthr = blockDim.x, tid = threadIdx.x;
   const int per = (E + nthr - 1) / nthr;
@@ -109,6 +111,7 @@ __global__ void __launch_bounds__(32) perm_scatter(const int32_t* __restrict__ i
                                                    const int* __restrict__ offsets,
                                                    int32_t* __restrict__ row_to_route,
                                                    int32_t* __restrict__ route_to_row) {
+  pdl_wait();  // everything below reads results of earlier launches
   extern __shared__ int cur[];
   const int lane = threadIdx.x;
   const int* off = offsets + (size_t)blockIdx.x * E;
@@ -156,6 +159,7 @@ __global__ void __launch_bounds__(1024) perm_scatter_cta(const int32_t* __restri
                                                          int E, const int* __restrict__ offsets,
                                                          int32_t* __restrict__ row_to_route,
                                                          int32_t* __restrict__ route_to_row) {
+  pdl_wait();  // everything below reads results of earlier launches
   extern __shared__ int wcnt[];  // [W][E]: counts, then exclusive row bases
   const int W = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -214,6 +218,7 @@ __global__ void __launch_bounds__(256) perm_gather(const char* __restrict__ hidd
                                                    const int32_t* __restrict__ seg_end, int E,
                                                    int K, int T, size_t row_bytes,
                                                    char* __restrict__ out, int* status) {
+  pdl_wait();  // everything below reads results of earlier launches
   const int warps = blockDim.x >> 5;
   const int row = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -320,6 +325,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
                                                       const int32_t* __restrict__ r2r, int Tn,
                                                       int K, int H, int M, float scale,
                                                       T* __restrict__ out) {
+  pdl_wait();  // everything below reads results of earlier launches
   const int nvec = H / VEC;
   const long long items = (long long)Tn * nvec;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -348,8 +354,8 @@ cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int 
   }
   const int C = (M + kPermuteChunk - 1) / kPermuteChunk;
   const size_t hist_smem = (size_t)E * 4;
-  perm_count<<<C, 256, hist_smem, s>>>(ids, M, E, counts, status);
-  perm_scan<<<1, 1024, 0, s>>>(counts, C, E, seg_end, active, num_active);
+  launch_pdl(perm_count, C, 256, hist_smem, s, ids, M, E, counts, status);
+  launch_pdl(perm_scan, 1, 1024, 0, s, counts, C, E, seg_end, active, num_active);
   // one CTA of W warps per chunk while W x E counts fit in 96 KB of shared
   // memory; otherwise one warp per chunk
   int W = 32;
@@ -362,9 +368,9 @@ cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int 
                            96 * 1024);
       attr_set = true;
     }
-    perm_scatter_cta<<<C, W * 32, sm, s>>>(ids, M, E, counts, row_to_route, route_to_row);
+    launch_pdl(perm_scatter_cta, C, W * 32, sm, s, ids, M, E, counts, row_to_route, route_to_row);
   } else {
-    perm_scatter<<<C, 32, hist_smem, s>>>(ids, M, E, counts, row_to_route, route_to_row);
+    launch_pdl(perm_scatter, C, 32, hist_smem, s, ids, M, E, counts, row_to_route, route_to_row);
   }
   count_launch(3);
   if (expert_input) {
@@ -374,13 +380,11 @@ cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int 
     const bool vec = (row_bytes % 16 == 0) && ((uintptr_t)hidden % 16 == 0) &&
                      ((uintptr_t)expert_input % 16 == 0);
     if (vec)
-      perm_gather<16><<<grid, 256, 0, s>>>(static_cast<const char*>(hidden), row_to_route,
-                                           seg_end, E, K, T, row_bytes,
-                                           static_cast<char*>(expert_input), status);
+      launch_pdl(perm_gather<16>, grid, 256, 0, s, static_cast<const char*>(hidden), row_to_route,
+          seg_end, E, K, T, row_bytes, static_cast<char*>(expert_input), status);
     else
-      perm_gather<2><<<grid, 256, 0, s>>>(static_cast<const char*>(hidden), row_to_route, seg_end,
-                                          E, K, T, row_bytes, static_cast<char*>(expert_input),
-                                          status);
+      launch_pdl(perm_gather<2>, grid, 256, 0, s, static_cast<const char*>(hidden), row_to_route,
+          seg_end, E, K, T, row_bytes, static_cast<char*>(expert_input), status);
     count_launch();
   }
   return cudaGetLastError();
@@ -399,20 +403,18 @@ cudaError_t launch_combine(const void* y, const float* w, const int32_t* r2r, in
   if (dt == MOE_BF16) {
     using B = __nv_bfloat16;
     if (aligned && H % 8 == 0)
-      combine_kernel<B, 8><<<grid_for(8), 256, 0, s>>>(static_cast<const B*>(y), w, r2r, T, K, H,
-                                                       M, scale, static_cast<B*>(out));
+      launch_pdl(combine_kernel<B, 8>, grid_for(8), 256, 0, s, static_cast<const B*>(y), w, r2r, T,
+          K, H, M, scale, static_cast<B*>(out));
     else
-      combine_kernel<B, 1><<<grid_for(1), 256, 0, s>>>(static_cast<const B*>(y), w, r2r, T, K, H,
-                                                       M, scale, static_cast<B*>(out));
+      launch_pdl(combine_kernel<B, 1>, grid_for(1), 256, 0, s, static_cast<const B*>(y), w, r2r, T,
+          K, H, M, scale, static_cast<B*>(out));
   } else {
     if (aligned && H % 4 == 0)
-      combine_kernel<float, 4><<<grid_for(4), 256, 0, s>>>(static_cast<const float*>(y), w, r2r,
-                                                           T, K, H, M, scale,
-                                                           static_cast<float*>(out));
+      launch_pdl(combine_kernel<float, 4>, grid_for(4), 256, 0, s, static_cast<const float*>(y), w,
+          r2r, T, K, H, M, scale, static_cast<float*>(out));
     else
-      combine_kernel<float, 1><<<grid_for(1), 256, 0, s>>>(static_cast<const float*>(y), w, r2r,
-                                                           T, K, H, M, scale,
-                                                           static_cast<float*>(out));
+      launch_pdl(combine_kernel<float, 1>, grid_for(1), 256, 0, s, static_cast<const float*>(y), w,
+          r2r, T, K, H, M, scale, static_cast<float*>(out));
   }
   count_launch();
   return cudaGetLastError();

@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
                                                     int32_t* __restrict__ id_out,
                                                     float* __restrict__ probs,
                                                     float* __restrict__ wscale) {
+  pdl_wait();  // everything below reads results of earlier launches
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -238,8 +239,8 @@ cudaError_t launch_npl(const float* logits, const float* bias, const int32_t* id
                        cudaStream_t s) {
   const int warps = 8;
   dim3 grid((T + warps - 1) / warps);
-  route_kernel<NPL><<<grid, warps * 32, 0, s>>>(logits, bias, ids_in, T, E, a, w, ids, probs,
-                                                wscale);
+  launch_pdl(route_kernel<NPL>, grid, warps * 32, 0, s, logits, bias, ids_in, T, E, a, w, ids,
+      probs, wscale);
   count_launch();
   return cudaGetLastError();
 }

@@ -14,6 +14,7 @@ __global__ void __launch_bounds__(256) swiglu_kernel(const T* __restrict__ gate,
                                                      const T* __restrict__ up, int64_t R, int I,
                                                      int fusion, float limit, float alpha,
                                                      float beta, T* __restrict__ out) {
+  pdl_wait();  // everything below reads results of earlier launches
   const int64_t n = R * (int64_t)I;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -46,14 +47,11 @@ cudaError_t launch_swiglu(const void* gate, const void* up, int64_t R, int I, mo
   if (blocks > cap) blocks = cap;
   if (dt == MOE_BF16) {
     using B = __nv_bfloat16;
-    swiglu_kernel<B><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const B*>(gate),
-                                                      static_cast<const B*>(up), R, I, fusion,
-                                                      limit, alpha, beta, static_cast<B*>(out));
+    launch_pdl(swiglu_kernel<B>, (unsigned)blocks, 256, 0, s, static_cast<const B*>(gate),
+        static_cast<const B*>(up), R, I, fusion, limit, alpha, beta, static_cast<B*>(out));
   } else {
-    swiglu_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(static_cast<const float*>(gate),
-                                                          static_cast<const float*>(up), R, I,
-                                                          fusion, limit, alpha, beta,
-                                                          static_cast<float*>(out));
+    launch_pdl(swiglu_kernel<float>, (unsigned)blocks, 256, 0, s, static_cast<const float*>(gate),
+        static_cast<const float*>(up), R, I, fusion, limit, alpha, beta, static_cast<float*>(out));
   }
   count_launch();
   return cudaGetLastError();
