@@ -243,7 +243,12 @@ def stage_cost(cfg, D):
     return {
         "route": (0.0, route),
         "permute": (0.0, M * 4 * 3 + E * 4 + T * H * b + M * H * b),
+        # the forward's own stages on the tensor-core path: the permute builds
+        # the index maps only and the gate_up GEMM reads the hidden rows
+        # through them (each hidden row counted once)
+        "permute_maps": (0.0, M * 4 * 3 + E * 4),
         "gemm_act": (4.0 * M * H * F, D * 2 * F * H * b + bias1 + M * H * b + M * F * b),
+        "gemm_act_gathered": (4.0 * M * H * F, D * 2 * F * H * b + bias1 + T * H * b + M * F * b),
         "gemm_down": (2.0 * M * F * H, D * H * F * b + bias2 + M * F * b + M * H * b),
         "combine": (0.0, M * H * b + M * 8 + T * H * b),
         "indexed_mlp": (6.0 * M * H * F, D * 3 * F * H * b + T * H * b + M * 8 + T * H * b),
@@ -281,6 +286,10 @@ def run_ours(args, rank, world, local):
                and cfg.bias_std is None and cfg.dtype == "bf16" and cfg.H % 128 == 0
                and cfg.F % 256 == 0)
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
+    # the forward reads the gate_up rows through the permutation on the
+    # tensor-core path (bf16, 16-byte rows, not the two-SM kernel)
+    gathered = (not indexed and cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
+                and not os.environ.get("MOE_TC_KERNEL", "").startswith("2"))
     tdt = synth.torch_dtype(cfg.dtype)
     mdt = moe.MOE_BF16 if cfg.dtype == "bf16" else moe.MOE_F32
     out = torch.empty((T, H), dtype=tdt, device=dev)
@@ -382,6 +391,18 @@ def run_ours(args, rank, world, local):
             stages["indexed_mlp"] = lambda: moe.moe_indexed_mlp(inp["hidden"], inp["w_gate_up"],
                                                                 inp["w_down"], tw, ti, out=out,
                                                                 ws=ws)
+        elif gathered:
+            stages.update({
+                "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"],
+                                                   with_gather=False),
+                "gemm_act": lambda: moe.moe_grouped_gemm_act_gathered(
+                    inp["hidden"], perm["row_to_route"], K, inp["w_gate_up"], perm["seg_end"], F,
+                    a, inp["b_gate_up"], out=act_out, ws=stage_ws),
+                "gemm_down": lambda: moe.moe_grouped_gemm_down(act_out, inp["w_down"],
+                                                               perm["seg_end"], inp["b_down"],
+                                                               out=y, ws=stage_ws),
+                "combine": lambda: moe.moe_combine(y, tw, perm["route_to_row"], out=out),
+            })
         else:
             stages.update({
                 "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"]),
@@ -398,7 +419,8 @@ def run_ours(args, rank, world, local):
         for name, fn in stages.items():
             st, nl = timed(fn, max(5, args.steps), 3)
             us = 1e3 * sum(st) / len(st)
-            fl, by = costs[name]
+            fl, by = costs[{"permute": "permute_maps", "gemm_act": "gemm_act_gathered"}
+                           .get(name, name) if gathered else name]
             t_tc = fl / (pk["bf16_tflops"] * 1e12)
             t_hbm = by / (pk["hbm_gbs"] * 1e9)
             bound = "tensor" if t_tc > t_hbm else "hbm"
@@ -417,7 +439,7 @@ def run_ours(args, rank, world, local):
             kname = f"gemm_tc_kernel ({dom})"
             traffic = profile_traffic("gemm_tc_kernel", GEMM_SOURCES) if (
                 dom == "gemm_act" and args.workload == WORKLOAD) else None
-        fl, by = costs[dom]
+        fl, by = costs["gemm_act_gathered" if gathered and dom == "gemm_act" else dom]
         b = breakdown[dom]
         if b["bound"] == "tensor":
             ach, peak, unit = fl / (b["us"] * 1e-6) / 1e12, pk["bf16_tflops"], "TFLOP/s"
@@ -466,7 +488,8 @@ def run_ours(args, rank, world, local):
                        "scoring": cfg.scoring, "renormalize": cfg.renormalize,
                        "groups": [cfg.G, cfg.TG], "rsf": cfg.rsf,
                        "act": ["silu_and_mul", "swiglu", "identity"][cfg.act],
-                       "path": "indexed" if indexed else "staged",
+                       "path": "indexed" if indexed else
+                               "gathered gate_up" if gathered else "staged",
                        "moerouter_slice": [cfg.local_start, cfg.local_count],
                        "l2": "flushed before every timed step (512 MiB write, then 512 MiB "
                              "read so no dirty lines are written back inside the step)",
@@ -485,28 +508,39 @@ def run_ours(args, rank, world, local):
 
 
 def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
-    """One stage alone on the workload's inputs (for profiler captures)."""
+    """One stage alone on the workload's inputs, as the forward runs it (for
+    profiler captures)."""
     import torch
 
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
     dev = inp["hidden"].device
+    gathered = (cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
+                and not os.environ.get("MOE_TC_KERNEL", "").startswith("2"))
     p = moe.config_params(cfg.replace(local_count=0))[0]
     tw, ti, _, _ = moe.moe_route(inp["logits"], p, inp["correction_bias"], inp["expert_ids"])
     perm = moe.moe_permute(ti, E, inp["hidden"])
-    act_out = torch.empty((T * K, F), dtype=torch.bfloat16, device=dev)
-    y = torch.empty((T * K, H), dtype=torch.bfloat16, device=dev)
-    moe.moe_grouped_gemm_act(perm["expert_input"], inp["w_gate_up"], perm["seg_end"], F, a,
-                             out=act_out)
-    moe.moe_grouped_gemm_down(act_out, inp["w_down"], perm["seg_end"], out=y)
+    act_out = torch.empty((T * K, F), dtype=inp["hidden"].dtype, device=dev)
+    y = torch.empty((T * K, H), dtype=inp["hidden"].dtype, device=dev)
+
+    def gemm_act():
+        if gathered:
+            return moe.moe_grouped_gemm_act_gathered(inp["hidden"], perm["row_to_route"], K,
+                                                     inp["w_gate_up"], perm["seg_end"], F, a,
+                                                     inp["b_gate_up"], out=act_out)
+        return moe.moe_grouped_gemm_act(perm["expert_input"], inp["w_gate_up"], perm["seg_end"],
+                                        F, a, inp["b_gate_up"], out=act_out)
+
+    gemm_act()
+    moe.moe_grouped_gemm_down(act_out, inp["w_down"], perm["seg_end"], inp["b_down"], out=y)
     fns = {
         "indexed_mlp": lambda: moe.moe_indexed_mlp(inp["hidden"], inp["w_gate_up"], inp["w_down"],
                                                    tw, ti),
         "route": lambda: moe.moe_route(inp["logits"], p, topk_weights=tw, topk_ids=ti),
-        "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"]),
-        "gemm_act": lambda: moe.moe_grouped_gemm_act(perm["expert_input"], inp["w_gate_up"],
-                                                     perm["seg_end"], F, a, out=act_out),
+        "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"],
+                                           with_gather=not gathered),
+        "gemm_act": gemm_act,
         "gemm_down": lambda: moe.moe_grouped_gemm_down(act_out, inp["w_down"], perm["seg_end"],
-                                                       out=y),
+                                                       inp["b_down"], out=y),
         "combine": lambda: moe.moe_combine(y, tw, perm["route_to_row"]),
     }
     st, nl = timed(fns[args.stage], args.steps, args.warmup)

@@ -212,6 +212,29 @@ moe_status moe_grouped_gemm_act(const void* a, const void* w_gate_up, const void
                                 size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* moe_grouped_gemm_act over gathered rows (an addition; the pages' grouped
+ * GEMM takes the permuted copy of the activations).  Row m of the operand is
+ * hidden[row_to_route[m] / top_k], read straight from the token-ordered hidden
+ * states, so the [M, H] permuted copy (moe_permute's expert_input) is neither
+ * written nor read: moe_permute with expert_input == NULL builds the maps.
+ * The result equals moe_grouped_gemm_act on that copy, bit for bit.
+ *
+ *   hidden        [T, H] bf16, 16-byte aligned, H % 8 == 0
+ *   row_to_route  [M] i32 from moe_permute (route index t*top_k + k of row m)
+ *   w_gate_up, b_gate_up, seg_end, act, out, ws: as moe_grouped_gemm_act with
+ *   Hk = H (F % 8 == 0; w_gate_up and out 16-byte aligned)
+ * Only rows below seg_end[E-1] are read; an entry of row_to_route outside
+ * [0, T*top_k) gives a zero row.  bf16 on the tcgen05 path only: other dtypes,
+ * shapes or alignments return MOE_ERR_UNSUPPORTED (use moe_permute with an
+ * expert_input buffer and moe_grouped_gemm_act instead). */
+moe_status moe_grouped_gemm_act_gathered(const void* hidden, int T, const int32_t* row_to_route,
+                                         int top_k, const void* w_gate_up,
+                                         const void* b_gate_up, const int32_t* seg_end, int M,
+                                         int F, int H, int E, moe_dtype dtype,
+                                         const moe_act_params* act, void* out, void* ws,
+                                         size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Plain grouped down GEMM [TileOPs, MoEGroupedGemmFwdOp (no activation),
  * MoEExpertMLPFwdOp]: out[m, :] = a[m, :] . w_down[e]^T (+ b_down[e]) in fp32,
  * cast to dtype, for the rows m of expert e.

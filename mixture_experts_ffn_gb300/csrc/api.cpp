@@ -191,6 +191,32 @@ moe_status moe_grouped_gemm_act(const void* a, const void* w_gate_up, const void
                                   static_cast<int*>(ws), stream));
 }
 
+moe_status moe_grouped_gemm_act_gathered(const void* hidden, int T, const int32_t* row_to_route,
+                                         int top_k, const void* w_gate_up,
+                                         const void* b_gate_up, const int32_t* seg_end, int M,
+                                         int F, int H, int E, moe_dtype dtype,
+                                         const moe_act_params* act, void* out, void* ws,
+                                         size_t ws_bytes, cudaStream_t stream) {
+  if (T < 0 || top_k < 1 || M < 0 || F < 1 || H < 1 || E < 1 || E > kMaxExperts ||
+      !dtype_ok(dtype) || !act_ok(act))
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)T * top_k >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+  if (!seg_end || !w_gate_up || (M > 0 && (!hidden || !row_to_route || !out)))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, MOE_STATUS_BYTES)) return MOE_ERR_WORKSPACE;
+  const size_t N1 = act->kind == MOE_ACT_IDENTITY ? (size_t)F : 2 * (size_t)F;
+  Span outs[] = {{out, (size_t)M * F * 2}};
+  Span ins[] = {{hidden, (size_t)T * H * 2}, {row_to_route, (size_t)M * 4},
+                {w_gate_up, (size_t)E * N1 * H * 2}, {b_gate_up, b_gate_up ? (size_t)E * N1 * 2 : 0},
+                {seg_end, (size_t)E * 4}, {ws, MOE_STATUS_BYTES}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  if (dtype != MOE_BF16 || !tc_ok(hidden, w_gate_up, out, F, H, M) || !gemm_tc_can_gather())
+    return MOE_ERR_UNSUPPORTED;
+  if (M == 0) return MOE_OK;
+  return cuda_status(launch_gemm_tc(hidden, w_gate_up, b_gate_up, seg_end, M, F, H, E, act, out,
+                                    static_cast<int*>(ws), stream, row_to_route, top_k, T));
+}
+
 moe_status moe_grouped_gemm_down(const void* a, const void* w_down, const void* b_down,
                                  const int32_t* seg_end, int M, int H, int F, int E,
                                  moe_dtype dtype, void* out, void* ws, size_t ws_bytes,
@@ -319,11 +345,21 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   void* a1 = base + L.act;
   void* y = base + L.y;
   int* status = reinterpret_cast<int*>(base);
-  err = launch_permute(hidden, (int)esz, ti, T, H, E, K, xin, seg_end, r2r, route_to_row, ws,
-                       stream);
+  // On the tcgen05 path the gate_up GEMM reads its rows straight from the
+  // token-ordered hidden states through row_to_route, so the permute only
+  // builds the index maps and the permuted copy of the activations is never
+  // written or read back.
+  const bool fused_gather = dtype == MOE_BF16 && tc_ok(hidden, w_gate_up, a1, F, H, (int)M) &&
+                            gemm_tc_can_gather();
+  err = launch_permute(hidden, (int)esz, ti, T, H, E, K, fused_gather ? nullptr : xin, seg_end,
+                       r2r, route_to_row, ws, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
-  err = grouped_gemm(xin, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, dtype, act, a1, status,
-                     stream);
+  if (fused_gather)
+    err = launch_gemm_tc(hidden, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, act, a1, status,
+                         stream, r2r, K, T);
+  else
+    err = grouped_gemm(xin, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, dtype, act, a1,
+                       status, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   err = grouped_gemm(a1, w_down, b_down, seg_end, (int)M, H, F, E, dtype, nullptr, y, status,
                      stream);

@@ -33,6 +33,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -50,6 +51,12 @@ constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
+// With the row gather (A rows read from the token-ordered hidden states through
+// the permutation, so the permuted copy of the activations is never written),
+// four more warps load A with cp.async: TMA copies only whole boxes of a
+// tensor, not rows picked by an index.
+constexpr int NUM_THREADS_GATHER = NUM_THREADS + 128;
+constexpr int kLoaderWarp0 = NUM_THREADS / 32;
 
 struct TcShared {
   uint64_t full[STAGES];
@@ -94,13 +101,17 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 }
 
 
-template <int MODE, int ACT>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// GATHER: row r of A is row grows[r] / gdiv of gsrc (the hidden states, gsrc_rows
+// rows; grows is row_to_route, gdiv = top_k); tm_a is unused.
+template <int MODE, int ACT, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __nv_bfloat16* __restrict__ bias, const int32_t* __restrict__ seg_end,
                    int M, int Nout, int N1, int K, int E, float limit, float alpha, float beta,
                    const __grid_constant__ CUtensorMap tm_out, int tma_out,
-                   __nv_bfloat16* __restrict__ out, int* status) {
+                   __nv_bfloat16* __restrict__ out, int* status,
+                   const __nv_bfloat16* __restrict__ gsrc, const int32_t* __restrict__ grows,
+                   int gdiv, int gsrc_rows) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -111,7 +122,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sh->full[s], 1);
+      // the producer's expect-tx arrival, plus one per A-loader thread
+      mbar_init(&sh->full[s], GATHER ? 1 + 128 : 1);
       mbar_init(&sh->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -162,9 +174,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
           uint8_t* a_dst = smem + (size_t)stage * STAGE_BYTES;
           uint8_t* b_dst = a_dst + A_BYTES;
-          mbar_expect_tx(&sh->full[stage], STAGE_BYTES);
           const int k0 = kb * BK;
-          tma_2d(a_dst, &tm_a, &sh->full[stage], k0, st.m0);
+          if constexpr (GATHER) {
+            mbar_expect_tx(&sh->full[stage], B_BYTES);  // A comes from the loader warps
+          } else {
+            mbar_expect_tx(&sh->full[stage], STAGE_BYTES);
+            tma_2d(a_dst, &tm_a, &sh->full[stage], k0, st.m0);
+          }
           if constexpr (MODE == kTcStacked) {  // gate rows j0.. then up rows F+j0.. in one box
             tma_4d(b_dst, &tm_b, &sh->full[stage], k0, st.n_idx * (BN / 2), 0, st.e);
           } else {
@@ -197,6 +213,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_fast(&sh->full[stage], phase, abort_flag, status)) { ok = false; break; }
+          // cp.async wrote A through the generic proxy; tcgen05.mma reads it
+          // through the async proxy
+          if constexpr (GATHER) fence_proxy_async_smem();
           tc_fence_after();
           const uint64_t off = (uint64_t)((stage * STAGE_BYTES) >> 4);
           umma_kblock(d_tmem, adesc0 + off, bdesc0 + off, kb != 0 ? 1u : 0u, empty_addr[stage]);
@@ -212,6 +231,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         drain_wait(&sh->drain, 0);
       }
     }
+  } else if (GATHER && warp >= kLoaderWarp0) {
+    // ------------------------------------------------ A loaders (gather mode)
+    // 128 threads copy the 128 rows x 128 bytes of a k-block: thread lt owns
+    // 16-byte chunk lt % 8 of rows lt / 8 + 16 i (i < 8), so 8 neighbouring
+    // lanes read one 128-byte row piece; the destination follows the 128-byte
+    // swizzle of the TMA boxes (chunk ch of row r at chunk ch ^ (r % 8)).
+    const int lt = threadIdx.x - kLoaderWarp0 * 32;
+    const int ch = lt & 7, r0 = lt >> 3;
+    const uint32_t dst0 = (uint32_t)(r0 * 128 + ((ch ^ (r0 & 7)) << 4));
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    // The row map entries of a tile are loaded one tile ahead, so their
+    // latency never delays the first copies of the next tile.
+    auto load_map = [&](int tile, int (&r)[8]) {
+      const SegTile t = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        // Only rows of the tile's own expert segment are read: the map holds
+        // defined entries for rows below seg_end[E-1] only (routes with an
+        // out-of-range id get no row); padding rows are zero-filled.
+        const int row = t.m0 + r0 + 16 * i;
+        r[i] = row < t.m_end ? grows[row] : -1;
+      }
+    };
+    int cur[8], nxt[8];
+    if (blockIdx.x < total) load_map(blockIdx.x, cur);
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      if (tile + (int)gridDim.x < total) load_map(tile + gridDim.x, nxt);
+      const __nv_bfloat16* src[8];
+      uint32_t valid = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        int t = 0;
+        if (cur[i] >= 0 && cur[i] / gdiv < gsrc_rows) {
+          t = cur[i] / gdiv;
+          valid |= 1u << i;
+        }
+        src[i] = gsrc + (size_t)t * K + ch * 8;
+      }
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
+        const uint32_t a_dst = su32(smem + (size_t)stage * STAGE_BYTES) + dst0;
+        const int k0 = kb * BK;
+        const bool kin = k0 + ch * 8 < K;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const bool v = kin && ((valid >> i) & 1u);
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(a_dst + i * 16 * 128),
+                       "l"(v ? src[i] + k0 : gsrc), "r"(v ? 16 : 0)
+                       : "memory");
+        }
+        // arrives on the stage's full barrier once this thread's copies land
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                         su32(&sh->full[stage]))
+                     : "memory");
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // nothing in flight at exit
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
     const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
@@ -246,9 +327,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ------------------------------------------------------------ host side
 }  // namespace
 
+bool gemm_tc_can_gather() {
+  const char* v = getenv("MOE_TC_KERNEL");
+  return !(v && v[0] == '2');
+}
+
 cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
-                           int* status, cudaStream_t s) {
+                           int* status, cudaStream_t s, const int32_t* gather_rows,
+                           int gather_div, int gather_src_rows) {
   if (M == 0 || N == 0) return cudaSuccess;
   // The two-SM (cta_group::2) kernel with MOE_TC_KERNEL=2sm.  Its SMs load a
   // third fewer bytes per MMA, which wins on long uniform segments, but its
@@ -259,8 +346,11 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     const char* v = getenv("MOE_TC_KERNEL");
     return v && v[0] == '2';
   }();
-  if (two_sm && num_sms() >= 2)
+  const bool gather = gather_rows != nullptr;
+  if (two_sm && num_sms() >= 2) {
+    if (gather) return cudaErrorNotSupported;  // callers check gemm_tc_can_gather()
     return launch_gemm_tc2(a, w, bias, seg_end, M, N, K, E, act, out, status, s);
+  }
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
   if (act && act->kind != MOE_ACT_IDENTITY) {
@@ -272,7 +362,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     beta = act->beta;
   }
   CUtensorMap ma, mb;
-  {
+  if (!gather) {  // (gathered rows of A are loaded without a tensor map)
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {BK, BM};
@@ -289,12 +379,17 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     cuuint32_t box[3] = {BK, BN, 1};
     if (!tmap::encode_bf16(&mb, w, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
+  if (gather) ma = mb;  // unused by the kernel
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
-    for (const void* fn : {(const void*)gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY>,
-                           (const void*)gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>,
-                           (const void*)gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU>,
-                           (const void*)gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU>})
+    for (const void* fn : {(const void*)gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY, false>,
+                           (const void*)gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, false>,
+                           (const void*)gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU, false>,
+                           (const void*)gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU, false>,
+                           (const void*)gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY, true>,
+                           (const void*)gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, true>,
+                           (const void*)gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU, true>,
+                           (const void*)gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU, true>})
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   });
   const int n_tiles = mode == kTcPlain ? (N + BN - 1) / BN : (N + BN / 2 - 1) / (BN / 2);
@@ -311,15 +406,20 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     cuuint32_t box[2] = {OUT_BOX, OUT_BOX};
     tma_out = tmap::encode_bf16(&mo, out, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
   }
-  if (!tma_out) mo = ma;  // unused
+  if (!tma_out) mo = mb;  // unused
   const auto* bias_p = static_cast<const __nv_bfloat16*>(bias);
   auto* out_p = static_cast<__nv_bfloat16*>(out);
-  auto* kern = mode == kTcPlain       ? gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY>
-               : mode == kTcInterleaved ? gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU>
-               : kind == MOE_ACT_SWIGLU ? gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU>
-                                        : gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>;
-  launch_pdl(kern, grid, NUM_THREADS, kSmemBytes, s, ma, mb, bias_p, seg_end, M, N, N1, K, E,
-      limit, alpha, beta, mo, tma_out, out_p, status);
+  auto pick = [&](auto g) {
+    constexpr bool G = decltype(g)::value;
+    return mode == kTcPlain       ? gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY, G>
+           : mode == kTcInterleaved ? gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU, G>
+           : kind == MOE_ACT_SWIGLU ? gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU, G>
+                                    : gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, G>;
+  };
+  auto* kern = gather ? pick(std::true_type{}) : pick(std::false_type{});
+  launch_pdl(kern, grid, gather ? NUM_THREADS_GATHER : NUM_THREADS, kSmemBytes, s, ma, mb,
+             bias_p, seg_end, M, N, N1, K, E, limit, alpha, beta, mo, tma_out, out_p, status,
+             static_cast<const __nv_bfloat16*>(a), gather_rows, gather_div, gather_src_rows);
   count_launch();
   return cudaGetLastError();
 }

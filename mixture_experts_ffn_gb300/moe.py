@@ -46,6 +46,8 @@ _SIGNATURES = {
     "moe_route": [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_permute": [_vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_act": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp],
+    "moe_grouped_gemm_act_gathered": [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
+                                      _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_down": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
     "moe_combine": [_vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _vp],
     "swiglu": [_vp, _vp, _i64, _i, _i, _i, _f, _f, _f, _vp, _vp],
@@ -214,6 +216,27 @@ def moe_grouped_gemm_act(a, w_gate_up, seg_end, F: int, act: ActParams, b_gate_u
            lib.moe_grouped_gemm_act(_p(a), _p(w_gate_up), _p(b_gate_up), _p(seg_end), M, F, Hk, E,
                                     _dt(a), ctypes.byref(act), _p(out), _p(ws), ws.numel(),
                                     _stream()))
+    return out
+
+
+def moe_grouped_gemm_act_gathered(hidden, row_to_route, top_k: int, w_gate_up, seg_end, F: int,
+                                  act: ActParams, b_gate_up=None, out=None, ws=None):
+    """moe_grouped_gemm_act with row m of the operand read as
+    hidden[row_to_route[m] // top_k] (no permuted copy of the activations)."""
+    lib = load_library()
+    _cuda(hidden, row_to_route, w_gate_up, seg_end, b_gate_up)
+    T, H = hidden.shape
+    M = row_to_route.numel()
+    E = w_gate_up.shape[0]
+    if out is None:
+        out = torch.empty((M, F), dtype=hidden.dtype, device=hidden.device)
+    if ws is None:
+        ws = _ws(MOE_STATUS_BYTES, hidden.device)
+    _check("moe_grouped_gemm_act_gathered",
+           lib.moe_grouped_gemm_act_gathered(_p(hidden), T, _p(row_to_route), top_k,
+                                             _p(w_gate_up), _p(b_gate_up), _p(seg_end), M, F, H,
+                                             E, _dt(hidden), ctypes.byref(act), _p(out), _p(ws),
+                                             ws.numel(), _stream()))
     return out
 
 

@@ -2,6 +2,8 @@
 ragged expert segments: empty experts, segments shorter and longer than a
 128-row tile, column tiles and k-blocks with ragged tails, every activation
 layout, with and without bias, on the tcgen05 path, the SIMT path and fp32."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -132,3 +134,54 @@ def test_gemm_act_large_sampled(moe):
     a_np = a[torch.from_numpy(rows).cuda()].float().cpu().numpy()
     exact = O.grouped_gemm_act(a_np, LazyExperts(w), np.cumsum(sub_counts), F, 0, dtype=None)
     assert_rounded_once(np_(out)[rows], exact, "bf16", "gemm_act large")
+
+
+@pytest.mark.parametrize("T,K,E,H,F,act,bias", [
+    (64, 2, 5, 256, 192, "silu", False),
+    (300, 4, 7, 320, 160, "swiglu_inter", True),
+    (300, 4, 7, 320, 160, "swiglu_concat", True),
+    (97, 8, 16, 128, 64, "silu", True),      # ragged segments, some experts empty
+    (1, 1, 3, 64, 8, "silu", False),         # one route
+    (513, 2, 4, 200, 96, "swiglu_noclamp", False),  # long segments, ragged k-block
+])
+def test_gemm_act_gathered(moe, T, K, E, H, F, act, bias):
+    """The gate_up GEMM reading its rows through row_to_route from the
+    token-ordered hidden states equals the GEMM on the permuted copy bit for
+    bit, and the oracle on the rows the oracle's own permutation selects."""
+    if os.environ.get("MOE_TC_KERNEL", "").startswith("2"):
+        pytest.skip("the two-SM kernel has no gathered-row mode")
+    assert K <= E, "top-k ids are distinct experts"
+    spec = ACTS[act]
+    N1 = 2 * F
+    g = torch.Generator().manual_seed(T * 31 + H)
+    hidden = torch.randn((T, H), generator=g).to(torch.bfloat16)
+    w = (torch.randn((E, N1, H), generator=g) / H ** 0.5).to(torch.bfloat16)
+    b = (torch.randn((E, N1), generator=g) * 0.02).to(torch.bfloat16) if bias else None
+    ids = torch.stack([torch.randperm(E, generator=g)[:K] for _ in range(T)]).to(torch.int32)
+    p = moe.act_params(**spec)
+    perm = moe.moe_permute(ids.cuda(), E, hidden.cuda())
+    bc = None if b is None else b.cuda()
+    got = moe.moe_grouped_gemm_act_gathered(hidden.cuda(), perm["row_to_route"], K, w.cuda(),
+                                            perm["seg_end"], F, p, bc)
+    ref_perm = moe.moe_grouped_gemm_act(perm["expert_input"], w.cuda(), perm["seg_end"], F, p, bc)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref_perm), "gathered rows differ from the permuted-copy GEMM"
+    o = O.permute(ids.numpy(), E)
+    assert np.array_equal(np_(perm["row_to_route"]).astype(np.int32), o["row_to_route"])
+    a = O.gather_rows(np_(hidden), o["row_to_route"], K)
+    exact = O.grouped_gemm_act(a, np_(w), o["seg_end"], F, spec["kind"],
+                               spec.get("swiglu_fusion", 2), spec.get("limit", 0.0),
+                               spec.get("alpha", 1.0), spec.get("beta", 0.0),
+                               None if b is None else np_(b), dtype=None)
+    assert_rounded_once(np_(got), exact, "bf16", f"gemm_act_gathered {act}")
+
+
+def test_gemm_act_gathered_rejects_unsupported(moe):
+    """fp32 (no tensor-core path) is refused, not silently computed elsewhere."""
+    hidden = torch.randn((8, 64), device="cuda")
+    w = torch.randn((2, 16, 64), device="cuda")
+    seg_end = torch.tensor([8, 16], dtype=torch.int32, device="cuda")
+    r2r = torch.arange(16, dtype=torch.int32, device="cuda")
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_grouped_gemm_act_gathered(hidden, r2r, 2, w, seg_end, 8, moe.act_params(0))
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED

@@ -1,7 +1,10 @@
 """The alternative tcgen05 grouped-GEMM kernel -- two-SM cta_group::2 tiles with
 the shared staged-store epilogue, selected with MOE_TC_KERNEL=2sm -- runs the
-whole grouped-GEMM parity file in a fresh process (the switch is read once per
-process)."""
+whole grouped-GEMM parity file and the small whole-forward cases in a fresh
+process (the switch is read once per process).  That kernel has no
+gathered-row mode, so under it the forward also takes the staged route
+(permuted copy of the activations, then the grouped GEMM), which the default
+forward replaces with the gathered gate_up GEMM."""
 import os
 import subprocess
 import sys
@@ -17,6 +20,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 def test_alternative_gemm_kernel_parity(kernel):
     env = dict(os.environ, MOE_TC_KERNEL=kernel)
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(HERE, "test_gpu_gemm.py"),
-                        "-q", "-p", "no:cacheprovider"], env=env, capture_output=True, text=True,
-                       timeout=900)
+                        os.path.join(HERE, "test_gpu_ffn.py"), "-k",
+                        "not full_size and not indexed", "-q", "-p", "no:cacheprovider"],
+                       env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
