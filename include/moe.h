@@ -282,7 +282,8 @@ moe_status swiglu(const void* gate, const void* up, int64_t R, int I, moe_dtype 
  * result as permute + the two grouped GEMMs (silu_and_mul, no bias) +
  * combine, dispatched per route.  Routes sharing an expert are grouped and
  * each distinct expert's weights are streamed from HBM once, for all of its
- * routes, with 128-bit loads.  bf16 only; H % 128 == 0, F % 256 == 0.
+ * routes, with 128-bit loads.  bf16 only; H % 128 == 0, F % 256 == 0,
+ * hidden / w_gate_up / w_down 16-byte aligned (MOE_ERR_UNSUPPORTED otherwise).
  *
  *   hidden [T, H] bf16;  w_gate_up [E, 2F, H] bf16 (stacked);  w_down [E, H, F];
  *   topk_weights [T, K] f32;  topk_ids [T, K] i32;  out [T, H] bf16;
@@ -296,8 +297,9 @@ moe_status moe_indexed_mlp(const void* hidden, const void* w_gate_up, const void
 /* The whole routed MoE FFN forward [TileOPs, FusedMoEFwdOp and
  * FusedMoEExpertsFwdOp].  Routes with moe_route (rsf folded into the weights,
  * so it applies once), then runs the indexed path when T*K <= 2E, the
- * activation is silu_and_mul, there is no bias, dtype is bf16, H % 128 == 0
- * and F % 256 == 0 [TileOPs, FusedMoEExpertsFwdOp dispatch rule]; otherwise
+ * activation is silu_and_mul, there is no bias, dtype is bf16, H % 128 == 0,
+ * F % 256 == 0 and hidden and the weights are 16-byte aligned [TileOPs,
+ * FusedMoEExpertsFwdOp dispatch rule]; otherwise
  * the staged pipeline permute -> gate_up+act -> down -> combine.
  *
  *   hidden [T, H] dtype;  logits [T, E] f32;  w_gate_up [E, N1, H];

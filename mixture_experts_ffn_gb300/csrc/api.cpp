@@ -114,9 +114,11 @@ cudaError_t grouped_gemm(const void* a, const void* w, const void* bias, const i
 }
 
 bool indexed_rule(int T, int H, int F, int E, int K, moe_dtype dt, const moe_act_params* act,
-                  const void* b1, const void* b2) {
+                  const void* b1, const void* b2, const void* hidden, const void* w1,
+                  const void* w2) {
   return (long long)T * K <= 2LL * E && act->kind == MOE_ACT_SILU_AND_MUL && !b1 && !b2 &&
-         dt == MOE_BF16 && H % 128 == 0 && F % 256 == 0;
+         dt == MOE_BF16 && H % 128 == 0 && F % 256 == 0 && aligned16(hidden) &&
+         aligned16(w1) && aligned16(w2);
 }
 
 }  // namespace
@@ -279,6 +281,9 @@ moe_status moe_indexed_mlp(const void* hidden, const void* w_gate_up, const void
   if (H % 128 != 0 || F % 256 != 0) return MOE_ERR_UNSUPPORTED;
   if (!w_gate_up || !w_down || (T > 0 && (!hidden || !topk_weights || !topk_ids || !out)))
     return MOE_ERR_INVALID_ARG;
+  // rows are streamed with 16-byte bulk copies and vector loads
+  if (!aligned16(w_gate_up) || !aligned16(w_down) || (T > 0 && !aligned16(hidden)))
+    return MOE_ERR_UNSUPPORTED;
   ForwardWs L(T, H, F, E, K, 2);
   if (!ws_ok(ws, ws_bytes, L.total)) return MOE_ERR_WORKSPACE;
   const size_t M = (size_t)T * K;
@@ -334,7 +339,7 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   if (err != cudaSuccess) return MOE_ERR_CUDA;
 
   // routed_scaling_factor is folded into tw by the router: the combine scale is 1
-  if (indexed_rule(T, H, F, E, K, dtype, act, b_gate_up, b_down))
+  if (indexed_rule(T, H, F, E, K, dtype, act, b_gate_up, b_down, hidden, w_gate_up, w_down))
     return cuda_status(
         launch_indexed(hidden, w_gate_up, w_down, tw, ti, T, H, F, E, K, 1.0f, out, ws, L, stream));
 

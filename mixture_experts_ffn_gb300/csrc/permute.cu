@@ -12,6 +12,7 @@
 //             warp match-any, so rows inside an expert follow ascending route
 //   gather  : one warp per row copies the hidden row with 128-bit accesses
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -64,6 +65,14 @@ __device__ int block_exclusive_scan(int v, int* warp_tot /*>= 33*/, int* total) 
   return r;
 }
 
+// One CTA.  Thread i owns a contiguous run of experts; for each it sums the
+// expert's count over the chunks (coalesced across the warp, 16 loads in
+// flight), the totals are scanned across the block into segment starts, and
+// counts[c][e] is overwritten with the first row of expert e's routes in chunk
+// c (start + routes of e in earlier chunks).  The experts that have routes are
+// listed in ascending order.
+constexpr int kScanBatch = 16;
+
 __global__ void __launch_bounds__(1024) perm_scan(int* __restrict__ counts, int C, int E,
                                                   int32_t* __restrict__ seg_end,
                                                   int* __restrict__ active,
@@ -73,19 +82,17 @@ __global__ void __launch_bounds__(1024) perm_scan(int* __restrict__ counts, int 
   const int nthr = blockDim.x, tid = threadIdx.x;
   const int per = (E + nthr - 1) / nthr;
   const int lo = min(E, tid * per), hi = min(E, lo + per);
-  // per-expert totals of this thread's experts
   int tot_local = 0, act_local = 0;
   for (int e = lo; e < hi; ++e) {
-    int s0 = 0, s1 = 0, s2 = 0, s3 = 0;
-    int c = 0;
-    for (; c + 4 <= C; c += 4) {  // independent loads in flight
-      s0 += counts[(size_t)c * E + e];
-      s1 += counts[(size_t)(c + 1) * E + e];
-      s2 += counts[(size_t)(c + 2) * E + e];
-      s3 += counts[(size_t)(c + 3) * E + e];
+    int s = 0;
+    for (int c0 = 0; c0 < C; c0 += kScanBatch) {
+      int v[kScanBatch];
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j)
+        v[j] = c0 + j < C ? counts[(size_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) s += v[j];
     }
-    for (; c < C; ++c) s0 += counts[(size_t)c * E + e];
-    const int s = s0 + s1 + s2 + s3;
     tot_local += s;
     act_local += s > 0;
   }
@@ -94,11 +101,16 @@ __global__ void __launch_bounds__(1024) perm_scan(int* __restrict__ counts, int 
   int astart = block_exclusive_scan(act_local, wt, &n_act);
   for (int e = lo; e < hi; ++e) {
     int run = start;
-    for (int c = 0; c < C; ++c) {
-      int* p = counts + (size_t)c * E + e;
-      int n = *p;
-      *p = run;  // becomes the first row of expert e's routes in chunk c
-      run += n;
+    for (int c0 = 0; c0 < C; c0 += kScanBatch) {
+      int v[kScanBatch];
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j)
+        v[j] = c0 + j < C ? counts[(size_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < kScanBatch; ++j) {
+        if (c0 + j < C) counts[(size_t)(c0 + j) * E + e] = run;
+        run += v[j];
+      }
     }
     seg_end[e] = run;
     if (run > start) active[astart++] = e;

@@ -39,6 +39,9 @@ def _ids(T, K, E, gen, mode="random"):
     (257, 6, 16, 128, "one", torch.float32),
     (4096, 8, 128, 2048, "random", torch.bfloat16),
     (8192, 8, 256, 64, "random", torch.bfloat16),
+    (3000, 8, 2000, 16, "random", torch.bfloat16),     # E > 1024, one warp per chunk
+    (5000, 8, 12288, 16, "random", torch.bfloat16),    # the largest E accepted
+    (70000, 2, 384, 16, "skewed", torch.bfloat16),     # 137 chunks: scan over > 128 chunks
 ])
 def test_permute_bit_exact(moe, T, K, E, H, mode, dtype):
     g = torch.Generator().manual_seed(T * 7 + E)
