@@ -436,8 +436,10 @@ def run_ours(args, rank, world, local):
             traffic = None
         else:
             dom = max(("gemm_act", "gemm_down"), key=lambda k: breakdown[k]["us"])
-            kname = f"gemm_tc_kernel ({dom})"
-            traffic = profile_traffic("gemm_tc_kernel", GEMM_SOURCES) if (
+            # bf16 with 16-byte rows runs the tcgen05 kernel, anything else the SIMT one
+            tc = cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
+            kname = f"{'gemm_tc_kernel' if tc else 'gemm_simt_kernel'} ({dom})"
+            traffic = profile_traffic("gemm_tc_kernel", GEMM_SOURCES) if tc and (
                 dom == "gemm_act" and args.workload == WORKLOAD) else None
         fl, by = costs["gemm_act_gathered" if gathered and dom == "gemm_act" else dom]
         b = breakdown[dom]
