@@ -334,15 +334,6 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   char* base = static_cast<char*>(ws);
   float* tw = topk_weights_out ? topk_weights_out : reinterpret_cast<float*>(base + L.topk_w);
   int32_t* ti = topk_ids_out ? topk_ids_out : reinterpret_cast<int32_t*>(base + L.topk_ids);
-  cudaError_t err = launch_route(logits, correction_bias, expert_ids, T, E, *p, tw, ti,
-                                 router_probs, weight_scale, stream);
-  if (err != cudaSuccess) return MOE_ERR_CUDA;
-
-  // routed_scaling_factor is folded into tw by the router: the combine scale is 1
-  if (indexed_rule(T, H, F, E, K, dtype, act, b_gate_up, b_down, hidden, w_gate_up, w_down))
-    return cuda_status(
-        launch_indexed(hidden, w_gate_up, w_down, tw, ti, T, H, F, E, K, 1.0f, out, ws, L, stream));
-
   int32_t* seg_end = reinterpret_cast<int32_t*>(base + L.seg_end);
   int32_t* r2r = reinterpret_cast<int32_t*>(base + L.row_to_route);
   int32_t* route_to_row = reinterpret_cast<int32_t*>(base + L.route_to_row);
@@ -350,15 +341,34 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   void* a1 = base + L.act;
   void* y = base + L.y;
   int* status = reinterpret_cast<int*>(base);
+  const bool indexed =
+      indexed_rule(T, H, F, E, K, dtype, act, b_gate_up, b_down, hidden, w_gate_up, w_down);
   // On the tcgen05 path the gate_up GEMM reads its rows straight from the
   // token-ordered hidden states through row_to_route, so the permute only
   // builds the index maps and the permuted copy of the activations is never
   // written or read back.
-  const bool fused_gather = dtype == MOE_BF16 && tc_ok(hidden, w_gate_up, a1, F, H, (int)M) &&
-                            gemm_tc_can_gather();
-  err = launch_permute(hidden, (int)esz, ti, T, H, E, K, fused_gather ? nullptr : xin, seg_end,
-                       r2r, route_to_row, ws, stream);
+  const bool fused_gather = !indexed && dtype == MOE_BF16 &&
+                            tc_ok(hidden, w_gate_up, a1, F, H, (int)M) && gemm_tc_can_gather();
+  // When only the index maps are needed, routing and the maps take one launch.
+  const bool fused_maps = (indexed || fused_gather) && route_permute_ok(E);
+  cudaError_t err =
+      fused_maps ? launch_route_permute(logits, correction_bias, expert_ids, T, E, *p, tw, ti,
+                                        router_probs, weight_scale, seg_end, r2r, route_to_row,
+                                        ws, stream)
+                 : launch_route(logits, correction_bias, expert_ids, T, E, *p, tw, ti,
+                                router_probs, weight_scale, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
+
+  // routed_scaling_factor is folded into tw by the router: the combine scale is 1
+  if (indexed)
+    return cuda_status(launch_indexed(hidden, w_gate_up, w_down, tw, ti, T, H, F, E, K, 1.0f, out,
+                                      ws, L, stream, fused_maps));
+
+  if (!fused_maps) {
+    err = launch_permute(hidden, (int)esz, ti, T, H, E, K, fused_gather ? nullptr : xin, seg_end,
+                         r2r, route_to_row, ws, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if (fused_gather)
     err = launch_gemm_tc(hidden, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, act, a1, status,
                          stream, r2r, K, T);

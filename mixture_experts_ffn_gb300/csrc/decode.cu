@@ -182,7 +182,8 @@ __global__ void __launch_bounds__(kWarps * 32) indexed_down(
 
 cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, const float* w,
                            const int32_t* ids, int T, int H, int F, int E, int K, float scale,
-                           void* out, void* ws, const ForwardWs& L, cudaStream_t s) {
+                           void* out, void* ws, const ForwardWs& L, cudaStream_t s,
+                           bool maps_ready) {
   const int M = T * K;
   if (M == 0) return cudaSuccess;
   char* base = static_cast<char*>(ws);
@@ -195,9 +196,11 @@ cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, c
   const int* active = reinterpret_cast<const int*>(base + P.active);
   const int* num_active = reinterpret_cast<const int*>(base + P.num_active);
 
-  cudaError_t err = launch_permute(nullptr, 2, ids, T, H, E, K, nullptr, seg_end, r2r,
-                                   route_to_row, ws, s);
-  if (err != cudaSuccess) return err;
+  cudaError_t err = cudaSuccess;
+  if (!maps_ready) {
+    err = launch_permute(nullptr, 2, ids, T, H, E, K, nullptr, seg_end, r2r, route_to_row, ws, s);
+    if (err != cudaSuccess) return err;
+  }
   const int grid = num_sms() * 4;
   launch_pdl(indexed_gate_up, grid, kWarps * 32, 0, s, static_cast<const __nv_bfloat16*>(hidden),
       static_cast<const __nv_bfloat16*>(w1), seg_end, r2r, active, num_active, T, H, F, K, act);

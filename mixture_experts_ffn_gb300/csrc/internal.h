@@ -84,6 +84,17 @@ cudaError_t launch_route(const float* logits, const float* bias, const int32_t* 
                          int E, const moe_route_params& p, float* w, int32_t* ids, float* probs,
                          float* wscale, cudaStream_t s);
 
+// Router + permute index maps in one launch (bit-identical to launch_route
+// then launch_permute without the gather); route_permute_ok(E) says whether
+// E is within its limit (E <= 512).  Uses ws's permute scratch and two ints
+// of its status area.
+bool route_permute_ok(int E);
+cudaError_t launch_route_permute(const float* logits, const float* bias, const int32_t* ids_in,
+                                 int T, int E, const moe_route_params& p, float* w, int32_t* ids,
+                                 float* probs, float* wscale, int32_t* seg_end,
+                                 int32_t* row_to_route, int32_t* route_to_row, void* ws,
+                                 cudaStream_t s);
+
 cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int T, int H, int E,
                            int K, void* expert_input, int32_t* seg_end, int32_t* row_to_route,
                            int32_t* route_to_row, void* ws, cudaStream_t s);
@@ -121,6 +132,7 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
 // indexed per-route decode path (bf16, silu_and_mul, no bias)
 cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, const float* w,
                            const int32_t* ids, int T, int H, int F, int E, int K, float scale,
-                           void* out, void* ws, const ForwardWs& L, cudaStream_t s);
+                           void* out, void* ws, const ForwardWs& L, cudaStream_t s,
+                           bool maps_ready = false);
 
 }  // namespace moe

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "permute_dev.cuh"
 
 namespace moe {
 namespace {
@@ -23,46 +24,7 @@ __global__ void __launch_bounds__(256) perm_count(const int32_t* __restrict__ id
                                                   int* __restrict__ counts, int* status) {
   pdl_wait();  // everything below reads results of earlier launches
   extern __shared__ int hist[];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-  __syncthreads();
-  const int r0 = blockIdx.x * kPermuteChunk, r1 = min(M, r0 + kPermuteChunk);
-  bool bad = false;
-  for (int r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
-    int id = __ldg(ids + r);
-    if (id >= 0 && id < E) atomicAdd(&hist[id], 1);
-    else bad = true;
-  }
-  if (bad) latch_error(status, kDevBadIndex);
-  __syncthreads();
-  int* out = counts + (size_t)blockIdx.x * E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) out[e] = hist[e];
-}
-
-// Exclusive block scan of one value per thread (blockDim.x <= 1024).
-__device__ int block_exclusive_scan(int v, int* warp_tot /*>= 33*/, int* total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += n;
-  }
-  if (lane == 31) warp_tot[wid] = x;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int w = 0; w < nw; ++w) {
-      int t = warp_tot[w];
-      warp_tot[w] = acc;
-      acc += t;
-    }
-    warp_tot[32] = acc;
-  }
-  __syncthreads();
-  int r = warp_tot[wid] + x - v;
-  *total = warp_tot[32];
-  __syncthreads();
-  return r;
+  pm::count_chunk(ids, M, E, blockIdx.x, hist, counts + (size_t)blockIdx.x * E, status);
 }
 
 // One CTA.  Thread i owns a contiguous run of experts; for each it sums the
@@ -97,8 +59,8 @@ __global__ void __launch_bounds__(1024) perm_scan(int* __restrict__ counts, int 
     act_local += s > 0;
   }
   int total, n_act;
-  int start = block_exclusive_scan(tot_local, wt, &total);
-  int astart = block_exclusive_scan(act_local, wt, &n_act);
+  int start = pm::block_exclusive_scan(tot_local, wt, &total);
+  int astart = pm::block_exclusive_scan(act_local, wt, &n_act);
   for (int e = lo; e < hi; ++e) {
     int run = start;
     for (int c0 = 0; c0 < C; c0 += kScanBatch) {
@@ -162,65 +124,15 @@ __global__ void __launch_bounds__(32) perm_scatter(const int32_t* __restrict__ i
   }
 }
 
-// Scatter of one chunk by W warps: warp w ranks its routes with match-any
-// (one round per 32 routes), the per-warp expert counts are prefixed across
-// warps in shared memory, then every route gets row = chunk start of its
-// expert + routes of that expert in earlier warps + its rank in the warp.
-// Rows inside an expert therefore follow ascending route index.
+// Scatter of one chunk per CTA (pm::scatter_chunk).
 __global__ void __launch_bounds__(1024) perm_scatter_cta(const int32_t* __restrict__ ids, int M,
                                                          int E, const int* __restrict__ offsets,
                                                          int32_t* __restrict__ row_to_route,
                                                          int32_t* __restrict__ route_to_row) {
   pdl_wait();  // everything below reads results of earlier launches
-  extern __shared__ int wcnt[];  // [W][E]: counts, then exclusive row bases
-  const int W = blockDim.x >> 5;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int per_warp = kPermuteChunk / W;  // routes per warp, a multiple of 32
-  for (int i = threadIdx.x; i < W * E; i += blockDim.x) wcnt[i] = 0;
-  __syncthreads();
-  const int r0 = blockIdx.x * kPermuteChunk + warp * per_warp;
-  const int r1 = min(M, min(blockIdx.x * kPermuteChunk + kPermuteChunk, r0 + per_warp));
-  const uint32_t lt = (1u << lane) - 1u;
-  int* mine = wcnt + (size_t)warp * E;
-  constexpr int kMaxRounds = kPermuteChunk / 32;
-  int rank_of[kMaxRounds];  // rank of this lane's route in round j
-  for (int j = 0; j * 32 < per_warp; ++j) {
-    const int r = r0 + j * 32 + lane;
-    const bool valid = r < r1;
-    const int id = valid ? __ldg(ids + r) : -1;
-    const bool ok = valid && id >= 0 && id < E;
-    const int key = ok ? id : -1 - lane;
-    const uint32_t peers = __match_any_sync(0xffffffffu, key);
-    const int before = ok ? mine[id] : 0;
-    __syncwarp();
-    if (ok && __popc(peers & lt) == 0) mine[id] = before + __popc(peers);
-    __syncwarp();
-    rank_of[j & (kMaxRounds - 1)] = before + __popc(peers & lt);
-  }
-  __syncthreads();
-  // exclusive prefix over warps, per expert, seeded with the chunk's start row
-  const int* off = offsets + (size_t)blockIdx.x * E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = off[e];
-    for (int w = 0; w < W; ++w) {
-      const int c = wcnt[(size_t)w * E + e];
-      wcnt[(size_t)w * E + e] = run;
-      run += c;
-    }
-  }
-  __syncthreads();
-  for (int j = 0; j * 32 < per_warp; ++j) {
-    const int r = r0 + j * 32 + lane;
-    if (r >= r1) break;
-    const int id = __ldg(ids + r);
-    if (id >= 0 && id < E) {
-      const int row = mine[id] + rank_of[j & (kMaxRounds - 1)];
-      row_to_route[row] = r;
-      route_to_row[r] = row;
-    } else {
-      route_to_row[r] = -1;
-    }
-  }
+  extern __shared__ int wcnt[];  // [W][E]
+  pm::scatter_chunk(ids, M, E, blockIdx.x, offsets + (size_t)blockIdx.x * E, wcnt, row_to_route,
+                    route_to_row);
 }
 
 // expert_input[row] = hidden[row_to_route[row] / K], rows < seg_end[E-1]

@@ -1,40 +1,10 @@
-// Router: one warp per token, scores in registers, group pruning and top-k by
-// warp arg-max rounds.  Implements the routing of TileOPs "MoE Operators"
-// (FusedTopKFwdOp, FusedMoEFwdOp) and the MoERouter log-domain outputs of
-// ONNX Runtime PR #32126 "[CUDA] Add MoERouter and SwiGLU contrib operators".
-#include <math.h>
-
-#include "common.cuh"
+// Router kernel: one warp per token (route_dev.cuh).
+#include "route_dev.cuh"
 
 namespace moe {
 namespace {
 
-struct RouteArgs {
-  int K, scoring, renorm, G, TG, ls, lc;
-  float rsf, route_scale;
-};
-
-// r[i] of a register array by a warp-uniform or per-lane index, without local memory
-template <int NPL>
-__device__ __forceinline__ float pick(const float (&r)[NPL], int i) {
-  float v = 0.f;
-#pragma unroll
-  for (int j = 0; j < NPL; ++j) v = (j == i) ? r[j] : v;
-  return v;
-}
-
-// (value, index) arg-max across the warp; ties go to the lower index
-__device__ __forceinline__ void warp_argmax(float& v, int& idx) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    float ov = __shfl_xor_sync(0xffffffffu, v, o);
-    int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-    if (ov > v || (ov == v && oi < idx)) {
-      v = ov;
-      idx = oi;
-    }
-  }
-}
+using rt::RouteArgs;
 
 template <int NPL>
 __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits,
@@ -46,191 +16,9 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
                                                     float* __restrict__ probs,
                                                     float* __restrict__ wscale) {
   pdl_wait();  // everything below reads results of earlier launches
-  const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float* z = logits + (size_t)t * E;
-  const int K = a.K;
-
-  // ---- scores s (float32), experts e = lane + 32 i
-  float s[NPL];
-#pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    int e = lane + 32 * i;
-    s[i] = e < E ? __ldg(z + e) : -INFINITY;
-  }
-  if (a.scoring == MOE_SCORING_SOFTMAX) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) m = fmaxf(m, s[i]);
-    m = warp_max(m);
-    float sum = 0.f;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      int e = lane + 32 * i;
-      s[i] = e < E ? expf(s[i] - m) : 0.f;
-      sum += s[i];
-    }
-    sum = warp_sum(sum);
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) s[i] = s[i] / sum;
-  } else {
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      int e = lane + 32 * i;
-      s[i] = e < E ? 1.0f / (1.0f + expf(-s[i])) : 0.f;
-    }
-  }
-
-  uint32_t sel = 0;  // bit i: expert lane + 32 i selected (selection path)
-  float total = 0.f; // sum of the chosen scores (with multiplicity)
-  const bool hash = ids_in != nullptr;
-  if (hash) {
-    // fixed ids: selection skipped, bias ignored
-    for (int k = 0; k < K; ++k) {
-      int id = __ldg(ids_in + (size_t)t * K + k);
-      bool ok = id >= 0 && id < E;
-      int idc = ok ? id : 0;
-      float sc = __shfl_sync(0xffffffffu, pick(s, idc >> 5), idc & 31);
-      total += ok ? sc : 0.f;
-    }
-  } else {
-    // ---- selection scores u = s + bias
-    float u[NPL];
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      int e = lane + 32 * i;
-      u[i] = e < E ? (bias ? s[i] + __ldg(bias + e) : s[i]) : -INFINITY;
-    }
-    // ---- group restriction
-    if (a.G > 1) {
-      const int S = E / a.G;
-      float my_gs = -INFINITY;  // lane g holds group g's score
-      for (int g = 0; g < a.G; ++g) {
-        float b1 = -INFINITY, b2 = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < NPL; ++i) {
-          int e = lane + 32 * i;
-          if (e >= g * S && e < (g + 1) * S) {
-            float v = u[i];
-            if (v > b1) { b2 = b1; b1 = v; } else if (v > b2) { b2 = v; }
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          float o1 = __shfl_xor_sync(0xffffffffu, b1, o);
-          float o2 = __shfl_xor_sync(0xffffffffu, b2, o);
-          float n1 = fmaxf(b1, o1);
-          float n2 = fmaxf(fminf(b1, o1), fmaxf(b2, o2));
-          b1 = n1;
-          b2 = n2;
-        }
-        float gs = bias ? b1 + b2 : b1;
-        if (lane == g) my_gs = gs;
-      }
-      uint32_t keep = 0;
-      float cand = lane < a.G ? my_gs : -INFINITY;
-      for (int r = 0; r < a.TG; ++r) {
-        float v = cand;
-        int idx = lane < a.G ? lane : 0x7fffffff;
-        if (lane >= a.G) v = -INFINITY;
-        // already kept groups are out of the running
-        if ((keep >> lane) & 1u) { v = -INFINITY; idx = 0x7fffffff; }
-        warp_argmax(v, idx);
-        keep |= 1u << idx;
-      }
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        int e = lane + 32 * i;
-        if (e < E && !((keep >> (e / S)) & 1u)) u[i] = -INFINITY;
-      }
-    }
-    // ---- top-K, ties to the lower expert index
-    for (int r = 0; r < K; ++r) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) {
-        int e = lane + 32 * i;
-        // ascending e inside a lane: strict '>' keeps the lower index on ties
-        if (e < E && !((sel >> i) & 1u) && (be == 0x7fffffff || u[i] > bv)) {
-          bv = u[i];
-          be = e;
-        }
-      }
-      warp_argmax(bv, be);
-      if (be != 0x7fffffff && (be & 31) == lane) sel |= 1u << (be >> 5);
-    }
-    float part = 0.f;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) part += ((sel >> i) & 1u) ? s[i] : 0.f;
-    total = warp_sum(part);
-  }
-
-  // ---- topk ids / weights
-  if (hash) {
-    for (int k = 0; k < K; ++k) {
-      int id = __ldg(ids_in + (size_t)t * K + k);
-      bool ok = id >= 0 && id < E;
-      int idc = ok ? id : 0;
-      float sc = __shfl_sync(0xffffffffu, pick(s, idc >> 5), idc & 31);
-      sc = ok ? sc : 0.f;
-      if (lane == 0) {
-        float w = a.renorm ? sc / total : sc;
-        w_out[(size_t)t * K + k] = w * a.rsf;
-        id_out[(size_t)t * K + k] = id;
-      }
-    }
-  } else {
-    int base = 0;
-    const uint32_t lt = (1u << lane) - 1u;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      bool me = (sel >> i) & 1u;
-      uint32_t m = __ballot_sync(0xffffffffu, me);
-      if (me) {
-        int pos = base + __popc(m & lt);
-        float w = a.renorm ? s[i] / total : s[i];
-        w_out[(size_t)t * K + pos] = w * a.rsf;
-        id_out[(size_t)t * K + pos] = lane + 32 * i;
-      }
-      base += __popc(m);
-    }
-  }
-
-  // ---- MoERouter outputs over the local slice [ls, ls + lc)
-  if (a.lc > 0) {
-    float acc[NPL];  // w^ mass per owned expert
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) acc[i] = 0.f;
-    if (hash) {
-      for (int k = 0; k < K; ++k) {
-        int id = __ldg(ids_in + (size_t)t * K + k);
-        if (id < 0 || id >= E) continue;
-        float sc = __shfl_sync(0xffffffffu, pick(s, id >> 5), id & 31);
-        if ((id & 31) == lane) {
-#pragma unroll
-          for (int i = 0; i < NPL; ++i)
-            if (i == (id >> 5)) acc[i] += sc / total;
-        }
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < NPL; ++i) acc[i] = ((sel >> i) & 1u) ? s[i] / total : 0.f;
-    }
-    float local = 0.f;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-      int e = lane + 32 * i;
-      if (e >= a.ls && e < a.ls + a.lc && e < E) {
-        float v = acc[i];
-        probs[(size_t)t * a.lc + (e - a.ls)] = v > 0.f ? logf(v) : -1e30f;
-        local += v;
-      }
-    }
-    local = warp_sum(local);
-    if (lane == 0) wscale[t] = a.route_scale * local;
-  }
+  rt::route_token<NPL>(t, logits, bias, ids_in, E, a, w_out, id_out, probs, wscale);
 }
 
 template <int NPL>
@@ -251,16 +39,7 @@ cudaError_t launch_route(const float* logits, const float* bias, const int32_t* 
                          int E, const moe_route_params& p, float* w, int32_t* ids, float* probs,
                          float* wscale, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
-  RouteArgs a;
-  a.K = p.top_k;
-  a.scoring = p.scoring;
-  a.renorm = p.renormalize != 0;
-  a.G = p.num_expert_group;
-  a.TG = p.topk_group;
-  a.ls = p.local_expert_start;
-  a.lc = (probs && wscale) ? p.local_expert_count : 0;
-  a.rsf = p.routed_scaling_factor;
-  a.route_scale = p.route_scale;
+  const RouteArgs a = rt::route_args(p, probs, wscale);
   const int npl = (E + 31) / 32;
   if (npl <= 1) return launch_npl<1>(logits, bias, ids_in, T, E, a, w, ids, probs, wscale, s);
   if (npl <= 2) return launch_npl<2>(logits, bias, ids_in, T, E, a, w, ids, probs, wscale, s);

@@ -1,0 +1,186 @@
+// Fused route + permute index maps: one persistent launch (one CTA of 16
+// warps per SM) instead of the router and the three permute launches, whose
+// cost on the forward is mostly the fixed latency of each launch.
+//
+//   A  route: warp per token, grid-stride over tokens (route_dev.cuh)
+//   -- grid barrier (every token's ids written)
+//   B  count: CTA per chunk of kPermuteChunk routes, histogram -> counts[c][E]
+//   -- grid barrier (every chunk counted)
+//   C  scan:  every CTA that owns a chunk reads all counts, scans the expert
+//             totals into expert start rows (CTA 0 writes seg_end and the
+//             active-expert list) and, for its chunks, the first row of each
+//             expert in the chunk
+//   D  scatter: the chunk's routes get their rows (permute_dev.cuh)
+// The result is bit-identical to moe_route followed by moe_permute (same
+// routing code, same chunking, same in-order ranks).
+//
+// The grid barriers spin on two counters in the status area of the
+// workspace, zeroed on the stream before the launch.  All CTAs of the grid
+// are resident together (one per SM, at most one per SM is launched), and
+// every spin is bounded: a barrier that runs out latches the timeout bit and
+// the CTA stops.
+#include <algorithm>
+#include <mutex>
+#include <type_traits>
+
+#include "common.cuh"
+#include "permute_dev.cuh"
+#include "route_dev.cuh"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+using rt::RouteArgs;
+
+constexpr int kFusedWarps = 16;  // kPermuteChunk / 16 = 64 routes per warp in the scatter
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// All CTAs of the grid meet here; false (and the timeout bit) if one never came.
+__device__ bool grid_barrier(int* ctr, int* status) {
+  __shared__ int ok_s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's writes before its arrival
+    atomicAdd(ctr, 1);
+    const uint64_t t0 = global_ns();
+    int ok = 1;
+    while (ld_acquire(ctr) < (int)gridDim.x) {
+      if (global_ns() - t0 > tc::kTimeoutNs) {
+        latch_error(status, kDevTimeout);
+        ok = 0;
+        break;
+      }
+      __nanosleep(128);
+    }
+    __threadfence();
+    ok_s = ok;
+  }
+  __syncthreads();
+  return ok_s != 0;
+}
+
+// counts[0..n)[e] summed, 16 loads in flight
+__device__ __forceinline__ int column_sum(const int* __restrict__ counts, int E, int e, int n) {
+  int s = 0;
+  for (int c0 = 0; c0 < n; c0 += 16) {
+    int v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = c0 + j < n ? counts[(size_t)(c0 + j) * E + e] : 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) s += v[j];
+  }
+  return s;
+}
+
+template <int NPL>
+__global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
+    const float* __restrict__ logits, const float* __restrict__ bias,
+    const int32_t* __restrict__ ids_in, int T, int E, RouteArgs a, float* __restrict__ w_out,
+    int32_t* __restrict__ id_out, float* __restrict__ probs, float* __restrict__ wscale,
+    int C, int* __restrict__ counts, int32_t* __restrict__ seg_end, int* __restrict__ active,
+    int* __restrict__ num_active, int32_t* __restrict__ row_to_route,
+    int32_t* __restrict__ route_to_row, int* status, int* bar) {
+  extern __shared__ int smem[];  // [E] expert start | [E] chunk offsets / histogram | [W][E]
+  pdl_wait();  // everything below reads results of earlier launches
+  const int warp = threadIdx.x >> 5, W = blockDim.x >> 5, tid = threadIdx.x;
+  const int M = T * a.K;
+  // ---- A: route
+  for (int t = blockIdx.x * W + warp; t < T; t += gridDim.x * W)
+    rt::route_token<NPL>(t, logits, bias, ids_in, E, a, w_out, id_out, probs, wscale);
+  if (!grid_barrier(&bar[0], status)) return;
+  // ---- B: count
+  int* start = smem;
+  int* offs = smem + E;
+  int* wcnt = smem + 2 * E;
+  for (int c = blockIdx.x; c < C; c += gridDim.x)
+    pm::count_chunk(id_out, M, E, c, offs, counts + (size_t)c * E, status);
+  if (!grid_barrier(&bar[1], status)) return;
+  if ((int)blockIdx.x >= C) return;  // no chunk of its own
+  // ---- C: expert start rows (one thread per expert, E <= blockDim.x)
+  const int tot = tid < E ? column_sum(counts, E, tid, C) : 0;
+  __shared__ int wt[33];
+  int total, n_act;
+  const int first = pm::block_exclusive_scan(tot, wt, &total);
+  const int afirst = pm::block_exclusive_scan(tid < E && tot > 0 ? 1 : 0, wt, &n_act);
+  if (tid < E) {
+    start[tid] = first;
+    if (blockIdx.x == 0) {
+      seg_end[tid] = first + tot;
+      if (tot > 0) active[afirst] = tid;
+    }
+  }
+  if (blockIdx.x == 0 && tid == 0) *num_active = n_act;
+  __syncthreads();
+  // ---- D: this CTA's chunks
+  for (int c = blockIdx.x; c < C; c += gridDim.x) {
+    if (tid < E) offs[tid] = start[tid] + column_sum(counts, E, tid, c);
+    __syncthreads();
+    pm::scatter_chunk(id_out, M, E, c, offs, wcnt, row_to_route, route_to_row);
+  }
+}
+
+template <int NPL>
+cudaError_t launch_npl(const float* logits, const float* bias, const int32_t* ids_in, int T,
+                       int E, const RouteArgs& a, float* w, int32_t* ids, float* probs,
+                       float* wscale, int C, int* counts, int32_t* seg_end, int* active,
+                       int* num_active, int32_t* r2r, int32_t* route_to_row, int* status, int* bar,
+                       size_t smem, int grid, cudaStream_t s) {
+  static std::once_flag attr;
+  std::call_once(attr, [] {
+    cudaFuncSetAttribute(route_permute_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (2 + kFusedWarps) * kFusedWarps * 32 * 4);
+  });
+  return launch_pdl(route_permute_kernel<NPL>, grid, kFusedWarps * 32, smem, s, logits, bias,
+                    ids_in, T, E, a, w, ids, probs, wscale, C, counts, seg_end, active,
+                    num_active, r2r, route_to_row, status, bar);
+}
+
+}  // namespace
+
+bool route_permute_ok(int E) { return E >= 1 && E <= kFusedWarps * 32; }
+
+cudaError_t launch_route_permute(const float* logits, const float* bias, const int32_t* ids_in,
+                                 int T, int E, const moe_route_params& p, float* w, int32_t* ids,
+                                 float* probs, float* wscale, int32_t* seg_end,
+                                 int32_t* row_to_route, int32_t* route_to_row, void* ws,
+                                 cudaStream_t s) {
+  const int K = p.top_k;
+  const int M = T * K;
+  if (M == 0 || !route_permute_ok(E)) return cudaErrorInvalidValue;
+  PermuteWs L(M, E);
+  char* base = static_cast<char*>(ws);
+  int* status = reinterpret_cast<int*>(base);
+  int* bar = reinterpret_cast<int*>(base + 16);  // two barrier counters in the status area
+  int* counts = reinterpret_cast<int*>(base + L.counts);
+  int* active = reinterpret_cast<int*>(base + L.active);
+  int* num_active = reinterpret_cast<int*>(base + L.num_active);
+  const int C = (M + kPermuteChunk - 1) / kPermuteChunk;
+  const int grid = num_sms();
+  const size_t smem = (size_t)(2 + kFusedWarps) * E * 4;
+  cudaError_t e = cudaMemsetAsync(bar, 0, 2 * sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  const RouteArgs a = rt::route_args(p, probs, wscale);
+  const int npl = (E + 31) / 32;
+  auto go = [&](auto tag) {
+    constexpr int N = decltype(tag)::value;
+    return launch_npl<N>(logits, bias, ids_in, T, E, a, w, ids, probs, wscale, C, counts, seg_end,
+                         active, num_active, row_to_route, route_to_row, status, bar, smem, grid,
+                         s);
+  };
+  if (npl <= 1) e = go(std::integral_constant<int, 1>{});
+  else if (npl <= 2) e = go(std::integral_constant<int, 2>{});
+  else if (npl <= 4) e = go(std::integral_constant<int, 4>{});
+  else if (npl <= 8) e = go(std::integral_constant<int, 8>{});
+  else if (npl <= 12) e = go(std::integral_constant<int, 12>{});
+  else e = go(std::integral_constant<int, 16>{});
+  count_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace moe
