@@ -247,6 +247,7 @@ def stage_cost(cfg, D):
         # the index maps only and the gate_up GEMM reads the hidden rows
         # through them (each hidden row counted once)
         "permute_maps": (0.0, M * 4 * 3 + E * 4),
+        "route_permute": (0.0, route + M * 4 * 3 + E * 4),
         "gemm_act": (4.0 * M * H * F, D * 2 * F * H * b + bias1 + M * H * b + M * F * b),
         "gemm_act_gathered": (4.0 * M * H * F, D * 2 * F * H * b + bias1 + T * H * b + M * F * b),
         "gemm_down": (2.0 * M * F * H, D * H * F * b + bias2 + M * F * b + M * H * b),
@@ -382,19 +383,26 @@ def run_ours(args, rank, world, local):
         act_out = torch.empty((T * K, F), dtype=tdt, device=dev)
         y = torch.empty((T * K, H), dtype=tdt, device=dev)
         stage_ws = moe._ws(256, dev)
-        stages = {
-            "route": lambda: moe.moe_route(inp["logits"], p, inp["correction_bias"],
-                                           inp["expert_ids"], topk_weights=tw, topk_ids=ti,
-                                           router_probs=probs, weight_scale=wsc),
-        }
+        # the forward routes and builds the index maps in one launch when it
+        # needs the maps only (gathered gate_up or indexed path, E <= 512)
+        fused_maps = (indexed or gathered) and E <= 512
+        if fused_maps:
+            stages = {"route_permute": lambda: moe.moe_route_permute(
+                inp["logits"], p, inp["correction_bias"], inp["expert_ids"], ws=perm["ws"])}
+        else:
+            stages = {"route": lambda: moe.moe_route(inp["logits"], p, inp["correction_bias"],
+                                                     inp["expert_ids"], topk_weights=tw,
+                                                     topk_ids=ti, router_probs=probs,
+                                                     weight_scale=wsc)}
         if indexed:
             stages["indexed_mlp"] = lambda: moe.moe_indexed_mlp(inp["hidden"], inp["w_gate_up"],
                                                                 inp["w_down"], tw, ti, out=out,
                                                                 ws=ws)
         elif gathered:
+            if not fused_maps:
+                stages["permute"] = lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"],
+                                                            with_gather=False)
             stages.update({
-                "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"],
-                                                   with_gather=False),
                 "gemm_act": lambda: moe.moe_grouped_gemm_act_gathered(
                     inp["hidden"], perm["row_to_route"], K, inp["w_gate_up"], perm["seg_end"], F,
                     a, inp["b_gate_up"], out=act_out, ws=stage_ws),
@@ -538,6 +546,8 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
         "indexed_mlp": lambda: moe.moe_indexed_mlp(inp["hidden"], inp["w_gate_up"], inp["w_down"],
                                                    tw, ti),
         "route": lambda: moe.moe_route(inp["logits"], p, topk_weights=tw, topk_ids=ti),
+        "route_permute": lambda: moe.moe_route_permute(inp["logits"], p, inp["correction_bias"],
+                                                       inp["expert_ids"], ws=perm["ws"]),
         "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"],
                                            with_gather=not gathered),
         "gemm_act": gemm_act,
@@ -594,8 +604,8 @@ def main():
                     help="KEY=VAL[,KEY=VAL] changes to the workload recipe (profiling of "
                          "reduced cases only; the bench line of record uses none)")
     ap.add_argument("--stage", default=None,
-                    choices=["route", "permute", "gemm_act", "gemm_down", "combine",
-                             "indexed_mlp"],
+                    choices=["route", "route_permute", "permute", "gemm_act", "gemm_down",
+                             "combine", "indexed_mlp"],
                     help="time one stage alone (for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

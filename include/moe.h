@@ -138,6 +138,24 @@ moe_status moe_route(const float* logits, const float* correction_bias,
                      float* weight_scale, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* moe_route followed by moe_permute without the gather (expert_input NULL),
+ * in one launch (an addition; the forward uses it whenever it needs the index
+ * maps only).  Outputs are bit-identical to the two calls: topk_weights,
+ * topk_ids, router_probs, weight_scale as moe_route; seg_end, row_to_route,
+ * route_to_row as moe_permute.  E <= 512 (MOE_ERR_UNSUPPORTED above; use the
+ * two calls).  ws: >= moe_permute_workspace_size(T*K, E) bytes whose status
+ * word was cleared (moe_clear_status); the call also uses bytes 16..23 of the
+ * status area.  It runs one CTA per SM that meet at two bounded grid
+ * barriers, so it must not share the GPU with work that holds SMs for
+ * seconds (the barrier would time out and latch MOE_ERR_TIMEOUT). */
+moe_status moe_route_permute(const float* logits, const float* correction_bias,
+                             const int32_t* expert_ids, int T, int E, const moe_route_params* p,
+                             float* topk_weights, int32_t* topk_ids, float* router_probs,
+                             float* weight_scale, int32_t* seg_end, int32_t* row_to_route,
+                             int32_t* route_to_row, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Permute into the tight expert-contiguous layout ("contiguous ·
  * physical_psum": segment END rows) [TileOPs, MoEPrePermuteFwdOp and
  * MoEGroupedGemmFwdOp].

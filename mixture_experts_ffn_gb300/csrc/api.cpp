@@ -146,6 +146,34 @@ moe_status moe_route(const float* logits, const float* correction_bias, const in
                                   topk_ids, router_probs, weight_scale, stream));
 }
 
+moe_status moe_route_permute(const float* logits, const float* correction_bias,
+                             const int32_t* expert_ids, int T, int E, const moe_route_params* p,
+                             float* topk_weights, int32_t* topk_ids, float* router_probs,
+                             float* weight_scale, int32_t* seg_end, int32_t* row_to_route,
+                             int32_t* route_to_row, void* ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+  moe_status st = check_route(logits, correction_bias, T, E, p, topk_weights, topk_ids,
+                              router_probs, weight_scale);
+  if (st != MOE_OK) return st;
+  const long long TKl = (long long)T * p->top_k;
+  if (TKl >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+  if (!seg_end || (T > 0 && (!row_to_route || !route_to_row))) return MOE_ERR_INVALID_ARG;
+  if (!route_permute_ok(E)) return MOE_ERR_UNSUPPORTED;
+  const int M = (int)TKl;
+  if (!ws_ok(ws, ws_bytes, PermuteWs(M, E).total)) return MOE_ERR_WORKSPACE;
+  const size_t TK = (size_t)M, lc = (size_t)p->local_expert_count;
+  Span outs[] = {{topk_weights, TK * 4}, {topk_ids, TK * 4}, {router_probs, T * lc * 4},
+                 {weight_scale, (size_t)T * 4}, {seg_end, (size_t)E * 4},
+                 {row_to_route, TK * 4}, {route_to_row, TK * 4}, {ws, PermuteWs(M, E).total}};
+  Span ins[] = {{logits, (size_t)T * E * 4}, {correction_bias, (size_t)E * 4},
+                {expert_ids, TK * 4}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  if (T == 0) return cuda_status(cudaMemsetAsync(seg_end, 0, (size_t)E * 4, stream));
+  return cuda_status(launch_route_permute(logits, correction_bias, expert_ids, T, E, *p,
+                                          topk_weights, topk_ids, router_probs, weight_scale,
+                                          seg_end, row_to_route, route_to_row, ws, stream));
+}
+
 size_t moe_permute_workspace_size(int M, int E) {
   if (M < 0 || E < 1) return 0;
   return PermuteWs(M, E).total;

@@ -45,6 +45,8 @@ class ActParams(ctypes.Structure):
 _SIGNATURES = {
     "moe_route": [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp],
     "moe_permute": [_vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
+    "moe_route_permute": [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                          _sz, _vp],
     "moe_grouped_gemm_act": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_act_gathered": [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
                                       _vp, _vp, _sz, _vp],
@@ -200,6 +202,34 @@ def moe_permute(topk_ids, E: int, hidden=None, ws=None, with_gather=True):
                                           _p(route_to_row), _p(ws), ws.numel(), _stream()))
     return {"expert_input": xin, "seg_end": seg_end, "row_to_route": r2r,
             "route_to_row": route_to_row, "ws": ws}
+
+
+def moe_route_permute(logits, p: RouteParams, correction_bias=None, expert_ids=None, ws=None):
+    """moe_route then the index maps of moe_permute, in one launch; returns
+    (topk_weights, topk_ids, router_probs, weight_scale, maps) with maps =
+    dict(seg_end, row_to_route, route_to_row, ws)."""
+    lib = load_library()
+    _cuda(logits, correction_bias, expert_ids)
+    T, E = logits.shape
+    K = p.top_k
+    dev = logits.device
+    tw = torch.empty((T, K), dtype=torch.float32, device=dev)
+    ti = torch.empty((T, K), dtype=torch.int32, device=dev)
+    probs = wsc = None
+    if p.local_expert_count > 0:
+        probs = torch.empty((T, p.local_expert_count), dtype=torch.float32, device=dev)
+        wsc = torch.empty((T,), dtype=torch.float32, device=dev)
+    seg_end = torch.empty((E,), dtype=torch.int32, device=dev)
+    r2r = torch.empty((T * K,), dtype=torch.int32, device=dev)
+    route_to_row = torch.empty((T * K,), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = _ws(lib.moe_permute_workspace_size(T * K, E), dev)
+    _check("moe_route_permute",
+           lib.moe_route_permute(_p(logits), _p(correction_bias), _p(expert_ids), T, E,
+                                 ctypes.byref(p), _p(tw), _p(ti), _p(probs), _p(wsc), _p(seg_end),
+                                 _p(r2r), _p(route_to_row), _p(ws), ws.numel(), _stream()))
+    return tw, ti, probs, wsc, {"seg_end": seg_end, "row_to_route": r2r,
+                                "route_to_row": route_to_row, "ws": ws}
 
 
 def moe_grouped_gemm_act(a, w_gate_up, seg_end, F: int, act: ActParams, b_gate_up=None, out=None,

@@ -108,3 +108,67 @@ def test_route_golden_cases_on_gpu(moe):
         if "router_probs" in c:
             np.testing.assert_allclose(np_(probs), np.array(c["router_probs"]), rtol=1e-6)
             np.testing.assert_allclose(np_(wsc), np.array(c["weight_scale"]), rtol=1e-6)
+
+
+def _fused_vs_separate(moe, cfg, inp):
+    p, _ = moe.config_params(cfg)
+    w, ids, probs, wsc, maps = moe.moe_route_permute(inp["logits"], p, inp["correction_bias"],
+                                                     inp["expert_ids"])
+    w2, ids2, probs2, wsc2 = moe.moe_route(inp["logits"], p, inp["correction_bias"],
+                                           inp["expert_ids"])
+    perm = moe.moe_permute(ids2, cfg.E)
+    torch.cuda.synchronize()
+    assert moe.moe_sync_status(maps["ws"]) == moe.MOE_OK
+    assert torch.equal(w, w2) and torch.equal(ids, ids2)
+    if probs is not None:
+        assert torch.equal(probs, probs2) and torch.equal(wsc, wsc2)
+    for k in ("seg_end", "row_to_route", "route_to_row"):
+        assert torch.equal(maps[k], perm[k]), k
+    return ids
+
+
+@pytest.mark.parametrize("name,T", [
+    ("tiny_fp32", 64), ("qwen3_bf16", 4096), ("deepseek_v3_bf16", 8192),
+    ("gpt_oss_bf16", 2048), ("kimi_k2_decode_bf16", 16),
+    ("qwen3_bf16", 1), ("qwen3_bf16", 20000),   # one token; 157 chunks on 152 SMs
+])
+def test_route_permute_fused_matches_separate(moe, name, T):
+    """The one-launch route + index maps equals moe_route then moe_permute bit
+    for bit (ids, weights, MoERouter outputs, seg_end and both maps), and its
+    maps equal the oracle's permutation of the oracle's routing."""
+    cfg = synth.CONFIGS[name].replace(T=T, H=64, F=64)
+    inp, ref = make(cfg)
+    ids = _fused_vs_separate(moe, cfg, inp)
+    r = O.route(ref["logits"], cfg.K, cfg.scoring, cfg.renormalize, cfg.G, cfg.TG, cfg.rsf,
+                ref["correction_bias"], ref["expert_ids"], cfg.local_start, cfg.local_count,
+                cfg.route_scale)
+    np.testing.assert_array_equal(np_(ids), r["topk_ids"])
+
+
+@pytest.mark.parametrize("E", [8, 384, 512])
+def test_route_permute_fused_expert_counts(moe, E):
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=777, E=E, K=min(8, E), H=64, F=64,
+                                              local_count=0)
+    inp, _ = make(cfg)
+    _fused_vs_separate(moe, cfg, inp)
+
+
+def test_route_permute_fused_hash_and_bad_ids(moe):
+    cfg = synth.CONFIGS["kimi_k2_decode_bf16"].replace(hash_ids=True, T=40, H=128, F=256)
+    inp, _ = make(cfg)
+    _fused_vs_separate(moe, cfg, inp)
+    p, _ = moe.config_params(cfg)
+    bad = inp["expert_ids"].clone()
+    bad[3, 2] = cfg.E + 5
+    *_, maps = moe.moe_route_permute(inp["logits"], p, inp["correction_bias"], bad)
+    assert moe.moe_sync_status(maps["ws"]) == moe.MOE_ERR_DEVICE
+    assert int(maps["seg_end"][-1]) == cfg.T * cfg.K - 1  # the bad route got no row
+
+
+def test_route_permute_rejects_large_e(moe):
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=8, E=640, K=8, H=64, F=64, local_count=0)
+    inp, _ = make(cfg)
+    p, _ = moe.config_params(cfg)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_route_permute(inp["logits"], p)
+    assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
