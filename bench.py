@@ -179,6 +179,19 @@ def profile_traffic(kernel: str, srcs):
 
 
 # --------------------------------------------------------------------- reference
+def workload_config(args, cfg, world, **extra):
+    """The `config` object of the JSON line, the same for both arms."""
+    from mixture_experts_ffn_gb300 import synth
+
+    c = {"workload": args.workload, "T": cfg.T, "H": cfg.H, "F": cfg.F, "E": cfg.E, "K": cfg.K,
+         "scoring": cfg.scoring, "renormalize": cfg.renormalize, "groups": [cfg.G, cfg.TG],
+         "rsf": cfg.rsf, "act": ["silu_and_mul", "swiglu", "identity"][cfg.act],
+         "moerouter_slice": [cfg.local_start, cfg.local_count],
+         "parallelism": f"replicas x{world}"}
+    c.update(extra)
+    return c
+
+
 def run_reference(args, rank, world):
     """The CPU oracle, as it stands, on a bounded token sample per step."""
     if rank != 0:
@@ -218,8 +231,8 @@ def run_reference(args, rank, world):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "T": cfg.T, "H": cfg.H, "F": cfg.F, "E": cfg.E,
-                   "K": cfg.K, "sample_tokens_per_step": sample},
+        "config": workload_config(args, cfg, world, path="CPU oracle (numpy float64)",
+                                  sample_tokens_per_step=sample),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{sample} tokens of the {cfg.T}-token workload per step "
                                    f"(all their routes and experts), numpy float64"},
@@ -494,17 +507,12 @@ def run_ours(args, rank, world, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": cfg.dtype, "data": "synthetic",
-            "config": {"workload": args.workload, "T": T, "H": H, "F": F, "E": E, "K": K,
-                       "scoring": cfg.scoring, "renormalize": cfg.renormalize,
-                       "groups": [cfg.G, cfg.TG], "rsf": cfg.rsf,
-                       "act": ["silu_and_mul", "swiglu", "identity"][cfg.act],
-                       "path": "indexed" if indexed else
-                               "gathered gate_up" if gathered else "staged",
-                       "moerouter_slice": [cfg.local_start, cfg.local_count],
-                       "l2": "flushed before every timed step (512 MiB write, then 512 MiB "
-                             "read so no dirty lines are written back inside the step)",
-                       "soak_steps": soak,
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config(
+                args, cfg, world,
+                path="indexed" if indexed else "gathered gate_up" if gathered else "staged",
+                l2="flushed before every timed step (512 MiB write, then 512 MiB read so no "
+                   "dirty lines are written back inside the step)",
+                soak_steps=soak),
             "gpu_launches": launches,
             "launches_per_step": launches // args.steps,
             "status": int(status),
