@@ -12,7 +12,8 @@
  * epilogue (moe_grouped_gemm_act) -> grouped down GEMM (moe_grouped_gemm_down)
  * -> unpermute and weighted combine (moe_combine); or, when the routes are few,
  * the indexed per-route path (moe_indexed_mlp).  moe_ffn_forward runs the whole
- * layer.  Sources are cited per function as (page title, section):
+ * layer, fusing stages where it can (moe_route_permute,
+ * moe_grouped_gemm_act_gathered).  Sources are cited per function as (page title, section):
  *   [TileOPs]    TileOPs "MoE Operators" (one section per op),
  *   [MoERouter]  ONNX Runtime PR #32126 "[CUDA] Add MoERouter and SwiGLU
  *                contrib operators",
@@ -319,6 +320,14 @@ moe_status moe_indexed_mlp(const void* hidden, const void* w_gate_up, const void
  * F % 256 == 0 and hidden and the weights are 16-byte aligned [TileOPs,
  * FusedMoEExpertsFwdOp dispatch rule]; otherwise
  * the staged pipeline permute -> gate_up+act -> down -> combine.
+ * When the gate_up GEMM runs on the tensor cores (bf16, H % 8 == 0,
+ * F % 8 == 0, 16-byte aligned hidden, weights and workspace sections), the
+ * permuted copy of the activations is never materialised: routing and the
+ * index maps take one launch (moe_route_permute, E <= 512) and the gate_up
+ * GEMM reads its rows through row_to_route (moe_grouped_gemm_act_gathered),
+ * so the layer is four launches; the results are the same as the staged
+ * calls'.  Every launch is made with programmatic dependent launch, so each
+ * overlaps the tail of the previous one.
  *
  *   hidden [T, H] dtype;  logits [T, E] f32;  w_gate_up [E, N1, H];
  *   w_down [E, H, F];  correction_bias [E] f32 | NULL;  expert_ids [T, K] | NULL;
