@@ -45,6 +45,26 @@ def dist_env():
     return rank, world, local
 
 
+def reduce_max(x: float) -> float:
+    """x maximised over the ranks of the default process group (x itself when
+    there is none): the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    dev = (torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl"
+           else torch.device("cpu"))
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, slowest_ms: float) -> float:
+    """Whole-job rate: the units every rank processed over the slowest rank's time."""
+    return world * units_per_rank / (slowest_ms / 1e3)
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -378,12 +398,8 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize()
         clk.mark(False)
     status = moe.moe_sync_status(ws)
-    ms = sum(times) / len(times)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T / (ms / 1e3)
+    ms = reduce_max(sum(times) / len(times))
+    value = job_throughput(T, world, ms)
 
     # ---- per-stage breakdown (rank 0), same inputs, each stage timed alone
     breakdown = {}
@@ -478,23 +494,27 @@ def run_ours(args, rank, world, local):
         breakdown["forward_roofline_frac"] = round(t_roof / (ms * 1e-3), 3)
         breakdown["forward_tflops"] = round(fwd_fl / (ms * 1e-3) / 1e12, 1)
 
-        # ---- end to end through the C ABI with host buffers
-        h_host = inp["hidden"].cpu().pin_memory()
-        l_host = inp["logits"].cpu().pin_memory()
-        o_host = torch.empty((T, H), dtype=tdt).pin_memory()
-        p_host, _ = moe.config_params(cfg.replace(local_count=0))
-        ws_h = moe._ws(moe.moe_workspace_size_host(T, H, F, E, K, mdt), dev)
+    # ---- end to end through the C ABI with host buffers, every rank
+    h_host = inp["hidden"].cpu().pin_memory()
+    l_host = inp["logits"].cpu().pin_memory()
+    o_host = torch.empty((T, H), dtype=tdt).pin_memory()
+    p_host, _ = moe.config_params(cfg.replace(local_count=0))
+    ws_h = moe._ws(moe.moe_workspace_size_host(T, H, F, E, K, mdt), dev)
 
-        def fwd_host():
-            moe.moe_ffn_forward_host(h_host, l_host, inp["w_gate_up"], inp["w_down"], p_host, a,
-                                     o_host, ws_h, inp["correction_bias"], inp["expert_ids"],
-                                     inp["b_gate_up"], inp["b_down"])
+    def fwd_host():
+        moe.moe_ffn_forward_host(h_host, l_host, inp["w_gate_up"], inp["w_down"], p_host, a,
+                                 o_host, ws_h, inp["correction_bias"], inp["expert_ids"],
+                                 inp["b_gate_up"], inp["b_down"])
 
-        et, _ = timed(fwd_host, args.steps, args.warmup)
-        e_ms = sum(et) / len(et)
-        eb = 2 if cfg.dtype == "bf16" else 4
-        e2e = {"value": T / (e_ms / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": T * H * eb + T * E * 4, "d2h_bytes_per_step": T * H * eb}
+    if world > 1:
+        dist.barrier()
+    et, _ = timed(fwd_host, args.steps, args.warmup)
+    e_ms = reduce_max(sum(et) / len(et))
+    eb = 2 if cfg.dtype == "bf16" else 4
+    e2e = {"value": job_throughput(T, world, e_ms), "unit": "tokens/s",
+           # bytes of the whole job (every rank copies its own inputs and result)
+           "h2d_bytes_per_step": world * (T * H * eb + T * E * 4),
+           "d2h_bytes_per_step": world * T * H * eb}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
