@@ -147,8 +147,9 @@ moe_status moe_route(const float* logits, const float* correction_bias,
  * two calls).  ws: >= moe_permute_workspace_size(T*K, E) bytes whose status
  * word was cleared (moe_clear_status); the call also uses bytes 16..23 of the
  * status area.  It runs one CTA per SM that meet at two bounded grid
- * barriers, so it must not share the GPU with work that holds SMs for
- * seconds (the barrier would time out and latch MOE_ERR_TIMEOUT). */
+ * barriers; the launch is cooperative, so the grid starts only when all of
+ * its CTAs can be resident (concurrent calls on other streams are safe).  A
+ * barrier that still waits after 2 s latches MOE_ERR_TIMEOUT. */
 moe_status moe_route_permute(const float* logits, const float* correction_bias,
                              const int32_t* expert_ids, int T, int E, const moe_route_params* p,
                              float* topk_weights, int32_t* topk_ids, float* router_probs,

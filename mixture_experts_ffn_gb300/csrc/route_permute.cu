@@ -15,11 +15,12 @@
 // routing code, same chunking, same in-order ranks).
 //
 // The grid barriers spin on two counters in the status area of the
-// workspace, zeroed on the stream before the launch.  All CTAs of the grid
-// are resident together (one per SM, at most one per SM is launched), and
-// every spin is bounded: a barrier that runs out latches the timeout bit and
-// the CTA stops.
+// workspace, zeroed on the stream before the launch.  The launch is
+// cooperative (one CTA per SM), so all CTAs of the grid are resident
+// together, and every spin is bounded: a barrier that runs out latches the
+// timeout bit and the CTA stops.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -131,14 +132,42 @@ cudaError_t launch_npl(const float* logits, const float* bias, const int32_t* id
                        float* wscale, int C, int* counts, int32_t* seg_end, int* active,
                        int* num_active, int32_t* r2r, int32_t* route_to_row, int* status, int* bar,
                        size_t smem, int grid, cudaStream_t s) {
-  static std::once_flag attr;
-  std::call_once(attr, [] {
+  static std::once_flag smem_attr;
+  std::call_once(smem_attr, [] {
     cudaFuncSetAttribute(route_permute_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          (2 + kFusedWarps) * kFusedWarps * 32 * 4);
   });
-  return launch_pdl(route_permute_kernel<NPL>, grid, kFusedWarps * 32, smem, s, logits, bias,
-                    ids_in, T, E, a, w, ids, probs, wscale, C, counts, seg_end, active,
-                    num_active, r2r, route_to_row, status, bar);
+  // A cooperative launch: the scheduler starts the grid only when all of its
+  // CTAs can be resident at once, so two of these kernels running on two
+  // streams never each hold part of the GPU while waiting at a barrier for
+  // CTAs the other one keeps out.  Programmatic serialisation is asked for too
+  // (the kernel waits on the previous grid before it reads anything); a driver
+  // that refuses the pair gets the cooperative launch alone.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kFusedWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  static std::atomic<int> n_attrs{2};
+  cfg.numAttrs = n_attrs.load();
+  cudaError_t e = cudaLaunchKernelEx(&cfg, route_permute_kernel<NPL>, logits, bias, ids_in, T, E,
+                                     a, w, ids, probs, wscale, C, counts, seg_end, active,
+                                     num_active, r2r, route_to_row, status, bar);
+  if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
+    (void)cudaGetLastError();
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, route_permute_kernel<NPL>, logits, bias, ids_in, T, E, a, w, ids,
+                           probs, wscale, C, counts, seg_end, active, num_active, r2r,
+                           route_to_row, status, bar);
+    if (e == cudaSuccess) n_attrs.store(1);
+  }
+  return e;
 }
 
 }  // namespace

@@ -169,3 +169,28 @@ def test_empty_batch(moe):
     p, a = moe.config_params(cfg)
     out = moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a)
     assert out.shape == (0, 128)
+
+
+def test_concurrent_forwards_on_two_streams(moe):
+    """Two forwards enqueued alternately on two streams (each with its own
+    workspace) run concurrently on the GPU: both finish with status OK and
+    give, bit for bit, the output of a forward run alone."""
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=512, H=256, F=128, E=32, K=8, local_count=0)
+    inp, _ = make(cfg)
+    p, a = moe.config_params(cfg)
+    dt = moe.MOE_BF16
+    ref = moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    wss = [torch.zeros(moe.moe_workspace_size(cfg.T, cfg.H, cfg.F, cfg.E, cfg.K, dt),
+                       dtype=torch.uint8, device="cuda") for _ in streams]
+    outs = [torch.empty_like(ref) for _ in streams]
+    for _ in range(40):
+        for s, ws, o in zip(streams, wss, outs):
+            with torch.cuda.stream(s):
+                moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"],
+                                    inp["w_down"], p, a, out=o, ws=ws)
+    torch.cuda.synchronize()
+    for ws, o in zip(wss, outs):
+        assert moe.moe_sync_status(ws) == moe.MOE_OK
+        assert torch.equal(o, ref)
