@@ -321,9 +321,8 @@ def run_ours(args, rank, world, local):
                and cfg.F % 256 == 0)
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
     # the forward reads the gate_up rows through the permutation on the
-    # tensor-core path (bf16, 16-byte rows, not the two-SM kernel)
-    gathered = (not indexed and cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
-                and not os.environ.get("MOE_TC_KERNEL", "").startswith("2"))
+    # tensor-core path (bf16, 16-byte rows)
+    gathered = not indexed and cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
     tdt = synth.torch_dtype(cfg.dtype)
     mdt = moe.MOE_BF16 if cfg.dtype == "bf16" else moe.MOE_F32
     out = torch.empty((T, H), dtype=tdt, device=dev)
@@ -552,8 +551,7 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
 
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
     dev = inp["hidden"].device
-    gathered = (cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
-                and not os.environ.get("MOE_TC_KERNEL", "").startswith("2"))
+    gathered = cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
     p = moe.config_params(cfg.replace(local_count=0))[0]
     tw, ti, _, _ = moe.moe_route(inp["logits"], p, inp["correction_bias"], inp["expert_ids"])
     perm = moe.moe_permute(ti, E, inp["hidden"])

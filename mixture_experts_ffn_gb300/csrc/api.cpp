@@ -240,7 +240,7 @@ moe_status moe_grouped_gemm_act_gathered(const void* hidden, int T, const int32_
                 {w_gate_up, (size_t)E * N1 * H * 2}, {b_gate_up, b_gate_up ? (size_t)E * N1 * 2 : 0},
                 {seg_end, (size_t)E * 4}, {ws, MOE_STATUS_BYTES}};
   if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
-  if (dtype != MOE_BF16 || !tc_ok(hidden, w_gate_up, out, F, H, M) || !gemm_tc_can_gather())
+  if (dtype != MOE_BF16 || !tc_ok(hidden, w_gate_up, out, F, H, M))
     return MOE_ERR_UNSUPPORTED;
   if (M == 0) return MOE_OK;
   return cuda_status(launch_gemm_tc(hidden, w_gate_up, b_gate_up, seg_end, M, F, H, E, act, out,
@@ -376,7 +376,7 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   // builds the index maps and the permuted copy of the activations is never
   // written or read back.
   const bool fused_gather = !indexed && dtype == MOE_BF16 &&
-                            tc_ok(hidden, w_gate_up, a1, F, H, (int)M) && gemm_tc_can_gather();
+                            tc_ok(hidden, w_gate_up, a1, F, H, (int)M);
   // When only the index maps are needed, routing and the maps take one launch.
   const bool fused_maps = (indexed || fused_gather) && route_permute_ok(E);
   cudaError_t err =

@@ -49,17 +49,20 @@ __device__ __forceinline__ float gated(float g, float u, float limit, float alph
   }
 }
 
-// Epilogue of one 128-lane x 256-column accumulator for the 32 rows of the
-// calling warp (TMEM lanes 32*(warp%4).., row wrow0 + lane): bias, activation,
-// bf16 rounding and the store.  Rows at or past m_end (the end of the tile's
-// expert segment) are not written.
+// Epilogue of nchunks x 32 output columns for the 32 rows of the calling
+// warp (TMEM lanes 32*(warp%4).., row wrow0 + lane), starting at output (or,
+// gated, activation) column col_base: bias, activation, bf16 rounding and the
+// store.  TMEM column layout from tbase: plain, chunk c at 32c; stacked, gate
+// at 32c and up at up_off + 32c; interleaved, (gate, up) pairs at 64c.  Rows
+// at or past m_end (the end of the tile's expert segment) are not written.
 template <int MODE, int ACT>
-__device__ __forceinline__ void drain_acc(uint32_t tbase, int wrow0, int m_end, int n_idx, int e,
-                                          const __nv_bfloat16* __restrict__ bias, int N1, int Nout,
-                                          float limit, float alpha, float beta,
-                                          const CUtensorMap* tm_out, int tma_out,
-                                          __nv_bfloat16* __restrict__ out, uint8_t* obufs,
-                                          int& obuf, int lane) {
+__device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end, int col_base,
+                                           int nchunks, int up_off, int e,
+                                           const __nv_bfloat16* __restrict__ bias, int N1,
+                                           int Nout, float limit, float alpha, float beta,
+                                           const CUtensorMap* tm_out, int tma_out,
+                                           __nv_bfloat16* __restrict__ out, uint8_t* obufs,
+                                           int& obuf, int lane) {
   const int row = wrow0 + lane;
   const bool row_ok = row < m_end;
   const __nv_bfloat16* be = bias ? bias + (size_t)e * N1 : nullptr;
@@ -96,10 +99,9 @@ __device__ __forceinline__ void drain_acc(uint32_t tbase, int wrow0, int m_end, 
     }
   };
   if constexpr (MODE == kTcPlain) {
-    const int n0 = n_idx * kEpiCols;
 #pragma unroll 1
-    for (int c = 0; c < kEpiCols / 32; ++c) {
-      const int col0 = n0 + c * 32;
+    for (int c = 0; c < nchunks; ++c) {
+      const int col0 = col_base + c * 32;
       if (col0 >= Nout) break;  // warp-uniform
       uint32_t r[32];
       tmem_ld32(tbase + c * 32, r);
@@ -115,15 +117,14 @@ __device__ __forceinline__ void drain_acc(uint32_t tbase, int wrow0, int m_end, 
       emit(v, col0);
     }
   } else {
-    const int j0 = n_idx * (kEpiCols / 2);
 #pragma unroll 1
-    for (int c = 0; c < kEpiCols / 64; ++c) {
-      const int col0 = j0 + c * 32;  // activation column
+    for (int c = 0; c < nchunks; ++c) {
+      const int col0 = col_base + c * 32;  // activation column
       if (col0 >= Nout) break;
       uint32_t g[32], u[32];
       if constexpr (MODE == kTcStacked) {
-        tmem_ld32(tbase + c * 32, g);             // gate columns
-        tmem_ld32(tbase + kEpiCols / 2 + c * 32, u);    // up columns
+        tmem_ld32(tbase + c * 32, g);           // gate columns
+        tmem_ld32(tbase + up_off + c * 32, u);  // up columns
       } else {
         tmem_ld32(tbase + c * 64, g);             // (gate, up) pairs
         tmem_ld32(tbase + c * 64 + 32, u);
@@ -157,6 +158,25 @@ __device__ __forceinline__ void drain_acc(uint32_t tbase, int wrow0, int m_end, 
       emit(v, col0);
     }
   }
+}
+
+// The whole 128-lane x 256-column accumulator of a tile: 256 output columns
+// (plain) or 128 activation columns (gated, up columns 128 to the right when
+// stacked) of column tile n_idx.
+template <int MODE, int ACT>
+__device__ __forceinline__ void drain_acc(uint32_t tbase, int wrow0, int m_end, int n_idx, int e,
+                                          const __nv_bfloat16* __restrict__ bias, int N1, int Nout,
+                                          float limit, float alpha, float beta,
+                                          const CUtensorMap* tm_out, int tma_out,
+                                          __nv_bfloat16* __restrict__ out, uint8_t* obufs,
+                                          int& obuf, int lane) {
+  if constexpr (MODE == kTcPlain)
+    drain_cols<MODE, ACT>(tbase, wrow0, m_end, n_idx * kEpiCols, kEpiCols / 32, 0, e, bias, N1,
+                          Nout, limit, alpha, beta, tm_out, tma_out, out, obufs, obuf, lane);
+  else
+    drain_cols<MODE, ACT>(tbase, wrow0, m_end, n_idx * (kEpiCols / 2), kEpiCols / 64,
+                          kEpiCols / 2, e, bias, N1, Nout, limit, alpha, beta, tm_out, tma_out,
+                          out, obufs, obuf, lane);
 }
 
 }  // namespace tc

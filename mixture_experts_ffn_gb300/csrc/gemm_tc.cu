@@ -327,11 +327,6 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
 // ------------------------------------------------------------ host side
 }  // namespace
 
-bool gemm_tc_can_gather() {
-  const char* v = getenv("MOE_TC_KERNEL");
-  return !(v && v[0] == '2');
-}
-
 cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s, const int32_t* gather_rows,
@@ -347,10 +342,9 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     return v && v[0] == '2';
   }();
   const bool gather = gather_rows != nullptr;
-  if (two_sm && num_sms() >= 2) {
-    if (gather) return cudaErrorNotSupported;  // callers check gemm_tc_can_gather()
-    return launch_gemm_tc2(a, w, bias, seg_end, M, N, K, E, act, out, status, s);
-  }
+  if (two_sm && num_sms() >= 2)
+    return launch_gemm_tc2(a, w, bias, seg_end, M, N, K, E, act, out, status, s, gather_rows,
+                           gather_div, gather_src_rows);
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
   if (act && act->kind != MOE_ACT_IDENTITY) {

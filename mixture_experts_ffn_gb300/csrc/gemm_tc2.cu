@@ -28,6 +28,7 @@
 #include <algorithm>
 #include <cstdlib>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "gemm_epilogue.cuh"
@@ -41,6 +42,7 @@ using namespace tc;
 
 constexpr int BMP = 256;                        // rows per CTA pair
 constexpr int BMC = 128;                        // rows per CTA
+constexpr int BMS = 64;                         // rows per CTA of a short (128-row) pair tile
 constexpr int BN = 256;                         // accumulator columns
 constexpr int BK = 64;
 constexpr int STAGES = 6;
@@ -49,10 +51,19 @@ constexpr int BH_BYTES = (BN / 2) * BK * 2;     // 16 KB: this CTA's half of B
 constexpr int STAGE_BYTES = A_BYTES + BH_BYTES; // 32 KB
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
+// Gathered-row mode: four more warps per CTA copy the CTA's A rows from the
+// token-ordered hidden states through the permutation with cp.async (as in
+// the one-SM kernel).  Their completions can only arrive on a barrier of
+// their own CTA, so in the peer they arrive on afull and warp 1 of the peer
+// (idle otherwise) forwards each completed stage to the leader's full barrier.
+constexpr int NUM_THREADS_GATHER = NUM_THREADS + 128;
+constexpr int kLoaderWarp0 = NUM_THREADS / 32;
 constexpr uint32_t kIdesc2 = idesc_bf16(BMP, BN);
+constexpr uint32_t kIdesc2s = idesc_bf16(2 * BMS, BN);
 
 struct Tc2Shared {
   uint64_t full[STAGES];   // leader: both CTAs' copies of a stage complete here
+  uint64_t afull[STAGES];  // peer, gathered rows: the peer's A copies of a stage
   uint64_t empty[STAGES];  // both: the leader's MMA commit frees the stage
   uint64_t tfull[2];       // both: accumulator ready
   uint64_t tempty[2];      // leader: both epilogues have drained the accumulator
@@ -90,6 +101,10 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                : "memory");
 }
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
 // TMA load into this CTA's shared memory, completing on a barrier of either
 // CTA of the pair (shared::cluster address)
 __device__ __forceinline__ void tma2_2d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
@@ -116,17 +131,9 @@ __device__ __forceinline__ void tma2_4d(void* dst, const CUtensorMap* m, uint32_
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
-__device__ __forceinline__ void umma2(uint32_t d_tmem, uint64_t ad, uint64_t bd, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(ad), "l"(bd), "r"(kIdesc2), "r"(acc)
-      : "memory");
-}
 // the four K16 MMAs of a k-block plus the commit that frees the stage in both CTAs
 __device__ __forceinline__ void umma2_kblock(uint32_t d_tmem, uint64_t ad, uint64_t bd,
-                                             uint32_t accumulate, uint32_t bar) {
+                                             uint32_t idesc, uint32_t accumulate, uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred p, t;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -137,7 +144,7 @@ __device__ __forceinline__ void umma2_kblock(uint32_t d_tmem, uint64_t ad, uint6
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %10, %11, %3, t;\n\t"
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%5], %12;\n\t}" ::"r"(d_tmem),
-      "l"(ad), "l"(bd), "r"(kIdesc2), "r"(accumulate), "r"(bar), "l"(ad + 2), "l"(bd + 2),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate), "r"(bar), "l"(ad + 2), "l"(bd + 2),
       "l"(ad + 4), "l"(bd + 4), "l"(ad + 6), "l"(bd + 6), "h"((uint16_t)3)
       : "memory");
 }
@@ -157,14 +164,20 @@ __device__ __forceinline__ void umma2_commit_self(uint64_t* bar) {
       : "memory");
 }
 
-template <int MODE, int ACT>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// GATHER: row r of A is row grows[r] / gdiv of gsrc (the hidden states, gsrc_rows
+// rows; grows is row_to_route, gdiv = top_k); tm_a and tm_a_s are unused.
+template <int MODE, int ACT, bool GATHER>
+__global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b,
+                    const __grid_constant__ CUtensorMap tm_a_s,
+                    const __grid_constant__ CUtensorMap tm_b_s,
                     const __nv_bfloat16* __restrict__ bias, const int32_t* __restrict__ seg_end,
                     int M, int Nout, int N1, int K, int E, float limit, float alpha, float beta,
                     const __grid_constant__ CUtensorMap tm_out, int tma_out,
-                    __nv_bfloat16* __restrict__ out, int* status) {
+                    __nv_bfloat16* __restrict__ out, int* status,
+                    const __nv_bfloat16* __restrict__ gsrc, const int32_t* __restrict__ grows,
+                    int gdiv, int gsrc_rows) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -177,7 +190,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sh->full[s], 1);
+      // the leader's expect-tx arrival; gathered rows: plus one per leader
+      // A-loader thread and the peer's forwarded arrival
+      mbar_init(&sh->full[s], GATHER ? 1 + 128 + 1 : 1);
+      mbar_init(&sh->afull[s], 128);
       mbar_init(&sh->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -191,6 +207,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a_s)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b_s)) : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -221,19 +239,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       for (int tile = pair; tile < total && ok; tile += npairs) {
         const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
+        const bool tall = st.m_end - st.m0 > BMC;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
           uint8_t* a_dst = smem + (size_t)stage * STAGE_BYTES;
           uint8_t* b_dst = a_dst + A_BYTES;
-          if (leader) mbar_expect_tx(&sh->full[stage], 2 * STAGE_BYTES);
+          if (leader) {  // A comes from the loader warps in gather mode
+            const int a_bytes = GATHER ? 0 : tall ? A_BYTES : A_BYTES / 2;
+            mbar_expect_tx(&sh->full[stage], 2 * (a_bytes + BH_BYTES));
+          }
           const uint32_t bar = map_to_rank(su32(&sh->full[stage]), 0);
           const int k0 = kb * BK;
-          tma2_2d(a_dst, &tm_a, bar, k0, st.m0 + BMC * (int)rank);
-          if constexpr (MODE == kTcStacked) {
-            tma2_4d(b_dst, &tm_b, bar, k0, st.n_idx * (BN / 2), (int)rank, st.e);
+          if (tall) {
+            if constexpr (!GATHER) tma2_2d(a_dst, &tm_a, bar, k0, st.m0 + BMC * (int)rank);
+            if constexpr (MODE == kTcStacked)
+              tma2_4d(b_dst, &tm_b, bar, k0, st.n_idx * (BN / 2), (int)rank, st.e);
           } else {
-            tma2_3d(b_dst, &tm_b, bar, k0, st.n_idx * BN + (BN / 2) * (int)rank, st.e);
+            // short tile: 64 rows per CTA; a stacked B half holds the gate
+            // and the up rows of this CTA's 64 activation columns
+            if constexpr (!GATHER) tma2_2d(a_dst, &tm_a_s, bar, k0, st.m0 + BMS * (int)rank);
+            if constexpr (MODE == kTcStacked)
+              tma2_4d(b_dst, &tm_b_s, bar, k0, st.n_idx * (BN / 2) + BMS * (int)rank, 0, st.e);
           }
+          if constexpr (MODE != kTcStacked)
+            tma2_3d(b_dst, &tm_b, bar, k0, st.n_idx * BN + (BN / 2) * (int)rank, st.e);
           ++issued[stage];
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -254,14 +283,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t empty_addr[STAGES];
       for (int s = 0; s < STAGES; ++s) empty_addr[s] = su32(&sh->empty[s]);
       for (int tile = pair; tile < total && ok; tile += npairs) {
+        const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
+        const uint32_t idesc = st.m_end - st.m0 > BMC ? kIdesc2 : kIdesc2s;
         if (!wait_fast(&sh->tempty[acc], aphase ^ 1u, abort_flag, status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_fast(&sh->full[stage], phase, abort_flag, status)) { ok = false; break; }
+          // the leader's A rows were written by cp.async through the generic
+          // proxy; tcgen05.mma reads them through the async proxy (the peer's
+          // forwarder fences its own CTA's rows)
+          if constexpr (GATHER) fence_proxy_async_smem();
           tc_fence_after();
           const uint64_t off = (uint64_t)((stage * STAGE_BYTES) >> 4);
-          umma2_kblock(d_tmem, adesc0 + off, bdesc0 + off, kb != 0 ? 1u : 0u, empty_addr[stage]);
+          umma2_kblock(d_tmem, adesc0 + off, bdesc0 + off, idesc, kb != 0 ? 1u : 0u,
+                       empty_addr[stage]);
           any = true;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -274,6 +310,82 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         drain_wait(&sh->drain, 0);
       }
     }
+    if constexpr (GATHER) {
+      if (lane == 0 && !leader) {
+        // ---------------------------------------------- forwarder (peer)
+        int stage = 0;
+        uint32_t phase = 0;
+        const uint32_t full_remote0 = map_to_rank(su32(&sh->full[0]), 0);
+        bool ok = true;
+        for (int tile = pair; tile < total && ok; tile += npairs) {
+          for (int kb = 0; kb < nkb; ++kb) {
+            if (!wait_fast(&sh->afull[stage], phase, abort_flag, status)) { ok = false; break; }
+            // This CTA's A rows are read by this CTA's own tensor core when the
+            // leader's MMAs run: order them for the async proxy here, and
+            // release at CTA scope only (a cluster-scope release waits for the
+            // SM's copies in flight and serialises the ring).
+            fence_proxy_async_smem();
+            mbar_arrive_remote_cta(full_remote0 + (uint32_t)(stage * sizeof(uint64_t)));
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+    }
+  } else if (GATHER && warp >= kLoaderWarp0) {
+    // ------------------------------------------------ A loaders (gather mode)
+    // 128 threads copy this CTA's 128 (64 in a short tile) rows x 128 bytes
+    // of a k-block: thread lt owns 16-byte chunk lt % 8 of rows lt / 8 + 16 i,
+    // in the 128-byte swizzle of the TMA boxes (chunk ch of row r at chunk
+    // ch ^ (r % 8)); rows outside the tile's segment are zero-filled.
+    const int lt = threadIdx.x - kLoaderWarp0 * 32;
+    const int ch = lt & 7, r0 = lt >> 3;
+    const uint32_t dst0 = (uint32_t)(r0 * 128 + ((ch ^ (r0 & 7)) << 4));
+    uint64_t* arrive_bar = leader ? sh->full : sh->afull;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    constexpr int kRows = BMC / 16;  // rows per loader thread in a 256-row pair tile
+    for (int tile = pair; tile < total && ok; tile += npairs) {
+      const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
+      const bool tall = st.m_end - st.m0 > BMC;
+      const int rbase = st.m0 + (tall ? BMC : BMS) * (int)rank;
+      const int nrows = tall ? kRows : kRows / 2;
+      const __nv_bfloat16* src[kRows];
+      uint32_t valid = 0;
+#pragma unroll
+      for (int i = 0; i < kRows; ++i) {
+        // only rows of the tile's own segment are read (the map holds defined
+        // entries below seg_end[E-1] only)
+        const int row = rbase + r0 + 16 * i;
+        const int rt = i < nrows && row < st.m_end ? grows[row] : -1;
+        int t = 0;
+        if (rt >= 0 && rt / gdiv < gsrc_rows) {
+          t = rt / gdiv;
+          valid |= 1u << i;
+        }
+        src[i] = gsrc + (size_t)t * K + ch * 8;
+      }
+      for (int kb = 0; kb < nkb; ++kb) {
+        if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
+        const uint32_t a_dst = su32(smem + (size_t)stage * STAGE_BYTES) + dst0;
+        const int k0 = kb * BK;
+        const bool kin = k0 + ch * 8 < K;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+          if (i >= nrows) break;
+          const bool v = kin && ((valid >> i) & 1u);
+          asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(a_dst + i * 16 * 128),
+                       "l"(v ? src[i] + k0 : gsrc), "r"(v ? 16 : 0)
+                       : "memory");
+        }
+        // arrives on this CTA's stage barrier once this thread's copies land
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                         su32(&arrive_bar[stage]))
+                     : "memory");
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // nothing in flight at exit
   } else {
     // ------------------------------------------------ epilogue (both CTAs)
     const int quad = warp & 3;
@@ -287,10 +399,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
       if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
       tc_fence_after();
-      drain_acc<MODE, ACT>(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN),
-                           st.m0 + BMC * (int)rank + quad * 32, st.m_end, st.n_idx, st.e, bias,
-                           N1, Nout, limit, alpha, beta, &tm_out, tma_out, out, obufs, obuf,
-                           lane);
+      const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+      if (st.m_end - st.m0 > BMC) {
+        drain_acc<MODE, ACT>(tbase, st.m0 + BMC * (int)rank + quad * 32, st.m_end, st.n_idx,
+                             st.e, bias, N1, Nout, limit, alpha, beta, &tm_out, tma_out, out,
+                             obufs, obuf, lane);
+      } else {
+        // short tile (M128 over the pair): TMEM lane 64h + r holds row
+        // 64 * rank + r with accumulator columns 128h.. in columns 0..127
+        const int wrow0 = st.m0 + BMS * (int)rank + 32 * (quad & 1);
+        const int h = quad >> 1;
+        if (wrow0 < st.m_end) {  // warp-uniform
+          if constexpr (MODE == kTcPlain)
+            drain_cols<MODE, ACT>(tbase, wrow0, st.m_end, st.n_idx * BN + (BN / 2) * h,
+                                  BN / 2 / 32, 0, st.e, bias, N1, Nout, limit, alpha, beta,
+                                  &tm_out, tma_out, out, obufs, obuf, lane);
+          else
+            drain_cols<MODE, ACT>(tbase, wrow0, st.m_end, st.n_idx * (BN / 2) + BMS * h,
+                                  BMS / 32, BMS, st.e, bias, N1, Nout, limit, alpha, beta,
+                                  &tm_out, tma_out, out, obufs, obuf, lane);
+        }
+      }
       tc_fence_before();
       mbar_arrive_remote(tempty_remote[acc]);
       if (++acc == 2) { acc = 0; aphase ^= 1u; }
@@ -313,7 +442,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
                             const int32_t* seg_end, int M, int N, int K, int E,
-                            const moe_act_params* act, void* out, int* status, cudaStream_t s) {
+                            const moe_act_params* act, void* out, int* status, cudaStream_t s,
+                            const int32_t* gather_rows, int gather_div, int gather_src_rows) {
   if (M == 0 || N == 0) return cudaSuccess;
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
@@ -325,30 +455,44 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
     alpha = act->alpha;
     beta = act->beta;
   }
-  CUtensorMap ma, mb;
-  {
+  // ma / mb: 128 A rows and one 128-row half of B per CTA (256-row pair
+  // tiles); ma_s / mb_s: 64 A rows, and for stacked weights 64 gate rows then
+  // the 64 matching up rows (128-row pair tiles)
+  const bool gather = gather_rows != nullptr;
+  CUtensorMap ma, mb, ma_s, mb_s;
+  if (!gather) {  // (gathered rows of A are loaded without a tensor map)
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {BK, BMC};
     if (!tmap::encode_bf16(&ma, a, 2, dims, str, box)) return cudaErrorInvalidValue;
+    cuuint32_t box_s[2] = {BK, BMS};
+    if (!tmap::encode_bf16(&ma_s, a, 2, dims, str, box_s)) return cudaErrorInvalidValue;
   }
   if (mode == kTcStacked) {
     cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)N, 2, (cuuint64_t)E};
     cuuint64_t str[3] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2, (cuuint64_t)2 * N * K * 2};
     cuuint32_t box[4] = {BK, BN / 2, 1, 1};
     if (!tmap::encode_bf16(&mb, w, 4, dims, str, box)) return cudaErrorInvalidValue;
+    cuuint32_t box_s[4] = {BK, BMS, 2, 1};
+    if (!tmap::encode_bf16(&mb_s, w, 4, dims, str, box_s)) return cudaErrorInvalidValue;
   } else {
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N1, (cuuint64_t)E};
     cuuint64_t str[2] = {(cuuint64_t)K * 2, (cuuint64_t)N1 * K * 2};
     cuuint32_t box[3] = {BK, BN / 2, 1};
     if (!tmap::encode_bf16(&mb, w, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
+  if (mode != kTcStacked) mb_s = mb;  // unused
+  if (gather) ma = ma_s = mb;           // unused
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
-    for (const void* fn : {(const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY>,
-                           (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>,
-                           (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU>,
-                           (const void*)gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU>})
+    for (const void* fn : {(const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY, false>,
+                           (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, false>,
+                           (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU, false>,
+                           (const void*)gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU, false>,
+                           (const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY, true>,
+                           (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, true>,
+                           (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU, true>,
+                           (const void*)gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU, true>})
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   });
   // output map for the staged TMA stores (rows stored directly when the
@@ -361,14 +505,14 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
     cuuint32_t box[2] = {OUT_BOX, OUT_BOX};
     tma_out = tmap::encode_bf16(&mo, out, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
   }
-  if (!tma_out) mo = ma;  // unused
+  if (!tma_out) mo = mb;  // unused
   const int n_tiles = mode == kTcPlain ? (N + BN - 1) / BN : (N + BN / 2 - 1) / (BN / 2);
   const long long max_tiles = (long long)((M + BMP - 1) / BMP + E) * n_tiles;
   const int pairs = (int)std::max<long long>(1, std::min<long long>(max_tiles, num_sms() / 2));
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.blockDim = dim3(gather ? NUM_THREADS_GATHER : NUM_THREADS);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -380,13 +524,20 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  auto* kern = mode == kTcPlain       ? gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY>
-               : mode == kTcInterleaved ? gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU>
-               : kind == MOE_ACT_SWIGLU ? gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU>
-                                        : gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL>;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, static_cast<const __nv_bfloat16*>(bias),
+  auto pick = [&](auto g) {
+    constexpr bool G = decltype(g)::value;
+    return mode == kTcPlain       ? gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY, G>
+           : mode == kTcInterleaved ? gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU, G>
+           : kind == MOE_ACT_SWIGLU ? gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU, G>
+                                    : gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, G>;
+  };
+  auto* kern = gather ? pick(std::true_type{}) : pick(std::false_type{});
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ma, mb, ma_s, mb_s,
+                                     static_cast<const __nv_bfloat16*>(bias),
                                      seg_end, M, N, N1, K, E, limit, alpha, beta, mo, tma_out,
-                                     static_cast<__nv_bfloat16*>(out), status);
+                                     static_cast<__nv_bfloat16*>(out), status,
+                                     static_cast<const __nv_bfloat16*>(a), gather_rows,
+                                     gather_div, gather_src_rows);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -116,18 +116,17 @@ cudaError_t launch_gemm_simt(const void* a, const void* w, const void* bias,
 // gather_rows, row r of A is row gather_rows[r] / gather_div of `a` (the
 // token-ordered hidden states, gather_src_rows rows, read through row_to_route
 // so the permuted copy is never materialised); only rows inside their expert's
-// segment are read.  gemm_tc_can_gather() says whether the kernel in use
-// supports it.
+// segment are read.
 cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s, const int32_t* gather_rows = nullptr,
                            int gather_div = 1, int gather_src_rows = 0);
-bool gemm_tc_can_gather();
 
 // two-SM (cta_group::2) variant of launch_gemm_tc, same contract
 cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
                             const int32_t* seg_end, int M, int N, int K, int E,
-                            const moe_act_params* act, void* out, int* status, cudaStream_t s);
+                            const moe_act_params* act, void* out, int* status, cudaStream_t s,
+                            const int32_t* gather_rows, int gather_div, int gather_src_rows);
 
 // indexed per-route decode path (bf16, silu_and_mul, no bias)
 cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, const float* w,

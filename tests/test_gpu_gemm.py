@@ -143,13 +143,12 @@ def test_gemm_act_large_sampled(moe):
     (97, 8, 16, 128, 64, "silu", True),      # ragged segments, some experts empty
     (1, 1, 3, 64, 8, "silu", False),         # one route
     (513, 2, 4, 200, 96, "swiglu_noclamp", False),  # long segments, ragged k-block
+    (1200, 2, 4, 256, 128, "silu", True),    # ~600-row segments: several 256-row tiles
 ])
 def test_gemm_act_gathered(moe, T, K, E, H, F, act, bias):
     """The gate_up GEMM reading its rows through row_to_route from the
     token-ordered hidden states equals the GEMM on the permuted copy bit for
     bit, and the oracle on the rows the oracle's own permutation selects."""
-    if os.environ.get("MOE_TC_KERNEL", "").startswith("2"):
-        pytest.skip("the two-SM kernel has no gathered-row mode")
     assert K <= E, "top-k ids are distinct experts"
     spec = ACTS[act]
     N1 = 2 * F

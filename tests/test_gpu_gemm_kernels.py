@@ -1,10 +1,7 @@
 """The alternative tcgen05 grouped-GEMM kernel -- two-SM cta_group::2 tiles with
 the shared staged-store epilogue, selected with MOE_TC_KERNEL=2sm -- runs the
-whole grouped-GEMM parity file and the small whole-forward cases in a fresh
-process (the switch is read once per process).  That kernel has no
-gathered-row mode, so under it the forward also takes the staged route
-(permuted copy of the activations, then the grouped GEMM), which the default
-forward replaces with the gathered gate_up GEMM."""
+whole grouped-GEMM parity file (gathered rows included) and the small
+whole-forward cases in a fresh process (the switch is read once per process)."""
 import os
 import subprocess
 import sys
