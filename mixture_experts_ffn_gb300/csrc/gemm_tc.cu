@@ -333,10 +333,10 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            int gather_div, int gather_src_rows) {
   if (M == 0 || N == 0) return cudaSuccess;
   // The two-SM (cta_group::2) kernel with MOE_TC_KERNEL=2sm.  Its SMs load a
-  // third fewer bytes per MMA, which wins on long uniform segments, but its
-  // 256-row pair tiles pad ragged expert segments (a tail of a few rows costs
-  // a whole pair tile), and on the routed workloads measured it is level or
-  // slower, so it is not the default.
+  // third fewer bytes per MMA on 256-row pair tiles, but on the routed
+  // workloads measured it is level with this kernel or slower (short
+  // segments, and its gathered mode forwards the peer's row copies through a
+  // second barrier), so it is not the default.
   static const bool two_sm = [] {
     const char* v = getenv("MOE_TC_KERNEL");
     return v && v[0] == '2';
