@@ -145,7 +145,7 @@ moe_status moe_route(const float* logits, const float* correction_bias,
  * topk_ids, router_probs, weight_scale as moe_route; seg_end, row_to_route,
  * route_to_row as moe_permute.  E <= 512 (MOE_ERR_UNSUPPORTED above; use the
  * two calls).  ws: >= moe_permute_workspace_size(T*K, E) bytes whose status
- * word was cleared (moe_clear_status); the call also uses bytes 16..23 of the
+ * word was cleared (moe_clear_status); the call also uses bytes 16..27 of the
  * status area.  It runs one CTA per SM that meet at two bounded grid
  * barriers; the launch is cooperative, so the grid starts only when all of
  * its CTAs can be resident (concurrent calls on other streams are safe).  A
@@ -371,7 +371,10 @@ size_t moe_workspace_size_host(int T, int H, int F, int E, int K, moe_dtype dtyp
 /* Sizes and status.  (The workspace query plays the role of the peak-memory
  * query of [ORT-MoE].) */
 
-/* Bytes at the start of every workspace that hold the device status word. */
+/* Bytes at the start of every workspace that hold the device status word
+ * (and the grid-barrier counters of the fused route + permute launch, which
+ * reset themselves after every successful launch).  Clear them with
+ * moe_clear_status before a workspace's first use and after an error. */
 #define MOE_STATUS_BYTES 256
 
 /* Workspace bytes moe_ffn_forward / moe_indexed_mlp need for these extents. */

@@ -15,10 +15,14 @@
 // routing code, same chunking, same in-order ranks).
 //
 // The grid barriers spin on two counters in the status area of the
-// workspace, zeroed on the stream before the launch.  The launch is
-// cooperative (one CTA per SM), so all CTAs of the grid are resident
-// together, and every spin is bounded: a barrier that runs out latches the
-// timeout bit and the CTA stops.
+// workspace (zero when the status area is cleared) and reset them for the
+// next launch: a third counter counts the CTAs past the second barrier, and
+// the last one zeroes all three (no CTA reads them again in this launch; the
+// next launch reads them after the grids in between have completed).  The
+// launch is cooperative (one CTA per SM), so all CTAs of the grid are
+// resident together, and every spin is bounded: a barrier that runs out
+// latches the timeout bit and the CTA stops, leaving the counters for the
+// status clear that the error requires.
 #include <algorithm>
 #include <atomic>
 #include <mutex>
@@ -102,6 +106,12 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
   for (int c = blockIdx.x; c < C; c += gridDim.x)
     pm::count_chunk(id_out, M, E, c, offs, counts + (size_t)c * E, status);
   if (!grid_barrier(&bar[1], status)) return;
+  if (threadIdx.x == 0 && atomicAdd(&bar[2], 1) == (int)gridDim.x - 1) {
+    // every CTA is past both barriers: ready for the next launch
+    bar[0] = 0;
+    bar[1] = 0;
+    bar[2] = 0;
+  }
   if ((int)blockIdx.x >= C) return;  // no chunk of its own
   // ---- C: expert start rows (one thread per expert, E <= blockDim.x)
   const int tot = tid < E ? column_sum(counts, E, tid, C) : 0;
@@ -185,15 +195,14 @@ cudaError_t launch_route_permute(const float* logits, const float* bias, const i
   PermuteWs L(M, E);
   char* base = static_cast<char*>(ws);
   int* status = reinterpret_cast<int*>(base);
-  int* bar = reinterpret_cast<int*>(base + 16);  // two barrier counters in the status area
+  int* bar = reinterpret_cast<int*>(base + 16);  // barrier counters in the status area
   int* counts = reinterpret_cast<int*>(base + L.counts);
   int* active = reinterpret_cast<int*>(base + L.active);
   int* num_active = reinterpret_cast<int*>(base + L.num_active);
   const int C = (M + kPermuteChunk - 1) / kPermuteChunk;
   const int grid = num_sms();
   const size_t smem = (size_t)(2 + kFusedWarps) * E * 4;
-  cudaError_t e = cudaMemsetAsync(bar, 0, 2 * sizeof(int), s);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
   const RouteArgs a = rt::route_args(p, probs, wscale);
   const int npl = (E + 31) / 32;
   auto go = [&](auto tag) {

@@ -165,6 +165,24 @@ def test_route_permute_fused_hash_and_bad_ids(moe):
     assert int(maps["seg_end"][-1]) == cfg.T * cfg.K - 1  # the bad route got no row
 
 
+def test_route_permute_reuses_workspace(moe):
+    """The grid-barrier counters reset themselves: launches back to back on one
+    workspace (no status clear between them) give the same maps, and leave
+    the counters (status bytes 16..27) at zero."""
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=3000, H=64, F=64)
+    inp, _ = make(cfg)
+    p, _ = moe.config_params(cfg)
+    first = moe.moe_route_permute(inp["logits"], p, inp["correction_bias"])
+    ws = first[4]["ws"]
+    for _ in range(3):
+        again = moe.moe_route_permute(inp["logits"], p, inp["correction_bias"], ws=ws)
+        for k in ("seg_end", "row_to_route", "route_to_row"):
+            assert torch.equal(again[4][k], first[4][k]), k
+        assert torch.equal(again[1], first[1])
+    assert moe.moe_sync_status(ws) == moe.MOE_OK
+    assert int(ws[16:28].count_nonzero()) == 0
+
+
 def test_route_permute_rejects_large_e(moe):
     cfg = synth.CONFIGS["qwen3_bf16"].replace(T=8, E=640, K=8, H=64, F=64, local_count=0)
     inp, _ = make(cfg)
