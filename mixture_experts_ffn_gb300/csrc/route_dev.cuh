@@ -49,27 +49,38 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
   }
 }
 
-// Route token t (the calling warp; all 32 lanes).  Writes topk weights and ids
-// of t, and its MoERouter row when a.lc > 0.
+// Logits of token t in the calling lane's registers: z[i] = logit of expert
+// lane + 32 i (-inf past E).
 template <int NPL>
-__device__ __forceinline__ void route_token(int t, const float* __restrict__ logits,
-                                            const float* __restrict__ bias,
-                                            const int32_t* __restrict__ ids_in, int E,
-                                            const RouteArgs& a, float* __restrict__ w_out,
-                                            int32_t* __restrict__ id_out,
-                                            float* __restrict__ probs,
-                                            float* __restrict__ wscale) {
+__device__ __forceinline__ void load_logits(int t, const float* __restrict__ logits, int E,
+                                            float (&z)[NPL]) {
   const int lane = threadIdx.x & 31;
-  const float* z = logits + (size_t)t * E;
+  const float* row = logits + (size_t)t * E;
+#pragma unroll
+  for (int i = 0; i < NPL; ++i) {
+    const int e = lane + 32 * i;
+    z[i] = e < E ? __ldg(row + e) : -INFINITY;
+  }
+}
+
+// Route token t (the calling warp; all 32 lanes) from its logits z (as
+// load_logits leaves them).  Writes topk weights and ids of t, and its
+// MoERouter row when a.lc > 0.
+template <int NPL>
+__device__ __forceinline__ void route_loaded(int t, const float (&z)[NPL],
+                                             const float* __restrict__ bias,
+                                             const int32_t* __restrict__ ids_in, int E,
+                                             const RouteArgs& a, float* __restrict__ w_out,
+                                             int32_t* __restrict__ id_out,
+                                             float* __restrict__ probs,
+                                             float* __restrict__ wscale) {
+  const int lane = threadIdx.x & 31;
   const int K = a.K;
 
   // ---- scores s (float32), experts e = lane + 32 i
   float s[NPL];
 #pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    int e = lane + 32 * i;
-    s[i] = e < E ? __ldg(z + e) : -INFINITY;
-  }
+  for (int i = 0; i < NPL; ++i) s[i] = z[i];
   if (a.scoring == MOE_SCORING_SOFTMAX) {
     float m = -INFINITY;
 #pragma unroll
@@ -247,6 +258,20 @@ __device__ __forceinline__ void route_token(int t, const float* __restrict__ log
     local = warp_sum(local);
     if (lane == 0) wscale[t] = a.route_scale * local;
   }
+}
+
+// Route token t (the calling warp): load_logits then route_loaded.
+template <int NPL>
+__device__ __forceinline__ void route_token(int t, const float* __restrict__ logits,
+                                            const float* __restrict__ bias,
+                                            const int32_t* __restrict__ ids_in, int E,
+                                            const RouteArgs& a, float* __restrict__ w_out,
+                                            int32_t* __restrict__ id_out,
+                                            float* __restrict__ probs,
+                                            float* __restrict__ wscale) {
+  float z[NPL];
+  load_logits<NPL>(t, logits, E, z);
+  route_loaded<NPL>(t, z, bias, ids_in, E, a, w_out, id_out, probs, wscale);
 }
 
 // RouteArgs from the C-ABI parameters (the MoERouter outputs are skipped when

@@ -70,17 +70,29 @@ __device__ bool grid_barrier(int* ctr, int* status) {
   return ok_s != 0;
 }
 
-// counts[0..n)[e] summed, 16 loads in flight
-__device__ __forceinline__ int column_sum(const int* __restrict__ counts, int E, int e, int n) {
-  int s = 0;
+// counts[0..n)[e] summed (all) and counts[0..c)[e] summed (before), one
+// pass with 16 loads in flight
+__device__ __forceinline__ void column_sums(const int* __restrict__ counts, int E, int e, int n,
+                                            int c, int& all, int& before) {
+  int sa = 0, sb = 0;
   for (int c0 = 0; c0 < n; c0 += 16) {
     int v[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = c0 + j < n ? counts[(size_t)(c0 + j) * E + e] : 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) s += v[j];
+    for (int j = 0; j < 16; ++j) {
+      sa += v[j];
+      sb += c0 + j < c ? v[j] : 0;
+    }
   }
-  return s;
+  all = sa;
+  before = sb;
+}
+// counts[0..n)[e] summed
+__device__ __forceinline__ int column_sum(const int* __restrict__ counts, int E, int e, int n) {
+  int all, before;
+  column_sums(counts, E, e, n, 0, all, before);
+  return all;
 }
 
 template <int NPL>
@@ -95,9 +107,19 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
   pdl_wait();  // everything below reads results of earlier launches
   const int warp = threadIdx.x >> 5, W = blockDim.x >> 5, tid = threadIdx.x;
   const int M = T * a.K;
-  // ---- A: route
-  for (int t = blockIdx.x * W + warp; t < T; t += gridDim.x * W)
-    rt::route_token<NPL>(t, logits, bias, ids_in, E, a, w_out, id_out, probs, wscale);
+  // ---- A: route (the next token's logits are loaded before this one is routed)
+  {
+    const int stride = gridDim.x * W;
+    int t = blockIdx.x * W + warp;
+    float z[NPL], zn[NPL];
+    if (t < T) rt::load_logits<NPL>(t, logits, E, z);
+    for (; t < T; t += stride) {
+      if (t + stride < T) rt::load_logits<NPL>(t + stride, logits, E, zn);
+      rt::route_loaded<NPL>(t, z, bias, ids_in, E, a, w_out, id_out, probs, wscale);
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) z[i] = zn[i];
+    }
+  }
   if (!grid_barrier(&bar[0], status)) return;
   // ---- B: count
   int* start = smem;
@@ -113,8 +135,10 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
     bar[2] = 0;
   }
   if ((int)blockIdx.x >= C) return;  // no chunk of its own
-  // ---- C: expert start rows (one thread per expert, E <= blockDim.x)
-  const int tot = tid < E ? column_sum(counts, E, tid, C) : 0;
+  // ---- C: expert start rows (one thread per expert, E <= blockDim.x); the
+  // same pass sums the counts of the chunks before this CTA's first chunk
+  int tot = 0, before = 0;
+  if (tid < E) column_sums(counts, E, tid, C, blockIdx.x, tot, before);
   __shared__ int wt[33];
   int total, n_act;
   const int first = pm::block_exclusive_scan(tot, wt, &total);
@@ -130,7 +154,8 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
   __syncthreads();
   // ---- D: this CTA's chunks
   for (int c = blockIdx.x; c < C; c += gridDim.x) {
-    if (tid < E) offs[tid] = start[tid] + column_sum(counts, E, tid, c);
+    if (tid < E)
+      offs[tid] = start[tid] + (c == (int)blockIdx.x ? before : column_sum(counts, E, tid, c));
     __syncthreads();
     pm::scatter_chunk(id_out, M, E, c, offs, wcnt, row_to_route, route_to_row);
   }
