@@ -280,6 +280,7 @@ def stage_cost(cfg, D):
         # the index maps only and the gate_up GEMM reads the hidden rows
         # through them (each hidden row counted once)
         "permute_maps": (0.0, M * 4 * 3 + E * 4),
+        "permute_gather": (0.0, M * 4 + E * 4 + T * H * b + M * H * b),
         "route_permute": (0.0, route + M * 4 * 3 + E * 4),
         "gemm_act": (4.0 * M * H * F, D * 2 * F * H * b + bias1 + M * H * b + M * F * b),
         "gemm_act_gathered": (4.0 * M * H * F, D * 2 * F * H * b + bias1 + T * H * b + M * F * b),
@@ -411,9 +412,9 @@ def run_ours(args, rank, world, local):
         act_out = torch.empty((T * K, F), dtype=tdt, device=dev)
         y = torch.empty((T * K, H), dtype=tdt, device=dev)
         stage_ws = moe._ws(256, dev)
-        # the forward routes and builds the index maps in one launch when it
-        # needs the maps only (gathered gate_up or indexed path, E <= 512)
-        fused_maps = (indexed or gathered) and E <= 512
+        # the forward routes and builds the index maps in one launch (E <= 512);
+        # the staged path then copies the permuted rows in a launch of its own
+        fused_maps = E <= 512
         if fused_maps:
             stages = {"route_permute": lambda: moe.moe_route_permute(
                 inp["logits"], p, inp["correction_bias"], inp["expert_ids"], ws=perm["ws"])}
@@ -440,8 +441,13 @@ def run_ours(args, rank, world, local):
                 "combine": lambda: moe.moe_combine(y, tw, perm["route_to_row"], out=out),
             })
         else:
+            if fused_maps:
+                stages["permute_gather"] = lambda: moe.moe_permute_gather(
+                    inp["hidden"], perm["seg_end"], perm["row_to_route"], K,
+                    out=perm["expert_input"], ws=stage_ws)
+            else:
+                stages["permute"] = lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"])
             stages.update({
-                "permute": lambda: moe.moe_permute(ti, E, inp["hidden"], ws=perm["ws"]),
                 "gemm_act": lambda: moe.moe_grouped_gemm_act(perm["expert_input"],
                                                              inp["w_gate_up"], perm["seg_end"], F,
                                                              a, inp["b_gate_up"], out=act_out,

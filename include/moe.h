@@ -140,8 +140,8 @@ moe_status moe_route(const float* logits, const float* correction_bias,
 
 /* ------------------------------------------------------------------------ */
 /* moe_route followed by moe_permute without the gather (expert_input NULL),
- * in one launch (an addition; the forward uses it whenever it needs the index
- * maps only).  Outputs are bit-identical to the two calls: topk_weights,
+ * in one launch (an addition; the forward uses it whenever E <= 512).
+ * Outputs are bit-identical to the two calls: topk_weights,
  * topk_ids, router_probs, weight_scale as moe_route; seg_end, row_to_route,
  * route_to_row as moe_permute.  E <= 512 (MOE_ERR_UNSUPPORTED above; use the
  * two calls).  ws: >= moe_permute_workspace_size(T*K, E) bytes whose status
@@ -177,6 +177,20 @@ moe_status moe_permute(const void* hidden, moe_dtype dtype, const int32_t* topk_
                        int H, int E, int K, void* expert_input, int32_t* seg_end,
                        int32_t* row_to_route, int32_t* route_to_row, void* ws,
                        size_t ws_bytes, cudaStream_t stream);
+
+/* The gather step of moe_permute on its own (an addition), from index maps
+ * already built (moe_route_permute, or moe_permute without the gather):
+ * expert_input[row, :] = hidden[row_to_route[row] / K, :] for every row below
+ * seg_end[E-1].  Bit-identical to moe_permute's expert_input.
+ *
+ *   hidden [T, H] dtype;  seg_end [E] i32;  row_to_route [T*K] i32;
+ *   expert_input [T*K, H] dtype out (rows past seg_end[E-1] not written);
+ *   ws >= MOE_STATUS_BYTES bytes.
+ * A map entry outside [0, T*K) latches MOE_ERR_DEVICE and its row is not
+ * written. */
+moe_status moe_permute_gather(const void* hidden, moe_dtype dtype, const int32_t* seg_end,
+                              const int32_t* row_to_route, int T, int H, int E, int K,
+                              void* expert_input, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* moe_permute for callers that cannot allocate device memory.  (The pages have
@@ -321,13 +335,14 @@ moe_status moe_indexed_mlp(const void* hidden, const void* w_gate_up, const void
  * F % 256 == 0 and hidden and the weights are 16-byte aligned [TileOPs,
  * FusedMoEExpertsFwdOp dispatch rule]; otherwise
  * the staged pipeline permute -> gate_up+act -> down -> combine.
- * When the gate_up GEMM runs on the tensor cores (bf16, H % 8 == 0,
- * F % 8 == 0, 16-byte aligned hidden, weights and workspace sections), the
- * permuted copy of the activations is never materialised: routing and the
- * index maps take one launch (moe_route_permute, E <= 512) and the gate_up
- * GEMM reads its rows through row_to_route (moe_grouped_gemm_act_gathered),
- * so the layer is four launches; the results are the same as the staged
- * calls'.  Every launch is made with programmatic dependent launch, so each
+ * Routing and the index maps take one launch when E <= 512
+ * (moe_route_permute).  When the gate_up GEMM runs on the tensor cores (bf16,
+ * H % 8 == 0, F % 8 == 0, 16-byte aligned hidden, weights and workspace
+ * sections), the permuted copy of the activations is never materialised: the
+ * gate_up GEMM reads its rows through row_to_route
+ * (moe_grouped_gemm_act_gathered), so the layer is four launches; otherwise
+ * the permuted copy takes a launch of its own after the maps.  The results
+ * are the same as the staged calls'.  Every launch is made with programmatic dependent launch, so each
  * overlaps the tail of the previous one.
  *
  *   hidden [T, H] dtype;  logits [T, E] f32;  w_gate_up [E, N1, H];

@@ -201,6 +201,25 @@ moe_status moe_permute(const void* hidden, moe_dtype dtype, const int32_t* topk_
                                     row_to_route, route_to_row, ws, stream));
 }
 
+moe_status moe_permute_gather(const void* hidden, moe_dtype dtype, const int32_t* seg_end,
+                              const int32_t* row_to_route, int T, int H, int E, int K,
+                              void* expert_input, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (T < 0 || H < 1 || K < 1 || E < 1 || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
+  if ((long long)T * K >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+  if (!seg_end || (T > 0 && (!hidden || !row_to_route || !expert_input)))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, MOE_STATUS_BYTES)) return MOE_ERR_WORKSPACE;
+  const int M = T * K;
+  const size_t esz = esize(dtype);
+  Span outs[] = {{expert_input, (size_t)M * H * esz}};
+  Span ins[] = {{hidden, (size_t)T * H * esz}, {seg_end, (size_t)E * 4},
+                {row_to_route, (size_t)M * 4}, {ws, MOE_STATUS_BYTES}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  if (M == 0) return MOE_OK;
+  return cuda_status(launch_permute_gather(hidden, (int)esz, T, H, E, K, seg_end, row_to_route,
+                                           expert_input, ws, stream));
+}
+
 moe_status moe_grouped_gemm_act(const void* a, const void* w_gate_up, const void* b_gate_up,
                                 const int32_t* seg_end, int M, int F, int Hk, int E,
                                 moe_dtype dtype, const moe_act_params* act, void* out, void* ws,
@@ -377,8 +396,9 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   // written or read back.
   const bool fused_gather = !indexed && dtype == MOE_BF16 &&
                             tc_ok(hidden, w_gate_up, a1, F, H, (int)M);
-  // When only the index maps are needed, routing and the maps take one launch.
-  const bool fused_maps = (indexed || fused_gather) && route_permute_ok(E);
+  // Routing and the index maps take one launch; the staged path then copies
+  // the permuted activations in a launch of its own.
+  const bool fused_maps = route_permute_ok(E);
   cudaError_t err =
       fused_maps ? launch_route_permute(logits, correction_bias, expert_ids, T, E, *p, tw, ti,
                                         router_probs, weight_scale, seg_end, r2r, route_to_row,
@@ -395,6 +415,9 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   if (!fused_maps) {
     err = launch_permute(hidden, (int)esz, ti, T, H, E, K, fused_gather ? nullptr : xin, seg_end,
                          r2r, route_to_row, ws, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (!fused_gather) {
+    err = launch_permute_gather(hidden, (int)esz, T, H, E, K, seg_end, r2r, xin, ws, stream);
     if (err != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (fused_gather)

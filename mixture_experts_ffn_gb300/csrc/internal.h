@@ -86,8 +86,8 @@ cudaError_t launch_route(const float* logits, const float* bias, const int32_t* 
 
 // Router + permute index maps in one launch (bit-identical to launch_route
 // then launch_permute without the gather); route_permute_ok(E) says whether
-// E is within its limit (E <= 512).  Uses ws's permute scratch and two ints
-// of its status area.
+// E is within its limit (E <= 512).  Uses ws's permute scratch and three
+// ints of its status area (grid-barrier counters that reset themselves).
 bool route_permute_ok(int E);
 cudaError_t launch_route_permute(const float* logits, const float* bias, const int32_t* ids_in,
                                  int T, int E, const moe_route_params& p, float* w, int32_t* ids,
@@ -98,6 +98,11 @@ cudaError_t launch_route_permute(const float* logits, const float* bias, const i
 cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int T, int H, int E,
                            int K, void* expert_input, int32_t* seg_end, int32_t* row_to_route,
                            int32_t* route_to_row, void* ws, cudaStream_t s);
+// The gather step of launch_permute alone: expert_input[row] = hidden[row_to_route[row] / K]
+// for the rows below seg_end[E-1], from maps already built (launch_route_permute).
+cudaError_t launch_permute_gather(const void* hidden, int esz, int T, int H, int E, int K,
+                                  const int32_t* seg_end, const int32_t* row_to_route,
+                                  void* expert_input, void* ws, cudaStream_t s);
 
 cudaError_t launch_combine(const void* y, const float* w, const int32_t* route_to_row, int T,
                            int K, int H, moe_dtype dt, float scale, void* out, cudaStream_t s);

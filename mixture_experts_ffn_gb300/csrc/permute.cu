@@ -297,20 +297,30 @@ cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int 
     launch_pdl(perm_scatter, C, 32, hist_smem, s, ids, M, E, counts, row_to_route, route_to_row);
   }
   count_launch(3);
-  if (expert_input) {
-    const size_t row_bytes = (size_t)H * esz;
-    const int rows_per_block = 8;
-    dim3 grid((M + rows_per_block - 1) / rows_per_block);
-    const bool vec = (row_bytes % 16 == 0) && ((uintptr_t)hidden % 16 == 0) &&
-                     ((uintptr_t)expert_input % 16 == 0);
-    if (vec)
-      launch_pdl(perm_gather<16>, grid, 256, 0, s, static_cast<const char*>(hidden), row_to_route,
-          seg_end, E, K, T, row_bytes, static_cast<char*>(expert_input), status);
-    else
-      launch_pdl(perm_gather<2>, grid, 256, 0, s, static_cast<const char*>(hidden), row_to_route,
-          seg_end, E, K, T, row_bytes, static_cast<char*>(expert_input), status);
-    count_launch();
-  }
+  if (expert_input)
+    return launch_permute_gather(hidden, esz, T, H, E, K, seg_end, row_to_route, expert_input, ws,
+                                 s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_gather(const void* hidden, int esz, int T, int H, int E, int K,
+                                  const int32_t* seg_end, const int32_t* row_to_route,
+                                  void* expert_input, void* ws, cudaStream_t s) {
+  const int M = T * K;
+  if (M == 0) return cudaSuccess;
+  int* status = static_cast<int*>(ws);
+  const size_t row_bytes = (size_t)H * esz;
+  const int rows_per_block = 8;
+  dim3 grid((M + rows_per_block - 1) / rows_per_block);
+  const bool vec = (row_bytes % 16 == 0) && ((uintptr_t)hidden % 16 == 0) &&
+                   ((uintptr_t)expert_input % 16 == 0);
+  if (vec)
+    launch_pdl(perm_gather<16>, grid, 256, 0, s, static_cast<const char*>(hidden), row_to_route,
+               seg_end, E, K, T, row_bytes, static_cast<char*>(expert_input), status);
+  else
+    launch_pdl(perm_gather<2>, grid, 256, 0, s, static_cast<const char*>(hidden), row_to_route,
+               seg_end, E, K, T, row_bytes, static_cast<char*>(expert_input), status);
+  count_launch();
   return cudaGetLastError();
 }
 

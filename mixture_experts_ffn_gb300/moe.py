@@ -47,6 +47,7 @@ _SIGNATURES = {
     "moe_permute": [_vp, _i, _vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_route_permute": [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                           _sz, _vp],
+    "moe_permute_gather": [_vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_act": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_act_gathered": [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
                                       _vp, _vp, _sz, _vp],
@@ -202,6 +203,23 @@ def moe_permute(topk_ids, E: int, hidden=None, ws=None, with_gather=True):
                                           _p(route_to_row), _p(ws), ws.numel(), _stream()))
     return {"expert_input": xin, "seg_end": seg_end, "row_to_route": r2r,
             "route_to_row": route_to_row, "ws": ws}
+
+
+def moe_permute_gather(hidden, seg_end, row_to_route, K: int, out=None, ws=None):
+    """The permuted copy of the activations from index maps already built:
+    out[row] = hidden[row_to_route[row] // K] for the rows below seg_end[-1]."""
+    lib = load_library()
+    _cuda(hidden, seg_end, row_to_route)
+    T, H = hidden.shape
+    E = seg_end.numel()
+    if out is None:
+        out = torch.empty((T * K, H), dtype=hidden.dtype, device=hidden.device)
+    if ws is None:
+        ws = _ws(MOE_STATUS_BYTES, hidden.device)
+    _check("moe_permute_gather",
+           lib.moe_permute_gather(_p(hidden), _dt(hidden), _p(seg_end), _p(row_to_route), T, H, E,
+                                  K, _p(out), _p(ws), ws.numel(), _stream()))
+    return out
 
 
 def moe_route_permute(logits, p: RouteParams, correction_bias=None, expert_ids=None, ws=None):

@@ -142,6 +142,14 @@ def test_stage_entry_points_reject_bad_arguments(lib):
     need = lib.moe_permute_workspace_size(64, 8)
     assert lib.moe_permute(A(0), moe.MOE_BF16, A(1), 32, 64, 8, 2, A(2), A(3), A(4), A(5), ws,
                            need - 256, None) == moe.MOE_ERR_WORKSPACE
+    # permute gather: missing hidden, small workspace, out inside hidden
+    assert lib.moe_permute_gather(None, moe.MOE_BF16, A(1), A(2), 32, 64, 8, 2, A(3), ws, 4096,
+                                  None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute_gather(A(0), moe.MOE_BF16, A(1), A(2), 32, 64, 8, 2, A(3), ws, 64,
+                                  None) == moe.MOE_ERR_WORKSPACE
+    assert lib.moe_permute_gather(A(0), moe.MOE_BF16, A(1), A(2), 32, 64, 8, 2,
+                                  ctypes.c_void_p(A(0).value + 256), ws, 4096,
+                                  None) == moe.MOE_ERR_OVERLAP
     # the forward checks the router parameters too
     p = moe.route_params(3, num_expert_group=2, topk_group=1)
     need = lib.moe_workspace_size(16, 64, 32, 4, 3, moe.MOE_BF16)

@@ -183,6 +183,22 @@ def test_route_permute_reuses_workspace(moe):
     assert int(ws[16:28].count_nonzero()) == 0
 
 
+@pytest.mark.parametrize("dtype,H", [("bf16", 2048), ("bf16", 100), ("f32", 64)])
+def test_permute_gather_after_fused_maps(moe, dtype, H):
+    """The gather step on its own, from the maps of the one-launch route +
+    permute, equals moe_permute's permuted copy bit for bit (16-byte rows and
+    ragged rows)."""
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=777, H=H, F=64, local_count=0)
+    inp, _ = make(cfg)
+    p, _ = moe.config_params(cfg)
+    hidden = inp["hidden"].to(synth.torch_dtype(dtype))
+    _, ti, _, _, maps = moe.moe_route_permute(inp["logits"], p, inp["correction_bias"])
+    got = moe.moe_permute_gather(hidden, maps["seg_end"], maps["row_to_route"], cfg.K)
+    ref = moe.moe_permute(ti, cfg.E, hidden)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref["expert_input"])
+
+
 def test_route_permute_rejects_large_e(moe):
     cfg = synth.CONFIGS["qwen3_bf16"].replace(T=8, E=640, K=8, H=64, F=64, local_count=0)
     inp, _ = make(cfg)
