@@ -362,14 +362,19 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
 
 /* ------------------------------------------------------------------------ */
 /* moe_ffn_forward for a caller whose activations live in HOST memory:
- * hidden_host [T, H] dtype and logits_host [T, E] f32 are copied to device
- * staging space inside `ws` (cudaMemcpyAsync on `stream`), the layer runs as in
- * moe_ffn_forward, and the result is copied back into out_host [T, H].  All of
- * it is asynchronous on `stream`: out_host is valid after the stream is
- * synchronised.  Host buffers should be page-locked for the copies to overlap
- * the host; pageable memory works but the copies then synchronise.  Weights,
- * biases and expert_ids stay device pointers.  Routing outputs are not
- * returned.  ws >= moe_workspace_size_host(T, H, F, E, K, dtype). */
+ * hidden_host [T, H] dtype and logits_host [T, E] f32 are brought to device
+ * staging space inside `ws`, the layer runs as in moe_ffn_forward, and the
+ * result lands in out_host [T, H].  The activations come in on a side stream
+ * of the library's (one per device, created on first use, joined back to
+ * `stream` through events) while the logits are copied and the tokens routed
+ * on `stream`; page-locked activations are read by a copy kernel, others by
+ * cudaMemcpyAsync.  A page-locked out_host is written in place by the combine
+ * (its writes overlap the combine's reads); otherwise the result is staged in
+ * `ws` and copied back (always so on the indexed decode path).  All of it is
+ * asynchronous on `stream`: out_host is valid after the stream is
+ * synchronised.  Pageable buffers work, but their copies synchronise.
+ * Weights, biases and expert_ids stay device pointers.  Routing outputs are
+ * not returned.  ws >= moe_workspace_size_host(T, H, F, E, K, dtype). */
 moe_status moe_ffn_forward_host(const void* hidden_host, const float* logits_host,
                                 const void* w_gate_up, const void* w_down,
                                 const float* correction_bias, const int32_t* expert_ids,

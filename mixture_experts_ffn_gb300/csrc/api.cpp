@@ -343,13 +343,27 @@ moe_status moe_indexed_mlp(const void* hidden, const void* w_gate_up, const void
                                     K, scale, out, ws, L, stream));
 }
 
-moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* w_gate_up,
-                           const void* w_down, const float* correction_bias,
-                           const int32_t* expert_ids, const void* b_gate_up, const void* b_down,
-                           int T, int H, int F, int E, moe_dtype dtype, const moe_route_params* p,
-                           const moe_act_params* act, void* out, float* topk_weights_out,
-                           int32_t* topk_ids_out, float* router_probs, float* weight_scale,
-                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+namespace {
+
+// What moe_ffn_forward_host changes in the forward: the stream waits on
+// hidden_ready after routing (the first step that reads the activations, whose
+// copy runs on a side stream meanwhile), and the combine writes its result to
+// out_direct (page-locked host memory the device addresses) when set.  The
+// indexed path keeps writing `out`.
+struct HostHooks {
+  cudaEvent_t hidden_ready = nullptr;
+  void* out_direct = nullptr;
+  bool waited = false;
+  bool wrote_direct = false;
+};
+
+moe_status ffn_forward(const void* hidden, const float* logits, const void* w_gate_up,
+                       const void* w_down, const float* correction_bias,
+                       const int32_t* expert_ids, const void* b_gate_up, const void* b_down,
+                       int T, int H, int F, int E, moe_dtype dtype, const moe_route_params* p,
+                       const moe_act_params* act, void* out, float* topk_weights_out,
+                       int32_t* topk_ids_out, float* router_probs, float* weight_scale,
+                       void* ws, size_t ws_bytes, cudaStream_t stream, HostHooks* hooks) {
   if (!dtype_ok(dtype) || !act_ok(act) || H < 1 || F < 1) return MOE_ERR_INVALID_ARG;
   float dummy_w = 0.f;
   int32_t dummy_i = 0;
@@ -406,6 +420,10 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
                  : launch_route(logits, correction_bias, expert_ids, T, E, *p, tw, ti,
                                 router_probs, weight_scale, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
+  if (hooks && hooks->hidden_ready) {
+    if (cudaStreamWaitEvent(stream, hooks->hidden_ready, 0) != cudaSuccess) return MOE_ERR_CUDA;
+    hooks->waited = true;
+  }
 
   // routed_scaling_factor is folded into tw by the router: the combine scale is 1
   if (indexed)
@@ -430,7 +448,59 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   err = grouped_gemm(a1, w_down, b_down, seg_end, (int)M, H, F, E, dtype, nullptr, y, status,
                      stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
-  return cuda_status(launch_combine(y, tw, route_to_row, T, K, H, dtype, 1.0f, out, stream));
+  void* dst = out;
+  if (hooks && hooks->out_direct) {
+    dst = hooks->out_direct;
+    hooks->wrote_direct = true;
+  }
+  return cuda_status(launch_combine(y, tw, route_to_row, T, K, H, dtype, 1.0f, dst, stream));
+}
+
+// The device address of page-locked host memory (nullptr for anything else,
+// e.g. pageable memory the runtime does not know).
+void* mapped_host(const void* p) {
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return pa.type == cudaMemoryTypeHost ? pa.devicePointer : nullptr;
+}
+
+// One non-blocking side stream per device for the activation copy of
+// moe_ffn_forward_host, created on first use and kept until the process
+// exits.  Calls share it; each call's copy is ordered on it and joined back
+// to the caller's stream through an event of its own.
+constexpr int kMaxSideDevices = 64;
+std::mutex g_side_mu;
+cudaStream_t g_side[kMaxSideDevices] = {};
+
+cudaError_t side_stream(cudaStream_t* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxSideDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_side_mu);
+  if (!g_side[dev]) {
+    e = cudaStreamCreateWithFlags(&g_side[dev], cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+  }
+  *out = g_side[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* w_gate_up,
+                           const void* w_down, const float* correction_bias,
+                           const int32_t* expert_ids, const void* b_gate_up, const void* b_down,
+                           int T, int H, int F, int E, moe_dtype dtype, const moe_route_params* p,
+                           const moe_act_params* act, void* out, float* topk_weights_out,
+                           int32_t* topk_ids_out, float* router_probs, float* weight_scale,
+                           void* ws, size_t ws_bytes, cudaStream_t stream) {
+  return ffn_forward(hidden, logits, w_gate_up, w_down, correction_bias, expert_ids, b_gate_up,
+                     b_down, T, H, F, E, dtype, p, act, out, topk_weights_out, topk_ids_out,
+                     router_probs, weight_scale, ws, ws_bytes, stream, nullptr);
 }
 
 size_t moe_workspace_size_host(int T, int H, int F, int E, int K, moe_dtype dtype) {
@@ -456,21 +526,60 @@ moe_status moe_ffn_forward_host(const void* hidden_host, const float* logits_hos
   if (T == 0) return MOE_OK;
   const size_t esz = esize(dtype);
   const size_t fwd = moe_workspace_size(T, H, F, E, p->top_k, dtype);
+  const size_t act_bytes = (size_t)T * H * esz;
   char* base = static_cast<char*>(ws);
   void* d_hidden = base + fwd;
-  void* d_out = base + fwd + align256((size_t)T * H * esz);
-  float* d_logits = reinterpret_cast<float*>(base + fwd + 2 * align256((size_t)T * H * esz));
-  if (cudaMemcpyAsync(d_hidden, hidden_host, (size_t)T * H * esz, cudaMemcpyHostToDevice,
-                      stream) != cudaSuccess ||
-      cudaMemcpyAsync(d_logits, logits_host, (size_t)T * E * 4, cudaMemcpyHostToDevice,
-                      stream) != cudaSuccess)
+  void* d_out = base + fwd + align256(act_bytes);
+  float* d_logits = reinterpret_cast<float*>(base + fwd + 2 * align256(act_bytes));
+  cudaStream_t side = nullptr;
+  if (side_stream(&side) != cudaSuccess) return MOE_ERR_CUDA;
+  // The activation copy runs on the side stream while the logits copy and the
+  // routing run on `stream`; the forward waits for it after routing.
+  cudaEvent_t fork = nullptr, ready = nullptr;
+  if (cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaEventCreateWithFlags(&ready, cudaEventDisableTiming) != cudaSuccess) {
+    cudaEventDestroy(fork);
     return MOE_ERR_CUDA;
-  moe_status st = moe_ffn_forward(d_hidden, d_logits, w_gate_up, w_down, correction_bias,
-                                  expert_ids, b_gate_up, b_down, T, H, F, E, dtype, p, act, d_out,
-                                  nullptr, nullptr, nullptr, nullptr, ws, fwd, stream);
+  }
+  moe_status st = MOE_OK;
+  bool copied = false;
+  // Page-locked activations are read by a copy kernel (one CTA per SM, so it
+  // runs beside the routing launch), which outruns a copy engine over the
+  // host link; anything else takes cudaMemcpyAsync.
+  const void* h_dev = mapped_host(hidden_host);
+  auto copy_in = [&]() {
+    if (h_dev && act_bytes % 16 == 0 && (uintptr_t)h_dev % 16 == 0)
+      return launch_copy16(h_dev, d_hidden, act_bytes, side);
+    return cudaMemcpyAsync(d_hidden, hidden_host, act_bytes, cudaMemcpyHostToDevice, side);
+  };
+  if (cudaEventRecord(fork, stream) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess ||
+      copy_in() != cudaSuccess || cudaEventRecord(ready, side) != cudaSuccess) {
+    st = MOE_ERR_CUDA;
+  } else {
+    copied = true;
+    if (cudaMemcpyAsync(d_logits, logits_host, (size_t)T * E * 4, cudaMemcpyHostToDevice,
+                        stream) != cudaSuccess)
+      st = MOE_ERR_CUDA;
+  }
+  // The result is written in place when out_host is page-locked memory the
+  // device can address (no staging copy; its writes overlap the combine's
+  // reads); otherwise it is staged in `ws` and copied back.
+  HostHooks hk;
+  hk.hidden_ready = ready;
+  if (st == MOE_OK) {
+    hk.out_direct = mapped_host(out_host);
+    st = ffn_forward(d_hidden, d_logits, w_gate_up, w_down, correction_bias, expert_ids,
+                     b_gate_up, b_down, T, H, F, E, dtype, p, act, d_out, nullptr, nullptr,
+                     nullptr, nullptr, ws, fwd, stream, &hk);
+  }
+  // Whatever happened, nothing later on `stream` runs before the side copy.
+  if (copied && !hk.waited && cudaStreamWaitEvent(stream, ready, 0) != cudaSuccess)
+    st = MOE_ERR_CUDA;
+  cudaEventDestroy(fork);  // released once the recorded work completes
+  cudaEventDestroy(ready);
   if (st != MOE_OK) return st;
-  return cuda_status(
-      cudaMemcpyAsync(out_host, d_out, (size_t)T * H * esz, cudaMemcpyDeviceToHost, stream));
+  if (hk.wrote_direct) return MOE_OK;
+  return cuda_status(cudaMemcpyAsync(out_host, d_out, act_bytes, cudaMemcpyDeviceToHost, stream));
 }
 
 moe_status moe_clear_status(void* ws, cudaStream_t stream) {

@@ -104,6 +104,11 @@ cudaError_t launch_permute_gather(const void* hidden, int esz, int T, int H, int
                                   const int32_t* seg_end, const int32_t* row_to_route,
                                   void* expert_input, void* ws, cudaStream_t s);
 
+// dst[0, bytes) = src[0, bytes) by the SMs (16-byte aligned pointers and
+// size; cudaErrorInvalidValue otherwise); src may be page-locked host memory
+// mapped for the device.
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s);
+
 cudaError_t launch_combine(const void* y, const float* w, const int32_t* route_to_row, int T,
                            int K, int H, moe_dtype dt, float scale, void* out, cudaStream_t s);
 

@@ -259,7 +259,33 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
   }
 }
 
+// Plain copy by the SMs, 16 bytes per thread and step (a grid-stride loop over
+// one CTA per SM): used to bring page-locked host activations in, where the
+// SMs' reads over the host link outrun a copy engine.
+__global__ void __launch_bounds__(256) copy16_kernel(const int4* __restrict__ src,
+                                                     int4* __restrict__ dst, long long n) {
+  long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (; i + 3 * stride < n; i += 4 * stride) {
+    const int4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
+    dst[i] = a;
+    dst[i + stride] = b;
+    dst[i + 2 * stride] = c;
+    dst[i + 3 * stride] = d;
+  }
+  for (; i < n; i += stride) dst[i] = src[i];
+}
+
 }  // namespace
+
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s) {
+  if (bytes == 0) return cudaSuccess;
+  if (bytes % 16 || (uintptr_t)src % 16 || (uintptr_t)dst % 16) return cudaErrorInvalidValue;
+  copy16_kernel<<<num_sms(), 256, 0, s>>>(static_cast<const int4*>(src), static_cast<int4*>(dst),
+                                          (long long)(bytes / 16));
+  count_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int T, int H, int E,
                            int K, void* expert_input, int32_t* seg_end, int32_t* row_to_route,

@@ -194,3 +194,37 @@ def test_concurrent_forwards_on_two_streams(moe):
     for ws, o in zip(wss, outs):
         assert moe.moe_sync_status(ws) == moe.MOE_OK
         assert torch.equal(o, ref)
+
+
+@pytest.mark.parametrize("name,over", [
+    ("qwen3_bf16", dict(T=300, H=256, F=128, local_count=0)),        # gathered gate_up
+    ("gpt_oss_bf16", dict(T=200, H=256, F=128)),                     # gathered, biases, SwiGLU
+    ("tiny_fp32", dict()),                                           # staged, SIMT GEMMs
+    ("kimi_k2_decode_bf16", dict(T=8, H=256, F=256)),                # indexed decode path
+])
+@pytest.mark.parametrize("pinned", [True, False])
+def test_forward_host_matches_device(moe, name, over, pinned):
+    """moe_ffn_forward_host (host activations and result; the activation copy
+    on a side stream, the result written in place when it is page-locked)
+    equals moe_ffn_forward on device copies of the same inputs bit for bit,
+    with a page-locked or a pageable result buffer."""
+    cfg = synth.CONFIGS[name].replace(**over)
+    inp, _ = make(cfg)
+    p, a = moe.config_params(cfg)
+    ref = moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a,
+                              inp["correction_bias"], inp["expert_ids"], inp["b_gate_up"],
+                              inp["b_down"])
+    h_host = inp["hidden"].cpu()
+    l_host = inp["logits"].cpu()
+    o_host = torch.full(tuple(ref.shape), float("nan"), dtype=ref.dtype)
+    if pinned:
+        h_host, l_host, o_host = h_host.pin_memory(), l_host.pin_memory(), o_host.pin_memory()
+    dt = moe.MOE_BF16 if cfg.dtype == "bf16" else moe.MOE_F32
+    ws = moe._ws(moe.moe_workspace_size_host(cfg.T, cfg.H, cfg.F, cfg.E, cfg.K, dt), "cuda")
+    for _ in range(2):  # the second call reuses the side stream and the workspace
+        o_host.fill_(float("nan"))
+        moe.moe_ffn_forward_host(h_host, l_host, inp["w_gate_up"], inp["w_down"], p, a, o_host, ws,
+                                 inp["correction_bias"], inp["expert_ids"], inp["b_gate_up"],
+                                 inp["b_down"])
+        assert moe.moe_sync_status(ws) == moe.MOE_OK
+        assert torch.equal(o_host, ref.cpu())
