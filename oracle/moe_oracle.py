@@ -437,6 +437,36 @@ def ffn_forward(hidden, logits, w_gate_up, w_down, K: int, F: int, scoring="soft
     return r
 
 
+def shared_expert_mlp(hidden, w_gate_up, w_down, dtype: Optional[str] = "bf16") -> np.ndarray:
+    """Dense gated MLP of the shared expert, applied to every token
+    [TileOPs SharedExpertMLPFwdOp]: with w_gate_up [2S, H] the gate rows (0..S)
+    stacked over the up rows (S..2S) and w_down [H, S],
+        out = down(silu(hidden @ gate^T) * (hidden @ up^T)),
+    both products accumulated in float64 here (float32 on the GPU), the gated
+    activation rounded to the input dtype before the down projection, the
+    result rounded to it too."""
+    X = np.asarray(hidden, dtype=np.float64)
+    Wgu = np.asarray(w_gate_up, dtype=np.float64)
+    Wd = np.asarray(w_down, dtype=np.float64)
+    S = Wgu.shape[0] // 2
+    g = X @ Wgu[:S].T
+    u = X @ Wgu[S:].T
+    a = round_to(g * sigmoid64(g) * u, dtype)
+    return round_to(a @ Wd.T, dtype)
+
+
+def ffn_forward_shared(hidden, logits, w_gate_up, w_down, shared_w_gate_up, shared_w_down,
+                       dtype: Optional[str] = "bf16", **routed) -> dict:
+    """Shared + routed MoE FFN [TileOPs FusedMoESharedExpertFwdOp]: the two
+    outputs are returned apart, ``shared`` from shared_expert_mlp and the
+    routed result of ffn_forward (routed_scaling_factor scales the routed
+    output only, once, through the routing weights)."""
+    r = ffn_forward(hidden, logits, w_gate_up, w_down, dtype=dtype, **routed)
+    X = np.asarray(hidden)[r["tokens"]]
+    r["shared"] = shared_expert_mlp(X, shared_w_gate_up, shared_w_down, dtype)
+    return r
+
+
 # --------------------------------------------------------------------------
 # brute force (tiny inputs only): used by the pins, never by the GPU tests
 # --------------------------------------------------------------------------

@@ -417,6 +417,60 @@ def test_linearity_in_rsf_and_combine_one_hot():
     np.testing.assert_array_equal(out, exp)
 
 
+def test_shared_expert_golden_points():
+    """SharedExpertMLPFwdOp on the hand-derived points (no casts)."""
+    L = math.log(3.0)
+    w_gu = np.array([[L, 0.0], [0.0, L], [2.0, 7.0], [4.0, 1.0]])
+    w_d = np.array([[1.0, 3.0], [-2.0, 5.0]])
+    n = 0
+    for line in _golden_lines("shared_expert_points.txt"):
+        x0, x1, o0, o1 = (float(v) for v in line.split())
+        out = O.shared_expert_mlp(np.array([[x0, x1]]), w_gu, w_d, dtype=None)
+        np.testing.assert_allclose(out[0], [o0, o1], rtol=1e-13, atol=1e-13)
+        n += 1
+    assert n == 3
+
+
+def test_shared_expert_brute_force_with_casts():
+    """The shared expert against explicit loops over tokens, hidden and
+    intermediate columns, with the casts where SharedExpertMLPFwdOp puts them
+    (the gated activation rounded to the input dtype before the down GEMM,
+    the result rounded too)."""
+    rng = np.random.default_rng(11)
+    T, H, S = 3, 5, 4
+    x = O.round_bf16(rng.standard_normal((T, H)))
+    w_gu = O.round_bf16(rng.standard_normal((2 * S, H)) * 0.5)
+    w_d = O.round_bf16(rng.standard_normal((H, S)) * 0.5)
+    want = np.zeros((T, H))
+    for t in range(T):
+        act = []
+        for s in range(S):
+            g = sum(x[t, h] * w_gu[s, h] for h in range(H))
+            u = sum(x[t, h] * w_gu[S + s, h] for h in range(H))
+            act.append(float(O.round_bf16(g / (1.0 + math.exp(-g)) * u)))
+        for h in range(H):
+            want[t, h] = float(O.round_bf16(sum(act[s] * w_d[h, s] for s in range(S))))
+    np.testing.assert_array_equal(O.shared_expert_mlp(x, w_gu, w_d, dtype="bf16"), want)
+
+
+def test_shared_plus_routed_returns_both_apart():
+    """FusedMoESharedExpertFwdOp: the routed output is the routed forward's
+    (rsf applied once, to it only) and the shared output the shared MLP's."""
+    rng = np.random.default_rng(12)
+    T, H, F, E, K, S = 6, 8, 4, 4, 2, 6
+    x = O.round_bf16(rng.standard_normal((T, H)))
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    w_gu = O.round_bf16(rng.standard_normal((E, 2 * F, H)) * 0.3)
+    w_d = O.round_bf16(rng.standard_normal((E, H, F)) * 0.3)
+    s_gu = O.round_bf16(rng.standard_normal((2 * S, H)) * 0.3)
+    s_d = O.round_bf16(rng.standard_normal((H, S)) * 0.3)
+    r1 = O.ffn_forward_shared(x, logits, w_gu, w_d, s_gu, s_d, dtype=None, K=K, F=F, rsf=1.0)
+    r3 = O.ffn_forward_shared(x, logits, w_gu, w_d, s_gu, s_d, dtype=None, K=K, F=F, rsf=3.0)
+    np.testing.assert_allclose(r3["out"], 3.0 * r1["out"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(r3["shared"], r1["shared"])
+    np.testing.assert_array_equal(r1["shared"], O.shared_expert_mlp(x, s_gu, s_d, dtype=None))
+
+
 def test_planted_mistakes_are_caught(monkeypatch):
     """A wrong sign in the sigmoid, swapped gate/up halves, or ties to the higher
     index each make one of the pins above fail."""
@@ -425,6 +479,25 @@ def test_planted_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_swiglu_golden_points()
     monkeypatch.setattr(O, "sigmoid64", orig)
+
+    # the shared expert: a flipped sigmoid, swapped gate/up halves or a
+    # transposed down weight each fail its golden points
+    monkeypatch.setattr(O, "sigmoid64", lambda x: orig(-np.asarray(x)))
+    with pytest.raises(AssertionError):
+        test_shared_expert_golden_points()
+    monkeypatch.setattr(O, "sigmoid64", orig)
+    orig_shared = O.shared_expert_mlp
+
+    def swapped(hidden, w_gate_up, w_down, dtype="bf16"):
+        S = np.asarray(w_gate_up).shape[0] // 2
+        w = np.concatenate([np.asarray(w_gate_up)[S:], np.asarray(w_gate_up)[:S]])
+        return orig_shared(hidden, w, w_down, dtype)
+
+    for bad in (swapped, lambda h, gu, d, dtype="bf16": orig_shared(h, gu, np.asarray(d).T, dtype)):
+        monkeypatch.setattr(O, "shared_expert_mlp", bad)
+        with pytest.raises(AssertionError):
+            test_shared_expert_golden_points()
+    monkeypatch.setattr(O, "shared_expert_mlp", orig_shared)
 
     orig_split = O.split_gate_up
     monkeypatch.setattr(O, "split_gate_up", lambda P, F, f: orig_split(P, F, f)[::-1])
