@@ -555,6 +555,8 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
     profiler captures)."""
     import torch
 
+    from mixture_experts_ffn_gb300 import synth
+
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
     dev = inp["hidden"].device
     gathered = cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
@@ -587,9 +589,36 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
                                                        inp["b_down"], out=y),
         "combine": lambda: moe.moe_combine(y, tw, perm["route_to_row"]),
     }
+    extra = {}
+    if args.stage == "shared_mlp":
+        # the shared expert (dense gated MLP, intermediate size --shared-s) on
+        # the workload's tokens
+        S = args.shared_s
+        sw = synth.make_shared_expert(cfg, S, dev)
+        sh_out = torch.empty_like(inp["hidden"])
+        sh_ws = moe._ws(moe.moe_shared_expert_workspace_size(
+            T, H, S, moe.MOE_BF16 if cfg.dtype == "bf16" else moe.MOE_F32), dev)
+        fns["shared_mlp"] = lambda: moe.moe_shared_expert_mlp(
+            inp["hidden"], sw["shared_w_gate_up"], sw["shared_w_down"], out=sh_out, ws=sh_ws)
+        b = 2 if cfg.dtype == "bf16" else 4
+        extra = {"S": S, "flops": 6.0 * T * H * S,
+                 "bytes": 3 * S * H * b + 2 * T * H * b + 2 * T * S * b}
     st, nl = timed(fns[args.stage], args.steps, args.warmup)
-    print(json.dumps({"stage": args.stage, "workload": args.workload,
-                      "us": [round(1e3 * x, 2) for x in st], "launches": nl}), flush=True)
+    line = {"stage": args.stage, "workload": args.workload,
+            "us": [round(1e3 * x, 2) for x in st], "launches": nl}
+    if extra:
+        pk, pk_src = load_peaks()
+        us = 1e3 * sorted(st)[len(st) // 2]
+        tf = extra["flops"] / (us * 1e-6) / 1e12
+        gbs = extra["bytes"] / (us * 1e-6) / 1e9
+        bound = ("tensor" if extra["flops"] / (pk["bf16_tflops"] * 1e12)
+                 > extra["bytes"] / (pk["hbm_gbs"] * 1e9) else "hbm")
+        extra.update({"us_median": round(us, 2), "tflops": round(tf, 1), "gbs": round(gbs, 1),
+                      "bound": bound,
+                      "frac": round(tf / pk["bf16_tflops"] if bound == "tensor"
+                                    else gbs / pk["hbm_gbs"], 3), "peak_source": pk_src})
+        line.update(extra)
+    print(json.dumps(line), flush=True)
 
 
 def cpu_baseline(args, cfg, inp):
@@ -637,8 +666,11 @@ def main():
                          "reduced cases only; the bench line of record uses none)")
     ap.add_argument("--stage", default=None,
                     choices=["route", "route_permute", "permute", "gemm_act", "gemm_down",
-                             "combine", "indexed_mlp"],
+                             "combine", "indexed_mlp", "shared_mlp"],
                     help="time one stage alone (for profiler captures)")
+    ap.add_argument("--shared-s", type=int, default=2048,
+                    help="intermediate size of the shared expert timed by --stage shared_mlp "
+                         "(DeepSeek-V3: 2048)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     rank, world, local = dist_env()

@@ -388,6 +388,42 @@ moe_status moe_ffn_forward_host(const void* hidden_host, const float* logits_hos
 size_t moe_workspace_size_host(int T, int H, int F, int E, int K, moe_dtype dtype);
 
 /* ------------------------------------------------------------------------ */
+/* Shared expert [TileOPs, SharedExpertMLPFwdOp]: the dense gated MLP applied
+ * to every token,
+ *     out = down(silu(hidden @ gate^T) * (hidden @ up^T)),
+ * both products accumulated in fp32, the gated activation rounded to the
+ * operand dtype before the down projection.  Run as the grouped GEMMs over a
+ * single segment of T rows (bf16 on the tensor cores when H % 8 == 0 and
+ * S % 8 == 0 with 16-byte aligned buffers; the exact-fp32 SIMT GEMM
+ * otherwise).
+ *
+ *   hidden [T, H] dtype;  w_gate_up [2S, H] dtype (the S gate rows, then the
+ *   S up rows);  w_down [H, S] dtype;  out [T, H] dtype;
+ *   ws >= moe_shared_expert_workspace_size(T, H, S, dtype) (its status word
+ *   as in every call). */
+moe_status moe_shared_expert_mlp(const void* hidden, const void* w_gate_up, const void* w_down,
+                                 int T, int H, int S, moe_dtype dtype, void* out, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream);
+size_t moe_shared_expert_workspace_size(int T, int H, int S, moe_dtype dtype);
+
+/* Shared + routed MoE FFN [TileOPs, FusedMoESharedExpertFwdOp] with
+ * tp_size 1: routed_out as moe_ffn_forward (no expert_ids, no biases;
+ * routed_scaling_factor scales the routed output only, once) and shared_out
+ * as moe_shared_expert_mlp, returned apart.  shared_w_gate_up and
+ * shared_w_down are passed together (then shared_out is written) or both
+ * NULL (shared_out untouched, S ignored).  The two halves run one after the
+ * other on `stream` and share `ws`:
+ * ws >= moe_workspace_size_shared(T, H, F, S, E, K, dtype). */
+moe_status moe_ffn_forward_shared(const void* hidden, const float* logits, const void* w_gate_up,
+                                  const void* w_down, const float* correction_bias,
+                                  const void* shared_w_gate_up, const void* shared_w_down, int T,
+                                  int H, int F, int S, int E, moe_dtype dtype,
+                                  const moe_route_params* p, const moe_act_params* act,
+                                  void* routed_out, void* shared_out, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream);
+size_t moe_workspace_size_shared(int T, int H, int F, int S, int E, int K, moe_dtype dtype);
+
+/* ------------------------------------------------------------------------ */
 /* Sizes and status.  (The workspace query plays the role of the peak-memory
  * query of [ORT-MoE].) */
 

@@ -3,6 +3,7 @@
 // an invalid call writes nothing.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -501,6 +502,104 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   return ffn_forward(hidden, logits, w_gate_up, w_down, correction_bias, expert_ids, b_gate_up,
                      b_down, T, H, F, E, dtype, p, act, out, topk_weights_out, topk_ids_out,
                      router_probs, weight_scale, ws, ws_bytes, stream, nullptr);
+}
+
+// ---- shared expert [TileOPs, SharedExpertMLPFwdOp]: the grouped GEMMs over one
+// segment of T rows (no routing, no permutation): gate_up with silu_and_mul
+// fused (gate rows then up rows, the stacked layout), then down.
+namespace {
+struct SharedWs {
+  size_t seg_end, act, total;
+  SharedWs(int T, int S, size_t esz) {
+    seg_end = MOE_STATUS_BYTES;
+    act = seg_end + 256;
+    total = act + align256((size_t)T * S * esz);
+  }
+};
+
+moe_status shared_checked(const void* hidden, const void* w_gate_up, const void* w_down, int T,
+                          int H, int S, moe_dtype dtype, void* out, void* ws, cudaStream_t stream) {
+  if (T == 0) return MOE_OK;
+  const size_t esz = esize(dtype);
+  SharedWs L(T, S, esz);
+  char* base = static_cast<char*>(ws);
+  int* status = reinterpret_cast<int*>(base);
+  int32_t* seg_end = reinterpret_cast<int32_t*>(base + L.seg_end);
+  void* a1 = base + L.act;
+  moe_act_params act{};
+  act.kind = MOE_ACT_SILU_AND_MUL;
+  act.swiglu_fusion = 2;
+  if (launch_fill_i32(seg_end, T, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (grouped_gemm(hidden, w_gate_up, nullptr, seg_end, T, S, H, 1, dtype, &act, a1, status,
+                   stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return cuda_status(
+      grouped_gemm(a1, w_down, nullptr, seg_end, T, H, S, 1, dtype, nullptr, out, status, stream));
+}
+}  // namespace
+
+size_t moe_shared_expert_workspace_size(int T, int H, int S, moe_dtype dtype) {
+  if (T < 0 || H < 1 || S < 1 || !dtype_ok(dtype)) return 0;
+  return SharedWs(T, S, esize(dtype)).total;
+}
+
+moe_status moe_shared_expert_mlp(const void* hidden, const void* w_gate_up, const void* w_down,
+                                 int T, int H, int S, moe_dtype dtype, void* out, void* ws,
+                                 size_t ws_bytes, cudaStream_t stream) {
+  if (T < 0 || H < 1 || S < 1 || !dtype_ok(dtype)) return MOE_ERR_INVALID_ARG;
+  if ((long long)T >= (1LL << 30)) return MOE_ERR_INVALID_ARG;
+  if (!w_gate_up || !w_down || (T > 0 && (!hidden || !out))) return MOE_ERR_INVALID_ARG;
+  const size_t esz = esize(dtype);
+  SharedWs L(T, S, esz);
+  if (!ws_ok(ws, ws_bytes, L.total)) return MOE_ERR_WORKSPACE;
+  Span outs[] = {{out, (size_t)T * H * esz}, {ws, L.total}};
+  Span ins[] = {{hidden, (size_t)T * H * esz},
+                {w_gate_up, (size_t)2 * S * H * esz},
+                {w_down, (size_t)H * S * esz}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  return shared_checked(hidden, w_gate_up, w_down, T, H, S, dtype, out, ws, stream);
+}
+
+size_t moe_workspace_size_shared(int T, int H, int F, int S, int E, int K, moe_dtype dtype) {
+  const size_t a = moe_workspace_size(T, H, F, E, K, dtype);
+  const size_t b = moe_shared_expert_workspace_size(T, H, S, dtype);
+  return a == 0 || b == 0 ? 0 : std::max(a, b);
+}
+
+moe_status moe_ffn_forward_shared(const void* hidden, const float* logits, const void* w_gate_up,
+                                  const void* w_down, const float* correction_bias,
+                                  const void* shared_w_gate_up, const void* shared_w_down, int T,
+                                  int H, int F, int S, int E, moe_dtype dtype,
+                                  const moe_route_params* p, const moe_act_params* act,
+                                  void* routed_out, void* shared_out, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+  const bool has_shared = shared_w_gate_up != nullptr;
+  if (has_shared != (shared_w_down != nullptr) || (has_shared && !shared_out))
+    return MOE_ERR_INVALID_ARG;
+  if (has_shared && (S < 1 || (long long)T >= (1LL << 30))) return MOE_ERR_INVALID_ARG;
+  if (!p) return MOE_ERR_INVALID_ARG;
+  const size_t need = has_shared ? moe_workspace_size_shared(T, H, F, S, E, p->top_k, dtype)
+                                 : moe_workspace_size(T, H, F, E, p->top_k, dtype);
+  if (need == 0) return MOE_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, need)) return MOE_ERR_WORKSPACE;
+  if (has_shared) {
+    const size_t esz = esize(dtype);
+    Span outs[] = {{shared_out, (size_t)T * H * esz}, {routed_out, (size_t)T * H * esz},
+                   {ws, need}};
+    Span ins[] = {{hidden, (size_t)T * H * esz},
+                  {shared_w_gate_up, (size_t)2 * S * H * esz},
+                  {shared_w_down, (size_t)H * S * esz}};
+    if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  }
+  // the routed half (its own checks; rsf folded into its weights, so it
+  // scales the routed output only), then the shared expert on the same
+  // workspace (the launches are ordered on the stream)
+  moe_status st = moe_ffn_forward(hidden, logits, w_gate_up, w_down, correction_bias, nullptr,
+                                  nullptr, nullptr, T, H, F, E, dtype, p, act, routed_out, nullptr,
+                                  nullptr, nullptr, nullptr, ws, ws_bytes, stream);
+  if (st != MOE_OK || !has_shared) return st;
+  return shared_checked(hidden, shared_w_gate_up, shared_w_down, T, H, S, dtype, shared_out, ws,
+                        stream);
 }
 
 size_t moe_workspace_size_host(int T, int H, int F, int E, int K, moe_dtype dtype) {

@@ -109,6 +109,9 @@ cudaError_t launch_permute_gather(const void* hidden, int esz, int T, int H, int
 // mapped for the device.
 cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s);
 
+// p[0, n) = v on the stream.
+cudaError_t launch_fill_i32(int32_t* p, int32_t v, int n, cudaStream_t s);
+
 cudaError_t launch_combine(const void* y, const float* w, const int32_t* route_to_row, int T,
                            int K, int H, moe_dtype dt, float scale, void* out, cudaStream_t s);
 

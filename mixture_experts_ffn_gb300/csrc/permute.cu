@@ -276,7 +276,19 @@ __global__ void __launch_bounds__(256) copy16_kernel(const int4* __restrict__ sr
   for (; i < n; i += stride) dst[i] = src[i];
 }
 
+__global__ void fill_i32_kernel(int32_t* __restrict__ p, int32_t v, int n) {
+  pdl_wait();  // the buffer may still be read by the previous launch
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
+}
+
 }  // namespace
+
+cudaError_t launch_fill_i32(int32_t* p, int32_t v, int n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  launch_pdl(fill_i32_kernel, (n + 255) / 256, 256, 0, s, p, v, n);
+  count_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s) {
   if (bytes == 0) return cudaSuccess;

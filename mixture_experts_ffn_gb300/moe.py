@@ -59,6 +59,11 @@ _SIGNATURES = {
                         _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_ffn_forward_host": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
                              _vp, _vp, _vp, _sz, _vp],
+    "moe_shared_expert_mlp": [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
+    "moe_shared_expert_workspace_size": [_i, _i, _i, _i],
+    "moe_ffn_forward_shared": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
+                               _vp, _vp, _vp, _vp, _sz, _vp],
+    "moe_workspace_size_shared": [_i, _i, _i, _i, _i, _i, _i],
     "moe_workspace_size": [_i, _i, _i, _i, _i, _i],
     "moe_workspace_size_host": [_i, _i, _i, _i, _i, _i],
     "moe_permute_workspace_size": [_i, _i],
@@ -69,7 +74,8 @@ _SIGNATURES = {
     "moe_set_gemm_simt": [_i],
 }
 _RESTYPES = {"moe_workspace_size": _sz, "moe_permute_workspace_size": _sz,
-             "moe_workspace_size_host": _sz,
+             "moe_workspace_size_host": _sz, "moe_shared_expert_workspace_size": _sz,
+             "moe_workspace_size_shared": _sz,
              "moe_status_string": ctypes.c_char_p, "moe_launch_count": ctypes.c_uint64}
 
 _lib = None
@@ -366,6 +372,58 @@ def moe_ffn_forward(hidden, logits, w_gate_up, w_down, p: RouteParams, act: ActP
                                _p(topk_weights_out), _p(topk_ids_out), _p(router_probs),
                                _p(weight_scale), _p(ws), ws.numel(), _stream()))
     return out
+
+
+def moe_shared_expert_workspace_size(T, H, S, dtype=MOE_BF16) -> int:
+    return load_library().moe_shared_expert_workspace_size(T, H, S, dtype)
+
+
+def moe_workspace_size_shared(T, H, F, S, E, K, dtype=MOE_BF16) -> int:
+    return load_library().moe_workspace_size_shared(T, H, F, S, E, K, dtype)
+
+
+def moe_shared_expert_mlp(hidden, w_gate_up, w_down, out=None, ws=None):
+    """Shared expert: down(silu(hidden @ gate^T) * (hidden @ up^T)) for every
+    token; w_gate_up [2S, H] (gate rows then up rows), w_down [H, S]."""
+    lib = load_library()
+    _cuda(hidden, w_gate_up, w_down)
+    T, H = hidden.shape
+    S = w_down.shape[1]
+    if out is None:
+        out = torch.empty_like(hidden)
+    if ws is None:
+        ws = _ws(lib.moe_shared_expert_workspace_size(T, H, S, _dt(hidden)), hidden.device)
+    _check("moe_shared_expert_mlp",
+           lib.moe_shared_expert_mlp(_p(hidden), _p(w_gate_up), _p(w_down), T, H, S, _dt(hidden),
+                                     _p(out), _p(ws), ws.numel(), _stream()))
+    return out
+
+
+def moe_ffn_forward_shared(hidden, logits, w_gate_up, w_down, p: RouteParams, act: ActParams,
+                           correction_bias=None, shared_w_gate_up=None, shared_w_down=None,
+                           routed_out=None, shared_out=None, ws=None):
+    """Shared + routed MoE FFN; returns (shared_out or None, routed_out)."""
+    lib = load_library()
+    _cuda(hidden, logits, w_gate_up, w_down, correction_bias, shared_w_gate_up, shared_w_down)
+    T, H = hidden.shape
+    E, _, F = w_down.shape
+    S = shared_w_down.shape[1] if shared_w_down is not None else 0
+    if routed_out is None:
+        routed_out = torch.empty_like(hidden)
+    if shared_w_gate_up is not None and shared_out is None:
+        shared_out = torch.empty_like(hidden)
+    if ws is None:
+        need = (lib.moe_workspace_size_shared(T, H, F, S, E, p.top_k, _dt(hidden)) if S else
+                lib.moe_workspace_size(T, H, F, E, p.top_k, _dt(hidden)))
+        ws = _ws(need, hidden.device)
+    _check("moe_ffn_forward_shared",
+           lib.moe_ffn_forward_shared(_p(hidden), _p(logits), _p(w_gate_up), _p(w_down),
+                                      _p(correction_bias), _p(shared_w_gate_up),
+                                      _p(shared_w_down), T, H, F, S, E, _dt(hidden),
+                                      ctypes.byref(p), ctypes.byref(act), _p(routed_out),
+                                      _p(shared_out if shared_w_gate_up is not None else None),
+                                      _p(ws), ws.numel(), _stream()))
+    return (shared_out if shared_w_gate_up is not None else None), routed_out
 
 
 def moe_workspace_size_host(T, H, F, E, K, dtype=MOE_BF16) -> int:

@@ -34,6 +34,7 @@ import torch
 
 # tensor ids used in the per-tensor seed
 TID_HIDDEN, TID_LOGITS, TID_W1, TID_W2, TID_CBIAS, TID_B1, TID_B2, TID_IDS = range(8)
+TID_SW1, TID_SW2 = 8, 9  # shared-expert weights
 
 # activation kinds (mirror the values of the C header's moe_act_kind)
 ACT_SILU_AND_MUL = 0
@@ -185,6 +186,19 @@ def make_inputs(cfg: MoEConfig, device="cpu", weight_device=None, logits=None) -
     inp["w_down"] = _normal_rows(cfg.E, (cfg.H, cfg.F), 1.0 / math.sqrt(cfg.F),
                                  _gen(cfg, TID_W2, wdev), wdev, dt).to(device)
     return inp
+
+
+def make_shared_expert(cfg: MoEConfig, S: int, device="cpu") -> dict:
+    """Weights of a shared expert with intermediate size S for ``cfg``'s
+    hidden size: w_gate_up [2S, H] (std 1/sqrt(H)) and w_down [H, S]
+    (std 1/sqrt(S)), drawn on ``device`` in the operand dtype."""
+    dt = torch_dtype(cfg.dtype)
+    return {
+        "shared_w_gate_up": _normal((2 * S, cfg.H), 1.0 / math.sqrt(cfg.H),
+                                    _gen(cfg, TID_SW1, device), device, dt),
+        "shared_w_down": _normal((cfg.H, S), 1.0 / math.sqrt(S), _gen(cfg, TID_SW2, device),
+                                 device, dt),
+    }
 
 
 def subset_tokens(T: int, n: int = 256) -> list:
