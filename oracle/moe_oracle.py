@@ -468,6 +468,56 @@ def ffn_forward_shared(hidden, logits, w_gate_up, w_down, shared_w_gate_up, shar
 
 
 # --------------------------------------------------------------------------
+# block-scaled FP8 grouped GEMM over a masked slab [TileOPs MoEGroupedGemmFP8FwdOp]
+# --------------------------------------------------------------------------
+def e4m3_to_float(codes) -> np.ndarray:
+    """Values of float8_e4m3fn codes (uint8): 1 sign bit, 4 exponent bits with
+    bias 7, 3 mantissa bits; exponent 0 encodes subnormals m/8 * 2**-6; no
+    infinities, and S.1111.111 (0x7F, 0xFF) is NaN."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    out = sign * mag
+    return np.where((c & 0x7F) == 0x7F, np.nan, out)
+
+
+FP8_BLOCK = 128  # K (and N) block of one scale [TileOPs MoEGroupedGemmFP8FwdOp]
+
+
+def grouped_gemm_fp8_masked(a_codes, a_scale, b_codes, b_scale, counts,
+                            dtype: Optional[str] = "bf16") -> np.ndarray:
+    """out[g, :m_g] = a[g, :m_g] @ b[g]^T with one float32 scale per row and
+    128 K-columns of a (a_scale [E, max_m, K/128]) and one per 128 x 128 block
+    of b (b_scale [E, N/128, K/128]): each 128-wide K block is contracted from
+    the raw FP8 values, multiplied by its two scales and added to the
+    accumulator; m_g = counts[g] read as min(max(m_g, 0), max_m).  Rows at or
+    past m_g are undefined on the pages; NaN here.  Float64 arithmetic, the
+    result rounded to ``dtype`` [TileOPs MoEGroupedGemmFP8FwdOp]."""
+    A = e4m3_to_float(a_codes)
+    B = e4m3_to_float(b_codes)
+    sa = np.asarray(a_scale, dtype=np.float64)
+    sb = np.asarray(b_scale, dtype=np.float64)
+    E, max_m, K = A.shape
+    N = B.shape[1]
+    if K % FP8_BLOCK or N % FP8_BLOCK:
+        raise ValueError("K and N must be multiples of 128")
+    nkb = K // FP8_BLOCK
+    out = np.full((E, max_m, N), np.nan)
+    for g in range(E):
+        m = min(max(int(counts[g]), 0), max_m)
+        acc = np.zeros((m, N))
+        for kb in range(nkb):
+            ks = slice(kb * FP8_BLOCK, (kb + 1) * FP8_BLOCK)
+            part = A[g, :m, ks] @ B[g, :, ks].T                     # raw FP8 values
+            bs = np.repeat(sb[g, :, kb], FP8_BLOCK)[:N]             # b scale of each column
+            acc += part * sa[g, :m, kb][:, None] * bs[None, :]
+        out[g, :m] = round_to(acc, dtype)
+    return out
+
+
+# --------------------------------------------------------------------------
 # brute force (tiny inputs only): used by the pins, never by the GPU tests
 # --------------------------------------------------------------------------
 def brute_force_selection(u_row, K: int, G: int, TG: int, biased: bool):

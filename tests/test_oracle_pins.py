@@ -471,6 +471,102 @@ def test_shared_plus_routed_returns_both_apart():
     np.testing.assert_array_equal(r1["shared"], O.shared_expert_mlp(x, s_gu, s_d, dtype=None))
 
 
+def test_e4m3_golden_points():
+    n = 0
+    for line in _golden_lines("e4m3_points.txt"):
+        code, val = line.split()[:2]
+        got = float(O.e4m3_to_float(np.array([int(code, 16)], dtype=np.uint8))[0])
+        if val == "nan":
+            assert math.isnan(got), code
+        else:
+            assert got == float(val) and math.copysign(1.0, got) == math.copysign(1.0, float(val)), code
+        n += 1
+    assert n == 16
+
+
+def test_e4m3_every_code_matches_torch():
+    """Every code decodes as torch's own float8_e4m3fn conversion does."""
+    codes = np.arange(256, dtype=np.uint8)
+    mine = O.e4m3_to_float(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(np.isnan(mine), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(mine[ok], ref[ok])
+
+
+def _fp8_case(rng, E, max_m, N, K, int_values=False):
+    if int_values:  # small integers: 1..4 and their negatives are exact e4m3 values
+        lut = {1: 0x38, 2: 0x40, 3: 0x44, 4: 0x48}
+        va = rng.integers(-4, 5, size=(E, max_m, K))
+        vb = rng.integers(-4, 5, size=(E, N, K))
+        enc = np.vectorize(lambda v: 0 if v == 0 else (lut[abs(v)] | (0x80 if v < 0 else 0)))
+        a, b = enc(va).astype(np.uint8), enc(vb).astype(np.uint8)
+    else:
+        a = rng.integers(0, 256, size=(E, max_m, K)).astype(np.uint8)
+        b = rng.integers(0, 256, size=(E, N, K)).astype(np.uint8)
+        a[(a & 0x7F) == 0x7F] = 0x38   # no NaN codes
+        b[(b & 0x7F) == 0x7F] = 0x38
+    sa = np.exp2(rng.integers(-3, 4, size=(E, max_m, K // 128))).astype(np.float32)
+    sb = np.exp2(rng.integers(-3, 4, size=(E, N // 128, K // 128))).astype(np.float32)
+    return a, sa, b, sb
+
+
+def test_fp8_grouped_gemm_brute_force():
+    """Block-scaled FP8 masked GEMM against explicit loops: per 128-wide K
+    block the raw FP8 products are summed, then scaled by the row's and the
+    block's scale [TileOPs MoEGroupedGemmFP8FwdOp]; rows past the count are
+    left undefined."""
+    rng = np.random.default_rng(21)
+    E, max_m, N, K = 2, 3, 128, 256
+    a, sa, b, sb = _fp8_case(rng, E, max_m, N, K, int_values=True)
+    counts = [3, 2]
+    got = O.grouped_gemm_fp8_masked(a, sa, b, sb, counts, dtype=None)
+    va, vb = O.e4m3_to_float(a), O.e4m3_to_float(b)
+    for g in range(E):
+        for r in range(max_m):
+            if r >= counts[g]:
+                assert np.isnan(got[g, r]).all()
+                continue
+            for n in range(0, N, 37):
+                total = 0.0
+                for kb in range(K // 128):
+                    part = sum(va[g, r, k] * vb[g, n, k] for k in range(kb * 128, kb * 128 + 128))
+                    total += part * float(sa[g, r, kb]) * float(sb[g, n // 128, kb])
+                assert got[g, r, n] == total, (g, r, n)
+
+
+def test_fp8_scales_act_per_block():
+    """Doubling one K block's scales doubles that block's contribution only."""
+    rng = np.random.default_rng(22)
+    E, max_m, N, K = 1, 4, 256, 384
+    a, sa, b, sb = _fp8_case(rng, E, max_m, N, K)
+    base = O.grouped_gemm_fp8_masked(a, sa, b, sb, [4], dtype=None)
+    sa2 = sa.copy()
+    sa2[:, :, 1] *= 2
+    twice = O.grouped_gemm_fp8_masked(a, sa2, b, sb, [4], dtype=None)
+    va, vb = O.e4m3_to_float(a), O.e4m3_to_float(b)
+    blk = (va[0, :, 128:256] @ vb[0, :, 128:256].T) * sa[0, :, 1][:, None] * \
+        np.repeat(sb[0, :, 1], 128)[None, :]
+    np.testing.assert_allclose(twice[0] - base[0], blk, rtol=1e-12, atol=1e-9)
+    sb2 = sb.copy()
+    sb2[0, 1, 0] *= 4  # columns 128..255, K block 0
+    other = O.grouped_gemm_fp8_masked(a, sa, b, sb2, [4], dtype=None)
+    np.testing.assert_array_equal(other[0, :, :128], base[0, :, :128])
+    assert not np.array_equal(other[0, :, 128:], base[0, :, 128:])
+
+
+def test_fp8_counts_are_clamped():
+    """A count past max_m is read as max_m, a negative one as 0."""
+    rng = np.random.default_rng(23)
+    a, sa, b, sb = _fp8_case(rng, 3, 5, 128, 128)
+    got = O.grouped_gemm_fp8_masked(a, sa, b, sb, [-3, 99, 2], dtype=None)
+    assert np.isnan(got[0]).all()
+    assert not np.isnan(got[1]).any()
+    full = O.grouped_gemm_fp8_masked(a, sa, b, sb, [5, 5, 5], dtype=None)
+    np.testing.assert_array_equal(got[1], full[1])
+    np.testing.assert_array_equal(got[2, :2], full[2, :2])
+
+
 def test_planted_mistakes_are_caught(monkeypatch):
     """A wrong sign in the sigmoid, swapped gate/up halves, or ties to the higher
     index each make one of the pins above fail."""
@@ -498,6 +594,23 @@ def test_planted_mistakes_are_caught(monkeypatch):
         with pytest.raises(AssertionError):
             test_shared_expert_golden_points()
     monkeypatch.setattr(O, "shared_expert_mlp", orig_shared)
+
+    # fp8: a wrong exponent bias, or the b scale taken per row block instead
+    # of per column block, each fail a pin
+    orig_dec = O.e4m3_to_float
+    monkeypatch.setattr(O, "e4m3_to_float", lambda c: orig_dec(c) * 2.0)
+    with pytest.raises(AssertionError):
+        test_e4m3_golden_points()
+    monkeypatch.setattr(O, "e4m3_to_float", orig_dec)
+    orig_fp8 = O.grouped_gemm_fp8_masked
+
+    def scale_swapped(a, sa, b, sb, counts, dtype="bf16"):
+        return orig_fp8(a, sa, b, np.ascontiguousarray(np.asarray(sb)[:, ::-1]), counts, dtype)
+
+    monkeypatch.setattr(O, "grouped_gemm_fp8_masked", scale_swapped)
+    with pytest.raises(AssertionError):
+        test_fp8_scales_act_per_block()
+    monkeypatch.setattr(O, "grouped_gemm_fp8_masked", orig_fp8)
 
     orig_split = O.split_gate_up
     monkeypatch.setattr(O, "split_gate_up", lambda P, F, f: orig_split(P, F, f)[::-1])
