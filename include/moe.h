@@ -388,6 +388,26 @@ moe_status moe_ffn_forward_host(const void* hidden_host, const float* logits_hos
 size_t moe_workspace_size_host(int T, int H, int F, int E, int K, moe_dtype dtype);
 
 /* ------------------------------------------------------------------------ */
+/* Block-scaled FP8 grouped GEMM over a masked slab [TileOPs, "MoE Operators",
+ * MoEGroupedGemmFP8FwdOp]: out[g, :m_g] = a[g, :m_g] @ b[g]^T.
+ *
+ * a [E, max_m, K] and b [E, N, K] hold float8_e4m3fn codes (one byte each);
+ * a_scale [E, max_m, K/128] f32 holds one scale per row and 128 columns of a,
+ * b_scale [E, N/128, K/128] f32 one per 128 x 128 block of b; K and N are
+ * multiples of 128.  Each 128-wide K block is contracted from the raw FP8
+ * values, then multiplied by its two scales and added to an fp32
+ * accumulator; out [E, max_m, N] is bf16.  m_g = layout_metadata[g] is read
+ * as min(max(m_g, 0), max_m) on the device (counts are not checked on the
+ * host); rows at or past m_g are not written (their contents are
+ * undefined), and nothing outside out is.  a and b 16-byte aligned, the
+ * scales 4-byte aligned (MOE_ERR_UNSUPPORTED otherwise); ws >=
+ * MOE_STATUS_BYTES bytes.  E <= 1024. */
+moe_status moe_grouped_gemm_fp8_masked(const void* a, const float* a_scale, const void* b,
+                                       const float* b_scale, const int32_t* layout_metadata,
+                                       int E, int max_m, int N, int K, void* out, void* ws,
+                                       size_t ws_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Shared expert [TileOPs, SharedExpertMLPFwdOp]: the dense gated MLP applied
  * to every token,
  *     out = down(silu(hidden @ gate^T) * (hidden @ up^T)),

@@ -221,6 +221,30 @@ moe_status moe_permute_gather(const void* hidden, moe_dtype dtype, const int32_t
                                            expert_input, ws, stream));
 }
 
+moe_status moe_grouped_gemm_fp8_masked(const void* a, const float* a_scale, const void* b,
+                                       const float* b_scale, const int32_t* layout_metadata,
+                                       int E, int max_m, int N, int K, void* out, void* ws,
+                                       size_t ws_bytes, cudaStream_t stream) {
+  if (E < 1 || E > kMaxExperts || max_m < 0 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (K % 128 || N % 128) return MOE_ERR_INVALID_ARG;  // scale blocks of 128
+  if ((long long)E * max_m >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+  if (!layout_metadata || (max_m > 0 && (!a || !a_scale || !b || !b_scale || !out)))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, MOE_STATUS_BYTES)) return MOE_ERR_WORKSPACE;
+  if (max_m > 0 && (!aligned16(a) || !aligned16(b) || ((uintptr_t)a_scale & 3) ||
+                    ((uintptr_t)b_scale & 3) || ((uintptr_t)out & 1)))
+    return MOE_ERR_UNSUPPORTED;
+  const size_t nkb = (size_t)K / 128, rows = (size_t)E * max_m;
+  Span outs[] = {{out, rows * N * 2}};
+  Span ins[] = {{a, rows * K}, {a_scale, rows * nkb * 4}, {b, (size_t)E * N * K},
+                {b_scale, (size_t)E * (N / 128) * nkb * 4}, {layout_metadata, (size_t)E * 4},
+                {ws, MOE_STATUS_BYTES}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  if (max_m == 0) return MOE_OK;
+  return cuda_status(launch_gemm_fp8(a, a_scale, b, b_scale, layout_metadata, E, max_m, N, K, out,
+                                     static_cast<int*>(ws), stream));
+}
+
 moe_status moe_grouped_gemm_act(const void* a, const void* w_gate_up, const void* b_gate_up,
                                 const int32_t* seg_end, int M, int F, int Hk, int E,
                                 moe_dtype dtype, const moe_act_params* act, void* out, void* ws,

@@ -26,7 +26,7 @@ constexpr int kEpiCols = 256;  // accumulator columns of one tile
 // path that tcgen05.mma reads its operands through).
 constexpr int OUT_BOX = 32;                        // rows and columns of one staged box
 constexpr int OUT_BUF_BYTES = OUT_BOX * OUT_BOX * 2;  // 2 KB
-constexpr int OUT_BYTES = 4 * 2 * OUT_BUF_BYTES;      // 4 warps x 2 buffers
+constexpr int OUT_BYTES = 8 * OUT_BUF_BYTES;          // 4 warps x 2 buffers, or 8 x 1
 
 // Epilogue activation math.  The exponential and the quotient use the fast
 // hardware approximations (relative error about 1e-6 over the arguments an
@@ -46,6 +46,44 @@ __device__ __forceinline__ float gated(float g, float u, float limit, float alph
       u = fmaxf(fminf(u, limit), -limit);
     }
     return g * fast_sigmoid(alpha * g) * (u + beta);
+  }
+}
+
+// One 32-column chunk of the calling warp's 32 output rows (row wrow0 + lane,
+// columns col0..): a whole 32 x 32 box staged in shared memory and written by
+// one TMA store when `boxed` (all 32 rows inside the segment), else row by
+// row for the rows that are (row_ok).  obufs holds NBUF 2 KB buffers of the
+// warp; obuf is the next one.
+template <int NBUF>
+__device__ __forceinline__ void emit_chunk32(const float (&v)[32], int col0, int wrow0,
+                                             bool boxed, bool row_ok,
+                                             __nv_bfloat16* __restrict__ orow, int ncols_left,
+                                             const CUtensorMap* tm_out, uint8_t* obufs,
+                                             int& obuf, int lane) {
+  if (boxed) {
+    uint8_t* buf = obufs + obuf * OUT_BUF_BYTES;
+    if (lane == 0) bulk_wait_read<NBUF - 1>();  // the last store from this buffer
+    __syncwarp();
+    // row `lane`, 16-byte chunk q lands at chunk q ^ ((lane >> 1) & 3)
+    // (the 64-byte swizzle the output map describes): conflict-free
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 u;
+      u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+      *reinterpret_cast<uint4*>(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = u;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tm_out, buf, col0, wrow0);
+      bulk_commit();
+    }
+    obuf = NBUF == 1 ? 0 : obuf ^ 1;
+  } else if (row_ok) {
+    store_row32(orow + col0, v, ncols_left);
   }
 }
 
@@ -72,31 +110,7 @@ __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end,
   // never writes rows of the next segment.
   const bool boxed = tma_out && m_end - wrow0 >= OUT_BOX;
   auto emit = [&](const float (&v)[32], int col0) {
-    if (boxed) {
-      uint8_t* buf = obufs + obuf * OUT_BUF_BYTES;
-      if (lane == 0) bulk_wait_read<1>();  // the store from this buffer two boxes ago
-      __syncwarp();
-      // row `lane`, 16-byte chunk q lands at chunk q ^ ((lane >> 1) & 3)
-      // (the 64-byte swizzle the output map describes): conflict-free
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint4 u;
-        u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-        u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-        u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-        u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
-        *reinterpret_cast<uint4*>(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = u;
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(tm_out, buf, col0, wrow0);
-        bulk_commit();
-      }
-      obuf ^= 1;
-    } else if (row_ok) {
-      store_row32(orow + col0, v, Nout - col0);
-    }
+    emit_chunk32<2>(v, col0, wrow0, boxed, row_ok, orow, Nout - col0, tm_out, obufs, obuf, lane);
   };
   if constexpr (MODE == kTcPlain) {
 #pragma unroll 1

@@ -135,6 +135,12 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            int* status, cudaStream_t s, const int32_t* gather_rows = nullptr,
                            int gather_div = 1, int gather_src_rows = 0);
 
+// block-scaled FP8 grouped GEMM over a masked slab (e4m3 operands, fp32
+// scales per row x 128 K of a and per 128 x 128 block of b, bf16 out)
+cudaError_t launch_gemm_fp8(const void* a, const float* a_scale, const void* b,
+                            const float* b_scale, const int32_t* counts, int E, int max_m, int N,
+                            int K, void* out, int* status, cudaStream_t s);
+
 // two-SM (cta_group::2) variant of launch_gemm_tc, same contract
 cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
                             const int32_t* seg_end, int M, int N, int K, int E,

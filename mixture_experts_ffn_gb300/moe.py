@@ -60,6 +60,7 @@ _SIGNATURES = {
     "moe_ffn_forward_host": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
                              _vp, _vp, _vp, _sz, _vp],
     "moe_shared_expert_mlp": [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
+    "moe_grouped_gemm_fp8_masked": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
     "moe_shared_expert_workspace_size": [_i, _i, _i, _i],
     "moe_ffn_forward_shared": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                                _vp, _vp, _vp, _vp, _sz, _vp],
@@ -371,6 +372,26 @@ def moe_ffn_forward(hidden, logits, w_gate_up, w_down, p: RouteParams, act: ActP
                                H, F, E, _dt(hidden), ctypes.byref(p), ctypes.byref(act), _p(out),
                                _p(topk_weights_out), _p(topk_ids_out), _p(router_probs),
                                _p(weight_scale), _p(ws), ws.numel(), _stream()))
+    return out
+
+
+def moe_grouped_gemm_fp8_masked(a, a_scale, b, b_scale, layout_metadata, out=None, ws=None):
+    """Block-scaled FP8 GEMM per expert over a masked slab: a [E, max_m, K] and
+    b [E, N, K] float8_e4m3fn (or their uint8 codes), a_scale [E, max_m, K/128]
+    and b_scale [E, N/128, K/128] float32, layout_metadata [E] int32 valid row
+    counts; returns out [E, max_m, N] bf16 (rows past a count undefined)."""
+    lib = load_library()
+    _cuda(a, a_scale, b, b_scale, layout_metadata)
+    E, max_m, K = a.shape
+    N = b.shape[1]
+    if out is None:
+        out = torch.empty((E, max_m, N), dtype=torch.bfloat16, device=a.device)
+    if ws is None:
+        ws = _ws(MOE_STATUS_BYTES, a.device)
+    _check("moe_grouped_gemm_fp8_masked",
+           lib.moe_grouped_gemm_fp8_masked(_p(a), _p(a_scale), _p(b), _p(b_scale),
+                                           _p(layout_metadata), E, max_m, N, K, _p(out), _p(ws),
+                                           ws.numel(), _stream()))
     return out
 
 

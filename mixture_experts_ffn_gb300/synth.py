@@ -201,6 +201,44 @@ def make_shared_expert(cfg: MoEConfig, S: int, device="cpu") -> dict:
     }
 
 
+def _quantize_blocks(x: torch.Tensor, rows_per_block: int):
+    """Block-scaled e4m3 codes of x [.., R, K] with one fp32 scale per
+    rows_per_block rows x 128 columns: scale = amax / 448 (the largest finite
+    e4m3 value), codes = x / scale rounded to float8_e4m3fn by torch."""
+    *lead, R, K = x.shape
+    xb = x.reshape(*lead, R // rows_per_block, rows_per_block, K // 128, 128)
+    amax = xb.abs().amax(dim=(-3, -1)).clamp_min(1e-12)          # [.., R/rb, K/128]
+    scale = (amax / 448.0).to(torch.float32)
+    q = (xb / scale[..., :, None, :, None]).reshape(*lead, R, K).to(torch.float8_e4m3fn)
+    return q, scale
+
+
+def make_fp8_masked(E: int, max_m: int, N: int, K: int, seed: int, device="cpu",
+                    counts=None) -> dict:
+    """Inputs of the block-scaled FP8 masked grouped GEMM: activations
+    a [E, max_m, K] ~ N(0, 1) quantised per row and 128 columns, weights
+    b [E, N, K] ~ N(0, 1/sqrt(K)) quantised per 128 x 128 block, and valid row
+    counts uniform in [max_m/2, max_m] unless given.  Drawn on ``device`` one
+    expert at a time."""
+    g = torch.Generator(device=device)
+    g.manual_seed(7_000_000 + seed)
+    a = torch.empty((E, max_m, K), dtype=torch.float8_e4m3fn, device=device)
+    b = torch.empty((E, N, K), dtype=torch.float8_e4m3fn, device=device)
+    a_scale = torch.empty((E, max_m, K // 128), dtype=torch.float32, device=device)
+    b_scale = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=device)
+    for e in range(E):
+        xa = torch.randn((max_m, K), generator=g, device=device, dtype=torch.float32)
+        a[e], a_scale[e] = _quantize_blocks(xa, 1)
+        xb = torch.randn((N, K), generator=g, device=device, dtype=torch.float32) / math.sqrt(K)
+        b[e], b_scale[e] = _quantize_blocks(xb, 128)
+    if counts is None:
+        gc = torch.Generator()
+        gc.manual_seed(7_100_000 + seed)
+        counts = torch.randint(max_m // 2, max_m + 1, (E,), generator=gc, dtype=torch.int32)
+    counts = torch.as_tensor(counts, dtype=torch.int32).to(device)
+    return {"a": a, "a_scale": a_scale, "b": b, "b_scale": b_scale, "counts": counts}
+
+
 def subset_tokens(T: int, n: int = 256) -> list:
     """Fixed token subset t_i = floor(i * T / n), i < n (all tokens when T <= n)."""
     if T <= n:
