@@ -603,20 +603,36 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
         b = 2 if cfg.dtype == "bf16" else 4
         extra = {"S": S, "flops": 6.0 * T * H * S,
                  "bytes": 3 * S * H * b + 2 * T * H * b + 2 * T * S * b}
+    if args.stage == "fp8_gemm":
+        # block-scaled FP8 masked grouped GEMM, DeepSeek-V3-style expert-parallel
+        # shapes: 8 local experts of up to 256 rows, N 4096 (2F), K 7168 (H)
+        E8, mm, N8, K8 = 8, 256, 4096, 7168
+        f8 = synth.make_fp8_masked(E8, mm, N8, K8, seed=3, device=dev)
+        f8_out = torch.empty((E8, mm, N8), dtype=torch.bfloat16, device=dev)
+        f8_ws = moe._ws(256, dev)
+        fns["fp8_gemm"] = lambda: moe.moe_grouped_gemm_fp8_masked(
+            f8["a"], f8["a_scale"], f8["b"], f8["b_scale"], f8["counts"], out=f8_out, ws=f8_ws)
+        rows = int(f8["counts"].clamp(0, mm).sum())
+        extra = {"E": E8, "max_m": mm, "N": N8, "K": K8, "rows": rows,
+                 "flops": 2.0 * rows * N8 * K8,
+                 "bytes": E8 * N8 * K8 + rows * K8 + rows * N8 * 2
+                 + (E8 * mm + E8 * (N8 // 128)) * (K8 // 128) * 4,
+                 "tensor_peak_dtype": "fp8 (measured bf16 x 2, the nominal fp8 / bf16 ratio)"}
     st, nl = timed(fns[args.stage], args.steps, args.warmup)
     line = {"stage": args.stage, "workload": args.workload,
             "us": [round(1e3 * x, 2) for x in st], "launches": nl}
     if extra:
         pk, pk_src = load_peaks()
+        tpk = pk["bf16_tflops"] * (2.0 if args.stage == "fp8_gemm" else 1.0)
         us = 1e3 * sorted(st)[len(st) // 2]
         tf = extra["flops"] / (us * 1e-6) / 1e12
         gbs = extra["bytes"] / (us * 1e-6) / 1e9
-        bound = ("tensor" if extra["flops"] / (pk["bf16_tflops"] * 1e12)
+        bound = ("tensor" if extra["flops"] / (tpk * 1e12)
                  > extra["bytes"] / (pk["hbm_gbs"] * 1e9) else "hbm")
         extra.update({"us_median": round(us, 2), "tflops": round(tf, 1), "gbs": round(gbs, 1),
                       "bound": bound,
-                      "frac": round(tf / pk["bf16_tflops"] if bound == "tensor"
-                                    else gbs / pk["hbm_gbs"], 3), "peak_source": pk_src})
+                      "frac": round(tf / tpk if bound == "tensor" else gbs / pk["hbm_gbs"], 3),
+                      "peak_source": pk_src})
         line.update(extra)
     print(json.dumps(line), flush=True)
 
@@ -666,7 +682,7 @@ def main():
                          "reduced cases only; the bench line of record uses none)")
     ap.add_argument("--stage", default=None,
                     choices=["route", "route_permute", "permute", "gemm_act", "gemm_down",
-                             "combine", "indexed_mlp", "shared_mlp"],
+                             "combine", "indexed_mlp", "shared_mlp", "fp8_gemm"],
                     help="time one stage alone (for profiler captures)")
     ap.add_argument("--shared-s", type=int, default=2048,
                     help="intermediate size of the shared expert timed by --stage shared_mlp "
