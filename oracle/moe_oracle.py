@@ -437,6 +437,32 @@ def ffn_forward(hidden, logits, w_gate_up, w_down, K: int, F: int, scoring="soft
     return r
 
 
+def ffn_forward_local(hidden, router_probs, weight_scale, w_gate_up, w_down, K: int, F: int,
+                      act=ACT_SILU_AND_MUL, fusion=2, limit=0.0, alpha=1.0, beta=0.0,
+                      dtype: Optional[str] = "bf16") -> np.ndarray:
+    """The layer of one expert-parallel rank holding lc experts (w_gate_up and
+    w_down of those experts only), fed by the MoERouter outputs of its slice
+    [MoERouter: "QMoE's own softmax over the local block returns w_e /
+    W_local", "weight_scale ... multiplies that factor back out of the expert
+    output before the all-reduce"]: the softmax of the token's router_probs
+    row (float32, as the router computes it), its top min(K, lc) experts (ties
+    to the lower index), the weighted sum of their expert MLPs, multiplied by
+    weight_scale[t] and cast once.  Summed over the ranks' slices this is the
+    routed layer with normalised weights (times route_scale)."""
+    rp = np.asarray(router_probs, dtype=np.float32)
+    lc = rp.shape[1]
+    Kl = min(K, lc)
+    r = route(rp, Kl, "softmax", renormalize=False)
+    X = np.asarray(hidden, dtype=np.float64)
+    Xr = np.repeat(X, Kl, axis=0)
+    Y = expert_mlp_routes(Xr, r["topk_ids"].reshape(-1), w_gate_up, w_down, F, act, fusion,
+                          limit, alpha, beta, None, None, dtype)
+    acc = np.zeros_like(X)
+    for k in range(Kl):
+        acc += r["topk_weights"][:, k:k + 1] * Y[k::Kl]
+    return round_to(np.asarray(weight_scale, dtype=np.float64)[:, None] * acc, dtype)
+
+
 def shared_expert_mlp(hidden, w_gate_up, w_down, dtype: Optional[str] = "bf16") -> np.ndarray:
     """Dense gated MLP of the shared expert, applied to every token
     [TileOPs SharedExpertMLPFwdOp]: with w_gate_up [2S, H] the gate rows (0..S)

@@ -294,6 +294,31 @@ def test_moerouter_qmoe_softmax_invariant():
     np.testing.assert_allclose(recon, w_hat, rtol=1e-10, atol=1e-300)
 
 
+def test_expert_parallel_slices_sum_to_the_layer():
+    """The expert-parallel contract end to end: every rank runs its experts
+    from its own MoERouter outputs (router_probs through its own softmax and
+    top-k, the sum scaled by weight_scale); the ranks' outputs add up to the
+    routed layer with normalised weights, on every token, including tokens
+    with no expert on a rank."""
+    rng = np.random.default_rng(31)
+    T, H, F, E, K, lc = 40, 8, 4, 16, 4, 4
+    x = O.round_bf16(rng.standard_normal((T, H)))
+    z = rng.standard_normal((T, E)).astype(np.float32) * 2.0
+    w_gu = O.round_bf16(rng.standard_normal((E, 2 * F, H)) * 0.3)
+    w_d = O.round_bf16(rng.standard_normal((E, H, F)) * 0.3)
+    full = O.ffn_forward(x, z, w_gu, w_d, K=K, F=F, renormalize=True, rsf=1.0, dtype=None)["out"]
+    total = np.zeros_like(full)
+    n_empty = 0
+    for start in range(0, E, lc):
+        r = O.route(z, K, "softmax", True, local_start=start, local_count=lc, route_scale=1.0)
+        n_empty += int((r["weight_scale"] == 0).sum())
+        total += O.ffn_forward_local(x, r["router_probs"], r["weight_scale"],
+                                     w_gu[start:start + lc], w_d[start:start + lc], K, F,
+                                     dtype=None)
+    assert n_empty > 0  # some rank holds none of some token's experts
+    np.testing.assert_allclose(total, full, rtol=2e-6, atol=2e-6 * np.abs(full).max())
+
+
 def test_moerouter_normalises_even_without_renormalize():
     z = np.log(np.array([[1.0, 2.0, 3.0, 4.0]], np.float32))
     r = O.route(z, 2, "softmax", False, rsf=3.0, local_start=0, local_count=4)
@@ -611,6 +636,14 @@ def test_planted_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_fp8_scales_act_per_block()
     monkeypatch.setattr(O, "grouped_gemm_fp8_masked", orig_fp8)
+
+    # expert parallelism: a rank that forgets weight_scale breaks the sum
+    orig_local = O.ffn_forward_local
+    monkeypatch.setattr(O, "ffn_forward_local",
+                        lambda x, rp, ws, *a, **k: orig_local(x, rp, np.ones_like(ws), *a, **k))
+    with pytest.raises(AssertionError):
+        test_expert_parallel_slices_sum_to_the_layer()
+    monkeypatch.setattr(O, "ffn_forward_local", orig_local)
 
     orig_split = O.split_gate_up
     monkeypatch.setattr(O, "split_gate_up", lambda P, F, f: orig_split(P, F, f)[::-1])
