@@ -361,6 +361,31 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
                            float* weight_scale, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* The layer of one expert-parallel rank, fed by the MoERouter outputs of its
+ * slice of lc experts [ONNX Runtime PR #32126 "[CUDA] Add MoERouter and
+ * SwiGLU contrib operators", MoERouter: the expert op's own softmax over the
+ * local row of router_probs returns w_e / W_local, and weight_scale
+ * multiplies that factor back out before the ranks' outputs are summed].
+ * Routes each token by the softmax of its router_probs row (fp32) and its top
+ * min(K, lc) experts (ties to the lower index, no renormalisation), runs the
+ * expert MLPs of this rank's experts as moe_ffn_forward does (the tensor-core
+ * or staged path; not the indexed one), and multiplies each token's combined
+ * sum by weight_scale[t] before the single cast.  Summed over the ranks the
+ * outputs give the routed layer with normalised weights times route_scale; a
+ * token with no expert on this rank has weight_scale 0 and contributes 0.
+ *
+ *   hidden [T, H] dtype;  router_probs [T, lc] f32;  weight_scale [T] f32;
+ *   w_gate_up [lc, N1, H], w_down [lc, H, F] (this rank's experts);
+ *   b_gate_up [lc, N1] | NULL, b_down [lc, H] | NULL;  out [T, H] dtype;
+ *   ws >= moe_workspace_size(T, H, F, lc, min(K, lc), dtype). */
+moe_status moe_ffn_forward_local(const void* hidden, const float* router_probs,
+                                 const float* weight_scale, const void* w_gate_up,
+                                 const void* w_down, const void* b_gate_up, const void* b_down,
+                                 int T, int H, int F, int lc, int K, moe_dtype dtype,
+                                 const moe_act_params* act, void* out, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* moe_ffn_forward for a caller whose activations live in HOST memory:
  * hidden_host [T, H] dtype and logits_host [T, E] f32 are brought to device
  * staging space inside `ws`, the layer runs as in moe_ffn_forward, and the

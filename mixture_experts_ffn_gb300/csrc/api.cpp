@@ -370,14 +370,16 @@ moe_status moe_indexed_mlp(const void* hidden, const void* w_gate_up, const void
 
 namespace {
 
-// What moe_ffn_forward_host changes in the forward: the stream waits on
-// hidden_ready after routing (the first step that reads the activations, whose
-// copy runs on a side stream meanwhile), and the combine writes its result to
-// out_direct (page-locked host memory the device addresses) when set.  The
-// indexed path keeps writing `out`.
+// What the entry points built on the forward change in it: the stream waits
+// on hidden_ready after routing (the first step that reads the activations,
+// whose copy runs on a side stream meanwhile); the combine writes its result
+// to out_direct (page-locked host memory the device addresses) when set (the
+// indexed path keeps writing `out`); token_scale [T] multiplies each token's
+// combined sum (the indexed path is then not taken).
 struct HostHooks {
   cudaEvent_t hidden_ready = nullptr;
   void* out_direct = nullptr;
+  const float* token_scale = nullptr;
   bool waited = false;
   bool wrote_direct = false;
 };
@@ -428,6 +430,7 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
   void* y = base + L.y;
   int* status = reinterpret_cast<int*>(base);
   const bool indexed =
+      !(hooks && hooks->token_scale) &&
       indexed_rule(T, H, F, E, K, dtype, act, b_gate_up, b_down, hidden, w_gate_up, w_down);
   // On the tcgen05 path the gate_up GEMM reads its rows straight from the
   // token-ordered hidden states through row_to_route, so the permute only
@@ -478,7 +481,8 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
     dst = hooks->out_direct;
     hooks->wrote_direct = true;
   }
-  return cuda_status(launch_combine(y, tw, route_to_row, T, K, H, dtype, 1.0f, dst, stream));
+  return cuda_status(launch_combine(y, tw, route_to_row, T, K, H, dtype, 1.0f, dst, stream,
+                                    hooks ? hooks->token_scale : nullptr));
 }
 
 // The device address of page-locked host memory (nullptr for anything else,
@@ -515,6 +519,33 @@ cudaError_t side_stream(cudaStream_t* out) {
 }
 
 }  // namespace
+
+moe_status moe_ffn_forward_local(const void* hidden, const float* router_probs,
+                                 const float* weight_scale, const void* w_gate_up,
+                                 const void* w_down, const void* b_gate_up, const void* b_down,
+                                 int T, int H, int F, int lc, int K, moe_dtype dtype,
+                                 const moe_act_params* act, void* out, void* ws, size_t ws_bytes,
+                                 cudaStream_t stream) {
+  if (lc < 1 || K < 1 || (T > 0 && !weight_scale)) return MOE_ERR_INVALID_ARG;
+  moe_route_params p{};
+  p.top_k = std::min(K, lc);
+  p.scoring = MOE_SCORING_SOFTMAX;
+  p.renormalize = 0;
+  p.num_expert_group = 1;
+  p.topk_group = 1;
+  p.routed_scaling_factor = 1.0f;
+  p.route_scale = 1.0f;
+  if (T > 0) {
+    Span outs[] = {{out, (size_t)T * H * esize(dtype)}};
+    Span ins[] = {{weight_scale, (size_t)T * 4}};
+    if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  }
+  HostHooks hk;
+  hk.token_scale = weight_scale;
+  return ffn_forward(hidden, router_probs, w_gate_up, w_down, nullptr, nullptr, b_gate_up, b_down,
+                     T, H, F, lc, dtype, &p, act, out, nullptr, nullptr, nullptr, nullptr, ws,
+                     ws_bytes, stream, &hk);
+}
 
 moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* w_gate_up,
                            const void* w_down, const float* correction_bias,

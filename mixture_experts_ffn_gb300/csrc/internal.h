@@ -112,8 +112,10 @@ cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t
 // p[0, n) = v on the stream.
 cudaError_t launch_fill_i32(int32_t* p, int32_t v, int n, cudaStream_t s);
 
+// token_scale (optional, [T] f32) multiplies token t's sum as well
 cudaError_t launch_combine(const void* y, const float* w, const int32_t* route_to_row, int T,
-                           int K, int H, moe_dtype dt, float scale, void* out, cudaStream_t s);
+                           int K, int H, moe_dtype dt, float scale, void* out, cudaStream_t s,
+                           const float* token_scale = nullptr);
 
 cudaError_t launch_swiglu(const void* gate, const void* up, int64_t R, int I, moe_dtype dt,
                           int fusion, float limit, float alpha, float beta, void* out,

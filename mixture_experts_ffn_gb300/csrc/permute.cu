@@ -184,7 +184,8 @@ template <typename T, int VEC>
 __device__ __forceinline__ void combine_item(const T* __restrict__ y, const float* __restrict__ w,
                                              const int32_t* __restrict__ r2r, int K, int H,
                                              int M, float scale, T* __restrict__ out, int t,
-                                             int v) {
+                                             int v, const float* __restrict__ tscale) {
+  if (tscale) scale *= __ldg(tscale + t);
   float acc[VEC];
 #pragma unroll
   for (int i = 0; i < VEC; ++i) acc[i] = 0.f;
@@ -248,14 +249,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y,
                                                       const float* __restrict__ w,
                                                       const int32_t* __restrict__ r2r, int Tn,
                                                       int K, int H, int M, float scale,
-                                                      T* __restrict__ out) {
+                                                      T* __restrict__ out,
+                                                      const float* __restrict__ tscale) {
   pdl_wait();  // everything below reads results of earlier launches
   const int nvec = H / VEC;
   const long long items = (long long)Tn * nvec;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < items; i += stride) {
     const int t = (int)(i / nvec), v = (int)(i - (long long)t * nvec);
-    combine_item<T, VEC>(y, w, r2r, K, H, M, scale, out, t, v);
+    combine_item<T, VEC>(y, w, r2r, K, H, M, scale, out, t, v, tscale);
   }
 }
 
@@ -363,7 +365,8 @@ cudaError_t launch_permute_gather(const void* hidden, int esz, int T, int H, int
 }
 
 cudaError_t launch_combine(const void* y, const float* w, const int32_t* r2r, int T, int K, int H,
-                           moe_dtype dt, float scale, void* out, cudaStream_t s) {
+                           moe_dtype dt, float scale, void* out, cudaStream_t s,
+                           const float* token_scale) {
   if (T == 0 || H == 0) return cudaSuccess;
   const int M = T * K;
   const bool aligned = ((uintptr_t)y % 16 == 0) && ((uintptr_t)out % 16 == 0);
@@ -376,17 +379,17 @@ cudaError_t launch_combine(const void* y, const float* w, const int32_t* r2r, in
     using B = __nv_bfloat16;
     if (aligned && H % 8 == 0)
       launch_pdl(combine_kernel<B, 8>, grid_for(8), 256, 0, s, static_cast<const B*>(y), w, r2r, T,
-          K, H, M, scale, static_cast<B*>(out));
+          K, H, M, scale, static_cast<B*>(out), token_scale);
     else
       launch_pdl(combine_kernel<B, 1>, grid_for(1), 256, 0, s, static_cast<const B*>(y), w, r2r, T,
-          K, H, M, scale, static_cast<B*>(out));
+          K, H, M, scale, static_cast<B*>(out), token_scale);
   } else {
     if (aligned && H % 4 == 0)
       launch_pdl(combine_kernel<float, 4>, grid_for(4), 256, 0, s, static_cast<const float*>(y), w,
-          r2r, T, K, H, M, scale, static_cast<float*>(out));
+          r2r, T, K, H, M, scale, static_cast<float*>(out), token_scale);
     else
       launch_pdl(combine_kernel<float, 1>, grid_for(1), 256, 0, s, static_cast<const float*>(y), w,
-          r2r, T, K, H, M, scale, static_cast<float*>(out));
+          r2r, T, K, H, M, scale, static_cast<float*>(out), token_scale);
   }
   count_launch();
   return cudaGetLastError();

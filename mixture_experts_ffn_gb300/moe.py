@@ -60,6 +60,8 @@ _SIGNATURES = {
     "moe_ffn_forward_host": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
                              _vp, _vp, _vp, _sz, _vp],
     "moe_shared_expert_mlp": [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
+    "moe_ffn_forward_local": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
+                              _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_fp8_masked": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
     "moe_shared_expert_workspace_size": [_i, _i, _i, _i],
     "moe_ffn_forward_shared": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
@@ -445,6 +447,26 @@ def moe_ffn_forward_shared(hidden, logits, w_gate_up, w_down, p: RouteParams, ac
                                       _p(shared_out if shared_w_gate_up is not None else None),
                                       _p(ws), ws.numel(), _stream()))
     return (shared_out if shared_w_gate_up is not None else None), routed_out
+
+
+def moe_ffn_forward_local(hidden, router_probs, weight_scale, w_gate_up, w_down, K: int,
+                          act: ActParams, b_gate_up=None, b_down=None, out=None, ws=None):
+    """The expert-parallel rank's layer from its MoERouter outputs
+    (router_probs [T, lc], weight_scale [T]) and its lc experts' weights."""
+    lib = load_library()
+    _cuda(hidden, router_probs, weight_scale, w_gate_up, w_down, b_gate_up, b_down)
+    T, H = hidden.shape
+    lc, _, F = w_down.shape
+    if out is None:
+        out = torch.empty_like(hidden)
+    if ws is None:
+        ws = _ws(lib.moe_workspace_size(T, H, F, lc, min(K, lc), _dt(hidden)), hidden.device)
+    _check("moe_ffn_forward_local",
+           lib.moe_ffn_forward_local(_p(hidden), _p(router_probs), _p(weight_scale),
+                                     _p(w_gate_up), _p(w_down), _p(b_gate_up), _p(b_down), T, H,
+                                     F, lc, K, _dt(hidden), ctypes.byref(act), _p(out), _p(ws),
+                                     ws.numel(), _stream()))
+    return out
 
 
 def moe_workspace_size_host(T, H, F, E, K, dtype=MOE_BF16) -> int:

@@ -1,0 +1,68 @@
+"""Expert parallelism emulated on one GPU (ONNX Runtime PR #32126 "[CUDA]
+Add MoERouter and SwiGLU contrib operators", MoERouter): every rank routes
+with its slice's MoERouter outputs (router_probs, weight_scale) and runs
+moe_ffn_forward_local on its own experts; each rank's output matches the
+oracle's rank, and the ranks' outputs sum to the routed layer with
+normalised weights (no collective: the sum is taken here)."""
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_ffn_gb300 import synth
+from oracle import moe_oracle as O
+
+from gpu_cases import act_kwargs, make, np_
+from tolerances import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from mixture_experts_ffn_gb300 import build, moe as m
+
+    build.build()
+    return m
+
+
+@pytest.mark.parametrize("name,over,lc", [
+    ("qwen3_bf16", dict(T=300, H=256, F=128, E=32, K=8), 8),
+    ("deepseek_v3_bf16", dict(T=200, H=256, F=128, E=64, K=8, rsf=1.0, route_scale=2.5), 16),
+])
+def test_expert_parallel_ranks_sum_to_the_layer(moe, name, over, lc):
+    cfg = synth.CONFIGS[name].replace(local_count=0, **over)
+    inp, ref = make(cfg)
+    p, a = moe.config_params(cfg)
+    E, K = cfg.E, cfg.K
+    # the whole layer with normalised weights times route_scale
+    pg = moe.route_params(K, cfg.scoring, True, cfg.G, cfg.TG, cfg.route_scale)
+    full = moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], pg,
+                               a, inp["correction_bias"])
+    total = torch.zeros_like(full, dtype=torch.float32)
+    want_total = np.zeros(tuple(full.shape))
+    for start in range(0, E, lc):
+        pr = moe.route_params(K, cfg.scoring, cfg.renormalize, cfg.G, cfg.TG, cfg.rsf,
+                              local_expert_start=start, local_expert_count=lc,
+                              route_scale=cfg.route_scale)
+        _, _, probs, wsc = moe.moe_route(inp["logits"], pr, inp["correction_bias"])
+        part = moe.moe_ffn_forward_local(inp["hidden"], probs, wsc,
+                                         inp["w_gate_up"][start:start + lc].contiguous(),
+                                         inp["w_down"][start:start + lc].contiguous(), K, a)
+        torch.cuda.synchronize()
+        r = O.route(ref["logits"], K, cfg.scoring, cfg.renormalize, cfg.G, cfg.TG, cfg.rsf,
+                    ref["correction_bias"], None, start, lc, cfg.route_scale)
+        want = O.ffn_forward_local(ref["hidden"], r["router_probs"], r["weight_scale"],
+                                   ref["w_gate_up"][start:start + lc],
+                                   ref["w_down"][start:start + lc], K, cfg.F,
+                                   dtype=cfg.dtype, **act_kwargs(cfg))
+        assert_close(np_(part), want, cfg.dtype, f"{name} rank at {start}")
+        total += part.float()
+        want_total += want
+    # the ranks' outputs are each rounded to bf16 before they are summed (as an
+    # all-reduce of their results would), so the sum is compared with the
+    # oracle's sum of its rounded ranks, and with the layer (rounded once)
+    # within the error of those extra roundings
+    assert_close(np_(total), want_total, cfg.dtype, f"{name} sum of ranks")
+    err = np_(total) - np_(full)
+    rms = float(np.sqrt(np.mean(np_(full) ** 2)))
+    assert float(np.sqrt(np.mean(err ** 2))) <= 5e-3 * rms, f"{name} sum vs layer"
