@@ -49,6 +49,11 @@ NEG_SENTINEL_F32 = -1e30  # [MoERouter] "a large negative value elsewhere (-1e30
 ACT_SILU_AND_MUL = 0
 ACT_SWIGLU = 1
 ACT_IDENTITY = 2
+ACT_GELU_AND_MUL = 3   # gated, stacked [TileOPs MoEGroupedGemmFwdOp]
+ACT_RELU = 4           # non-gated [ORT-MoE activation_type]
+ACT_GELU = 5
+ACT_SILU = 6
+GATED_ACTS = (ACT_SILU_AND_MUL, ACT_SWIGLU, ACT_GELU_AND_MUL)
 
 
 # --------------------------------------------------------------------------
@@ -90,8 +95,9 @@ def round_to(x, dtype: Optional[str]) -> np.ndarray:
 # --------------------------------------------------------------------------
 def expert_scores(logits, scoring: str, score_dtype=np.float32) -> np.ndarray:
     """Per-token expert scores.  softmax: s_e = exp(z_e - max z) / sum exp(z - max z);
-    sigmoid: s_e = 1 / (1 + exp(-z_e)).  Computed in ``score_dtype`` (float32 per
-    [TileOPs FusedTopKFwdOp])."""
+    sigmoid: s_e = 1 / (1 + exp(-z_e)); sqrt_softplus [MoERouter scoring]:
+    s_e = sqrt(log(1 + exp(z_e))) (the name read literally).  Computed in
+    ``score_dtype`` (float32 per [TileOPs FusedTopKFwdOp])."""
     z = np.asarray(logits).astype(score_dtype)
     if scoring == "softmax":
         zmax = z.max(axis=1, keepdims=True)
@@ -100,6 +106,8 @@ def expert_scores(logits, scoring: str, score_dtype=np.float32) -> np.ndarray:
     if scoring == "sigmoid":
         one = score_dtype(1.0)
         return one / (one + np.exp(-z))
+    if scoring == "sqrt_softplus":
+        return np.sqrt(np.logaddexp(score_dtype(0.0), z))
     raise ValueError(scoring)
 
 
@@ -257,6 +265,15 @@ def sigmoid64(x):
     return 1.0 / (1.0 + np.exp(-np.asarray(x, dtype=np.float64)))
 
 
+def gelu64(x):
+    """GELU x * Phi(x) = x/2 * (1 + erf(x / sqrt(2))), the exact (erf) form:
+    the pages name the activation without an approximation."""
+    from scipy.special import erf
+
+    x = np.asarray(x, dtype=np.float64)
+    return 0.5 * x * (1.0 + erf(x / math.sqrt(2.0)))
+
+
 def swiglu_math(g, l, limit: float, alpha: float, beta: float) -> np.ndarray:
     """G = min(g, limit); L = max(min(l, limit), -limit);
     out = G * sigmoid(alpha * G) * (L + beta).  limit <= 0 disables both clamps
@@ -295,11 +312,21 @@ def gated_activation(P, F: int, act: int, fusion: int = 2, limit: float = 0.0,
     if act == ACT_SILU_AND_MUL:
         g, u = split_gate_up(P, F, 2)
         return g * sigmoid64(g) * u
+    if act == ACT_GELU_AND_MUL:
+        g, u = split_gate_up(P, F, 2)
+        return gelu64(g) * u
     if act == ACT_SWIGLU:
         g, l = split_gate_up(P, F, fusion)
         return swiglu_math(g, l, limit, alpha, beta)
+    p = np.asarray(P, dtype=np.float64)[..., :F]
     if act == ACT_IDENTITY:
-        return np.asarray(P, dtype=np.float64)[..., :F]
+        return p
+    if act == ACT_RELU:
+        return np.maximum(p, 0.0)
+    if act == ACT_GELU:
+        return gelu64(p)
+    if act == ACT_SILU:
+        return p * sigmoid64(p)
     raise ValueError(act)
 
 

@@ -592,6 +592,46 @@ def test_fp8_counts_are_clamped():
     np.testing.assert_array_equal(got[2, :2], full[2, :2])
 
 
+def test_activation_and_score_golden_points():
+    kinds = {"relu": O.ACT_RELU, "gelu": O.ACT_GELU, "silu": O.ACT_SILU}
+    n = 0
+    for line in _golden_lines("activation_points.txt"):
+        kind, a, b, want = line.split()[:4]
+        a, b, want = float(a), float(b), float(want)
+        if kind in kinds:
+            got = O.gated_activation(np.array([[a]]), 1, kinds[kind])[0, 0]
+        elif kind == "gelu_and_mul":
+            got = O.gated_activation(np.array([[a, b]]), 1, O.ACT_GELU_AND_MUL)[0, 0]
+        else:
+            got = O.expert_scores(np.array([[a]]), "sqrt_softplus", np.float64)[0, 0]
+        assert abs(got - want) <= 1e-15 * max(1.0, abs(want)), (kind, a, got, want)
+        n += 1
+    assert n == 12
+
+
+def test_gelu_odd_part_and_stacked_layout():
+    """gelu(x) - gelu(-x) = x (Phi(-x) = 1 - Phi(x)); gelu_and_mul takes the
+    gate from the first F columns and the up from the last F."""
+    x = np.linspace(-6, 6, 97)
+    np.testing.assert_allclose(O.gelu64(x) - O.gelu64(-x), x, rtol=0, atol=1e-14)
+    P = np.array([[1.0, 2.0, 3.0, 5.0]])
+    np.testing.assert_allclose(O.gated_activation(P, 2, O.ACT_GELU_AND_MUL)[0],
+                               [O.gelu64(1.0) * 3.0, O.gelu64(2.0) * 5.0], rtol=1e-15)
+
+
+def test_sqrt_softplus_routes_like_any_monotone_score():
+    """sqrt_softplus is increasing, so without bias and groups it selects the K
+    largest logits; the weights are its scores, renormalised."""
+    rng = np.random.default_rng(41)
+    z = rng.standard_normal((20, 12)).astype(np.float32)
+    r = O.route(z, 3, "sqrt_softplus", True)
+    want = np.sort(np.argsort(-z, axis=1, kind="stable")[:, :3], axis=1)
+    np.testing.assert_array_equal(r["topk_ids"], want)
+    s = np.sqrt(np.log1p(np.exp(z.astype(np.float64))))
+    w = np.take_along_axis(s, want, axis=1)
+    np.testing.assert_allclose(r["topk_weights"], w / w.sum(1, keepdims=True), rtol=1e-6)
+
+
 def test_planted_mistakes_are_caught(monkeypatch):
     """A wrong sign in the sigmoid, swapped gate/up halves, or ties to the higher
     index each make one of the pins above fail."""
@@ -644,6 +684,13 @@ def test_planted_mistakes_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_expert_parallel_slices_sum_to_the_layer()
     monkeypatch.setattr(O, "ffn_forward_local", orig_local)
+
+    # the tanh form of GELU instead of the exact one fails the points
+    monkeypatch.setattr(O, "gelu64", lambda x: 0.5 * np.asarray(x) * (1 + np.tanh(
+        math.sqrt(2 / math.pi) * (np.asarray(x) + 0.044715 * np.asarray(x) ** 3))))
+    with pytest.raises(AssertionError):
+        test_activation_and_score_golden_points()
+    monkeypatch.undo()
 
     orig_split = O.split_gate_up
     monkeypatch.setattr(O, "split_gate_up", lambda P, F, f: orig_split(P, F, f)[::-1])
