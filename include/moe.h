@@ -67,7 +67,14 @@ typedef enum moe_status {
 
 typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
-typedef enum moe_scoring { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 } moe_scoring;
+/* Router scores of the logits z [MoERouter scoring; TileOPs FusedTopKFwdOp]:
+ * softmax over the experts; sigmoid(z); sqrt(log(1 + exp(z))) (the name
+ * "sqrt_softplus" read literally). */
+typedef enum moe_scoring {
+  MOE_SCORING_SOFTMAX = 0,
+  MOE_SCORING_SIGMOID = 1,
+  MOE_SCORING_SQRT_SOFTPLUS = 2
+} moe_scoring;
 
 typedef enum moe_act_kind {
   /* silu(gate) * up over a STACKED w_gate_up: F gate rows, then F up rows
@@ -82,7 +89,15 @@ typedef enum moe_act_kind {
   MOE_ACT_SWIGLU = 1,
   /* non-gated identity: w_gate_up is [E, F, H] and act(p) = p
      [ORT-MoE, activation_type "identity"]. */
-  MOE_ACT_IDENTITY = 2
+  MOE_ACT_IDENTITY = 2,
+  /* gelu(gate) * up over a STACKED w_gate_up, gelu(x) = x * Phi(x) (the
+     exact, erf form) [TileOPs, MoEGroupedGemmFwdOp "gelu_and_mul"]. */
+  MOE_ACT_GELU_AND_MUL = 3,
+  /* non-gated: w_gate_up is [E, F, H] and act(p) = max(p, 0), gelu(p) or
+     p * sigmoid(p) [ORT-MoE, activation_type relu / gelu / silu]. */
+  MOE_ACT_RELU = 4,
+  MOE_ACT_GELU = 5,
+  MOE_ACT_SILU = 6
 } moe_act_kind;
 
 /* Router configuration [TileOPs, FusedTopKFwdOp / FusedMoEFwdOp; MoERouter]. */
@@ -127,7 +142,7 @@ typedef struct moe_act_params {
  * (0 when no chosen expert is local).
  *
  *   logits          [T, E] f32
- *   correction_bias [E] f32 or NULL; requires MOE_SCORING_SIGMOID
+ *   correction_bias [E] f32 or NULL; not with MOE_SCORING_SOFTMAX
  *   expert_ids      [T, K] i32 or NULL (hash routing)
  *   topk_weights    [T, K] f32 out;  topk_ids [T, K] i32 out
  *   router_probs    [T, local_expert_count] f32 out or NULL
@@ -234,7 +249,7 @@ moe_status moe_permute_noalloc(const void* hidden, moe_dtype dtype, const int32_
  * shapes outside those limits, run a SIMT kernel in exact fp32 FMA.
  *
  *   a          [M, Hk] dtype               w_gate_up [E, N1, Hk] dtype
- *              (N1 = 2F, or F for MOE_ACT_IDENTITY)
+ *              (N1 = 2F for the gated kinds, F for the non-gated ones)
  *   b_gate_up  [E, N1] dtype or NULL (in w_gate_up's row order)
  *   seg_end    [E] i32, non-decreasing, seg_end[E-1] <= M
  *   out        [M, F] dtype

@@ -69,9 +69,10 @@ moe_status check_route(const float* logits, const float* bias, int T, int E,
   if (!p || T < 0 || E < 1 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
   const int K = p->top_k, G = p->num_expert_group, TG = p->topk_group;
   if (K < 1 || K > E || K > 64) return MOE_ERR_INVALID_ARG;
-  if (p->scoring != MOE_SCORING_SOFTMAX && p->scoring != MOE_SCORING_SIGMOID)
+  if (p->scoring != MOE_SCORING_SOFTMAX && p->scoring != MOE_SCORING_SIGMOID &&
+      p->scoring != MOE_SCORING_SQRT_SOFTPLUS)
     return MOE_ERR_INVALID_ARG;
-  if (bias && p->scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (bias && p->scoring == MOE_SCORING_SOFTMAX) return MOE_ERR_INVALID_ARG;
   if (G < 1 || G > 32 || E % G != 0) return MOE_ERR_INVALID_ARG;
   if (TG < 1 || TG > G || (long long)TG * (E / G) < K) return MOE_ERR_INVALID_ARG;
   if (bias && G > 1 && E / G < 2) return MOE_ERR_INVALID_ARG;
@@ -89,11 +90,15 @@ moe_status check_route(const float* logits, const float* bias, int T, int E,
   return MOE_OK;
 }
 
+// the gated kinds read 2F gate_up rows, the others F
+bool gated_kind(int k) {
+  return k == MOE_ACT_SILU_AND_MUL || k == MOE_ACT_SWIGLU || k == MOE_ACT_GELU_AND_MUL;
+}
+
 bool act_ok(const moe_act_params* a) {
   if (!a) return false;
-  if (a->kind == MOE_ACT_SILU_AND_MUL || a->kind == MOE_ACT_IDENTITY) return true;
   if (a->kind == MOE_ACT_SWIGLU) return a->swiglu_fusion == 1 || a->swiglu_fusion == 2;
-  return false;
+  return a->kind >= MOE_ACT_SILU_AND_MUL && a->kind <= MOE_ACT_SILU;
 }
 
 bool ws_ok(const void* ws, size_t have, size_t need) {
@@ -254,7 +259,7 @@ moe_status moe_grouped_gemm_act(const void* a, const void* w_gate_up, const void
   if (!seg_end || !w_gate_up || (M > 0 && (!a || !out))) return MOE_ERR_INVALID_ARG;
   if (!ws_ok(ws, ws_bytes, MOE_STATUS_BYTES)) return MOE_ERR_WORKSPACE;
   const size_t esz = esize(dtype);
-  const size_t N1 = act->kind == MOE_ACT_IDENTITY ? (size_t)F : 2 * (size_t)F;
+  const size_t N1 = gated_kind(act->kind) ? 2 * (size_t)F : (size_t)F;
   Span outs[] = {{out, (size_t)M * F * esz}};
   Span ins[] = {{a, (size_t)M * Hk * esz}, {w_gate_up, (size_t)E * N1 * Hk * esz},
                 {b_gate_up, b_gate_up ? (size_t)E * N1 * esz : 0}, {seg_end, (size_t)E * 4},
@@ -278,7 +283,7 @@ moe_status moe_grouped_gemm_act_gathered(const void* hidden, int T, const int32_
   if (!seg_end || !w_gate_up || (M > 0 && (!hidden || !row_to_route || !out)))
     return MOE_ERR_INVALID_ARG;
   if (!ws_ok(ws, ws_bytes, MOE_STATUS_BYTES)) return MOE_ERR_WORKSPACE;
-  const size_t N1 = act->kind == MOE_ACT_IDENTITY ? (size_t)F : 2 * (size_t)F;
+  const size_t N1 = gated_kind(act->kind) ? 2 * (size_t)F : (size_t)F;
   Span outs[] = {{out, (size_t)M * F * 2}};
   Span ins[] = {{hidden, (size_t)T * H * 2}, {row_to_route, (size_t)M * 4},
                 {w_gate_up, (size_t)E * N1 * H * 2}, {b_gate_up, b_gate_up ? (size_t)E * N1 * 2 : 0},
@@ -403,7 +408,7 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
   if (M >= (1ULL << 31)) return MOE_ERR_INVALID_ARG;
   ForwardWs L(T, H, F, E, K, (int)esz);
   if (!ws_ok(ws, ws_bytes, L.total)) return MOE_ERR_WORKSPACE;
-  const size_t N1 = act->kind == MOE_ACT_IDENTITY ? (size_t)F : 2 * (size_t)F;
+  const size_t N1 = gated_kind(act->kind) ? 2 * (size_t)F : (size_t)F;
   const size_t lc = (size_t)p->local_expert_count;
   Span outs[] = {{out, (size_t)T * H * esz},        {topk_weights_out, M * 4},
                  {topk_ids_out, M * 4},             {router_probs, T * lc * 4},

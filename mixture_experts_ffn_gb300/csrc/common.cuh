@@ -41,6 +41,24 @@ __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf
 // silu(g) * u  (silu_and_mul)
 __device__ __forceinline__ float silu_mul(float g, float u) { return g * sigmoidf_(g) * u; }
 
+// gelu(x) = x * Phi(x) = x/2 * (1 + erf(x / sqrt 2))
+__device__ __forceinline__ float gelu_f(float x) {
+  return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f));
+}
+
+// the gated kinds read 2F rows (gate and up), the others F
+__host__ __device__ constexpr bool act_is_gated(int kind) {
+  return kind == MOE_ACT_SILU_AND_MUL || kind == MOE_ACT_SWIGLU || kind == MOE_ACT_GELU_AND_MUL;
+}
+
+// non-gated activation of one value (identity, relu, gelu, silu)
+__device__ __forceinline__ float act_plain(int kind, float x) {
+  return kind == MOE_ACT_RELU ? fmaxf(x, 0.0f)
+         : kind == MOE_ACT_GELU ? gelu_f(x)
+         : kind == MOE_ACT_SILU ? x * sigmoidf_(x)
+                                : x;
+}
+
 // clamped SwiGLU; limit <= 0 disables both clamps
 __device__ __forceinline__ float swiglu_f(float g, float l, float limit, float alpha, float beta) {
   if (limit > 0.0f) {

@@ -40,6 +40,8 @@ template <int ACT>
 __device__ __forceinline__ float gated(float g, float u, float limit, float alpha, float beta) {
   if constexpr (ACT == MOE_ACT_SILU_AND_MUL) {
     return g * fast_sigmoid(g) * u;
+  } else if constexpr (ACT == MOE_ACT_GELU_AND_MUL) {
+    return gelu_f(g) * u;
   } else {
     if (limit > 0.0f) {
       g = fminf(g, limit);
@@ -127,6 +129,16 @@ __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end,
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           if (col0 + i < Nout) v[i] += __bfloat162float(be[col0 + i]);
+      }
+      if constexpr (ACT == MOE_ACT_RELU) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
+      } else if constexpr (ACT == MOE_ACT_GELU) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = gelu_f(v[i]);
+      } else if constexpr (ACT == MOE_ACT_SILU) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = v[i] * fast_sigmoid(v[i]);
       }
       emit(v, col0);
     }

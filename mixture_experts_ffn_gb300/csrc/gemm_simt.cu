@@ -97,13 +97,15 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
         if (c >= Nout) continue;
         float v;
         if (MODE == kPlain) {
-          v = accg[i][j] + (be ? Elem<T>::to_f(be[c]) : 0.f);
+          v = act_plain(act_kind, accg[i][j] + (be ? Elem<T>::to_f(be[c]) : 0.f));
         } else {
           int rg = MODE == kStacked ? c : 2 * c;
           int ru = MODE == kStacked ? Nout + c : 2 * c + 1;
           float g = accg[i][j] + (be ? Elem<T>::to_f(be[rg]) : 0.f);
           float u = accu[i][j] + (be ? Elem<T>::to_f(be[ru]) : 0.f);
-          v = act_kind == MOE_ACT_SILU_AND_MUL ? silu_mul(g, u) : swiglu_f(g, u, limit, alpha, beta);
+          v = act_kind == MOE_ACT_SILU_AND_MUL   ? silu_mul(g, u)
+              : act_kind == MOE_ACT_GELU_AND_MUL ? gelu_f(g) * u
+                                                 : swiglu_f(g, u, limit, alpha, beta);
         }
         out[(size_t)m * Nout + c] = Elem<T>::from_f(v);
       }
@@ -116,8 +118,8 @@ cudaError_t launch_t(const void* a, const void* w, const void* bias, const int32
                      int Nout, int K, int E, const moe_act_params* act, void* out, cudaStream_t s) {
   int mode = kPlain, kind = MOE_ACT_IDENTITY, N1 = Nout;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
-  if (act && act->kind != MOE_ACT_IDENTITY) {
-    kind = act->kind;
+  if (act) kind = act->kind;
+  if (act && act_is_gated(act->kind)) {
     mode = (kind == MOE_ACT_SWIGLU && act->swiglu_fusion == 1) ? kInterleaved : kStacked;
     N1 = 2 * Nout;
     limit = act->limit;

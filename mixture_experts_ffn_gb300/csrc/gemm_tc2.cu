@@ -447,8 +447,8 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
   if (M == 0 || N == 0) return cudaSuccess;
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
-  if (act && act->kind != MOE_ACT_IDENTITY) {
-    kind = act->kind;
+  if (act) kind = act->kind;
+  if (act && act_is_gated(act->kind)) {
     mode = (kind == MOE_ACT_SWIGLU && act->swiglu_fusion == 1) ? kTcInterleaved : kTcStacked;
     N1 = 2 * N;
     limit = act->limit;
@@ -486,10 +486,18 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
     for (const void* fn : {(const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY, false>,
+                           (const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_RELU, false>,
+                           (const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_GELU, false>,
+                           (const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_SILU, false>,
+                           (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_GELU_AND_MUL, false>,
                            (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, false>,
                            (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU, false>,
                            (const void*)gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU, false>,
                            (const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY, true>,
+                           (const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_RELU, true>,
+                           (const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_GELU, true>,
+                           (const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_SILU, true>,
+                           (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_GELU_AND_MUL, true>,
                            (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, true>,
                            (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU, true>,
                            (const void*)gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU, true>})
@@ -526,9 +534,13 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
   cfg.numAttrs = 2;
   auto pick = [&](auto g) {
     constexpr bool G = decltype(g)::value;
-    return mode == kTcPlain       ? gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY, G>
+    return mode == kTcPlain ? (kind == MOE_ACT_RELU   ? gemm_tc2_kernel<kTcPlain, MOE_ACT_RELU, G>
+                               : kind == MOE_ACT_GELU ? gemm_tc2_kernel<kTcPlain, MOE_ACT_GELU, G>
+                               : kind == MOE_ACT_SILU ? gemm_tc2_kernel<kTcPlain, MOE_ACT_SILU, G>
+                                                      : gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY, G>)
            : mode == kTcInterleaved ? gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU, G>
            : kind == MOE_ACT_SWIGLU ? gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU, G>
+           : kind == MOE_ACT_GELU_AND_MUL ? gemm_tc2_kernel<kTcStacked, MOE_ACT_GELU_AND_MUL, G>
                                     : gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, G>;
   };
   auto* kern = gather ? pick(std::true_type{}) : pick(std::false_type{});

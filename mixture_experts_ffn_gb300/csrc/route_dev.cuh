@@ -96,6 +96,14 @@ __device__ __forceinline__ void route_loaded(int t, const float (&z)[NPL],
     sum = warp_sum(sum);
 #pragma unroll
     for (int i = 0; i < NPL; ++i) s[i] = s[i] / sum;
+  } else if (a.scoring == MOE_SCORING_SQRT_SOFTPLUS) {
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      int e = lane + 32 * i;
+      // softplus(z) = max(z, 0) + log1p(exp(-|z|)), without overflow
+      const float z = s[i];
+      s[i] = e < E ? sqrtf(fmaxf(z, 0.f) + log1pf(expf(-fabsf(z)))) : 0.f;
+    }
   } else {
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {

@@ -20,8 +20,9 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_OVERLAP, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, \
     MOE_ERR_TIMEOUT, MOE_ERR_DEVICE, MOE_ERR_WORKSPACE = range(8)
 MOE_F32, MOE_BF16 = 0, 1
-MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
-MOE_ACT_SILU_AND_MUL, MOE_ACT_SWIGLU, MOE_ACT_IDENTITY = 0, 1, 2
+MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID, MOE_SCORING_SQRT_SOFTPLUS = 0, 1, 2
+MOE_ACT_SILU_AND_MUL, MOE_ACT_SWIGLU, MOE_ACT_IDENTITY, MOE_ACT_GELU_AND_MUL = 0, 1, 2, 3
+MOE_ACT_RELU, MOE_ACT_GELU, MOE_ACT_SILU = 4, 5, 6
 MOE_STATUS_BYTES = 256
 
 # C entry points and their argument types (mirrors include/moe.h)
@@ -148,7 +149,8 @@ def _ws(nbytes: int, device) -> torch.Tensor:
 def route_params(top_k, scoring="softmax", renormalize=True, num_expert_group=1, topk_group=1,
                  routed_scaling_factor=1.0, local_expert_start=0, local_expert_count=0,
                  route_scale=1.0) -> RouteParams:
-    sc = {"softmax": MOE_SCORING_SOFTMAX, "sigmoid": MOE_SCORING_SIGMOID}.get(scoring, scoring)
+    sc = {"softmax": MOE_SCORING_SOFTMAX, "sigmoid": MOE_SCORING_SIGMOID,
+          "sqrt_softplus": MOE_SCORING_SQRT_SOFTPLUS}.get(scoring, scoring)
     return RouteParams(top_k, sc, int(bool(renormalize)), num_expert_group, topk_group,
                        routed_scaling_factor, local_expert_start, local_expert_count, route_scale)
 

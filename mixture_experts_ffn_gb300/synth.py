@@ -40,6 +40,9 @@ TID_SW1, TID_SW2 = 8, 9  # shared-expert weights
 ACT_SILU_AND_MUL = 0
 ACT_SWIGLU = 1
 ACT_IDENTITY = 2
+ACT_GELU_AND_MUL = 3
+ACT_RELU, ACT_GELU, ACT_SILU = 4, 5, 6
+GATED_ACTS = (ACT_SILU_AND_MUL, ACT_SWIGLU, ACT_GELU_AND_MUL)
 
 
 @dataclasses.dataclass
@@ -77,7 +80,7 @@ class MoEConfig:
     @property
     def n_gate_up(self) -> int:
         """Rows of w_gate_up per expert: 2F for gated activations, F otherwise."""
-        return self.F if self.act == ACT_IDENTITY else 2 * self.F
+        return 2 * self.F if self.act in GATED_ACTS else self.F
 
     def replace(self, **kw) -> "MoEConfig":
         return dataclasses.replace(self, **kw)

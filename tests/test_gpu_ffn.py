@@ -93,6 +93,20 @@ def test_ffn_small(moe, name):
     check(moe, cfg)
 
 
+@pytest.mark.parametrize("name,over", [
+    ("qwen3_bf16", dict(T=300, H=256, F=128, act=synth.ACT_GELU_AND_MUL,
+                        scoring="sqrt_softplus")),                    # gathered gate_up
+    ("gpt_oss_bf16", dict(T=200, H=256, F=128, act=synth.ACT_GELU, swiglu_fusion=2)),  # non-gated
+    ("tiny_fp32", dict(act=synth.ACT_RELU)),                          # SIMT, fp32
+    ("deepseek_v3_bf16", dict(T=256, H=256, F=128, act=synth.ACT_SILU,
+                              scoring="sqrt_softplus")),              # bias + groups
+])
+def test_ffn_activation_and_scoring_variants(moe, name, over):
+    """gelu_and_mul, the non-gated relu / gelu / silu and sqrt_softplus
+    scoring through the whole forward against the oracle."""
+    check(moe, synth.CONFIGS[name].replace(**over))
+
+
 def test_ffn_small_hash_routing(moe):
     cfg = synth.CONFIGS["kimi_k2_decode_bf16"].replace(hash_ids=True, T=16, H=256, F=256, E=96)
     check(moe, cfg)

@@ -42,7 +42,12 @@ ACTS = {
     "swiglu_concat": dict(kind=1, swiglu_fusion=2, limit=3.0, alpha=1.0, beta=0.0),
     "swiglu_noclamp": dict(kind=1, swiglu_fusion=1, limit=0.0, alpha=1.3, beta=0.5),
     "identity": dict(kind=2),
+    "gelu_mul": dict(kind=3),
+    "relu": dict(kind=4),
+    "gelu": dict(kind=5),
+    "silu_plain": dict(kind=6),
 }
+GATED = (0, 1, 3)
 
 
 @pytest.mark.parametrize("counts,Hk,F,act,bias,dtype,simt", [
@@ -58,10 +63,18 @@ ACTS = {
     ([16] * 8, 128, 64, "silu", False, "f32", False),                        # fp32 (SIMT)
     ([40, 0, 25, 63], 100, 50, "swiglu_inter", True, "f32", False),
     ([300, 5, 0, 211], 132, 36, "silu", False, "bf16", False),               # F % 8 != 0 -> SIMT
+    ([3, 0, 130, 1, 300], 256, 192, "gelu_mul", True, "bf16", False),       # gelu_and_mul
+    ([129, 127, 0, 256], 320, 160, "gelu_mul", False, "bf16", True),
+    ([40, 0, 25, 63], 100, 48, "gelu_mul", True, "f32", False),
+    ([200, 56, 100], 128, 384, "relu", True, "bf16", False),                 # non-gated
+    ([200, 56, 100], 128, 384, "gelu", False, "bf16", False),
+    ([129, 1, 300], 256, 256, "silu_plain", True, "bf16", False),
+    ([40, 0, 25, 63], 100, 48, "gelu", True, "f32", False),
+    ([40, 0, 25, 63], 100, 44, "silu_plain", False, "bf16", True),
 ])
 def test_gemm_act(moe, counts, Hk, F, act, bias, dtype, simt):
     spec = ACTS[act]
-    N1 = F if spec["kind"] == 2 else 2 * F
+    N1 = 2 * F if spec["kind"] in GATED else F
     a, w, b, seg_end = _problem(counts, Hk, N1, dtype, bias, seed=len(counts) * 1000 + Hk)
     M = a.shape[0]
     p = moe.act_params(**spec)
@@ -143,6 +156,7 @@ def test_gemm_act_large_sampled(moe):
     (97, 8, 16, 128, 64, "silu", True),      # ragged segments, some experts empty
     (1, 1, 3, 64, 8, "silu", False),         # one route
     (513, 2, 4, 200, 96, "swiglu_noclamp", False),  # long segments, ragged k-block
+    (300, 4, 7, 256, 128, "gelu_mul", True),
     (1200, 2, 4, 256, 128, "silu", True),    # ~600-row segments: several 256-row tiles
 ])
 def test_gemm_act_gathered(moe, T, K, E, H, F, act, bias):

@@ -33,9 +33,7 @@ def _route_both(moe, cfg, inp, ref):
             None if ws is None else np_(ws)), r
 
 
-@pytest.mark.parametrize("name", list(synth.CONFIGS))
-def test_route_configs(moe, name):
-    cfg = synth.CONFIGS[name]
+def _check_route(moe, cfg):
     inp, ref = make(cfg.replace(H=64, F=64))  # routing does not depend on H, F
     (w, ids, probs, wsc), r = _route_both(moe, cfg, inp, ref)
     np.testing.assert_array_equal(ids, r["topk_ids"])
@@ -45,6 +43,20 @@ def test_route_configs(moe, name):
         np.testing.assert_array_equal(probs == np.float32(-1e30), sent)
         np.testing.assert_allclose(probs[~sent], r["router_probs"][~sent], rtol=0, atol=1e-5)
         np.testing.assert_allclose(wsc, r["weight_scale"], rtol=1e-5, atol=1e-7)
+
+
+@pytest.mark.parametrize("name", list(synth.CONFIGS))
+def test_route_configs(moe, name):
+    _check_route(moe, synth.CONFIGS[name])
+
+
+@pytest.mark.parametrize("name,over", [
+    ("qwen3_bf16", dict(scoring="sqrt_softplus")),                # MoERouter slice outputs too
+    ("deepseek_v3_bf16", dict(scoring="sqrt_softplus", T=2048)),  # correction bias, 8 groups
+    ("kimi_k2_decode_bf16", dict(scoring="sqrt_softplus", T=300)),
+])
+def test_route_sqrt_softplus(moe, name, over):
+    _check_route(moe, synth.CONFIGS[name].replace(**over))
 
 
 @pytest.mark.parametrize("hash_ids", [False, True])
