@@ -252,6 +252,32 @@ def permute(topk_ids, E: int) -> dict:
             "row_to_route": row_to_route, "route_to_row": route_to_row}
 
 
+def permute_align(topk_ids, E: int, block_size: int) -> dict:
+    """The padded layout of MoEPermuteAlignFwdOp [TileOPs "MoE Operators"]:
+    with numel = T*K routes and count[e] of them on expert e,
+    num_tokens_post_pad = sum over e of count[e] rounded up to block_size;
+    sorted_token_ids (length numel + (E + 1) * (block_size - 1)) holds one range
+    per expert, in expert order, of that rounded-up length, whose first count[e]
+    slots are the routes on e (ascending route index here: the pages leave the
+    order open) and the rest numel; every entry past num_tokens_post_pad is
+    numel.  expert_ids (one per block_size block of sorted_token_ids) names
+    the owner of each block of the ranges and is -1 past them."""
+    flat = np.asarray(topk_ids, dtype=np.int64).reshape(-1)
+    numel = flat.size
+    L = numel + (E + 1) * (block_size - 1)
+    sorted_ids = np.full(L, numel, dtype=np.int32)
+    expert_ids = np.full(-(-L // block_size), -1, dtype=np.int32)
+    pos = 0
+    for e in range(E):
+        routes = np.nonzero(flat == e)[0]
+        padded = -(-len(routes) // block_size) * block_size
+        sorted_ids[pos:pos + len(routes)] = routes
+        expert_ids[pos // block_size:(pos + padded) // block_size] = e
+        pos += padded
+    return {"sorted_token_ids": sorted_ids, "expert_ids": expert_ids,
+            "num_tokens_post_pad": np.int32(pos)}
+
+
 def gather_rows(hidden, row_to_route, K: int) -> np.ndarray:
     """expert_input[row] = hidden[row_to_route[row] // K]."""
     h = np.asarray(hidden, dtype=np.float64)

@@ -632,6 +632,43 @@ def test_sqrt_softplus_routes_like_any_monotone_score():
     np.testing.assert_allclose(r["topk_weights"], w / w.sum(1, keepdims=True), rtol=1e-6)
 
 
+def test_permute_align_golden_case():
+    vals = {}
+    for line in _golden_lines("permute_align_case.txt"):
+        key, *rest = line.split()
+        vals[key] = [int(v) for v in rest]
+    ids = np.array(vals["topk_ids"], dtype=np.int32).reshape(3, 2)
+    r = O.permute_align(ids, 3, 4)
+    assert int(r["num_tokens_post_pad"]) == vals["num_tokens_post_pad"][0]
+    np.testing.assert_array_equal(r["sorted_token_ids"], vals["sorted_token_ids"])
+    np.testing.assert_array_equal(r["expert_ids"], vals["expert_ids"])
+
+
+@pytest.mark.parametrize("T,K,E,bs", [(37, 3, 5, 16), (1, 1, 1, 64), (50, 8, 64, 8), (9, 2, 40, 4)])
+def test_permute_align_invariants(T, K, E, bs):
+    """Each expert's range holds exactly its routes, then numel; the ranges
+    follow in expert order, each a multiple of block_size long (empty experts
+    take none); expert_ids names each block's owner; the rest is padding."""
+    rng = np.random.default_rng(T * 100 + E)
+    ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    r = O.permute_align(ids, E, bs)
+    flat = ids.reshape(-1)
+    numel = flat.size
+    sid, eid = r["sorted_token_ids"], r["expert_ids"]
+    assert sid.size == numel + (E + 1) * (bs - 1) and eid.size == -(-sid.size // bs)
+    pos = 0
+    for e in range(E):
+        routes = np.nonzero(flat == e)[0]
+        padded = -(-len(routes) // bs) * bs
+        blk = sid[pos:pos + padded]
+        assert sorted(blk[:len(routes)].tolist()) == routes.tolist()
+        assert (blk[len(routes):] == numel).all()
+        assert (eid[pos // bs:(pos + padded) // bs] == e).all()
+        pos += padded
+    assert int(r["num_tokens_post_pad"]) == pos
+    assert (sid[pos:] == numel).all() and ((eid[pos // bs:] < 0) | (eid[pos // bs:] >= E)).all()
+
+
 def test_planted_mistakes_are_caught(monkeypatch):
     """A wrong sign in the sigmoid, swapped gate/up halves, or ties to the higher
     index each make one of the pins above fail."""
