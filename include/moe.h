@@ -193,6 +193,25 @@ moe_status moe_permute(const void* hidden, moe_dtype dtype, const int32_t* topk_
                        int32_t* row_to_route, int32_t* route_to_row, void* ws,
                        size_t ws_bytes, cudaStream_t stream);
 
+/* Padded permute-align layout [TileOPs "MoE Operators", MoEPermuteAlignFwdOp]:
+ * with numel = T*K routes and count[e] on expert e, num_tokens_post_pad[0] =
+ * sum over e of count[e] rounded up to block_size; sorted_token_ids holds one
+ * range per expert, in expert order, of that rounded-up length: its first
+ * count[e] slots are the routes on e in ascending route index (the order the
+ * pages leave open, fixed here), the rest numel; every entry past
+ * num_tokens_post_pad is numel.  expert_ids names the owner of each
+ * block_size block of the ranges and is -1 past them.  An id outside [0, E)
+ * drops its route and latches MOE_ERR_DEVICE, as in moe_permute.
+ *
+ *   topk_ids [T, K] i32;  sorted_token_ids [T*K + (E+1)*(block_size-1)] i32 out;
+ *   expert_ids [ceil(that / block_size)] i32 out;  num_tokens_post_pad [1] i32 out;
+ *   ws >= moe_permute_align_workspace_size(T, K, E).  E <= 12288. */
+moe_status moe_permute_align(const int32_t* topk_ids, int T, int K, int E, int block_size,
+                             int32_t* sorted_token_ids, int32_t* expert_ids,
+                             int32_t* num_tokens_post_pad, void* ws, size_t ws_bytes,
+                             cudaStream_t stream);
+size_t moe_permute_align_workspace_size(int T, int K, int E);
+
 /* The gather step of moe_permute on its own (an addition), from index maps
  * already built (moe_route_permute, or moe_permute without the gather):
  * expert_input[row, :] = hidden[row_to_route[row] / K, :] for every row below

@@ -207,6 +207,52 @@ moe_status moe_permute(const void* hidden, moe_dtype dtype, const int32_t* topk_
                                     row_to_route, route_to_row, ws, stream));
 }
 
+namespace {
+// permute-align scratch: the permute's, then the tight maps and padded starts
+struct AlignWs {
+  size_t seg_end, r2r, route_to_row, pstart, total;
+  AlignWs(int M, int E) {
+    const size_t base = PermuteWs(M, E).total;
+    seg_end = base;
+    r2r = align256(seg_end + (size_t)E * 4);
+    route_to_row = align256(r2r + (size_t)M * 4);
+    pstart = align256(route_to_row + (size_t)M * 4);
+    total = align256(pstart + (size_t)E * 4);
+  }
+};
+}  // namespace
+
+size_t moe_permute_align_workspace_size(int T, int K, int E) {
+  if (T < 0 || K < 1 || E < 1) return 0;
+  return AlignWs(T * K, E).total;
+}
+
+moe_status moe_permute_align(const int32_t* topk_ids, int T, int K, int E, int block_size,
+                             int32_t* sorted_token_ids, int32_t* expert_ids,
+                             int32_t* num_tokens_post_pad, void* ws, size_t ws_bytes,
+                             cudaStream_t stream) {
+  if (T < 0 || K < 1 || E < 1 || E > 12288 || block_size < 1 || block_size > (1 << 20))
+    return MOE_ERR_INVALID_ARG;
+  const long long L = (long long)T * K + (long long)(E + 1) * (block_size - 1);
+  if (L >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
+  if (!sorted_token_ids || !expert_ids || !num_tokens_post_pad || (T > 0 && !topk_ids))
+    return MOE_ERR_INVALID_ARG;
+  const int M = T * K;
+  AlignWs A(M, E);
+  if (!ws_ok(ws, ws_bytes, A.total)) return MOE_ERR_WORKSPACE;
+  const size_t nb = (size_t)((L + block_size - 1) / block_size);
+  Span outs[] = {{sorted_token_ids, (size_t)L * 4}, {expert_ids, nb * 4},
+                 {num_tokens_post_pad, 4}, {ws, A.total}};
+  Span ins[] = {{topk_ids, (size_t)M * 4}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  char* base = static_cast<char*>(ws);
+  return cuda_status(launch_permute_align(
+      topk_ids, T, K, E, block_size, sorted_token_ids, expert_ids, num_tokens_post_pad,
+      reinterpret_cast<int32_t*>(base + A.seg_end), reinterpret_cast<int32_t*>(base + A.r2r),
+      reinterpret_cast<int32_t*>(base + A.route_to_row),
+      reinterpret_cast<int32_t*>(base + A.pstart), ws, stream));
+}
+
 moe_status moe_permute_gather(const void* hidden, moe_dtype dtype, const int32_t* seg_end,
                               const int32_t* row_to_route, int T, int H, int E, int K,
                               void* expert_input, void* ws, size_t ws_bytes, cudaStream_t stream) {

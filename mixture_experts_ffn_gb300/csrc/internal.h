@@ -98,6 +98,13 @@ cudaError_t launch_route_permute(const float* logits, const float* bias, const i
 cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int T, int H, int E,
                            int K, void* expert_input, int32_t* seg_end, int32_t* row_to_route,
                            int32_t* route_to_row, void* ws, cudaStream_t s);
+// The padded permute-align layout from topk_ids (tight maps in seg_end,
+// row_to_route, route_to_row; padded starts in pstart [E]; ws as the permute's).
+cudaError_t launch_permute_align(const int32_t* ids, int T, int K, int E, int block_size,
+                                 int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_pad,
+                                 int32_t* seg_end, int32_t* row_to_route, int32_t* route_to_row,
+                                 int32_t* pstart, void* ws, cudaStream_t s);
+
 // The gather step of launch_permute alone: expert_input[row] = hidden[row_to_route[row] / K]
 // for the rows below seg_end[E-1], from maps already built (launch_route_permute).
 cudaError_t launch_permute_gather(const void* hidden, int esz, int T, int H, int E, int K,

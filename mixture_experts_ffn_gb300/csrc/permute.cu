@@ -278,12 +278,97 @@ __global__ void __launch_bounds__(256) copy16_kernel(const int4* __restrict__ sr
   for (; i < n; i += stride) dst[i] = src[i];
 }
 
+// ---- padded permute-align layout (TileOPs "MoE Operators",
+// MoEPermuteAlignFwdOp), built from the tight layout's maps: every expert's
+// range is its segment of the tight layout moved to a start rounded up to
+// block_size, the rest of the range numel.
+
+// sorted_token_ids[0, L) = numel, expert_ids[0, nb) = -1
+__global__ void align_fill_kernel(int32_t* __restrict__ sorted_ids, long long L, int32_t numel,
+                                  int32_t* __restrict__ expert_ids, int nb) {
+  pdl_wait();
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < L; i += stride)
+    sorted_ids[i] = numel;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nb; i += stride)
+    expert_ids[i] = -1;
+}
+
+// One CTA: padded starts (exclusive prefix of the counts rounded up to
+// block_size) into pstart, the owner of every block of the ranges into
+// expert_ids, and the padded total.
+__global__ void __launch_bounds__(1024) align_scan_kernel(const int32_t* __restrict__ seg_end,
+                                                          int E, int block_size,
+                                                          int32_t* __restrict__ pstart,
+                                                          int32_t* __restrict__ expert_ids,
+                                                          int32_t* __restrict__ num_post_pad) {
+  pdl_wait();
+  __shared__ int wt[33];
+  int base = 0;
+  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+    const int e = e0 + (int)threadIdx.x;
+    int padded = 0;
+    if (e < E) {
+      const int cnt = seg_end[e] - (e == 0 ? 0 : seg_end[e - 1]);
+      padded = (cnt + block_size - 1) / block_size * block_size;
+    }
+    int total;
+    const int first = base + pm::block_exclusive_scan(padded, wt, &total);
+    if (e < E) {
+      pstart[e] = first;
+      for (int b = first / block_size; b < (first + padded) / block_size; ++b) expert_ids[b] = e;
+    }
+    base += total;
+  }
+  if (threadIdx.x == 0) *num_post_pad = base;
+}
+
+// Row i of the tight layout (expert e) goes to pstart[e] + (i - start of e).
+__global__ void align_scatter_kernel(const int32_t* __restrict__ seg_end, int E,
+                                     const int32_t* __restrict__ row_to_route,
+                                     const int32_t* __restrict__ pstart,
+                                     int32_t* __restrict__ sorted_ids) {
+  pdl_wait();
+  const int n = seg_end[E - 1];
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    int lo = 0, hi = E - 1;  // first expert whose segment ends past i
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (seg_end[mid] > i) hi = mid; else lo = mid + 1;
+    }
+    const int start = lo == 0 ? 0 : seg_end[lo - 1];
+    sorted_ids[pstart[lo] + (i - start)] = row_to_route[i];
+  }
+}
+
 __global__ void fill_i32_kernel(int32_t* __restrict__ p, int32_t v, int n) {
   pdl_wait();  // the buffer may still be read by the previous launch
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
 }
 
 }  // namespace
+
+cudaError_t launch_permute_align(const int32_t* ids, int T, int K, int E, int block_size,
+                                 int32_t* sorted_ids, int32_t* expert_ids, int32_t* num_post_pad,
+                                 int32_t* seg_end, int32_t* row_to_route, int32_t* route_to_row,
+                                 int32_t* pstart, void* ws, cudaStream_t s) {
+  const int M = T * K;
+  const long long L = (long long)M + (long long)(E + 1) * (block_size - 1);
+  const int nb = (int)((L + block_size - 1) / block_size);
+  cudaError_t e = launch_permute(nullptr, 4, ids, T, 0, E, K, nullptr, seg_end, row_to_route,
+                                 route_to_row, ws, s);
+  if (e != cudaSuccess) return e;
+  const int fill_grid = (int)std::min<long long>((L + 255) / 256, (long long)num_sms() * 4);
+  launch_pdl(align_fill_kernel, std::max(fill_grid, 1), 256, 0, s, sorted_ids, L, (int32_t)M,
+             expert_ids, nb);
+  launch_pdl(align_scan_kernel, 1, 1024, 0, s, (const int32_t*)seg_end, E, block_size, pstart,
+             expert_ids, num_post_pad);
+  const int sc_grid = std::max(1, std::min((M + 255) / 256, num_sms() * 4));
+  launch_pdl(align_scatter_kernel, sc_grid, 256, 0, s, (const int32_t*)seg_end, E,
+             (const int32_t*)row_to_route, (const int32_t*)pstart, sorted_ids);
+  count_launch(3);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fill_i32(int32_t* p, int32_t v, int n, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;

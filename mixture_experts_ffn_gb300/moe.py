@@ -49,6 +49,8 @@ _SIGNATURES = {
     "moe_route_permute": [_vp, _vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                           _sz, _vp],
     "moe_permute_gather": [_vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
+    "moe_permute_align": [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp],
+    "moe_permute_align_workspace_size": [_i, _i, _i],
     "moe_grouped_gemm_act": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_act_gathered": [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
                                       _vp, _vp, _sz, _vp],
@@ -79,7 +81,7 @@ _SIGNATURES = {
 }
 _RESTYPES = {"moe_workspace_size": _sz, "moe_permute_workspace_size": _sz,
              "moe_workspace_size_host": _sz, "moe_shared_expert_workspace_size": _sz,
-             "moe_workspace_size_shared": _sz,
+             "moe_workspace_size_shared": _sz, "moe_permute_align_workspace_size": _sz,
              "moe_status_string": ctypes.c_char_p, "moe_launch_count": ctypes.c_uint64}
 
 _lib = None
@@ -214,6 +216,24 @@ def moe_permute(topk_ids, E: int, hidden=None, ws=None, with_gather=True):
                                           _p(route_to_row), _p(ws), ws.numel(), _stream()))
     return {"expert_input": xin, "seg_end": seg_end, "row_to_route": r2r,
             "route_to_row": route_to_row, "ws": ws}
+
+
+def moe_permute_align(topk_ids, E: int, block_size: int = 64, ws=None):
+    """Padded layout: returns (sorted_token_ids, expert_ids, num_tokens_post_pad)."""
+    lib = load_library()
+    _cuda(topk_ids)
+    T, K = topk_ids.shape
+    dev = topk_ids.device
+    L = T * K + (E + 1) * (block_size - 1)
+    sorted_ids = torch.empty((L,), dtype=torch.int32, device=dev)
+    expert_ids = torch.empty(((L + block_size - 1) // block_size,), dtype=torch.int32, device=dev)
+    npp = torch.empty((1,), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = _ws(lib.moe_permute_align_workspace_size(T, K, E), dev)
+    _check("moe_permute_align",
+           lib.moe_permute_align(_p(topk_ids), T, K, E, block_size, _p(sorted_ids),
+                                 _p(expert_ids), _p(npp), _p(ws), ws.numel(), _stream()))
+    return sorted_ids, expert_ids, npp
 
 
 def moe_permute_gather(hidden, seg_end, row_to_route, K: int, out=None, ws=None):

@@ -91,3 +91,24 @@ def test_combine(moe, T, K, H, dtype, scale):
     # deterministic: a second call is bitwise identical
     out2 = moe.moe_combine(y.cuda(), w.cuda(), r2r.cuda(), scale)
     assert torch.equal(out, out2)
+
+
+@pytest.mark.parametrize("T,K,E,bs", [
+    (4096, 8, 128, 64),      # Qwen3-style routes
+    (37, 3, 5, 16),
+    (1, 1, 1, 64),
+    (2000, 4, 2000, 16),     # many empty experts
+    (0, 2, 8, 16),           # no tokens
+])
+def test_permute_align(moe, T, K, E, bs):
+    """MoEPermuteAlignFwdOp: equal to the oracle (ascending route index inside
+    each range, the order this build fixes), entry for entry."""
+    g = torch.Generator().manual_seed(T * 7 + E)
+    ids = (torch.stack([torch.randperm(E, generator=g)[:K] for _ in range(T)]).to(torch.int32)
+           if T else torch.empty((0, K), dtype=torch.int32))
+    sid, eid, npp = moe.moe_permute_align(ids.cuda(), E, bs)
+    torch.cuda.synchronize()
+    want = O.permute_align(ids.numpy(), E, bs)
+    assert int(npp[0]) == int(want["num_tokens_post_pad"])
+    np.testing.assert_array_equal(sid.cpu().numpy(), want["sorted_token_ids"])
+    np.testing.assert_array_equal(eid.cpu().numpy(), want["expert_ids"])
