@@ -407,6 +407,46 @@ def grouped_gemm_act(a, w_gate_up, seg_end, F: int, act: int, fusion: int = 2,
     return round_to(gated_activation(P, F, act, fusion, limit, alpha, beta), dtype)
 
 
+def grouped_gemm_layout(a, b, layout: str, meta, act: Optional[int] = None, F: int = 0,
+                        fusion: int = 2, limit: float = 0.0, alpha: float = 1.0,
+                        beta: float = 0.0, bias=None, dtype: Optional[str] = "bf16"):
+    """MoEGroupedGemmFwdOp over its three row layouts [TileOPs "MoE
+    Operators", MoEGroupedGemmFwdOp layout table]: "psum" (a [M, K], meta the
+    segment END rows), "per_row" (a [M, K], meta [M] the expert of every row,
+    rows grouped by expert in ascending order, as the layout requires), or
+    "masked" (a [E, max_m, K], meta [E] valid rows per expert, read as
+    min(max(m, 0), max_m); out [E, max_m, N] with the rows past the count NaN
+    here, "unspecified" on the pages).  With ``act`` the gated or non-gated
+    activation is fused as in grouped_gemm_act, else the plain product (+
+    bias) cast to ``dtype``."""
+    def run(rows, seg_end):
+        if act is None:
+            return round_to(grouped_gemm(rows, b, seg_end, bias), dtype)
+        return grouped_gemm_act(rows, b, seg_end, F, act, fusion, limit, alpha, beta, bias, dtype)
+
+    if layout == "psum":
+        return run(a, meta)
+    if layout == "per_row":
+        ids = np.asarray(meta, dtype=np.int64)
+        if ids.size and np.any(np.diff(ids) < 0):
+            raise ValueError("per_row ids must be grouped in ascending expert order")
+        E = np.asarray(b).shape[0]
+        return run(a, np.cumsum(np.bincount(ids, minlength=E)))
+    if layout == "masked":
+        A = np.asarray(a, dtype=np.float64)
+        E, max_m, _ = A.shape
+        m = np.clip(np.asarray(meta, dtype=np.int64), 0, max_m)
+        packed = np.concatenate([A[e, :m[e]] for e in range(E)])
+        y = run(packed, np.cumsum(m))
+        out = np.full((E, max_m, y.shape[1]), np.nan)
+        pos = 0
+        for e in range(E):
+            out[e, :m[e]] = y[pos:pos + m[e]]
+            pos += m[e]
+        return out
+    raise ValueError(layout)
+
+
 def grouped_gemm_down(a, w_down, seg_end, b_down=None, dtype: Optional[str] = "bf16"):
     """down GEMM: a @ W2[g]^T + b2[g] in float64, cast to the operand dtype
     [TileOPs MoEExpertMLPFwdOp]."""

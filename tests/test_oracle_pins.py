@@ -669,6 +669,29 @@ def test_permute_align_invariants(T, K, E, bs):
     assert (sid[pos:] == numel).all() and ((eid[pos // bs:] < 0) | (eid[pos // bs:] >= E)).all()
 
 
+def test_grouped_gemm_layouts_against_row_loops():
+    """per_row and masked rows against explicit loops: out[row] = a[row] @
+    b[expert of row]^T (+ bias, activation), every valid row, nothing else."""
+    rng = np.random.default_rng(51)
+    E, K, N = 4, 6, 5
+    b = rng.standard_normal((E, N, K))
+    bias = rng.standard_normal((E, N))
+    ids = np.array([0, 0, 2, 2, 2, 3])              # expert 1 empty
+    a = rng.standard_normal((ids.size, K))
+    got = O.grouped_gemm_layout(a, b, "per_row", ids, bias=bias, dtype=None)
+    for r, e in enumerate(ids):
+        np.testing.assert_allclose(got[r], a[r] @ b[e].T + bias[e], rtol=1e-13)
+    am = rng.standard_normal((E, 3, K))
+    counts = [2, -1, 9, 0]                           # clamped to 2, 0, 3, 0
+    got = O.grouped_gemm_layout(am, b, "masked", counts, act=O.ACT_RELU, F=N, dtype=None)
+    for e, m in enumerate([2, 0, 3, 0]):
+        for r in range(3):
+            if r < m:
+                np.testing.assert_allclose(got[e, r], np.maximum(am[e, r] @ b[e].T, 0), rtol=1e-13)
+            else:
+                assert np.isnan(got[e, r]).all()
+
+
 def test_planted_mistakes_are_caught(monkeypatch):
     """A wrong sign in the sigmoid, swapped gate/up halves, or ties to the higher
     index each make one of the pins above fail."""
