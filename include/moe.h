@@ -447,6 +447,33 @@ moe_status moe_ffn_forward_host(const void* hidden_host, const float* logits_hos
 size_t moe_workspace_size_host(int T, int H, int F, int E, int K, moe_dtype dtype);
 
 /* ------------------------------------------------------------------------ */
+/* The grouped GEMM over any of its row layouts [TileOPs "MoE Operators",
+ * MoEGroupedGemmFwdOp, layout table]:
+ *   MOE_LAYOUT_PSUM     a [rows, K]; layout_metadata [E] segment END rows
+ *                       (as moe_grouped_gemm_act / _down); out [rows, N]
+ *   MOE_LAYOUT_PER_ROW  a [rows, K]; layout_metadata [rows] the expert of
+ *                       every row, rows grouped by expert in ascending order
+ *                       (not checked, as on the pages); out [rows, N]
+ *   MOE_LAYOUT_MASKED   a [E, rows, K] (rows = max_m); layout_metadata [E]
+ *                       valid rows of each expert, read as
+ *                       min(max(m, 0), max_m); out [E, max_m, N], rows past
+ *                       the count not written
+ * w [E, N1, K] with N1 = 2N for a gated act (gate rows then up rows, or
+ * interleaved for SwiGLU fusion 1), N otherwise; act NULL for the plain
+ * product; bias [E, N1] | NULL, added before the activation and the cast.
+ * ws >= moe_grouped_gemm_workspace_size(layout, rows, E). */
+typedef enum moe_layout {
+  MOE_LAYOUT_PSUM = 0,
+  MOE_LAYOUT_PER_ROW = 1,
+  MOE_LAYOUT_MASKED = 2
+} moe_layout;
+moe_status moe_grouped_gemm(const void* a, const void* w, const void* bias, int layout,
+                            const int32_t* layout_metadata, int rows, int N, int K, int E,
+                            moe_dtype dtype, const moe_act_params* act, void* out, void* ws,
+                            size_t ws_bytes, cudaStream_t stream);
+size_t moe_grouped_gemm_workspace_size(int layout, int rows, int E);
+
+/* ------------------------------------------------------------------------ */
 /* Block-scaled FP8 grouped GEMM over a masked slab [TileOPs, "MoE Operators",
  * MoEGroupedGemmFP8FwdOp]: out[g, :m_g] = a[g, :m_g] @ b[g]^T.
  *

@@ -113,10 +113,12 @@ bool tc_ok(const void* a, const void* w, const void* out, int Nout, int Kd, int 
 // grouped GEMM dispatch; act == nullptr for the plain (down) GEMM
 cudaError_t grouped_gemm(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                          int M, int Nout, int Kd, int E, moe_dtype dt, const moe_act_params* act,
-                         void* out, int* status, cudaStream_t s) {
+                         void* out, int* status, cudaStream_t s, int seg_stride = 0) {
   if (dt == MOE_BF16 && tc_ok(a, w, out, Nout, Kd, M))
-    return launch_gemm_tc(a, w, bias, seg_end, M, Nout, Kd, E, act, out, status, s);
-  return launch_gemm_simt(a, w, bias, seg_end, M, Nout, Kd, E, dt, act, out, status, s);
+    return launch_gemm_tc(a, w, bias, seg_end, M, Nout, Kd, E, act, out, status, s, nullptr, 1, 0,
+                          seg_stride);
+  return launch_gemm_simt(a, w, bias, seg_end, M, Nout, Kd, E, dt, act, out, status, s,
+                          seg_stride);
 }
 
 bool indexed_rule(int T, int H, int F, int E, int K, moe_dtype dt, const moe_act_params* act,
@@ -294,6 +296,46 @@ moe_status moe_grouped_gemm_fp8_masked(const void* a, const float* a_scale, cons
   if (max_m == 0) return MOE_OK;
   return cuda_status(launch_gemm_fp8(a, a_scale, b, b_scale, layout_metadata, E, max_m, N, K, out,
                                      static_cast<int*>(ws), stream));
+}
+
+size_t moe_grouped_gemm_workspace_size(int layout, int rows, int E) {
+  if (rows < 0 || E < 1) return 0;
+  if (layout == MOE_LAYOUT_PER_ROW) return MOE_STATUS_BYTES + align256((size_t)E * 4);
+  return MOE_STATUS_BYTES;
+}
+
+moe_status moe_grouped_gemm(const void* a, const void* w, const void* bias, int layout,
+                            const int32_t* layout_metadata, int rows, int N, int K, int E,
+                            moe_dtype dtype, const moe_act_params* act, void* out, void* ws,
+                            size_t ws_bytes, cudaStream_t stream) {
+  if (rows < 0 || N < 1 || K < 1 || E < 1 || E > kMaxExperts || !dtype_ok(dtype))
+    return MOE_ERR_INVALID_ARG;
+  if (layout < MOE_LAYOUT_PSUM || layout > MOE_LAYOUT_MASKED) return MOE_ERR_INVALID_ARG;
+  if (act && !act_ok(act)) return MOE_ERR_INVALID_ARG;
+  const bool masked = layout == MOE_LAYOUT_MASKED;
+  const long long M = masked ? (long long)E * rows : rows;
+  if (M >= (1LL << 30)) return MOE_ERR_INVALID_ARG;
+  if (!w || !layout_metadata || (M > 0 && (!a || !out))) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe_grouped_gemm_workspace_size(layout, rows, E);
+  if (!ws_ok(ws, ws_bytes, need)) return MOE_ERR_WORKSPACE;
+  const size_t esz = esize(dtype);
+  const size_t N1 = act && gated_kind(act->kind) ? 2 * (size_t)N : (size_t)N;
+  const size_t meta_n = layout == MOE_LAYOUT_PER_ROW ? (size_t)M : (size_t)E;
+  Span outs[] = {{out, (size_t)M * N * esz}, {ws, need}};
+  Span ins[] = {{a, (size_t)M * K * esz}, {w, (size_t)E * N1 * K * esz},
+                {bias, bias ? (size_t)E * N1 * esz : 0}, {layout_metadata, meta_n * 4}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  if (M == 0) return MOE_OK;
+  int* status = static_cast<int*>(ws);
+  const int32_t* seg = layout_metadata;
+  if (layout == MOE_LAYOUT_PER_ROW) {
+    int32_t* seg_end = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + MOE_STATUS_BYTES);
+    if (launch_ids_to_seg_end(layout_metadata, (int)M, E, seg_end, stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    seg = seg_end;
+  }
+  return cuda_status(grouped_gemm(a, w, bias, seg, (int)M, N, K, E, dtype, act, out, status,
+                                  stream, masked ? rows : 0));
 }
 
 moe_status moe_grouped_gemm_act(const void* a, const void* w_gate_up, const void* b_gate_up,

@@ -105,17 +105,33 @@ __device__ __forceinline__ uint64_t global_ns() {
 // round trip is needed.
 // Block-wide exclusive prefix of tiles; prefix has E + 1 entries.  Returns the
 // total tile count.  All threads of the block must call it.
+// Rows [s, t) of expert e: with stride 0, the segment between seg_end[e-1]
+// and seg_end[e] (clamped to [0, M]); with stride > 0 (a masked slab), the
+// first min(max(seg_end[e], 0), stride) rows from e * stride (seg_end then
+// holds the valid-row counts).
+__device__ __forceinline__ void seg_bounds(const int32_t* __restrict__ seg_end, int e, int M,
+                                           int stride, int& s, int& t) {
+  if (stride > 0) {
+    s = e * stride;
+    t = s + min(max(seg_end[e], 0), stride);
+  } else {
+    s = e == 0 ? 0 : seg_end[e - 1];
+    t = seg_end[e];
+    s = max(0, min(s, M));
+    t = max(s, min(t, M));
+  }
+}
+
 __device__ inline int build_tile_prefix(const int32_t* __restrict__ seg_end, int E, int M, int BM,
-                                        int n_tiles, int* prefix, int* scratch /*>= 33 ints*/) {
+                                        int n_tiles, int* prefix, int* scratch /*>= 33 ints*/,
+                                        int stride = 0) {
   const int nthr = blockDim.x, tid = threadIdx.x;
   const int per = (E + nthr - 1) / nthr;
   const int lo = tid * per, hi = min(E, lo + per);
   int local = 0;
   for (int e = lo; e < hi; ++e) {
-    int s = e == 0 ? 0 : seg_end[e - 1];
-    int t = seg_end[e];
-    s = max(0, min(s, M));
-    t = max(s, min(t, M));
+    int s, t;
+    seg_bounds(seg_end, e, M, stride, s, t);
     int mt = (t - s + BM - 1) / BM;
     local += mt * n_tiles;
   }
@@ -142,10 +158,8 @@ __device__ inline int build_tile_prefix(const int32_t* __restrict__ seg_end, int
   int run = scratch[wid] + v - local;  // exclusive prefix of this thread
   for (int e = lo; e < hi; ++e) {
     prefix[e] = run;
-    int s = e == 0 ? 0 : seg_end[e - 1];
-    int t = seg_end[e];
-    s = max(0, min(s, M));
-    t = max(s, min(t, M));
+    int s, t;
+    seg_bounds(seg_end, e, M, stride, s, t);
     run += ((t - s + BM - 1) / BM) * n_tiles;
   }
   if (tid == 0) prefix[E] = scratch[32];
@@ -164,7 +178,8 @@ struct SegTile {
 // are the outer loop and row tiles the inner one, so concurrent CTAs share
 // each weight tile through L2.
 __device__ __forceinline__ SegTile decode_tile(int t, const int* prefix, const int32_t* seg_end,
-                                               int E, int M, int BM, int n_tiles) {
+                                               int E, int M, int BM, int n_tiles,
+                                               int stride = 0) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {  // last e with prefix[e] <= t (skips empty experts)
     int mid = (lo + hi + 1) >> 1;
@@ -172,10 +187,8 @@ __device__ __forceinline__ SegTile decode_tile(int t, const int* prefix, const i
   }
   SegTile r;
   r.e = lo;
-  int s = lo == 0 ? 0 : seg_end[lo - 1];
-  int e_end = seg_end[lo];
-  s = max(0, min(s, M));
-  e_end = max(s, min(e_end, M));
+  int s, e_end;
+  seg_bounds(seg_end, lo, M, stride, s, e_end);
   int mt = (e_end - s + BM - 1) / BM;
   int local = t - prefix[lo];
   r.n_idx = local / mt;

@@ -19,7 +19,7 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(
     const T* __restrict__ a, const T* __restrict__ w, const T* __restrict__ bias,
     const int32_t* __restrict__ seg_end, int M, int Nout, int N1, int K, int E, int act_kind,
-    float limit, float alpha, float beta, T* __restrict__ out) {
+    float limit, float alpha, float beta, T* __restrict__ out, int seg_stride) {
   __shared__ float As[SBK][SBM + 4];
   __shared__ float Bg[SBK][SBN + 4];
   __shared__ float Bu[MODE == kPlain ? 1 : SBK][SBN + 4];
@@ -28,11 +28,11 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
   pdl_wait();  // everything below reads results of earlier launches
 
   const int n_tiles = (Nout + SBN - 1) / SBN;
-  const int total = build_tile_prefix(seg_end, E, M, SBM, n_tiles, prefix, scan_tmp);
+  const int total = build_tile_prefix(seg_end, E, M, SBM, n_tiles, prefix, scan_tmp, seg_stride);
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
 
   for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-    const SegTile st = decode_tile(tile, prefix, seg_end, E, M, SBM, n_tiles);
+    const SegTile st = decode_tile(tile, prefix, seg_end, E, M, SBM, n_tiles, seg_stride);
     const int n0 = st.n_idx * SBN;
     const T* we = w + (size_t)st.e * N1 * K;
     float accg[4][4], accu[4][4];
@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
 
 template <typename T>
 cudaError_t launch_t(const void* a, const void* w, const void* bias, const int32_t* seg_end, int M,
-                     int Nout, int K, int E, const moe_act_params* act, void* out, cudaStream_t s) {
+                     int Nout, int K, int E, const moe_act_params* act, void* out, cudaStream_t s,
+                     int seg_stride) {
   int mode = kPlain, kind = MOE_ACT_IDENTITY, N1 = Nout;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
   if (act) kind = act->kind;
@@ -136,13 +137,13 @@ cudaError_t launch_t(const void* a, const void* w, const void* bias, const int32
   T* O = static_cast<T*>(out);
   if (mode == kPlain)
     launch_pdl(gemm_simt_kernel<T, kPlain>, (unsigned)grid, 256, 0, s, A, W, B, seg_end, M, Nout,
-        N1, K, E, kind, limit, alpha, beta, O);
+        N1, K, E, kind, limit, alpha, beta, O, seg_stride);
   else if (mode == kStacked)
     launch_pdl(gemm_simt_kernel<T, kStacked>, (unsigned)grid, 256, 0, s, A, W, B, seg_end, M, Nout,
-        N1, K, E, kind, limit, alpha, beta, O);
+        N1, K, E, kind, limit, alpha, beta, O, seg_stride);
   else
     launch_pdl(gemm_simt_kernel<T, kInterleaved>, (unsigned)grid, 256, 0, s, A, W, B, seg_end, M,
-        Nout, N1, K, E, kind, limit, alpha, beta, O);
+        Nout, N1, K, E, kind, limit, alpha, beta, O, seg_stride);
   count_launch();
   return cudaGetLastError();
 }
@@ -151,12 +152,12 @@ cudaError_t launch_t(const void* a, const void* w, const void* bias, const int32
 
 cudaError_t launch_gemm_simt(const void* a, const void* w, const void* bias,
                              const int32_t* seg_end, int M, int N, int K, int E, moe_dtype dt,
-                             const moe_act_params* act, void* out, int* status, cudaStream_t s) {
+                             const moe_act_params* act, void* out, int* status, cudaStream_t s, int seg_stride) {
   (void)status;
   if (M == 0 || N == 0) return cudaSuccess;
   if (dt == MOE_BF16)
-    return launch_t<__nv_bfloat16>(a, w, bias, seg_end, M, N, K, E, act, out, s);
-  return launch_t<float>(a, w, bias, seg_end, M, N, K, E, act, out, s);
+    return launch_t<__nv_bfloat16>(a, w, bias, seg_end, M, N, K, E, act, out, s, seg_stride);
+  return launch_t<float>(a, w, bias, seg_end, M, N, K, E, act, out, s, seg_stride);
 }
 
 }  // namespace moe

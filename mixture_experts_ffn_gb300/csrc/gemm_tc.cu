@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_out, int tma_out,
                    __nv_bfloat16* __restrict__ out, int* status,
                    const __nv_bfloat16* __restrict__ gsrc, const int32_t* __restrict__ grows,
-                   int gdiv, int gsrc_rows) {
+                   int gdiv, int gsrc_rows, int seg_stride) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -149,7 +149,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
   // barrier init, tensor-map prefetch and TMEM allocation above overlap the
   // previous launch; seg_end and the operands are read only after this
   pdl_wait();
-  const int total = build_tile_prefix(seg_end, E, M, BM, n_tiles, sh->prefix, sh->scan_tmp);
+  const int total = build_tile_prefix(seg_end, E, M, BM, n_tiles, sh->prefix, sh->scan_tmp, seg_stride);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -166,10 +166,10 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       bool ok = true;
       int tile = blockIdx.x;
       SegTile st{}, nx{};
-      if (tile < total) st = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles);
+      if (tile < total) st = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles, seg_stride);
       for (; tile < total && ok; tile += gridDim.x) {
         if (tile + (int)gridDim.x < total)
-          nx = decode_tile(tile + gridDim.x, sh->prefix, seg_end, E, M, BM, n_tiles);
+          nx = decode_tile(tile + gridDim.x, sh->prefix, seg_end, E, M, BM, n_tiles, seg_stride);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
           uint8_t* a_dst = smem + (size_t)stage * STAGE_BYTES;
@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     // The row map entries of a tile are loaded one tile ahead, so their
     // latency never delays the first copies of the next tile.
     auto load_map = [&](int tile, int (&r)[8]) {
-      const SegTile t = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles);
+      const SegTile t = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles, seg_stride);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         // Only rows of the tile's own expert segment are read: the map holds
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     uint8_t* obufs = out_stage + quad * 2 * OUT_BUF_BYTES;
     int obuf = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles);
+      const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles, seg_stride);
       if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
       tc_fence_after();
       drain_acc<MODE, ACT>(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN),
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
 cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s, const int32_t* gather_rows,
-                           int gather_div, int gather_src_rows) {
+                           int gather_div, int gather_src_rows, int seg_stride) {
   if (M == 0 || N == 0) return cudaSuccess;
   // The two-SM (cta_group::2) kernel with MOE_TC_KERNEL=2sm.  Its SMs load a
   // third fewer bytes per MMA on 256-row pair tiles, but on the routed
@@ -344,7 +344,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
   const bool gather = gather_rows != nullptr;
   if (two_sm && num_sms() >= 2)
     return launch_gemm_tc2(a, w, bias, seg_end, M, N, K, E, act, out, status, s, gather_rows,
-                           gather_div, gather_src_rows);
+                           gather_div, gather_src_rows, seg_stride);
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
   if (act) kind = act->kind;
@@ -425,7 +425,8 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
   auto* kern = gather ? pick(std::true_type{}) : pick(std::false_type{});
   launch_pdl(kern, grid, gather ? NUM_THREADS_GATHER : NUM_THREADS, kSmemBytes, s, ma, mb,
              bias_p, seg_end, M, N, N1, K, E, limit, alpha, beta, mo, tma_out, out_p, status,
-             static_cast<const __nv_bfloat16*>(a), gather_rows, gather_div, gather_src_rows);
+             static_cast<const __nv_bfloat16*>(a), gather_rows, gather_div, gather_src_rows,
+             seg_stride);
   count_launch();
   return cudaGetLastError();
 }

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_out, int tma_out,
                     __nv_bfloat16* __restrict__ out, int* status,
                     const __nv_bfloat16* __restrict__ gsrc, const int32_t* __restrict__ grows,
-                    int gdiv, int gsrc_rows) {
+                    int gdiv, int gsrc_rows, int seg_stride) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
   // barrier init, tensor-map prefetch and TMEM allocation above overlap the
   // previous launch; seg_end and the operands are read only after this
   pdl_wait();
-  const int total = build_tile_prefix(seg_end, E, M, BMP, n_tiles, sh->prefix, sh->scan_tmp);
+  const int total = build_tile_prefix(seg_end, E, M, BMP, n_tiles, sh->prefix, sh->scan_tmp, seg_stride);
   tc_fence_before();
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       for (int s = 0; s < STAGES; ++s) issued[s] = 0;
       bool ok = true;
       for (int tile = pair; tile < total && ok; tile += npairs) {
-        const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
+        const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles, seg_stride);
         const bool tall = st.m_end - st.m0 > BMC;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       uint32_t empty_addr[STAGES];
       for (int s = 0; s < STAGES; ++s) empty_addr[s] = su32(&sh->empty[s]);
       for (int tile = pair; tile < total && ok; tile += npairs) {
-        const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
+        const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles, seg_stride);
         const uint32_t idesc = st.m_end - st.m0 > BMC ? kIdesc2 : kIdesc2s;
         if (!wait_fast(&sh->tempty[acc], aphase ^ 1u, abort_flag, status)) { ok = false; break; }
         tc_fence_after();
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     bool ok = true;
     constexpr int kRows = BMC / 16;  // rows per loader thread in a 256-row pair tile
     for (int tile = pair; tile < total && ok; tile += npairs) {
-      const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
+      const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles, seg_stride);
       const bool tall = st.m_end - st.m0 > BMC;
       const int rbase = st.m0 + (tall ? BMC : BMS) * (int)rank;
       const int nrows = tall ? kRows : kRows / 2;
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
     uint8_t* obufs = out_stage + quad * 2 * OUT_BUF_BYTES;
     int obuf = 0;
     for (int tile = pair; tile < total; tile += npairs) {
-      const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles);
+      const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BMP, n_tiles, seg_stride);
       if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
@@ -443,7 +443,8 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
 cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
                             const int32_t* seg_end, int M, int N, int K, int E,
                             const moe_act_params* act, void* out, int* status, cudaStream_t s,
-                            const int32_t* gather_rows, int gather_div, int gather_src_rows) {
+                            const int32_t* gather_rows, int gather_div, int gather_src_rows,
+                            int seg_stride) {
   if (M == 0 || N == 0) return cudaSuccess;
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
@@ -549,7 +550,7 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
                                      seg_end, M, N, N1, K, E, limit, alpha, beta, mo, tma_out,
                                      static_cast<__nv_bfloat16*>(out), status,
                                      static_cast<const __nv_bfloat16*>(a), gather_rows,
-                                     gather_div, gather_src_rows);
+                                     gather_div, gather_src_rows, seg_stride);
   count_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }

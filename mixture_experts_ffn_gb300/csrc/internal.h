@@ -116,6 +116,10 @@ cudaError_t launch_permute_gather(const void* hidden, int esz, int T, int H, int
 // mapped for the device.
 cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, cudaStream_t s);
 
+// seg_end [E] of a per_row layout (ids [M] grouped in ascending expert order).
+cudaError_t launch_ids_to_seg_end(const int32_t* ids, int M, int E, int32_t* seg_end,
+                                  cudaStream_t s);
+
 // p[0, n) = v on the stream.
 cudaError_t launch_fill_i32(int32_t* p, int32_t v, int n, cudaStream_t s);
 
@@ -132,7 +136,8 @@ cudaError_t launch_swiglu(const void* gate, const void* up, int64_t R, int I, mo
 // with N output columns; otherwise N = F act columns read from N1 rows.
 cudaError_t launch_gemm_simt(const void* a, const void* w, const void* bias,
                              const int32_t* seg_end, int M, int N, int K, int E, moe_dtype dt,
-                             const moe_act_params* act, void* out, int* status, cudaStream_t s);
+                             const moe_act_params* act, void* out, int* status, cudaStream_t s,
+                             int seg_stride = 0);
 
 // tcgen05 grouped GEMM (bf16 operands, fp32 TMEM accumulators).  With
 // gather_rows, row r of A is row gather_rows[r] / gather_div of `a` (the
@@ -142,7 +147,7 @@ cudaError_t launch_gemm_simt(const void* a, const void* w, const void* bias,
 cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s, const int32_t* gather_rows = nullptr,
-                           int gather_div = 1, int gather_src_rows = 0);
+                           int gather_div = 1, int gather_src_rows = 0, int seg_stride = 0);
 
 // block-scaled FP8 grouped GEMM over a masked slab (e4m3 operands, fp32
 // scales per row x 128 K of a and per 128 x 128 block of b, bf16 out)
@@ -154,7 +159,8 @@ cudaError_t launch_gemm_fp8(const void* a, const float* a_scale, const void* b,
 cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
                             const int32_t* seg_end, int M, int N, int K, int E,
                             const moe_act_params* act, void* out, int* status, cudaStream_t s,
-                            const int32_t* gather_rows, int gather_div, int gather_src_rows);
+                            const int32_t* gather_rows, int gather_div, int gather_src_rows,
+                            int seg_stride);
 
 // indexed per-route decode path (bf16, silu_and_mul, no bias)
 cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, const float* w,

@@ -341,6 +341,21 @@ __global__ void align_scatter_kernel(const int32_t* __restrict__ seg_end, int E,
   }
 }
 
+// seg_end[e] = number of rows whose id is <= e, for ids grouped in ascending
+// expert order (the per_row layout): an upper-bound search per expert.
+__global__ void ids_to_seg_end_kernel(const int32_t* __restrict__ ids, int M, int E,
+                                      int32_t* __restrict__ seg_end) {
+  pdl_wait();
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+    int lo = 0, hi = M;  // first row whose id exceeds e
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (ids[mid] <= e) lo = mid + 1; else hi = mid;
+    }
+    seg_end[e] = lo;
+  }
+}
+
 __global__ void fill_i32_kernel(int32_t* __restrict__ p, int32_t v, int n) {
   pdl_wait();  // the buffer may still be read by the previous launch
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = v;
@@ -367,6 +382,13 @@ cudaError_t launch_permute_align(const int32_t* ids, int T, int K, int E, int bl
   launch_pdl(align_scatter_kernel, sc_grid, 256, 0, s, (const int32_t*)seg_end, E,
              (const int32_t*)row_to_route, (const int32_t*)pstart, sorted_ids);
   count_launch(3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ids_to_seg_end(const int32_t* ids, int M, int E, int32_t* seg_end,
+                                  cudaStream_t s) {
+  launch_pdl(ids_to_seg_end_kernel, (E + 255) / 256, 256, 0, s, ids, M, E, seg_end);
+  count_launch();
   return cudaGetLastError();
 }
 

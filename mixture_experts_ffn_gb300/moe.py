@@ -24,6 +24,7 @@ MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID, MOE_SCORING_SQRT_SOFTPLUS = 0, 1, 2
 MOE_ACT_SILU_AND_MUL, MOE_ACT_SWIGLU, MOE_ACT_IDENTITY, MOE_ACT_GELU_AND_MUL = 0, 1, 2, 3
 MOE_ACT_RELU, MOE_ACT_GELU, MOE_ACT_SILU = 4, 5, 6
 MOE_STATUS_BYTES = 256
+MOE_LAYOUT_PSUM, MOE_LAYOUT_PER_ROW, MOE_LAYOUT_MASKED = 0, 1, 2
 
 # C entry points and their argument types (mirrors include/moe.h)
 _vp, _i, _i64, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, \
@@ -50,6 +51,8 @@ _SIGNATURES = {
                           _sz, _vp],
     "moe_permute_gather": [_vp, _i, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
     "moe_permute_align": [_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _sz, _vp],
+    "moe_grouped_gemm": [_vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp],
+    "moe_grouped_gemm_workspace_size": [_i, _i, _i],
     "moe_permute_align_workspace_size": [_i, _i, _i],
     "moe_grouped_gemm_act": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_act_gathered": [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
@@ -82,6 +85,7 @@ _SIGNATURES = {
 _RESTYPES = {"moe_workspace_size": _sz, "moe_permute_workspace_size": _sz,
              "moe_workspace_size_host": _sz, "moe_shared_expert_workspace_size": _sz,
              "moe_workspace_size_shared": _sz, "moe_permute_align_workspace_size": _sz,
+             "moe_grouped_gemm_workspace_size": _sz,
              "moe_status_string": ctypes.c_char_p, "moe_launch_count": ctypes.c_uint64}
 
 _lib = None
@@ -216,6 +220,27 @@ def moe_permute(topk_ids, E: int, hidden=None, ws=None, with_gather=True):
                                           _p(route_to_row), _p(ws), ws.numel(), _stream()))
     return {"expert_input": xin, "seg_end": seg_end, "row_to_route": r2r,
             "route_to_row": route_to_row, "ws": ws}
+
+
+def moe_grouped_gemm(a, w, layout: int, layout_metadata, N: int, act=None, bias=None, out=None,
+                     ws=None):
+    """The grouped GEMM over a row layout (MOE_LAYOUT_PSUM / PER_ROW: a [M, K],
+    out [M, N]; MASKED: a [E, max_m, K], out [E, max_m, N]); w [E, N1, K]."""
+    lib = load_library()
+    _cuda(a, w, bias, layout_metadata)
+    E, _, K = w.shape
+    masked = layout == MOE_LAYOUT_MASKED
+    rows = a.shape[1] if masked else a.shape[0]
+    if out is None:
+        shape = (E, rows, N) if masked else (rows, N)
+        out = torch.empty(shape, dtype=a.dtype, device=a.device)
+    if ws is None:
+        ws = _ws(lib.moe_grouped_gemm_workspace_size(layout, rows, E), a.device)
+    _check("moe_grouped_gemm",
+           lib.moe_grouped_gemm(_p(a), _p(w), _p(bias), layout, _p(layout_metadata), rows, N, K, E,
+                                _dt(a), None if act is None else ctypes.byref(act), _p(out),
+                                _p(ws), ws.numel(), _stream()))
+    return out
 
 
 def moe_permute_align(topk_ids, E: int, block_size: int = 64, ws=None):

@@ -198,3 +198,61 @@ def test_gemm_act_gathered_rejects_unsupported(moe):
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_grouped_gemm_act_gathered(hidden, r2r, 2, w, seg_end, 8, moe.act_params(0))
     assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("layout,counts,max_m,K,F,act,bias,dtype", [
+    ("per_row", [3, 0, 130, 1, 300], 0, 256, 192, "silu", True, "bf16"),
+    ("per_row", [200, 56, 100], 0, 128, 384, None, True, "bf16"),
+    ("per_row", [16] * 8, 0, 128, 64, "gelu", False, "f32"),
+    ("masked", [130, -2, 99999, 7], 200, 256, 128, "gelu_mul", True, "bf16"),  # clamped counts
+    ("masked", [50, 0, 200], 200, 128, 256, None, True, "bf16"),
+    ("masked", [5, 3], 8, 64, 32, "relu", False, "f32"),
+])
+def test_gemm_row_layouts(moe, layout, counts, max_m, K, F, act, bias, dtype):
+    """MoEGroupedGemmFwdOp's per_row and masked layouts: against the oracle on
+    the valid rows, untouched rows past the masked counts, and bit for bit the
+    segment-end result on the same rows."""
+    spec = ACTS[act] if act else None
+    N1 = 2 * F if spec and spec["kind"] in GATED else F
+    E = len(counts)
+    eff = [min(max(c, 0), max_m) for c in counts] if layout == "masked" else counts
+    a, w, b, seg_end = _problem(eff, K, N1, dtype, bias, seed=K * 10 + E)
+    p = moe.act_params(**spec) if spec else None
+    tdt = a.dtype
+    if layout == "per_row":
+        ids = torch.repeat_interleave(torch.arange(E), torch.tensor(counts)).to(torch.int32)
+        got = moe.moe_grouped_gemm(a.cuda(), w.cuda(), moe.MOE_LAYOUT_PER_ROW, ids.cuda(), F, p,
+                                   None if b is None else b.cuda())
+        meta, a_in = ids.numpy(), np_(a)
+    else:
+        slab = torch.zeros((E, max_m, K), dtype=tdt)
+        pos = 0
+        for e, m in enumerate(eff):
+            slab[e, :m] = a[pos:pos + m]
+            pos += m
+        out = torch.full((E, max_m, F), float("nan"), dtype=tdt, device="cuda")
+        got = moe.moe_grouped_gemm(slab.cuda(), w.cuda(), moe.MOE_LAYOUT_MASKED,
+                                   torch.tensor(counts, dtype=torch.int32).cuda(), F, p,
+                                   None if b is None else b.cuda(), out=out)
+        meta, a_in = np.array(counts), np_(slab)
+    torch.cuda.synchronize()
+    kw = dict(act=spec["kind"], F=F, fusion=spec.get("swiglu_fusion", 2), limit=spec.get("limit", 0.0),
+              alpha=spec.get("alpha", 1.0), beta=spec.get("beta", 0.0)) if spec else {}
+    exact = O.grouped_gemm_layout(a_in, np_(w), layout, meta, bias=None if b is None else np_(b),
+                                  dtype=None, **kw)
+    g = np_(got)
+    if layout == "masked":
+        for e, m in enumerate(eff):
+            assert np.isnan(g[e, m:]).all(), "rows past the count were written"
+        g = np.concatenate([g[e, :m] for e, m in enumerate(eff)])
+        exact = np.concatenate([exact[e, :m] for e, m in enumerate(eff)])
+    assert_rounded_once(g, exact, dtype, f"{layout} {act}")
+    # the same rows through the segment-end layout, bit for bit
+    if spec:
+        ref = moe.moe_grouped_gemm_act(a.cuda(), w.cuda(), seg_end.cuda(), F, p,
+                                       None if b is None else b.cuda())
+    else:
+        ref = moe.moe_grouped_gemm_down(a.cuda(), w.cuda(), seg_end.cuda(),
+                                        None if b is None else b.cuda())
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(g, np_(ref))
