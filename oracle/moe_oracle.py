@@ -407,6 +407,21 @@ def grouped_gemm_act(a, w_gate_up, seg_end, F: int, act: int, fusion: int = 2,
     return round_to(gated_activation(P, F, act, fusion, limit, alpha, beta), dtype)
 
 
+def grouped_gemm_act_split(a, w_gate, w_up, seg_end, act: int, limit: float = 0.0,
+                           alpha: float = 1.0, beta: float = 0.0, b_gate=None, b_up=None,
+                           dtype: Optional[str] = "bf16") -> np.ndarray:
+    """The gated gate_up GEMM with the gate and up projections in two weight
+    tensors [ORT-spec "Fusion Behavior": swiglu_fusion 0, "two GEMMs are
+    computed independently", FC1 giving g and FC3 giving l]: g = a @ Wg[e]^T
+    (+ bg[e]), l = a @ Wu[e]^T (+ bu[e]), out = act(g, l) cast to ``dtype``,
+    for act silu_and_mul, gelu_and_mul or the clamped SwiGLU."""
+    g = grouped_gemm(a, w_gate, seg_end, b_gate)
+    l = grouped_gemm(a, w_up, seg_end, b_up)
+    F = g.shape[1]
+    return round_to(gated_activation(np.concatenate([g, l], axis=1), F, act, 2, limit, alpha,
+                                     beta), dtype)
+
+
 def grouped_gemm_layout(a, b, layout: str, meta, act: Optional[int] = None, F: int = 0,
                         fusion: int = 2, limit: float = 0.0, alpha: float = 1.0,
                         beta: float = 0.0, bias=None, dtype: Optional[str] = "bf16"):

@@ -692,6 +692,25 @@ def test_grouped_gemm_layouts_against_row_loops():
                 assert np.isnan(got[e, r]).all()
 
 
+def test_swiglu_fusion0_two_tensors_against_row_loops():
+    """SwiGLU fusion 0 (gate from FC1, up from FC3, two tensors): every row
+    against an explicit loop over its expert's two projections."""
+    rng = np.random.default_rng(61)
+    E, K, F = 3, 5, 4
+    wg, wu = rng.standard_normal((E, F, K)), rng.standard_normal((E, F, K))
+    bg, bu = rng.standard_normal((E, F)), rng.standard_normal((E, F))
+    seg_end = np.array([2, 2, 5])
+    a = rng.standard_normal((5, K)) * 3
+    got = O.grouped_gemm_act_split(a, wg, wu, seg_end, O.ACT_SWIGLU, 2.0, 1.5, 0.5, bg, bu,
+                                   dtype=None)
+    for r in range(5):
+        e = int(np.searchsorted(seg_end, r, side="right"))
+        g = a[r] @ wg[e].T + bg[e]
+        l = a[r] @ wu[e].T + bu[e]
+        G, L = np.minimum(g, 2.0), np.clip(l, -2.0, 2.0)
+        np.testing.assert_allclose(got[r], G / (1 + np.exp(-1.5 * G)) * (L + 0.5), rtol=1e-13)
+
+
 def test_planted_mistakes_are_caught(monkeypatch):
     """A wrong sign in the sigmoid, swapped gate/up halves, or ties to the higher
     index each make one of the pins above fail."""
