@@ -116,7 +116,8 @@ typedef struct moe_route_params {
 /* Gated activation fused into the gate_up GEMM epilogue. */
 typedef struct moe_act_params {
   int32_t kind;          /* moe_act_kind                                          */
-  int32_t swiglu_fusion; /* MOE_ACT_SWIGLU only: 1 interleaved, 2 concatenated      */
+  int32_t swiglu_fusion; /* MOE_ACT_SWIGLU only: 1 interleaved, 2 concatenated,
+                            0 two tensors (the *_split entry points)             */
   float limit;           /* SwiGLU clamp; <= 0 disables both clamps                */
   float alpha;           /* SwiGLU sigmoid scale                                   */
   float beta;            /* SwiGLU linear offset                                   */
@@ -279,6 +280,23 @@ moe_status moe_grouped_gemm_act(const void* a, const void* w_gate_up, const void
                                 moe_dtype dtype, const moe_act_params* act, void* out, void* ws,
                                 size_t ws_bytes, cudaStream_t stream);
 
+/* The same GEMM with the gate and up projections in two tensors [ORT-spec,
+ * "Fusion Behavior", swiglu_fusion 0: FC1 gives g, FC3 gives l, two GEMMs
+ * computed independently]:
+ *   g = a[m, :] . w_gate[e, j, :] (+ b_gate[e, j]),
+ *   l = a[m, :] . w_up[e, j, :] (+ b_up[e, j]),   out[m, j] = act(g, l).
+ * Both projections feed one accumulator tile, so neither is written out.
+ * act->kind: MOE_ACT_SILU_AND_MUL, MOE_ACT_GELU_AND_MUL, or MOE_ACT_SWIGLU
+ * with swiglu_fusion 0 (MOE_ERR_INVALID_ARG otherwise).
+ *   w_gate, w_up [E, F, Hk] dtype;  b_gate, b_up [E, F] dtype, both or neither;
+ *   a, seg_end, out, ws and the tensor-core rule as moe_grouped_gemm_act
+ *   (w_up 16-byte aligned as well). */
+moe_status moe_grouped_gemm_act_split(const void* a, const void* w_gate, const void* w_up,
+                                      const void* b_gate, const void* b_up,
+                                      const int32_t* seg_end, int M, int F, int Hk, int E,
+                                      moe_dtype dtype, const moe_act_params* act, void* out,
+                                      void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* moe_grouped_gemm_act over gathered rows (an addition; the pages' grouped
  * GEMM takes the permuted copy of the activations).  Row m of the operand is
@@ -393,6 +411,21 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
                            const moe_route_params* p, const moe_act_params* act, void* out,
                            float* topk_weights_out, int32_t* topk_ids_out, float* router_probs,
                            float* weight_scale, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* moe_ffn_forward with the gate and up projections of the experts in two
+ * tensors (SwiGLU fusion 0 [ORT-spec, "Fusion Behavior"]; act as
+ * moe_grouped_gemm_act_split): w_gate, w_up [E, F, H]; b_gate, b_up [E, F] |
+ * NULL, both or neither.  Always the staged pipeline (the indexed path reads
+ * stacked weights); the gate_up GEMM reads both tensors into one accumulator
+ * tile.  Everything else, ws included, as moe_ffn_forward. */
+moe_status moe_ffn_forward_split(const void* hidden, const float* logits, const void* w_gate,
+                                 const void* w_up, const void* w_down,
+                                 const float* correction_bias, const int32_t* expert_ids,
+                                 const void* b_gate, const void* b_up, const void* b_down, int T,
+                                 int H, int F, int E, moe_dtype dtype, const moe_route_params* p,
+                                 const moe_act_params* act, void* out, float* topk_weights_out,
+                                 int32_t* topk_ids_out, float* router_probs, float* weight_scale,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* The layer of one expert-parallel rank, fed by the MoERouter outputs of its

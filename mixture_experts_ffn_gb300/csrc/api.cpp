@@ -101,6 +101,17 @@ bool act_ok(const moe_act_params* a) {
   return a->kind >= MOE_ACT_SILU_AND_MUL && a->kind <= MOE_ACT_SILU;
 }
 
+// SwiGLU fusion 0 (gate and up projections in two tensors): a gated kind, with
+// swiglu_fusion 0 for the clamped SwiGLU.  The launchers get a copy marked
+// stacked, the layout whose accumulator they share.
+bool split_act(const moe_act_params* a, moe_act_params* stacked) {
+  if (!a || !gated_kind(a->kind)) return false;
+  if (a->kind == MOE_ACT_SWIGLU && a->swiglu_fusion != 0) return false;
+  *stacked = *a;
+  stacked->swiglu_fusion = 2;
+  return true;
+}
+
 bool ws_ok(const void* ws, size_t have, size_t need) {
   return ws && ((uintptr_t)ws & 255u) == 0 && have >= need;
 }
@@ -113,12 +124,13 @@ bool tc_ok(const void* a, const void* w, const void* out, int Nout, int Kd, int 
 // grouped GEMM dispatch; act == nullptr for the plain (down) GEMM
 cudaError_t grouped_gemm(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                          int M, int Nout, int Kd, int E, moe_dtype dt, const moe_act_params* act,
-                         void* out, int* status, cudaStream_t s, int seg_stride = 0) {
-  if (dt == MOE_BF16 && tc_ok(a, w, out, Nout, Kd, M))
+                         void* out, int* status, cudaStream_t s, int seg_stride = 0,
+                         const SplitUp* split = nullptr) {
+  if (dt == MOE_BF16 && tc_ok(a, w, out, Nout, Kd, M) && (!split || aligned16(split->w_up)))
     return launch_gemm_tc(a, w, bias, seg_end, M, Nout, Kd, E, act, out, status, s, nullptr, 1, 0,
-                          seg_stride);
+                          seg_stride, split);
   return launch_gemm_simt(a, w, bias, seg_end, M, Nout, Kd, E, dt, act, out, status, s,
-                          seg_stride);
+                          seg_stride, split);
 }
 
 bool indexed_rule(int T, int H, int F, int E, int K, moe_dtype dt, const moe_act_params* act,
@@ -358,6 +370,30 @@ moe_status moe_grouped_gemm_act(const void* a, const void* w_gate_up, const void
                                   static_cast<int*>(ws), stream));
 }
 
+moe_status moe_grouped_gemm_act_split(const void* a, const void* w_gate, const void* w_up,
+                                      const void* b_gate, const void* b_up,
+                                      const int32_t* seg_end, int M, int F, int Hk, int E,
+                                      moe_dtype dtype, const moe_act_params* act, void* out,
+                                      void* ws, size_t ws_bytes, cudaStream_t stream) {
+  moe_act_params st{};
+  if (M < 0 || F < 1 || Hk < 1 || E < 1 || E > kMaxExperts || !dtype_ok(dtype) ||
+      !split_act(act, &st))
+    return MOE_ERR_INVALID_ARG;
+  if (!seg_end || !w_gate || !w_up || (M > 0 && (!a || !out)) || (!b_gate != !b_up))
+    return MOE_ERR_INVALID_ARG;
+  if (!ws_ok(ws, ws_bytes, MOE_STATUS_BYTES)) return MOE_ERR_WORKSPACE;
+  const size_t esz = esize(dtype);
+  const size_t wn = (size_t)E * F * Hk * esz, bn = b_gate ? (size_t)E * F * esz : 0;
+  Span outs[] = {{out, (size_t)M * F * esz}};
+  Span ins[] = {{a, (size_t)M * Hk * esz}, {w_gate, wn}, {w_up, wn}, {b_gate, bn}, {b_up, bn},
+                {seg_end, (size_t)E * 4}, {ws, MOE_STATUS_BYTES}};
+  if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
+  if (M == 0) return MOE_OK;
+  const SplitUp split{w_up, b_up};
+  return cuda_status(grouped_gemm(a, w_gate, b_gate, seg_end, M, F, Hk, E, dtype, &st, out,
+                                  static_cast<int*>(ws), stream, 0, &split));
+}
+
 moe_status moe_grouped_gemm_act_gathered(const void* hidden, int T, const int32_t* row_to_route,
                                          int top_k, const void* w_gate_up,
                                          const void* b_gate_up, const int32_t* seg_end, int M,
@@ -468,8 +504,11 @@ namespace {
 // whose copy runs on a side stream meanwhile); the combine writes its result
 // to out_direct (page-locked host memory the device addresses) when set (the
 // indexed path keeps writing `out`); token_scale [T] multiplies each token's
-// combined sum (the indexed path is then not taken).
+// combined sum (the indexed path is then not taken); split.w_up, when set, is
+// the up projection [E, F, H] of a gate_up GEMM whose w_gate_up / b_gate_up
+// then hold only the gate projection (SwiGLU fusion 0; split.b_up its bias).
 struct HostHooks {
+  SplitUp split{nullptr, nullptr};
   cudaEvent_t hidden_ready = nullptr;
   void* out_direct = nullptr;
   const float* token_scale = nullptr;
@@ -484,6 +523,12 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
                        const moe_act_params* act, void* out, float* topk_weights_out,
                        int32_t* topk_ids_out, float* router_probs, float* weight_scale,
                        void* ws, size_t ws_bytes, cudaStream_t stream, HostHooks* hooks) {
+  const SplitUp* split = hooks && hooks->split.w_up ? &hooks->split : nullptr;
+  moe_act_params split_st{};
+  if (split) {
+    if (!split_act(act, &split_st) || (!b_gate_up != !split->b_up)) return MOE_ERR_INVALID_ARG;
+    act = &split_st;
+  }
   if (!dtype_ok(dtype) || !act_ok(act) || H < 1 || F < 1) return MOE_ERR_INVALID_ARG;
   float dummy_w = 0.f;
   int32_t dummy_i = 0;
@@ -496,7 +541,9 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
   if (M >= (1ULL << 31)) return MOE_ERR_INVALID_ARG;
   ForwardWs L(T, H, F, E, K, (int)esz);
   if (!ws_ok(ws, ws_bytes, L.total)) return MOE_ERR_WORKSPACE;
-  const size_t N1 = gated_kind(act->kind) ? 2 * (size_t)F : (size_t)F;
+  // rows of w_gate_up (and of the up tensor, when split)
+  const size_t N1 = gated_kind(act->kind) && !split ? 2 * (size_t)F : (size_t)F;
+  const size_t n_up = split ? N1 : 0;
   const size_t lc = (size_t)p->local_expert_count;
   Span outs[] = {{out, (size_t)T * H * esz},        {topk_weights_out, M * 4},
                  {topk_ids_out, M * 4},             {router_probs, T * lc * 4},
@@ -508,7 +555,9 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
                 {correction_bias, correction_bias ? (size_t)E * 4 : 0},
                 {expert_ids, expert_ids ? M * 4 : 0},
                 {b_gate_up, b_gate_up ? (size_t)E * N1 * esz : 0},
-                {b_down, b_down ? (size_t)E * H * esz : 0}};
+                {b_down, b_down ? (size_t)E * H * esz : 0},
+                {split ? split->w_up : nullptr, (size_t)E * n_up * H * esz},
+                {split ? split->b_up : nullptr, split && split->b_up ? (size_t)E * n_up * esz : 0}};
   if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
   if (T == 0) return MOE_OK;
 
@@ -523,14 +572,15 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
   void* y = base + L.y;
   int* status = reinterpret_cast<int*>(base);
   const bool indexed =
-      !(hooks && hooks->token_scale) &&
+      !(hooks && hooks->token_scale) && !split &&
       indexed_rule(T, H, F, E, K, dtype, act, b_gate_up, b_down, hidden, w_gate_up, w_down);
   // On the tcgen05 path the gate_up GEMM reads its rows straight from the
   // token-ordered hidden states through row_to_route, so the permute only
   // builds the index maps and the permuted copy of the activations is never
   // written or read back.
   const bool fused_gather = !indexed && dtype == MOE_BF16 &&
-                            tc_ok(hidden, w_gate_up, a1, F, H, (int)M);
+                            tc_ok(hidden, w_gate_up, a1, F, H, (int)M) &&
+                            (!split || aligned16(split->w_up));
   // Routing and the index maps take one launch; the staged path then copies
   // the permuted activations in a launch of its own.
   const bool fused_maps = route_permute_ok(E);
@@ -561,10 +611,10 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
   }
   if (fused_gather)
     err = launch_gemm_tc(hidden, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, act, a1, status,
-                         stream, r2r, K, T);
+                         stream, r2r, K, T, 0, split);
   else
     err = grouped_gemm(xin, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, dtype, act, a1,
-                       status, stream);
+                       status, stream, 0, split);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
   err = grouped_gemm(a1, w_down, b_down, seg_end, (int)M, H, F, E, dtype, nullptr, y, status,
                      stream);
@@ -650,6 +700,22 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
   return ffn_forward(hidden, logits, w_gate_up, w_down, correction_bias, expert_ids, b_gate_up,
                      b_down, T, H, F, E, dtype, p, act, out, topk_weights_out, topk_ids_out,
                      router_probs, weight_scale, ws, ws_bytes, stream, nullptr);
+}
+
+moe_status moe_ffn_forward_split(const void* hidden, const float* logits, const void* w_gate,
+                                 const void* w_up, const void* w_down,
+                                 const float* correction_bias, const int32_t* expert_ids,
+                                 const void* b_gate, const void* b_up, const void* b_down, int T,
+                                 int H, int F, int E, moe_dtype dtype, const moe_route_params* p,
+                                 const moe_act_params* act, void* out, float* topk_weights_out,
+                                 int32_t* topk_ids_out, float* router_probs, float* weight_scale,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream) {
+  if (!w_up) return MOE_ERR_INVALID_ARG;
+  HostHooks hk;
+  hk.split = SplitUp{w_up, b_up};
+  return ffn_forward(hidden, logits, w_gate, w_down, correction_bias, expert_ids, b_gate, b_down,
+                     T, H, F, E, dtype, p, act, out, topk_weights_out, topk_ids_out,
+                     router_probs, weight_scale, ws, ws_bytes, stream, &hk);
 }
 
 // ---- shared expert [TileOPs, SharedExpertMLPFwdOp]: the grouped GEMMs over one

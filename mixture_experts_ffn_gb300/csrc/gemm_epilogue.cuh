@@ -95,10 +95,14 @@ __device__ __forceinline__ void emit_chunk32(const float (&v)[32], int col0, int
 // store.  TMEM column layout from tbase: plain, chunk c at 32c; stacked, gate
 // at 32c and up at up_off + 32c; interleaved, (gate, up) pairs at 64c.  Rows
 // at or past m_end (the end of the tile's expert segment) are not written.
+// Bias rows are N1 wide; the up bias of a stacked tile is column Nout + j of
+// the expert's row, or column j of bias_up's row when the up projection is a
+// tensor of its own (bias_up != nullptr, N1 = Nout).
 template <int MODE, int ACT>
 __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end, int col_base,
                                            int nchunks, int up_off, int e,
-                                           const __nv_bfloat16* __restrict__ bias, int N1,
+                                           const __nv_bfloat16* __restrict__ bias,
+                                           const __nv_bfloat16* __restrict__ bias_up, int N1,
                                            int Nout, float limit, float alpha, float beta,
                                            const CUtensorMap* tm_out, int tma_out,
                                            __nv_bfloat16* __restrict__ out, uint8_t* obufs,
@@ -106,6 +110,7 @@ __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end,
   const int row = wrow0 + lane;
   const bool row_ok = row < m_end;
   const __nv_bfloat16* be = bias ? bias + (size_t)e * N1 : nullptr;
+  const __nv_bfloat16* bu = bias_up ? bias_up + (size_t)e * N1 : be ? be + Nout : nullptr;
   __nv_bfloat16* orow = out + (size_t)row * Nout;
   // Whole-box TMA stores only where all 32 rows of this warp belong to the
   // tile's expert segment; a ragged tail stores row by row instead so it
@@ -171,10 +176,13 @@ __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end,
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           if (col0 + i < Nout) {
-            const int rg = MODE == kTcStacked ? col0 + i : 2 * (col0 + i);
-            const int ru = MODE == kTcStacked ? Nout + col0 + i : rg + 1;
-            gv[i] += __bfloat162float(be[rg]);
-            uv[i] += __bfloat162float(be[ru]);
+            if constexpr (MODE == kTcStacked) {
+              gv[i] += __bfloat162float(be[col0 + i]);
+              uv[i] += __bfloat162float(bu[col0 + i]);
+            } else {
+              gv[i] += __bfloat162float(be[2 * (col0 + i)]);
+              uv[i] += __bfloat162float(be[2 * (col0 + i) + 1]);
+            }
           }
         }
       }
@@ -191,17 +199,19 @@ __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end,
 // stacked) of column tile n_idx.
 template <int MODE, int ACT>
 __device__ __forceinline__ void drain_acc(uint32_t tbase, int wrow0, int m_end, int n_idx, int e,
-                                          const __nv_bfloat16* __restrict__ bias, int N1, int Nout,
+                                          const __nv_bfloat16* __restrict__ bias,
+                                          const __nv_bfloat16* __restrict__ bias_up, int N1, int Nout,
                                           float limit, float alpha, float beta,
                                           const CUtensorMap* tm_out, int tma_out,
                                           __nv_bfloat16* __restrict__ out, uint8_t* obufs,
                                           int& obuf, int lane) {
   if constexpr (MODE == kTcPlain)
-    drain_cols<MODE, ACT>(tbase, wrow0, m_end, n_idx * kEpiCols, kEpiCols / 32, 0, e, bias, N1,
+    drain_cols<MODE, ACT>(tbase, wrow0, m_end, n_idx * kEpiCols, kEpiCols / 32, 0, e, bias,
+                          bias_up, N1,
                           Nout, limit, alpha, beta, tm_out, tma_out, out, obufs, obuf, lane);
   else
     drain_cols<MODE, ACT>(tbase, wrow0, m_end, n_idx * (kEpiCols / 2), kEpiCols / 64,
-                          kEpiCols / 2, e, bias, N1, Nout, limit, alpha, beta, tm_out, tma_out,
+                          kEpiCols / 2, e, bias, bias_up, N1, Nout, limit, alpha, beta, tm_out, tma_out,
                           out, obufs, obuf, lane);
 }
 

@@ -19,7 +19,8 @@ template <typename T, int MODE>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(
     const T* __restrict__ a, const T* __restrict__ w, const T* __restrict__ bias,
     const int32_t* __restrict__ seg_end, int M, int Nout, int N1, int K, int E, int act_kind,
-    float limit, float alpha, float beta, T* __restrict__ out, int seg_stride) {
+    float limit, float alpha, float beta, T* __restrict__ out, int seg_stride,
+    const T* __restrict__ w_up, const T* __restrict__ bias_up) {
   __shared__ float As[SBK][SBM + 4];
   __shared__ float Bg[SBK][SBN + 4];
   __shared__ float Bu[MODE == kPlain ? 1 : SBK][SBN + 4];
@@ -35,6 +36,9 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
     const SegTile st = decode_tile(tile, prefix, seg_end, E, M, SBM, n_tiles, seg_stride);
     const int n0 = st.n_idx * SBN;
     const T* we = w + (size_t)st.e * N1 * K;
+    // stacked up rows: Nout.. of the same expert, or 0.. of the up tensor
+    const T* wu = w_up ? w_up + (size_t)st.e * N1 * K : we;
+    const int up0 = w_up ? 0 : Nout;
     float accg[4][4], accu[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -58,11 +62,11 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
         int j = n0 + c, k = k0 + kk;
         bool ok = j < Nout && k < K;
         int rg, ru;
-        if (MODE == kStacked) { rg = j; ru = Nout + j; }
+        if (MODE == kStacked) { rg = j; ru = up0 + j; }
         else if (MODE == kInterleaved) { rg = 2 * j; ru = 2 * j + 1; }
         else { rg = j; ru = 0; }
         Bg[kk][c] = ok ? Elem<T>::to_f(we[(size_t)rg * K + k]) : 0.f;
-        if (MODE != kPlain) Bu[kk][c] = ok ? Elem<T>::to_f(we[(size_t)ru * K + k]) : 0.f;
+        if (MODE != kPlain) Bu[kk][c] = ok ? Elem<T>::to_f(wu[(size_t)ru * K + k]) : 0.f;
       }
       __syncthreads();
 #pragma unroll
@@ -87,6 +91,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
     }
     // epilogue: bias in fp32, activation, one cast
     const T* be = bias ? bias + (size_t)st.e * N1 : nullptr;
+    const T* bue = bias_up ? bias_up + (size_t)st.e * N1 : be;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       int m = st.m0 + ty * 4 + i;
@@ -100,9 +105,9 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
           v = act_plain(act_kind, accg[i][j] + (be ? Elem<T>::to_f(be[c]) : 0.f));
         } else {
           int rg = MODE == kStacked ? c : 2 * c;
-          int ru = MODE == kStacked ? Nout + c : 2 * c + 1;
+          int ru = MODE == kStacked ? up0 + c : 2 * c + 1;
           float g = accg[i][j] + (be ? Elem<T>::to_f(be[rg]) : 0.f);
-          float u = accu[i][j] + (be ? Elem<T>::to_f(be[ru]) : 0.f);
+          float u = accu[i][j] + (bue ? Elem<T>::to_f(bue[ru]) : 0.f);
           v = act_kind == MOE_ACT_SILU_AND_MUL   ? silu_mul(g, u)
               : act_kind == MOE_ACT_GELU_AND_MUL ? gelu_f(g) * u
                                                  : swiglu_f(g, u, limit, alpha, beta);
@@ -116,7 +121,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(
 template <typename T>
 cudaError_t launch_t(const void* a, const void* w, const void* bias, const int32_t* seg_end, int M,
                      int Nout, int K, int E, const moe_act_params* act, void* out, cudaStream_t s,
-                     int seg_stride) {
+                     int seg_stride, const SplitUp* split) {
   int mode = kPlain, kind = MOE_ACT_IDENTITY, N1 = Nout;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
   if (act) kind = act->kind;
@@ -127,6 +132,10 @@ cudaError_t launch_t(const void* a, const void* w, const void* bias, const int32
     alpha = act->alpha;
     beta = act->beta;
   }
+  if (split && mode != kStacked) return cudaErrorInvalidValue;
+  if (split) N1 = Nout;  // two [E, Nout, K] tensors
+  const T* WU = split ? static_cast<const T*>(split->w_up) : nullptr;
+  const T* BU = split ? static_cast<const T*>(split->b_up) : nullptr;
   // enough CTAs to cover the worst-case tile count, capped at a few waves
   long long max_tiles = (long long)((M + SBM - 1) / SBM + E) * ((Nout + SBN - 1) / SBN);
   long long grid = std::min<long long>(max_tiles, (long long)num_sms() * 4);
@@ -137,13 +146,13 @@ cudaError_t launch_t(const void* a, const void* w, const void* bias, const int32
   T* O = static_cast<T*>(out);
   if (mode == kPlain)
     launch_pdl(gemm_simt_kernel<T, kPlain>, (unsigned)grid, 256, 0, s, A, W, B, seg_end, M, Nout,
-        N1, K, E, kind, limit, alpha, beta, O, seg_stride);
+        N1, K, E, kind, limit, alpha, beta, O, seg_stride, WU, BU);
   else if (mode == kStacked)
     launch_pdl(gemm_simt_kernel<T, kStacked>, (unsigned)grid, 256, 0, s, A, W, B, seg_end, M, Nout,
-        N1, K, E, kind, limit, alpha, beta, O, seg_stride);
+        N1, K, E, kind, limit, alpha, beta, O, seg_stride, WU, BU);
   else
     launch_pdl(gemm_simt_kernel<T, kInterleaved>, (unsigned)grid, 256, 0, s, A, W, B, seg_end, M,
-        Nout, N1, K, E, kind, limit, alpha, beta, O, seg_stride);
+        Nout, N1, K, E, kind, limit, alpha, beta, O, seg_stride, WU, BU);
   count_launch();
   return cudaGetLastError();
 }
@@ -152,12 +161,13 @@ cudaError_t launch_t(const void* a, const void* w, const void* bias, const int32
 
 cudaError_t launch_gemm_simt(const void* a, const void* w, const void* bias,
                              const int32_t* seg_end, int M, int N, int K, int E, moe_dtype dt,
-                             const moe_act_params* act, void* out, int* status, cudaStream_t s, int seg_stride) {
+                             const moe_act_params* act, void* out, int* status, cudaStream_t s,
+                             int seg_stride, const SplitUp* split) {
   (void)status;
   if (M == 0 || N == 0) return cudaSuccess;
   if (dt == MOE_BF16)
-    return launch_t<__nv_bfloat16>(a, w, bias, seg_end, M, N, K, E, act, out, s, seg_stride);
-  return launch_t<float>(a, w, bias, seg_end, M, N, K, E, act, out, s, seg_stride);
+    return launch_t<__nv_bfloat16>(a, w, bias, seg_end, M, N, K, E, act, out, s, seg_stride, split);
+  return launch_t<float>(a, w, bias, seg_end, M, N, K, E, act, out, s, seg_stride, split);
 }
 
 }  // namespace moe

@@ -12,6 +12,8 @@
 //   Gated modes use the 256 accumulator columns as 128 gate + 128 up columns
 //   (stacked: one 4-D box of gate rows j0.. then up rows F+j0..; interleaved:
 //   256 consecutive rows 2*j0..), giving 128 activation columns per tile.
+//   With the gate and up projections in two tensors (SwiGLU fusion 0), two
+//   3-D boxes of 128 rows each land in the same shared-memory layout.
 // Roles (192 threads, one CTA per SM)
 //   warp 0 lane 0 : TMA producer
 //   warp 1        : TMEM allocator; lane 0 issues tcgen05.mma (M128 N256 K16)
@@ -111,7 +113,9 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
                    const __grid_constant__ CUtensorMap tm_out, int tma_out,
                    __nv_bfloat16* __restrict__ out, int* status,
                    const __nv_bfloat16* __restrict__ gsrc, const int32_t* __restrict__ grows,
-                   int gdiv, int gsrc_rows, int seg_stride) {
+                   int gdiv, int gsrc_rows, int seg_stride,
+                   const __grid_constant__ CUtensorMap tm_b_up, int split,
+                   const __nv_bfloat16* __restrict__ bias_up) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -137,6 +141,9 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b)) : "memory");
+    if (split)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_b_up))
+                   : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -181,8 +188,14 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
             mbar_expect_tx(&sh->full[stage], STAGE_BYTES);
             tma_2d(a_dst, &tm_a, &sh->full[stage], k0, st.m0);
           }
-          if constexpr (MODE == kTcStacked) {  // gate rows j0.. then up rows F+j0.. in one box
-            tma_4d(b_dst, &tm_b, &sh->full[stage], k0, st.n_idx * (BN / 2), 0, st.e);
+          if constexpr (MODE == kTcStacked) {  // gate rows j0.. then up rows F+j0..
+            if (split) {
+              tma_3d(b_dst, &tm_b, &sh->full[stage], k0, st.n_idx * (BN / 2), st.e);
+              tma_3d(b_dst + B_BYTES / 2, &tm_b_up, &sh->full[stage], k0, st.n_idx * (BN / 2),
+                     st.e);
+            } else {
+              tma_4d(b_dst, &tm_b, &sh->full[stage], k0, st.n_idx * (BN / 2), 0, st.e);
+            }
           } else {
             tma_3d(b_dst, &tm_b, &sh->full[stage], k0, st.n_idx * BN, st.e);
           }
@@ -305,7 +318,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
       tc_fence_after();
       drain_acc<MODE, ACT>(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN),
-                           st.m0 + quad * 32, st.m_end, st.n_idx, st.e, bias, N1, Nout, limit,
+                           st.m0 + quad * 32, st.m_end, st.n_idx, st.e, bias, bias_up, N1, Nout, limit,
                            alpha, beta, &tm_out, tma_out, out, obufs, obuf, lane);
       tc_fence_before();
       mbar_arrive(&sh->tempty[acc]);
@@ -330,7 +343,8 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
 cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s, const int32_t* gather_rows,
-                           int gather_div, int gather_src_rows, int seg_stride) {
+                           int gather_div, int gather_src_rows, int seg_stride,
+                           const SplitUp* split) {
   if (M == 0 || N == 0) return cudaSuccess;
   // The two-SM (cta_group::2) kernel with MOE_TC_KERNEL=2sm.  Its SMs load a
   // third fewer bytes per MMA on 256-row pair tiles, but on the routed
@@ -342,7 +356,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     return v && v[0] == '2';
   }();
   const bool gather = gather_rows != nullptr;
-  if (two_sm && num_sms() >= 2)
+  if (two_sm && num_sms() >= 2 && !split)
     return launch_gemm_tc2(a, w, bias, seg_end, M, N, K, E, act, out, status, s, gather_rows,
                            gather_div, gather_src_rows, seg_stride);
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
@@ -355,14 +369,25 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     alpha = act->alpha;
     beta = act->beta;
   }
-  CUtensorMap ma, mb;
+  // split weights: w is the gate projection [E, N, K], split->w_up the up
+  // projection, both read by 128-row boxes (only with a stacked gated mode)
+  if (split && mode != kTcStacked) return cudaErrorInvalidValue;
+  if (split) N1 = N;
+  CUtensorMap ma, mb, mb_up;
   if (!gather) {  // (gathered rows of A are loaded without a tensor map)
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {BK, BM};
     if (!tmap::encode_bf16(&ma, a, 2, dims, str, box)) return cudaErrorInvalidValue;
   }
-  if (mode == kTcStacked) {
+  if (split) {
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)E};
+    cuuint64_t str[2] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2};
+    cuuint32_t box[3] = {BK, BN / 2, 1};
+    if (!tmap::encode_bf16(&mb, w, 3, dims, str, box) ||
+        !tmap::encode_bf16(&mb_up, split->w_up, 3, dims, str, box))
+      return cudaErrorInvalidValue;
+  } else if (mode == kTcStacked) {
     cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)N, 2, (cuuint64_t)E};
     cuuint64_t str[3] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2, (cuuint64_t)2 * N * K * 2};
     cuuint32_t box[4] = {BK, BN / 2, 2, 1};  // 128 gate rows then 128 up rows
@@ -374,6 +399,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     if (!tmap::encode_bf16(&mb, w, 3, dims, str, box)) return cudaErrorInvalidValue;
   }
   if (gather) ma = mb;  // unused by the kernel
+  if (!split) mb_up = mb;  // unused
   static std::once_flag attr_once;
   std::call_once(attr_once, [] {
     for (const void* fn : {(const void*)gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY, false>,
@@ -426,7 +452,8 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
   launch_pdl(kern, grid, gather ? NUM_THREADS_GATHER : NUM_THREADS, kSmemBytes, s, ma, mb,
              bias_p, seg_end, M, N, N1, K, E, limit, alpha, beta, mo, tma_out, out_p, status,
              static_cast<const __nv_bfloat16*>(a), gather_rows, gather_div, gather_src_rows,
-             seg_stride);
+             seg_stride, mb_up, split ? 1 : 0,
+             split ? static_cast<const __nv_bfloat16*>(split->b_up) : nullptr);
   count_launch();
   return cudaGetLastError();
 }

@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
       if (st.m_end - st.m0 > BMC) {
         drain_acc<MODE, ACT>(tbase, st.m0 + BMC * (int)rank + quad * 32, st.m_end, st.n_idx,
-                             st.e, bias, N1, Nout, limit, alpha, beta, &tm_out, tma_out, out,
+                             st.e, bias, nullptr, N1, Nout, limit, alpha, beta, &tm_out, tma_out, out,
                              obufs, obuf, lane);
       } else {
         // short tile (M128 over the pair): TMEM lane 64h + r holds row
@@ -412,11 +412,11 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
         if (wrow0 < st.m_end) {  // warp-uniform
           if constexpr (MODE == kTcPlain)
             drain_cols<MODE, ACT>(tbase, wrow0, st.m_end, st.n_idx * BN + (BN / 2) * h,
-                                  BN / 2 / 32, 0, st.e, bias, N1, Nout, limit, alpha, beta,
+                                  BN / 2 / 32, 0, st.e, bias, nullptr, N1, Nout, limit, alpha, beta,
                                   &tm_out, tma_out, out, obufs, obuf, lane);
           else
             drain_cols<MODE, ACT>(tbase, wrow0, st.m_end, st.n_idx * (BN / 2) + BMS * h,
-                                  BMS / 32, BMS, st.e, bias, N1, Nout, limit, alpha, beta,
+                                  BMS / 32, BMS, st.e, bias, nullptr, N1, Nout, limit, alpha, beta,
                                   &tm_out, tma_out, out, obufs, obuf, lane);
         }
       }

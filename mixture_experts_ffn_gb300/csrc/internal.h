@@ -132,12 +132,20 @@ cudaError_t launch_swiglu(const void* gate, const void* up, int64_t R, int I, mo
                           int fusion, float limit, float alpha, float beta, void* out,
                           cudaStream_t s);
 
+// SwiGLU fusion 0: the gate and up projections of a gated gate_up GEMM as two
+// tensors, [E, F, K] each, with optional biases [E, F] each.  The launchers'
+// w / bias then hold the gate projection and its bias.
+struct SplitUp {
+  const void* w_up;
+  const void* b_up;
+};
+
 // SIMT grouped GEMM (exact fp32 FMA; any dtype).  act == nullptr: plain GEMM
 // with N output columns; otherwise N = F act columns read from N1 rows.
 cudaError_t launch_gemm_simt(const void* a, const void* w, const void* bias,
                              const int32_t* seg_end, int M, int N, int K, int E, moe_dtype dt,
                              const moe_act_params* act, void* out, int* status, cudaStream_t s,
-                             int seg_stride = 0);
+                             int seg_stride = 0, const SplitUp* split = nullptr);
 
 // tcgen05 grouped GEMM (bf16 operands, fp32 TMEM accumulators).  With
 // gather_rows, row r of A is row gather_rows[r] / gather_div of `a` (the
@@ -147,7 +155,8 @@ cudaError_t launch_gemm_simt(const void* a, const void* w, const void* bias,
 cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s, const int32_t* gather_rows = nullptr,
-                           int gather_div = 1, int gather_src_rows = 0, int seg_stride = 0);
+                           int gather_div = 1, int gather_src_rows = 0, int seg_stride = 0,
+                           const SplitUp* split = nullptr);
 
 // block-scaled FP8 grouped GEMM over a masked slab (e4m3 operands, fp32
 // scales per row x 128 K of a and per 128 x 128 block of b, bf16 out)

@@ -55,6 +55,10 @@ _SIGNATURES = {
     "moe_grouped_gemm_workspace_size": [_i, _i, _i],
     "moe_permute_align_workspace_size": [_i, _i, _i],
     "moe_grouped_gemm_act": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _sz, _vp],
+    "moe_grouped_gemm_act_split": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp,
+                                   _vp, _sz, _vp],
+    "moe_ffn_forward_split": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i,
+                              _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_act_gathered": [_vp, _i, _vp, _i, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
                                       _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_down": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
@@ -323,6 +327,25 @@ def moe_grouped_gemm_act(a, w_gate_up, seg_end, F: int, act: ActParams, b_gate_u
     return out
 
 
+def moe_grouped_gemm_act_split(a, w_gate, w_up, seg_end, act: ActParams, b_gate=None, b_up=None,
+                               out=None, ws=None):
+    """moe_grouped_gemm_act with the gate and up projections in two tensors
+    w_gate, w_up [E, F, Hk] (SwiGLU fusion 0); returns out [M, F]."""
+    lib = load_library()
+    _cuda(a, w_gate, w_up, seg_end, b_gate, b_up)
+    M, Hk = a.shape
+    E, F, _ = w_gate.shape
+    if out is None:
+        out = torch.empty((M, F), dtype=a.dtype, device=a.device)
+    if ws is None:
+        ws = _ws(MOE_STATUS_BYTES, a.device)
+    _check("moe_grouped_gemm_act_split",
+           lib.moe_grouped_gemm_act_split(_p(a), _p(w_gate), _p(w_up), _p(b_gate), _p(b_up),
+                                          _p(seg_end), M, F, Hk, E, _dt(a), ctypes.byref(act),
+                                          _p(out), _p(ws), ws.numel(), _stream()))
+    return out
+
+
 def moe_grouped_gemm_act_gathered(hidden, row_to_route, top_k: int, w_gate_up, seg_end, F: int,
                                   act: ActParams, b_gate_up=None, out=None, ws=None):
     """moe_grouped_gemm_act with row m of the operand read as
@@ -421,6 +444,31 @@ def moe_ffn_forward(hidden, logits, w_gate_up, w_down, p: RouteParams, act: ActP
                                H, F, E, _dt(hidden), ctypes.byref(p), ctypes.byref(act), _p(out),
                                _p(topk_weights_out), _p(topk_ids_out), _p(router_probs),
                                _p(weight_scale), _p(ws), ws.numel(), _stream()))
+    return out
+
+
+def moe_ffn_forward_split(hidden, logits, w_gate, w_up, w_down, p: RouteParams, act: ActParams,
+                          correction_bias=None, expert_ids=None, b_gate=None, b_up=None,
+                          b_down=None, out=None, topk_weights_out=None, topk_ids_out=None,
+                          router_probs=None, weight_scale=None, ws=None):
+    """moe_ffn_forward with the gate and up projections in two tensors
+    w_gate, w_up [E, F, H] (SwiGLU fusion 0); returns ``out`` [T, H]."""
+    lib = load_library()
+    _cuda(hidden, logits, w_gate, w_up, w_down, correction_bias, expert_ids, b_gate, b_up,
+          b_down)
+    T, H = hidden.shape
+    E, _, F = w_down.shape
+    if out is None:
+        out = torch.empty_like(hidden)
+    if ws is None:
+        ws = _ws(lib.moe_workspace_size(T, H, F, E, p.top_k, _dt(hidden)), hidden.device)
+    _check("moe_ffn_forward_split",
+           lib.moe_ffn_forward_split(_p(hidden), _p(logits), _p(w_gate), _p(w_up), _p(w_down),
+                                     _p(correction_bias), _p(expert_ids), _p(b_gate), _p(b_up),
+                                     _p(b_down), T, H, F, E, _dt(hidden), ctypes.byref(p),
+                                     ctypes.byref(act), _p(out), _p(topk_weights_out),
+                                     _p(topk_ids_out), _p(router_probs), _p(weight_scale),
+                                     _p(ws), ws.numel(), _stream()))
     return out
 
 
