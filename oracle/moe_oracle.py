@@ -44,7 +44,10 @@ from typing import Optional
 
 import numpy as np
 
-NEG_SENTINEL_F32 = -1e30  # [MoERouter] "a large negative value elsewhere (-1e30 ...)"
+# [MoERouter] router_probs of an expert that is not chosen: -1e30, except in
+# float16, whose largest finite magnitude (65504) it exceeds; there -1e4
+NEG_SENTINEL_F32 = -1e30
+NEG_SENTINEL_F16 = -1e4
 
 ACT_SILU_AND_MUL = 0
 ACT_SWIGLU = 1
@@ -87,6 +90,8 @@ def round_to(x, dtype: Optional[str]) -> np.ndarray:
         return x.astype(np.float32).astype(np.float64)
     if dtype == "bf16":
         return round_bf16(x)
+    if dtype == "f16":  # IEEE binary16, round to nearest even
+        return x.astype(np.float16).astype(np.float64)
     raise ValueError(dtype)
 
 
@@ -156,7 +161,8 @@ def topk_ascending(u, K: int) -> np.ndarray:
 def route(logits, K: int, scoring: str = "softmax", renormalize: bool = True,
           G: int = 1, TG: int = 1, rsf: float = 1.0, correction_bias=None,
           expert_ids=None, local_start: int = 0, local_count: int = 0,
-          route_scale: float = 1.0, score_dtype=np.float32) -> dict:
+          route_scale: float = 1.0, score_dtype=np.float32,
+          probs_dtype: Optional[str] = None) -> dict:
     """Router of one layer.
 
     Returns ``topk_ids`` [T,K] int32, ``topk_weights`` [T,K] float64 and, when
@@ -175,6 +181,9 @@ def route(logits, K: int, scoring: str = "softmax", renormalize: bool = True,
          router_probs[t, j] = log(sum of w^ over routes on expert local_start+j)
          when that expert is chosen, -1e30 otherwise; weight_scale[t] =
          route_scale * (sum of w^ over local routes), 0 when none is local.
+         ``probs_dtype`` (the MoERouter tensor type of router_probs): the logs
+         rounded to it, and the sentinel -1e4 in "f16" (-1e30 rounded to it
+         otherwise); None keeps float64 values and -1e30.
     """
     s = expert_scores(logits, scoring, score_dtype)
     T, E = s.shape
@@ -192,7 +201,8 @@ def route(logits, K: int, scoring: str = "softmax", renormalize: bool = True,
     out = {"topk_ids": ids, "topk_weights": w}
     if local_count > 0:
         wn = chosen / chosen.sum(axis=1, keepdims=True)
-        probs = np.full((T, local_count), NEG_SENTINEL_F32, dtype=np.float64)
+        sentinel = NEG_SENTINEL_F16 if probs_dtype == "f16" else NEG_SENTINEL_F32
+        probs = np.full((T, local_count), sentinel, dtype=np.float64)
         scale = np.zeros(T, dtype=np.float64)
         for t in range(T):
             acc = {}
@@ -203,7 +213,7 @@ def route(logits, K: int, scoring: str = "softmax", renormalize: bool = True,
             for j, v in acc.items():
                 probs[t, j] = math.log(v)
             scale[t] = route_scale * sum(acc.values()) if acc else 0.0
-        out["router_probs"] = probs
+        out["router_probs"] = round_to(probs, probs_dtype)
         out["weight_scale"] = scale
     return out
 

@@ -319,6 +319,75 @@ def test_expert_parallel_slices_sum_to_the_layer():
     np.testing.assert_allclose(total, full, rtol=2e-6, atol=2e-6 * np.abs(full).max())
 
 
+def _f16_grid():
+    """Every finite IEEE binary16 value, built from its fields (sign, 5-bit
+    exponent with bias 15, 10-bit fraction; exponent 0 subnormal), ascending,
+    with the parity of each value's fraction field."""
+    val, par = [], []
+    for f in range(1024):  # zero and the subnormals
+        val.append(f * 2.0 ** -24)
+        par.append(f & 1)
+    for e in range(1, 31):
+        for f in range(1024):
+            val.append((1024 + f) * 2.0 ** (e - 25))
+            par.append(f & 1)
+    val, par = np.array(val), np.array(par)
+    return np.concatenate([-val[:0:-1], val]), np.concatenate([par[:0:-1], par])
+
+
+def test_f16_rounding_against_the_grid():
+    """round_to(x, "f16") is the nearest binary16 value, ties to the even
+    fraction, overflow to infinity at 65520 = 65504 + half its spacing."""
+    grid, odd = _f16_grid()
+    assert grid[-1] == 65504.0 and len(grid) == 2 * 31744 - 1
+    rng = np.random.default_rng(17)
+    x = np.concatenate([rng.standard_normal(3000) * 10.0 ** rng.uniform(-8, 4.8, 3000),
+                        (grid[:-1] + grid[1:]) / 2])  # every midpoint: a tie
+    x = x[np.abs(x) < 65504.0]
+    got = O.round_to(x, "f16")
+    for v, g in zip(x, got):
+        j = np.searchsorted(grid, v)
+        lo, hi = grid[j - 1], grid[j]
+        want = lo if (v - lo < hi - v or (v - lo == hi - v and not odd[j - 1])) else hi
+        assert g == want or (g == 0 and want == 0), (v, g, want)
+    assert np.isinf(O.round_to(np.array([65520.0, -1e30]), "f16")).all()
+    assert O.round_to(np.array([65519.99]), "f16")[0] == 65504.0
+
+
+def test_moerouter_f16_sentinel_survives_and_keeps_the_invariant():
+    """In float16 router_probs, -1e30 would overflow to -inf (a token with no
+    local expert would give QMoE's softmax a row of -inf: NaN); the -1e4
+    sentinel stays finite, that row's softmax is the degenerate uniform one
+    (weight_scale 0 removes it), and on other rows the softmax over the f16
+    logs still returns w_e / W_local to float16 precision and exactly 0 at
+    the sentinel."""
+    from scipy.special import softmax
+
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=256)
+    z = cases.guarded_logits(cfg).numpy()
+    E, K, lc = cfg.E, cfg.K, 16
+    assert np.isinf(O.round_to(np.array([O.NEG_SENTINEL_F32]), "f16")).all()
+    n_empty = 0
+    for start in range(0, E, lc):
+        r = O.route(z, K, "softmax", True, local_start=start, local_count=lc, probs_dtype="f16")
+        x = O.route(z, K, "softmax", True, local_start=start, local_count=lc)
+        p = r["router_probs"]
+        np.testing.assert_array_equal(p, O.round_to(p, "f16"))  # representable
+        assert np.isfinite(p).all()
+        for t in range(z.shape[0]):
+            sm = softmax(p[t].astype(np.float32))
+            assert np.isfinite(sm).all()
+            if r["weight_scale"][t] == 0:
+                n_empty += 1
+                assert np.all(p[t] == -1e4)
+                continue
+            want = softmax(x["router_probs"][t])
+            assert np.all(sm[want == 0] == 0)
+            # |log w| <= ~12 here, so one f16 rounding of a log moves w by < 2^-11 * 12
+            np.testing.assert_allclose(sm, want, rtol=8e-3, atol=0)
+    assert n_empty > 0
+
+
 def test_moerouter_normalises_even_without_renormalize():
     z = np.log(np.array([[1.0, 2.0, 3.0, 4.0]], np.float32))
     r = O.route(z, 2, "softmax", False, rsf=3.0, local_start=0, local_count=4)
