@@ -65,7 +65,13 @@ typedef enum moe_status {
   MOE_ERR_WORKSPACE = 7    /* ws is NULL, misaligned or smaller than required      */
 } moe_status;
 
-typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+/* Element types [ORT-MoE and MoERouter, tensor type T: float, float16,
+ * bfloat16].  Arithmetic is float32 for every type; results are rounded to
+ * the operand type (round to nearest even) at the points the bf16 path
+ * rounds.  MOE_F16 takes the same paths as MOE_BF16 (tcgen05 GEMMs with
+ * kind::f16 float16 operands) except the indexed decode kernel, which is
+ * bf16 only. */
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_F16 = 2 } moe_dtype;
 
 /* Router scores of the logits z [MoERouter scoring; TileOPs FusedTopKFwdOp]:
  * softmax over the experts; sigmoid(z); sqrt(log(1 + exp(z))) (the name
@@ -111,6 +117,10 @@ typedef struct moe_route_params {
   int32_t local_expert_start;    /* MoERouter slice [start, start + count) of [0, E)   */
   int32_t local_expert_count;    /* 0: no router_probs / weight_scale outputs          */
   float route_scale;             /* MoERouter weight_scale multiplier                  */
+  int32_t dtype;                 /* moe_dtype of logits and router_probs (MoERouter's
+                                    T; 0 = float32).  Scores are float32 whatever T;
+                                    the router_probs sentinel is -1e30, or -1e4 in
+                                    float16 (-1e30 overflows it)                      */
 } moe_route_params;
 
 /* Gated activation fused into the gate_up GEMM epilogue. */
@@ -149,9 +159,9 @@ typedef struct moe_act_params {
  *   router_probs    [T, local_expert_count] f32 out or NULL
  *   weight_scale    [T] f32 out or NULL (both or neither when count > 0)
  * E <= 1024.  T == 0 is a no-op. */
-moe_status moe_route(const float* logits, const float* correction_bias,
+moe_status moe_route(const void* logits, const float* correction_bias,
                      const int32_t* expert_ids, int T, int E, const moe_route_params* p,
-                     float* topk_weights, int32_t* topk_ids, float* router_probs,
+                     float* topk_weights, int32_t* topk_ids, void* router_probs,
                      float* weight_scale, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
@@ -166,9 +176,9 @@ moe_status moe_route(const float* logits, const float* correction_bias,
  * barriers; the launch is cooperative, so the grid starts only when all of
  * its CTAs can be resident (concurrent calls on other streams are safe).  A
  * barrier that still waits after 2 s latches MOE_ERR_TIMEOUT. */
-moe_status moe_route_permute(const float* logits, const float* correction_bias,
+moe_status moe_route_permute(const void* logits, const float* correction_bias,
                              const int32_t* expert_ids, int T, int E, const moe_route_params* p,
-                             float* topk_weights, int32_t* topk_ids, float* router_probs,
+                             float* topk_weights, int32_t* topk_ids, void* router_probs,
                              float* weight_scale, int32_t* seg_end, int32_t* row_to_route,
                              int32_t* route_to_row, void* ws, size_t ws_bytes,
                              cudaStream_t stream);
@@ -404,12 +414,12 @@ moe_status moe_indexed_mlp(const void* hidden, const void* w_gate_up, const void
  *   (optional copies of the routing);  router_probs / weight_scale as in
  *   moe_route (NULL unless p->local_expert_count > 0);
  *   ws >= moe_workspace_size(T, H, F, E, K, dtype). */
-moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* w_gate_up,
+moe_status moe_ffn_forward(const void* hidden, const void* logits, const void* w_gate_up,
                            const void* w_down, const float* correction_bias,
                            const int32_t* expert_ids, const void* b_gate_up, const void* b_down,
                            int T, int H, int F, int E, moe_dtype dtype,
                            const moe_route_params* p, const moe_act_params* act, void* out,
-                           float* topk_weights_out, int32_t* topk_ids_out, float* router_probs,
+                           float* topk_weights_out, int32_t* topk_ids_out, void* router_probs,
                            float* weight_scale, void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* moe_ffn_forward with the gate and up projections of the experts in two
@@ -418,13 +428,13 @@ moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* 
  * NULL, both or neither.  Always the staged pipeline (the indexed path reads
  * stacked weights); the gate_up GEMM reads both tensors into one accumulator
  * tile.  Everything else, ws included, as moe_ffn_forward. */
-moe_status moe_ffn_forward_split(const void* hidden, const float* logits, const void* w_gate,
+moe_status moe_ffn_forward_split(const void* hidden, const void* logits, const void* w_gate,
                                  const void* w_up, const void* w_down,
                                  const float* correction_bias, const int32_t* expert_ids,
                                  const void* b_gate, const void* b_up, const void* b_down, int T,
                                  int H, int F, int E, moe_dtype dtype, const moe_route_params* p,
                                  const moe_act_params* act, void* out, float* topk_weights_out,
-                                 int32_t* topk_ids_out, float* router_probs, float* weight_scale,
+                                 int32_t* topk_ids_out, void* router_probs, float* weight_scale,
                                  void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
@@ -433,7 +443,7 @@ moe_status moe_ffn_forward_split(const void* hidden, const float* logits, const 
  * SwiGLU contrib operators", MoERouter: the expert op's own softmax over the
  * local row of router_probs returns w_e / W_local, and weight_scale
  * multiplies that factor back out before the ranks' outputs are summed].
- * Routes each token by the softmax of its router_probs row (fp32) and its top
+ * Routes each token by the softmax (in fp32) of its router_probs row and its top
  * min(K, lc) experts (ties to the lower index, no renormalisation), runs the
  * expert MLPs of this rank's experts as moe_ffn_forward does (the tensor-core
  * or staged path; not the indexed one), and multiplies each token's combined
@@ -441,16 +451,17 @@ moe_status moe_ffn_forward_split(const void* hidden, const float* logits, const 
  * outputs give the routed layer with normalised weights times route_scale; a
  * token with no expert on this rank has weight_scale 0 and contributes 0.
  *
- *   hidden [T, H] dtype;  router_probs [T, lc] f32;  weight_scale [T] f32;
+ *   hidden [T, H] dtype;  router_probs [T, lc] probs_dtype (as the router
+ *   wrote it: f32, bf16, or f16 with its -1e4 sentinel);  weight_scale [T] f32;
  *   w_gate_up [lc, N1, H], w_down [lc, H, F] (this rank's experts);
  *   b_gate_up [lc, N1] | NULL, b_down [lc, H] | NULL;  out [T, H] dtype;
  *   ws >= moe_workspace_size(T, H, F, lc, min(K, lc), dtype). */
-moe_status moe_ffn_forward_local(const void* hidden, const float* router_probs,
+moe_status moe_ffn_forward_local(const void* hidden, const void* router_probs,
                                  const float* weight_scale, const void* w_gate_up,
                                  const void* w_down, const void* b_gate_up, const void* b_down,
                                  int T, int H, int F, int lc, int K, moe_dtype dtype,
-                                 const moe_act_params* act, void* out, void* ws, size_t ws_bytes,
-                                 cudaStream_t stream);
+                                 moe_dtype probs_dtype, const moe_act_params* act, void* out,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* moe_ffn_forward for a caller whose activations live in HOST memory:
@@ -467,7 +478,7 @@ moe_status moe_ffn_forward_local(const void* hidden, const float* router_probs,
  * synchronised.  Pageable buffers work, but their copies synchronise.
  * Weights, biases and expert_ids stay device pointers.  Routing outputs are
  * not returned.  ws >= moe_workspace_size_host(T, H, F, E, K, dtype). */
-moe_status moe_ffn_forward_host(const void* hidden_host, const float* logits_host,
+moe_status moe_ffn_forward_host(const void* hidden_host, const void* logits_host,
                                 const void* w_gate_up, const void* w_down,
                                 const float* correction_bias, const int32_t* expert_ids,
                                 const void* b_gate_up, const void* b_down, int T, int H, int F,
@@ -553,7 +564,7 @@ size_t moe_shared_expert_workspace_size(int T, int H, int S, moe_dtype dtype);
  * NULL (shared_out untouched, S ignored).  The two halves run one after the
  * other on `stream` and share `ws`:
  * ws >= moe_workspace_size_shared(T, H, F, S, E, K, dtype). */
-moe_status moe_ffn_forward_shared(const void* hidden, const float* logits, const void* w_gate_up,
+moe_status moe_ffn_forward_shared(const void* hidden, const void* logits, const void* w_gate_up,
                                   const void* w_down, const float* correction_bias,
                                   const void* shared_w_gate_up, const void* shared_w_down, int T,
                                   int H, int F, int S, int E, moe_dtype dtype,

@@ -56,17 +56,19 @@ bool any_overlap(const Span (&outs)[NO], const Span (&ins)[NI]) {
   return false;
 }
 
-size_t esize(moe_dtype d) { return d == MOE_BF16 ? 2 : 4; }
-bool dtype_ok(int d) { return d == MOE_F32 || d == MOE_BF16; }
+size_t esize(moe_dtype d) { return d == MOE_F32 ? 4 : 2; }
+bool dtype_ok(int d) { return d == MOE_F32 || d == MOE_BF16 || d == MOE_F16; }
+// bytes of one logit / router_probs element (the MoERouter type T)
+size_t rsz(const moe_route_params* p) { return esize((moe_dtype)p->dtype); }
 
 moe_status cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-moe_status check_route(const float* logits, const float* bias, int T, int E,
+moe_status check_route(const void* logits, const float* bias, int T, int E,
                        const moe_route_params* p, const float* w, const int32_t* ids,
-                       const float* probs, const float* wscale) {
-  if (!p || T < 0 || E < 1 || E > kMaxExperts) return MOE_ERR_INVALID_ARG;
+                       const void* probs, const float* wscale) {
+  if (!p || T < 0 || E < 1 || E > kMaxExperts || !dtype_ok(p->dtype)) return MOE_ERR_INVALID_ARG;
   const int K = p->top_k, G = p->num_expert_group, TG = p->topk_group;
   if (K < 1 || K > E || K > 64) return MOE_ERR_INVALID_ARG;
   if (p->scoring != MOE_SCORING_SOFTMAX && p->scoring != MOE_SCORING_SIGMOID &&
@@ -126,9 +128,9 @@ cudaError_t grouped_gemm(const void* a, const void* w, const void* bias, const i
                          int M, int Nout, int Kd, int E, moe_dtype dt, const moe_act_params* act,
                          void* out, int* status, cudaStream_t s, int seg_stride = 0,
                          const SplitUp* split = nullptr) {
-  if (dt == MOE_BF16 && tc_ok(a, w, out, Nout, Kd, M) && (!split || aligned16(split->w_up)))
+  if (dt != MOE_F32 && tc_ok(a, w, out, Nout, Kd, M) && (!split || aligned16(split->w_up)))
     return launch_gemm_tc(a, w, bias, seg_end, M, Nout, Kd, E, act, out, status, s, nullptr, 1, 0,
-                          seg_stride, split);
+                          seg_stride, split, dt == MOE_F16);
   return launch_gemm_simt(a, w, bias, seg_end, M, Nout, Kd, E, dt, act, out, status, s,
                           seg_stride, split);
 }
@@ -148,27 +150,27 @@ using namespace moe;
 
 extern "C" {
 
-moe_status moe_route(const float* logits, const float* correction_bias, const int32_t* expert_ids,
+moe_status moe_route(const void* logits, const float* correction_bias, const int32_t* expert_ids,
                      int T, int E, const moe_route_params* p, float* topk_weights,
-                     int32_t* topk_ids, float* router_probs, float* weight_scale,
+                     int32_t* topk_ids, void* router_probs, float* weight_scale,
                      cudaStream_t stream) {
   moe_status st = check_route(logits, correction_bias, T, E, p, topk_weights, topk_ids,
                               router_probs, weight_scale);
   if (st != MOE_OK) return st;
   if (T == 0) return MOE_OK;
   const size_t TK = (size_t)T * p->top_k, lc = (size_t)p->local_expert_count;
-  Span outs[] = {{topk_weights, TK * 4}, {topk_ids, TK * 4}, {router_probs, T * lc * 4},
+  Span outs[] = {{topk_weights, TK * 4}, {topk_ids, TK * 4}, {router_probs, T * lc * rsz(p)},
                  {weight_scale, (size_t)T * 4}};
-  Span ins[] = {{logits, (size_t)T * E * 4}, {correction_bias, (size_t)E * 4},
+  Span ins[] = {{logits, (size_t)T * E * rsz(p)}, {correction_bias, (size_t)E * 4},
                 {expert_ids, TK * 4}};
   if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
   return cuda_status(launch_route(logits, correction_bias, expert_ids, T, E, *p, topk_weights,
                                   topk_ids, router_probs, weight_scale, stream));
 }
 
-moe_status moe_route_permute(const float* logits, const float* correction_bias,
+moe_status moe_route_permute(const void* logits, const float* correction_bias,
                              const int32_t* expert_ids, int T, int E, const moe_route_params* p,
-                             float* topk_weights, int32_t* topk_ids, float* router_probs,
+                             float* topk_weights, int32_t* topk_ids, void* router_probs,
                              float* weight_scale, int32_t* seg_end, int32_t* row_to_route,
                              int32_t* route_to_row, void* ws, size_t ws_bytes,
                              cudaStream_t stream) {
@@ -182,10 +184,10 @@ moe_status moe_route_permute(const float* logits, const float* correction_bias,
   const int M = (int)TKl;
   if (!ws_ok(ws, ws_bytes, PermuteWs(M, E).total)) return MOE_ERR_WORKSPACE;
   const size_t TK = (size_t)M, lc = (size_t)p->local_expert_count;
-  Span outs[] = {{topk_weights, TK * 4}, {topk_ids, TK * 4}, {router_probs, T * lc * 4},
+  Span outs[] = {{topk_weights, TK * 4}, {topk_ids, TK * 4}, {router_probs, T * lc * rsz(p)},
                  {weight_scale, (size_t)T * 4}, {seg_end, (size_t)E * 4},
                  {row_to_route, TK * 4}, {route_to_row, TK * 4}, {ws, PermuteWs(M, E).total}};
-  Span ins[] = {{logits, (size_t)T * E * 4}, {correction_bias, (size_t)E * 4},
+  Span ins[] = {{logits, (size_t)T * E * rsz(p)}, {correction_bias, (size_t)E * 4},
                 {expert_ids, TK * 4}};
   if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
   if (T == 0) return cuda_status(cudaMemsetAsync(seg_end, 0, (size_t)E * 4, stream));
@@ -413,11 +415,12 @@ moe_status moe_grouped_gemm_act_gathered(const void* hidden, int T, const int32_
                 {w_gate_up, (size_t)E * N1 * H * 2}, {b_gate_up, b_gate_up ? (size_t)E * N1 * 2 : 0},
                 {seg_end, (size_t)E * 4}, {ws, MOE_STATUS_BYTES}};
   if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
-  if (dtype != MOE_BF16 || !tc_ok(hidden, w_gate_up, out, F, H, M))
+  if (dtype == MOE_F32 || !tc_ok(hidden, w_gate_up, out, F, H, M))
     return MOE_ERR_UNSUPPORTED;
   if (M == 0) return MOE_OK;
   return cuda_status(launch_gemm_tc(hidden, w_gate_up, b_gate_up, seg_end, M, F, H, E, act, out,
-                                    static_cast<int*>(ws), stream, row_to_route, top_k, T));
+                                    static_cast<int*>(ws), stream, row_to_route, top_k, T, 0,
+                                    nullptr, dtype == MOE_F16));
 }
 
 moe_status moe_grouped_gemm_down(const void* a, const void* w_down, const void* b_down,
@@ -516,12 +519,12 @@ struct HostHooks {
   bool wrote_direct = false;
 };
 
-moe_status ffn_forward(const void* hidden, const float* logits, const void* w_gate_up,
+moe_status ffn_forward(const void* hidden, const void* logits, const void* w_gate_up,
                        const void* w_down, const float* correction_bias,
                        const int32_t* expert_ids, const void* b_gate_up, const void* b_down,
                        int T, int H, int F, int E, moe_dtype dtype, const moe_route_params* p,
                        const moe_act_params* act, void* out, float* topk_weights_out,
-                       int32_t* topk_ids_out, float* router_probs, float* weight_scale,
+                       int32_t* topk_ids_out, void* router_probs, float* weight_scale,
                        void* ws, size_t ws_bytes, cudaStream_t stream, HostHooks* hooks) {
   const SplitUp* split = hooks && hooks->split.w_up ? &hooks->split : nullptr;
   moe_act_params split_st{};
@@ -546,10 +549,10 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
   const size_t n_up = split ? N1 : 0;
   const size_t lc = (size_t)p->local_expert_count;
   Span outs[] = {{out, (size_t)T * H * esz},        {topk_weights_out, M * 4},
-                 {topk_ids_out, M * 4},             {router_probs, T * lc * 4},
+                 {topk_ids_out, M * 4},             {router_probs, T * lc * rsz(p)},
                  {weight_scale, (size_t)T * 4},     {ws, L.total}};
   Span ins[] = {{hidden, (size_t)T * H * esz},
-                {logits, (size_t)T * E * 4},
+                {logits, (size_t)T * E * rsz(p)},
                 {w_gate_up, (size_t)E * N1 * H * esz},
                 {w_down, (size_t)E * H * F * esz},
                 {correction_bias, correction_bias ? (size_t)E * 4 : 0},
@@ -578,7 +581,7 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
   // token-ordered hidden states through row_to_route, so the permute only
   // builds the index maps and the permuted copy of the activations is never
   // written or read back.
-  const bool fused_gather = !indexed && dtype == MOE_BF16 &&
+  const bool fused_gather = !indexed && dtype != MOE_F32 &&
                             tc_ok(hidden, w_gate_up, a1, F, H, (int)M) &&
                             (!split || aligned16(split->w_up));
   // Routing and the index maps take one launch; the staged path then copies
@@ -611,7 +614,7 @@ moe_status ffn_forward(const void* hidden, const float* logits, const void* w_ga
   }
   if (fused_gather)
     err = launch_gemm_tc(hidden, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, act, a1, status,
-                         stream, r2r, K, T, 0, split);
+                         stream, r2r, K, T, 0, split, dtype == MOE_F16);
   else
     err = grouped_gemm(xin, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, dtype, act, a1,
                        status, stream, 0, split);
@@ -663,14 +666,15 @@ cudaError_t side_stream(cudaStream_t* out) {
 
 }  // namespace
 
-moe_status moe_ffn_forward_local(const void* hidden, const float* router_probs,
+moe_status moe_ffn_forward_local(const void* hidden, const void* router_probs,
                                  const float* weight_scale, const void* w_gate_up,
                                  const void* w_down, const void* b_gate_up, const void* b_down,
                                  int T, int H, int F, int lc, int K, moe_dtype dtype,
-                                 const moe_act_params* act, void* out, void* ws, size_t ws_bytes,
-                                 cudaStream_t stream) {
+                                 moe_dtype probs_dtype, const moe_act_params* act, void* out,
+                                 void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (lc < 1 || K < 1 || (T > 0 && !weight_scale)) return MOE_ERR_INVALID_ARG;
   moe_route_params p{};
+  p.dtype = probs_dtype;
   p.top_k = std::min(K, lc);
   p.scoring = MOE_SCORING_SOFTMAX;
   p.renormalize = 0;
@@ -690,25 +694,25 @@ moe_status moe_ffn_forward_local(const void* hidden, const float* router_probs,
                      ws_bytes, stream, &hk);
 }
 
-moe_status moe_ffn_forward(const void* hidden, const float* logits, const void* w_gate_up,
+moe_status moe_ffn_forward(const void* hidden, const void* logits, const void* w_gate_up,
                            const void* w_down, const float* correction_bias,
                            const int32_t* expert_ids, const void* b_gate_up, const void* b_down,
                            int T, int H, int F, int E, moe_dtype dtype, const moe_route_params* p,
                            const moe_act_params* act, void* out, float* topk_weights_out,
-                           int32_t* topk_ids_out, float* router_probs, float* weight_scale,
+                           int32_t* topk_ids_out, void* router_probs, float* weight_scale,
                            void* ws, size_t ws_bytes, cudaStream_t stream) {
   return ffn_forward(hidden, logits, w_gate_up, w_down, correction_bias, expert_ids, b_gate_up,
                      b_down, T, H, F, E, dtype, p, act, out, topk_weights_out, topk_ids_out,
                      router_probs, weight_scale, ws, ws_bytes, stream, nullptr);
 }
 
-moe_status moe_ffn_forward_split(const void* hidden, const float* logits, const void* w_gate,
+moe_status moe_ffn_forward_split(const void* hidden, const void* logits, const void* w_gate,
                                  const void* w_up, const void* w_down,
                                  const float* correction_bias, const int32_t* expert_ids,
                                  const void* b_gate, const void* b_up, const void* b_down, int T,
                                  int H, int F, int E, moe_dtype dtype, const moe_route_params* p,
                                  const moe_act_params* act, void* out, float* topk_weights_out,
-                                 int32_t* topk_ids_out, float* router_probs, float* weight_scale,
+                                 int32_t* topk_ids_out, void* router_probs, float* weight_scale,
                                  void* ws, size_t ws_bytes, cudaStream_t stream) {
   if (!w_up) return MOE_ERR_INVALID_ARG;
   HostHooks hk;
@@ -780,7 +784,7 @@ size_t moe_workspace_size_shared(int T, int H, int F, int S, int E, int K, moe_d
   return a == 0 || b == 0 ? 0 : std::max(a, b);
 }
 
-moe_status moe_ffn_forward_shared(const void* hidden, const float* logits, const void* w_gate_up,
+moe_status moe_ffn_forward_shared(const void* hidden, const void* logits, const void* w_gate_up,
                                   const void* w_down, const float* correction_bias,
                                   const void* shared_w_gate_up, const void* shared_w_down, int T,
                                   int H, int F, int S, int E, moe_dtype dtype,
@@ -823,7 +827,7 @@ size_t moe_workspace_size_host(int T, int H, int F, int E, int K, moe_dtype dtyp
   return base + align256((size_t)T * H * esz) * 2 + align256((size_t)T * E * 4);
 }
 
-moe_status moe_ffn_forward_host(const void* hidden_host, const float* logits_host,
+moe_status moe_ffn_forward_host(const void* hidden_host, const void* logits_host,
                                 const void* w_gate_up, const void* w_down,
                                 const float* correction_bias, const int32_t* expert_ids,
                                 const void* b_gate_up, const void* b_down, int T, int H, int F,
@@ -870,7 +874,7 @@ moe_status moe_ffn_forward_host(const void* hidden_host, const float* logits_hos
     st = MOE_ERR_CUDA;
   } else {
     copied = true;
-    if (cudaMemcpyAsync(d_logits, logits_host, (size_t)T * E * 4, cudaMemcpyHostToDevice,
+    if (cudaMemcpyAsync(d_logits, logits_host, (size_t)T * E * rsz(p), cudaMemcpyHostToDevice,
                         stream) != cudaSuccess)
       st = MOE_ERR_CUDA;
   }

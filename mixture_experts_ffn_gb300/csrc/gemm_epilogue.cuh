@@ -55,8 +55,8 @@ __device__ __forceinline__ float gated(float g, float u, float limit, float alph
 // columns col0..): a whole 32 x 32 box staged in shared memory and written by
 // one TMA store when `boxed` (all 32 rows inside the segment), else row by
 // row for the rows that are (row_ok).  obufs holds NBUF 2 KB buffers of the
-// warp; obuf is the next one.
-template <int NBUF>
+// warp; obuf is the next one.  F16: the output is float16, else bfloat16.
+template <int NBUF, bool F16 = false>
 __device__ __forceinline__ void emit_chunk32(const float (&v)[32], int col0, int wrow0,
                                              bool boxed, bool row_ok,
                                              __nv_bfloat16* __restrict__ orow, int ncols_left,
@@ -71,10 +71,10 @@ __device__ __forceinline__ void emit_chunk32(const float (&v)[32], int col0, int
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint4 u;
-      u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-      u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-      u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-      u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+      u.x = pack2<F16>(v[8 * q + 0], v[8 * q + 1]);
+      u.y = pack2<F16>(v[8 * q + 2], v[8 * q + 3]);
+      u.z = pack2<F16>(v[8 * q + 4], v[8 * q + 5]);
+      u.w = pack2<F16>(v[8 * q + 6], v[8 * q + 7]);
       *reinterpret_cast<uint4*>(buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) = u;
     }
     fence_proxy_async_smem();
@@ -85,7 +85,7 @@ __device__ __forceinline__ void emit_chunk32(const float (&v)[32], int col0, int
     }
     obuf = NBUF == 1 ? 0 : obuf ^ 1;
   } else if (row_ok) {
-    store_row32(orow + col0, v, ncols_left);
+    store_row32<F16>(orow + col0, v, ncols_left);
   }
 }
 
@@ -97,8 +97,9 @@ __device__ __forceinline__ void emit_chunk32(const float (&v)[32], int col0, int
 // at or past m_end (the end of the tile's expert segment) are not written.
 // Bias rows are N1 wide; the up bias of a stacked tile is column Nout + j of
 // the expert's row, or column j of bias_up's row when the up projection is a
-// tensor of its own (bias_up != nullptr, N1 = Nout).
-template <int MODE, int ACT>
+// tensor of its own (bias_up != nullptr, N1 = Nout).  F16: bias and output
+// are float16 (the pointers' bfloat16 type is nominal), else bfloat16.
+template <int MODE, int ACT, bool F16 = false>
 __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end, int col_base,
                                            int nchunks, int up_off, int e,
                                            const __nv_bfloat16* __restrict__ bias,
@@ -117,7 +118,8 @@ __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end,
   // never writes rows of the next segment.
   const bool boxed = tma_out && m_end - wrow0 >= OUT_BOX;
   auto emit = [&](const float (&v)[32], int col0) {
-    emit_chunk32<2>(v, col0, wrow0, boxed, row_ok, orow, Nout - col0, tm_out, obufs, obuf, lane);
+    emit_chunk32<2, F16>(v, col0, wrow0, boxed, row_ok, orow, Nout - col0, tm_out, obufs, obuf,
+                         lane);
   };
   if constexpr (MODE == kTcPlain) {
 #pragma unroll 1
@@ -133,7 +135,7 @@ __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end,
       if (be) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (col0 + i < Nout) v[i] += __bfloat162float(be[col0 + i]);
+          if (col0 + i < Nout) v[i] += ld16<F16>(be + col0 + i);
       }
       if constexpr (ACT == MOE_ACT_RELU) {
 #pragma unroll
@@ -177,11 +179,11 @@ __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end,
         for (int i = 0; i < 32; ++i) {
           if (col0 + i < Nout) {
             if constexpr (MODE == kTcStacked) {
-              gv[i] += __bfloat162float(be[col0 + i]);
-              uv[i] += __bfloat162float(bu[col0 + i]);
+              gv[i] += ld16<F16>(be + col0 + i);
+              uv[i] += ld16<F16>(bu + col0 + i);
             } else {
-              gv[i] += __bfloat162float(be[2 * (col0 + i)]);
-              uv[i] += __bfloat162float(be[2 * (col0 + i) + 1]);
+              gv[i] += ld16<F16>(be + 2 * (col0 + i));
+              uv[i] += ld16<F16>(be + 2 * (col0 + i) + 1);
             }
           }
         }
@@ -197,7 +199,7 @@ __device__ __forceinline__ void drain_cols(uint32_t tbase, int wrow0, int m_end,
 // The whole 128-lane x 256-column accumulator of a tile: 256 output columns
 // (plain) or 128 activation columns (gated, up columns 128 to the right when
 // stacked) of column tile n_idx.
-template <int MODE, int ACT>
+template <int MODE, int ACT, bool F16 = false>
 __device__ __forceinline__ void drain_acc(uint32_t tbase, int wrow0, int m_end, int n_idx, int e,
                                           const __nv_bfloat16* __restrict__ bias,
                                           const __nv_bfloat16* __restrict__ bias_up, int N1, int Nout,
@@ -206,11 +208,11 @@ __device__ __forceinline__ void drain_acc(uint32_t tbase, int wrow0, int m_end, 
                                           __nv_bfloat16* __restrict__ out, uint8_t* obufs,
                                           int& obuf, int lane) {
   if constexpr (MODE == kTcPlain)
-    drain_cols<MODE, ACT>(tbase, wrow0, m_end, n_idx * kEpiCols, kEpiCols / 32, 0, e, bias,
+    drain_cols<MODE, ACT, F16>(tbase, wrow0, m_end, n_idx * kEpiCols, kEpiCols / 32, 0, e, bias,
                           bias_up, N1,
                           Nout, limit, alpha, beta, tm_out, tma_out, out, obufs, obuf, lane);
   else
-    drain_cols<MODE, ACT>(tbase, wrow0, m_end, n_idx * (kEpiCols / 2), kEpiCols / 64,
+    drain_cols<MODE, ACT, F16>(tbase, wrow0, m_end, n_idx * (kEpiCols / 2), kEpiCols / 64,
                           kEpiCols / 2, e, bias, bias_up, N1, Nout, limit, alpha, beta, tm_out, tma_out,
                           out, obufs, obuf, lane);
 }

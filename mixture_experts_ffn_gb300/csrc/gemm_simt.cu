@@ -167,6 +167,8 @@ cudaError_t launch_gemm_simt(const void* a, const void* w, const void* bias,
   if (M == 0 || N == 0) return cudaSuccess;
   if (dt == MOE_BF16)
     return launch_t<__nv_bfloat16>(a, w, bias, seg_end, M, N, K, E, act, out, s, seg_stride, split);
+  if (dt == MOE_F16)
+    return launch_t<__half>(a, w, bias, seg_end, M, N, K, E, act, out, s, seg_stride, split);
   return launch_t<float>(a, w, bias, seg_end, M, N, K, E, act, out, s, seg_stride, split);
 }
 

@@ -76,11 +76,12 @@ constexpr size_t kSmemBytes =
 
 
 constexpr uint32_t kIdesc = idesc_bf16(BM, BN);
+constexpr uint32_t kIdescF16 = idesc_f16(BM, BN);
 
 // The four K16 MMAs of one 64-wide k-block and the commit that frees its stage,
 // in one block: descriptors advance by 32 bytes (2 in 16-byte units) per K16.
 __device__ __forceinline__ void umma_kblock(uint32_t d_tmem, uint64_t ad, uint64_t bd,
-                                            uint32_t accumulate, uint32_t bar) {
+                                            uint32_t idesc, uint32_t accumulate, uint32_t bar) {
   asm volatile(
       "{\n\t.reg .pred p, t;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -91,7 +92,7 @@ __device__ __forceinline__ void umma_kblock(uint32_t d_tmem, uint64_t ad, uint64
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %10, %11, %3, t;\n\t"
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(
           d_tmem),
-      "l"(ad), "l"(bd), "r"(kIdesc), "r"(accumulate), "r"(bar), "l"(ad + 2), "l"(bd + 2),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate), "r"(bar), "l"(ad + 2), "l"(bd + 2),
       "l"(ad + 4), "l"(bd + 4), "l"(ad + 6), "l"(bd + 6)
       : "memory");
 }
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
                    const __nv_bfloat16* __restrict__ gsrc, const int32_t* __restrict__ grows,
                    int gdiv, int gsrc_rows, int seg_stride,
                    const __grid_constant__ CUtensorMap tm_b_up, int split,
-                   const __nv_bfloat16* __restrict__ bias_up) {
+                   const __nv_bfloat16* __restrict__ bias_up, int f16) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       // descriptors of stage 0; stage s adds s * STAGE_BYTES to the address field
       const uint64_t adesc0 = sw128_desc(su32(smem));
       const uint64_t bdesc0 = sw128_desc(su32(smem + A_BYTES));
+      const uint32_t idesc = f16 ? kIdescF16 : kIdesc;  // A and B of one type
       uint32_t empty_addr[STAGES];
       for (int s = 0; s < STAGES; ++s) empty_addr[s] = su32(&sh->empty[s]);
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
@@ -231,7 +233,8 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
           if constexpr (GATHER) fence_proxy_async_smem();
           tc_fence_after();
           const uint64_t off = (uint64_t)((stage * STAGE_BYTES) >> 4);
-          umma_kblock(d_tmem, adesc0 + off, bdesc0 + off, kb != 0 ? 1u : 0u, empty_addr[stage]);
+          umma_kblock(d_tmem, adesc0 + off, bdesc0 + off, idesc, kb != 0 ? 1u : 0u,
+                      empty_addr[stage]);
           any = true;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -317,9 +320,15 @@ __global__ void __launch_bounds__(GATHER ? NUM_THREADS_GATHER : NUM_THREADS, 1)
       const SegTile st = decode_tile(tile, sh->prefix, seg_end, E, M, BM, n_tiles, seg_stride);
       if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
       tc_fence_after();
-      drain_acc<MODE, ACT>(tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN),
-                           st.m0 + quad * 32, st.m_end, st.n_idx, st.e, bias, bias_up, N1, Nout, limit,
-                           alpha, beta, &tm_out, tma_out, out, obufs, obuf, lane);
+      const uint32_t tb = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN);
+      if (f16)
+        drain_acc<MODE, ACT, true>(tb, st.m0 + quad * 32, st.m_end, st.n_idx, st.e, bias, bias_up,
+                                   N1, Nout, limit, alpha, beta, &tm_out, tma_out, out, obufs,
+                                   obuf, lane);
+      else
+        drain_acc<MODE, ACT, false>(tb, st.m0 + quad * 32, st.m_end, st.n_idx, st.e, bias,
+                                    bias_up, N1, Nout, limit, alpha, beta, &tm_out, tma_out, out,
+                                    obufs, obuf, lane);
       tc_fence_before();
       mbar_arrive(&sh->tempty[acc]);
       if (++acc == 2) { acc = 0; aphase ^= 1u; }
@@ -344,7 +353,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s, const int32_t* gather_rows,
                            int gather_div, int gather_src_rows, int seg_stride,
-                           const SplitUp* split) {
+                           const SplitUp* split, bool f16) {
   if (M == 0 || N == 0) return cudaSuccess;
   // The two-SM (cta_group::2) kernel with MOE_TC_KERNEL=2sm.  Its SMs load a
   // third fewer bytes per MMA on 256-row pair tiles, but on the routed
@@ -356,7 +365,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     return v && v[0] == '2';
   }();
   const bool gather = gather_rows != nullptr;
-  if (two_sm && num_sms() >= 2 && !split)
+  if (two_sm && num_sms() >= 2 && !split && !f16)
     return launch_gemm_tc2(a, w, bias, seg_end, M, N, K, E, act, out, status, s, gather_rows,
                            gather_div, gather_src_rows, seg_stride);
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
@@ -378,25 +387,29 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)K * 2};
     cuuint32_t box[2] = {BK, BM};
-    if (!tmap::encode_bf16(&ma, a, 2, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tmap::encode_bf16(&ma, a, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, f16))
+      return cudaErrorInvalidValue;
   }
   if (split) {
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)E};
     cuuint64_t str[2] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2};
     cuuint32_t box[3] = {BK, BN / 2, 1};
-    if (!tmap::encode_bf16(&mb, w, 3, dims, str, box) ||
-        !tmap::encode_bf16(&mb_up, split->w_up, 3, dims, str, box))
+    if (!tmap::encode_bf16(&mb, w, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, f16) ||
+        !tmap::encode_bf16(&mb_up, split->w_up, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B,
+                           f16))
       return cudaErrorInvalidValue;
   } else if (mode == kTcStacked) {
     cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)N, 2, (cuuint64_t)E};
     cuuint64_t str[3] = {(cuuint64_t)K * 2, (cuuint64_t)N * K * 2, (cuuint64_t)2 * N * K * 2};
     cuuint32_t box[4] = {BK, BN / 2, 2, 1};  // 128 gate rows then 128 up rows
-    if (!tmap::encode_bf16(&mb, w, 4, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tmap::encode_bf16(&mb, w, 4, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, f16))
+      return cudaErrorInvalidValue;
   } else {
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N1, (cuuint64_t)E};
     cuuint64_t str[2] = {(cuuint64_t)K * 2, (cuuint64_t)N1 * K * 2};
     cuuint32_t box[3] = {BK, BN, 1};
-    if (!tmap::encode_bf16(&mb, w, 3, dims, str, box)) return cudaErrorInvalidValue;
+    if (!tmap::encode_bf16(&mb, w, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, f16))
+      return cudaErrorInvalidValue;
   }
   if (gather) ma = mb;  // unused by the kernel
   if (!split) mb_up = mb;  // unused
@@ -432,7 +445,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
     cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)N * 2};
     cuuint32_t box[2] = {OUT_BOX, OUT_BOX};
-    tma_out = tmap::encode_bf16(&mo, out, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
+    tma_out = tmap::encode_bf16(&mo, out, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B, f16) ? 1 : 0;
   }
   if (!tma_out) mo = mb;  // unused
   const auto* bias_p = static_cast<const __nv_bfloat16*>(bias);
@@ -453,7 +466,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
              bias_p, seg_end, M, N, N1, K, E, limit, alpha, beta, mo, tma_out, out_p, status,
              static_cast<const __nv_bfloat16*>(a), gather_rows, gather_div, gather_src_rows,
              seg_stride, mb_up, split ? 1 : 0,
-             split ? static_cast<const __nv_bfloat16*>(split->b_up) : nullptr);
+             split ? static_cast<const __nv_bfloat16*>(split->b_up) : nullptr, f16 ? 1 : 0);
   count_launch();
   return cudaGetLastError();
 }

@@ -80,8 +80,8 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 // ---- launchers (return cudaGetLastError() of their launches) ----
-cudaError_t launch_route(const float* logits, const float* bias, const int32_t* ids_in, int T,
-                         int E, const moe_route_params& p, float* w, int32_t* ids, float* probs,
+cudaError_t launch_route(const void* logits, const float* bias, const int32_t* ids_in, int T,
+                         int E, const moe_route_params& p, float* w, int32_t* ids, void* probs,
                          float* wscale, cudaStream_t s);
 
 // Router + permute index maps in one launch (bit-identical to launch_route
@@ -89,9 +89,9 @@ cudaError_t launch_route(const float* logits, const float* bias, const int32_t* 
 // E is within its limit (E <= 512).  Uses ws's permute scratch and three
 // ints of its status area (grid-barrier counters that reset themselves).
 bool route_permute_ok(int E);
-cudaError_t launch_route_permute(const float* logits, const float* bias, const int32_t* ids_in,
+cudaError_t launch_route_permute(const void* logits, const float* bias, const int32_t* ids_in,
                                  int T, int E, const moe_route_params& p, float* w, int32_t* ids,
-                                 float* probs, float* wscale, int32_t* seg_end,
+                                 void* probs, float* wscale, int32_t* seg_end,
                                  int32_t* row_to_route, int32_t* route_to_row, void* ws,
                                  cudaStream_t s);
 
@@ -147,7 +147,8 @@ cudaError_t launch_gemm_simt(const void* a, const void* w, const void* bias,
                              const moe_act_params* act, void* out, int* status, cudaStream_t s,
                              int seg_stride = 0, const SplitUp* split = nullptr);
 
-// tcgen05 grouped GEMM (bf16 operands, fp32 TMEM accumulators).  With
+// tcgen05 grouped GEMM (bf16 operands, or float16 with f16, fp32 TMEM
+// accumulators).  With
 // gather_rows, row r of A is row gather_rows[r] / gather_div of `a` (the
 // token-ordered hidden states, gather_src_rows rows, read through row_to_route
 // so the permuted copy is never materialised); only rows inside their expert's
@@ -156,7 +157,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s, const int32_t* gather_rows = nullptr,
                            int gather_div = 1, int gather_src_rows = 0, int seg_stride = 0,
-                           const SplitUp* split = nullptr);
+                           const SplitUp* split = nullptr, bool f16 = false);
 
 // block-scaled FP8 grouped GEMM over a masked slab (e4m3 operands, fp32
 // scales per row x 128 K of a and per 128 x 128 block of b, bf16 out)

@@ -13,6 +13,7 @@
 //   gather  : one warp per row copies the hidden row with 128-bit accesses
 #include <algorithm>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "permute_dev.cuh"
@@ -205,13 +206,14 @@ __device__ __forceinline__ void combine_item(const T* __restrict__ y, const floa
     for (int j = 0; j < 8; ++j) {
       const bool ok = row[j] >= 0 && row[j] < M;
       const T* src = y + (size_t)(ok ? row[j] : 0) * H + (size_t)v * VEC;
-      if constexpr (VEC == 8) {  // bf16 x 8 = 16 bytes
+      if constexpr (VEC == 8) {  // bf16 or f16 x 8 = 16 bytes
+        constexpr bool H16 = std::is_same<T, __half>::value;
         int4 q = ok ? __ldg(reinterpret_cast<const int4*>(src)) : make_int4(0, 0, 0, 0);
         const uint32_t u[4] = {(uint32_t)q.x, (uint32_t)q.y, (uint32_t)q.z, (uint32_t)q.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          acc[2 * i] = fmaf(wk[j], bf16_lo(u[i]), acc[2 * i]);
-          acc[2 * i + 1] = fmaf(wk[j], bf16_hi(u[i]), acc[2 * i + 1]);
+          acc[2 * i] = fmaf(wk[j], lo16<H16>(u[i]), acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wk[j], hi16<H16>(u[i]), acc[2 * i + 1]);
         }
       } else if constexpr (VEC == 4) {  // f32 x 4
         float4 q = ok ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0, 0, 0, 0);
@@ -229,11 +231,12 @@ __device__ __forceinline__ void combine_item(const T* __restrict__ y, const floa
   }
   T* dst = out + (size_t)t * H + (size_t)v * VEC;
   if constexpr (VEC == 8) {
+    constexpr bool H16 = std::is_same<T, __half>::value;
     int4 q;
-    q.x = (int)pack_bf16x2(scale * acc[0], scale * acc[1]);
-    q.y = (int)pack_bf16x2(scale * acc[2], scale * acc[3]);
-    q.z = (int)pack_bf16x2(scale * acc[4], scale * acc[5]);
-    q.w = (int)pack_bf16x2(scale * acc[6], scale * acc[7]);
+    q.x = (int)pack2<H16>(scale * acc[0], scale * acc[1]);
+    q.y = (int)pack2<H16>(scale * acc[2], scale * acc[3]);
+    q.z = (int)pack2<H16>(scale * acc[4], scale * acc[5]);
+    q.w = (int)pack2<H16>(scale * acc[6], scale * acc[7]);
     *reinterpret_cast<int4*>(dst) = q;
   } else if constexpr (VEC == 4) {
     *reinterpret_cast<float4*>(dst) =
@@ -482,14 +485,19 @@ cudaError_t launch_combine(const void* y, const float* w, const int32_t* r2r, in
     const long long cap = (long long)num_sms() * 8;
     return (unsigned)std::max<long long>(1, std::min<long long>(cap, (items + 255) / 256));
   };
-  if (dt == MOE_BF16) {
-    using B = __nv_bfloat16;
+  auto half_width = [&](auto tag) {
+    using B = decltype(tag);
     if (aligned && H % 8 == 0)
       launch_pdl(combine_kernel<B, 8>, grid_for(8), 256, 0, s, static_cast<const B*>(y), w, r2r, T,
           K, H, M, scale, static_cast<B*>(out), token_scale);
     else
       launch_pdl(combine_kernel<B, 1>, grid_for(1), 256, 0, s, static_cast<const B*>(y), w, r2r, T,
           K, H, M, scale, static_cast<B*>(out), token_scale);
+  };
+  if (dt == MOE_BF16) {
+    half_width(__nv_bfloat16{});
+  } else if (dt == MOE_F16) {
+    half_width(__half{});
   } else {
     if (aligned && H % 4 == 0)
       launch_pdl(combine_kernel<float, 4>, grid_for(4), 256, 0, s, static_cast<const float*>(y), w,

@@ -63,7 +63,7 @@ extern "C" moe_status moe_permute_noalloc(const void* hidden, moe_dtype dtype,
                                           void* expert_input, int32_t* seg_end,
                                           int32_t* row_to_route, int32_t* route_to_row,
                                           cudaStream_t stream) {
-  if (T < 0 || K < 1 || E < 1 || E > 12288 || (dtype != MOE_F32 && dtype != MOE_BF16))
+  if (T < 0 || K < 1 || E < 1 || E > 12288 || (dtype != MOE_F32 && dtype != MOE_BF16 && dtype != MOE_F16))
     return MOE_ERR_INVALID_ARG;
   if ((long long)T * K >= (1LL << 31)) return MOE_ERR_INVALID_ARG;
   if (expert_input && (!hidden || H < 1)) return MOE_ERR_INVALID_ARG;
@@ -71,7 +71,7 @@ extern "C" moe_status moe_permute_noalloc(const void* hidden, moe_dtype dtype,
     return MOE_ERR_INVALID_ARG;
   const int M = T * K;
   if (PermuteWs(M, E).total > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE;
-  const size_t esz = dtype == MOE_BF16 ? 2 : 4;
+  const size_t esz = dtype == MOE_F32 ? 4 : 2;
   const void* outs[4] = {expert_input, seg_end, row_to_route, route_to_row};
   const size_t out_n[4] = {expert_input ? (size_t)M * H * esz : 0, (size_t)E * 4, (size_t)M * 4,
                            (size_t)M * 4};

@@ -7,13 +7,13 @@ namespace {
 using rt::RouteArgs;
 
 template <int NPL>
-__global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ logits,
+__global__ void __launch_bounds__(256) route_kernel(const void* __restrict__ logits,
                                                     const float* __restrict__ bias,
                                                     const int32_t* __restrict__ ids_in, int T,
                                                     int E, RouteArgs a,
                                                     float* __restrict__ w_out,
                                                     int32_t* __restrict__ id_out,
-                                                    float* __restrict__ probs,
+                                                    void* __restrict__ probs,
                                                     float* __restrict__ wscale) {
   pdl_wait();  // everything below reads results of earlier launches
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -22,8 +22,8 @@ __global__ void __launch_bounds__(256) route_kernel(const float* __restrict__ lo
 }
 
 template <int NPL>
-cudaError_t launch_npl(const float* logits, const float* bias, const int32_t* ids_in, int T, int E,
-                       const RouteArgs& a, float* w, int32_t* ids, float* probs, float* wscale,
+cudaError_t launch_npl(const void* logits, const float* bias, const int32_t* ids_in, int T, int E,
+                       const RouteArgs& a, float* w, int32_t* ids, void* probs, float* wscale,
                        cudaStream_t s) {
   const int warps = 8;
   dim3 grid((T + warps - 1) / warps);
@@ -35,8 +35,8 @@ cudaError_t launch_npl(const float* logits, const float* bias, const int32_t* id
 
 }  // namespace
 
-cudaError_t launch_route(const float* logits, const float* bias, const int32_t* ids_in, int T,
-                         int E, const moe_route_params& p, float* w, int32_t* ids, float* probs,
+cudaError_t launch_route(const void* logits, const float* bias, const int32_t* ids_in, int T,
+                         int E, const moe_route_params& p, float* w, int32_t* ids, void* probs,
                          float* wscale, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   const RouteArgs a = rt::route_args(p, probs, wscale);

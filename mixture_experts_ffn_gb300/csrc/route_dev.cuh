@@ -16,6 +16,7 @@ namespace rt {
 struct RouteArgs {
   int K, scoring, renorm, G, TG, ls, lc;
   float rsf, route_scale;
+  int dt;  // moe_dtype of the logits and router_probs (the MoERouter type T)
 };
 
 // r[i] of a register array by a warp-uniform or per-lane index, without local memory
@@ -52,14 +53,27 @@ __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
 // Logits of token t in the calling lane's registers: z[i] = logit of expert
 // lane + 32 i (-inf past E).
 template <int NPL>
-__device__ __forceinline__ void load_logits(int t, const float* __restrict__ logits, int E,
+__device__ __forceinline__ void load_logits(int t, const void* __restrict__ logits, int E, int dt,
                                             float (&z)[NPL]) {
   const int lane = threadIdx.x & 31;
-  const float* row = logits + (size_t)t * E;
+  // scores are float32 whatever the logits' type (16-bit logits widen exactly)
+  if (dt == MOE_F32) {
+    const float* row = static_cast<const float*>(logits) + (size_t)t * E;
 #pragma unroll
-  for (int i = 0; i < NPL; ++i) {
-    const int e = lane + 32 * i;
-    z[i] = e < E ? __ldg(row + e) : -INFINITY;
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      z[i] = e < E ? __ldg(row + e) : -INFINITY;
+    }
+  } else {
+    const unsigned short* row = static_cast<const unsigned short*>(logits) + (size_t)t * E;
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+      const int e = lane + 32 * i;
+      const unsigned short u = e < E ? __ldg(row + e) : 0;
+      z[i] = e >= E            ? -INFINITY
+             : dt == MOE_F16 ? __half2float(__ushort_as_half(u))
+                             : __uint_as_float((uint32_t)u << 16);
+    }
   }
 }
 
@@ -72,7 +86,7 @@ __device__ __forceinline__ void route_loaded(int t, const float (&z)[NPL],
                                              const int32_t* __restrict__ ids_in, int E,
                                              const RouteArgs& a, float* __restrict__ w_out,
                                              int32_t* __restrict__ id_out,
-                                             float* __restrict__ probs,
+                                             void* __restrict__ probs,
                                              float* __restrict__ wscale) {
   const int lane = threadIdx.x & 31;
   const int K = a.K;
@@ -259,7 +273,15 @@ __device__ __forceinline__ void route_loaded(int t, const float (&z)[NPL],
       int e = lane + 32 * i;
       if (e >= a.ls && e < a.ls + a.lc && e < E) {
         float v = acc[i];
-        probs[(size_t)t * a.lc + (e - a.ls)] = v > 0.f ? logf(v) : -1e30f;
+        // the sentinel for an expert not chosen: -1e30, or -1e4 in float16,
+        // where -1e30 would overflow to -inf
+        const size_t o = (size_t)t * a.lc + (e - a.ls);
+        if (a.dt == MOE_F32)
+          static_cast<float*>(probs)[o] = v > 0.f ? logf(v) : -1e30f;
+        else if (a.dt == MOE_F16)
+          static_cast<__half*>(probs)[o] = __float2half_rn(v > 0.f ? logf(v) : -1e4f);
+        else
+          static_cast<__nv_bfloat16*>(probs)[o] = __float2bfloat16_rn(v > 0.f ? logf(v) : -1e30f);
         local += v;
       }
     }
@@ -270,21 +292,21 @@ __device__ __forceinline__ void route_loaded(int t, const float (&z)[NPL],
 
 // Route token t (the calling warp): load_logits then route_loaded.
 template <int NPL>
-__device__ __forceinline__ void route_token(int t, const float* __restrict__ logits,
+__device__ __forceinline__ void route_token(int t, const void* __restrict__ logits,
                                             const float* __restrict__ bias,
                                             const int32_t* __restrict__ ids_in, int E,
                                             const RouteArgs& a, float* __restrict__ w_out,
                                             int32_t* __restrict__ id_out,
-                                            float* __restrict__ probs,
+                                            void* __restrict__ probs,
                                             float* __restrict__ wscale) {
   float z[NPL];
-  load_logits<NPL>(t, logits, E, z);
+  load_logits<NPL>(t, logits, E, a.dt, z);
   route_loaded<NPL>(t, z, bias, ids_in, E, a, w_out, id_out, probs, wscale);
 }
 
 // RouteArgs from the C-ABI parameters (the MoERouter outputs are skipped when
 // either of their buffers is absent).
-inline RouteArgs route_args(const moe_route_params& p, const float* probs, const float* wscale) {
+inline RouteArgs route_args(const moe_route_params& p, const void* probs, const float* wscale) {
   RouteArgs a;
   a.K = p.top_k;
   a.scoring = p.scoring;
@@ -295,6 +317,7 @@ inline RouteArgs route_args(const moe_route_params& p, const float* probs, const
   a.lc = (probs && wscale) ? p.local_expert_count : 0;
   a.rsf = p.routed_scaling_factor;
   a.route_scale = p.route_scale;
+  a.dt = p.dtype;
   return a;
 }
 

@@ -97,9 +97,9 @@ __device__ __forceinline__ int column_sum(const int* __restrict__ counts, int E,
 
 template <int NPL>
 __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
-    const float* __restrict__ logits, const float* __restrict__ bias,
+    const void* __restrict__ logits, const float* __restrict__ bias,
     const int32_t* __restrict__ ids_in, int T, int E, RouteArgs a, float* __restrict__ w_out,
-    int32_t* __restrict__ id_out, float* __restrict__ probs, float* __restrict__ wscale,
+    int32_t* __restrict__ id_out, void* __restrict__ probs, float* __restrict__ wscale,
     int C, int* __restrict__ counts, int32_t* __restrict__ seg_end, int* __restrict__ active,
     int* __restrict__ num_active, int32_t* __restrict__ row_to_route,
     int32_t* __restrict__ route_to_row, int* status, int* bar) {
@@ -112,9 +112,9 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
     const int stride = gridDim.x * W;
     int t = blockIdx.x * W + warp;
     float z[NPL], zn[NPL];
-    if (t < T) rt::load_logits<NPL>(t, logits, E, z);
+    if (t < T) rt::load_logits<NPL>(t, logits, E, a.dt, z);
     for (; t < T; t += stride) {
-      if (t + stride < T) rt::load_logits<NPL>(t + stride, logits, E, zn);
+      if (t + stride < T) rt::load_logits<NPL>(t + stride, logits, E, a.dt, zn);
       rt::route_loaded<NPL>(t, z, bias, ids_in, E, a, w_out, id_out, probs, wscale);
 #pragma unroll
       for (int i = 0; i < NPL; ++i) z[i] = zn[i];
@@ -162,8 +162,8 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
 }
 
 template <int NPL>
-cudaError_t launch_npl(const float* logits, const float* bias, const int32_t* ids_in, int T,
-                       int E, const RouteArgs& a, float* w, int32_t* ids, float* probs,
+cudaError_t launch_npl(const void* logits, const float* bias, const int32_t* ids_in, int T,
+                       int E, const RouteArgs& a, float* w, int32_t* ids, void* probs,
                        float* wscale, int C, int* counts, int32_t* seg_end, int* active,
                        int* num_active, int32_t* r2r, int32_t* route_to_row, int* status, int* bar,
                        size_t smem, int grid, cudaStream_t s) {
@@ -209,9 +209,9 @@ cudaError_t launch_npl(const float* logits, const float* bias, const int32_t* id
 
 bool route_permute_ok(int E) { return E >= 1 && E <= kFusedWarps * 32; }
 
-cudaError_t launch_route_permute(const float* logits, const float* bias, const int32_t* ids_in,
+cudaError_t launch_route_permute(const void* logits, const float* bias, const int32_t* ids_in,
                                  int T, int E, const moe_route_params& p, float* w, int32_t* ids,
-                                 float* probs, float* wscale, int32_t* seg_end,
+                                 void* probs, float* wscale, int32_t* seg_end,
                                  int32_t* row_to_route, int32_t* route_to_row, void* ws,
                                  cudaStream_t s) {
   const int K = p.top_k;

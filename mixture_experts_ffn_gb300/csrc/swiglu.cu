@@ -49,6 +49,10 @@ cudaError_t launch_swiglu(const void* gate, const void* up, int64_t R, int I, mo
     using B = __nv_bfloat16;
     launch_pdl(swiglu_kernel<B>, (unsigned)blocks, 256, 0, s, static_cast<const B*>(gate),
         static_cast<const B*>(up), R, I, fusion, limit, alpha, beta, static_cast<B*>(out));
+  } else if (dt == MOE_F16) {
+    using B = __half;
+    launch_pdl(swiglu_kernel<B>, (unsigned)blocks, 256, 0, s, static_cast<const B*>(gate),
+        static_cast<const B*>(up), R, I, fusion, limit, alpha, beta, static_cast<B*>(out));
   } else {
     launch_pdl(swiglu_kernel<float>, (unsigned)blocks, 256, 0, s, static_cast<const float*>(gate),
         static_cast<const float*>(up), R, I, fusion, limit, alpha, beta, static_cast<float*>(out));

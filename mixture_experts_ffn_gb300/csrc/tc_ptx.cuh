@@ -155,23 +155,30 @@ __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// store 32 bf16 values (64 bytes) of one row; vector path when all columns valid
+// store 32 bf16 (F16: float16) values (64 bytes) of one row; vector path when
+// all columns are valid
+template <bool F16 = false>
 __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)[32], int n_valid) {
   if (n_valid >= 32) {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       uint4 u;
-      u.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
-      u.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
-      u.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
-      u.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+      u.x = pack2<F16>(v[8 * q + 0], v[8 * q + 1]);
+      u.y = pack2<F16>(v[8 * q + 2], v[8 * q + 3]);
+      u.z = pack2<F16>(v[8 * q + 4], v[8 * q + 5]);
+      u.w = pack2<F16>(v[8 * q + 6], v[8 * q + 7]);
       d4[q] = u;
     }
   } else {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (i < n_valid) dst[i] = __float2bfloat16_rn(v[i]);
+      if (i < n_valid) {
+        if constexpr (F16)
+          reinterpret_cast<__half*>(dst)[i] = __float2half_rn(v[i]);
+        else
+          dst[i] = __float2bfloat16_rn(v[i]);
+      }
   }
 }
 
@@ -179,6 +186,18 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const float (&v)
 constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
+}
+// The same with A and B float16 (format code 0 in both fields).
+constexpr uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// One 16-bit operand-dtype element (bias) as float.
+template <bool F16>
+__device__ __forceinline__ float ld16(const __nv_bfloat16* p) {
+  if constexpr (F16)
+    return __half2float(*reinterpret_cast<const __half*>(p));
+  else
+    return __bfloat162float(*p);
 }
 
 }  // namespace tc

@@ -32,14 +32,17 @@ inline EncodeFn get_encode() {
 
 // rank-D bf16 map: dims[0] is the contiguous dimension; strides in bytes for
 // dims 1..D-1; box in elements.  The swizzle defaults to 128 bytes (operand
-// tiles read by tcgen05.mma); output staging uses 64 bytes.
+// tiles read by tcgen05.mma); output staging uses 64 bytes.  f16: the
+// elements are float16 (same 2-byte layout; only the type recorded differs).
 inline bool encode_bf16(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
                         const cuuint64_t* strides, const cuuint32_t* box,
-                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+                        bool f16 = false) {
   EncodeFn fn = get_encode();
   if (!fn) return false;
   cuuint32_t es[5] = {1, 1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims,
+  return fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+            (cuuint32_t)rank, const_cast<void*>(ptr), dims,
             strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

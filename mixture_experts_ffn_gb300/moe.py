@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_OVERLAP, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, \
     MOE_ERR_TIMEOUT, MOE_ERR_DEVICE, MOE_ERR_WORKSPACE = range(8)
-MOE_F32, MOE_BF16 = 0, 1
+MOE_F32, MOE_BF16, MOE_F16 = 0, 1, 2
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID, MOE_SCORING_SQRT_SOFTPLUS = 0, 1, 2
 MOE_ACT_SILU_AND_MUL, MOE_ACT_SWIGLU, MOE_ACT_IDENTITY, MOE_ACT_GELU_AND_MUL = 0, 1, 2, 3
 MOE_ACT_RELU, MOE_ACT_GELU, MOE_ACT_SILU = 4, 5, 6
@@ -36,7 +36,7 @@ class RouteParams(ctypes.Structure):
                 ("renormalize", ctypes.c_int32), ("num_expert_group", ctypes.c_int32),
                 ("topk_group", ctypes.c_int32), ("routed_scaling_factor", ctypes.c_float),
                 ("local_expert_start", ctypes.c_int32), ("local_expert_count", ctypes.c_int32),
-                ("route_scale", ctypes.c_float)]
+                ("route_scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
 
 
 class ActParams(ctypes.Structure):
@@ -70,8 +70,8 @@ _SIGNATURES = {
     "moe_ffn_forward_host": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
                              _vp, _vp, _vp, _sz, _vp],
     "moe_shared_expert_mlp": [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
-    "moe_ffn_forward_local": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
-                              _vp, _vp, _sz, _vp],
+    "moe_ffn_forward_local": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
+                              _vp, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_fp8_masked": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
     "moe_shared_expert_workspace_size": [_i, _i, _i, _i],
     "moe_ffn_forward_shared": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
@@ -136,6 +136,8 @@ def _dt(t: torch.Tensor) -> int:
         return MOE_BF16
     if t.dtype == torch.float32:
         return MOE_F32
+    if t.dtype == torch.float16:
+        return MOE_F16
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
@@ -162,7 +164,16 @@ def route_params(top_k, scoring="softmax", renormalize=True, num_expert_group=1,
     sc = {"softmax": MOE_SCORING_SOFTMAX, "sigmoid": MOE_SCORING_SIGMOID,
           "sqrt_softplus": MOE_SCORING_SQRT_SOFTPLUS}.get(scoring, scoring)
     return RouteParams(top_k, sc, int(bool(renormalize)), num_expert_group, topk_group,
-                       routed_scaling_factor, local_expert_start, local_expert_count, route_scale)
+                       routed_scaling_factor, local_expert_start, local_expert_count, route_scale,
+                       MOE_F32)
+
+
+def _rp(p: RouteParams, logits) -> RouteParams:
+    """A copy of p whose MoERouter type T (logits and router_probs) is the
+    logits tensor's dtype."""
+    q = RouteParams.from_buffer_copy(p)
+    q.dtype = _dt(logits)
+    return q
 
 
 def act_params(kind=MOE_ACT_SILU_AND_MUL, swiglu_fusion=2, limit=0.0, alpha=1.0,
@@ -192,11 +203,11 @@ def moe_route(logits, p: RouteParams, correction_bias=None, expert_ids=None, top
         topk_ids = torch.empty((T, p.top_k), dtype=torch.int32, device=dev)
     if p.local_expert_count > 0:
         if router_probs is None:
-            router_probs = torch.empty((T, p.local_expert_count), dtype=torch.float32, device=dev)
+            router_probs = torch.empty((T, p.local_expert_count), dtype=logits.dtype, device=dev)
         if weight_scale is None:
             weight_scale = torch.empty((T,), dtype=torch.float32, device=dev)
     _check("moe_route", lib.moe_route(_p(logits), _p(correction_bias), _p(expert_ids), T, E,
-                                      ctypes.byref(p), _p(topk_weights), _p(topk_ids),
+                                      ctypes.byref(_rp(p, logits)), _p(topk_weights), _p(topk_ids),
                                       _p(router_probs), _p(weight_scale), _stream()))
     return topk_weights, topk_ids, router_probs, weight_scale
 
@@ -295,7 +306,7 @@ def moe_route_permute(logits, p: RouteParams, correction_bias=None, expert_ids=N
     ti = torch.empty((T, K), dtype=torch.int32, device=dev)
     probs = wsc = None
     if p.local_expert_count > 0:
-        probs = torch.empty((T, p.local_expert_count), dtype=torch.float32, device=dev)
+        probs = torch.empty((T, p.local_expert_count), dtype=logits.dtype, device=dev)
         wsc = torch.empty((T,), dtype=torch.float32, device=dev)
     seg_end = torch.empty((E,), dtype=torch.int32, device=dev)
     r2r = torch.empty((T * K,), dtype=torch.int32, device=dev)
@@ -304,7 +315,8 @@ def moe_route_permute(logits, p: RouteParams, correction_bias=None, expert_ids=N
         ws = _ws(lib.moe_permute_workspace_size(T * K, E), dev)
     _check("moe_route_permute",
            lib.moe_route_permute(_p(logits), _p(correction_bias), _p(expert_ids), T, E,
-                                 ctypes.byref(p), _p(tw), _p(ti), _p(probs), _p(wsc), _p(seg_end),
+                                 ctypes.byref(_rp(p, logits)), _p(tw), _p(ti), _p(probs), _p(wsc),
+                                 _p(seg_end),
                                  _p(r2r), _p(route_to_row), _p(ws), ws.numel(), _stream()))
     return tw, ti, probs, wsc, {"seg_end": seg_end, "row_to_route": r2r,
                                 "route_to_row": route_to_row, "ws": ws}
@@ -441,7 +453,8 @@ def moe_ffn_forward(hidden, logits, w_gate_up, w_down, p: RouteParams, act: ActP
     _check("moe_ffn_forward",
            lib.moe_ffn_forward(_p(hidden), _p(logits), _p(w_gate_up), _p(w_down),
                                _p(correction_bias), _p(expert_ids), _p(b_gate_up), _p(b_down), T,
-                               H, F, E, _dt(hidden), ctypes.byref(p), ctypes.byref(act), _p(out),
+                               H, F, E, _dt(hidden), ctypes.byref(_rp(p, logits)),
+                               ctypes.byref(act), _p(out),
                                _p(topk_weights_out), _p(topk_ids_out), _p(router_probs),
                                _p(weight_scale), _p(ws), ws.numel(), _stream()))
     return out
@@ -465,7 +478,8 @@ def moe_ffn_forward_split(hidden, logits, w_gate, w_up, w_down, p: RouteParams, 
     _check("moe_ffn_forward_split",
            lib.moe_ffn_forward_split(_p(hidden), _p(logits), _p(w_gate), _p(w_up), _p(w_down),
                                      _p(correction_bias), _p(expert_ids), _p(b_gate), _p(b_up),
-                                     _p(b_down), T, H, F, E, _dt(hidden), ctypes.byref(p),
+                                     _p(b_down), T, H, F, E, _dt(hidden),
+                                     ctypes.byref(_rp(p, logits)),
                                      ctypes.byref(act), _p(out), _p(topk_weights_out),
                                      _p(topk_ids_out), _p(router_probs), _p(weight_scale),
                                      _p(ws), ws.numel(), _stream()))
@@ -538,7 +552,8 @@ def moe_ffn_forward_shared(hidden, logits, w_gate_up, w_down, p: RouteParams, ac
            lib.moe_ffn_forward_shared(_p(hidden), _p(logits), _p(w_gate_up), _p(w_down),
                                       _p(correction_bias), _p(shared_w_gate_up),
                                       _p(shared_w_down), T, H, F, S, E, _dt(hidden),
-                                      ctypes.byref(p), ctypes.byref(act), _p(routed_out),
+                                      ctypes.byref(_rp(p, logits)), ctypes.byref(act),
+                                      _p(routed_out),
                                       _p(shared_out if shared_w_gate_up is not None else None),
                                       _p(ws), ws.numel(), _stream()))
     return (shared_out if shared_w_gate_up is not None else None), routed_out
@@ -559,7 +574,8 @@ def moe_ffn_forward_local(hidden, router_probs, weight_scale, w_gate_up, w_down,
     _check("moe_ffn_forward_local",
            lib.moe_ffn_forward_local(_p(hidden), _p(router_probs), _p(weight_scale),
                                      _p(w_gate_up), _p(w_down), _p(b_gate_up), _p(b_down), T, H,
-                                     F, lc, K, _dt(hidden), ctypes.byref(act), _p(out), _p(ws),
+                                     F, lc, K, _dt(hidden), _dt(router_probs), ctypes.byref(act),
+                                     _p(out), _p(ws),
                                      ws.numel(), _stream()))
     return out
 
@@ -583,7 +599,8 @@ def moe_ffn_forward_host(hidden_host, logits_host, w_gate_up, w_down, p: RoutePa
     _check("moe_ffn_forward_host",
            lib.moe_ffn_forward_host(_p(hidden_host), _p(logits_host), _p(w_gate_up), _p(w_down),
                                     _p(correction_bias), _p(expert_ids), _p(b_gate_up),
-                                    _p(b_down), T, H, F, E, _dt(hidden_host), ctypes.byref(p),
+                                    _p(b_down), T, H, F, E, _dt(hidden_host),
+                                    ctypes.byref(_rp(p, logits_host)),
                                     ctypes.byref(act), _p(out_host), _p(ws), ws.numel(),
                                     _stream()))
     return out_host

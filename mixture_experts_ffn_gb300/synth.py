@@ -54,7 +54,7 @@ class MoEConfig:
     F: int
     E: int
     K: int
-    dtype: str = "bf16"  # "bf16" or "f32"
+    dtype: str = "bf16"  # "bf16", "f16" or "f32"
     scoring: str = "softmax"  # "softmax" or "sigmoid"
     renormalize: bool = True
     G: int = 1  # num_expert_group
@@ -106,7 +106,7 @@ CONFIGS = {
 
 
 def torch_dtype(name: str) -> torch.dtype:
-    return {"bf16": torch.bfloat16, "f32": torch.float32}[name]
+    return {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[name]
 
 
 def _gen(cfg: MoEConfig, tid: int, device, salt: int = 0) -> torch.Generator:

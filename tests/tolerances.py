@@ -14,6 +14,11 @@ RMS(err) <= 2e-3 * RMS(ref).  ``bf16_report`` returns the raw figures too.
 (The tensor cores' fp32 accumulation differs from a sequential fp32 sum, so
 the GPU sees more such one-ulp flips than a CPU fp32 emulation: at the full
 Qwen3-style size about 1.6e-5 of the elements.)
+
+f16 outputs: no bound is stated for float16; the bf16 bounds are scaled by
+the ratio of the two formats' unit roundoffs (2^-11 / 2^-8 = 1/8):
+|err| <= 2.5e-3 * RMS(ref) + 2 ulp_f16(ref) per element, at most 1e-4 of
+the elements above 2.5e-3 * RMS(ref), RMS(err) <= 2.5e-4 * RMS(ref).
 """
 import numpy as np
 
@@ -23,6 +28,41 @@ def ulp_bf16(x):
     a = np.abs(np.asarray(x, dtype=np.float64))
     a = np.maximum(a, 2.0 ** -126)
     return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 7)
+
+
+def ulp_f16(x):
+    """Spacing of IEEE binary16 numbers at |x| (11 significant bits; 2^-24
+    below the smallest normal 2^-14)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    a = np.maximum(a, 2.0 ** -14)
+    return np.ldexp(1.0, np.floor(np.log2(a)).astype(np.int64) - 10)
+
+
+def f16_report(got, ref) -> dict:
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    err = np.abs(got - ref)
+    rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    bound = 2.5e-3 * rms
+    return {
+        "n": int(ref.size),
+        "rms_ref": rms,
+        "max_err_over_rms": float(err.max() / rms) if ref.size and rms > 0 else 0.0,
+        "rms_err_over_rms": float(np.sqrt(np.mean(err ** 2)) / rms) if ref.size and rms > 0 else 0.0,
+        "n_above_bound": int((err > bound).sum()),
+        "n_above_bound_plus_2ulp": int((err > bound + 2 * ulp_f16(ref)).sum()),
+    }
+
+
+def assert_f16_close(got, ref, what=""):
+    r = f16_report(got, ref)
+    if r["n"] == 0:
+        return r
+    allowed = max(2, int(1e-4 * r["n"]))
+    assert r["n_above_bound_plus_2ulp"] == 0, (what, r)
+    assert r["n_above_bound"] <= allowed, (what, r)
+    assert r["rms_err_over_rms"] <= 2.5e-4, (what, r)
+    return r
 
 
 def bf16_report(got, ref) -> dict:
@@ -65,12 +105,14 @@ def assert_f32_close(got, ref, what=""):
 def assert_close(got, ref, dtype, what=""):
     if dtype == "f32":
         return assert_f32_close(got, ref, what)
+    if dtype == "f16":
+        return assert_f16_close(got, ref, what)
     return assert_bf16_close(got, ref, what)
 
 
 def assert_rounded_once(got, exact, dtype, what=""):
     """For a stage whose only rounding is its final cast: ``got`` must lie within
-    one unit in the last place of the unrounded oracle value ``exact`` (bf16),
+    one unit in the last place of the unrounded oracle value ``exact`` (bf16, f16),
     plus 1e-5 * RMS(exact) for sums that cancel to near zero; fp32 outputs use
     the fp32 bound."""
     got = np.asarray(got, dtype=np.float64)
@@ -81,6 +123,6 @@ def assert_rounded_once(got, exact, dtype, what=""):
         return assert_f32_close(got, exact, what)
     rms = float(np.sqrt(np.mean(exact ** 2)))
     err = np.abs(got - exact)
-    lim = ulp_bf16(exact) + 1e-5 * rms
+    lim = (ulp_f16(exact) if dtype == "f16" else ulp_bf16(exact)) + 1e-5 * rms
     bad = err > lim
     assert not bad.any(), (what, int(bad.sum()), float((err / lim).max()))
