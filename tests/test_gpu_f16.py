@@ -102,7 +102,7 @@ def test_combine_and_swiglu_f16(moe):
         y = torch.randn((T * K, h), generator=g).half()
         w = torch.rand((T, K), generator=g)
         r2r = torch.randperm(T * K, generator=g).to(torch.int32)
-        out = moe.moe_combine(y.cuda(), w.cuda(), r2r.cuda(), K, scale=1.5)
+        out = moe.moe_combine(y.cuda(), w.cuda(), r2r.cuda(), scale=1.5)
         exact = O.combine(np_(y), np_(w), np_(r2r), T, K, 1.5, dtype=None)
         assert_rounded_once(np_(out), exact, "f16", f"combine f16 H={h}")
     gate = torch.randn((33, 2 * 48), generator=g).half()
