@@ -269,7 +269,7 @@ def stage_cost(cfg, D):
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
     M = T * K
     lc = cfg.local_count
-    b = 2 if cfg.dtype == "bf16" else 4
+    b = 4 if cfg.dtype == "f32" else 2
     bias1 = D * 2 * F * b if cfg.bias_std is not None else 0
     bias2 = D * H * b if cfg.bias_std is not None else 0
     route = T * E * 4 + M * 8 + T * lc * 4 + (T * 4 if lc else 0)
@@ -322,10 +322,10 @@ def run_ours(args, rank, world, local):
                and cfg.F % 256 == 0)
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
     # the forward reads the gate_up rows through the permutation on the
-    # tensor-core path (bf16, 16-byte rows)
-    gathered = not indexed and cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
+    # tensor-core path (bf16 or f16, 16-byte rows)
+    gathered = not indexed and cfg.dtype != "f32" and H % 8 == 0 and F % 8 == 0
     tdt = synth.torch_dtype(cfg.dtype)
-    mdt = moe.MOE_BF16 if cfg.dtype == "bf16" else moe.MOE_F32
+    mdt = {"bf16": moe.MOE_BF16, "f16": moe.MOE_F16, "f32": moe.MOE_F32}[cfg.dtype]
     out = torch.empty((T, H), dtype=tdt, device=dev)
     tw = torch.empty((T, K), dtype=torch.float32, device=dev)
     ti = torch.empty((T, K), dtype=torch.int32, device=dev)
@@ -478,8 +478,8 @@ def run_ours(args, rank, world, local):
             traffic = None
         else:
             dom = max(("gemm_act", "gemm_down"), key=lambda k: breakdown[k]["us"])
-            # bf16 with 16-byte rows runs the tcgen05 kernel, anything else the SIMT one
-            tc = cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
+            # bf16 / f16 with 16-byte rows runs the tcgen05 kernel, anything else the SIMT one
+            tc = cfg.dtype != "f32" and H % 8 == 0 and F % 8 == 0
             kname = f"{'gemm_tc_kernel' if tc else 'gemm_simt_kernel'} ({dom})"
             traffic = profile_traffic("gemm_tc_kernel", GEMM_SOURCES) if tc and (
                 dom == "gemm_act" and args.workload == WORKLOAD) else None
@@ -515,7 +515,7 @@ def run_ours(args, rank, world, local):
         dist.barrier()
     et, _ = timed(fwd_host, args.steps, args.warmup)
     e_ms = reduce_max(sum(et) / len(et))
-    eb = 2 if cfg.dtype == "bf16" else 4
+    eb = 4 if cfg.dtype == "f32" else 2
     e2e = {"value": job_throughput(T, world, e_ms), "unit": "tokens/s",
            # bytes of the whole job (every rank copies its own inputs and result)
            "h2d_bytes_per_step": world * (T * H * eb + T * E * 4),
@@ -559,7 +559,7 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
 
     T, H, F, E, K = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K
     dev = inp["hidden"].device
-    gathered = cfg.dtype == "bf16" and H % 8 == 0 and F % 8 == 0
+    gathered = cfg.dtype != "f32" and H % 8 == 0 and F % 8 == 0
     p = moe.config_params(cfg.replace(local_count=0))[0]
     tw, ti, _, _ = moe.moe_route(inp["logits"], p, inp["correction_bias"], inp["expert_ids"])
     perm = moe.moe_permute(ti, E, inp["hidden"])
@@ -597,10 +597,10 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
         sw = synth.make_shared_expert(cfg, S, dev)
         sh_out = torch.empty_like(inp["hidden"])
         sh_ws = moe._ws(moe.moe_shared_expert_workspace_size(
-            T, H, S, moe.MOE_BF16 if cfg.dtype == "bf16" else moe.MOE_F32), dev)
+            T, H, S, {"bf16": moe.MOE_BF16, "f16": moe.MOE_F16, "f32": moe.MOE_F32}[cfg.dtype]), dev)
         fns["shared_mlp"] = lambda: moe.moe_shared_expert_mlp(
             inp["hidden"], sw["shared_w_gate_up"], sw["shared_w_down"], out=sh_out, ws=sh_ws)
-        b = 2 if cfg.dtype == "bf16" else 4
+        b = 4 if cfg.dtype == "f32" else 2
         extra = {"S": S, "flops": 6.0 * T * H * S,
                  "bytes": 3 * S * H * b + 2 * T * H * b + 2 * T * S * b}
     if args.stage == "fp8_gemm":
