@@ -205,7 +205,8 @@ def workload_config(args, cfg, world, **extra):
 
     c = {"workload": args.workload, "T": cfg.T, "H": cfg.H, "F": cfg.F, "E": cfg.E, "K": cfg.K,
          "scoring": cfg.scoring, "renormalize": cfg.renormalize, "groups": [cfg.G, cfg.TG],
-         "rsf": cfg.rsf, "act": ["silu_and_mul", "swiglu", "identity"][cfg.act],
+         "rsf": cfg.rsf, "act": ["silu_and_mul", "swiglu", "identity", "gelu_and_mul", "relu", "gelu",
+                                                     "silu"][cfg.act],
          "moerouter_slice": [cfg.local_start, cfg.local_count],
          "parallelism": f"replicas x{world}"}
     c.update(extra)
