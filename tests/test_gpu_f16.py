@@ -176,3 +176,17 @@ def test_local_forward_f16_router_probs(moe):
     ref = O.ffn_forward_local(np_(inp["hidden"]), r["router_probs"], np_(wsc), np_(w1), np_(w2),
                               cfg.K, cfg.F, dtype="f16")
     assert_close(np_(out), ref, "f16", "local forward f16")
+
+
+def test_shared_expert_f16(moe):
+    """The shared expert's dense gated MLP in float16 (one segment of T rows
+    through the same tcgen05 GEMMs)."""
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=384, dtype="f16")
+    hidden = synth.make_inputs(cfg, "cpu")["hidden"]
+    sw = synth.make_shared_expert(cfg, 512)
+    out = moe.moe_shared_expert_mlp(hidden.cuda(), sw["shared_w_gate_up"].cuda(),
+                                    sw["shared_w_down"].cuda())
+    assert out.dtype == torch.float16
+    ref = O.shared_expert_mlp(np_(hidden), np_(sw["shared_w_gate_up"]), np_(sw["shared_w_down"]),
+                              dtype="f16")
+    assert_close(np_(out), ref, "f16", "shared expert f16")
