@@ -182,7 +182,7 @@ def test_shared_expert_f16(moe):
     """The shared expert's dense gated MLP in float16 (one segment of T rows
     through the same tcgen05 GEMMs)."""
     cfg = synth.CONFIGS["qwen3_bf16"].replace(T=384, dtype="f16")
-    hidden = synth.make_inputs(cfg, "cpu")["hidden"]
+    hidden = torch.randn((cfg.T, cfg.H), generator=torch.Generator().manual_seed(4)).half()
     sw = synth.make_shared_expert(cfg, 512)
     out = moe.moe_shared_expert_mlp(hidden.cuda(), sw["shared_w_gate_up"].cuda(),
                                     sw["shared_w_down"].cuda())
