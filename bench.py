@@ -604,6 +604,39 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
         b = 4 if cfg.dtype == "f32" else 2
         extra = {"S": S, "flops": 6.0 * T * H * S,
                  "bytes": 3 * S * H * b + 2 * T * H * b + 2 * T * S * b}
+    if args.stage == "gemm_act_split":
+        extra = {}
+        # the gated gate_up GEMM with the gate and up projections in two
+        # tensors (SwiGLU fusion 0), on the permuted copy of the activations
+        wg = inp["w_gate_up"][:, :F].contiguous()
+        wu = inp["w_gate_up"][:, F:].contiguous()
+        bg = bu = None
+        if inp["b_gate_up"] is not None:
+            bg = inp["b_gate_up"][:, :F].contiguous()
+            bu = inp["b_gate_up"][:, F:].contiguous()
+        a0 = moe.act_params(a.kind, 0 if a.kind == synth.ACT_SWIGLU else a.swiglu_fusion,
+                            a.limit, a.alpha, a.beta)
+        fns["gemm_act_split"] = lambda: moe.moe_grouped_gemm_act_split(
+            perm["expert_input"], wg, wu, perm["seg_end"], a0, bg, bu, out=act_out)
+        # and the whole forward with the split weights (same workspace sizes)
+        f_out = torch.empty_like(inp["hidden"])
+        f_ws = moe._ws(moe.moe_workspace_size(T, H, F, E, K, {"bf16": moe.MOE_BF16,
+                       "f16": moe.MOE_F16, "f32": moe.MOE_F32}[cfg.dtype]), dev)
+        split_fwd = lambda: moe.moe_ffn_forward_split(  # noqa: E731
+            inp["hidden"], inp["logits"], wg, wu, inp["w_down"], p, a0, inp["correction_bias"],
+            inp["expert_ids"], bg, bu, inp["b_down"], out=f_out, ws=f_ws)
+        fwd = lambda: moe.moe_ffn_forward(  # noqa: E731
+            inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a,
+            inp["correction_bias"], inp["expert_ids"], inp["b_gate_up"], inp["b_down"],
+            out=f_out, ws=f_ws)
+        extra["forward_split_us"] = [round(1e3 * x, 2) for x in timed(split_fwd, args.steps,
+                                                                       args.warmup)[0]]
+        extra["forward_stacked_us"] = [round(1e3 * x, 2) for x in timed(fwd, args.steps,
+                                                                         args.warmup)[0]]
+        b = 4 if cfg.dtype == "f32" else 2
+        M = T * K
+        extra.update({"flops": 2.0 * M * 2 * F * H,
+                      "bytes": E * 2 * F * H * b + M * H * b + M * F * b})
     if args.stage == "fp8_gemm":
         # block-scaled FP8 masked grouped GEMM, DeepSeek-V3-style expert-parallel
         # shapes: 8 local experts of up to 256 rows, N 4096 (2F), K 7168 (H)
@@ -683,7 +716,8 @@ def main():
                          "reduced cases only; the bench line of record uses none)")
     ap.add_argument("--stage", default=None,
                     choices=["route", "route_permute", "permute", "gemm_act", "gemm_down",
-                             "combine", "indexed_mlp", "shared_mlp", "fp8_gemm"],
+                             "combine", "indexed_mlp", "shared_mlp", "fp8_gemm",
+                             "gemm_act_split"],
                     help="time one stage alone (for profiler captures)")
     ap.add_argument("--shared-s", type=int, default=2048,
                     help="intermediate size of the shared expert timed by --stage shared_mlp "
