@@ -149,14 +149,15 @@ typedef struct moe_act_params {
  * MoERouter outputs (when local_expert_count > 0): with w^_k = s[id_k] /
  * sum_j s[id_j] (always normalised, no rsf), router_probs[t, j] =
  * log(sum of w^_k over routes on expert local_expert_start + j) if chosen,
- * else -1e30; weight_scale[t] = route_scale * sum of w^ over local routes
- * (0 when no chosen expert is local).
+ * else -1e30 (-1e4 when p->dtype is MOE_F16: -1e30 overflows float16);
+ * weight_scale[t] = route_scale * sum of w^ over local routes (0 when no
+ * chosen expert is local).
  *
- *   logits          [T, E] f32
+ *   logits          [T, E] p->dtype (f32, bf16 or f16; scores in f32)
  *   correction_bias [E] f32 or NULL; not with MOE_SCORING_SOFTMAX
  *   expert_ids      [T, K] i32 or NULL (hash routing)
  *   topk_weights    [T, K] f32 out;  topk_ids [T, K] i32 out
- *   router_probs    [T, local_expert_count] f32 out or NULL
+ *   router_probs    [T, local_expert_count] p->dtype out or NULL
  *   weight_scale    [T] f32 out or NULL (both or neither when count > 0)
  * E <= 1024.  T == 0 is a no-op. */
 moe_status moe_route(const void* logits, const float* correction_bias,
@@ -407,7 +408,7 @@ moe_status moe_indexed_mlp(const void* hidden, const void* w_gate_up, const void
  * are the same as the staged calls'.  Every launch is made with programmatic dependent launch, so each
  * overlaps the tail of the previous one.
  *
- *   hidden [T, H] dtype;  logits [T, E] f32;  w_gate_up [E, N1, H];
+ *   hidden [T, H] dtype;  logits [T, E] p->dtype;  w_gate_up [E, N1, H];
  *   w_down [E, H, F];  correction_bias [E] f32 | NULL;  expert_ids [T, K] | NULL;
  *   b_gate_up [E, N1] | NULL;  b_down [E, H] | NULL;  out [T, H] dtype;
  *   topk_weights_out [T, K] f32 | NULL, topk_ids_out [T, K] i32 | NULL
