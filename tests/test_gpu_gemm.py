@@ -98,6 +98,28 @@ def test_gemm_act(moe, counts, Hk, F, act, bias, dtype, simt):
     assert_rounded_once(got[:M], exact, dtype, f"gemm_act {act}")
 
 
+@pytest.mark.parametrize("simt", [False, True])
+def test_gemm_act_largest_expert_count(moe, simt):
+    """E = 1024 (the largest accepted): mostly empty or one-row segments, a few
+    longer ones, so the shared tile builder's scan runs over every expert."""
+    rng = np.random.default_rng(1024)
+    counts = rng.choice([0, 0, 1, 2, 5, 130], size=1024).tolist()
+    a, w, b, seg_end = _problem(counts, 64, 128, "bf16", True, seed=1024)
+    M, F = a.shape[0], 64
+    out = torch.full((M, F), float("nan"), dtype=a.dtype, device="cuda")
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    old = moe.moe_set_gemm_simt(simt)
+    try:
+        moe.moe_grouped_gemm_act(a.cuda(), w.cuda(), seg_end.cuda(), F, moe.act_params(kind=0),
+                                 b.cuda(), out=out, ws=ws)
+        assert moe.moe_sync_status(ws) == moe.MOE_OK
+    finally:
+        moe.moe_set_gemm_simt(old)
+    exact = O.grouped_gemm_act(np_(a), np_(w), np_(seg_end), F, 0, 2, 0.0, 1.0, 0.0, np_(b),
+                               dtype=None)
+    assert_rounded_once(np_(out), exact, "bf16", "gemm_act E=1024")
+
+
 @pytest.mark.parametrize("counts,F,H,bias,dtype,simt", [
     ([3, 0, 130, 1, 300], 192, 320, True, "bf16", False),
     ([257, 0, 31], 128, 256, False, "bf16", False),

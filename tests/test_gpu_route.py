@@ -99,6 +99,38 @@ def test_route_ties_and_edges(moe):
         np.testing.assert_allclose(w, r["topk_weights"], rtol=1e-5)
 
 
+@pytest.mark.parametrize("E,K,G,TG,scoring", [
+    (1024, 64, 32, 32, "sigmoid"),   # the largest E, K and G accepted
+    (1024, 64, 32, 8, "sigmoid"),    # group pruning at the largest G
+    (1024, 8, 1, 1, "softmax"),
+    (64, 64, 1, 1, "softmax"),       # K = E = 64
+])
+def test_route_maximum_sizes(moe, E, K, G, TG, scoring):
+    cfg = synth.MoEConfig("max", 11, T=300, H=8, F=8, E=E, K=K, scoring=scoring, G=G, TG=TG,
+                          rsf=2.5, cbias_std=0.1 if scoring == "sigmoid" else None,
+                          local_start=E - 96, local_count=96)
+    inp, ref = make(cfg)
+    (w, ids, probs, wsc), r = _route_both(moe, cfg, inp, ref)
+    np.testing.assert_array_equal(ids, r["topk_ids"])
+    np.testing.assert_allclose(w, r["topk_weights"], rtol=1e-5)
+    sent = r["router_probs"] == -1e30
+    np.testing.assert_array_equal(probs == np.float32(-1e30), sent)
+    np.testing.assert_allclose(probs[~sent], r["router_probs"][~sent], rtol=0, atol=1e-5)
+    np.testing.assert_allclose(wsc, r["weight_scale"], rtol=1e-5, atol=1e-7)
+
+
+def test_route_rejects_past_the_limits(moe):
+    z = torch.randn((4, 1025), device="cuda")
+    with pytest.raises(moe.MoEError):
+        moe.moe_route(z, moe.route_params(8, "softmax", True))          # E > 1024
+    z = torch.randn((4, 128), device="cuda")
+    with pytest.raises(moe.MoEError):
+        moe.moe_route(z, moe.route_params(65, "softmax", True))         # K > 64
+    with pytest.raises(moe.MoEError):
+        moe.moe_route(z, moe.route_params(8, "sigmoid", True, num_expert_group=64,
+                                          topk_group=4))                # G > 32
+
+
 def test_route_golden_cases_on_gpu(moe):
     import json
     import os
