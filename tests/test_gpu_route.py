@@ -108,7 +108,7 @@ def test_route_ties_and_edges(moe):
 def test_route_maximum_sizes(moe, E, K, G, TG, scoring):
     cfg = synth.MoEConfig("max", 11, T=300, H=8, F=8, E=E, K=K, scoring=scoring, G=G, TG=TG,
                           rsf=2.5, cbias_std=0.1 if scoring == "sigmoid" else None,
-                          local_start=E - 96, local_count=96)
+                          local_start=max(0, E - 96), local_count=min(96, E))
     inp, ref = make(cfg)
     (w, ids, probs, wsc), r = _route_both(moe, cfg, inp, ref)
     np.testing.assert_array_equal(ids, r["topk_ids"])
