@@ -33,7 +33,7 @@ ACTS = {
 
 def _split_problem(counts, Hk, F, dtype, bias, seed):
     g = torch.Generator().manual_seed(seed)
-    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
     E, M = len(counts), int(sum(counts))
     a = torch.randn((M, Hk), generator=g).to(tdt)
     wg = (torch.randn((E, F, Hk), generator=g) / Hk ** 0.5).to(tdt)
@@ -57,6 +57,7 @@ def _cu(t):
     ([129, 127, 0, 256], 320, 160, "swiglu0", True, "bf16", True),       # SIMT, bf16
     ([300, 5, 0, 211], 132, 36, "silu", True, "bf16", False),            # F % 8 != 0 -> SIMT
     ([40, 0, 25, 63], 100, 48, "swiglu0", True, "f32", False),           # fp32 (SIMT)
+    ([129, 127, 0, 256], 320, 160, "swiglu0", True, "f16", False),       # float16 operands
 ])
 def test_gemm_act_split(moe, counts, Hk, F, act, bias, dtype, simt):
     spec = ACTS[act]
@@ -106,11 +107,12 @@ def test_split_rejects(moe):
     (300, 256, 192, 8, 2, "swiglu0", True, "bf16"),     # tcgen05, gathered rows
     (40, 128, 256, 16, 4, "silu", False, "bf16"),       # small T*K: still the staged path
     (200, 96, 72, 6, 2, "swiglu0_noclamp", True, "f32"),
+    (300, 256, 192, 8, 2, "gelu_mul", True, "f16"),
 ])
 def test_forward_split(moe, T, H, F, E, K, act, bias, dtype):
     spec = ACTS[act]
     g = torch.Generator().manual_seed(T + H + F)
-    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
     hidden = torch.randn((T, H), generator=g).to(tdt)
     logits = torch.randn((T, E), generator=g)
     wg = (torch.randn((E, F, H), generator=g) / H ** 0.5).to(tdt)
