@@ -138,3 +138,33 @@ def test_forward_split(moe, T, H, F, E, K, act, bias, dtype):
                       fusion=2, limit=spec.get("limit", 0.0), alpha=spec.get("alpha", 1.0),
                       beta=spec.get("beta", 0.0))
     assert_close(np_(out), r["out"], dtype, f"forward_split {act}")
+
+
+@pytest.mark.parametrize("name", ["qwen3_bf16", "gpt_oss_bf16"])
+def test_forward_split_full_size(moe, name):
+    """At the full workload sizes, in the forward's launch configuration: the
+    forward with the two tensors is bit for bit the stacked forward."""
+    from mixture_experts_ffn_gb300 import synth
+
+    from gpu_cases import make
+
+    cfg = synth.CONFIGS[name].replace(local_count=0)
+    inp, _ = make(cfg)
+    p, a = moe.config_params(cfg)
+    F = cfg.F
+    w1 = inp["w_gate_up"]
+    b1 = inp["b_gate_up"]
+    if a.swiglu_fusion == 1:  # interleaved rows: gate rows 2j, up rows 2j + 1
+        wg, wu = w1[:, 0::2].contiguous(), w1[:, 1::2].contiguous()
+        bg, bu = (None, None) if b1 is None else (b1[:, 0::2].contiguous(), b1[:, 1::2].contiguous())
+    else:
+        wg, wu = w1[:, :F].contiguous(), w1[:, F:].contiguous()
+        bg, bu = (None, None) if b1 is None else (b1[:, :F].contiguous(), b1[:, F:].contiguous())
+    a0 = moe.act_params(a.kind, 0 if a.kind == 1 else a.swiglu_fusion, a.limit, a.alpha, a.beta)
+    out = moe.moe_ffn_forward_split(inp["hidden"], inp["logits"], wg, wu, inp["w_down"], p, a0,
+                                    inp["correction_bias"], inp["expert_ids"], bg, bu,
+                                    inp["b_down"])
+    ref = moe.moe_ffn_forward(inp["hidden"], inp["logits"], w1, inp["w_down"], p, a,
+                              inp["correction_bias"], inp["expert_ids"], b1, inp["b_down"])
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
