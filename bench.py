@@ -643,7 +643,7 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
         E8, mm, N8, K8 = 8, 256, 4096, 7168
         f8 = synth.make_fp8_masked(E8, mm, N8, K8, seed=3, device=dev)
         f8_out = torch.empty((E8, mm, N8), dtype=torch.bfloat16, device=dev)
-        f8_ws = moe._ws(moe.load_library().moe_grouped_gemm_fp8_workspace_size(), dev)
+        f8_ws = moe._ws(256, dev)
         fns["fp8_gemm"] = lambda: moe.moe_grouped_gemm_fp8_masked(
             f8["a"], f8["a_scale"], f8["b"], f8["b_scale"], f8["counts"], out=f8_out, ws=f8_ws)
         rows = int(f8["counts"].clamp(0, mm).sum())

@@ -532,19 +532,11 @@ size_t moe_grouped_gemm_workspace_size(int layout, int rows, int E);
  * host); rows at or past m_g are not written (their contents are
  * undefined), and nothing outside out is.  a and b 16-byte aligned, the
  * scales 4-byte aligned (MOE_ERR_UNSUPPORTED otherwise); ws >=
- * MOE_STATUS_BYTES bytes.  E <= 1024.
- * With ws >= moe_grouped_gemm_fp8_workspace_size() bytes the tiles of a last,
- * partly filled round of the persistent grid are split over the idle SMs by
- * ranges of K blocks, and their fp32 partial tiles are added in a fixed order
- * (results then round once more in fp32 than the unsplit tiles', and the same
- * on every call with the same inputs and SM count). */
+ * MOE_STATUS_BYTES bytes.  E <= 1024. */
 moe_status moe_grouped_gemm_fp8_masked(const void* a, const float* a_scale, const void* b,
                                        const float* b_scale, const int32_t* layout_metadata,
                                        int E, int max_m, int N, int K, void* out, void* ws,
                                        size_t ws_bytes, cudaStream_t stream);
-/* Workspace bytes that let moe_grouped_gemm_fp8_masked split its last round
- * of tiles (about 64 KB per SM of the current device; 0 when no device). */
-size_t moe_grouped_gemm_fp8_workspace_size(void);
 
 /* ------------------------------------------------------------------------ */
 /* Shared expert [TileOPs, SharedExpertMLPFwdOp]: the dense gated MLP applied

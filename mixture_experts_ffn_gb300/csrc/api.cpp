@@ -308,26 +308,8 @@ moe_status moe_grouped_gemm_fp8_masked(const void* a, const float* a_scale, cons
                 {ws, MOE_STATUS_BYTES}};
   if (any_overlap(outs, ins)) return MOE_ERR_OVERLAP;
   if (max_m == 0) return MOE_OK;
-  // the split of the last round of tiles, when ws holds its scratch
-  void* split_ws = nullptr;
-  if (ws_bytes >= MOE_STATUS_BYTES + gemm_fp8_split_bytes()) {
-    split_ws = static_cast<char*>(ws) + MOE_STATUS_BYTES;
-    Span outs2[] = {{out, rows * N * 2}};
-    Span ins2[] = {{split_ws, gemm_fp8_split_bytes()}};
-    if (any_overlap(outs2, ins2)) return MOE_ERR_OVERLAP;
-  }
   return cuda_status(launch_gemm_fp8(a, a_scale, b, b_scale, layout_metadata, E, max_m, N, K, out,
-                                     static_cast<int*>(ws), stream, split_ws));
-}
-
-size_t moe_grouped_gemm_fp8_workspace_size(void) {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return 0;
-  }
-  return MOE_STATUS_BYTES + gemm_fp8_split_bytes();
+                                     static_cast<int*>(ws), stream));
 }
 
 size_t moe_grouped_gemm_workspace_size(int layout, int rows, int E) {

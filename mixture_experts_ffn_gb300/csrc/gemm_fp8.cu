@@ -23,13 +23,6 @@
 //                   (tile rows) and accumulator columns 64*((w-2)/4).. (64
 //                   fp32 registers of accumulator per thread), and writes its
 //                   rows as bf16 through staged 32 x 32 TMA stores
-// Tail split: when the tiles do not fill the last round of the persistent
-//   grid (tiles = full rounds x CTAs + tail, tail <= CTAs / 2), each tail tile
-//   is cut into S = min(CTAs / tail, K blocks, 8) ranges of K blocks that idle
-//   CTAs take as work items.  Each writes its fp32 partial tile to the
-//   workspace; per 32 x 64 region a counter tells the last of the S writers,
-//   which adds the S partials in range order (so the result does not depend on
-//   which CTA finishes last) and stores the bf16 region.
 // Every mbarrier wait is bounded (as in gemm_tc.cu): a wait that runs out sets
 // the timeout bit, raises the block's abort flag, and the block drains its
 // copies and MMAs in flight before freeing TMEM.
@@ -61,8 +54,6 @@ constexpr int kColsPerWarp = BN / 2;  // accumulator columns of one epilogue war
 // 0 in bits 7..9 and 10..12), N / 8 at bit 17, M / 16 at bit 24
 constexpr uint32_t kIdescFp8 =
     (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-constexpr int kMaxSplit = 8;
-constexpr size_t kPartialBytes = (size_t)BM * BN * 4;  // one fp32 partial tile
 
 struct Fp8Shared {
   uint64_t full[STAGES];
@@ -146,17 +137,6 @@ __device__ __forceinline__ MaskedTile decode_masked(int t, const int* prefix,
   return r;
 }
 
-// Work item i -> tile and K-block range [kb0, kb1); tj >= 0 marks the chunk c
-// of tail tile tj (items past the full rounds when the tail is split S ways).
-struct WorkItem {
-  int tile, kb0, kb1, chunk, tj;
-};
-__device__ __forceinline__ WorkItem work_item(int i, int full, int S, int nkb) {
-  if (S == 1 || i < full) return {i, 0, nkb, 0, -1};
-  const int j = i - full, tj = j / S, c = j - tj * S;
-  return {full + tj, c * nkb / S, (c + 1) * nkb / S, c, tj};
-}
-
 // The four K32 MMAs of one 128-wide K block into a fresh partial sum.
 __device__ __forceinline__ void umma_fp8_block(uint32_t d_tmem, uint64_t ad, uint64_t bd) {
   asm volatile(
@@ -183,8 +163,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const __grid_constant__ CUtensorMap tm_b, const float* __restrict__ a_scale,
                     const float* __restrict__ b_scale, const int32_t* __restrict__ counts, int E,
                     int max_m, int N, int K, const __grid_constant__ CUtensorMap tm_out,
-                    int tma_out, __nv_bfloat16* __restrict__ out, int* status,
-                    float* __restrict__ partials, int* __restrict__ tail_count) {
+                    int tma_out, __nv_bfloat16* __restrict__ out, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -221,12 +200,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int nkb = K / BKB;
   pdl_wait();  // the operands, scales and counts are read only after this
   const int total = build_masked_prefix(counts, E, max_m, n_tiles, sh->prefix, sh->scan_tmp);
-  // tail split (partials != nullptr when the workspace holds the partial tiles)
-  const int G = gridDim.x;
-  const int full = (total / G) * G, tail = total - full;
-  int S = 1;
-  if (partials && tail > 0 && 2 * tail <= G) S = min(min(G / tail, nkb), kMaxSplit);
-  const int items = S > 1 ? full + tail * S : total;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -240,10 +213,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = 0;
       bool ok = true;
-      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const WorkItem wi = work_item(it, full, S, nkb);
-        const MaskedTile st = decode_masked(wi.tile, sh->prefix, counts, E, max_m, n_tiles);
-        for (int kb = wi.kb0; kb < wi.kb1; ++kb) {
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const MaskedTile st = decode_masked(tile, sh->prefix, counts, E, max_m, n_tiles);
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
           uint8_t* a_dst = smem + (size_t)stage * STAGE_BYTES;
           mbar_expect_tx(&sh->full[stage], STAGE_BYTES);
@@ -266,9 +238,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true, any = false;
       const uint64_t adesc0 = sw128_desc(su32(smem));
       const uint64_t bdesc0 = sw128_desc(su32(smem + A_BYTES));
-      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const WorkItem wi = work_item(it, full, S, nkb);
-        for (int kb = wi.kb0; kb < wi.kb1; ++kb) {
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!wait_fast(&sh->pempty[pb], pph ^ 1u, abort_flag, status)) { ok = false; break; }
           if (!wait_fast(&sh->full[stage], phase, abort_flag, status)) { ok = false; break; }
           tc_fence_after();
@@ -295,9 +266,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t pph = 0;
     bool ok = true;
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-      const WorkItem wi = work_item(it, full, S, nkb);
-      const MaskedTile st = decode_masked(wi.tile, sh->prefix, counts, E, max_m, n_tiles);
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      const MaskedTile st = decode_masked(tile, sh->prefix, counts, E, max_m, n_tiles);
       const int row = st.m0 + quad * 32 + lane;  // row inside the expert's slab
       const bool in_slab = row < max_m;
       const float* sa = a_scale + ((size_t)st.g * max_m + (in_slab ? row : 0)) * nkb;
@@ -305,10 +275,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       float acc[kColsPerWarp];
 #pragma unroll
       for (int i = 0; i < kColsPerWarp; ++i) acc[i] = 0.f;
-      float sa_next = in_slab ? __ldg(sa + wi.kb0) : 0.f, sb_next = __ldg(sb + wi.kb0);
-      for (int kb = wi.kb0; kb < wi.kb1; ++kb) {
+      float sa_next = in_slab ? __ldg(sa) : 0.f, sb_next = __ldg(sb);
+      for (int kb = 0; kb < nkb; ++kb) {
         const float s = sa_next * sb_next;
-        if (kb + 1 < wi.kb1) {
+        if (kb + 1 < nkb) {
           sa_next = in_slab ? __ldg(sa + kb + 1) : 0.f;
           sb_next = __ldg(sb + kb + 1);
         }
@@ -329,38 +299,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (++pb == 2) { pb = 0; pph ^= 1u; }
       }
       if (!ok) break;
-      if (wi.tj >= 0) {
-        // a chunk of a split tail tile: store this thread's 64 partial sums
-        // (row quad*32 + lane, columns half*64..), then count the region in
-        const size_t prow = (size_t)(quad * 32 + lane) * BN + half * kColsPerWarp;
-        float4* dst = reinterpret_cast<float4*>(
-            partials + (size_t)(wi.tj * S + wi.chunk) * (BM * BN) + prow);
-#pragma unroll
-        for (int q = 0; q < kColsPerWarp / 4; ++q)
-          dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-        __threadfence();
-        __syncwarp();
-        int prev = 0;
-        if (lane == 0) prev = atomicAdd(&tail_count[wi.tj * kEpiWarps + (warp - 2)], 1);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev != S - 1) continue;  // another chunk's warp finishes this region
-        __threadfence();
-        // the last writer: the S partials added in chunk order
-#pragma unroll
-        for (int i = 0; i < kColsPerWarp; ++i) acc[i] = 0.f;
-        for (int c = 0; c < S; ++c) {
-          const float4* src = reinterpret_cast<const float4*>(
-              partials + (size_t)(wi.tj * S + c) * (BM * BN) + prow);
-#pragma unroll
-          for (int q = 0; q < kColsPerWarp / 4; ++q) {
-            const float4 v = __ldcg(src + q);
-            acc[4 * q] += v.x;
-            acc[4 * q + 1] += v.y;
-            acc[4 * q + 2] += v.z;
-            acc[4 * q + 3] += v.w;
-          }
-        }
-      }
       // rows of the flattened [E * max_m, N] output; rows at or past the
       // expert's count are not written
       const int wrow0 = st.g * max_m + st.m0 + quad * 32;
@@ -393,14 +331,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
-size_t gemm_fp8_split_bytes() {
-  const size_t G = (size_t)num_sms();
-  return ((G * kEpiWarps * 4 + 255) / 256) * 256 + G * kPartialBytes;
-}
-
 cudaError_t launch_gemm_fp8(const void* a, const float* a_scale, const void* b,
                             const float* b_scale, const int32_t* counts, int E, int max_m, int N,
-                            int K, void* out, int* status, cudaStream_t s, void* split_ws) {
+                            int K, void* out, int* status, cudaStream_t s) {
   if (E == 0 || max_m == 0) return cudaSuccess;
   CUtensorMap ma, mb, mo;
   {
@@ -430,21 +363,8 @@ cudaError_t launch_gemm_fp8(const void* a, const float* a_scale, const void* b,
   });
   const long long max_tiles = (long long)E * ((max_m + BM - 1) / BM) * (N / BN);
   const int grid = (int)std::max<long long>(1, std::min<long long>(max_tiles, num_sms()));
-  // split_ws: region counters (cleared here; each split tail tile has
-  // kEpiWarps of them, at most grid / 2 tail tiles) then the partial tiles
-  // (at most grid of them)
-  int* tail_count = nullptr;
-  float* partials = nullptr;
-  if (split_ws) {
-    const size_t cbytes = (((size_t)grid * kEpiWarps * 4 + 255) / 256) * 256;
-    tail_count = static_cast<int*>(split_ws);
-    partials = reinterpret_cast<float*>(static_cast<char*>(split_ws) + cbytes);
-    cudaError_t e = cudaMemsetAsync(tail_count, 0, (size_t)grid * kEpiWarps * 4, s);
-    if (e != cudaSuccess) return e;
-  }
   launch_pdl(gemm_fp8_kernel, grid, NUM_THREADS, kSmemBytes, s, ma, mb, a_scale, b_scale, counts,
-             E, max_m, N, K, mo, tma_out, static_cast<__nv_bfloat16*>(out), status, partials,
-             tail_count);
+             E, max_m, N, K, mo, tma_out, static_cast<__nv_bfloat16*>(out), status);
   count_launch();
   return cudaGetLastError();
 }

@@ -163,11 +163,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
 // scales per row x 128 K of a and per 128 x 128 block of b, bf16 out)
 cudaError_t launch_gemm_fp8(const void* a, const float* a_scale, const void* b,
                             const float* b_scale, const int32_t* counts, int E, int max_m, int N,
-                            int K, void* out, int* status, cudaStream_t s,
-                            void* split_ws = nullptr);
-// bytes of split_ws that let launch_gemm_fp8 split its last partial round of
-// tiles (region counters + one fp32 partial tile per CTA)
-size_t gemm_fp8_split_bytes();
+                            int K, void* out, int* status, cudaStream_t s);
 
 // two-SM (cta_group::2) variant of launch_gemm_tc, same contract
 cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,

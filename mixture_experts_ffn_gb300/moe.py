@@ -74,7 +74,6 @@ _SIGNATURES = {
                               _vp, _vp, _vp, _sz, _vp],
     "moe_grouped_gemm_fp8_masked": [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
     "moe_shared_expert_workspace_size": [_i, _i, _i, _i],
-    "moe_grouped_gemm_fp8_workspace_size": [],
     "moe_ffn_forward_shared": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                                _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_workspace_size_shared": [_i, _i, _i, _i, _i, _i, _i],
@@ -91,7 +90,6 @@ _RESTYPES = {"moe_workspace_size": _sz, "moe_permute_workspace_size": _sz,
              "moe_workspace_size_host": _sz, "moe_shared_expert_workspace_size": _sz,
              "moe_workspace_size_shared": _sz, "moe_permute_align_workspace_size": _sz,
              "moe_grouped_gemm_workspace_size": _sz,
-             "moe_grouped_gemm_fp8_workspace_size": _sz,
              "moe_status_string": ctypes.c_char_p, "moe_launch_count": ctypes.c_uint64}
 
 _lib = None
@@ -499,8 +497,8 @@ def moe_grouped_gemm_fp8_masked(a, a_scale, b, b_scale, layout_metadata, out=Non
     N = b.shape[1]
     if out is None:
         out = torch.empty((E, max_m, N), dtype=torch.bfloat16, device=a.device)
-    if ws is None:  # with room for the split of the last round of tiles
-        ws = _ws(max(MOE_STATUS_BYTES, lib.moe_grouped_gemm_fp8_workspace_size()), a.device)
+    if ws is None:
+        ws = _ws(MOE_STATUS_BYTES, a.device)
     _check("moe_grouped_gemm_fp8_masked",
            lib.moe_grouped_gemm_fp8_masked(_p(a), _p(a_scale), _p(b), _p(b_scale),
                                            _p(layout_metadata), E, max_m, N, K, _p(out), _p(ws),

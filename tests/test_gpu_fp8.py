@@ -65,40 +65,6 @@ def test_fp8_masked_gemm(moe, E, max_m, N, K, counts):
     assert torch.isnan(flat[E * max_m * N:]).all(), "wrote past out"
 
 
-@pytest.mark.parametrize("E,max_m,N,K,counts", [
-    # 160 tiles on 152 CTAs: 8 tail tiles split 8 ways
-    (8, 256, 2048, 1024, [256, 256, 128, 128, 128, 128, 128, 1]),
-    # one tile on a grid of 4 (sized from max_m): split 4 ways
-    (2, 256, 128, 2048, [1, 0]),
-    # five K blocks in ragged ranges
-    (3, 256, 128, 640, [40, 0, 0]),
-])
-@pytest.mark.parametrize("split", [True, False])
-def test_fp8_masked_gemm_tail_split(moe, E, max_m, N, K, counts, split):
-    """The last partial round of tiles split by K ranges over idle CTAs (the
-    default workspace), and the same call without that workspace: both
-    against the oracle, both the same on a second call."""
-    inp = synth.make_fp8_masked(E, max_m, N, K, seed=E * 77 + K, device="cuda", counts=counts)
-    nbytes = moe.load_library().moe_grouped_gemm_fp8_workspace_size() if split else 256
-    outs = []
-    for _ in range(2):
-        out = torch.full((E, max_m, N), float("nan"), dtype=torch.bfloat16, device="cuda")
-        ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
-        moe.moe_grouped_gemm_fp8_masked(inp["a"], inp["a_scale"], inp["b"], inp["b_scale"],
-                                        inp["counts"], out=out, ws=ws)
-        assert moe.moe_sync_status(ws) == moe.MOE_OK
-        outs.append(out)
-    ref = O.grouped_gemm_fp8_masked(_codes(inp["a"]), inp["a_scale"].cpu().numpy(),
-                                    _codes(inp["b"]), inp["b_scale"].cpu().numpy(),
-                                    inp["counts"].cpu().numpy(), dtype=None)
-    got = outs[0].float().cpu().numpy()
-    for g in range(E):
-        m = min(max(counts[g], 0), max_m)
-        _check(got[g, :m], ref[g, :m], K, f"expert {g}, split={split}")
-        assert np.isnan(got[g, m:]).all(), "rows past the count were written"
-        assert torch.equal(outs[0][g, :m], outs[1][g, :m]), "not deterministic"
-
-
 def test_fp8_masked_gemm_deepseek_size_sampled(moe):
     """DeepSeek-V3-style expert-parallel shapes (8 local experts, up to 256
     rows each, N 4096, K 7168); the oracle checks 4 rows of every expert."""
