@@ -22,7 +22,7 @@ class LazyExperts:
 def make(cfg, guard=True):
     """Inputs of ``cfg`` on cuda:0 and the oracle's view of them."""
     logits = cases.guarded_logits(cfg) if guard else None
-    wbytes = cfg.E * (cfg.n_gate_up + cfg.F) * cfg.H * (2 if cfg.dtype == "bf16" else 4)
+    wbytes = cfg.E * (cfg.n_gate_up + cfg.F) * cfg.H * (4 if cfg.dtype == "f32" else 2)
     wdev = "cuda" if wbytes > BIG_WEIGHT_BYTES else "cpu"
     inp = synth.make_inputs(cfg, "cuda", weight_device=wdev, logits=logits)
     ref = {k: cases.to_np(v) for k, v in inp.items() if k not in ("w_gate_up", "w_down")}

@@ -34,7 +34,8 @@ def run_forward(moe, cfg, inp):
         probs = torch.empty((T, cfg.local_count), dtype=torch.float32, device="cuda")
         wsc = torch.empty((T,), dtype=torch.float32, device="cuda")
     ws = torch.empty(moe.moe_workspace_size(T, cfg.H, cfg.F, cfg.E, cfg.K,
-                                            moe.MOE_BF16 if cfg.dtype == "bf16" else moe.MOE_F32),
+                                            {"bf16": moe.MOE_BF16, "f16": moe.MOE_F16,
+                                             "f32": moe.MOE_F32}[cfg.dtype]),
                      dtype=torch.uint8, device="cuda")
     moe.moe_clear_status(ws)
     out = moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a,
@@ -127,6 +128,17 @@ def test_ffn_full_size(moe, name, hash_ids):
         tokens = synth.subset_tokens(cfg.T)
     rep, _ = check(moe, cfg, tokens)
     print(name, rep)
+
+
+@pytest.mark.parametrize("name", ["gpt_oss_bf16", "deepseek_v3_bf16", "kimi_k2_decode_bf16"])
+def test_ffn_full_size_float16(moe, name):
+    """The other recipes at their full sizes with float16 operands (the
+    decode recipe then takes the staged path: the indexed kernel is bf16),
+    on the fixed token subset."""
+    cfg = synth.CONFIGS[name].replace(dtype="f16")
+    tokens = None if cfg.T <= 256 else synth.subset_tokens(cfg.T)
+    rep, _ = check(moe, cfg, tokens)
+    print(name, "f16", rep)
 
 
 def test_indexed_path_matches_staged(moe):
