@@ -144,7 +144,10 @@ __device__ __forceinline__ void route_loaded(int t, const float (&z)[NPL],
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
       int e = lane + 32 * i;
-      u[i] = e < E ? (bias ? s[i] + __ldg(bias + e) : s[i]) : -INFINITY;
+      const float v = bias && e < E ? s[i] + __ldg(bias + e) : s[i];
+      // a NaN score ranks below every number (it is never preferred to a
+      // finite score, for its group or for the top-K)
+      u[i] = e < E && !isnan(v) ? v : -INFINITY;
     }
     // ---- group restriction
     if (a.G > 1) {
@@ -181,7 +184,7 @@ __device__ __forceinline__ void route_loaded(int t, const float (&z)[NPL],
         // already kept groups are out of the running
         if ((keep >> lane) & 1u) { v = -INFINITY; idx = 0x7fffffff; }
         warp_argmax(v, idx);
-        keep |= 1u << idx;
+        if (idx < a.G) keep |= 1u << idx;  // (always true: TG <= G groups to keep)
       }
 #pragma unroll
       for (int i = 0; i < NPL; ++i) {

@@ -118,10 +118,15 @@ def expert_scores(logits, scoring: str, score_dtype=np.float32) -> np.ndarray:
 
 def selection_scores(scores, correction_bias=None) -> np.ndarray:
     """u_e = s_e + bias_e when a correction bias is passed: it steers the
-    selection only [TileOPs FusedMoEFwdOp, FusedTopKFwdOp init]."""
+    selection only [TileOPs FusedMoEFwdOp, FusedTopKFwdOp init].  The pages
+    leave NaN open; the reading taken: a NaN selection score ranks below every
+    number (u = -inf), so it never displaces a finite score, in a group score
+    or in the top-K."""
     if correction_bias is None:
-        return np.array(scores, copy=True)
-    return scores + np.asarray(correction_bias).astype(scores.dtype)[None, :]
+        u = np.array(scores, copy=True)
+    else:
+        u = scores + np.asarray(correction_bias).astype(scores.dtype)[None, :]
+    return np.where(np.isnan(u), -np.inf, u).astype(u.dtype)
 
 
 def group_scores(u, G: int, biased: bool) -> np.ndarray:
@@ -551,13 +556,14 @@ def ffn_forward(hidden, logits, w_gate_up, w_down, K: int, F: int, scoring="soft
         acc += w[:, k:k + 1] * Y[k::K]
     r["out_unrounded"] = acc
     r["out"] = round_to(acc, dtype)
+    r["route_out"] = Y  # y of route (i, k) at row i*K + k, rounded to dtype
     r["tokens"] = tok
     return r
 
 
 def ffn_forward_local(hidden, router_probs, weight_scale, w_gate_up, w_down, K: int, F: int,
                       act=ACT_SILU_AND_MUL, fusion=2, limit=0.0, alpha=1.0, beta=0.0,
-                      dtype: Optional[str] = "bf16") -> np.ndarray:
+                      dtype: Optional[str] = "bf16", parts: bool = False):
     """The layer of one expert-parallel rank holding lc experts (w_gate_up and
     w_down of those experts only), fed by the MoERouter outputs of its slice
     [MoERouter: "QMoE's own softmax over the local block returns w_e /
@@ -566,7 +572,9 @@ def ffn_forward_local(hidden, router_probs, weight_scale, w_gate_up, w_down, K: 
     row (float32, as the router computes it), its top min(K, lc) experts (ties
     to the lower index), the weighted sum of their expert MLPs, multiplied by
     weight_scale[t] and cast once.  Summed over the ranks' slices this is the
-    routed layer with normalised weights (times route_scale)."""
+    routed layer with normalised weights (times route_scale).  ``parts``:
+    return a dict with ``out``, ``out_unrounded`` (before the cast),
+    ``route_out`` and ``topk_weights`` instead of the output alone."""
     rp = np.asarray(router_probs, dtype=np.float32)
     lc = rp.shape[1]
     Kl = min(K, lc)
@@ -578,17 +586,23 @@ def ffn_forward_local(hidden, router_probs, weight_scale, w_gate_up, w_down, K: 
     acc = np.zeros_like(X)
     for k in range(Kl):
         acc += r["topk_weights"][:, k:k + 1] * Y[k::Kl]
-    return round_to(np.asarray(weight_scale, dtype=np.float64)[:, None] * acc, dtype)
+    exact = np.asarray(weight_scale, dtype=np.float64)[:, None] * acc
+    if parts:
+        return {"out": round_to(exact, dtype), "out_unrounded": exact, "route_out": Y,
+                "topk_weights": r["topk_weights"]}
+    return round_to(exact, dtype)
 
 
-def shared_expert_mlp(hidden, w_gate_up, w_down, dtype: Optional[str] = "bf16") -> np.ndarray:
+def shared_expert_mlp(hidden, w_gate_up, w_down, dtype: Optional[str] = "bf16",
+                      unrounded: bool = False) -> np.ndarray:
     """Dense gated MLP of the shared expert, applied to every token
     [TileOPs SharedExpertMLPFwdOp]: with w_gate_up [2S, H] the gate rows (0..S)
     stacked over the up rows (S..2S) and w_down [H, S],
         out = down(silu(hidden @ gate^T) * (hidden @ up^T)),
     both products accumulated in float64 here (float32 on the GPU), the gated
     activation rounded to the input dtype before the down projection, the
-    result rounded to it too."""
+    result rounded to it too (``unrounded``: the down product before that
+    last cast)."""
     X = np.asarray(hidden, dtype=np.float64)
     Wgu = np.asarray(w_gate_up, dtype=np.float64)
     Wd = np.asarray(w_down, dtype=np.float64)
@@ -596,6 +610,8 @@ def shared_expert_mlp(hidden, w_gate_up, w_down, dtype: Optional[str] = "bf16") 
     g = X @ Wgu[:S].T
     u = X @ Wgu[S:].T
     a = round_to(g * sigmoid64(g) * u, dtype)
+    if unrounded:
+        return a @ Wd.T
     return round_to(a @ Wd.T, dtype)
 
 
@@ -607,7 +623,9 @@ def ffn_forward_shared(hidden, logits, w_gate_up, w_down, shared_w_gate_up, shar
     output only, once, through the routing weights)."""
     r = ffn_forward(hidden, logits, w_gate_up, w_down, dtype=dtype, **routed)
     X = np.asarray(hidden)[r["tokens"]]
-    r["shared"] = shared_expert_mlp(X, shared_w_gate_up, shared_w_down, dtype)
+    r["shared_unrounded"] = shared_expert_mlp(X, shared_w_gate_up, shared_w_down, dtype,
+                                              unrounded=True)
+    r["shared"] = round_to(r["shared_unrounded"], dtype)
     return r
 
 
