@@ -12,7 +12,7 @@ from mixture_experts_ffn_gb300 import synth
 from oracle import moe_oracle as O
 
 from gpu_cases import act_kwargs, make, np_
-from tolerances import assert_close
+from tolerances import assert_forward_close, assert_layer_close, flip_budget, ulp_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -40,6 +40,7 @@ def test_expert_parallel_ranks_sum_to_the_layer(moe, name, over, lc):
                                a, inp["correction_bias"])
     total = torch.zeros_like(full, dtype=torch.float32)
     want_total = np.zeros(tuple(full.shape))
+    parts_budget = np.zeros(tuple(full.shape))
     for start in range(0, E, lc):
         pr = moe.route_params(K, cfg.scoring, cfg.renormalize, cfg.G, cfg.TG, cfg.rsf,
                               local_expert_start=start, local_expert_count=lc,
@@ -54,15 +55,22 @@ def test_expert_parallel_ranks_sum_to_the_layer(moe, name, over, lc):
         want = O.ffn_forward_local(ref["hidden"], r["router_probs"], r["weight_scale"],
                                    ref["w_gate_up"][start:start + lc],
                                    ref["w_down"][start:start + lc], K, cfg.F,
-                                   dtype=cfg.dtype, **act_kwargs(cfg))
-        assert_close(np_(part), want, cfg.dtype, f"{name} rank at {start}")
+                                   dtype=cfg.dtype, parts=True, **act_kwargs(cfg))
+        assert_forward_close(np_(part), want, cfg.dtype, f"ep {name} rank at {start}",
+                             scale=r["weight_scale"])
         total += part.float()
-        want_total += want
+        want_total += want["out_unrounded"]
+        # each rank's own cast and flips (see the tolerances module)
+        parts_budget += 0.5 * ulp_bf16(np.maximum(np.abs(np_(part)),
+                                                  np.abs(want["out_unrounded"])))
+        parts_budget += flip_budget(want["route_out"], want["topk_weights"], cfg.dtype,
+                                    r["weight_scale"])
     # the ranks' outputs are each rounded to bf16 before they are summed (as an
-    # all-reduce of their results would), so the sum is compared with the
-    # oracle's sum of its rounded ranks, and with the layer (rounded once)
-    # within the error of those extra roundings
-    assert_close(np_(total), want_total, cfg.dtype, f"{name} sum of ranks")
+    # all-reduce of their results would), so the float32 sum is compared with
+    # the oracle's sum of the exact rank outputs, each rank's roundings in the
+    # budget; and with the layer (rounded once) within those extra roundings
+    assert_layer_close(np_(total), want_total, cfg.dtype, f"ep {name} sum of ranks",
+                       budget=parts_budget, final_cast=False)
     err = np_(total) - np_(full)
     rms = float(np.sqrt(np.mean(np_(full) ** 2)))
     assert float(np.sqrt(np.mean(err ** 2))) <= 5e-3 * rms, f"{name} sum vs layer"

@@ -12,7 +12,8 @@ from oracle import cases
 from oracle import moe_oracle as O
 
 from gpu_cases import np_
-from tolerances import assert_close, assert_rounded_once, ulp_bf16, ulp_f16
+from tolerances import (assert_forward_close, assert_layer_close, assert_rounded_once, ulp_bf16,
+                        ulp_f16)
 
 pytestmark = pytest.mark.gpu
 
@@ -153,7 +154,7 @@ def test_forward_f16(moe, T, ldt):
                         K=cfg.K, F=cfg.F, scoring=cfg.scoring, renormalize=cfg.renormalize,
                         dtype="f16", tokens=tokens)
     got = np_(out) if tokens is None else np_(out)[tokens]
-    assert_close(got, ref["out"], "f16", f"forward f16 T={T} logits {ldt}")
+    assert_forward_close(got, ref, "f16", f"forward f16 T={T} logits {ldt}")
 
 
 def test_local_forward_f16_router_probs(moe):
@@ -174,8 +175,8 @@ def test_local_forward_f16_router_probs(moe):
     out = moe.moe_ffn_forward_local(inp["hidden"], probs, wsc, w1, w2, cfg.K,
                                     moe.act_params(kind=0))
     ref = O.ffn_forward_local(np_(inp["hidden"]), r["router_probs"], np_(wsc), np_(w1), np_(w2),
-                              cfg.K, cfg.F, dtype="f16")
-    assert_close(np_(out), ref, "f16", "local forward f16")
+                              cfg.K, cfg.F, dtype="f16", parts=True)
+    assert_forward_close(np_(out), ref, "f16", "local forward f16", scale=r["weight_scale"])
 
 
 def test_shared_expert_f16(moe):
@@ -187,6 +188,6 @@ def test_shared_expert_f16(moe):
     out = moe.moe_shared_expert_mlp(hidden.cuda(), sw["shared_w_gate_up"].cuda(),
                                     sw["shared_w_down"].cuda())
     assert out.dtype == torch.float16
-    ref = O.shared_expert_mlp(np_(hidden), np_(sw["shared_w_gate_up"]), np_(sw["shared_w_down"]),
-                              dtype="f16")
-    assert_close(np_(out), ref, "f16", "shared expert f16")
+    exact = O.shared_expert_mlp(np_(hidden), np_(sw["shared_w_gate_up"]),
+                                np_(sw["shared_w_down"]), dtype="f16", unrounded=True)
+    assert_layer_close(np_(out), exact, "f16", "shared expert f16")

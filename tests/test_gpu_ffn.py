@@ -11,7 +11,7 @@ from mixture_experts_ffn_gb300 import synth
 from oracle import moe_oracle as O
 
 from gpu_cases import act_kwargs, make, np_
-from tolerances import assert_close
+from tolerances import assert_forward_close
 
 pytestmark = pytest.mark.gpu
 
@@ -56,7 +56,13 @@ def oracle_forward(cfg, ref, tokens=None):
                          **act_kwargs(cfg))
 
 
-def check(moe, cfg, tokens=None):
+# Cases whose bare max|err| exceeds the stated bf16 bound of 2e-2 * RMS(ref)
+# (against the exact, unrounded layer output); they assert the secondary
+# bound instead.  Every other bf16 case asserts the stated bound as written.
+STATED_BOUND_NOT_MET = set()
+
+
+def check(moe, cfg, tokens=None, what=None):
     inp, ref = make(cfg)
     out, tw, ti, probs, wsc, status = run_forward(moe, cfg, inp)
     assert status == moe.MOE_OK
@@ -76,7 +82,9 @@ def check(moe, cfg, tokens=None):
     r = oracle_forward(cfg, ref, tokens)
     tok = r["tokens"]
     got = np_(out)[tok]
-    return assert_close(got, r["out"], cfg.dtype, cfg.name), out
+    what = what or cfg.name
+    return assert_forward_close(got, r, cfg.dtype, what,
+                                stated=what not in STATED_BOUND_NOT_MET), out
 
 
 SMALL = {
@@ -91,7 +99,7 @@ SMALL = {
 @pytest.mark.parametrize("name", list(SMALL))
 def test_ffn_small(moe, name):
     cfg = synth.CONFIGS[name].replace(**SMALL[name])
-    check(moe, cfg)
+    check(moe, cfg, what=f"small {name}")
 
 
 @pytest.mark.parametrize("name,over", [
@@ -105,12 +113,12 @@ def test_ffn_small(moe, name):
 def test_ffn_activation_and_scoring_variants(moe, name, over):
     """gelu_and_mul, the non-gated relu / gelu / silu and sqrt_softplus
     scoring through the whole forward against the oracle."""
-    check(moe, synth.CONFIGS[name].replace(**over))
+    check(moe, synth.CONFIGS[name].replace(**over), what=f"variant {name} act {over.get('act')}")
 
 
 def test_ffn_small_hash_routing(moe):
     cfg = synth.CONFIGS["kimi_k2_decode_bf16"].replace(hash_ids=True, T=16, H=256, F=256, E=96)
-    check(moe, cfg)
+    check(moe, cfg, what="small kimi_k2_decode_bf16 hash")
 
 
 @pytest.mark.parametrize("name,hash_ids", [
@@ -126,7 +134,7 @@ def test_ffn_full_size(moe, name, hash_ids):
     tokens = None if cfg.T <= 4096 else synth.subset_tokens(cfg.T)
     if name == "gpt_oss_bf16":
         tokens = synth.subset_tokens(cfg.T)
-    rep, _ = check(moe, cfg, tokens)
+    rep, _ = check(moe, cfg, tokens, what=f"full {name}{' hash' if hash_ids else ''}")
     print(name, rep)
 
 
@@ -137,7 +145,7 @@ def test_ffn_full_size_float16(moe, name):
     on the fixed token subset."""
     cfg = synth.CONFIGS[name].replace(dtype="f16")
     tokens = None if cfg.T <= 256 else synth.subset_tokens(cfg.T)
-    rep, _ = check(moe, cfg, tokens)
+    rep, _ = check(moe, cfg, tokens, what=f"full {name} f16")
     print(name, "f16", rep)
 
 
@@ -155,8 +163,10 @@ def test_indexed_path_matches_staged(moe):
     y_st = moe.moe_combine(y, w, perm["route_to_row"])
     torch.cuda.synchronize()
     r = oracle_forward(cfg, ref)
-    assert_close(np_(y_idx), r["out"], "bf16", "indexed")
-    assert_close(np_(y_st), r["out"], "bf16", "staged")
+    assert_forward_close(np_(y_idx), r, "bf16", "indexed vs oracle",
+                         stated="indexed vs oracle" not in STATED_BOUND_NOT_MET)
+    assert_forward_close(np_(y_st), r, "bf16", "staged vs oracle",
+                         stated="staged vs oracle" not in STATED_BOUND_NOT_MET)
 
 
 def test_forward_is_deterministic(moe):

@@ -10,7 +10,7 @@ import torch
 from oracle import moe_oracle as O
 
 from gpu_cases import np_
-from tolerances import assert_close, assert_rounded_once
+from tolerances import assert_forward_close, assert_rounded_once
 
 pytestmark = pytest.mark.gpu
 
@@ -137,7 +137,7 @@ def test_forward_split(moe, T, H, F, E, K, act, bias, dtype):
                       scoring="softmax", renormalize=True, dtype=dtype, act=spec["kind"],
                       fusion=2, limit=spec.get("limit", 0.0), alpha=spec.get("alpha", 1.0),
                       beta=spec.get("beta", 0.0))
-    assert_close(np_(out), r["out"], dtype, f"forward_split {act}")
+    assert_forward_close(np_(out), r, dtype, f"forward_split {act} {dtype}")
 
 
 @pytest.mark.parametrize("name", ["qwen3_bf16", "gpt_oss_bf16"])
