@@ -477,15 +477,20 @@ moe_status moe_ffn_forward_local(const void* hidden, const void* router_probs,
  * `ws` and copied back (always so on the indexed decode path).  All of it is
  * asynchronous on `stream`: out_host is valid after the stream is
  * synchronised.  Pageable buffers work, but their copies synchronise.
- * Weights, biases and expert_ids stay device pointers.  Routing outputs are
- * not returned.  ws >= moe_workspace_size_host(T, H, F, E, K, dtype). */
+ * Weights, biases and expert_ids stay device pointers.  topk_weights and
+ * topk_ids are not returned; the MoERouter outputs of the local slice, when
+ * p->local_expert_count > 0, go to the DEVICE buffers router_probs
+ * [T, local_expert_count] and weight_scale [T] as in moe_ffn_forward (both
+ * required then, ignored otherwise).
+ * ws >= moe_workspace_size_host(T, H, F, E, K, dtype). */
 moe_status moe_ffn_forward_host(const void* hidden_host, const void* logits_host,
                                 const void* w_gate_up, const void* w_down,
                                 const float* correction_bias, const int32_t* expert_ids,
                                 const void* b_gate_up, const void* b_down, int T, int H, int F,
                                 int E, moe_dtype dtype, const moe_route_params* p,
-                                const moe_act_params* act, void* out_host, void* ws,
-                                size_t ws_bytes, cudaStream_t stream);
+                                const moe_act_params* act, void* out_host, void* router_probs,
+                                float* weight_scale, void* ws, size_t ws_bytes,
+                                cudaStream_t stream);
 
 /* Workspace bytes of moe_ffn_forward_host: moe_workspace_size plus device
  * staging for hidden, logits and out. */
@@ -609,6 +614,19 @@ uint64_t moe_launch_count(void);
  * previous setting.  Process-wide; not meant to change while calls are in
  * flight. */
 int moe_set_gemm_simt(int enable);
+
+/* Test hook, off by default (no counterpart on the pages; it exists so that
+ * a test can make a bounded device wait run out without faulting or hanging
+ * anything).  With enable != 0, both grid barriers of the fused route +
+ * index-map launch (moe_route_permute, and the first launch of the forward
+ * when E <= 512) wait for one arrival more than the grid provides and give up
+ * after limit_ns instead of 2 s: every CTA then latches MOE_ERR_TIMEOUT in the
+ * workspace status word and returns, leaving the index maps unwritten and the
+ * barrier counters as they stand (moe_clear_status resets both the status
+ * word and the counters).  enable = 0 restores the normal barriers and the
+ * 2 s limit.  Process-wide, read when a call is issued; returns the previous
+ * enable state. */
+int moe_test_force_wait_timeout(int enable, long long limit_ns);
 
 #ifdef __cplusplus
 }

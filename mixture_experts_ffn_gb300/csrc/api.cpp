@@ -8,6 +8,8 @@
 #include <cmath>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "internal.h"
 
@@ -28,6 +30,20 @@ int num_sms() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+cudaError_t set_smem_limit(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::set<std::pair<int, const void*>> done;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(dev, kernel);
+  if (done.count(key)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert(key);
+  return e;
 }
 
 static int g_force_simt = 0;
@@ -832,10 +848,10 @@ moe_status moe_ffn_forward_host(const void* hidden_host, const void* logits_host
                                 const float* correction_bias, const int32_t* expert_ids,
                                 const void* b_gate_up, const void* b_down, int T, int H, int F,
                                 int E, moe_dtype dtype, const moe_route_params* p,
-                                const moe_act_params* act, void* out_host, void* ws,
-                                size_t ws_bytes, cudaStream_t stream) {
+                                const moe_act_params* act, void* out_host, void* router_probs,
+                                float* weight_scale, void* ws, size_t ws_bytes,
+                                cudaStream_t stream) {
   if (!p || !dtype_ok(dtype) || T < 0 || H < 1 || F < 1 || E < 1) return MOE_ERR_INVALID_ARG;
-  if (p->local_expert_count != 0) return MOE_ERR_INVALID_ARG;  // no routing outputs here
   if (T > 0 && (!hidden_host || !logits_host || !out_host)) return MOE_ERR_INVALID_ARG;
   const size_t need = moe_workspace_size_host(T, H, F, E, p->top_k, dtype);
   if (need == 0) return MOE_ERR_INVALID_ARG;
@@ -887,7 +903,7 @@ moe_status moe_ffn_forward_host(const void* hidden_host, const void* logits_host
     hk.out_direct = mapped_host(out_host);
     st = ffn_forward(d_hidden, d_logits, w_gate_up, w_down, correction_bias, expert_ids,
                      b_gate_up, b_down, T, H, F, E, dtype, p, act, d_out, nullptr, nullptr,
-                     nullptr, nullptr, ws, fwd, stream, &hk);
+                     router_probs, weight_scale, ws, fwd, stream, &hk);
   }
   // Whatever happened, nothing later on `stream` runs before the side copy.
   if (copied && !hk.waited && cudaStreamWaitEvent(stream, ready, 0) != cudaSuccess)
@@ -936,6 +952,10 @@ int moe_set_gemm_simt(int enable) {
   int old = g_force_simt;
   g_force_simt = enable ? 1 : 0;
   return old;
+}
+
+int moe_test_force_wait_timeout(int enable, long long limit_ns) {
+  return set_wait_timeout_test(enable, limit_ns);
 }
 
 }  // extern "C"

@@ -356,11 +356,7 @@ cudaError_t launch_gemm_fp8(const void* a, const float* a_scale, const void* b,
     tma_out = tmap::encode_bf16(&mo, out, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_64B) ? 1 : 0;
   }
   if (!tma_out) mo = mb;  // unused
-  static std::once_flag attr_once;
-  std::call_once(attr_once, [] {
-    cudaFuncSetAttribute(gemm_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kSmemBytes);
-  });
+  set_smem_limit((const void*)gemm_fp8_kernel, (int)kSmemBytes);
   const long long max_tiles = (long long)E * ((max_m + BM - 1) / BM) * (N / BN);
   const int grid = (int)std::max<long long>(1, std::min<long long>(max_tiles, num_sms()));
   launch_pdl(gemm_fp8_kernel, grid, NUM_THREADS, kSmemBytes, s, ma, mb, a_scale, b_scale, counts,

@@ -23,10 +23,12 @@
 //                   stores (gemm_epilogue.cuh)
 //   Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
 //   tile overlap the main loop of the next.
-// What bounds it: the TMA load stream.  Timed apart, the MMAs alone run at
-// close to the tensor peak and the loads alone take ~80% of the whole kernel:
-// each SM takes in about 45-50 bytes per cycle of TMA tiles, well below what
-// DRAM and L2 deliver in aggregate (their counters stay near half of peak).
+// What bounds it: shared-memory traffic per SM.  Each 64-wide k-block writes
+// 48 KB into shared memory (A 16 KB + B 32 KB) and the four M128 N256 K16 MMAs
+// read the same 48 KB back; at 128 bytes per cycle that is >= 750 cycles per
+// k-block against 512 cycles of MMA, and the measured ~950 cycles put shared
+// memory about 79% busy.  Timed apart, the MMAs alone and the loads alone each
+// run faster than the whole kernel, and deeper rings do not help.
 // Every mbarrier wait is bounded: a wait that runs out sets MOE's timeout bit
 // in the status word, raises a block-wide abort flag, and the block drains its
 // in-flight copies and MMAs (again bounded) before freeing TMEM and returning.
@@ -413,8 +415,7 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
   }
   if (gather) ma = mb;  // unused by the kernel
   if (!split) mb_up = mb;  // unused
-  static std::once_flag attr_once;
-  std::call_once(attr_once, [] {
+  {
     for (const void* fn : {(const void*)gemm_tc_kernel<kTcPlain, MOE_ACT_IDENTITY, false>,
                            (const void*)gemm_tc_kernel<kTcPlain, MOE_ACT_RELU, false>,
                            (const void*)gemm_tc_kernel<kTcPlain, MOE_ACT_GELU, false>,
@@ -431,8 +432,8 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            (const void*)gemm_tc_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, true>,
                            (const void*)gemm_tc_kernel<kTcStacked, MOE_ACT_SWIGLU, true>,
                            (const void*)gemm_tc_kernel<kTcInterleaved, MOE_ACT_SWIGLU, true>})
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  });
+      set_smem_limit(fn, (int)kSmemBytes);
+  }
   const int n_tiles = mode == kTcPlain ? (N + BN - 1) / BN : (N + BN / 2 - 1) / (BN / 2);
   const long long max_tiles = (long long)((M + BM - 1) / BM + E) * n_tiles;
   const int grid = (int)std::max<long long>(1, std::min<long long>(max_tiles, num_sms()));

@@ -484,8 +484,7 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
   }
   if (mode != kTcStacked) mb_s = mb;  // unused
   if (gather) ma = ma_s = mb;           // unused
-  static std::once_flag attr_once;
-  std::call_once(attr_once, [] {
+  {
     for (const void* fn : {(const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_IDENTITY, false>,
                            (const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_RELU, false>,
                            (const void*)gemm_tc2_kernel<kTcPlain, MOE_ACT_GELU, false>,
@@ -502,8 +501,8 @@ cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
                            (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SILU_AND_MUL, true>,
                            (const void*)gemm_tc2_kernel<kTcStacked, MOE_ACT_SWIGLU, true>,
                            (const void*)gemm_tc2_kernel<kTcInterleaved, MOE_ACT_SWIGLU, true>})
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-  });
+      set_smem_limit(fn, (int)kSmemBytes);
+  }
   // output map for the staged TMA stores (rows stored directly when the
   // output's base or pitch is not 16-byte aligned)
   CUtensorMap mo;

@@ -57,6 +57,11 @@ struct ForwardWs {
 void count_launch(int n = 1);
 int num_sms();
 
+// Raises the dynamic shared-memory limit of `kernel` to `bytes` on the
+// current device, once per (device, kernel): the setting belongs to the
+// device's context, so a second GPU needs its own call.  Thread-safe.
+cudaError_t set_smem_limit(const void* kernel, int bytes);
+
 // Launch with programmatic stream serialization: the kernel may be scheduled
 // while the previous kernel of the stream is still finishing, runs whatever
 // does not read earlier results (shared-memory set-up, barrier init, TMEM
@@ -89,6 +94,8 @@ cudaError_t launch_route(const void* logits, const float* bias, const int32_t* i
 // E is within its limit (E <= 512).  Uses ws's permute scratch and three
 // ints of its status area (grid-barrier counters that reset themselves).
 bool route_permute_ok(int E);
+// Test hook behind moe_test_force_wait_timeout; returns the previous state.
+int set_wait_timeout_test(int enable, long long limit_ns);
 cudaError_t launch_route_permute(const void* logits, const float* bias, const int32_t* ids_in,
                                  int T, int E, const moe_route_params& p, float* w, int32_t* ids,
                                  void* probs, float* wscale, int32_t* seg_end,

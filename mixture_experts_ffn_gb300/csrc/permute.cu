@@ -436,12 +436,7 @@ cudaError_t launch_permute(const void* hidden, int esz, const int32_t* ids, int 
   while (W > 1 && (size_t)W * E * 4 > 96 * 1024) W >>= 1;
   if (W >= 4) {
     const size_t sm = (size_t)W * E * 4;
-    static bool attr_set = false;
-    if (!attr_set) {
-      cudaFuncSetAttribute(perm_scatter_cta, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           96 * 1024);
-      attr_set = true;
-    }
+    set_smem_limit((const void*)perm_scatter_cta, 96 * 1024);
     launch_pdl(perm_scatter_cta, C, W * 32, sm, s, ids, M, E, counts, row_to_route, route_to_row);
   } else {
     launch_pdl(perm_scatter, C, 32, hist_smem, s, ids, M, E, counts, row_to_route, route_to_row);

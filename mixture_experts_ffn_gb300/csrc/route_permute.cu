@@ -46,8 +46,16 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
   return v;
 }
 
+// Barrier parameters: the arrivals a barrier waits for beyond the grid's
+// own CTAs (0; 1 only under the test hook, so that the wait cannot end) and
+// the limit of each wait.
+struct BarrierArgs {
+  int extra;
+  uint64_t limit_ns;
+};
+
 // All CTAs of the grid meet here; false (and the timeout bit) if one never came.
-__device__ bool grid_barrier(int* ctr, int* status) {
+__device__ bool grid_barrier(int* ctr, int* status, BarrierArgs b) {
   __shared__ int ok_s;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -55,8 +63,8 @@ __device__ bool grid_barrier(int* ctr, int* status) {
     atomicAdd(ctr, 1);
     const uint64_t t0 = global_ns();
     int ok = 1;
-    while (ld_acquire(ctr) < (int)gridDim.x) {
-      if (global_ns() - t0 > tc::kTimeoutNs) {
+    while (ld_acquire(ctr) < (int)gridDim.x + b.extra) {
+      if (global_ns() - t0 > b.limit_ns) {
         latch_error(status, kDevTimeout);
         ok = 0;
         break;
@@ -102,7 +110,7 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
     int32_t* __restrict__ id_out, void* __restrict__ probs, float* __restrict__ wscale,
     int C, int* __restrict__ counts, int32_t* __restrict__ seg_end, int* __restrict__ active,
     int* __restrict__ num_active, int32_t* __restrict__ row_to_route,
-    int32_t* __restrict__ route_to_row, int* status, int* bar) {
+    int32_t* __restrict__ route_to_row, int* status, int* bar, BarrierArgs ba) {
   extern __shared__ int smem[];  // [E] expert start | [E] chunk offsets / histogram | [W][E]
   pdl_wait();  // everything below reads results of earlier launches
   const int warp = threadIdx.x >> 5, W = blockDim.x >> 5, tid = threadIdx.x;
@@ -120,14 +128,14 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
       for (int i = 0; i < NPL; ++i) z[i] = zn[i];
     }
   }
-  if (!grid_barrier(&bar[0], status)) return;
+  if (!grid_barrier(&bar[0], status, ba)) return;
   // ---- B: count
   int* start = smem;
   int* offs = smem + E;
   int* wcnt = smem + 2 * E;
   for (int c = blockIdx.x; c < C; c += gridDim.x)
     pm::count_chunk(id_out, M, E, c, offs, counts + (size_t)c * E, status);
-  if (!grid_barrier(&bar[1], status)) return;
+  if (!grid_barrier(&bar[1], status, ba)) return;
   if (threadIdx.x == 0 && atomicAdd(&bar[2], 1) == (int)gridDim.x - 1) {
     // every CTA is past both barriers: ready for the next launch
     bar[0] = 0;
@@ -166,12 +174,9 @@ cudaError_t launch_npl(const void* logits, const float* bias, const int32_t* ids
                        int E, const RouteArgs& a, float* w, int32_t* ids, void* probs,
                        float* wscale, int C, int* counts, int32_t* seg_end, int* active,
                        int* num_active, int32_t* r2r, int32_t* route_to_row, int* status, int* bar,
-                       size_t smem, int grid, cudaStream_t s) {
-  static std::once_flag smem_attr;
-  std::call_once(smem_attr, [] {
-    cudaFuncSetAttribute(route_permute_kernel<NPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (2 + kFusedWarps) * kFusedWarps * 32 * 4);
-  });
+                       size_t smem, int grid, BarrierArgs ba, cudaStream_t s) {
+  set_smem_limit((const void*)route_permute_kernel<NPL>,
+                 (2 + kFusedWarps) * kFusedWarps * 32 * 4);
   // A cooperative launch: the scheduler starts the grid only when all of its
   // CTAs can be resident at once, so two of these kernels running on two
   // streams never each hold part of the GPU while waiting at a barrier for
@@ -193,19 +198,28 @@ cudaError_t launch_npl(const void* logits, const float* bias, const int32_t* ids
   cfg.numAttrs = n_attrs.load();
   cudaError_t e = cudaLaunchKernelEx(&cfg, route_permute_kernel<NPL>, logits, bias, ids_in, T, E,
                                      a, w, ids, probs, wscale, C, counts, seg_end, active,
-                                     num_active, r2r, route_to_row, status, bar);
+                                     num_active, r2r, route_to_row, status, bar, ba);
   if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
     (void)cudaGetLastError();
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, route_permute_kernel<NPL>, logits, bias, ids_in, T, E, a, w, ids,
                            probs, wscale, C, counts, seg_end, active, num_active, r2r,
-                           route_to_row, status, bar);
+                           route_to_row, status, bar, ba);
     if (e == cudaSuccess) n_attrs.store(1);
   }
   return e;
 }
 
+// Test hook state (see moe_test_force_wait_timeout): off by default.
+std::atomic<int> g_force_timeout{0};
+std::atomic<long long> g_force_timeout_ns{0};
+
 }  // namespace
+
+int set_wait_timeout_test(int enable, long long limit_ns) {
+  if (enable) g_force_timeout_ns.store(limit_ns > 0 ? limit_ns : 1);
+  return g_force_timeout.exchange(enable ? 1 : 0);
+}
 
 bool route_permute_ok(int E) { return E >= 1 && E <= kFusedWarps * 32; }
 
@@ -230,11 +244,13 @@ cudaError_t launch_route_permute(const void* logits, const float* bias, const in
   cudaError_t e = cudaSuccess;
   const RouteArgs a = rt::route_args(p, probs, wscale);
   const int npl = (E + 31) / 32;
+  BarrierArgs ba{0, tc::kTimeoutNs};
+  if (g_force_timeout.load()) ba = BarrierArgs{1, (uint64_t)g_force_timeout_ns.load()};
   auto go = [&](auto tag) {
     constexpr int N = decltype(tag)::value;
     return launch_npl<N>(logits, bias, ids_in, T, E, a, w, ids, probs, wscale, C, counts, seg_end,
                          active, num_active, row_to_route, route_to_row, status, bar, smem, grid,
-                         s);
+                         ba, s);
   };
   if (npl <= 1) e = go(std::integral_constant<int, 1>{});
   else if (npl <= 2) e = go(std::integral_constant<int, 2>{});

@@ -68,7 +68,7 @@ _SIGNATURES = {
     "moe_ffn_forward": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp,
                         _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_ffn_forward_host": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp,
-                             _vp, _vp, _vp, _sz, _vp],
+                             _vp, _vp, _vp, _vp, _vp, _sz, _vp],
     "moe_shared_expert_mlp": [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _vp, _sz, _vp],
     "moe_ffn_forward_local": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i,
                               _vp, _vp, _vp, _sz, _vp],
@@ -85,6 +85,7 @@ _SIGNATURES = {
     "moe_status_string": [_i],
     "moe_launch_count": [],
     "moe_set_gemm_simt": [_i],
+    "moe_test_force_wait_timeout": [_i, ctypes.c_longlong],
 }
 _RESTYPES = {"moe_workspace_size": _sz, "moe_permute_workspace_size": _sz,
              "moe_workspace_size_host": _sz, "moe_shared_expert_workspace_size": _sz,
@@ -586,11 +587,14 @@ def moe_workspace_size_host(T, H, F, E, K, dtype=MOE_BF16) -> int:
 
 def moe_ffn_forward_host(hidden_host, logits_host, w_gate_up, w_down, p: RouteParams,
                          act: ActParams, out_host, ws, correction_bias=None, expert_ids=None,
-                         b_gate_up=None, b_down=None):
+                         b_gate_up=None, b_down=None, router_probs=None, weight_scale=None):
     """moe_ffn_forward with hidden / logits / out in host memory (pinned for
-    asynchronous copies); asynchronous on the current stream."""
+    asynchronous copies); asynchronous on the current stream.  router_probs /
+    weight_scale (device tensors) receive the MoERouter slice outputs when
+    ``p`` has a local slice."""
     lib = load_library()
-    _cuda(w_gate_up, w_down, correction_bias, expert_ids, b_gate_up, b_down, ws)
+    _cuda(w_gate_up, w_down, correction_bias, expert_ids, b_gate_up, b_down, ws, router_probs,
+          weight_scale)
     for t in (hidden_host, logits_host, out_host):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError("moe_ffn_forward_host takes contiguous host tensors")
@@ -601,8 +605,8 @@ def moe_ffn_forward_host(hidden_host, logits_host, w_gate_up, w_down, p: RoutePa
                                     _p(correction_bias), _p(expert_ids), _p(b_gate_up),
                                     _p(b_down), T, H, F, E, _dt(hidden_host),
                                     ctypes.byref(_rp(p, logits_host)),
-                                    ctypes.byref(act), _p(out_host), _p(ws), ws.numel(),
-                                    _stream()))
+                                    ctypes.byref(act), _p(out_host), _p(router_probs),
+                                    _p(weight_scale), _p(ws), ws.numel(), _stream()))
     return out_host
 
 
@@ -621,6 +625,12 @@ def moe_launch_count() -> int:
 
 def moe_set_gemm_simt(enable: bool) -> bool:
     return bool(load_library().moe_set_gemm_simt(int(bool(enable))))
+
+
+def moe_test_force_wait_timeout(enable: bool, limit_ns: int = 50_000_000) -> bool:
+    """Test hook: make the fused route launch's grid barriers wait for an
+    arrival that never comes and give up after ``limit_ns`` (see moe.h)."""
+    return bool(load_library().moe_test_force_wait_timeout(int(bool(enable)), int(limit_ns)))
 
 
 def config_params(cfg):
