@@ -38,7 +38,8 @@ def pytest_terminal_summary(terminalreporter):
 
     tr = terminalreporter
     tr.section("parity figures (layer outputs against the exact oracle value)")
-    for what, r in parity_log:
+    # the full-size workloads last, so that they end the log
+    for what, r in sorted(parity_log, key=lambda x: x[0].startswith("full")):
         if r.get("dtype") == "f32":
             tr.write_line(f"{what}: f32 max|err|/max|ref| {r['max_err_over_max_ref']:.2e}")
             continue
