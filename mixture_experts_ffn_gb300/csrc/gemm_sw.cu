@@ -1,0 +1,650 @@
+// Grouped GEMM with the weights as the MMA's M operand and the tokens as its
+// N operand, on SM pairs (tcgen05.mma.cta_group::2), for the expert-segmented
+// row layout of TileOPs "MoE Operators", MoEGroupedGemmFwdOp:
+//   out[rows of e] = act(a[rows of e] @ w[e]^T (+ bias[e]))
+// with the gated activation (silu_and_mul / gelu_and_mul / clamped SwiGLU over
+// stacked or interleaved gate/up rows) fused into the epilogue.
+//
+// Why this orientation: an expert's segment holds a few hundred rows whose
+// count is arbitrary.  As the MMA's M dimension (128 rows per tile) a
+// segment pads to a multiple of 128 (28% more MMA work on the DeepSeek-V3-
+// style routing, 100% on gpt-oss-style); as its N dimension it pads to a
+// multiple of 16 (5% and 12%), and tcgen05.mma time scales with N (N/2
+// cycles per K16 step from N = 96 up, measured).  The weights fill M with
+// no padding: 256 weight rows per CTA pair.
+//
+// Work decomposition
+//   pair tile = 256 weight rows (128 per CTA) x one token chunk of an expert
+//   (N <= 256 tokens, a multiple of 16; an expert of n rows is cut into
+//   ceil(n / 256) chunks of equal size rounded up to 16); k-block = 64.
+//   Each CTA loads its 128 weight rows (TMA, 16 KB) and half of the chunk's
+//   token rows (TMA tile::gather4 through the row map, N/2 x 128 B) per
+//   k-block into a 6-stage ring; both CTAs' copies complete on the leader's
+//   barrier, and the leader issues M256 x N x K16 MMAs into the pair's TMEM.
+//   Gated modes: a 5-D tensor map loads each group of 8 gate rows next to its
+//   8 up rows, so TMEM lane l (gate) and lane l ^ 8 (up) of one warp hold the
+//   two halves of one activation column; 64 activation columns per CTA.
+// Roles (192 threads per CTA)
+//   warp 0       : producer -- lane 0 the weight copy (and, in the leader, the
+//                  stage's expected bytes), every lane one gather4 of 4 rows
+//   warp 1       : TMEM allocation (pair); lane 0 of the leader issues MMAs
+//   warps 2..5   : epilogue of the CTA's 128 TMEM lanes (bias, activation,
+//                  rounding, transposed staging and TMA stores)
+// Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
+// tile overlap the main loop of the next.  Every wait is bounded (2 s); on a
+// timeout the block latches the timeout bit, drains what it issued and frees
+// TMEM.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstdlib>
+#include <type_traits>
+
+#include "common.cuh"
+#include "gemm_epilogue.cuh"
+#include "tc_ptx.cuh"
+#include "tmap.h"
+
+namespace moe {
+namespace {
+
+using namespace tc;
+
+constexpr int BK = 64;
+constexpr int ROWS = 128;                        // weight rows per CTA
+constexpr int NMAX = 256;                        // tokens per chunk (MMA N)
+constexpr int STAGES = 6;
+constexpr int A_BYTES = ROWS * BK * 2;           // 16 KB of weights
+constexpr int B_BYTES = (NMAX / 2) * BK * 2;     // up to 16 KB of tokens (half the chunk)
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB
+constexpr int TMEM_COLS = 512;
+constexpr int NUM_THREADS = 192;
+
+// Accumulator layouts: plain (lane = weight row = output column), or gated
+// groups of 8 gate rows then their 8 up rows.
+enum SwMode { kSwPlain = 0, kSwGated = 1 };
+
+struct SwShared {
+  uint64_t full[STAGES];   // leader: both CTAs' copies of a stage complete here
+  uint64_t empty[STAGES];  // both: the leader's MMA commit frees the stage
+  uint64_t tfull[2];       // both: accumulator ready
+  uint64_t tempty[2];      // leader: both CTAs' epilogues drained the accumulator
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int prefix[kMaxExperts + 1];
+  int scan_tmp[33];
+};
+constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + OUT_BYTES + sizeof(SwShared) + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+// Weight box into this CTA's shared memory, completing on the leader's barrier.
+__device__ __forceinline__ void tma_w3(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                       int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_w5(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                       int c3, int c4) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(0), "r"(0), "r"(c3), "r"(c4)
+      : "memory");
+}
+// Four rows (r0..r3) x 64 columns from k0 of a row-major 2-D tensor, placed as
+// consecutive 128-byte rows at dst (the 128-byte swizzle follows the shared
+// address, so a group of 4 rows lands where a tiled box would put them).
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint32_t bar, int k0,
+                                            int r0, int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(k0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+      : "memory");
+}
+// the four K16 MMAs of a k-block and the commit that frees the stage in both CTAs
+__device__ __forceinline__ void umma2_kblock(uint32_t d_tmem, uint64_t ad, uint64_t bd,
+                                             uint32_t idesc, uint32_t accumulate, uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "setp.eq.b32 t, %4, %4;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %6, %7, %3, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %8, %9, %3, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %10, %11, %3, t;\n\t"
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%5], %12;\n\t}" ::"r"(d_tmem),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate), "r"(bar), "l"(ad + 2), "l"(bd + 2),
+      "l"(ad + 4), "l"(bd + 4), "l"(ad + 6), "l"(bd + 6), "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void umma2_commit_both(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(su32(bar)),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void umma2_commit_self(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          su32(bar))
+      : "memory");
+}
+// Instruction descriptor, kind::f16 with f32 accumulation, both operands
+// K-major: bf16 (or float16 when f16) A and B, M x N.
+__device__ __forceinline__ uint32_t idesc_sw(int M, int N, int f16) {
+  const uint32_t fmt = f16 ? 0u : ((1u << 7) | (1u << 10));
+  return (1u << 4) | fmt | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// One pair tile: expert e, weight-row tile nt (256 rows: 128 per CTA), and a
+// chunk of the expert's rows [m0, m0 + nv) as the N dimension (N columns,
+// nv <= N <= 256, N a multiple of 16 and at least 32).  nv == 0: an empty
+// tile (every role skips it alike).
+struct SwTile {
+  int e, nt, m0, nv, N;
+};
+
+// Tile t of the list built by build_tile_prefix(.., NMAX, n_ftiles, ..):
+// expert e owns n_ftiles * ce tiles, ce = ceil(n / 256) chunks; inside an
+// expert the chunk index runs fastest, so the pairs that share a weight tile
+// run together and the L2 serves its re-reads.
+__device__ __forceinline__ SwTile sw_decode(int t, const int* prefix, const int32_t* seg_end,
+                                            int E, int M, int n_ftiles, int stride) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {  // last e with prefix[e] <= t (skips empty experts)
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  int s, u;
+  seg_bounds(seg_end, lo, M, stride, s, u);
+  const int n = u - s;
+  const int ce = (n + NMAX - 1) / NMAX;
+  const int local = t - prefix[lo];
+  SwTile r;
+  r.e = lo;
+  r.nt = local / ce;
+  const int ci = local % ce;
+  const int per = (((n + ce - 1) / ce) + 15) & ~15;
+  const int start = min(ci * per, n);
+  r.m0 = s + start;
+  r.nv = min(per, n - start);
+  r.N = max(32, (r.nv + 15) & ~15);
+  return r;
+}
+
+template <bool F16>
+__device__ __forceinline__ void st16(__nv_bfloat16* p, float v) {
+  if constexpr (F16)
+    *reinterpret_cast<__half*>(p) = __float2half_rn(v);
+  else
+    *p = __float2bfloat16_rn(v);
+}
+template <bool F16>
+__device__ __forceinline__ uint16_t bits16(float v) {
+  if constexpr (F16)
+    return __half_as_ushort(__float2half_rn(v));
+  else
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+__device__ __forceinline__ void sts16(uint32_t addr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+template <int ACT>
+__device__ __forceinline__ float act1(float x) {
+  if constexpr (ACT == MOE_ACT_RELU) return fmaxf(x, 0.0f);
+  else if constexpr (ACT == MOE_ACT_GELU) return gelu_f(x);
+  else if constexpr (ACT == MOE_ACT_SILU) return x * fast_sigmoid(x);
+  else return x;
+}
+
+// Plain epilogue of the calling warp: TMEM lane l holds output column
+// f0 + l for the tile's tokens (TMEM column j = token m0 + j).  32 tokens at a
+// time: a whole 32 x 32 box goes through swizzled staging and one TMA store;
+// a ragged tail (< 32 tokens) is stored row by row (64 contiguous bytes per
+// token).  Columns at or past Nout are not written.
+template <int ACT, bool F16>
+__device__ __forceinline__ void sw_drain_plain(uint32_t tbase, int nv, int m0, int f0, int Nout,
+                                               const __nv_bfloat16* __restrict__ bias_e,
+                                               const CUtensorMap* tm_out, int tma_out,
+                                               __nv_bfloat16* __restrict__ out, uint8_t* obufs,
+                                               int& obuf, int lane) {
+  const int f = f0 + lane;
+  const bool fok = f < Nout;
+  const float b = bias_e && fok ? ld16<F16>(bias_e + f) : 0.0f;
+#pragma unroll 1
+  for (int c0 = 0; c0 < nv; c0 += 32) {
+    uint32_t r[32];
+    tmem_ld32(tbase + (uint32_t)c0, r);
+    tmem_wait_ld();
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = act1<ACT>(__uint_as_float(r[i]) + b);
+    const int nval = min(32, nv - c0);
+    if (tma_out && nval == 32 && f0 < Nout) {
+      uint8_t* buf = obufs + obuf * OUT_BUF_BYTES;
+      if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer
+      __syncwarp();
+      // token i, column lane: row i of the box, 64-byte swizzle
+      const uint32_t base = su32(buf) + (uint32_t)((lane & 7) * 2);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        sts16(base + i * 64 + ((((lane >> 3) ^ ((i >> 1) & 3))) << 4), bits16<F16>(v[i]));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm_out, buf, f0, m0 + c0);
+        bulk_commit();
+      }
+      obuf ^= 1;
+    } else if (fok) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (i < nval) st16<F16>(out + (size_t)(m0 + c0 + i) * Nout + f, v[i]);
+    }
+  }
+}
+
+// Gated epilogue of the calling warp: lanes 0..7 and 16..23 hold gate rows,
+// lanes l ^ 8 the matching up rows, of the 16 activation columns f0 ..
+// f0 + 15 (lane l: column f0 + 8 (l >> 4) + (l & 7)).  Per 32 tokens the two
+// partners swap half of their values (shfl_xor 8): the gate lane then holds
+// (gate, up) of tokens 0..15, the up lane those of tokens 16..31, and each
+// computes its 16 activations.  Whole 32-token boxes go through staging
+// (16 columns x 32 tokens) and one TMA store; a ragged tail is stored
+// directly.  Bias: b[gate row] / b[up row] of the lane's own weight row.
+template <int ACT, bool F16>
+__device__ __forceinline__ void sw_drain_gated(uint32_t tbase, int nv, int m0, int f0, int Nout,
+                                               int F, int interleaved,
+                                               const __nv_bfloat16* __restrict__ bias_e,
+                                               float limit, float alpha, float beta,
+                                               const CUtensorMap* tm_out, int tma_out,
+                                               __nv_bfloat16* __restrict__ out, uint8_t* obufs,
+                                               int& obuf, int lane) {
+  const bool is_gate = (lane & 8) == 0;
+  const int fl = 8 * (lane >> 4) + (lane & 7);  // column within the warp's 16
+  const int f = f0 + fl;
+  const bool fok = f < Nout;
+  float b = 0.0f;
+  if (bias_e && fok) {
+    const int row = interleaved ? 2 * f + (is_gate ? 0 : 1) : (is_gate ? f : F + f);
+    b = ld16<F16>(bias_e + row);
+  }
+#pragma unroll 1
+  for (int c0 = 0; c0 < nv; c0 += 32) {
+    uint32_t r[32];
+    tmem_ld32(tbase + (uint32_t)c0, r);
+    tmem_wait_ld();
+    float a[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float lo = __uint_as_float(r[i]) + b, hi = __uint_as_float(r[16 + i]) + b;
+      const float recv = __shfl_xor_sync(0xffffffffu, is_gate ? hi : lo, 8);
+      a[i] = is_gate ? gated<ACT>(lo, recv, limit, alpha, beta)
+                     : gated<ACT>(recv, hi, limit, alpha, beta);
+    }
+    const int tok0 = is_gate ? 0 : 16;  // this lane's tokens: c0 + tok0 + i
+    const int nval = min(32, nv - c0);
+    if (tma_out && nval == 32 && f0 < Nout) {
+      uint8_t* buf = obufs + obuf * OUT_BUF_BYTES;
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+      const uint32_t base = su32(buf) + (uint32_t)(tok0 * 32 + fl * 2);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sts16(base + i * 32, bits16<F16>(a[i]));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tm_out, buf, f0, m0 + c0);
+        bulk_commit();
+      }
+      obuf ^= 1;
+    } else if (fok) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        if (tok0 + i < nval) st16<F16>(out + (size_t)(m0 + c0 + tok0 + i) * Nout + f, a[i]);
+    }
+  }
+}
+
+// tm_w: weights, 3-D [E][N1][K] box {64, 128, 1} (plain) or the 5-D gated view
+// [E][F/8][2][8][K] box {64, 8, 2, 8, 1}; tm_a: the token rows' source, 2-D
+// [rows][K] with a one-row box for gather4.  Row r of the segmented row space
+// is source row grows[r] / gdiv (the hidden states read through the
+// permutation; rows with an out-of-range entry read row 0) or, without
+// grows, row r itself.
+template <int MODE, int ACT, bool F16>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_sw_kernel(const __grid_constant__ CUtensorMap tm_w,
+                   const __grid_constant__ CUtensorMap tm_a,
+                   const __grid_constant__ CUtensorMap tm_out, int tma_out,
+                   const __nv_bfloat16* __restrict__ bias, const int32_t* __restrict__ seg_end,
+                   int M, int Nout, int N1, int K, int E, int interleaved, float limit,
+                   float alpha, float beta, __nv_bfloat16* __restrict__ out, int* status,
+                   const int32_t* __restrict__ grows, int gdiv, int src_rows, int seg_stride) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* out_stage = smem + (size_t)STAGES * STAGE_BYTES;  // 1024-byte aligned
+  SwShared* sh = reinterpret_cast<SwShared*>(out_stage + OUT_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  volatile int* abort_flag = &sh->abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sh->full[s], 1);  // the leader's expect-tx arrival (+ both CTAs' bytes)
+      mbar_init(&sh->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&sh->tfull[a], 1);
+      mbar_init(&sh->tempty[a], 2 * 128);
+    }
+    mbar_init(&sh->drain, 1);
+    sh->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     su32(&sh->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  const int n_ftiles = MODE == kSwPlain ? (Nout + 2 * ROWS - 1) / (2 * ROWS)
+                                        : (Nout + ROWS - 1) / ROWS;
+  // everything above overlaps the previous launch; seg_end and the operands
+  // are read only after this
+  pdl_wait();
+  const int total =
+      build_tile_prefix(seg_end, E, M, NMAX, n_ftiles, sh->prefix, sh->scan_tmp, seg_stride);
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = sh->tmem_base;
+  const int nkb = (K + BK - 1) / BK;
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  auto decode = [&](int t) { return sw_decode(t, sh->prefix, seg_end, E, M, n_ftiles, seg_stride); };
+
+  if (warp == 0) {
+    // ------------------------------------------------ producer (both CTAs)
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued[STAGES];
+    for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+    bool ok = true;
+    for (int tile = pair; tile < total && ok; tile += npairs) {
+      const SwTile st = decode(tile);
+      if (st.nv == 0) continue;
+      const int half = st.N >> 1;              // token rows of this CTA
+      const bool active = 4 * lane < half;     // lanes with a gather4 of 4 rows
+      int rr[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        // padding tokens (past nv) repeat the chunk's last row: their columns
+        // are never stored
+        const int j = min((int)rank * half + 4 * lane + u, st.nv - 1);
+        const int row = st.m0 + j;
+        int src = row;
+        if (grows) {
+          const int rt = active ? grows[row] : 0;
+          src = rt >= 0 && rt / gdiv < src_rows ? rt / gdiv : 0;
+        }
+        rr[u] = src;
+      }
+      const uint32_t tx = (uint32_t)(A_BYTES + half * BK * 2);
+      for (int kb = 0; kb < nkb; ++kb) {
+        int good = 1;
+        if (lane == 0) good = wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status) ? 1 : 0;
+        good = __shfl_sync(0xffffffffu, good, 0);
+        if (!good) { ok = false; break; }
+        uint8_t* a_dst = smem + (size_t)stage * STAGE_BYTES;
+        uint8_t* b_dst = a_dst + A_BYTES;
+        const uint32_t bar = map_to_rank(su32(&sh->full[stage]), 0);
+        const int k0 = kb * BK;
+        if (lane == 0) {
+          if (leader) mbar_expect_tx(&sh->full[stage], 2 * tx);
+          if constexpr (MODE == kSwPlain)
+            tma_w3(a_dst, &tm_w, bar, k0, st.nt * 2 * ROWS + ROWS * (int)rank, st.e);
+          else
+            tma_w5(a_dst, &tm_w, bar, k0, st.nt * 16 + 8 * (int)rank, st.e);
+          ++issued[stage];
+        }
+        if (active)
+          tma_gather4(b_dst + lane * 4 * BK * 2, &tm_a, bar, k0, rr[0], rr[1], rr[2], rr[3]);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok && leader && lane == 0) {  // both CTAs' copies complete on the leader's barriers
+      for (int s = 0; s < STAGES; ++s)
+        if (issued[s]) drain_wait(&sh->full[s], (issued[s] - 1u) & 1u);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ------------------------------------------------ MMA issuer (leader)
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, aphase = 0;
+      bool ok = true, any = false;
+      const uint64_t adesc0 = sw128_desc(su32(smem));
+      const uint64_t bdesc0 = sw128_desc(su32(smem + A_BYTES));
+      uint32_t empty_addr[STAGES];
+      for (int s = 0; s < STAGES; ++s) empty_addr[s] = su32(&sh->empty[s]);
+      for (int tile = pair; tile < total && ok; tile += npairs) {
+        const SwTile st = decode(tile);
+        if (st.nv == 0) continue;
+        const uint32_t idesc = idesc_sw(2 * ROWS, st.N, F16 ? 1 : 0);
+        if (!wait_fast(&sh->tempty[acc], aphase ^ 1u, abort_flag, status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * NMAX);
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!wait_fast(&sh->full[stage], phase, abort_flag, status)) { ok = false; break; }
+          tc_fence_after();
+          const uint64_t off = (uint64_t)((stage * STAGE_BYTES) >> 4);
+          umma2_kblock(d_tmem, adesc0 + off, bdesc0 + off, idesc, kb != 0 ? 1u : 0u,
+                       empty_addr[stage]);
+          any = true;
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma2_commit_both(&sh->tfull[acc]);
+        if (++acc == 2) { acc = 0; aphase ^= 1u; }
+      }
+      if (!ok && any) {
+        umma2_commit_self(&sh->drain);
+        drain_wait(&sh->drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (both CTAs)
+    const int quad = warp & 3;
+    int acc = 0;
+    uint32_t aphase = 0;
+    const uint32_t tempty_remote[2] = {map_to_rank(su32(&sh->tempty[0]), 0),
+                                       map_to_rank(su32(&sh->tempty[1]), 0)};
+    uint8_t* obufs = out_stage + quad * 2 * OUT_BUF_BYTES;
+    int obuf = 0;
+    for (int tile = pair; tile < total; tile += npairs) {
+      const SwTile st = decode(tile);
+      if (st.nv == 0) continue;
+      if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
+      tc_fence_after();
+      const uint32_t tb =
+          tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * NMAX);
+      const __nv_bfloat16* be = bias ? bias + (size_t)st.e * N1 : nullptr;
+      if constexpr (MODE == kSwPlain)
+        sw_drain_plain<ACT, F16>(tb, st.nv, st.m0, st.nt * 2 * ROWS + ROWS * (int)rank + 32 * quad,
+                                 Nout, be, &tm_out, tma_out, out, obufs, obuf, lane);
+      else
+        sw_drain_gated<ACT, F16>(tb, st.nv, st.m0, st.nt * ROWS + (ROWS / 2) * (int)rank + 16 * quad,
+                                 Nout, Nout, interleaved, be, limit, alpha, beta, &tm_out, tma_out,
+                                 out, obufs, obuf, lane);
+      tc_fence_before();
+      mbar_arrive_remote(tempty_remote[acc]);
+      if (++acc == 2) { acc = 0; aphase ^= 1u; }
+    }
+    if (lane == 0) bulk_wait_all();  // every staged box written before the pair exits
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA frees TMEM or exits while its peer still works
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------ host side
+namespace {
+
+template <int MODE, int ACT, bool F16>
+const void* sw_kernel_ptr() {
+  return (const void*)gemm_sw_kernel<MODE, ACT, F16>;
+}
+
+template <bool F16>
+const void* pick_sw(int mode, int kind) {
+  if (mode == kSwPlain) {
+    switch (kind) {
+      case MOE_ACT_RELU: return sw_kernel_ptr<kSwPlain, MOE_ACT_RELU, F16>();
+      case MOE_ACT_GELU: return sw_kernel_ptr<kSwPlain, MOE_ACT_GELU, F16>();
+      case MOE_ACT_SILU: return sw_kernel_ptr<kSwPlain, MOE_ACT_SILU, F16>();
+      default: return sw_kernel_ptr<kSwPlain, MOE_ACT_IDENTITY, F16>();
+    }
+  }
+  switch (kind) {
+    case MOE_ACT_SWIGLU: return sw_kernel_ptr<kSwGated, MOE_ACT_SWIGLU, F16>();
+    case MOE_ACT_GELU_AND_MUL: return sw_kernel_ptr<kSwGated, MOE_ACT_GELU_AND_MUL, F16>();
+    default: return sw_kernel_ptr<kSwGated, MOE_ACT_SILU_AND_MUL, F16>();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const int32_t* seg_end,
+                           int M, int N, int K, int E, const moe_act_params* act, void* out,
+                           int* status, cudaStream_t s, const int32_t* gather_rows,
+                           int gather_div, int gather_src_rows, int seg_stride, bool f16) {
+  if (M == 0 || N == 0) return cudaSuccess;
+  int mode = kSwPlain, kind = MOE_ACT_IDENTITY, N1 = N, inter = 0;
+  float limit = 0.f, alpha = 1.f, beta = 0.f;
+  if (act) kind = act->kind;
+  if (act && act_is_gated(act->kind)) {
+    mode = kSwGated;
+    inter = (kind == MOE_ACT_SWIGLU && act->swiglu_fusion == 1) ? 1 : 0;
+    N1 = 2 * N;
+    limit = act->limit;
+    alpha = act->alpha;
+    beta = act->beta;
+  }
+  if (N % 8 != 0 || K % 8 != 0) return cudaErrorInvalidValue;
+  CUtensorMap mw, ma, mo;
+  const uint64_t K2 = (uint64_t)K * 2;
+  if (mode == kSwPlain) {
+    cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N1, (cuuint64_t)E};
+    cuuint64_t str[2] = {K2, (cuuint64_t)N1 * K2};
+    cuuint32_t box[3] = {BK, ROWS, 1};
+    if (!tmap::encode_bf16(&mw, w, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, f16))
+      return cudaErrorInvalidValue;
+  } else {
+    // groups of 8 activation columns: their 8 gate rows, then their 8 up rows
+    // (stacked: up rows F below the gate rows; interleaved: rows 2j, 2j + 1)
+    cuuint64_t dims[5] = {(cuuint64_t)K, 8, 2, (cuuint64_t)N / 8, (cuuint64_t)E};
+    cuuint64_t st_stacked[4] = {K2, (cuuint64_t)N * K2, 8 * K2, (cuuint64_t)N1 * K2};
+    cuuint64_t st_inter[4] = {2 * K2, K2, 16 * K2, (cuuint64_t)N1 * K2};
+    cuuint32_t box[5] = {BK, 8, 2, 8, 1};
+    if (!tmap::encode_bf16(&mw, w, 5, dims, inter ? st_inter : st_stacked, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, f16))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const int rows = gather_rows ? gather_src_rows : M;
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)std::max(rows, 1)};
+    cuuint64_t str[1] = {K2};
+    cuuint32_t box[2] = {BK, 1};
+    if (!tmap::encode_bf16(&ma, a, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, f16))
+      return cudaErrorInvalidValue;
+  }
+  // staged output boxes: 32 columns x 32 rows (64-byte swizzle), or 16 x 32
+  // for the gated mode; rows stored directly when the output's base or pitch
+  // is not 16-byte aligned
+  int tma_out = 0;
+  if ((reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t str[1] = {(cuuint64_t)N * 2};
+    cuuint32_t box[2] = {mode == kSwPlain ? 32u : 16u, 32u};
+    tma_out = tmap::encode_bf16(&mo, out, 2, dims, str, box,
+                                mode == kSwPlain ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                 : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                f16)
+                  ? 1
+                  : 0;
+  }
+  if (!tma_out) mo = mw;  // unused
+  const void* kern = f16 ? pick_sw<true>(mode, kind) : pick_sw<false>(mode, kind);
+  set_smem_limit(kern, (int)kSmemBytes);
+  const int n_ftiles = mode == kSwPlain ? (N + 2 * ROWS - 1) / (2 * ROWS) : (N + ROWS - 1) / ROWS;
+  const long long max_tiles = (long long)((M + NMAX - 1) / NMAX + E) * n_ftiles;
+  const int pairs = (int)std::max<long long>(1, std::min<long long>(max_tiles, num_sms() / 2));
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const __nv_bfloat16* bias_p = static_cast<const __nv_bfloat16*>(bias);
+  __nv_bfloat16* out_p = static_cast<__nv_bfloat16*>(out);
+  void* args[] = {&mw, &ma, &mo, &tma_out, &bias_p, &seg_end, &M, &N, &N1, &K, &E, &inter,
+                  &limit, &alpha, &beta, &out_p, &status, &gather_rows, &gather_div,
+                  &gather_src_rows, &seg_stride};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
+  count_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace moe

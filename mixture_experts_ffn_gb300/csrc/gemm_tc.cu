@@ -357,17 +357,20 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            int gather_div, int gather_src_rows, int seg_stride,
                            const SplitUp* split, bool f16) {
   if (M == 0 || N == 0) return cudaSuccess;
-  // The two-SM (cta_group::2) kernel with MOE_TC_KERNEL=2sm.  Its SMs load a
-  // third fewer bytes per MMA on 256-row pair tiles, but on the routed
-  // workloads measured it is level with this kernel or slower (short
-  // segments, and its gathered mode forwards the peer's row copies through a
-  // second barrier), so it is not the default.
-  static const bool two_sm = [] {
+  // The default is the weights-as-M kernel on SM pairs (gemm_sw.cu), which
+  // pads an expert's rows to 16 instead of 128; this one-SM kernel takes the
+  // split gate/up weights, and every call with MOE_TC_KERNEL=1sm (kept to
+  // check the two against each other).  MOE_TC_KERNEL=2sm: the row-tile
+  // kernel on SM pairs (gemm_tc2.cu).
+  static const int which = [] {
     const char* v = getenv("MOE_TC_KERNEL");
-    return v && v[0] == '2';
+    return v && v[0] == '1' ? 1 : v && v[0] == '2' ? 2 : 0;
   }();
   const bool gather = gather_rows != nullptr;
-  if (two_sm && num_sms() >= 2 && !split && !f16)
+  if (which == 0 && !split && num_sms() >= 2 && N % 8 == 0 && K % 8 == 0)
+    return launch_gemm_sw(a, w, bias, seg_end, M, N, K, E, act, out, status, s, gather_rows,
+                          gather_div, gather_src_rows, seg_stride, f16);
+  if (which == 2 && num_sms() >= 2 && !split && !f16)
     return launch_gemm_tc2(a, w, bias, seg_end, M, N, K, E, act, out, status, s, gather_rows,
                            gather_div, gather_src_rows, seg_stride);
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;

@@ -166,6 +166,13 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            int gather_div = 1, int gather_src_rows = 0, int seg_stride = 0,
                            const SplitUp* split = nullptr, bool f16 = false);
 
+// The weights-as-M tcgen05 grouped GEMM on SM pairs (gemm_sw.cu): the same
+// contract as launch_gemm_tc without split weights; N and K multiples of 8.
+cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const int32_t* seg_end,
+                           int M, int N, int K, int E, const moe_act_params* act, void* out,
+                           int* status, cudaStream_t s, const int32_t* gather_rows,
+                           int gather_div, int gather_src_rows, int seg_stride, bool f16);
+
 // block-scaled FP8 grouped GEMM over a masked slab (e4m3 operands, fp32
 // scales per row x 128 K of a and per 128 x 128 block of b, bf16 out)
 cudaError_t launch_gemm_fp8(const void* a, const float* a_scale, const void* b,

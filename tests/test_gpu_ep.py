@@ -69,8 +69,11 @@ def test_expert_parallel_ranks_sum_to_the_layer(moe, name, over, lc):
     # all-reduce of their results would), so the float32 sum is compared with
     # the oracle's sum of the exact rank outputs, each rank's roundings in the
     # budget; and with the layer (rounded once) within those extra roundings
+    # (a float32 sum of rounded rank outputs is not itself a layer output of
+    # the method, so the stated bound does not apply to it; the secondary
+    # bound with every rank's roundings does)
     assert_layer_close(np_(total), want_total, cfg.dtype, f"ep {name} sum of ranks",
-                       budget=parts_budget, final_cast=False)
+                       budget=parts_budget, stated=False, final_cast=False)
     err = np_(total) - np_(full)
     rms = float(np.sqrt(np.mean(np_(full) ** 2)))
     assert float(np.sqrt(np.mean(err ** 2))) <= 5e-3 * rms, f"{name} sum vs layer"

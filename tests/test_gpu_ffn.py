@@ -56,12 +56,6 @@ def oracle_forward(cfg, ref, tokens=None):
                          **act_kwargs(cfg))
 
 
-# Cases whose bare max|err| exceeds the stated bf16 bound of 2e-2 * RMS(ref)
-# (against the exact, unrounded layer output); they assert the secondary
-# bound instead.  Every other bf16 case asserts the stated bound as written.
-STATED_BOUND_NOT_MET = set()
-
-
 def check(moe, cfg, tokens=None, what=None):
     inp, ref = make(cfg)
     out, tw, ti, probs, wsc, status = run_forward(moe, cfg, inp)
@@ -83,8 +77,7 @@ def check(moe, cfg, tokens=None, what=None):
     tok = r["tokens"]
     got = np_(out)[tok]
     what = what or cfg.name
-    return assert_forward_close(got, r, cfg.dtype, what,
-                                stated=what not in STATED_BOUND_NOT_MET), out
+    return assert_forward_close(got, r, cfg.dtype, what), out
 
 
 SMALL = {
@@ -163,10 +156,8 @@ def test_indexed_path_matches_staged(moe):
     y_st = moe.moe_combine(y, w, perm["route_to_row"])
     torch.cuda.synchronize()
     r = oracle_forward(cfg, ref)
-    assert_forward_close(np_(y_idx), r, "bf16", "indexed vs oracle",
-                         stated="indexed vs oracle" not in STATED_BOUND_NOT_MET)
-    assert_forward_close(np_(y_st), r, "bf16", "staged vs oracle",
-                         stated="staged vs oracle" not in STATED_BOUND_NOT_MET)
+    assert_forward_close(np_(y_idx), r, "bf16", "indexed vs oracle")
+    assert_forward_close(np_(y_st), r, "bf16", "staged vs oracle")
 
 
 def test_forward_is_deterministic(moe):
