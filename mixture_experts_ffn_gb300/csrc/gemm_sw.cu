@@ -50,13 +50,16 @@ namespace {
 
 using namespace tc;
 
-constexpr int BK = 64;
+constexpr int BK = 64;                           // one 128-byte swizzle atom of K
+constexpr int KA = 2;                            // K atoms per ring stage
+constexpr int BKS = BK * KA;                     // K per stage
 constexpr int ROWS = 128;                        // weight rows per CTA
 constexpr int NMAX = 256;                        // tokens per chunk (MMA N)
-constexpr int STAGES = 6;
-constexpr int A_BYTES = ROWS * BK * 2;           // 16 KB of weights
-constexpr int B_BYTES = (NMAX / 2) * BK * 2;     // up to 16 KB of tokens (half the chunk)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 32 KB
+constexpr int STAGES = 3;
+constexpr int ATOM_BYTES = ROWS * BK * 2;        // 16 KB: 128 rows of one atom
+constexpr int A_BYTES = KA * ATOM_BYTES;         // 32 KB of weights per stage
+constexpr int B_BYTES = KA * (NMAX / 2) * BK * 2;  // up to 32 KB of tokens (half the chunk)
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 64 KB
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
 
@@ -66,6 +69,7 @@ enum SwMode { kSwPlain = 0, kSwGated = 1 };
 
 struct SwShared {
   uint64_t full[STAGES];   // leader: both CTAs' copies of a stage complete here
+  uint64_t afull[STAGES];  // peer, cp.async rows: this CTA's rows of a stage landed
   uint64_t empty[STAGES];  // both: the leader's MMA commit frees the stage
   uint64_t tfull[2];       // both: accumulator ready
   uint64_t tempty[2];      // leader: both CTAs' epilogues drained the accumulator
@@ -98,37 +102,39 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
                : "memory");
 }
-// Weight box into this CTA's shared memory, completing on the leader's barrier.
-__device__ __forceinline__ void tma_w3(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
-                                       int c1, int c2) {
+// TMA loads into this CTA's shared memory that complete on the leader's
+// barrier (shared::cluster address); coordinates innermost first.
+__device__ __forceinline__ void tma2_2d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                        int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma2_3d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                        int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
       "bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(su32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-__device__ __forceinline__ void tma_w5(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
-                                       int c3, int c4) {
+__device__ __forceinline__ void tma2_5d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                        int c1, int c2, int c3, int c4) {
   asm volatile(
       "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
       "bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(su32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(0), "r"(0), "r"(c3), "r"(c4)
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4)
       : "memory");
 }
-// Four rows (r0..r3) x 64 columns from k0 of a row-major 2-D tensor, placed as
-// consecutive 128-byte rows at dst (the 128-byte swizzle follows the shared
-// address, so a group of 4 rows lands where a tiled box would put them).
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, uint32_t bar, int k0,
-                                            int r0, int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".cta_group::2 [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(su32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(k0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
-}
-// the four K16 MMAs of a k-block and the commit that frees the stage in both CTAs
-__device__ __forceinline__ void umma2_kblock(uint32_t d_tmem, uint64_t ad, uint64_t bd,
-                                             uint32_t idesc, uint32_t accumulate, uint32_t bar) {
+// The eight K16 MMAs of a stage (two K atoms; atom a of A at ad + a * 16 KB,
+// of B at bd + a * b_atom, descriptor units of 16 bytes) and the commit that
+// frees the stage in both CTAs.
+__device__ __forceinline__ void umma2_stage(uint32_t d_tmem, uint64_t ad, uint64_t bd,
+                                            uint32_t b_atom16, uint32_t idesc,
+                                            uint32_t accumulate, uint32_t bar) {
+  const uint64_t ad1 = ad + (ATOM_BYTES >> 4), bd1 = bd + b_atom16;
   asm volatile(
       "{\n\t.reg .pred p, t;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
@@ -137,10 +143,15 @@ __device__ __forceinline__ void umma2_kblock(uint32_t d_tmem, uint64_t ad, uint6
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %6, %7, %3, t;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %8, %9, %3, t;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %10, %11, %3, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %12, %13, %3, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %14, %15, %3, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %16, %17, %3, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %18, %19, %3, t;\n\t"
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%5], %12;\n\t}" ::"r"(d_tmem),
+      " [%5], %20;\n\t}" ::"r"(d_tmem),
       "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate), "r"(bar), "l"(ad + 2), "l"(bd + 2),
-      "l"(ad + 4), "l"(bd + 4), "l"(ad + 6), "l"(bd + 6), "h"((uint16_t)3)
+      "l"(ad + 4), "l"(bd + 4), "l"(ad + 6), "l"(bd + 6), "l"(ad1), "l"(bd1), "l"(ad1 + 2),
+      "l"(bd1 + 2), "l"(ad1 + 4), "l"(bd1 + 4), "l"(ad1 + 6), "l"(bd1 + 6), "h"((uint16_t)3)
       : "memory");
 }
 __device__ __forceinline__ void umma2_commit_both(uint64_t* bar) {
@@ -168,7 +179,7 @@ __device__ __forceinline__ uint32_t idesc_sw(int M, int N, int f16) {
 // nv <= N <= 256, N a multiple of 16 and at least 32).  nv == 0: an empty
 // tile (every role skips it alike).
 struct SwTile {
-  int e, nt, m0, nv, N;
+  int e, nt, ci, m0, nv, N;
 };
 
 // Tile t of the list built by build_tile_prefix(.., NMAX, n_ftiles, ..):
@@ -191,6 +202,7 @@ __device__ __forceinline__ SwTile sw_decode(int t, const int* prefix, const int3
   r.e = lo;
   r.nt = local / ce;
   const int ci = local % ce;
+  r.ci = ci;
   const int per = (((n + ce - 1) / ce) + 15) & ~15;
   const int start = min(ci * per, n);
   r.m0 = s + start;
@@ -334,21 +346,45 @@ __device__ __forceinline__ void sw_drain_gated(uint32_t tbase, int nv, int m0, i
   }
 }
 
-// tm_w: weights, 3-D [E][N1][K] box {64, 128, 1} (plain) or the 5-D gated view
-// [E][F/8][2][8][K] box {64, 8, 2, 8, 1}; tm_a: the token rows' source, 2-D
-// [rows][K] with a one-row box for gather4.  Row r of the segmented row space
-// is source row grows[r] / gdiv (the hidden states read through the
-// permutation; rows with an out-of-range entry read row 0) or, without
-// grows, row r itself.
-template <int MODE, int ACT, bool F16>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_sw_kernel(const __grid_constant__ CUtensorMap tm_w,
-                   const __grid_constant__ CUtensorMap tm_a,
+// How the token rows reach shared memory.
+enum SwTok {
+  kTokTiled = 0,    // contiguous rows: one tiled TMA box per stage
+  kTokCpAsync = 1,  // rows through the row map: cp.async by four loader warps
+};
+constexpr int kLoaderWarp0 = NUM_THREADS / 32;
+constexpr int NUM_THREADS_LOAD = NUM_THREADS + 128;
+
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+// Token-row boxes of 32, 64 and 128 rows x one K atom: 2-D maps [rows][K] of
+// the rows' source.
+struct TokMaps {
+  CUtensorMap m[3];
+};
+
+// The token rows of a stage sit as KA atoms of h rows each (h = 32, 64 or
+// 128, the smallest that holds the CTA's half of the chunk).
+__device__ __forceinline__ int tok_box_sel(int half) { return half <= 32 ? 0 : half <= 64 ? 1 : 2; }
+
+// tm_w: weights, 3-D [E][N1][K] box {64, 128, 1} (plain), or the 5-D gated
+// view [E][F/8][2][8][K] box {64, 8, 2, 8, 1} (a group is 8 activation
+// columns: their 8 gate rows, then their 8 up rows); one box per K atom, so
+// columns past K and rows past the expert's read as zeros.  Row r of the
+// segmented row space is source row grows[r] / gdiv (the hidden states read
+// through the permutation; rows with an out-of-range entry read zeros) or,
+// without grows, row r of the source itself.
+template <int MODE, int ACT, bool F16, int TOK>
+__global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_THREADS, 1)
+    gemm_sw_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ TokMaps tm_a,
                    const __grid_constant__ CUtensorMap tm_out, int tma_out,
                    const __nv_bfloat16* __restrict__ bias, const int32_t* __restrict__ seg_end,
                    int M, int Nout, int N1, int K, int E, int interleaved, float limit,
                    float alpha, float beta, __nv_bfloat16* __restrict__ out, int* status,
-                   const int32_t* __restrict__ grows, int gdiv, int src_rows, int seg_stride) {
+                   const __nv_bfloat16* __restrict__ asrc, const int32_t* __restrict__ grows,
+                   int gdiv, int src_rows, int seg_stride) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -361,7 +397,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&sh->full[s], 1);  // the leader's expect-tx arrival (+ both CTAs' bytes)
+      // the leader's expect-tx arrival (+ both CTAs' TMA bytes); with cp.async
+      // rows also one arrival per leader loader thread and the peer's
+      // forwarded arrival
+      mbar_init(&sh->full[s], TOK == kTokCpAsync ? 1 + 128 + 1 : 1);
+      mbar_init(&sh->afull[s], 128);
       mbar_init(&sh->empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -374,7 +414,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a)) : "memory");
+    if constexpr (TOK == kTokTiled)
+      for (int i = 0; i < 3; ++i)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_a.m[i]))
+                     : "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -394,66 +437,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
-  const int nkb = (K + BK - 1) / BK;
+  const int nks = (K + BKS - 1) / BKS;  // ring stages per tile
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   auto decode = [&](int t) { return sw_decode(t, sh->prefix, seg_end, E, M, n_ftiles, seg_stride); };
 
   if (warp == 0) {
-    // ------------------------------------------------ producer (both CTAs)
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t issued[STAGES];
-    for (int s = 0; s < STAGES; ++s) issued[s] = 0;
-    bool ok = true;
-    for (int tile = pair; tile < total && ok; tile += npairs) {
-      const SwTile st = decode(tile);
-      if (st.nv == 0) continue;
-      const int half = st.N >> 1;              // token rows of this CTA
-      const bool active = 4 * lane < half;     // lanes with a gather4 of 4 rows
-      int rr[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        // padding tokens (past nv) repeat the chunk's last row: their columns
-        // are never stored
-        const int j = min((int)rank * half + 4 * lane + u, st.nv - 1);
-        const int row = st.m0 + j;
-        int src = row;
-        if (grows) {
-          const int rt = active ? grows[row] : 0;
-          src = rt >= 0 && rt / gdiv < src_rows ? rt / gdiv : 0;
-        }
-        rr[u] = src;
-      }
-      const uint32_t tx = (uint32_t)(A_BYTES + half * BK * 2);
-      for (int kb = 0; kb < nkb; ++kb) {
-        int good = 1;
-        if (lane == 0) good = wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status) ? 1 : 0;
-        good = __shfl_sync(0xffffffffu, good, 0);
-        if (!good) { ok = false; break; }
-        uint8_t* a_dst = smem + (size_t)stage * STAGE_BYTES;
-        uint8_t* b_dst = a_dst + A_BYTES;
-        const uint32_t bar = map_to_rank(su32(&sh->full[stage]), 0);
-        const int k0 = kb * BK;
-        if (lane == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------- producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
+      bool ok = true;
+      for (int tile = pair; tile < total && ok; tile += npairs) {
+        const SwTile st = decode(tile);
+        if (st.nv == 0) continue;
+        const int half = st.N >> 1;  // token rows of this CTA
+        const int bsel = tok_box_sel(half);
+        const uint32_t tx =
+            (uint32_t)A_BYTES + (TOK == kTokTiled ? (uint32_t)KA * (32u << bsel) * BK * 2 : 0u);
+        for (int ks = 0; ks < nks; ++ks) {
+          if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
+          uint8_t* a_dst = smem + (size_t)stage * STAGE_BYTES;
+          uint8_t* b_dst = a_dst + A_BYTES;
+          const uint32_t bar = map_to_rank(su32(&sh->full[stage]), 0);
           if (leader) mbar_expect_tx(&sh->full[stage], 2 * tx);
-          if constexpr (MODE == kSwPlain)
-            tma_w3(a_dst, &tm_w, bar, k0, st.nt * 2 * ROWS + ROWS * (int)rank, st.e);
-          else
-            tma_w5(a_dst, &tm_w, bar, k0, st.nt * 16 + 8 * (int)rank, st.e);
+#pragma unroll
+          for (int a = 0; a < KA; ++a) {  // one box per K atom and operand
+            const int k0 = ks * BKS + a * BK;
+            if constexpr (MODE == kSwPlain)
+              tma2_3d(a_dst + a * ATOM_BYTES, &tm_w, bar, k0,
+                      st.nt * 2 * ROWS + ROWS * (int)rank, st.e);
+            else
+              tma2_5d(a_dst + a * ATOM_BYTES, &tm_w, bar, k0, 0, 0,
+                      st.nt * 16 + 8 * (int)rank, st.e);
+            if constexpr (TOK == kTokTiled)
+              tma2_2d(b_dst + a * ((32 << bsel) * BK * 2), &tm_a.m[bsel], bar, k0,
+                      st.m0 + (int)rank * half);
+          }
           ++issued[stage];
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (active)
-          tma_gather4(b_dst + lane * 4 * BK * 2, &tm_a, bar, k0, rr[0], rr[1], rr[2], rr[3]);
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-    }
-    if (!ok && leader && lane == 0) {  // both CTAs' copies complete on the leader's barriers
-      for (int s = 0; s < STAGES; ++s)
-        if (issued[s]) drain_wait(&sh->full[s], (issued[s] - 1u) & 1u);
+      if (!ok && leader) {  // both CTAs' copies complete on the leader's barriers
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) drain_wait(&sh->full[s], (issued[s] - 1u) & 1u);
+      }
     }
   } else if (warp == 1) {
     if (lane == 0 && leader) {
-      // ------------------------------------------------ MMA issuer (leader)
+      // ---------------------------------------------- MMA issuer (leader)
       int stage = 0, acc = 0;
       uint32_t phase = 0, aphase = 0;
       bool ok = true, any = false;
@@ -465,15 +498,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const SwTile st = decode(tile);
         if (st.nv == 0) continue;
         const uint32_t idesc = idesc_sw(2 * ROWS, st.N, F16 ? 1 : 0);
+        // token atoms h rows apart (16-byte descriptor units)
+        const uint32_t b_atom16 = (uint32_t)((32 << tok_box_sel(st.N >> 1)) * BK * 2) >> 4;
         if (!wait_fast(&sh->tempty[acc], aphase ^ 1u, abort_flag, status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * NMAX);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int ks = 0; ks < nks; ++ks) {
           if (!wait_fast(&sh->full[stage], phase, abort_flag, status)) { ok = false; break; }
+          // cp.async rows of this CTA were written through the generic proxy;
+          // the MMA reads them through the async proxy (the peer's forwarder
+          // fences the peer's rows)
+          if constexpr (TOK == kTokCpAsync) fence_proxy_async_smem();
           tc_fence_after();
           const uint64_t off = (uint64_t)((stage * STAGE_BYTES) >> 4);
-          umma2_kblock(d_tmem, adesc0 + off, bdesc0 + off, idesc, kb != 0 ? 1u : 0u,
-                       empty_addr[stage]);
+          umma2_stage(d_tmem, adesc0 + off, bdesc0 + off, b_atom16, idesc, ks != 0 ? 1u : 0u,
+                      empty_addr[stage]);
           any = true;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -486,6 +525,90 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         drain_wait(&sh->drain, 0);
       }
     }
+    if constexpr (TOK == kTokCpAsync) {
+      if (lane == 0 && !leader) {
+        // -------------------------------------------- forwarder (peer)
+        // the peer's rows of a stage have landed: order them for the async
+        // proxy and pass one arrival to the leader's full barrier (released
+        // at CTA scope: a cluster-scope release would wait for every copy
+        // this SM has in flight)
+        int stage = 0;
+        uint32_t phase = 0;
+        const uint32_t full_remote0 = map_to_rank(su32(&sh->full[0]), 0);
+        bool ok = true;
+        for (int tile = pair; tile < total && ok; tile += npairs) {
+          if (decode(tile).nv == 0) continue;
+          for (int ks = 0; ks < nks; ++ks) {
+            if (!wait_fast(&sh->afull[stage], phase, abort_flag, status)) { ok = false; break; }
+            fence_proxy_async_smem();
+            mbar_arrive_remote_cta(full_remote0 + (uint32_t)(stage * sizeof(uint64_t)));
+            if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          }
+        }
+      }
+    }
+  } else if (TOK == kTokCpAsync && warp >= kLoaderWarp0) {
+    // ------------------------------------------------ token loaders (cp.async)
+    // thread lt copies 16-byte chunk lt % 8 of rows lt / 8 + 16 i of this
+    // CTA's half, for both K atoms of a stage, into the 128-byte swizzle
+    // (chunk ch of row r at ch ^ (r % 8)); padding rows and columns past K
+    // are zero-filled
+    const int lt = threadIdx.x - kLoaderWarp0 * 32;
+    const int ch = lt & 7, r0 = lt >> 3;
+    const uint32_t dst0 = (uint32_t)(r0 * 128 + ((ch ^ (r0 & 7)) << 4));
+    uint64_t* arrive_bar = leader ? sh->full : sh->afull;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = pair; tile < total && ok; tile += npairs) {
+      const SwTile st = decode(tile);
+      if (st.nv == 0) continue;
+      const int half = st.N >> 1;
+      const uint32_t atom_bytes = (uint32_t)(32 << tok_box_sel(half)) * BK * 2;
+      const __nv_bfloat16* src[8];
+      uint32_t valid = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = r0 + 16 * i;
+        const int j = (int)rank * half + r;
+        int t = 0;
+        if (r < half && j < st.nv) {
+          const int row = st.m0 + j;
+          if (grows) {
+            const int rt = grows[row];
+            if (rt >= 0 && rt / gdiv < src_rows) { t = rt / gdiv; valid |= 1u << i; }
+          } else {
+            t = row;
+            valid |= 1u << i;
+          }
+        }
+        src[i] = asrc + (size_t)t * K + ch * 8;
+      }
+      for (int ks = 0; ks < nks; ++ks) {
+        if (!wait_fast(&sh->empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
+        const uint32_t b_dst = su32(smem + (size_t)stage * STAGE_BYTES + A_BYTES) + dst0;
+#pragma unroll
+        for (int a = 0; a < KA; ++a) {
+          const int k0 = ks * BKS + a * BK;
+          const bool kin = k0 + ch * 8 < K;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            if (r0 + 16 * i >= half) break;
+            const bool v = kin && ((valid >> i) & 1u);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                             b_dst + a * atom_bytes + i * 16 * 128),
+                         "l"(v ? src[i] + k0 : asrc), "r"(v ? 16 : 0)
+                         : "memory");
+          }
+        }
+        // arrives on the stage's barrier of this CTA once this thread's copies land
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(
+                         su32(&arrive_bar[stage]))
+                     : "memory");
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // nothing in flight at exit
   } else {
     // ------------------------------------------------ epilogue (both CTAs)
     const int quad = warp & 3;
@@ -533,25 +656,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // ------------------------------------------------------------ host side
 namespace {
 
-template <int MODE, int ACT, bool F16>
+template <int MODE, int ACT, bool F16, int TOK>
 const void* sw_kernel_ptr() {
-  return (const void*)gemm_sw_kernel<MODE, ACT, F16>;
+  return (const void*)gemm_sw_kernel<MODE, ACT, F16, TOK>;
 }
 
-template <bool F16>
+template <bool F16, int TOK>
 const void* pick_sw(int mode, int kind) {
   if (mode == kSwPlain) {
     switch (kind) {
-      case MOE_ACT_RELU: return sw_kernel_ptr<kSwPlain, MOE_ACT_RELU, F16>();
-      case MOE_ACT_GELU: return sw_kernel_ptr<kSwPlain, MOE_ACT_GELU, F16>();
-      case MOE_ACT_SILU: return sw_kernel_ptr<kSwPlain, MOE_ACT_SILU, F16>();
-      default: return sw_kernel_ptr<kSwPlain, MOE_ACT_IDENTITY, F16>();
+      case MOE_ACT_RELU: return sw_kernel_ptr<kSwPlain, MOE_ACT_RELU, F16, TOK>();
+      case MOE_ACT_GELU: return sw_kernel_ptr<kSwPlain, MOE_ACT_GELU, F16, TOK>();
+      case MOE_ACT_SILU: return sw_kernel_ptr<kSwPlain, MOE_ACT_SILU, F16, TOK>();
+      default: return sw_kernel_ptr<kSwPlain, MOE_ACT_IDENTITY, F16, TOK>();
     }
   }
   switch (kind) {
-    case MOE_ACT_SWIGLU: return sw_kernel_ptr<kSwGated, MOE_ACT_SWIGLU, F16>();
-    case MOE_ACT_GELU_AND_MUL: return sw_kernel_ptr<kSwGated, MOE_ACT_GELU_AND_MUL, F16>();
-    default: return sw_kernel_ptr<kSwGated, MOE_ACT_SILU_AND_MUL, F16>();
+    case MOE_ACT_SWIGLU: return sw_kernel_ptr<kSwGated, MOE_ACT_SWIGLU, F16, TOK>();
+    case MOE_ACT_GELU_AND_MUL: return sw_kernel_ptr<kSwGated, MOE_ACT_GELU_AND_MUL, F16, TOK>();
+    default: return sw_kernel_ptr<kSwGated, MOE_ACT_SILU_AND_MUL, F16, TOK>();
   }
 }
 
@@ -574,7 +697,7 @@ cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const
     beta = act->beta;
   }
   if (N % 8 != 0 || K % 8 != 0) return cudaErrorInvalidValue;
-  CUtensorMap mw, ma, mo;
+  CUtensorMap mw, mo;
   const uint64_t K2 = (uint64_t)K * 2;
   if (mode == kSwPlain) {
     cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N1, (cuuint64_t)E};
@@ -593,13 +716,20 @@ cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const
                            CU_TENSOR_MAP_SWIZZLE_128B, f16))
       return cudaErrorInvalidValue;
   }
-  {
-    const int rows = gather_rows ? gather_src_rows : M;
-    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)std::max(rows, 1)};
+  // token rows: boxes of 32 / 64 / 128 rows of one K atom (contiguous rows);
+  // cp.async reads gathered rows without a map
+  const int tok = gather_rows ? kTokCpAsync : kTokTiled;
+  TokMaps ma;
+  if (tok == kTokTiled) {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)std::max(M, 1)};
     cuuint64_t str[1] = {K2};
-    cuuint32_t box[2] = {BK, 1};
-    if (!tmap::encode_bf16(&ma, a, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, f16))
-      return cudaErrorInvalidValue;
+    for (int i = 0; i < 3; ++i) {
+      cuuint32_t box[2] = {BK, 32u << i};
+      if (!tmap::encode_bf16(&ma.m[i], a, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, f16))
+        return cudaErrorInvalidValue;
+    }
+  } else {
+    ma.m[0] = ma.m[1] = ma.m[2] = mw;  // unused
   }
   // staged output boxes: 32 columns x 32 rows (64-byte swizzle), or 16 x 32
   // for the gated mode; rows stored directly when the output's base or pitch
@@ -617,7 +747,10 @@ cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const
                   : 0;
   }
   if (!tma_out) mo = mw;  // unused
-  const void* kern = f16 ? pick_sw<true>(mode, kind) : pick_sw<false>(mode, kind);
+  const void* kern = tok == kTokTiled ? (f16 ? pick_sw<true, kTokTiled>(mode, kind)
+                                              : pick_sw<false, kTokTiled>(mode, kind))
+                                       : (f16 ? pick_sw<true, kTokCpAsync>(mode, kind)
+                                              : pick_sw<false, kTokCpAsync>(mode, kind));
   set_smem_limit(kern, (int)kSmemBytes);
   const int n_ftiles = mode == kSwPlain ? (N + 2 * ROWS - 1) / (2 * ROWS) : (N + ROWS - 1) / ROWS;
   const long long max_tiles = (long long)((M + NMAX - 1) / NMAX + E) * n_ftiles;
@@ -625,7 +758,7 @@ cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.blockDim = dim3(tok == kTokCpAsync ? NUM_THREADS_LOAD : NUM_THREADS);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -639,8 +772,9 @@ cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const
   cfg.numAttrs = 2;
   const __nv_bfloat16* bias_p = static_cast<const __nv_bfloat16*>(bias);
   __nv_bfloat16* out_p = static_cast<__nv_bfloat16*>(out);
+  const __nv_bfloat16* a_p = static_cast<const __nv_bfloat16*>(a);
   void* args[] = {&mw, &ma, &mo, &tma_out, &bias_p, &seg_end, &M, &N, &N1, &K, &E, &inter,
-                  &limit, &alpha, &beta, &out_p, &status, &gather_rows, &gather_div,
+                  &limit, &alpha, &beta, &out_p, &status, &a_p, &gather_rows, &gather_div,
                   &gather_src_rows, &seg_stride};
   cudaError_t e = cudaLaunchKernelExC(&cfg, kern, args);
   count_launch();
