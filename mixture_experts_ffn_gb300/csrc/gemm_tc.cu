@@ -357,22 +357,24 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            int gather_div, int gather_src_rows, int seg_stride,
                            const SplitUp* split, bool f16) {
   if (M == 0 || N == 0) return cudaSuccess;
-  // The default is the weights-as-M kernel on SM pairs (gemm_sw.cu), which
-  // pads an expert's rows to 16 instead of 128; this one-SM kernel takes the
-  // split gate/up weights, and every call with MOE_TC_KERNEL=1sm (kept to
-  // check the two against each other).  MOE_TC_KERNEL=2sm: the row-tile
-  // kernel on SM pairs (gemm_tc2.cu).
+  // The weights-as-M kernel on SM pairs (gemm_sw.cu) pads an expert's rows to
+  // 16 instead of 128; measured against this kernel on the workloads, it is
+  // faster only on plain products over contiguous rows with long K (the
+  // DeepSeek-V3-style down GEMM: 1.63 vs 1.75 ms), where it is the default.
+  // MOE_TC_KERNEL=1sm keeps every call on this kernel, =sw sends every call it
+  // can take to the pair kernel (both settings exist to check the kernels
+  // against each other).
   static const int which = [] {
     const char* v = getenv("MOE_TC_KERNEL");
-    return v && v[0] == '1' ? 1 : v && v[0] == '2' ? 2 : 0;
+    return v && v[0] == '1' ? 1 : v && v[0] == 's' ? 2 : 0;
   }();
   const bool gather = gather_rows != nullptr;
-  if (which == 0 && !split && num_sms() >= 2 && N % 8 == 0 && K % 8 == 0)
+  const bool gated = act && act_is_gated(act->kind);
+  const bool sw_ok = !split && num_sms() >= 2 && N % 8 == 0 && K % 8 == 0;
+  const bool sw_pick = which == 2 || (which == 0 && !gather && !gated && K >= 2048);
+  if (sw_ok && sw_pick)
     return launch_gemm_sw(a, w, bias, seg_end, M, N, K, E, act, out, status, s, gather_rows,
                           gather_div, gather_src_rows, seg_stride, f16);
-  if (which == 2 && num_sms() >= 2 && !split && !f16)
-    return launch_gemm_tc2(a, w, bias, seg_end, M, N, K, E, act, out, status, s, gather_rows,
-                           gather_div, gather_src_rows, seg_stride);
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
   if (act) kind = act->kind;

@@ -179,13 +179,6 @@ cudaError_t launch_gemm_fp8(const void* a, const float* a_scale, const void* b,
                             const float* b_scale, const int32_t* counts, int E, int max_m, int N,
                             int K, void* out, int* status, cudaStream_t s);
 
-// two-SM (cta_group::2) variant of launch_gemm_tc, same contract
-cudaError_t launch_gemm_tc2(const void* a, const void* w, const void* bias,
-                            const int32_t* seg_end, int M, int N, int K, int E,
-                            const moe_act_params* act, void* out, int* status, cudaStream_t s,
-                            const int32_t* gather_rows, int gather_div, int gather_src_rows,
-                            int seg_stride);
-
 // indexed per-route decode path (bf16, silu_and_mul, no bias)
 cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, const float* w,
                            const int32_t* ids, int T, int H, int F, int E, int K, float scale,

@@ -1,9 +1,8 @@
-"""The alternative tcgen05 grouped-GEMM kernels -- the one-SM row-tile kernel
-(MOE_TC_KERNEL=1sm) and the row-tile kernel on SM pairs (MOE_TC_KERNEL=2sm),
-both with the staged-store epilogue -- run the whole grouped-GEMM parity file
-(gathered rows included) and the small whole-forward cases in a fresh process
-(the switch is read once per process); the default kernel is the
-weights-as-M one on SM pairs."""
+"""Both tcgen05 grouped-GEMM kernels on every call they can take: the one-SM
+row-tile kernel alone (MOE_TC_KERNEL=1sm) and the weights-as-M kernel on SM
+pairs (MOE_TC_KERNEL=sw), each running the whole grouped-GEMM parity file
+(gathered rows included) and the small whole-forward cases in a fresh
+process (the switch is read once per process)."""
 import os
 import subprocess
 import sys
@@ -15,7 +14,7 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-@pytest.mark.parametrize("kernel", ["1sm", "2sm"])
+@pytest.mark.parametrize("kernel", ["1sm", "sw"])
 def test_alternative_gemm_kernel_parity(kernel):
     env = dict(os.environ, MOE_TC_KERNEL=kernel)
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(HERE, "test_gpu_gemm.py"),
