@@ -359,8 +359,10 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
   if (M == 0 || N == 0) return cudaSuccess;
   // The weights-as-M kernel on SM pairs (gemm_sw.cu) pads an expert's rows to
   // 16 instead of 128; measured against this kernel on the workloads, it is
-  // faster only on plain products over contiguous rows with long K (the
-  // DeepSeek-V3-style down GEMM: 1.63 vs 1.75 ms), where it is the default.
+  // faster only on plain products over contiguous rows with long K and full
+  // 256-token chunks (the DeepSeek-V3-style down GEMM: 1.63 vs 1.75 ms; on
+  // the gpt-oss-style one, 64 rows per expert, 365 vs 356 us), where it is
+  // the default.
   // MOE_TC_KERNEL=1sm keeps every call on this kernel, =sw sends every call it
   // can take to the pair kernel (both settings exist to check the kernels
   // against each other).
@@ -371,7 +373,8 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
   const bool gather = gather_rows != nullptr;
   const bool gated = act && act_is_gated(act->kind);
   const bool sw_ok = !split && num_sms() >= 2 && N % 8 == 0 && K % 8 == 0;
-  const bool sw_pick = which == 2 || (which == 0 && !gather && !gated && K >= 2048);
+  const bool sw_pick =
+      which == 2 || (which == 0 && !gather && !gated && K >= 2048 && (long long)M >= 128LL * E);
   if (sw_ok && sw_pick)
     return launch_gemm_sw(a, w, bias, seg_end, M, N, K, E, act, out, status, s, gather_rows,
                           gather_div, gather_src_rows, seg_stride, f16);

@@ -56,8 +56,12 @@ def test_expert_parallel_ranks_sum_to_the_layer(moe, name, over, lc):
                                    ref["w_gate_up"][start:start + lc],
                                    ref["w_down"][start:start + lc], K, cfg.F,
                                    dtype=cfg.dtype, parts=True, **act_kwargs(cfg))
+        # a rank's output is its slice's share of the layer (weight_scale times
+        # the slice's softmax-weighted sum), not the layer output the stated
+        # bound is written for: the secondary bound is asserted, the bare
+        # figure logged
         assert_forward_close(np_(part), want, cfg.dtype, f"ep {name} rank at {start}",
-                             scale=r["weight_scale"])
+                             stated=False, scale=r["weight_scale"])
         total += part.float()
         want_total += want["out_unrounded"]
         # each rank's own cast and flips (see the tolerances module)

@@ -44,9 +44,7 @@ parity_log = []
 STATED_BOUND_NOT_MET = {
     "full qwen3_bf16",                     # 0.0354 (124 of 8388608 elements above)
     "full gpt_oss_bf16",                   # 0.0249 (7 of 737280)
-    "ep qwen3_bf16 rank at 0",             # 0.0240 (16 of 76800)
-    "ep deepseek_v3_bf16 rank at 32",      # 0.0261 (1 of 51200)
-    "forward_shared qwen3_bf16 routed",    # 0.0239 (2 of 65792)
+    "forward_shared qwen3_bf16 routed",    # 0.0239 (2 of 65792; T = 257, H = 256)
 }
 
 
