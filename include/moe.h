@@ -615,6 +615,17 @@ uint64_t moe_launch_count(void);
  * flight. */
 int moe_set_gemm_simt(int enable);
 
+/* Stage profile (a tracing aid; no counterpart on the pages): with
+ * MOE_PROFILE=1 in the environment when the library loads, every forward
+ * brackets its stages (route_permute or route, permute, gate_up, down,
+ * combine, or indexed_mlp) with CUDA events on the caller's stream.  This call
+ * waits for the recorded events, writes one line per stage, "name count
+ * total_us", into buf (NUL-terminated, truncated to buf_bytes - 1), drops the
+ * records and returns the length of the full text.  Without MOE_PROFILE
+ * nothing is recorded and the text is empty.  The events sit between the
+ * launches, so a profiled forward runs its launches without overlap. */
+int moe_profile_report(char* buf, size_t buf_bytes);
+
 /* Test hook, off by default (no counterpart on the pages; it exists so that
  * a test can make a bounded device wait run out without faulting or hanging
  * anything).  With enable != 0, both grid barriers of the fused route +

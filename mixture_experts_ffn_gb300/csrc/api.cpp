@@ -7,8 +7,13 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <cstdio>
+#include <cstdlib>
+#include <map>
 #include <mutex>
 #include <set>
+#include <string>
+#include <vector>
 #include <utility>
 
 #include "internal.h"
@@ -47,6 +52,56 @@ cudaError_t set_smem_limit(const void* kernel, int bytes) {
 }
 
 static int g_force_simt = 0;
+
+// ---------------------------------------------------------------- stage profile
+// With MOE_PROFILE=1 in the environment (read once), the forward brackets each
+// of its stages with a pair of CUDA events on the caller's stream;
+// moe_profile_report synchronises them and returns per-stage totals.  The
+// events sit between the launches, so a profiled forward loses the overlap of
+// one launch's start with the previous one's end.
+namespace {
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+std::vector<ProfRec> g_prof;
+
+bool profiling() {
+  static const bool on = [] {
+    const char* v = getenv("MOE_PROFILE");
+    return v && v[0] == '1';
+  }();
+  return on;
+}
+
+// Brackets the launches of one stage between its construction and done().
+struct StageTimer {
+  const char* name;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  StageTimer(const char* n, cudaStream_t st) : name(n), s(st) {
+    if (!profiling()) return;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventRecord(a, s) != cudaSuccess) a = nullptr;
+  }
+  void done() {
+    if (!a) return;
+    cudaEvent_t b = nullptr;
+    if (cudaEventCreate(&b) != cudaSuccess || cudaEventRecord(b, s) != cudaSuccess) {
+      cudaEventDestroy(a);
+      if (b) cudaEventDestroy(b);
+      a = nullptr;
+      return;
+    }
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    g_prof.push_back({name, a, b});
+    a = nullptr;
+  }
+  ~StageTimer() {
+    if (a) cudaEventDestroy(a);
+  }
+};
+}  // namespace
 
 namespace {
 
@@ -603,6 +658,7 @@ moe_status ffn_forward(const void* hidden, const void* logits, const void* w_gat
   // Routing and the index maps take one launch; the staged path then copies
   // the permuted activations in a launch of its own.
   const bool fused_maps = route_permute_ok(E);
+  StageTimer t_route(fused_maps ? "route_permute" : "route", stream);
   cudaError_t err =
       fused_maps ? launch_route_permute(logits, correction_bias, expert_ids, T, E, *p, tw, ti,
                                         router_probs, weight_scale, seg_end, r2r, route_to_row,
@@ -610,24 +666,32 @@ moe_status ffn_forward(const void* hidden, const void* logits, const void* w_gat
                  : launch_route(logits, correction_bias, expert_ids, T, E, *p, tw, ti,
                                 router_probs, weight_scale, stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
+  t_route.done();
   if (hooks && hooks->hidden_ready) {
     if (cudaStreamWaitEvent(stream, hooks->hidden_ready, 0) != cudaSuccess) return MOE_ERR_CUDA;
     hooks->waited = true;
   }
 
   // routed_scaling_factor is folded into tw by the router: the combine scale is 1
-  if (indexed)
-    return cuda_status(launch_indexed(hidden, w_gate_up, w_down, tw, ti, T, H, F, E, K, 1.0f, out,
-                                      ws, L, stream, fused_maps));
-
-  if (!fused_maps) {
-    err = launch_permute(hidden, (int)esz, ti, T, H, E, K, fused_gather ? nullptr : xin, seg_end,
-                         r2r, route_to_row, ws, stream);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
-  } else if (!fused_gather) {
-    err = launch_permute_gather(hidden, (int)esz, T, H, E, K, seg_end, r2r, xin, ws, stream);
-    if (err != cudaSuccess) return MOE_ERR_CUDA;
+  if (indexed) {
+    StageTimer t_idx("indexed_mlp", stream);
+    err = launch_indexed(hidden, w_gate_up, w_down, tw, ti, T, H, F, E, K, 1.0f, out, ws, L,
+                         stream, fused_maps);
+    t_idx.done();
+    return cuda_status(err);
   }
+
+  if (!fused_maps || !fused_gather) {
+    StageTimer t_perm("permute", stream);
+    if (!fused_maps)
+      err = launch_permute(hidden, (int)esz, ti, T, H, E, K, fused_gather ? nullptr : xin,
+                           seg_end, r2r, route_to_row, ws, stream);
+    else
+      err = launch_permute_gather(hidden, (int)esz, T, H, E, K, seg_end, r2r, xin, ws, stream);
+    if (err != cudaSuccess) return MOE_ERR_CUDA;
+    t_perm.done();
+  }
+  StageTimer t_gu("gate_up", stream);
   if (fused_gather)
     err = launch_gemm_tc(hidden, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, act, a1, status,
                          stream, r2r, K, T, 0, split, dtype == MOE_F16);
@@ -635,16 +699,22 @@ moe_status ffn_forward(const void* hidden, const void* logits, const void* w_gat
     err = grouped_gemm(xin, w_gate_up, b_gate_up, seg_end, (int)M, F, H, E, dtype, act, a1,
                        status, stream, 0, split);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
+  t_gu.done();
+  StageTimer t_down("down", stream);
   err = grouped_gemm(a1, w_down, b_down, seg_end, (int)M, H, F, E, dtype, nullptr, y, status,
                      stream);
   if (err != cudaSuccess) return MOE_ERR_CUDA;
+  t_down.done();
   void* dst = out;
   if (hooks && hooks->out_direct) {
     dst = hooks->out_direct;
     hooks->wrote_direct = true;
   }
-  return cuda_status(launch_combine(y, tw, route_to_row, T, K, H, dtype, 1.0f, dst, stream,
-                                    hooks ? hooks->token_scale : nullptr));
+  StageTimer t_comb("combine", stream);
+  err = launch_combine(y, tw, route_to_row, T, K, H, dtype, 1.0f, dst, stream,
+                       hooks ? hooks->token_scale : nullptr);
+  t_comb.done();
+  return cuda_status(err);
 }
 
 // The device address of page-locked host memory (nullptr for anything else,
@@ -952,6 +1022,44 @@ int moe_set_gemm_simt(int enable) {
   int old = g_force_simt;
   g_force_simt = enable ? 1 : 0;
   return old;
+}
+
+int moe_profile_report(char* buf, size_t buf_bytes) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lock(g_prof_mu);
+    recs.swap(g_prof);
+  }
+  std::vector<std::string> order;
+  std::map<std::string, std::pair<int, double>> agg;
+  for (const ProfRec& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      auto it = agg.find(r.name);
+      if (it == agg.end()) {
+        order.push_back(r.name);
+        agg[r.name] = {1, (double)ms};
+      } else {
+        it->second.first += 1;
+        it->second.second += ms;
+      }
+    }
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  std::string text;
+  char line[160];
+  for (const std::string& n : order) {
+    const auto& v = agg[n];
+    snprintf(line, sizeof line, "%s %d %.3f\n", n.c_str(), v.first, 1e3 * v.second);
+    text += line;
+  }
+  if (buf && buf_bytes > 0) {
+    const size_t n = std::min(buf_bytes - 1, text.size());
+    memcpy(buf, text.data(), n);
+    buf[n] = 0;
+  }
+  return (int)text.size();
 }
 
 int moe_test_force_wait_timeout(int enable, long long limit_ns) {

@@ -37,6 +37,11 @@ __device__ __forceinline__ unsigned order_key(float v) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// The score of an order key of a real (non-NaN) score.
+__device__ __forceinline__ float key_value(unsigned k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // (value, index) arg-max across the warp; ties go to the lower index
 __device__ __forceinline__ void warp_argmax(float& v, int& idx) {
 #pragma unroll
@@ -153,6 +158,35 @@ __device__ __forceinline__ void route_loaded(int t, const float (&z)[NPL],
     if (a.G > 1) {
       const int S = E / a.G;
       float my_gs = -INFINITY;  // lane g holds group g's score
+      if (S % 32 == 0 && S / 32 <= NPL) {
+        // A group is m = S / 32 whole registers of every lane (experts
+        // lane + 32 i, i in [g m, (g + 1) m)): per lane its two best of them,
+        // then the warp's best (max of the order keys) and its second best (the
+        // max again with the lowest lane holding the best giving its own
+        // second instead) -- the same two values, duplicates counted, as the
+        // shuffle reduction below.
+        const int m = S / 32;
+#pragma unroll
+        for (int g = 0; g < NPL; ++g) {
+          if (g >= a.G) break;
+          float l1 = -INFINITY, l2 = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < NPL; ++j) {
+            if (j >= g * m && j < (g + 1) * m) {
+              const float v = u[j];
+              if (v > l1) { l2 = l1; l1 = v; } else if (v > l2) { l2 = v; }
+            }
+          }
+          const unsigned k1 = __reduce_max_sync(0xffffffffu, order_key(l1));
+          const unsigned first =
+              __reduce_min_sync(0xffffffffu, order_key(l1) == k1 ? (unsigned)lane : 32u);
+          const unsigned k2 = __reduce_max_sync(
+              0xffffffffu, order_key((unsigned)lane == first ? l2 : l1));
+          const float b1 = key_value(k1), b2 = key_value(k2);
+          const float gs = bias ? b1 + b2 : b1;
+          if (lane == g) my_gs = gs;
+        }
+      } else
       for (int g = 0; g < a.G; ++g) {
         float b1 = -INFINITY, b2 = -INFINITY;
 #pragma unroll

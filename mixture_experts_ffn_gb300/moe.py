@@ -86,6 +86,7 @@ _SIGNATURES = {
     "moe_launch_count": [],
     "moe_set_gemm_simt": [_i],
     "moe_test_force_wait_timeout": [_i, ctypes.c_longlong],
+    "moe_profile_report": [ctypes.c_char_p, _sz],
 }
 _RESTYPES = {"moe_workspace_size": _sz, "moe_permute_workspace_size": _sz,
              "moe_workspace_size_host": _sz, "moe_shared_expert_workspace_size": _sz,
@@ -625,6 +626,19 @@ def moe_launch_count() -> int:
 
 def moe_set_gemm_simt(enable: bool) -> bool:
     return bool(load_library().moe_set_gemm_simt(int(bool(enable))))
+
+
+def moe_profile_report() -> dict:
+    """Per-stage totals of the forwards recorded since the last report (with
+    MOE_PROFILE=1 set before the library loads): {stage: (count, total_us)}."""
+    lib = load_library()
+    buf = ctypes.create_string_buffer(1 << 16)
+    lib.moe_profile_report(buf, len(buf))
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, count, us = line.split()
+        out[name] = (int(count), float(us))
+    return out
 
 
 def moe_test_force_wait_timeout(enable: bool, limit_ns: int = 50_000_000) -> bool:

@@ -85,3 +85,34 @@ def test_forward_after_a_timeout_matches_a_clean_forward(moe):
     got = fwd()
     assert moe.moe_sync_status(ws) == moe.MOE_OK
     assert torch.equal(got, ref)
+
+
+def test_stage_profile_in_a_fresh_process():
+    """MOE_PROFILE=1 (read when the library loads) records the forward's
+    stages with CUDA events; moe_profile_report returns one entry per stage
+    and empties the record."""
+    import os
+    import subprocess
+    import sys
+
+    code = r"""
+import sys, torch
+sys.path.insert(0, "tests")
+from mixture_experts_ffn_gb300 import moe, synth
+from gpu_cases import make
+cfg = synth.CONFIGS["qwen3_bf16"].replace(T=300, H=256, F=128, E=32, local_count=0)
+inp, _ = make(cfg)
+p, a = moe.config_params(cfg)
+for _ in range(3):
+    moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p, a)
+torch.cuda.synchronize()
+rep = moe.moe_profile_report()
+assert set(rep) == {"route_permute", "gate_up", "down", "combine"}, rep
+assert all(c == 3 and us > 0 for c, us in rep.values()), rep
+assert moe.moe_profile_report() == {}
+print("ok", rep)
+"""
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       env=dict(os.environ, MOE_PROFILE="1"), timeout=600)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
