@@ -475,14 +475,10 @@ cudaError_t launch_combine(const void* y, const float* w, const int32_t* r2r, in
   if (T == 0 || H == 0) return cudaSuccess;
   const int M = T * K;
   const bool aligned = ((uintptr_t)y % 16 == 0) && ((uintptr_t)out % 16 == 0);
-  // Grid: at most 8 CTAs of 256 threads per SM, sized so that every thread
-  // takes the same number of items (a last round that only part of the
-  // threads run would leave the SMs idle at the end).
   auto grid_for = [&](int vec) {
     const long long items = (long long)T * (H / vec);
-    const long long cap = (long long)num_sms() * 8 * 256;
-    const long long rounds = std::max<long long>(1, (items + cap - 1) / cap);
-    return (unsigned)std::max<long long>(1, (items + 256 * rounds - 1) / (256 * rounds));
+    const long long cap = (long long)num_sms() * 8;
+    return (unsigned)std::max<long long>(1, std::min<long long>(cap, (items + 255) / 256));
   };
   auto half_width = [&](auto tag) {
     using B = decltype(tag);
