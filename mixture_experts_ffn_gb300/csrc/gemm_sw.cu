@@ -556,6 +556,8 @@ __global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_TH
     const int lt = threadIdx.x - kLoaderWarp0 * 32;
     const int ch = lt & 7, r0 = lt >> 3;
     const uint32_t dst0 = (uint32_t)(r0 * 128 + ((ch ^ (r0 & 7)) << 4));
+    uint64_t keep_policy;  // the hidden rows stay in L2 ahead of the weight stream
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(keep_policy));
     uint64_t* arrive_bar = leader ? sh->full : sh->afull;
     int stage = 0;
     uint32_t phase = 0;
@@ -595,9 +597,9 @@ __global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_TH
           for (int i = 0; i < 8; ++i) {
             if (r0 + 16 * i >= half) break;
             const bool v = kin && ((valid >> i) & 1u);
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+            asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(
                              b_dst + a * atom_bytes + i * 16 * 128),
-                         "l"(v ? src[i] + k0 : asrc), "r"(v ? 16 : 0)
+                         "l"(v ? src[i] + k0 : asrc), "r"(v ? 16 : 0), "l"(keep_policy)
                          : "memory");
           }
         }
