@@ -10,30 +10,41 @@
 // segment pads to a multiple of 128 (28% more MMA work on the DeepSeek-V3-
 // style routing, 100% on gpt-oss-style); as its N dimension it pads to a
 // multiple of 16 (5% and 12%), and tcgen05.mma time scales with N (N/2
-// cycles per K16 step from N = 96 up, measured).  The weights fill M with
+// cycles per K16 step from N = 128 up, measured).  The weights fill M with
 // no padding: 256 weight rows per CTA pair.
 //
 // Work decomposition
 //   pair tile = 256 weight rows (128 per CTA) x one token chunk of an expert
 //   (N <= 256 tokens, a multiple of 16; an expert of n rows is cut into
-//   ceil(n / 256) chunks of equal size rounded up to 16); k-block = 64.
-//   Each CTA loads its 128 weight rows (TMA, 16 KB) and half of the chunk's
-//   token rows (TMA tile::gather4 through the row map, N/2 x 128 B) per
-//   k-block into a 6-stage ring; both CTAs' copies complete on the leader's
-//   barrier, and the leader issues M256 x N x K16 MMAs into the pair's TMEM.
+//   ceil(n / 256) chunks of equal size rounded up to 16).  A ring stage holds
+//   two 64-wide K atoms: per CTA its 128 weight rows (TMA, 2 x 16 KB) and its
+//   half of the chunk's token rows.  Contiguous token rows come by a tiled
+//   TMA box of 32, 64 or 128 rows per atom.  Rows gathered through the
+//   permutation (the forward's gate_up) come by cp.async from four loader
+//   warps, and the peer's loaders' arrivals reach the leader through a
+//   forwarding thread.  Both CTAs' copies complete on the leader's barriers;
+//   the leader issues eight M256 x N x K16 MMAs per stage into the pair's
+//   TMEM; 3 stages (192 KB).
 //   Gated modes: a 5-D tensor map loads each group of 8 gate rows next to its
 //   8 up rows, so TMEM lane l (gate) and lane l ^ 8 (up) of one warp hold the
 //   two halves of one activation column; 64 activation columns per CTA.
-// Roles (192 threads per CTA)
-//   warp 0       : producer -- lane 0 the weight copy (and, in the leader, the
-//                  stage's expected bytes), every lane one gather4 of 4 rows
-//   warp 1       : TMEM allocation (pair); lane 0 of the leader issues MMAs
-//   warps 2..5   : epilogue of the CTA's 128 TMEM lanes (bias, activation,
-//                  rounding, transposed staging and TMA stores)
+// Roles (192 threads per CTA, + 128 with cp.async token rows)
+//   warp 0 lane 0 : producer -- the weight boxes, the tiled token boxes, and
+//                   in the leader the stage's expected bytes
+//   warp 1        : TMEM allocation (pair); lane 0 of the leader issues MMAs,
+//                   lane 0 of the peer forwards its cp.async arrivals
+//   warps 2..5    : epilogue of the CTA's 128 TMEM lanes (bias, activation,
+//                   rounding, transposed staging and TMA stores)
+//   warps 6..9    : cp.async token loaders (gathered rows only)
 // Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
 // tile overlap the main loop of the next.  Every wait is bounded (2 s); on a
 // timeout the block latches the timeout bit, drains what it issued and frees
 // TMEM.
+//
+// Measured against the one-SM kernel (gemm_tc.cu), this kernel is faster only
+// on plain products over contiguous rows with long K (the DeepSeek-V3-style
+// down GEMM); both stream weights at ~60% of DRAM, bounded by how fast an
+// operand ring of ~192 KB per SM turns over against DRAM latency under load.
 #include <cuda.h>
 
 #include <algorithm>
