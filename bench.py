@@ -172,10 +172,27 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm), "source": "nvml"}
 
 
-# the files the tcgen05 GEMM kernel is compiled from (the ncu summary under
+# the files each tcgen05 GEMM kernel is compiled from (the ncu summary under
 # profiles/ records their hash, so a stale summary is never quoted)
-GEMM_SOURCES = [os.path.join(ROOT, "mixture_experts_ffn_gb300", "csrc", f)
-                for f in ("gemm_tc.cu", "gemm_epilogue.cuh", "tc_ptx.cuh", "common.cuh")]
+GEMM_SOURCES = {
+    k: [os.path.join(ROOT, "mixture_experts_ffn_gb300", "csrc", f) for f in files]
+    for k, files in {
+        "gemm_tc_kernel": ("gemm_tc.cu", "gemm_epilogue.cuh", "tc_ptx.cuh", "common.cuh"),
+        "gemm_sw_kernel": ("gemm_sw.cu", "gemm_epilogue.cuh", "tc_ptx.cuh", "common.cuh"),
+    }.items()}
+
+
+def gemm_kernel(M, N, K, E, split=False):
+    """The tcgen05 kernel the library picks for a bf16/f16 grouped GEMM of M
+    rows over E experts, N output (or activation) columns and depth K: the
+    SM-pair kernel with 256 weight rows per CTA for long K and segments
+    averaging >= 128 rows, else the one-SM row-tile kernel (the rule of
+    launch_gemm_tc, with no MOE_TC_KERNEL override)."""
+    env = os.environ.get("MOE_TC_KERNEL", "")
+    sw_ok = not split and N % 8 == 0 and K % 8 == 0
+    if sw_ok and (env[:1] in ("s", "w") or (env[:1] != "1" and K >= 2048 and M >= 128 * E)):
+        return "gemm_sw_kernel"
+    return "gemm_tc_kernel"
 
 
 def sources_sha256(paths):
@@ -500,10 +517,14 @@ def run_ours(args, rank, world, local):
             traffic = None
         else:
             dom = max(("gemm_act", "gemm_down"), key=lambda k: breakdown[k]["us"])
-            # bf16 / f16 with 16-byte rows runs the tcgen05 kernel, anything else the SIMT one
+            # bf16 / f16 with 16-byte rows runs a tcgen05 kernel, anything else the SIMT one
             tc = cfg.dtype != "f32" and H % 8 == 0 and F % 8 == 0
-            kname = f"{'gemm_tc_kernel' if tc else 'gemm_simt_kernel'} ({dom})"
-            traffic = profile_traffic("gemm_tc_kernel", GEMM_SOURCES) if tc and (
+            gated = cfg.act in synth.GATED_ACTS
+            kern = (gemm_kernel(T * K, F, H, E, split=gated and cfg.swiglu_fusion == 0)
+                    if dom == "gemm_act" else gemm_kernel(T * K, H, F, E)) if tc else \
+                "gemm_simt_kernel"
+            kname = f"{kern} ({dom})"
+            traffic = profile_traffic(kern, GEMM_SOURCES[kern]) if tc and (
                 dom == "gemm_act" and args.workload == WORKLOAD) else None
         fl, by = costs["gemm_act_gathered" if gathered and dom == "gemm_act" else dom]
         b = breakdown[dom]

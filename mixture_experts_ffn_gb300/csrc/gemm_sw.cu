@@ -62,26 +62,41 @@ namespace {
 using namespace tc;
 
 constexpr int BK = 64;                           // one 128-byte swizzle atom of K
-constexpr int KA = 2;                            // K atoms per ring stage
-constexpr int BKS = BK * KA;                     // K per stage
-constexpr int ROWS = 128;                        // weight rows per CTA
+constexpr int ROWS = 128;                        // weight rows per CTA and M half
 constexpr int NMAX = 256;                        // tokens per chunk (MMA N)
-constexpr int STAGES = 3;
 constexpr int ATOM_BYTES = ROWS * BK * 2;        // 16 KB: 128 rows of one atom
-constexpr int A_BYTES = KA * ATOM_BYTES;         // 32 KB of weights per stage
-constexpr int B_BYTES = KA * (NMAX / 2) * BK * 2;  // up to 32 KB of tokens (half the chunk)
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;   // 64 KB
 constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
+constexpr int kMaxStages = 4;
+constexpr int kOutBufs = 12;  // 2 KB output staging buffers: 4 warps x 2, or 12 warps x 1
+
+// Ring geometry by M halves per CTA (MH): MH = 1, 128 weight rows per CTA,
+// stages of two K atoms (weights 32 KB + tokens up to 32 KB) x 3, and two
+// accumulators so the epilogue of a tile overlaps the next tile's MMAs;
+// MH = 2, 256 weight rows per CTA (two M256 MMAs per K16 step share each
+// token slice), stages of one K atom (weights 32 KB + tokens up to 16 KB)
+// x 4, and one accumulator pair filling TMEM.  Both rings are 192 KB.
+template <int MH>
+struct SwGeom {
+  static constexpr int KA = MH == 2 ? 1 : 2;                    // K atoms per stage
+  static constexpr int BKS = BK * KA;                           // K per stage
+  static constexpr int STAGES = MH == 2 ? 4 : 3;
+  static constexpr int A_BYTES = MH * KA * ATOM_BYTES;          // weights per stage
+  static constexpr int B_BYTES = KA * (NMAX / 2) * BK * 2;      // tokens (half the chunk)
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int NACC = MH == 2 ? 1 : 2;                  // accumulator buffers
+  static_assert(STAGES <= kMaxStages && STAGES * STAGE_BYTES == 192 * 1024, "ring");
+};
+constexpr int kRingBytes = 192 * 1024;
 
 // Accumulator layouts: plain (lane = weight row = output column), or gated
 // groups of 8 gate rows then their 8 up rows.
 enum SwMode { kSwPlain = 0, kSwGated = 1 };
 
 struct SwShared {
-  uint64_t full[STAGES];   // leader: both CTAs' copies of a stage complete here
-  uint64_t afull[STAGES];  // peer, cp.async rows: this CTA's rows of a stage landed
-  uint64_t empty[STAGES];  // both: the leader's MMA commit frees the stage
+  uint64_t full[kMaxStages];   // leader: both CTAs' copies of a stage complete here
+  uint64_t afull[kMaxStages];  // peer, cp.async rows: this CTA's rows of a stage landed
+  uint64_t empty[kMaxStages];  // both: the leader's MMA commit frees the stage
   uint64_t tfull[2];       // both: accumulator ready
   uint64_t tempty[2];      // leader: both CTAs' epilogues drained the accumulator
   uint64_t drain;
@@ -90,7 +105,8 @@ struct SwShared {
   int prefix[kMaxExperts + 1];
   int scan_tmp[33];
 };
-constexpr size_t kSmemBytes = (size_t)STAGES * STAGE_BYTES + OUT_BYTES + sizeof(SwShared) + 1024;
+constexpr size_t kSmemBytes =
+    (size_t)kRingBytes + kOutBufs * OUT_BUF_BYTES + sizeof(SwShared) + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -109,10 +125,6 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-               : "memory");
-}
 // TMA loads into this CTA's shared memory that complete on the leader's
 // barrier (shared::cluster address); coordinates innermost first.
 __device__ __forceinline__ void tma2_2d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
@@ -129,6 +141,14 @@ __device__ __forceinline__ void tma2_3d(void* dst, const CUtensorMap* m, uint32_
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
       "bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(su32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma2_4d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
+                                        int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(su32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
 __device__ __forceinline__ void tma2_5d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
@@ -163,6 +183,33 @@ __device__ __forceinline__ void umma2_stage(uint32_t d_tmem, uint64_t ad, uint64
       "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate), "r"(bar), "l"(ad + 2), "l"(bd + 2),
       "l"(ad + 4), "l"(bd + 4), "l"(ad + 6), "l"(bd + 6), "l"(ad1), "l"(bd1), "l"(ad1 + 2),
       "l"(bd1 + 2), "l"(ad1 + 4), "l"(bd1 + 4), "l"(ad1 + 6), "l"(bd1 + 6), "h"((uint16_t)3)
+      : "memory");
+}
+// The eight K16 MMAs of a one-atom stage with two M halves per CTA: half h's
+// weight atom at ad + h * 16 KB accumulates into d0 + h * NMAX, both halves
+// reading the same token slice (bd); then the commit that frees the stage.
+__device__ __forceinline__ void umma2_stage_wide(uint32_t d0, uint64_t ad, uint64_t bd,
+                                                 uint32_t idesc, uint32_t accumulate,
+                                                 uint32_t bar) {
+  const uint64_t a1 = ad + (ATOM_BYTES >> 4);
+  const uint32_t d1 = d0 + NMAX;
+  asm volatile(
+      "{\n\t.reg .pred p, t;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "setp.eq.b32 t, %5, %5;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %2, %3, %4, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%1], %7, %3, %4, p;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %8, %9, %4, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%1], %10, %9, %4, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %11, %12, %4, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%1], %13, %12, %4, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %14, %15, %4, t;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%1], %16, %15, %4, t;\n\t"
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%6], %17;\n\t}" ::"r"(d0),
+      "r"(d1), "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate), "r"(bar), "l"(a1), "l"(ad + 2),
+      "l"(bd + 2), "l"(a1 + 2), "l"(ad + 4), "l"(bd + 4), "l"(a1 + 4), "l"(ad + 6), "l"(bd + 6),
+      "l"(a1 + 6), "h"((uint16_t)3)
       : "memory");
 }
 __device__ __forceinline__ void umma2_commit_both(uint64_t* bar) {
@@ -248,50 +295,94 @@ __device__ __forceinline__ float act1(float x) {
   else return x;
 }
 
+// One 32-token x 32-column box of the calling warp: lane l holds output
+// column f0 + l (fok: inside the output), v[i] the value of token m0 + i.  A
+// whole box goes through swizzled staging and one TMA store; a ragged tail
+// (nval < 32 tokens) is stored row by row (64 contiguous bytes per token).
+template <bool F16, int NBUF>
+__device__ __forceinline__ void sw_emit32(const float (&v)[32], int nval, int m0, int f0, int f,
+                                          int Nout, const CUtensorMap* tm_out, int tma_out,
+                                          __nv_bfloat16* __restrict__ out, uint8_t* obufs,
+                                          int& obuf, int lane) {
+  if (tma_out && nval == 32 && f0 < Nout) {
+    uint8_t* buf = obufs + obuf * OUT_BUF_BYTES;
+    if (lane == 0) bulk_wait_read<NBUF - 1>();  // the store that last read this buffer
+    __syncwarp();
+    // token i, column lane: row i of the box, 64-byte swizzle
+    const uint32_t base = su32(buf) + (uint32_t)((lane & 7) * 2);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      sts16(base + i * 64 + ((((lane >> 3) ^ ((i >> 1) & 3))) << 4), bits16<F16>(v[i]));
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tm_out, buf, f0, m0);
+      bulk_commit();
+    }
+    obuf = NBUF == 1 ? 0 : obuf ^ 1;
+  } else if (f < Nout) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nval) st16<F16>(out + (size_t)(m0 + i) * Nout + f, v[i]);
+  }
+}
+
 // Plain epilogue of the calling warp: TMEM lane l holds output column
-// f0 + l for the tile's tokens (TMEM column j = token m0 + j).  32 tokens at a
-// time: a whole 32 x 32 box goes through swizzled staging and one TMA store;
-// a ragged tail (< 32 tokens) is stored row by row (64 contiguous bytes per
-// token).  Columns at or past Nout are not written.
-template <int ACT, bool F16>
-__device__ __forceinline__ void sw_drain_plain(uint32_t tbase, int nv, int m0, int f0, int Nout,
+// f0 + l for the tile's tokens (TMEM column j = token m0 + j), 32 tokens at a
+// time, the 32-token chunks c0 = cs, cs + step, ...  Columns at or past Nout
+// are not written.
+template <int ACT, bool F16, int NBUF>
+__device__ __forceinline__ void sw_drain_plain(uint32_t tbase, int nv, int cs, int step, int m0,
+                                               int f0, int Nout,
                                                const __nv_bfloat16* __restrict__ bias_e,
                                                const CUtensorMap* tm_out, int tma_out,
                                                __nv_bfloat16* __restrict__ out, uint8_t* obufs,
                                                int& obuf, int lane) {
   const int f = f0 + lane;
-  const bool fok = f < Nout;
-  const float b = bias_e && fok ? ld16<F16>(bias_e + f) : 0.0f;
+  const float b = bias_e && f < Nout ? ld16<F16>(bias_e + f) : 0.0f;
 #pragma unroll 1
-  for (int c0 = 0; c0 < nv; c0 += 32) {
+  for (int c0 = cs; c0 < nv; c0 += step) {
     uint32_t r[32];
     tmem_ld32(tbase + (uint32_t)c0, r);
     tmem_wait_ld();
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = act1<ACT>(__uint_as_float(r[i]) + b);
-    const int nval = min(32, nv - c0);
-    if (tma_out && nval == 32 && f0 < Nout) {
-      uint8_t* buf = obufs + obuf * OUT_BUF_BYTES;
-      if (lane == 0) bulk_wait_read<1>();  // the store that last read this buffer
-      __syncwarp();
-      // token i, column lane: row i of the box, 64-byte swizzle
-      const uint32_t base = su32(buf) + (uint32_t)((lane & 7) * 2);
+    sw_emit32<F16, NBUF>(v, min(32, nv - c0), m0 + c0, f0, f, Nout, tm_out, tma_out, out, obufs,
+                         obuf, lane);
+  }
+}
+
+// Gated epilogue with the gate rows in one M half and the up rows in the
+// other (two M halves per CTA): TMEM lane l of both accumulators belongs to
+// activation column f0 + l, so each lane pairs its own gate and up values.
+// Bias: b[gate row] and b[up row] of the column (stacked: f and F + f;
+// interleaved: 2f and 2f + 1).  Chunks c0 = cs, cs + step, ...
+template <int ACT, bool F16, int NBUF>
+__device__ __forceinline__ void sw_drain_gated_split(
+    uint32_t tgate, uint32_t tup, int nv, int cs, int step, int m0, int f0, int Nout, int F, int interleaved,
+    const __nv_bfloat16* __restrict__ bias_e, float limit, float alpha, float beta,
+    const CUtensorMap* tm_out, int tma_out, __nv_bfloat16* __restrict__ out, uint8_t* obufs,
+    int& obuf, int lane) {
+  const int f = f0 + lane;
+  float bg = 0.0f, bu = 0.0f;
+  if (bias_e && f < Nout) {
+    bg = ld16<F16>(bias_e + (interleaved ? 2 * f : f));
+    bu = ld16<F16>(bias_e + (interleaved ? 2 * f + 1 : F + f));
+  }
+#pragma unroll 1
+  for (int c0 = cs; c0 < nv; c0 += step) {
+    uint32_t rg[32], ru[32];
+    tmem_ld32(tgate + (uint32_t)c0, rg);
+    tmem_ld32(tup + (uint32_t)c0, ru);
+    tmem_wait_ld();
+    float v[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        sts16(base + i * 64 + ((((lane >> 3) ^ ((i >> 1) & 3))) << 4), bits16<F16>(v[i]));
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(tm_out, buf, f0, m0 + c0);
-        bulk_commit();
-      }
-      obuf ^= 1;
-    } else if (fok) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (i < nval) st16<F16>(out + (size_t)(m0 + c0 + i) * Nout + f, v[i]);
-    }
+    for (int i = 0; i < 32; ++i)
+      v[i] = gated<ACT>(__uint_as_float(rg[i]) + bg, __uint_as_float(ru[i]) + bu, limit, alpha,
+                        beta);
+    sw_emit32<F16, NBUF>(v, min(32, nv - c0), m0 + c0, f0, f, Nout, tm_out, tma_out, out, obufs,
+                         obuf, lane);
   }
 }
 
@@ -330,8 +421,9 @@ __device__ __forceinline__ void sw_drain_gated(uint32_t tbase, int nv, int m0, i
     for (int i = 0; i < 16; ++i) {
       const float lo = __uint_as_float(r[i]) + b, hi = __uint_as_float(r[16 + i]) + b;
       const float recv = __shfl_xor_sync(0xffffffffu, is_gate ? hi : lo, 8);
-      a[i] = is_gate ? gated<ACT>(lo, recv, limit, alpha, beta)
-                     : gated<ACT>(recv, hi, limit, alpha, beta);
+      // one activation per value on selected operands (no per-lane branch)
+      const float g = is_gate ? lo : recv, u = is_gate ? recv : hi;
+      a[i] = gated<ACT>(g, u, limit, alpha, beta);
     }
     const int tok0 = is_gate ? 0 : 16;  // this lane's tokens: c0 + tok0 + i
     const int nval = min(32, nv - c0);
@@ -364,6 +456,18 @@ enum SwTok {
 };
 constexpr int kLoaderWarp0 = NUM_THREADS / 32;
 constexpr int NUM_THREADS_LOAD = NUM_THREADS + 128;
+// Epilogue warpgroups: three (warps 2..5, 6..9 and 10..13, taking the
+// 32-token chunks in turn) when the next tile's MMAs wait for the drain (two
+// M halves, one accumulator pair) and no loader warps are needed (tiled
+// token rows); else one (warps 2..5).
+template <int TOK, int MH>
+struct SwRoles {
+  static constexpr int EPI_GROUPS = TOK == kTokTiled && MH == 2 ? 3 : 1;
+  static constexpr int THREADS = EPI_GROUPS == 3 ? NUM_THREADS + 256
+                                 : TOK == kTokCpAsync ? NUM_THREADS_LOAD
+                                                      : NUM_THREADS;
+  static constexpr int NBUF = EPI_GROUPS > 1 ? 1 : 2;  // staging buffers per epilogue warp
+};
 
 __device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
@@ -387,8 +491,8 @@ __device__ __forceinline__ int tok_box_sel(int half) { return half <= 32 ? 0 : h
 // segmented row space is source row grows[r] / gdiv (the hidden states read
 // through the permutation; rows with an out-of-range entry read zeros) or,
 // without grows, row r of the source itself.
-template <int MODE, int ACT, bool F16, int TOK>
-__global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_THREADS, 1)
+template <int MODE, int ACT, bool F16, int TOK, int MH>
+__global__ void __launch_bounds__(SwRoles<TOK, MH>::THREADS, 1)
     gemm_sw_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ TokMaps tm_a,
                    const __grid_constant__ CUtensorMap tm_out, int tma_out,
                    const __nv_bfloat16* __restrict__ bias, const int32_t* __restrict__ seg_end,
@@ -396,11 +500,15 @@ __global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_TH
                    float alpha, float beta, __nv_bfloat16* __restrict__ out, int* status,
                    const __nv_bfloat16* __restrict__ asrc, const int32_t* __restrict__ grows,
                    int gdiv, int src_rows, int seg_stride) {
+  using G = SwGeom<MH>;
+  constexpr int STAGES = G::STAGES, STAGE_BYTES = G::STAGE_BYTES, A_BYTES = G::A_BYTES;
+  constexpr int KA = G::KA, BKS = G::BKS, NACC = G::NACC;
+  using R = SwRoles<TOK, MH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* out_stage = smem + (size_t)STAGES * STAGE_BYTES;  // 1024-byte aligned
-  SwShared* sh = reinterpret_cast<SwShared*>(out_stage + OUT_BYTES);
+  uint8_t* out_stage = smem + (size_t)kRingBytes;  // 1024-byte aligned
+  SwShared* sh = reinterpret_cast<SwShared*>(out_stage + kOutBufs * OUT_BUF_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
@@ -417,7 +525,7 @@ __global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_TH
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&sh->tfull[a], 1);
-      mbar_init(&sh->tempty[a], 2 * 128);
+      mbar_init(&sh->tempty[a], 2 * 128 * R::EPI_GROUPS);
     }
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
@@ -437,8 +545,10 @@ __global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_TH
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
-  const int n_ftiles = MODE == kSwPlain ? (Nout + 2 * ROWS - 1) / (2 * ROWS)
-                                        : (Nout + ROWS - 1) / ROWS;
+  // a pair tile covers 2 * ROWS * MH weight rows: as many output columns
+  // (plain), or half as many activation columns (gated)
+  const int n_ftiles = MODE == kSwPlain ? (Nout + 2 * ROWS * MH - 1) / (2 * ROWS * MH)
+                                        : (Nout + ROWS * MH - 1) / (ROWS * MH);
   // everything above overlaps the previous launch; seg_end and the operands
   // are read only after this
   pdl_wait();
@@ -474,14 +584,19 @@ __global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_TH
           const uint32_t bar = map_to_rank(su32(&sh->full[stage]), 0);
           if (leader) mbar_expect_tx(&sh->full[stage], 2 * tx);
 #pragma unroll
-          for (int a = 0; a < KA; ++a) {  // one box per K atom and operand
+          for (int a = 0; a < KA; ++a) {  // one box per K atom, M half and operand
             const int k0 = ks * BKS + a * BK;
-            if constexpr (MODE == kSwPlain)
-              tma2_3d(a_dst + a * ATOM_BYTES, &tm_w, bar, k0,
-                      st.nt * 2 * ROWS + ROWS * (int)rank, st.e);
-            else
-              tma2_5d(a_dst + a * ATOM_BYTES, &tm_w, bar, k0, 0, 0,
-                      st.nt * 16 + 8 * (int)rank, st.e);
+#pragma unroll
+            for (int h = 0; h < MH; ++h) {
+              uint8_t* dst = a_dst + (a * MH + h) * ATOM_BYTES;
+              if constexpr (MODE == kSwPlain)
+                tma2_3d(dst, &tm_w, bar, k0,
+                        (st.nt * MH + h) * 2 * ROWS + ROWS * (int)rank, st.e);
+              else if constexpr (MH == 2)  // half 0 the gate rows, half 1 the up rows
+                tma2_4d(dst, &tm_w, bar, k0, st.nt * 2 * ROWS + ROWS * (int)rank, h, st.e);
+              else
+                tma2_5d(dst, &tm_w, bar, k0, 0, 0, st.nt * 16 + 8 * (int)rank, st.e);
+            }
             if constexpr (TOK == kTokTiled)
               tma2_2d(b_dst + a * ((32 << bsel) * BK * 2), &tm_a.m[bsel], bar, k0,
                       st.m0 + (int)rank * half);
@@ -508,7 +623,7 @@ __global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_TH
       for (int tile = pair; tile < total && ok; tile += npairs) {
         const SwTile st = decode(tile);
         if (st.nv == 0) continue;
-        const uint32_t idesc = idesc_sw(2 * ROWS, st.N, F16 ? 1 : 0);
+        const uint32_t idesc = idesc_sw(2 * ROWS, st.N, F16 ? 1 : 0);  // M256 per MMA
         // token atoms h rows apart (16-byte descriptor units)
         const uint32_t b_atom16 = (uint32_t)((32 << tok_box_sel(st.N >> 1)) * BK * 2) >> 4;
         if (!wait_fast(&sh->tempty[acc], aphase ^ 1u, abort_flag, status)) { ok = false; break; }
@@ -522,14 +637,18 @@ __global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_TH
           if constexpr (TOK == kTokCpAsync) fence_proxy_async_smem();
           tc_fence_after();
           const uint64_t off = (uint64_t)((stage * STAGE_BYTES) >> 4);
-          umma2_stage(d_tmem, adesc0 + off, bdesc0 + off, b_atom16, idesc, ks != 0 ? 1u : 0u,
-                      empty_addr[stage]);
+          if constexpr (MH == 2)
+            umma2_stage_wide(d_tmem, adesc0 + off, bdesc0 + off, idesc, ks != 0 ? 1u : 0u,
+                             empty_addr[stage]);
+          else
+            umma2_stage(d_tmem, adesc0 + off, bdesc0 + off, b_atom16, idesc, ks != 0 ? 1u : 0u,
+                        empty_addr[stage]);
           any = true;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
         umma2_commit_both(&sh->tfull[acc]);
-        if (++acc == 2) { acc = 0; aphase ^= 1u; }
+        if (++acc == NACC) { acc = 0; aphase ^= 1u; }
       }
       if (!ok && any) {
         umma2_commit_self(&sh->drain);
@@ -625,30 +744,50 @@ __global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_TH
   } else {
     // ------------------------------------------------ epilogue (both CTAs)
     const int quad = warp & 3;
+    const int grp = (warp - 2) >> 2;  // epilogue warpgroup
+    const int cs = 32 * grp, step = 32 * R::EPI_GROUPS;
     int acc = 0;
     uint32_t aphase = 0;
     const uint32_t tempty_remote[2] = {map_to_rank(su32(&sh->tempty[0]), 0),
                                        map_to_rank(su32(&sh->tempty[1]), 0)};
-    uint8_t* obufs = out_stage + quad * 2 * OUT_BUF_BYTES;
+    // staging buffers of 2 KB: two per warp of one group, or one per warp
+    uint8_t* obufs = out_stage + (grp * 4 + quad) * R::NBUF * OUT_BUF_BYTES;
     int obuf = 0;
     for (int tile = pair; tile < total; tile += npairs) {
       const SwTile st = decode(tile);
       if (st.nv == 0) continue;
       if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
       tc_fence_after();
-      const uint32_t tb =
-          tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * NMAX);
       const __nv_bfloat16* be = bias ? bias + (size_t)st.e * N1 : nullptr;
-      if constexpr (MODE == kSwPlain)
-        sw_drain_plain<ACT, F16>(tb, st.nv, st.m0, st.nt * 2 * ROWS + ROWS * (int)rank + 32 * quad,
-                                 Nout, be, &tm_out, tma_out, out, obufs, obuf, lane);
-      else
-        sw_drain_gated<ACT, F16>(tb, st.nv, st.m0, st.nt * ROWS + (ROWS / 2) * (int)rank + 16 * quad,
-                                 Nout, Nout, interleaved, be, limit, alpha, beta, &tm_out, tma_out,
-                                 out, obufs, obuf, lane);
+      const uint32_t tq = tmem_base + ((uint32_t)(quad * 32) << 16);
+      if constexpr (MODE == kSwGated && MH == 2) {
+        sw_drain_gated_split<ACT, F16, R::NBUF>(tq, tq + NMAX, st.nv, cs, step, st.m0,
+                                       st.nt * 2 * ROWS + ROWS * (int)rank + 32 * quad, Nout, Nout,
+                                       interleaved, be, limit, alpha, beta, &tm_out, tma_out, out,
+                                       obufs, obuf, lane);
+      } else {
+#pragma unroll 1
+        for (int h = 0; h < MH; ++h) {
+          // MH = 2: half h in columns h * NMAX of the one accumulator pair
+          const uint32_t tb = tq + (uint32_t)((MH == 2 ? h : acc) * NMAX);
+          const int g = st.nt * MH + h;  // 256-weight-row group of the expert
+          if constexpr (MODE == kSwPlain)
+            sw_drain_plain<ACT, F16, R::NBUF>(tb, st.nv, cs, step, st.m0,
+                                     g * 2 * ROWS + ROWS * (int)rank + 32 * quad, Nout, be,
+                                     &tm_out, tma_out, out, obufs, obuf, lane);
+          else
+            sw_drain_gated<ACT, F16>(tb, st.nv, st.m0,
+                                     g * ROWS + (ROWS / 2) * (int)rank + 16 * quad, Nout, Nout,
+                                     interleaved, be, limit, alpha, beta, &tm_out, tma_out, out,
+                                     obufs, obuf, lane);
+        }
+      }
+      // the drain's TMEM loads have completed (tcgen05.wait::ld): a CTA-scope
+      // release orders them before the leader's next MMAs (a cluster-scope
+      // one would also wait for every copy this SM has in flight)
       tc_fence_before();
-      mbar_arrive_remote(tempty_remote[acc]);
-      if (++acc == 2) { acc = 0; aphase ^= 1u; }
+      mbar_arrive_remote_cta(tempty_remote[acc]);
+      if (++acc == NACC) { acc = 0; aphase ^= 1u; }
     }
     if (lane == 0) bulk_wait_all();  // every staged box written before the pair exits
   }
@@ -669,26 +808,35 @@ __global__ void __launch_bounds__(TOK == kTokCpAsync ? NUM_THREADS_LOAD : NUM_TH
 // ------------------------------------------------------------ host side
 namespace {
 
-template <int MODE, int ACT, bool F16, int TOK>
+template <int MODE, int ACT, bool F16, int TOK, int MH>
 const void* sw_kernel_ptr() {
-  return (const void*)gemm_sw_kernel<MODE, ACT, F16, TOK>;
+  return (const void*)gemm_sw_kernel<MODE, ACT, F16, TOK, MH>;
 }
 
-template <bool F16, int TOK>
+template <bool F16, int TOK, int MH>
 const void* pick_sw(int mode, int kind) {
   if (mode == kSwPlain) {
     switch (kind) {
-      case MOE_ACT_RELU: return sw_kernel_ptr<kSwPlain, MOE_ACT_RELU, F16, TOK>();
-      case MOE_ACT_GELU: return sw_kernel_ptr<kSwPlain, MOE_ACT_GELU, F16, TOK>();
-      case MOE_ACT_SILU: return sw_kernel_ptr<kSwPlain, MOE_ACT_SILU, F16, TOK>();
-      default: return sw_kernel_ptr<kSwPlain, MOE_ACT_IDENTITY, F16, TOK>();
+      case MOE_ACT_RELU: return sw_kernel_ptr<kSwPlain, MOE_ACT_RELU, F16, TOK, MH>();
+      case MOE_ACT_GELU: return sw_kernel_ptr<kSwPlain, MOE_ACT_GELU, F16, TOK, MH>();
+      case MOE_ACT_SILU: return sw_kernel_ptr<kSwPlain, MOE_ACT_SILU, F16, TOK, MH>();
+      default: return sw_kernel_ptr<kSwPlain, MOE_ACT_IDENTITY, F16, TOK, MH>();
     }
   }
   switch (kind) {
-    case MOE_ACT_SWIGLU: return sw_kernel_ptr<kSwGated, MOE_ACT_SWIGLU, F16, TOK>();
-    case MOE_ACT_GELU_AND_MUL: return sw_kernel_ptr<kSwGated, MOE_ACT_GELU_AND_MUL, F16, TOK>();
-    default: return sw_kernel_ptr<kSwGated, MOE_ACT_SILU_AND_MUL, F16, TOK>();
+    case MOE_ACT_SWIGLU: return sw_kernel_ptr<kSwGated, MOE_ACT_SWIGLU, F16, TOK, MH>();
+    case MOE_ACT_GELU_AND_MUL:
+      return sw_kernel_ptr<kSwGated, MOE_ACT_GELU_AND_MUL, F16, TOK, MH>();
+    default: return sw_kernel_ptr<kSwGated, MOE_ACT_SILU_AND_MUL, F16, TOK, MH>();
   }
+}
+
+template <int MH>
+const void* pick_sw_mh(bool f16, int tok, int mode, int kind) {
+  return tok == kTokTiled ? (f16 ? pick_sw<true, kTokTiled, MH>(mode, kind)
+                                 : pick_sw<false, kTokTiled, MH>(mode, kind))
+                          : (f16 ? pick_sw<true, kTokCpAsync, MH>(mode, kind)
+                                 : pick_sw<false, kTokCpAsync, MH>(mode, kind));
 }
 
 }  // namespace
@@ -696,7 +844,8 @@ const void* pick_sw(int mode, int kind) {
 cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s, const int32_t* gather_rows,
-                           int gather_div, int gather_src_rows, int seg_stride, bool f16) {
+                           int gather_div, int gather_src_rows, int seg_stride, bool f16,
+                           bool wide) {
   if (M == 0 || N == 0) return cudaSuccess;
   int mode = kSwPlain, kind = MOE_ACT_IDENTITY, N1 = N, inter = 0;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
@@ -717,6 +866,17 @@ cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const
     cuuint64_t str[2] = {K2, (cuuint64_t)N1 * K2};
     cuuint32_t box[3] = {BK, ROWS, 1};
     if (!tmap::encode_bf16(&mw, w, 3, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B, f16))
+      return cudaErrorInvalidValue;
+  } else if (wide) {
+    // [E][2][F][K]: the gate rows (index 0) and the up rows (index 1) of the
+    // activation columns (stacked: up rows F below the gate rows;
+    // interleaved: rows 2j, 2j + 1), one 128-row box per M half
+    cuuint64_t dims[4] = {(cuuint64_t)K, (cuuint64_t)N, 2, (cuuint64_t)E};
+    cuuint64_t st_stacked[3] = {K2, (cuuint64_t)N * K2, (cuuint64_t)N1 * K2};
+    cuuint64_t st_inter[3] = {2 * K2, K2, (cuuint64_t)N1 * K2};
+    cuuint32_t box[4] = {BK, ROWS, 1, 1};
+    if (!tmap::encode_bf16(&mw, w, 4, dims, inter ? st_inter : st_stacked, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, f16))
       return cudaErrorInvalidValue;
   } else {
     // groups of 8 activation columns: their 8 gate rows, then their 8 up rows
@@ -745,33 +905,34 @@ cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const
     ma.m[0] = ma.m[1] = ma.m[2] = mw;  // unused
   }
   // staged output boxes: 32 columns x 32 rows (64-byte swizzle), or 16 x 32
-  // for the gated mode; rows stored directly when the output's base or pitch
-  // is not 16-byte aligned
+  // for the gated mode with gate and up rows in one M half; rows stored
+  // directly when the output's base or pitch is not 16-byte aligned
   int tma_out = 0;
   if ((reinterpret_cast<uintptr_t>(out) & 15) == 0) {
+    const bool box32 = mode == kSwPlain || wide;
     cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
     cuuint64_t str[1] = {(cuuint64_t)N * 2};
-    cuuint32_t box[2] = {mode == kSwPlain ? 32u : 16u, 32u};
+    cuuint32_t box[2] = {box32 ? 32u : 16u, 32u};
     tma_out = tmap::encode_bf16(&mo, out, 2, dims, str, box,
-                                mode == kSwPlain ? CU_TENSOR_MAP_SWIZZLE_64B
-                                                 : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                box32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE,
                                 f16)
                   ? 1
                   : 0;
   }
   if (!tma_out) mo = mw;  // unused
-  const void* kern = tok == kTokTiled ? (f16 ? pick_sw<true, kTokTiled>(mode, kind)
-                                              : pick_sw<false, kTokTiled>(mode, kind))
-                                       : (f16 ? pick_sw<true, kTokCpAsync>(mode, kind)
-                                              : pick_sw<false, kTokCpAsync>(mode, kind));
+  const int mh = wide ? 2 : 1;
+  const void* kern = wide ? pick_sw_mh<2>(f16, tok, mode, kind) : pick_sw_mh<1>(f16, tok, mode, kind);
   set_smem_limit(kern, (int)kSmemBytes);
-  const int n_ftiles = mode == kSwPlain ? (N + 2 * ROWS - 1) / (2 * ROWS) : (N + ROWS - 1) / ROWS;
+  const int n_ftiles = mode == kSwPlain ? (N + 2 * ROWS * mh - 1) / (2 * ROWS * mh)
+                                        : (N + ROWS * mh - 1) / (ROWS * mh);
   const long long max_tiles = (long long)((M + NMAX - 1) / NMAX + E) * n_ftiles;
   const int pairs = (int)std::max<long long>(1, std::min<long long>(max_tiles, num_sms() / 2));
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(tok == kTokCpAsync ? NUM_THREADS_LOAD : NUM_THREADS);
+  cfg.blockDim = dim3(tok == kTokTiled && wide ? NUM_THREADS + 256
+                      : tok == kTokCpAsync    ? NUM_THREADS_LOAD
+                                              : NUM_THREADS);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];

@@ -365,26 +365,26 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
                            const SplitUp* split, bool f16) {
   if (M == 0 || N == 0) return cudaSuccess;
   // The weights-as-M kernel on SM pairs (gemm_sw.cu) pads an expert's rows to
-  // 16 instead of 128; measured against this kernel on the workloads, it is
-  // faster only on plain products over contiguous rows with long K and full
-  // 256-token chunks (the DeepSeek-V3-style down GEMM: 1.63 vs 1.75 ms; on
-  // the gpt-oss-style one, 64 rows per expert, 365 vs 356 us), where it is
-  // the default.
-  // MOE_TC_KERNEL=1sm keeps every call on this kernel, =sw sends every call it
-  // can take to the pair kernel (both settings exist to check the kernels
-  // against each other).
+  // 16 instead of 128.  Its wide form (256 weight rows per CTA, two M256
+  // accumulators) is the default for products with long K and segments
+  // averaging >= 128 rows, gathered or not, plain or gated: measured on the
+  // DeepSeek-V3-style GEMMs 2.87 vs 3.32 ms (gathered gate_up) and 1.61 vs
+  // 1.75 ms (down), on the Qwen3-style gate_up 195 vs 197 us; with short K
+  // (Qwen3-style down, 136 vs 111 us) or 64-row segments (gpt-oss-style, 674
+  // vs 640 us) this kernel is faster.
+  // MOE_TC_KERNEL=1sm keeps every call on this kernel, =sw sends every call
+  // the pair kernel can take to its 128-row form, =wide to its wide form
+  // (the settings exist to check the kernels against each other).
   static const int which = [] {
     const char* v = getenv("MOE_TC_KERNEL");
-    return v && v[0] == '1' ? 1 : v && v[0] == 's' ? 2 : 0;
+    return v && v[0] == '1' ? 1 : v && v[0] == 's' ? 2 : v && v[0] == 'w' ? 3 : 0;
   }();
   const bool gather = gather_rows != nullptr;
-  const bool gated = act && act_is_gated(act->kind);
   const bool sw_ok = !split && num_sms() >= 2 && N % 8 == 0 && K % 8 == 0;
-  const bool sw_pick =
-      which == 2 || (which == 0 && !gather && !gated && K >= 2048 && (long long)M >= 128LL * E);
-  if (sw_ok && sw_pick)
+  const bool wide_pick = which == 0 && K >= 2048 && (long long)M >= 128LL * E;
+  if (sw_ok && (which >= 2 || wide_pick))
     return launch_gemm_sw(a, w, bias, seg_end, M, N, K, E, act, out, status, s, gather_rows,
-                          gather_div, gather_src_rows, seg_stride, f16);
+                          gather_div, gather_src_rows, seg_stride, f16, which != 2);
   int mode = kTcPlain, kind = MOE_ACT_IDENTITY, N1 = N;
   float limit = 0.f, alpha = 1.f, beta = 0.f;
   if (act) kind = act->kind;

@@ -168,10 +168,12 @@ cudaError_t launch_gemm_tc(const void* a, const void* w, const void* bias, const
 
 // The weights-as-M tcgen05 grouped GEMM on SM pairs (gemm_sw.cu): the same
 // contract as launch_gemm_tc without split weights; N and K multiples of 8.
+// wide: 256 weight rows per CTA (two M256 accumulators) instead of 128.
 cudaError_t launch_gemm_sw(const void* a, const void* w, const void* bias, const int32_t* seg_end,
                            int M, int N, int K, int E, const moe_act_params* act, void* out,
                            int* status, cudaStream_t s, const int32_t* gather_rows,
-                           int gather_div, int gather_src_rows, int seg_stride, bool f16);
+                           int gather_div, int gather_src_rows, int seg_stride, bool f16,
+                           bool wide);
 
 // block-scaled FP8 grouped GEMM over a masked slab (e4m3 operands, fp32
 // scales per row x 128 K of a and per 128 x 128 block of b, bf16 out)

@@ -1,8 +1,9 @@
-"""Both tcgen05 grouped-GEMM kernels on every call they can take: the one-SM
-row-tile kernel alone (MOE_TC_KERNEL=1sm) and the weights-as-M kernel on SM
-pairs (MOE_TC_KERNEL=sw), each running the whole grouped-GEMM parity file
-(gathered rows included) and the small whole-forward cases in a fresh
-process (the switch is read once per process)."""
+"""Every tcgen05 grouped-GEMM kernel on every call it can take: the one-SM
+row-tile kernel alone (MOE_TC_KERNEL=1sm), and the weights-as-M kernel on SM
+pairs with 128 (MOE_TC_KERNEL=sw) or 256 (MOE_TC_KERNEL=wide) weight rows
+per CTA, each running the whole grouped-GEMM parity file (gathered rows
+included) and the small whole-forward cases in a fresh process (the switch
+is read once per process)."""
 import os
 import subprocess
 import sys
@@ -14,7 +15,7 @@ pytestmark = pytest.mark.gpu
 HERE = os.path.dirname(os.path.abspath(__file__))
 
 
-@pytest.mark.parametrize("kernel", ["1sm", "sw"])
+@pytest.mark.parametrize("kernel", ["1sm", "sw", "wide"])
 def test_alternative_gemm_kernel_parity(kernel):
     env = dict(os.environ, MOE_TC_KERNEL=kernel)
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(HERE, "test_gpu_gemm.py"),
