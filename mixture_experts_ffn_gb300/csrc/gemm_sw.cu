@@ -13,38 +13,56 @@
 // cycles per K16 step from N = 128 up, measured).  The weights fill M with
 // no padding: 256 weight rows per CTA pair.
 //
-// Work decomposition
-//   pair tile = 256 weight rows (128 per CTA) x one token chunk of an expert
-//   (N <= 256 tokens, a multiple of 16; an expert of n rows is cut into
-//   ceil(n / 256) chunks of equal size rounded up to 16).  A ring stage holds
-//   two 64-wide K atoms: per CTA its 128 weight rows (TMA, 2 x 16 KB) and its
-//   half of the chunk's token rows.  Contiguous token rows come by a tiled
-//   TMA box of 32, 64 or 128 rows per atom.  Rows gathered through the
-//   permutation (the forward's gate_up) come by cp.async from four loader
-//   warps, and the peer's loaders' arrivals reach the leader through a
-//   forwarding thread.  Both CTAs' copies complete on the leader's barriers;
-//   the leader issues eight M256 x N x K16 MMAs per stage into the pair's
-//   TMEM; 3 stages (192 KB).
-//   Gated modes: a 5-D tensor map loads each group of 8 gate rows next to its
-//   8 up rows, so TMEM lane l (gate) and lane l ^ 8 (up) of one warp hold the
-//   two halves of one activation column; 64 activation columns per CTA.
-// Roles (192 threads per CTA, + 128 with cp.async token rows)
+// Two forms, chosen per call (MH = M halves per CTA):
+//
+// Wide form (MH = 2; the default for long-K products whose segments
+// average >= 128 rows):
+//   pair tile = 512 weight rows (256 per CTA, two M halves) x one token chunk
+//   of an expert (N <= 256 tokens, a multiple of 16; an expert of n rows is
+//   cut into ceil(n / 256) chunks of equal size rounded up to 16).  Each K16
+//   step issues two M256 x N MMAs, one per half, both reading the same token
+//   slice, into two 256-column accumulators that fill TMEM.  A ring stage is
+//   one 64-wide K atom: per CTA 2 x 16 KB of weights and its half of the
+//   chunk's token rows (<= 16 KB); 4 stages.  Two thirds of every stage are
+//   weights, against half in the narrow form, so more DRAM bytes are in
+//   flight per SM.  Gated modes put a CTA's gate rows in one half and the
+//   matching up rows in the other (a 4-D map [E][2][F][K]), so TMEM lane l of
+//   both accumulators belongs to one activation column and each lane pairs
+//   its own values.  With one accumulator pair the next tile's MMAs wait for
+//   the drain: with tiled token rows three epilogue warpgroups share it.
+// Narrow form (MH = 1):
+//   pair tile = 256 weight rows (128 per CTA) x one token chunk; a stage
+//   holds two K atoms (weights 2 x 16 KB, tokens up to 32 KB); 3 stages; two
+//   256-column accumulators, so the epilogue of one tile overlaps the next
+//   tile's MMAs.  Gated modes: a 5-D tensor map loads each group of 8 gate
+//   rows next to its 8 up rows (TMEM lanes l and l ^ 8 of one warp), and the
+//   epilogue pairs them with one shfl_xor per value.
+// Both forms: contiguous token rows come by a tiled TMA box of 32, 64 or
+// 128 rows per atom; rows gathered through the permutation (the forward's
+// gate_up) come by cp.async from four loader warps, and the peer's loaders'
+// arrivals reach the leader through a forwarding thread.  Both CTAs' copies
+// complete on the leader's barriers; the leader issues eight MMAs per stage
+// and multicasts the commit that frees it in both CTAs.  The ring is 192 KB.
+// Roles (192 threads per CTA; 320 with cp.async token rows; 448 in the wide
+// form with tiled token rows)
 //   warp 0 lane 0 : producer -- the weight boxes, the tiled token boxes, and
 //                   in the leader the stage's expected bytes
 //   warp 1        : TMEM allocation (pair); lane 0 of the leader issues MMAs,
 //                   lane 0 of the peer forwards its cp.async arrivals
 //   warps 2..5    : epilogue of the CTA's 128 TMEM lanes (bias, activation,
 //                   rounding, transposed staging and TMA stores)
-//   warps 6..9    : cp.async token loaders (gathered rows only)
-// Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
-// tile overlap the main loop of the next.  Every wait is bounded (2 s); on a
-// timeout the block latches the timeout bit, drains what it issued and frees
-// TMEM.
+//   warps 6..9    : cp.async token loaders (gathered rows), or with 448
+//                   threads, like warps 10..13, more epilogue warpgroups
+//                   (the 32-token chunks of a tile taken in turn; loader
+//                   warps that also drained between their copies were
+//                   measured slower, 2.87 vs 2.81 ms)
+// Every wait is bounded (2 s); on a timeout the block latches the timeout
+// bit, drains what it issued and frees TMEM.
 //
-// Measured against the one-SM kernel (gemm_tc.cu), this kernel is faster only
-// on plain products over contiguous rows with long K (the DeepSeek-V3-style
-// down GEMM); both stream weights at ~60% of DRAM, bounded by how fast an
-// operand ring of ~192 KB per SM turns over against DRAM latency under load.
+// Measured (DeepSeek-V3-style workload, CUDA events): gathered gate_up 2.87
+// ms wide vs 3.25 ms narrow vs 3.32 ms for the one-SM row-tile kernel
+// (gemm_tc.cu); down 1.53 vs 1.61 vs 1.75 ms.  With short K (Qwen3-style
+// down) or 64-row segments (gpt-oss-style) the one-SM kernel is faster.
 #include <cuda.h>
 
 #include <algorithm>
