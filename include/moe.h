@@ -584,9 +584,10 @@ size_t moe_workspace_size_shared(int T, int H, int F, int S, int E, int K, moe_d
  * query of [ORT-MoE].) */
 
 /* Bytes at the start of every workspace that hold the device status word
- * (and the grid-barrier counters of the fused route + permute launch, which
- * reset themselves after every successful launch).  Clear them with
- * moe_clear_status before a workspace's first use and after an error. */
+ * (and the grid-barrier counters of the fused route + permute launch and the
+ * tile counters of the SM-pair grouped GEMM, which reset themselves after
+ * every successful launch).  Clear them with moe_clear_status before a
+ * workspace's first use and after an error. */
 #define MOE_STATUS_BYTES 256
 
 /* Workspace bytes moe_ffn_forward / moe_indexed_mlp need for these extents. */

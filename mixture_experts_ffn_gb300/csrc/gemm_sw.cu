@@ -43,6 +43,12 @@
 // arrivals reach the leader through a forwarding thread.  Both CTAs' copies
 // complete on the leader's barriers; the leader issues eight MMAs per stage
 // and multicasts the commit that frees it in both CTAs.  The ring is 192 KB.
+// Tile schedule: pairs take tiles round-robin except for the last two
+// rounds, whose tiles go to whichever pair asks first (a counter in the
+// workspace's status area that the launch's last pair resets), so that
+// pairs with light tiles do not idle while others finish heavy ones.  The
+// leader's producer picks each tile and publishes it to every role of both
+// CTAs through a small ring of shared-memory entries.
 // Roles (192 threads per CTA; 320 with cp.async token rows; 448 in the wide
 // form with tiled token rows)
 //   warp 0 lane 0 : producer -- the weight boxes, the tiled token boxes, and
@@ -87,6 +93,14 @@ constexpr int TMEM_COLS = 512;
 constexpr int NUM_THREADS = 192;
 constexpr int kMaxStages = 4;
 constexpr int kOutBufs = 12;  // 2 KB output staging buffers: 4 warps x 2, or 12 warps x 1
+// Dynamic tile schedule: the leader's producer takes the next tile of the
+// list from a global counter when it is ready to load it and publishes it to
+// both CTAs' rings of kSched entries.  No role of a pair trails the
+// producer by more than STAGES + 3 tiles (its ring stages wait for the MMAs,
+// which wait for the drain of the tile before last), so entries are never
+// overwritten unread.
+constexpr int kSched = 16;
+constexpr int kNoTile = 0x7fffffff;
 
 // Ring geometry by M halves per CTA (MH): MH = 1, 128 weight rows per CTA,
 // stages of two K atoms (weights 32 KB + tokens up to 32 KB) x 3, and two
@@ -122,6 +136,8 @@ struct SwShared {
   int abort;
   int prefix[kMaxExperts + 1];
   int scan_tmp[33];
+  int sched[kSched];        // tile of schedule entry j at j % kSched (kNoTile: none left)
+  uint64_t sfull[kSched];   // entry j written (phase (j / kSched) & 1)
 };
 constexpr size_t kSmemBytes =
     (size_t)kRingBytes + kOutBufs * OUT_BUF_BYTES + sizeof(SwShared) + 1024;
@@ -143,6 +159,46 @@ __device__ __forceinline__ void cluster_sync() {
       "barrier.cluster.wait.acquire.aligned;" ::
           : "memory");
 }
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait, acquiring at cluster scope (the entry may have been written
+// by the peer CTA); false on abort or timeout.
+__device__ __noinline__ bool wait_cluster(uint64_t* b, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  const uint32_t addr = su32(b);
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait_cluster(addr, parity)) {
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      latch_error(status, kDevTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+// v to the peer's shared memory at addr_cluster, completing on the peer's
+// barrier bar_cluster (4 bytes of transaction, and the one arrival the phase
+// expects): no fence, the barrier's transaction count orders the data.
+__device__ __forceinline__ void publish_remote_u32(uint32_t addr_cluster, uint32_t bar_cluster,
+                                                   int v) {
+  asm volatile(
+      "mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], 4;\n\t"
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%1], %2, [%0];" ::"r"(
+          bar_cluster),
+      "r"(addr_cluster), "r"(v)
+      : "memory");
+}
+
 // TMA loads into this CTA's shared memory that complete on the leader's
 // barrier (shared::cluster address); coordinates innermost first.
 __device__ __forceinline__ void tma2_2d(void* dst, const CUtensorMap* m, uint32_t bar, int c0,
@@ -546,6 +602,7 @@ __global__ void __launch_bounds__(SwRoles<TOK, MH>::THREADS, 1)
       mbar_init(&sh->tempty[a], 2 * 128 * R::EPI_GROUPS);
     }
     mbar_init(&sh->drain, 1);
+    for (int i = 0; i < kSched; ++i) mbar_init(&sh->sfull[i], 1);
     sh->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -579,6 +636,16 @@ __global__ void __launch_bounds__(SwRoles<TOK, MH>::THREADS, 1)
   const int nks = (K + BKS - 1) / BKS;  // ring stages per tile
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   auto decode = [&](int t) { return sw_decode(t, sh->prefix, seg_end, E, M, n_ftiles, seg_stride); };
+  // schedule: gctr[0] is the next tile of the list, gctr[1] the pairs done
+  // taking tiles; the last of them zeroes both for the next launch (a launch
+  // that failed leaves them for the status clear the error requires)
+  int* gctr = status + 8;
+  // entry j of the schedule (kNoTile: no tiles left, or the wait failed)
+  auto next_tile = [&](int j) -> int {
+    if (!wait_cluster(&sh->sfull[j % kSched], (uint32_t)(j / kSched) & 1u, abort_flag, status))
+      return kNoTile;
+    return *reinterpret_cast<volatile int*>(&sh->sched[j % kSched]);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -587,10 +654,36 @@ __global__ void __launch_bounds__(SwRoles<TOK, MH>::THREADS, 1)
       uint32_t phase = 0;
       uint32_t issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = 0;
-      bool ok = true;
-      for (int tile = pair; tile < total && ok; tile += npairs) {
+      bool ok = true, done = false;
+      // The leader's tiles: round-robin for all but the last two rounds (the
+      // pairs that share a weight tile stay in step), then the next tile of
+      // the rest from the counter (the pairs finish together).  It takes a
+      // tile one ahead (the counter's latency hides behind the current
+      // tile's copies), skips empty ones, and publishes it.
+      const int r_static = max(0, total / npairs - 2);
+      int k_static = 0;
+      auto grab = [&]() {
+        return k_static < r_static ? pair + npairs * k_static++
+                                   : npairs * r_static + atomicAdd(gctr, 1);
+      };
+      int ahead = leader ? grab() : 0;
+      for (int j = 0; ok; ++j) {
+        int tile;
+        if (leader) {
+          tile = ahead;
+          while (tile < total && decode(tile).nv == 0) tile = grab();
+          if (tile >= total) tile = kNoTile;
+          else ahead = grab();
+          const int slot = j % kSched;
+          *reinterpret_cast<volatile int*>(&sh->sched[slot]) = tile;
+          mbar_arrive(&sh->sfull[slot]);
+          publish_remote_u32(map_to_rank(su32(&sh->sched[slot]), 1),
+                             map_to_rank(su32(&sh->sfull[slot]), 1), tile);
+        } else {
+          tile = next_tile(j);
+        }
+        if (tile >= total) { done = tile == kNoTile; break; }
         const SwTile st = decode(tile);
-        if (st.nv == 0) continue;
         const int half = st.N >> 1;  // token rows of this CTA
         const int bsel = tok_box_sel(half);
         const uint32_t tx =
@@ -623,6 +716,14 @@ __global__ void __launch_bounds__(SwRoles<TOK, MH>::THREADS, 1)
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
+      if (leader && done && !*abort_flag) {
+        __threadfence();  // this pair's last grab before its done count
+        if (atomicAdd(gctr + 1, 1) == npairs - 1) {
+          __threadfence();  // every pair's grabs before the reset
+          atomicExch(gctr, 0);
+          atomicExch(gctr + 1, 0);
+        }
+      }
       if (!ok && leader) {  // both CTAs' copies complete on the leader's barriers
         for (int s = 0; s < STAGES; ++s)
           if (issued[s]) drain_wait(&sh->full[s], (issued[s] - 1u) & 1u);
@@ -638,9 +739,10 @@ __global__ void __launch_bounds__(SwRoles<TOK, MH>::THREADS, 1)
       const uint64_t bdesc0 = sw128_desc(su32(smem + A_BYTES));
       uint32_t empty_addr[STAGES];
       for (int s = 0; s < STAGES; ++s) empty_addr[s] = su32(&sh->empty[s]);
-      for (int tile = pair; tile < total && ok; tile += npairs) {
+      for (int j = 0; ok; ++j) {
+        const int tile = next_tile(j);
+        if (tile >= total) break;
         const SwTile st = decode(tile);
-        if (st.nv == 0) continue;
         const uint32_t idesc = idesc_sw(2 * ROWS, st.N, F16 ? 1 : 0);  // M256 per MMA
         // token atoms h rows apart (16-byte descriptor units)
         const uint32_t b_atom16 = (uint32_t)((32 << tok_box_sel(st.N >> 1)) * BK * 2) >> 4;
@@ -684,8 +786,8 @@ __global__ void __launch_bounds__(SwRoles<TOK, MH>::THREADS, 1)
         uint32_t phase = 0;
         const uint32_t full_remote0 = map_to_rank(su32(&sh->full[0]), 0);
         bool ok = true;
-        for (int tile = pair; tile < total && ok; tile += npairs) {
-          if (decode(tile).nv == 0) continue;
+        for (int j = 0; ok; ++j) {
+          if (next_tile(j) >= total) break;
           for (int ks = 0; ks < nks; ++ks) {
             if (!wait_fast(&sh->afull[stage], phase, abort_flag, status)) { ok = false; break; }
             fence_proxy_async_smem();
@@ -710,9 +812,10 @@ __global__ void __launch_bounds__(SwRoles<TOK, MH>::THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = pair; tile < total && ok; tile += npairs) {
+    for (int j = 0; ok; ++j) {
+      const int tile = next_tile(j);
+      if (tile >= total) break;
       const SwTile st = decode(tile);
-      if (st.nv == 0) continue;
       const int half = st.N >> 1;
       const uint32_t atom_bytes = (uint32_t)(32 << tok_box_sel(half)) * BK * 2;
       const __nv_bfloat16* src[8];
@@ -771,9 +874,10 @@ __global__ void __launch_bounds__(SwRoles<TOK, MH>::THREADS, 1)
     // staging buffers of 2 KB: two per warp of one group, or one per warp
     uint8_t* obufs = out_stage + (grp * 4 + quad) * R::NBUF * OUT_BUF_BYTES;
     int obuf = 0;
-    for (int tile = pair; tile < total; tile += npairs) {
+    for (int j = 0;; ++j) {
+      const int tile = next_tile(j);
+      if (tile >= total) break;
       const SwTile st = decode(tile);
-      if (st.nv == 0) continue;
       if (!wait_fast(&sh->tfull[acc], aphase, abort_flag, status)) break;
       tc_fence_after();
       const __nv_bfloat16* be = bias ? bias + (size_t)st.e * N1 : nullptr;
