@@ -41,6 +41,8 @@ def _check(got, ref, K, what):
     (4, 300, 384, 256, None),               # three row tiles per expert
     (1, 64, 128, 1024, [64]),
     (5, 130, 256, 640, [0, 130, 129, 2, 77]),
+    (4, 512, 512, 384, [300, 256, 257, 512]),  # two 256-row pair tiles per expert
+    (3, 256, 640, 256, [129, 128, 255]),       # peer half with 0, 1 and 127 valid rows
 ])
 def test_fp8_masked_gemm(moe, E, max_m, N, K, counts):
     inp = synth.make_fp8_masked(E, max_m, N, K, seed=E * 1000 + K, device="cuda", counts=counts)
@@ -67,19 +69,23 @@ def test_fp8_masked_gemm(moe, E, max_m, N, K, counts):
 
 def test_fp8_masked_gemm_deepseek_size_sampled(moe):
     """DeepSeek-V3-style expert-parallel shapes (8 local experts, up to 256
-    rows each, N 4096, K 7168); the oracle checks 4 rows of every expert."""
+    rows each, N 4096, K 7168); the oracle checks six rows of every expert,
+    from both 128-row halves of its tile, the last valid row included."""
     E, max_m, N, K = 8, 256, 4096, 7168
     inp = synth.make_fp8_masked(E, max_m, N, K, seed=3, device="cuda")
     out = moe.moe_grouped_gemm_fp8_masked(inp["a"], inp["a_scale"], inp["b"], inp["b_scale"],
                                           inp["counts"])
     torch.cuda.synchronize()
     counts = inp["counts"].cpu().numpy()
-    rows = [0, 1, 77, 127]  # counts are at least max_m / 2 = 128
-    assert all(r < c for r in rows for c in counts)
-    ref = O.grouped_gemm_fp8_masked(_codes(inp["a"][:, rows]),
-                                    inp["a_scale"][:, rows].cpu().numpy(), _codes(inp["b"]),
-                                    inp["b_scale"].cpu().numpy(), [len(rows)] * E, dtype=None)
-    _check(out[:, rows].float().cpu().numpy(), ref, K, "DeepSeek-V3 size")
+    for g in range(E):
+        c = int(min(max(counts[g], 0), max_m))
+        rows = sorted({r for r in (0, 1, 77, 127, 128, c - 1) if 0 <= r < c})
+        ref = O.grouped_gemm_fp8_masked(_codes(inp["a"][g:g + 1, rows]),
+                                        inp["a_scale"][g:g + 1, rows].cpu().numpy(),
+                                        _codes(inp["b"][g:g + 1]),
+                                        inp["b_scale"][g:g + 1].cpu().numpy(), [len(rows)],
+                                        dtype=None)
+        _check(out[g:g + 1, rows].float().cpu().numpy(), ref, K, f"DeepSeek-V3 size, expert {g}")
 
 
 def test_fp8_masked_gemm_rejects(moe):
