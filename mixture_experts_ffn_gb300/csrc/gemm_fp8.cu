@@ -64,7 +64,7 @@ constexpr int TMEM_COLS = 2 * BN;  // two partial-sum buffers
 constexpr int kEpiWarps = 8;
 constexpr int kEpiWarp0 = 2;  // promotion warps 2..9
 // ten warps: three share an SM sub-partition's 16384 registers, so a thread
-// gets at most 168 (the 128 accumulators and one 16-column chunk in flight)
+// gets at most 168 (the 128 accumulators and two 16-column chunks in flight)
 constexpr int NUM_THREADS = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr int kColsPerWarp = BN / 2;  // accumulator columns of one promotion warp
 // kind::f8f6f4 instruction descriptor: fp32 D (bit 4), e4m3 A and B (format
