@@ -309,9 +309,11 @@ __global__ void __launch_bounds__(NUM_THREADS)
       const bool col_ok = nb < nsb;        // warp-uniform
       const float* sa = a_scale + ((size_t)st.g * max_m + (in_slab ? row : 0)) * nkb;
       const float* sb = b_scale + ((size_t)st.g * nsb + (col_ok ? nb : 0)) * nkb;
-      float acc[kColsPerWarp];
+      // column pairs, added with the packed two-wide fp32 FMA (each half
+      // rounds as its own fmaf does)
+      float2 acc[kColsPerWarp / 2];
 #pragma unroll
-      for (int i = 0; i < kColsPerWarp; ++i) acc[i] = 0.f;
+      for (int i = 0; i < kColsPerWarp / 2; ++i) acc[i] = make_float2(0.f, 0.f);
       // scales two K blocks ahead of their use
       float sa0 = in_slab ? __ldg(sa) : 0.f, sb0 = col_ok ? __ldg(sb) : 0.f;
       float sa1 = 0.f, sb1 = 0.f;
@@ -322,6 +324,7 @@ __global__ void __launch_bounds__(NUM_THREADS)
 #pragma unroll 1
       for (int kb = 0; kb < nkb; ++kb) {
         const float s = sa0 * sb0;
+        const float2 s2 = make_float2(s, s);
         sa0 = sa1;
         sb0 = sb1;
         if (kb + 2 < nkb) {
@@ -347,8 +350,10 @@ __global__ void __launch_bounds__(NUM_THREADS)
             if (lane == 0) mbar_arrive_cluster(pb ? pempty_leader1 : pempty_leader0);
           }
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            acc[16 * c + i] = fmaf(__uint_as_float(p[c & 1][i]), s, acc[16 * c + i]);
+          for (int i = 0; i < 8; ++i)
+            acc[8 * c + i] = __ffma2_rn(make_float2(__uint_as_float(p[c & 1][2 * i]),
+                                                    __uint_as_float(p[c & 1][2 * i + 1])),
+                                        s2, acc[8 * c + i]);
         }
         if (++pb == 2) { pb = 0; pph ^= 1u; }
       }
@@ -365,7 +370,10 @@ __global__ void __launch_bounds__(NUM_THREADS)
         const int col0 = nb * 128 + c * 32;
         float v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = acc[c * 32 + i];
+        for (int i = 0; i < 16; ++i) {
+          v[2 * i] = acc[c * 16 + i].x;
+          v[2 * i + 1] = acc[c * 16 + i].y;
+        }
         emit_chunk32<1>(v, col0, wrow0, boxed, row_ok, orow, N - col0, &tm_out, obufs, obuf,
                         lane);
       }
