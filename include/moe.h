@@ -42,6 +42,10 @@
  *    moe_sync_status reports it as MOE_ERR_DEVICE.
  *  - Every wait inside a kernel is bounded; a wait that runs out latches
  *    MOE_ERR_TIMEOUT in the status word instead of hanging.
+ *  - A workspace serves one call at a time: calls that can run at the same
+ *    time on the GPU (on different streams) need workspaces of their own,
+ *    since the status word and the self-resetting counters at the start of
+ *    a workspace are state the call's kernels update.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H
