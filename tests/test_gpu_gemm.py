@@ -278,3 +278,30 @@ def test_gemm_row_layouts(moe, layout, counts, max_m, K, F, act, bias, dtype):
                                         None if b is None else b.cuda())
     torch.cuda.synchronize()
     np.testing.assert_array_equal(g, np_(ref))
+
+
+def test_pair_kernel_workspace_reuse(moe):
+    """The SM-pair kernel (K >= 2048, segments averaging >= 128 rows) hands
+    out the tiles of its last rounds from a counter in the workspace's status
+    area, which the launch's last pair resets.  Consecutive calls of
+    different shapes on one workspace give bit for bit the results of fresh
+    workspaces, match the oracle, and leave the counters at zero."""
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    cases = [([300, 0, 200, 100], 2048, 128, "silu"), ([129, 640, 7, 0, 260], 2304, 192, "silu"),
+             ([300, 0, 200, 100], 2048, 128, "swiglu_inter")]
+    for i, (counts, Hk, F, act) in enumerate(cases):
+        spec = ACTS[act]
+        a, w, b, seg_end = _problem(counts, Hk, 2 * F, "bf16", True, seed=40 + i)
+        args = (a.cuda(), w.cuda(), seg_end.cuda(), F, moe.act_params(**spec), b.cuda())
+        shared = moe.moe_grouped_gemm_act(*args, ws=ws)
+        fresh = moe.moe_grouped_gemm_act(*args, ws=torch.zeros(256, dtype=torch.uint8,
+                                                                device="cuda"))
+        torch.cuda.synchronize()
+        assert torch.equal(shared, fresh), f"case {i}: workspace reuse changed the result"
+        assert int(ws[32:40].view(torch.int32).abs().sum()) == 0, "tile counters not reset"
+        exact = O.grouped_gemm_act(np_(a), np_(w), np_(seg_end), F, spec["kind"],
+                                   spec.get("swiglu_fusion", 2), spec.get("limit", 0.0),
+                                   spec.get("alpha", 1.0), spec.get("beta", 0.0), np_(b),
+                                   dtype=None)
+        assert_rounded_once(np_(shared), exact, "bf16", f"pair kernel, shared workspace {i}")
+        assert moe.moe_sync_status(ws) == moe.MOE_OK
