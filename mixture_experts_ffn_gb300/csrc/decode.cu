@@ -6,21 +6,22 @@
 // silu(gate) * up rounded to bf16, down product rounded to bf16, fp32 weighted
 // combine in fixed k order.
 //
-//   gate_up : work item = (active expert, 64 activation columns); each warp
-//             streams 8 (gate row, up row) pairs with 16-byte loads and dots
+//   gate_up : work item = (active expert, 32 activation columns); each warp
+//             streams 4 (gate row, up row) pairs with 16-byte loads and dots
 //             them with every route's hidden row of that expert
-//   down    : work item = (active expert, 64 rows of w_down); each warp
-//             streams 8 rows and dots them with every route's activation row
+//   down    : work item = (active expert, 32 rows of w_down); each warp
+//             streams 4 rows and dots them with every route's activation row
 //   combine : the deterministic gather-combine of the staged pipeline
-// Both streaming kernels are persistent (a few CTAs per SM) over a device-side
-// list of the experts that have routes, so no host synchronisation is needed.
+// Both streaming kernels are persistent (one resident round of CTAs) over a
+// device-side list of the experts that have routes, so no host
+// synchronisation is needed.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
 constexpr int kNR = 8;          // routes of one expert handled per pass
-constexpr int kColsPerItem = 64;
+constexpr int kColsPerItem = 32;
 constexpr int kWarps = 8;
 
 __device__ __forceinline__ void fma8(float& acc, const uint4& w, const uint4& x) {
@@ -178,6 +179,17 @@ __global__ void __launch_bounds__(kWarps * 32) indexed_down(
   }
 }
 
+// CTAs of `kernel` (no dynamic shared memory) that one SM holds at once; at
+// least 1.
+int resident_ctas(const void* kernel, int threads) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 1;
+  }
+  return n < 1 ? 1 : n;
+}
+
 }  // namespace
 
 cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, const float* w,
@@ -201,10 +213,20 @@ cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, c
     err = launch_permute(nullptr, 2, ids, T, H, E, K, nullptr, seg_end, r2r, route_to_row, ws, s);
     if (err != cudaSuccess) return err;
   }
-  const int grid = num_sms() * 4;
-  launch_pdl(indexed_gate_up, grid, kWarps * 32, 0, s, static_cast<const __nv_bfloat16*>(hidden),
+  // One resident round of CTAs per kernel (its occupancy x the SM count):
+  // CTAs beyond what the SMs hold at once would start only when whole CTAs
+  // of the first round finish all their items, and that second round is
+  // what sets the tail (measured on the Kimi-K2-style decode: 1250 vs
+  // 1400 us with the grid at 4 CTAs per SM, which registers cap at 2 for
+  // the gate_up kernel and 3 for the down kernel; 32-column items instead
+  // of 64 then 1241 us).
+  static const int per_sm_gu = resident_ctas((const void*)indexed_gate_up, kWarps * 32);
+  static const int per_sm_dn = resident_ctas((const void*)indexed_down, kWarps * 32);
+  launch_pdl(indexed_gate_up, num_sms() * per_sm_gu, kWarps * 32, 0, s,
+      static_cast<const __nv_bfloat16*>(hidden),
       static_cast<const __nv_bfloat16*>(w1), seg_end, r2r, active, num_active, T, H, F, K, act);
-  launch_pdl(indexed_down, grid, kWarps * 32, 0, s, static_cast<const __nv_bfloat16*>(w2), act,
+  launch_pdl(indexed_down, num_sms() * per_sm_dn, kWarps * 32, 0, s,
+      static_cast<const __nv_bfloat16*>(w2), act,
       seg_end, active, num_active, H, F, y);
   count_launch(2);
   err = cudaGetLastError();
