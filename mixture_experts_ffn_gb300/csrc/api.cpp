@@ -11,6 +11,7 @@
 #include <cstdlib>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <set>
 #include <string>
 #include <vector>
@@ -35,6 +36,24 @@ int num_sms() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+int resident_ctas(const void* kernel, int threads, int smem_bytes) {
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_tuple(kernel, threads, smem_bytes);
+  const auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem_bytes) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    n = 1;
+  }
+  n = n < 1 ? 1 : n;
+  cache[key] = n;
+  return n;
 }
 
 cudaError_t set_smem_limit(const void* kernel, int bytes) {

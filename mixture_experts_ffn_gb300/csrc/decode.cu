@@ -179,17 +179,6 @@ __global__ void __launch_bounds__(kWarps * 32) indexed_down(
   }
 }
 
-// CTAs of `kernel` (no dynamic shared memory) that one SM holds at once; at
-// least 1.
-int resident_ctas(const void* kernel, int threads) {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess) {
-    (void)cudaGetLastError();
-    n = 1;
-  }
-  return n < 1 ? 1 : n;
-}
-
 }  // namespace
 
 cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, const float* w,
@@ -220,8 +209,8 @@ cudaError_t launch_indexed(const void* hidden, const void* w1, const void* w2, c
   // 1400 us with the grid at 4 CTAs per SM, which registers cap at 2 for
   // the gate_up kernel and 3 for the down kernel; 32-column items instead
   // of 64 then 1241 us).
-  static const int per_sm_gu = resident_ctas((const void*)indexed_gate_up, kWarps * 32);
-  static const int per_sm_dn = resident_ctas((const void*)indexed_down, kWarps * 32);
+  const int per_sm_gu = resident_ctas((const void*)indexed_gate_up, kWarps * 32);
+  const int per_sm_dn = resident_ctas((const void*)indexed_down, kWarps * 32);
   launch_pdl(indexed_gate_up, num_sms() * per_sm_gu, kWarps * 32, 0, s,
       static_cast<const __nv_bfloat16*>(hidden),
       static_cast<const __nv_bfloat16*>(w1), seg_end, r2r, active, num_active, T, H, F, K, act);

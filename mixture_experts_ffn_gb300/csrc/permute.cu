@@ -475,19 +475,20 @@ cudaError_t launch_combine(const void* y, const float* w, const int32_t* r2r, in
   if (T == 0 || H == 0) return cudaSuccess;
   const int M = T * K;
   const bool aligned = ((uintptr_t)y % 16 == 0) && ((uintptr_t)out % 16 == 0);
-  auto grid_for = [&](int vec) {
+  // at most one resident round of CTAs (a grid-stride loop covers the rest)
+  auto grid_for = [&](const void* kern, int vec) {
     const long long items = (long long)T * (H / vec);
-    const long long cap = (long long)num_sms() * 8;
+    const long long cap = (long long)num_sms() * resident_ctas(kern, 256);
     return (unsigned)std::max<long long>(1, std::min<long long>(cap, (items + 255) / 256));
   };
   auto half_width = [&](auto tag) {
     using B = decltype(tag);
     if (aligned && H % 8 == 0)
-      launch_pdl(combine_kernel<B, 8>, grid_for(8), 256, 0, s, static_cast<const B*>(y), w, r2r, T,
-          K, H, M, scale, static_cast<B*>(out), token_scale);
+      launch_pdl(combine_kernel<B, 8>, grid_for((const void*)combine_kernel<B, 8>, 8), 256, 0, s,
+          static_cast<const B*>(y), w, r2r, T, K, H, M, scale, static_cast<B*>(out), token_scale);
     else
-      launch_pdl(combine_kernel<B, 1>, grid_for(1), 256, 0, s, static_cast<const B*>(y), w, r2r, T,
-          K, H, M, scale, static_cast<B*>(out), token_scale);
+      launch_pdl(combine_kernel<B, 1>, grid_for((const void*)combine_kernel<B, 1>, 1), 256, 0, s,
+          static_cast<const B*>(y), w, r2r, T, K, H, M, scale, static_cast<B*>(out), token_scale);
   };
   if (dt == MOE_BF16) {
     half_width(__nv_bfloat16{});
@@ -495,11 +496,13 @@ cudaError_t launch_combine(const void* y, const float* w, const int32_t* r2r, in
     half_width(__half{});
   } else {
     if (aligned && H % 4 == 0)
-      launch_pdl(combine_kernel<float, 4>, grid_for(4), 256, 0, s, static_cast<const float*>(y), w,
-          r2r, T, K, H, M, scale, static_cast<float*>(out), token_scale);
+      launch_pdl(combine_kernel<float, 4>, grid_for((const void*)combine_kernel<float, 4>, 4), 256,
+          0, s, static_cast<const float*>(y), w, r2r, T, K, H, M, scale,
+          static_cast<float*>(out), token_scale);
     else
-      launch_pdl(combine_kernel<float, 1>, grid_for(1), 256, 0, s, static_cast<const float*>(y), w,
-          r2r, T, K, H, M, scale, static_cast<float*>(out), token_scale);
+      launch_pdl(combine_kernel<float, 1>, grid_for((const void*)combine_kernel<float, 1>, 1), 256,
+          0, s, static_cast<const float*>(y), w, r2r, T, K, H, M, scale,
+          static_cast<float*>(out), token_scale);
   }
   count_launch();
   return cudaGetLastError();
