@@ -689,6 +689,18 @@ def run_stage(args, moe, cfg, inp, p, a, ws, flush, timed):
         M = T * K
         extra.update({"flops": 2.0 * M * 2 * F * H,
                       "bytes": E * 2 * F * H * b + M * H * b + M * F * b})
+    if args.stage == "swiglu":
+        # the standalone clamped SwiGLU on the gated intermediate of this
+        # workload: [T*K, 2F] -> [T*K, F] with the row layout of its act
+        rows, tdt = T * K, inp["hidden"].dtype
+        fusion = cfg.swiglu_fusion if cfg.swiglu_fusion in (1, 2) else 2
+        lim, al, be = (cfg.limit, cfg.alpha, cfg.beta) if cfg.act == "swiglu" else (7.0, 1.702, 1.0)
+        g_in = torch.randn((rows, 2 * F), device=dev).to(tdt)
+        s_out = torch.empty((rows, F), dtype=tdt, device=dev)
+        fns["swiglu"] = lambda: moe.swiglu(g_in, None, fusion, lim, al, be, out=s_out)
+        eb = g_in.element_size()
+        extra = {"rows": rows, "I": F, "fusion": fusion, "flops": 0.0,
+                 "bytes": rows * 3 * F * eb}
     if args.stage == "fp8_gemm":
         # block-scaled FP8 masked grouped GEMM, DeepSeek-V3-style expert-parallel
         # shapes: 8 local experts of up to 256 rows, N 4096 (2F), K 7168 (H)
@@ -775,7 +787,7 @@ def main():
     ap.add_argument("--stage", default=None,
                     choices=["route", "route_permute", "permute", "gemm_act", "gemm_down",
                              "combine", "indexed_mlp", "shared_mlp", "fp8_gemm",
-                             "gemm_act_split"],
+                             "gemm_act_split", "swiglu"],
                     help="time one stage alone (for profiler captures)")
     ap.add_argument("--shared-s", type=int, default=2048,
                     help="intermediate size of the shared expert timed by --stage shared_mlp "

@@ -21,14 +21,16 @@ def moe():
     return m
 
 
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("with_up,fusion", [(True, 2), (False, 1), (False, 2)])
 @pytest.mark.parametrize("limit,alpha,beta", [(7.0, 1.702, 1.0), (0.0, 1.0, 0.0), (-1.0, 0.5, 2.0),
                                               (2.5, 3.0, -0.5)])
-def test_swiglu(moe, dtype, with_up, fusion, limit, alpha, beta):
+@pytest.mark.parametrize("R,I", [(257, 96),    # 16-byte items
+                                 (33, 97),     # odd width: one element per thread
+                                 (300, 2880)])  # gpt-oss-style intermediate width
+def test_swiglu(moe, dtype, with_up, fusion, limit, alpha, beta, R, I):
     g = torch.Generator().manual_seed(11)
-    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
-    R, I = 257, 96
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
     gate = (torch.randn((R, I if with_up else 2 * I), generator=g) * 6).to(tdt)
     up = (torch.randn((R, I), generator=g) * 6).to(tdt) if with_up else None
     out = moe.swiglu(gate.cuda(), None if up is None else up.cuda(), fusion, limit, alpha, beta)
