@@ -39,10 +39,12 @@ int num_sms() {
 }
 
 int resident_ctas(const void* kernel, int threads, int smem_bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
   static std::mutex mu;
-  static std::map<std::tuple<const void*, int, int>, int> cache;
+  static std::map<std::tuple<int, const void*, int, int>, int> cache;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_tuple(kernel, threads, smem_bytes);
+  const auto key = std::make_tuple(dev, kernel, threads, smem_bytes);
   const auto it = cache.find(key);
   if (it != cache.end()) return it->second;
   int n = 0;

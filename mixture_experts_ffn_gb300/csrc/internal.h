@@ -56,9 +56,9 @@ struct ForwardWs {
 
 void count_launch(int n = 1);
 int num_sms();
-// CTAs of `kernel` that one SM holds at once with `threads` threads and
-// `smem_bytes` of dynamic shared memory (an occupancy query, cached per
-// kernel and shape); at least 1.
+// CTAs of `kernel` that one SM of the current device holds at once with
+// `threads` threads and `smem_bytes` of dynamic shared memory (an occupancy
+// query, cached per device, kernel and shape); at least 1.
 int resident_ctas(const void* kernel, int threads, int smem_bytes = 0);
 
 // Raises the dynamic shared-memory limit of `kernel` to `bytes` on the
