@@ -204,6 +204,22 @@ def sources_sha256(paths):
     return h.hexdigest()
 
 
+def inputs_sha256(inp):
+    """SHA-256 (first 16 hex digits) of the bytes of each input drawn on the
+    host (activations, logits, correction bias, fixed ids, biases); the weight
+    stacks are drawn on the device from their seeds and are not hashed."""
+    import torch
+
+    out = {}
+    for k in ("hidden", "logits", "correction_bias", "expert_ids", "b_gate_up", "b_down"):
+        t = inp.get(k)
+        if t is None:
+            continue
+        b = t.detach().contiguous().view(-1).view(torch.uint8).cpu().numpy().tobytes()
+        out[k] = hashlib.sha256(b).hexdigest()[:16]
+    return out
+
+
 def profile_traffic(kernel: str, srcs):
     """DRAM bytes per launch from the committed ncu summary of ``kernel``, when
     the summary was taken on the current source of the kernel."""
@@ -596,6 +612,7 @@ def run_ours(args, rank, world, local):
             "status": int(status),
             "roofline": roofline, "e2e": e2e, "cpu_baseline": cpu,
             "clocks": clk.summary(), "breakdown": breakdown,
+            "inputs_sha256": inputs_sha256(inp),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
