@@ -43,6 +43,8 @@ def _check(got, ref, K, what):
     (5, 130, 256, 640, [0, 130, 129, 2, 77]),
     (4, 512, 512, 384, [300, 256, 257, 512]),  # two 256-row pair tiles per expert
     (3, 256, 640, 256, [129, 128, 255]),       # peer half with 0, 1 and 127 valid rows
+    (1024, 2, 128, 128, None),                 # the most experts, one or two rows each
+    (2, 1, 256, 384, [1, 0]),                  # one-row slab
 ])
 def test_fp8_masked_gemm(moe, E, max_m, N, K, counts):
     inp = synth.make_fp8_masked(E, max_m, N, K, seed=E * 1000 + K, device="cuda", counts=counts)
