@@ -160,6 +160,27 @@ def test_indexed_path_matches_staged(moe):
     assert_forward_close(np_(y_st), r, "bf16", "staged vs oracle")
 
 
+def test_indexed_path_many_routes_per_expert(moe):
+    """The indexed kernels take an expert's routes eight at a time: fixed ids
+    that give experts 0..3 every token (27 routes each: three full passes and
+    a tail of three) and spread the rest, checked against the oracle."""
+    cfg = synth.CONFIGS["kimi_k2_decode_bf16"].replace(T=27, H=1024, F=512, E=16, K=6,
+                                                       hash_ids=True)
+    inp, ref = make(cfg)
+    t = torch.arange(cfg.T, dtype=torch.int32).unsqueeze(1)
+    tail = torch.stack([4 + (t[:, 0] % 6), 10 + (t[:, 0] % 6)], dim=1)
+    ids = torch.cat([torch.arange(4, dtype=torch.int32).expand(cfg.T, 4), tail], dim=1)
+    inp["expert_ids"] = ids.contiguous().cuda()
+    ref["expert_ids"] = ids.numpy()
+    p, a = moe.config_params(cfg)
+    w, ids_out, _, _ = moe.moe_route(inp["logits"], p, inp["correction_bias"], inp["expert_ids"])
+    y_idx = moe.moe_indexed_mlp(inp["hidden"], inp["w_gate_up"], inp["w_down"], w, ids_out)
+    torch.cuda.synchronize()
+    assert torch.equal(ids_out.cpu(), ids), "fixed ids not passed through"
+    r = oracle_forward(cfg, ref)
+    assert_forward_close(np_(y_idx), r, "bf16", "indexed, 27 routes per expert")
+
+
 def test_forward_is_deterministic(moe):
     cfg = synth.CONFIGS["qwen3_bf16"].replace(T=512, H=512, F=256, E=64)
     inp, _ = make(cfg)
