@@ -604,7 +604,10 @@ size_t moe_permute_workspace_size(int M, int E);
 moe_status moe_clear_status(void* ws, cudaStream_t stream);
 
 /* Synchronise `stream`, then read and clear the status word of `ws`:
- * MOE_OK, MOE_ERR_DEVICE (bad id / index met) or MOE_ERR_TIMEOUT. */
+ * MOE_OK, MOE_ERR_DEVICE (bad id / index met) or MOE_ERR_TIMEOUT.  On a
+ * timeout the whole status area (MOE_STATUS_BYTES, with the counters a launch
+ * that gave up may have left set) is cleared, so the workspace is ready for
+ * the next call. */
 moe_status moe_sync_status(void* ws, cudaStream_t stream);
 
 /* Static text for a status code. */

@@ -1017,7 +1017,10 @@ moe_status moe_sync_status(void* ws, cudaStream_t stream) {
   int word = 0;
   if (cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return MOE_ERR_CUDA;
-  if (cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  // after a timeout the launch that gave up may have left its grid-barrier
+  // or tile counters set: the whole status area is cleared with the word
+  const size_t clear = (word & kDevTimeout) ? MOE_STATUS_BYTES : sizeof(int);
+  if (cudaMemset(ws, 0, clear) != cudaSuccess) return MOE_ERR_CUDA;
   if (word & kDevTimeout) return MOE_ERR_TIMEOUT;
   if (word & kDevBadIndex) return MOE_ERR_DEVICE;
   return MOE_OK;

@@ -43,6 +43,9 @@ def test_grid_barrier_timeout_is_reported_and_recovered(moe, name):
         assert not was_on
         _route_permute(moe, cfg, inp, ws)
         assert moe.moe_sync_status(ws) == moe.MOE_ERR_TIMEOUT
+        # reporting the timeout cleared the whole status area, the barrier
+        # counters the failed launch left set included
+        assert int(ws[:moe.MOE_STATUS_BYTES].to(torch.int32).sum()) == 0
     finally:
         moe.moe_test_force_wait_timeout(False)
     # the context is still usable: plain work on the same stream runs
@@ -82,6 +85,33 @@ def test_forward_after_a_timeout_matches_a_clean_forward(moe):
     finally:
         moe.moe_test_force_wait_timeout(False)
     moe.moe_clear_status(ws)
+    got = fwd()
+    assert moe.moe_sync_status(ws) == moe.MOE_OK
+    assert torch.equal(got, ref)
+
+
+def test_forward_after_a_reported_timeout_needs_no_clear(moe):
+    """moe_sync_status that reports a timeout leaves the workspace ready: the
+    next forward on it, with no status clear in between, is the clean one."""
+    # H = 2048 and 256 routes per expert: the gate_up runs on the SM-pair
+    # kernel, whose tile counters share the status area
+    cfg = synth.CONFIGS["qwen3_bf16"].replace(T=256, H=2048, F=256, E=8, local_count=0)
+    inp, _ = make(cfg)
+    p, a = moe.config_params(cfg)
+    ws = moe._ws(moe.moe_workspace_size(cfg.T, cfg.H, cfg.F, cfg.E, cfg.K, moe.MOE_BF16), "cuda")
+
+    def fwd():
+        return moe.moe_ffn_forward(inp["hidden"], inp["logits"], inp["w_gate_up"],
+                                   inp["w_down"], p, a, ws=ws)
+
+    ref = fwd().clone()
+    assert moe.moe_sync_status(ws) == moe.MOE_OK
+    moe.moe_test_force_wait_timeout(True, 50_000_000)
+    try:
+        fwd()
+        assert moe.moe_sync_status(ws) == moe.MOE_ERR_TIMEOUT
+    finally:
+        moe.moe_test_force_wait_timeout(False)
     got = fwd()
     assert moe.moe_sync_status(ws) == moe.MOE_OK
     assert torch.equal(got, ref)
