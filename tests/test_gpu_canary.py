@@ -129,3 +129,45 @@ def test_stage_calls_write_only_their_outputs(moe):
         assert g.intact(), f"wrote outside {what}"
         if what != "workspace":
             assert not torch.isnan(g.t.float()).any(), f"{what} not fully written"
+
+
+def test_shared_and_local_forwards_write_only_their_outputs(moe):
+    """The shared expert alone, the shared + routed forward (two outputs) and
+    an expert-parallel rank's forward from its MoERouter outputs."""
+    cfg = synth.CONFIGS["deepseek_v3_bf16"].replace(T=100, H=256, F=128, E=32, local_start=8,
+                                                    local_count=8)
+    inp, _ = make(cfg)
+    p, a = moe.config_params(cfg)
+    T, H, F, E, K, S = cfg.T, cfg.H, cfg.F, cfg.E, cfg.K, 192
+    tdt = inp["hidden"].dtype
+    g = torch.Generator(device="cuda").manual_seed(5)
+    sw1 = (torch.randn((2 * S, H), device="cuda", generator=g) / H ** 0.5).to(tdt)
+    sw2 = (torch.randn((H, S), device="cuda", generator=g) / S ** 0.5).to(tdt)
+    lib = moe.load_library()
+
+    so = Guarded((T, H), tdt)
+    ws1 = guarded_ws(lib.moe_shared_expert_workspace_size(T, H, S, moe.MOE_BF16))
+    moe.moe_shared_expert_mlp(inp["hidden"], sw1, sw2, out=so.t, ws=ws1.t)
+
+    ro, so2 = Guarded((T, H), tdt), Guarded((T, H), tdt)
+    ws2 = guarded_ws(lib.moe_workspace_size_shared(T, H, F, S, E, K, moe.MOE_BF16))
+    p0, _ = moe.config_params(cfg.replace(local_count=0))  # (no MoERouter outputs here)
+    moe.moe_ffn_forward_shared(inp["hidden"], inp["logits"], inp["w_gate_up"], inp["w_down"], p0,
+                               a, inp["correction_bias"], sw1, sw2, routed_out=ro.t,
+                               shared_out=so2.t, ws=ws2.t)
+
+    _, _, probs, wsc = moe.moe_route(inp["logits"], p, inp["correction_bias"])
+    ls, lc = cfg.local_start, cfg.local_count
+    lo = Guarded((T, H), tdt)
+    ws3 = guarded_ws(lib.moe_workspace_size(T, H, F, lc, min(K, lc), moe.MOE_BF16))
+    moe.moe_ffn_forward_local(inp["hidden"], probs, wsc, inp["w_gate_up"][ls:ls + lc].contiguous(),
+                              inp["w_down"][ls:ls + lc].contiguous(), K, a, out=lo.t, ws=ws3.t)
+    for ws in (ws1, ws2, ws3):
+        assert moe.moe_sync_status(ws.t) == moe.MOE_OK
+    torch.cuda.synchronize()
+    for what, gd in (("shared_mlp", so), ("routed", ro), ("shared", so2), ("local", lo),
+                     ("shared workspace", ws1), ("shared+routed workspace", ws2),
+                     ("local workspace", ws3)):
+        assert gd.intact(), f"wrote outside {what}"
+        if "workspace" not in what:
+            assert not torch.isnan(gd.t.float()).any(), f"{what} not fully written"
