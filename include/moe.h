@@ -567,8 +567,10 @@ moe_status moe_shared_expert_mlp(const void* hidden, const void* w_gate_up, cons
 size_t moe_shared_expert_workspace_size(int T, int H, int S, moe_dtype dtype);
 
 /* Shared + routed MoE FFN [TileOPs, FusedMoESharedExpertFwdOp] with
- * tp_size 1: routed_out as moe_ffn_forward (no expert_ids, no biases;
- * routed_scaling_factor scales the routed output only, once) and shared_out
+ * tp_size 1: routed_out as moe_ffn_forward (no expert_ids, no biases, no
+ * MoERouter outputs: p->local_expert_count must be 0, MOE_ERR_INVALID_ARG
+ * otherwise; routed_scaling_factor scales the routed output only, once) and
+ * shared_out
  * as moe_shared_expert_mlp, returned apart.  shared_w_gate_up and
  * shared_w_down are passed together (then shared_out is written) or both
  * NULL (shared_out untouched, S ignored).  The two halves run one after the
