@@ -170,11 +170,15 @@ __device__ __forceinline__ void route_loaded(int t, const float (&z)[NPL],
         for (int g = 0; g < NPL; ++g) {
           if (g >= a.G) break;
           float l1 = -INFINITY, l2 = -INFINITY;
+          if (m == 1) {  // one register a group (32 experts): its only value
+            l1 = u[g];
+          } else {
 #pragma unroll
-          for (int j = 0; j < NPL; ++j) {
-            if (j >= g * m && j < (g + 1) * m) {
-              const float v = u[j];
-              if (v > l1) { l2 = l1; l1 = v; } else if (v > l2) { l2 = v; }
+            for (int j = 0; j < NPL; ++j) {
+              if (j >= g * m && j < (g + 1) * m) {
+                const float v = u[j];
+                if (v > l1) { l2 = l1; l1 = v; } else if (v > l2) { l2 = v; }
+              }
             }
           }
           const unsigned k1 = __reduce_max_sync(0xffffffffu, order_key(l1));
