@@ -39,6 +39,12 @@ namespace {
 using rt::RouteArgs;
 
 constexpr int kFusedWarps = 16;  // kPermuteChunk / 16 = 64 routes per warp in the scatter
+// Large batches (more than two tokens a warp at 16 warps per SM) with at most
+// eight registers of scores a lane run 32 warps per CTA: the routing phase
+// then takes at most two tokens a warp on the DeepSeek-V3-style batch (the
+// launch 43.7 vs 47.7 us); smaller batches keep 16 (more registers a thread,
+// and 32 warps measured slower on the gpt-oss-style batch).
+constexpr int kFusedWarpsLarge = 32;
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
@@ -103,8 +109,8 @@ __device__ __forceinline__ int column_sum(const int* __restrict__ counts, int E,
   return all;
 }
 
-template <int NPL>
-__global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
+template <int NPL, int W>
+__global__ void __launch_bounds__(W * 32, 1) route_permute_kernel(
     const void* __restrict__ logits, const float* __restrict__ bias,
     const int32_t* __restrict__ ids_in, int T, int E, RouteArgs a, float* __restrict__ w_out,
     int32_t* __restrict__ id_out, void* __restrict__ probs, float* __restrict__ wscale,
@@ -113,7 +119,7 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
     int32_t* __restrict__ route_to_row, int* status, int* bar, BarrierArgs ba) {
   extern __shared__ int smem[];  // [E] expert start | [E] chunk offsets / histogram | [W][E]
   pdl_wait();  // everything below reads results of earlier launches
-  const int warp = threadIdx.x >> 5, W = blockDim.x >> 5, tid = threadIdx.x;
+  const int warp = threadIdx.x >> 5, tid = threadIdx.x;  // W warps (blockDim.x == 32 W)
   const int M = T * a.K;
   // ---- A: route (the next token's logits are loaded before this one is routed)
   {
@@ -169,14 +175,13 @@ __global__ void __launch_bounds__(kFusedWarps * 32, 1) route_permute_kernel(
   }
 }
 
-template <int NPL>
+template <int NPL, int W>
 cudaError_t launch_npl(const void* logits, const float* bias, const int32_t* ids_in, int T,
                        int E, const RouteArgs& a, float* w, int32_t* ids, void* probs,
                        float* wscale, int C, int* counts, int32_t* seg_end, int* active,
                        int* num_active, int32_t* r2r, int32_t* route_to_row, int* status, int* bar,
                        size_t smem, int grid, BarrierArgs ba, cudaStream_t s) {
-  set_smem_limit((const void*)route_permute_kernel<NPL>,
-                 (2 + kFusedWarps) * kFusedWarps * 32 * 4);
+  set_smem_limit((const void*)route_permute_kernel<NPL, W>, (2 + W) * kFusedWarps * 32 * 4);
   // A cooperative launch: the scheduler starts the grid only when all of its
   // CTAs can be resident at once, so two of these kernels running on two
   // streams never each hold part of the GPU while waiting at a barrier for
@@ -185,7 +190,7 @@ cudaError_t launch_npl(const void* logits, const float* bias, const int32_t* ids
   // that refuses the pair gets the cooperative launch alone.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kFusedWarps * 32);
+  cfg.blockDim = dim3(W * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -196,13 +201,13 @@ cudaError_t launch_npl(const void* logits, const float* bias, const int32_t* ids
   cfg.attrs = attr;
   static std::atomic<int> n_attrs{2};
   cfg.numAttrs = n_attrs.load();
-  cudaError_t e = cudaLaunchKernelEx(&cfg, route_permute_kernel<NPL>, logits, bias, ids_in, T, E,
+  cudaError_t e = cudaLaunchKernelEx(&cfg, route_permute_kernel<NPL, W>, logits, bias, ids_in, T, E,
                                      a, w, ids, probs, wscale, C, counts, seg_end, active,
                                      num_active, r2r, route_to_row, status, bar, ba);
   if (e == cudaErrorInvalidValue || e == cudaErrorNotSupported) {
     (void)cudaGetLastError();
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, route_permute_kernel<NPL>, logits, bias, ids_in, T, E, a, w, ids,
+    e = cudaLaunchKernelEx(&cfg, route_permute_kernel<NPL, W>, logits, bias, ids_in, T, E, a, w, ids,
                            probs, wscale, C, counts, seg_end, active, num_active, r2r,
                            route_to_row, status, bar, ba);
     if (e == cudaSuccess) n_attrs.store(1);
@@ -240,19 +245,31 @@ cudaError_t launch_route_permute(const void* logits, const float* bias, const in
   int* num_active = reinterpret_cast<int*>(base + L.num_active);
   const int C = (M + kPermuteChunk - 1) / kPermuteChunk;
   const int grid = num_sms();
-  const size_t smem = (size_t)(2 + kFusedWarps) * E * 4;
+  const int npl = (E + 31) / 32;
+  const bool large = npl <= 8 && T > 2 * kFusedWarps * grid;
+  const size_t smem = (size_t)(2 + (large ? kFusedWarpsLarge : kFusedWarps)) * E * 4;
   cudaError_t e = cudaSuccess;
   const RouteArgs a = rt::route_args(p, probs, wscale);
-  const int npl = (E + 31) / 32;
   BarrierArgs ba{0, tc::kTimeoutNs};
   if (g_force_timeout.load()) ba = BarrierArgs{1, (uint64_t)g_force_timeout_ns.load()};
   auto go = [&](auto tag) {
     constexpr int N = decltype(tag)::value;
-    return launch_npl<N>(logits, bias, ids_in, T, E, a, w, ids, probs, wscale, C, counts, seg_end,
-                         active, num_active, row_to_route, route_to_row, status, bar, smem, grid,
-                         ba, s);
+    return launch_npl<N, kFusedWarps>(logits, bias, ids_in, T, E, a, w, ids, probs, wscale, C,
+                                      counts, seg_end, active, num_active, row_to_route,
+                                      route_to_row, status, bar, smem, grid, ba, s);
   };
-  if (npl <= 1) e = go(std::integral_constant<int, 1>{});
+  auto go_large = [&](auto tag) {
+    constexpr int N = decltype(tag)::value;
+    return launch_npl<N, kFusedWarpsLarge>(logits, bias, ids_in, T, E, a, w, ids, probs, wscale,
+                                           C, counts, seg_end, active, num_active, row_to_route,
+                                           route_to_row, status, bar, smem, grid, ba, s);
+  };
+  if (large) {
+    if (npl <= 1) e = go_large(std::integral_constant<int, 1>{});
+    else if (npl <= 2) e = go_large(std::integral_constant<int, 2>{});
+    else if (npl <= 4) e = go_large(std::integral_constant<int, 4>{});
+    else e = go_large(std::integral_constant<int, 8>{});
+  } else if (npl <= 1) e = go(std::integral_constant<int, 1>{});
   else if (npl <= 2) e = go(std::integral_constant<int, 2>{});
   else if (npl <= 4) e = go(std::integral_constant<int, 4>{});
   else if (npl <= 8) e = go(std::integral_constant<int, 8>{});
